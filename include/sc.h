@@ -1,0 +1,216 @@
+/*
+ * sc.h -- C ABI of the GB300 (sm_103a) score-centering library.
+ *
+ * Score centering is the correction of the Agent Lightning docs page "Score
+ * Centering", section "Score Centering": for every generated position the
+ * sampler records its top-K candidate ids with their log-probabilities; the
+ * trainer scores the current policy p over the full vocabulary at the rollout
+ * temperature and minimises the token loss
+ *
+ *     -sg(A) * [ log p_a - sum_{v in H} sg(q_v - rho p_v) log p_v ],
+ *     rho = max(1 - Q_H, 1e-6) / max(1 - P_H, 1e-6),
+ *     P_H = sum_{v in H} p_v,  Q_H = sum_{v in H} q_v,
+ *
+ * whose gradient with respect to the raw logits z (x = z / T) is
+ *
+ *     g_v = grad_scale * (1/T) * (-A) * ( [v == a] - mu_hat_v ),
+ *     mu_hat_v = s p_v + [v in H] (q_v - rho p_v),   s = 1 - Q_H + rho P_H,
+ *
+ * i.e. the recorded head keeps the sampler's probabilities and the
+ * unrecorded tail is taken proportional to the current policy.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no memory; it keeps only a small per-process cache of launch
+ *     plans.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Argument errors are detected on the host before anything is launched
+ *     and returned as a status code; nothing is written in that case.
+ *   - Data errors found while the kernel runs (bad ids, bad counts, a wait
+ *     that ran out) are reported per row in the diagnostics' `flags` and,
+ *     OR-ed together, in the optional device status word, which the caller
+ *     reads after synchronising the stream.
+ *   - bf16 values travel as their raw 16-bit patterns (uint16_t).
+ *   - Entry points are thread-safe; calls that share output buffers and run
+ *     concurrently on different streams race on those buffers.
+ */
+#ifndef SC_H
+#define SC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* sc_stream_t;
+
+/* ---- status codes ---------------------------------------------------- */
+#define SC_OK 0
+#define SC_ERR_NULL 1        /* a required pointer is NULL                     */
+#define SC_ERR_ALIGN 2       /* a pointer or row stride breaks its alignment   */
+#define SC_ERR_SHAPE 3       /* a size is out of the supported range           */
+#define SC_ERR_ARG 4         /* a parameter value is invalid                   */
+#define SC_ERR_CUDA 5        /* the CUDA runtime reported an error             */
+#define SC_ERR_UNSUPPORTED 6 /* the current device cannot run this library     */
+
+/* ---- device status word bits (OR-ed by the kernels) ------------------- */
+#define SC_STATUS_DATA 0x1u             /* some row carried a data-error flag    */
+#define SC_STATUS_TIMEOUT_LOAD 0x2u     /* a bulk-copy wait ran out (about 1 s)  */
+#define SC_STATUS_TIMEOUT_EXCHANGE 0x4u /* a cluster exchange wait ran out       */
+
+/* ---- per-row flag bits (sc_row_diag.flags) ---------------------------- */
+#define SC_FLAG_MASKED 0x1u        /* padding row: row_response < 0             */
+#define SC_FLAG_BAD_ID 0x2u        /* a recorded id outside [0, V) was ignored   */
+#define SC_FLAG_DUP_ID 0x4u        /* a repeated recorded id was ignored         */
+#define SC_FLAG_BAD_SAMPLED 0x8u   /* sampled id outside [0, V): row zeroed      */
+#define SC_FLAG_BAD_COUNT 0x10u    /* rec_count outside [0, K_max]: clamped      */
+#define SC_FLAG_BAD_RESPONSE 0x20u /* row_response >= n_resp: row zeroed         */
+#define SC_FLAG_CLAMP_PI 0x40u     /* 1 - P_H < 1e-6: denominator clamped        */
+#define SC_FLAG_CLAMP_MU 0x80u     /* 1 - Q_H < 1e-6: numerator clamped          */
+#define SC_FLAG_IS_TRUNC 0x100u    /* tis: weight truncated at tis_max           */
+#define SC_FLAG_IS_REJECT 0x200u   /* mis: weight outside [mis_min, mis_max]     */
+#define SC_FLAG_DATA_ERRORS (SC_FLAG_BAD_ID | SC_FLAG_DUP_ID | SC_FLAG_BAD_SAMPLED | \
+                             SC_FLAG_BAD_COUNT | SC_FLAG_BAD_RESPONSE)
+
+/* Importance weighting modes: the `is_mode` setting (none / tis / mis) of the
+ * settings table in the docs' "Score Centering" section.  w = exp(log p_a -
+ * rollout logprob).  tis weights the token by min(w, tis_max); mis weights it
+ * by w inside [mis_min, mis_max] and by 0 outside. */
+#define SC_IS_NONE 0
+#define SC_IS_TIS 1
+#define SC_IS_MIS 2
+
+/* Parameters of sc_center_forward_backward.  Defaults (sc_params_default):
+ * the docs' settings table -- K = 128, is_mode none, tis_max 2.0,
+ * mis_min 0.5, mis_max 5.0, centering on -- at temperature 1, scale 1. */
+typedef struct sc_params {
+    int K_max;             /* row length of rec_ids / rec_logprobs, 0..1024     */
+    int is_mode;           /* SC_IS_NONE, SC_IS_TIS or SC_IS_MIS                 */
+    float tis_max;         /* > 0                                               */
+    float mis_min;         /* 0 <= mis_min <= mis_max                            */
+    float mis_max;
+    int centering;         /* 1: score centering; 0: plain (weighted) score      */
+    float inv_temperature; /* 1 / rollout temperature, finite, > 0               */
+    float grad_scale;      /* multiplies every gradient element, e.g. 1 / N_tok */
+    int cluster_size;      /* CTAs sharing one row: 0 = automatic, else 1..16   */
+    int threads;           /* threads per CTA: 0 = automatic, else 128, 256,
+                              384 or 512                                        */
+} sc_params;
+
+/* Per-row diagnostics, 64 bytes.  Masked and error rows hold zeros and their
+ * flags.  loss is the unscaled token loss; the batch loss whose gradient is
+ * grad_out is grad_scale * sum(loss). */
+typedef struct sc_row_diag {
+    float loss;        /* -A_w [log p_a - sum_H c_v log p_v]                    */
+    float logp_a;      /* log p_a (same as logp_out)                            */
+    float P_H;         /* current mass on the recorded ids                      */
+    float tail_pi;     /* 1 - P_H, accumulated directly over the unrecorded ids */
+    float Q_H;         /* recorded (sampler) mass                               */
+    float tail_mu;     /* 1 - Q_H                                               */
+    float rho;         /* max(1-Q_H,1e-6) / max(1-P_H,1e-6)                     */
+    float s;           /* 1 - Q_H + rho P_H (1 when centering is off)           */
+    float entropy;     /* -sum p log p                                          */
+    float k3;          /* exp(d) - 1 - d, d = log p_a - rollout logprob         */
+    float is_weight;   /* importance weight applied to A (1 for none)           */
+    float row_sum;     /* sum of the row's FP32 gradient before bf16 rounding   */
+    float adv;         /* the row's advantage A before the importance weight    */
+    int32_t n_valid_k; /* recorded ids used                                     */
+    uint32_t flags;    /* SC_FLAG_* bits                                        */
+    uint32_t reserved;
+} sc_row_diag;
+
+/* Fills *p with the defaults above.  Returns SC_OK or SC_ERR_NULL. */
+int sc_params_default(sc_params* p);
+
+/*
+ * GRPO group advantages (docs "Score Centering" page, section "Training":
+ * rollout-level advantages with group standard-deviation normalisation; the
+ * devotd.net release note, section 4: rewards stay fractional, no overflow in
+ * the denominator, and the paper's mean-only variant).
+ *
+ *   A_i = (r_i - mean_g) / (std_g + eps)   (normalize_std = 1)
+ *   A_i =  r_i - mean_g                    (normalize_std = 0)
+ *
+ * rewards : FP32 [n_groups * group_size], group-major (group g holds
+ *           rewards[g*group_size .. (g+1)*group_size)).
+ * adv_out : FP32 [n_groups * group_size]; may alias rewards exactly.
+ * std is the unbiased (n - 1) sample std, computed in FP64 with two passes;
+ * a group whose rewards are all equal (including a group of one) gets
+ * exactly 0.  n_groups == 0 is a no-op.
+ * Errors: SC_ERR_NULL (pointer NULL with n_groups > 0), SC_ERR_SHAPE
+ * (n_groups < 0, group_size < 1 or > 65536), SC_ERR_ARG (eps negative or
+ * not finite, partial overlap), SC_ERR_ALIGN (pointer not 4-byte aligned),
+ * SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
+ */
+int sc_group_advantages(const float* rewards, int n_groups, int group_size, int normalize_std,
+                        float eps, float* adv_out, sc_stream_t stream);
+
+/*
+ * Score-centered forward and backward over T token rows (docs "Score
+ * Centering" page, section "Score Centering"; one fused kernel).
+ *
+ * logits          : bf16 [T, logits_stride], the first V entries of each row
+ *                   are the trainer's raw logits; 16-byte aligned,
+ *                   logits_stride % 8 == 0, logits_stride >= V.  Finite
+ *                   values above -2^100 (the value -2^100 is reserved inside
+ *                   the kernel).
+ * rec_ids         : int32 [T, K_max] recorded candidate ids (top-K of the
+ *                   sampler); entries past rec_count[t] are ignored.
+ * rec_logprobs    : FP32 [T, K_max] their sampler log-probabilities, in
+ *                   their original normalisation (their sum may be below 1).
+ * rec_count       : int32 [T] number of recorded ids per row, or NULL for
+ *                   K_max everywhere.
+ * sampled_id      : int32 [T] the sampled token a (may lie outside H).
+ * rollout_logprob : FP32 [T] the sampler's own log-probability of a, or
+ *                   NULL (then k3 = 0; is_mode must be SC_IS_NONE).
+ * row_response    : int32 [T] response index of each row, -1 for padding.
+ * adv             : FP32 [n_resp] the responses' advantages A.
+ * grad_out        : bf16 [T, grad_stride], written for every row (zeros for
+ *                   padding and error rows), round-to-nearest-even; 16-byte
+ *                   aligned, grad_stride % 8 == 0.  May equal `logits` (in
+ *                   place) when grad_stride == logits_stride; any other
+ *                   overlap is rejected.  Entries past V are not touched.
+ * logp_out        : FP32 [T] log p_a (0 for padding and error rows).
+ * diag_out        : sc_row_diag [T] or NULL.
+ * status_dev      : one device uint32 or NULL; SC_STATUS_* bits are OR-ed
+ *                   into it (the caller clears it).
+ * Recorded ids outside [0, V) are ignored, and a repeated id is ignored
+ * after its first occurrence; both set row flags.
+ * Errors: SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE (T < 0, V < 1,
+ * V > 1048576, K_max outside 0..1024, n_resp < 0, strides < V), SC_ERR_ARG
+ * (bad parameter values or overlap), SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
+ * T == 0 is a no-op.
+ */
+int sc_center_forward_backward(const uint16_t* logits, long long T, int V, long long logits_stride,
+                               const int32_t* rec_ids, const float* rec_logprobs,
+                               const int32_t* rec_count, const int32_t* sampled_id,
+                               const float* rollout_logprob, const int32_t* row_response,
+                               const float* adv, int n_resp, const sc_params* p, uint16_t* grad_out,
+                               long long grad_stride, float* logp_out, sc_row_diag* diag_out,
+                               uint32_t* status_dev, sc_stream_t stream);
+
+/* Launch plan the library would use for a vocabulary of V and these
+ * parameters on the current device (no launch).  Any output pointer may be
+ * NULL.  cluster_size: CTAs per row; threads: per CTA; slice: vocabulary
+ * entries per CTA; smem_bytes: dynamic shared memory per CTA;
+ * max_clusters: clusters resident at once (the persistent grid size).
+ * Errors: as sc_center_forward_backward for V, K_max and p. */
+int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* threads, int* slice,
+                  int* smem_bytes, int* max_clusters);
+
+/* Short text for a status code. */
+const char* sc_status_string(int status);
+
+/* Text of the last error returned on this thread ("" if none). */
+const char* sc_last_error(void);
+
+/* ABI version: 100 * major + minor. */
+int sc_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SC_H */

@@ -1,0 +1,244 @@
+"""GB300 (sm_103a) score centering: Python binding of the C ABI in ``include/sc.h``.
+
+This module only marshals arguments.  Every step of the computation runs in
+the CUDA library ``_build/libsc_gb300.so`` (built by :func:`build`); there is
+no fallback, and calls raise if the library is missing or the device cannot
+run it.  PyTorch provides device memory and streams.
+
+Entry points (same names as the C ABI):
+
+* :func:`sc_group_advantages` -- GRPO group-std advantages (docs "Score
+  Centering" page, section "Training").
+* :func:`sc_center_forward_backward` -- the fused score-centered forward and
+  backward over ``[T, V]`` bf16 logits (section "Score Centering").
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+from . import build as _build_mod
+
+__all__ = [
+    "build", "lib", "ScError", "Params", "params", "DIAG_DTYPE", "DIAG_FIELDS",
+    "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
+    "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS",
+]
+
+SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
+SC_IS_NONE, SC_IS_TIS, SC_IS_MIS = 0, 1, 2
+SC_STATUS_DATA, SC_STATUS_TIMEOUT_LOAD, SC_STATUS_TIMEOUT_EXCHANGE = 0x1, 0x2, 0x4
+
+FLAG_MASKED = 0x1
+FLAG_BAD_ID = 0x2
+FLAG_DUP_ID = 0x4
+FLAG_BAD_SAMPLED = 0x8
+FLAG_BAD_COUNT = 0x10
+FLAG_BAD_RESPONSE = 0x20
+FLAG_CLAMP_PI = 0x40
+FLAG_CLAMP_MU = 0x80
+FLAG_IS_TRUNC = 0x100
+FLAG_IS_REJECT = 0x200
+
+# Symbols declared in include/sc.h.
+EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_center_forward_backward",
+           "sc_plan_query", "sc_status_string", "sc_last_error", "sc_abi_version"]
+
+
+class ScError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"status {status}: {message}")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("K_max", ctypes.c_int),
+        ("is_mode", ctypes.c_int),
+        ("tis_max", ctypes.c_float),
+        ("mis_min", ctypes.c_float),
+        ("mis_max", ctypes.c_float),
+        ("centering", ctypes.c_int),
+        ("inv_temperature", ctypes.c_float),
+        ("grad_scale", ctypes.c_float),
+        ("cluster_size", ctypes.c_int),
+        ("threads", ctypes.c_int),
+    ]
+
+
+DIAG_FIELDS = ["loss", "logp_a", "P_H", "tail_pi", "Q_H", "tail_mu", "rho", "s", "entropy", "k3",
+               "is_weight", "row_sum", "adv", "n_valid_k", "flags", "reserved"]
+DIAG_DTYPE = np.dtype({"names": DIAG_FIELDS,
+                       "formats": ["<f4"] * 13 + ["<i4", "<u4", "<u4"]})
+assert DIAG_DTYPE.itemsize == 64
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (in-tree) and return its path."""
+    return _build_mod.build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded CUDA library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build_mod.LIB_PATH
+            if not os.path.exists(path):
+                raise ScError(SC_ERR_UNSUPPORTED,
+                              f"CUDA library {path} is missing: run precision_off_policy_gb300.build()")
+            L = ctypes.CDLL(path)
+            vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+            L.sc_params_default.argtypes = [ctypes.POINTER(Params)]
+            L.sc_params_default.restype = i32
+            L.sc_group_advantages.argtypes = [vp, i32, i32, i32, f32, vp, vp]
+            L.sc_group_advantages.restype = i32
+            L.sc_center_forward_backward.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                     ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
+            L.sc_center_forward_backward.restype = i32
+            L.sc_plan_query.argtypes = [i32, ctypes.POINTER(Params)] + [ctypes.POINTER(i32)] * 5
+            L.sc_plan_query.restype = i32
+            L.sc_status_string.argtypes = [i32]
+            L.sc_status_string.restype = ctypes.c_char_p
+            L.sc_last_error.argtypes = []
+            L.sc_last_error.restype = ctypes.c_char_p
+            L.sc_abi_version.argtypes = []
+            L.sc_abi_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != SC_OK:
+        L = lib()
+        raise ScError(status, f"{L.sc_status_string(status).decode()}: {L.sc_last_error().decode()}")
+
+
+def params(K_max=128, is_mode=SC_IS_NONE, tis_max=2.0, mis_min=0.5, mis_max=5.0, centering=True,
+           inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0) -> Params:
+    """Defaults are the settings table of the docs' "Score Centering" section."""
+    return Params(int(K_max), int(is_mode), float(tis_max), float(mis_min), float(mis_max),
+                  int(bool(centering)), float(inv_temperature), float(grad_scale), int(cluster_size),
+                  int(threads))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, dev, ndim=None):
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+
+
+def _rows(t, name):
+    """Row stride of a 2-D tensor whose rows are contiguous."""
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), t.shape[1])
+
+
+def sc_group_advantages(rewards: torch.Tensor, n_groups: int, group_size: int,
+                        normalize_std: bool = True, eps: float = 1e-6,
+                        out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """FP32 rewards [n_groups * group_size] (device) -> FP32 advantages."""
+    dev = rewards.device
+    _need(rewards, "rewards", torch.float32, dev)
+    if not rewards.is_contiguous() or rewards.numel() != n_groups * group_size:
+        raise ValueError("rewards must be contiguous with n_groups * group_size entries")
+    if out is None:
+        out = torch.empty_like(rewards)
+    _need(out, "out", torch.float32, dev)
+    _check(lib().sc_group_advantages(_ptr(rewards), int(n_groups), int(group_size),
+                                     int(bool(normalize_std)), float(eps), _ptr(out), _stream(stream)))
+    return out
+
+
+def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | None,
+                               rec_logprobs: torch.Tensor | None, rec_count: torch.Tensor | None,
+                               sampled_id: torch.Tensor, rollout_logprob: torch.Tensor | None,
+                               row_response: torch.Tensor, adv: torch.Tensor, p: Params,
+                               V: int | None = None, grad_out: torch.Tensor | None = None,
+                               logp_out: torch.Tensor | None = None,
+                               diag_out: torch.Tensor | None = None,
+                               status: torch.Tensor | None = None, stream=None):
+    """Score-centered forward/backward.
+
+    logits: bf16 [T, >=V] on a CUDA device with contiguous rows; rec_ids int32
+    and rec_logprobs float32 [T, K_max]; rec_count int32 [T] or None;
+    sampled_id, row_response int32 [T]; rollout_logprob float32 [T] or None;
+    adv float32 [n_resp].  grad_out may be ``logits`` (in place).  diag_out,
+    when given, is an int32 [T, 16] tensor (64-byte records, see
+    :func:`diag_to_numpy`); status an int32 [1] tensor.
+    Returns (grad_out, logp_out, diag_out).
+    """
+    dev = logits.device
+    if dev.type != "cuda":
+        raise ValueError("logits must be on a CUDA device")
+    _need(logits, "logits", torch.bfloat16, dev, 2)
+    T = logits.shape[0]
+    V = logits.shape[1] if V is None else int(V)
+    K_max = int(p.K_max)
+    for name, t, dt, nd in [("rec_ids", rec_ids, torch.int32, 2), ("rec_logprobs", rec_logprobs, torch.float32, 2),
+                            ("rec_count", rec_count, torch.int32, 1), ("sampled_id", sampled_id, torch.int32, 1),
+                            ("rollout_logprob", rollout_logprob, torch.float32, 1),
+                            ("row_response", row_response, torch.int32, 1), ("adv", adv, torch.float32, 1)]:
+        _need(t, name, dt, dev, nd)
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if K_max > 0 and (rec_ids.shape != (T, K_max) or rec_logprobs.shape != (T, K_max)):
+        raise ValueError("rec_ids / rec_logprobs must be [T, K_max]")
+    if grad_out is None:
+        grad_out = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+    _need(grad_out, "grad_out", torch.bfloat16, dev, 2)
+    if logp_out is None:
+        logp_out = torch.empty(T, dtype=torch.float32, device=dev)
+    _need(logp_out, "logp_out", torch.float32, dev, 1)
+    if diag_out is not None:
+        _need(diag_out, "diag_out", torch.int32, dev, 2)
+        if diag_out.shape != (T, 16) or not diag_out.is_contiguous():
+            raise ValueError("diag_out must be a contiguous int32 [T, 16] tensor")
+    if status is not None:
+        _need(status, "status", torch.int32, dev, 1)
+    if T == 0:
+        return grad_out, logp_out, diag_out
+    _check(lib().sc_center_forward_backward(
+        _ptr(logits), T, V, _rows(logits, "logits"), _ptr(rec_ids) if K_max else None,
+        _ptr(rec_logprobs) if K_max else None, _ptr(rec_count), _ptr(sampled_id), _ptr(rollout_logprob),
+        _ptr(row_response), _ptr(adv), int(adv.numel()), ctypes.byref(p), _ptr(grad_out),
+        _rows(grad_out, "grad_out"), _ptr(logp_out), _ptr(diag_out), _ptr(status), _stream(stream)))
+    return grad_out, logp_out, diag_out
+
+
+def sc_plan_query(V: int, p: Params) -> dict:
+    """The launch plan the library uses for V on the current device."""
+    out = [ctypes.c_int(0) for _ in range(5)]
+    _check(lib().sc_plan_query(int(V), ctypes.byref(p), *[ctypes.byref(o) for o in out]))
+    return dict(zip(["cluster_size", "threads", "slice", "smem_bytes", "max_clusters"], [o.value for o in out]))
+
+
+def diag_to_numpy(diag: torch.Tensor) -> np.ndarray:
+    """int32 [T, 16] diagnostics tensor -> numpy structured array [T]."""
+    return diag.detach().cpu().contiguous().numpy().view(DIAG_DTYPE).reshape(-1)

@@ -1,0 +1,98 @@
+// sc_advantages.cu -- GRPO group advantages (one warp per group).
+//
+// Follows the "Training" section of the Agent Lightning "Score Centering"
+// docs page (rollout-level advantages with group standard-deviation
+// normalisation) and section 4 of the devotd.net release note (rewards stay
+// fractional FP32, no overflow in the denominator, mean-only variant).
+//
+// Statistics are taken in FP64 with two passes (mean, then the centred sum of
+// squares), so squares of large FP32 rewards cannot overflow.  A group whose
+// rewards are all equal is detected exactly (min == max) and gets A = 0
+// without any division.
+#include <cmath>
+
+#include "sc_internal.h"
+
+namespace sc {
+namespace {
+
+__device__ __forceinline__ double warp_sum_f64(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_min_f32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_max_f32(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Grid: one 32-thread block per group.
+__global__ void __launch_bounds__(32) group_adv_kernel(const float* rewards, int group_size,
+                                                       int normalize_std, float eps, float* adv) {
+    const int lane = threadIdx.x;
+    const long long base = static_cast<long long>(blockIdx.x) * group_size;
+    const float* r = rewards + base;
+    float mn = INFINITY, mx = -INFINITY;
+    double sum = 0.0;
+    for (int i = lane; i < group_size; i += 32) {
+        const float v = r[i];
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+        sum += static_cast<double>(v);
+    }
+    mn = warp_min_f32(mn);
+    mx = warp_max_f32(mx);
+    sum = warp_sum_f64(sum);
+    if (mn == mx) {  // all equal (also a group of one)
+        for (int i = lane; i < group_size; i += 32) adv[base + i] = 0.0f;
+        return;
+    }
+    const double mean = sum / group_size;
+    double ss = 0.0;
+    for (int i = lane; i < group_size; i += 32) {
+        const double d = static_cast<double>(r[i]) - mean;
+        ss += d * d;
+    }
+    ss = warp_sum_f64(ss);
+    const double denom = sqrt(ss / (group_size - 1)) + static_cast<double>(eps);
+    // Each lane reads and writes only its own indices, so adv may alias rewards.
+    for (int i = lane; i < group_size; i += 32) {
+        const double d = static_cast<double>(r[i]) - mean;
+        adv[base + i] = static_cast<float>(normalize_std ? d / denom : d);
+    }
+}
+
+}  // namespace
+}  // namespace sc
+
+extern "C" int sc_group_advantages(const float* rewards, int n_groups, int group_size,
+                                   int normalize_std, float eps, float* adv_out, sc_stream_t stream) {
+    using namespace sc;
+    if (n_groups < 0) return fail(SC_ERR_SHAPE, "n_groups = %d < 0", n_groups);
+    if (group_size < 1 || group_size > 65536)
+        return fail(SC_ERR_SHAPE, "group_size = %d outside 1..65536", group_size);
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(SC_ERR_ARG, "eps must be finite and >= 0");
+    if (n_groups == 0) return ok();
+    if (!rewards || !adv_out) return fail(SC_ERR_NULL, "rewards or adv_out is NULL");
+    if (!aligned(rewards, 4) || !aligned(adv_out, 4))
+        return fail(SC_ERR_ALIGN, "rewards and adv_out must be 4-byte aligned");
+    const char* r0 = reinterpret_cast<const char*>(rewards);
+    const char* a0 = reinterpret_cast<const char*>(adv_out);
+    const long long bytes = 4LL * n_groups * group_size;
+    if (r0 != a0 && r0 < a0 + bytes && a0 < r0 + bytes)
+        return fail(SC_ERR_ARG, "adv_out partially overlaps rewards");
+    int dev = 0;
+    int st = check_device(&dev);
+    if (st != SC_OK) return st;
+    group_adv_kernel<<<n_groups, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        rewards, group_size, normalize_std ? 1 : 0, eps, adv_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "group_adv_kernel launch");
+    return ok();
+}

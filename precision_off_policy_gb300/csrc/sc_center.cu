@@ -1,0 +1,880 @@
+// sc_center.cu -- fused score-centered forward/backward over [T, V] bf16 logits.
+//
+// Implements the token loss of the Agent Lightning docs page "Score
+// Centering", section "Score Centering":
+//   P_H = sum_H p_v,  Q_H = sum_H q_v,  rho = max(1-Q_H,1e-6)/max(1-P_H,1e-6),
+//   loss = -sg(A) [log p_a - sum_H sg(q_v - rho p_v) log p_v],
+// and its gradient with respect to the raw logits,
+//   g_v = scale (1/T) (-A) ([v==a] - mu_hat_v),
+//   mu_hat_v = s p_v + [v in H](q_v - rho p_v),  s = 1 - Q_H + rho P_H,
+// plus log p_a and per-row diagnostics (the section's K3, entropy, masses).
+//
+// GB300 design.  One row is shared by a cluster of C CTAs; CTA r owns the
+// vocabulary slice [r*S, min((r+1)*S, V)).  Per row and CTA:
+//   1. the slice is copied HBM -> shared memory by the TMA engine (1-D bulk
+//      copies in chunks, each completing on its own mbarrier);
+//   2. max pass on packed bf16 pairs as chunks land;
+//   3. warp 0 gathers the recorded ids that fall in the slice, drops repeats,
+//      pushes their logits to every CTA of the cluster (DSMEM) and overwrites
+//      them in shared memory with -2^100, so that
+//   4. the exp pass over the slice accumulates the unrecorded mass
+//      sum_{v not in H} e^{x_v - m} directly (no 1 - P_H cancellation) and
+//      the entropy term;
+//   5. partials travel to every CTA over DSMEM and an mbarrier with
+//      cluster-scope release/acquire; warp 0 of each CTA then computes the
+//      row scalars (LSE, P_H, Q_H, rho, s, loss, k3, IS weight) redundantly;
+//   6. the write pass recomputes p_v from shared memory and streams
+//      g_v = beta p_v straight to global memory with 16-byte stores and an
+//      evict-first L2 hint; the <= K+1 special entries (recorded ids and the
+//      sampled token) are patched in registers via a per-vector bitmap.
+// Every logit is read from HBM once and every gradient written once.  The
+// grid is persistent: as many clusters as fit, looping over rows.  Every
+// wait is bounded (about 1 s) and reports through the status word.
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "sc_device.cuh"
+#include "sc_internal.h"
+
+namespace sc {
+namespace {
+
+constexpr int kMaxCluster = 16;
+constexpr int kMaxChunks = 16;
+constexpr int kMaxK = 1024;
+constexpr int kMaxV = 1 << 20;
+constexpr int kMaxSmem = 232448;          // 227 KiB of dynamic shared memory per CTA
+constexpr int kTargetSliceBytes = 40960;  // automatic plan: ~40 KiB of logits per CTA
+constexpr int kChunkVecTarget = 256;      // 16-byte vectors per bulk copy (4 KiB)
+constexpr uint16_t kSentinel = 0xF180u;   // bf16 -2^100: marks recorded ids in shared memory
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kTailFloor = 1e-6f;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+struct Layout {
+    int off_bars, off_part, off_frs, off_za, off_xh, off_ids, off_lps, off_fixi, off_fixk, off_fixv,
+        off_bmp, off_red, off_scal, total;
+};
+
+struct KArgs {
+    const uint16_t* logits;
+    const int32_t* ids;
+    const float* lps;
+    const int32_t* cnt;
+    const int32_t* sampled;
+    const float* rollout;
+    const int32_t* resp;
+    const float* adv;
+    uint16_t* grad;
+    float* logp;
+    sc_row_diag* diag;
+    uint32_t* status;
+    long long T, lstride, gstride;
+    int V, K_max, n_resp;
+    int is_mode, centering;
+    float tis_max, mis_min, mis_max, inv_t, grad_scale;
+    int C, S, ncv;
+    Layout L;
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_or(uint32_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint16_t f_to_bf_bits(float x) {
+    return static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT) center_kernel(const __grid_constant__ KArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t crank = cluster_ctarank();
+    const uint32_t cid = cluster_id_x();
+    const uint32_t ncl = num_clusters_x();
+    const int C = a.C;
+    const int K_max = a.K_max;
+
+    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);
+    const uint32_t buf_s = smem_addr(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.L.off_bars);  // [kMaxChunks + 2]
+    float4* part = reinterpret_cast<float4*>(smem + a.L.off_part);      // [2][kMaxCluster]
+    float2* frs = reinterpret_cast<float2*>(smem + a.L.off_frs);        // [kMaxCluster]
+    float2* za = reinterpret_cast<float2*>(smem + a.L.off_za);          // [2]
+    float2* xh = reinterpret_cast<float2*>(smem + a.L.off_xh);          // [2][K_max]
+    int* ids_s = reinterpret_cast<int*>(smem + a.L.off_ids);            // [K_max]
+    float* lps_s = reinterpret_cast<float*>(smem + a.L.off_lps);        // [K_max]
+    int* fix_i = reinterpret_cast<int*>(smem + a.L.off_fixi);           // [K_max + 1]
+    int* fix_k = reinterpret_cast<int*>(smem + a.L.off_fixk);           // [K_max + 1]
+    float* fix_v = reinterpret_cast<float*>(smem + a.L.off_fixv);       // [K_max + 1]
+    uint32_t* bmp = reinterpret_cast<uint32_t*>(smem + a.L.off_bmp);    // one bit per 8 entries
+    float* red = reinterpret_cast<float*>(smem + a.L.off_red);          // [4][NW]
+    float* scal = reinterpret_cast<float*>(smem + a.L.off_scal);        // [8]
+    int* scal_i = reinterpret_cast<int*>(scal);
+
+    const int lo = static_cast<int>(crank) * a.S;
+    const int hi = min(lo + a.S, a.V);
+    const int n = max(hi - lo, 0);
+    const int n8 = n & ~7, nvb = n8 >> 3, tail = n - n8, nv = nvb + (tail ? 1 : 0);
+    const int nchunks = (nvb + a.ncv - 1) / a.ncv;
+    const int nwords = (a.S / 8 + 31) / 32;
+    const uint32_t xbar0 = smem_addr(&bars[kMaxChunks]);
+
+    if (tid == 0) {
+        for (int i = 0; i < kMaxChunks; ++i) mbar_init(smem_addr(&bars[i]), 1u);
+        // exchange barriers: every lane of warp 0 of every CTA arrives once per row
+        mbar_init(xbar0, 32u * static_cast<uint32_t>(C));
+        mbar_init(xbar0 + 8, 32u * static_cast<uint32_t>(C));
+        fence_mbar_init_cluster();
+    }
+    for (int i = tid; i < nwords; i += NT) bmp[i] = 0u;
+    cluster_sync_all();  // peers' barriers exist before anyone arrives on them
+
+    const uint64_t pol = l2_policy_evict_first();
+    const float kscale = a.inv_t * kLog2e;
+    uint32_t nvalid = 0;
+    float rs_prev = 0.0f;  // thread 0: this CTA's share of the previous valid row's sum
+    long long t_prev = -1;
+    bool abort = false;
+
+    for (long long t = cid; t < a.T; t += ncl) {
+        const int resp = __ldg(a.resp + t);
+        const int sa = __ldg(a.sampled + t);
+        uint32_t zflags = 0;
+        if (resp < 0)
+            zflags = SC_FLAG_MASKED;
+        else if (resp >= a.n_resp)
+            zflags = SC_FLAG_BAD_RESPONSE;
+        else if (sa < 0 || sa >= a.V)
+            zflags = SC_FLAG_BAD_SAMPLED;
+        uint16_t* grow = a.grad + t * a.gstride + lo;
+        if (zflags) {
+            for (int j = tid; j < nvb; j += NT) st_global_v4_hint(grow + 8 * j, 0u, 0u, 0u, 0u, pol);
+            if (tid < tail) grow[n8 + tid] = 0;
+            if (crank == 0 && tid == 0) {
+                a.logp[t] = 0.0f;
+                if (a.diag) {
+                    sc_row_diag d;
+                    memset(&d, 0, sizeof d);
+                    d.flags = zflags;
+                    a.diag[t] = d;
+                }
+                if ((zflags & SC_FLAG_DATA_ERRORS) && a.status) atomicOr(a.status, SC_STATUS_DATA);
+            }
+            continue;
+        }
+
+        const uint32_t par = nvalid & 1u;
+        const uint32_t lph = nvalid & 1u;
+        const uint32_t xph = (nvalid >> 1) & 1u;
+        const uint16_t* lrow = a.logits + t * a.lstride + lo;
+
+        // ---- 1. bulk copies of the slice, tail by plain loads ----------------
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            for (int i = 0; i < nchunks; ++i) {
+                const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+                const uint32_t bar = smem_addr(&bars[i]);
+                mbar_expect_tx(bar, bytes);
+                bulk_load(buf_s + 16u * v0, lrow + 8 * v0, bytes, bar, pol);
+            }
+        }
+        float tmax = -INFINITY;
+        if (tail && tid < 8) {
+            uint16_t h = kSentinel;
+            if (tid < tail) {
+                h = lrow[n8 + tid];
+                tmax = bf_to_f(h);
+            }
+            buf[n8 + tid] = h;
+        }
+        int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
+        uint32_t rflags = 0;
+        if (cnt < 0 || cnt > K_max) {
+            rflags |= SC_FLAG_BAD_COUNT;
+            cnt = cnt < 0 ? 0 : K_max;
+        }
+        const long long kbase = t * static_cast<long long>(K_max);
+        for (int k = tid; k < cnt; k += NT) {
+            ids_s[k] = __ldg(a.ids + kbase + k);
+            lps_s[k] = __ldg(a.lps + kbase + k);
+        }
+
+        // ---- 2. max pass, chunk by chunk as the copies land -------------------
+        uint32_t mx2 = 0xFF80FF80u;  // (-inf, -inf)
+        bool timed_out = false;
+        for (int i = 0; i < nchunks; ++i) {
+            const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+            if (!mbar_wait_bounded(smem_addr(&bars[i]), lph, kWaitLimitNs)) {
+                timed_out = true;
+                break;
+            }
+            for (int j = v0 + tid; j < v1; j += NT) {
+                const uint4 w = lds128(buf_s + 16u * j);
+                mx2 = bmax2(mx2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+            }
+        }
+        float m_loc = fmaxf(fmaxf(bf_lo(mx2), bf_hi(mx2)), tmax);
+        m_loc = warp_max(m_loc);
+        if (lane == 0) red[warp] = m_loc;
+        if (__syncthreads_or(timed_out)) {
+            if (tid == 0) {
+                if (a.status) atomicOr(a.status, SC_STATUS_TIMEOUT_LOAD);
+                // let copies still in flight land before the CTA stops (bounded again)
+                for (int i = 0; i < nchunks; ++i)
+                    (void)mbar_wait_bounded(smem_addr(&bars[i]), lph, kWaitLimitNs);
+            }
+            abort = true;
+            break;
+        }
+        m_loc = red[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) m_loc = fmaxf(m_loc, red[w]);
+
+        // ---- 3. gather the recorded ids of this slice (warp 0) ----------------
+        if (warp == 0) {
+            const bool a_own = sa >= lo && sa < hi;
+            if (a_own && lane == 0) {
+                const float zav = bf_to_f(buf[sa - lo]);
+                const uint32_t za_s = smem_addr(&za[par]);
+                for (int r = 0; r < C; ++r)
+                    st_cluster_v2(map_to_rank(za_s, r), __float_as_uint(zav), 1u);
+            }
+            __syncwarp();
+            int nfix = 0;
+            bool a_in_h = false;
+            const uint32_t xh_s = smem_addr(xh + static_cast<int>(par) * K_max);
+            for (int base = 0; base < cnt; base += 32) {
+                const int k = base + lane;
+                const bool in = k < cnt;
+                const int id = in ? ids_s[k] : -1;
+                const bool owned = in && id >= lo && id < hi;
+                const unsigned same = __match_any_sync(0xFFFFFFFFu, owned ? id : -1 - lane);
+                const bool first = owned && (same & lanemask_lt()) == 0u;
+                const uint16_t h = owned ? buf[id - lo] : static_cast<uint16_t>(0);
+                const bool valid = first && h != kSentinel;
+                __syncwarp();
+                if (valid) buf[id - lo] = kSentinel;
+                if (owned) {
+                    const uint32_t fz = __float_as_uint(bf_to_f(h));
+                    const uint32_t fl = valid ? 1u : 2u;
+                    for (int r = 0; r < C; ++r) st_cluster_v2(map_to_rank(xh_s + 8u * k, r), fz, fl);
+                }
+                const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
+                if (valid) {
+                    const int pos = nfix + __popc(vm & lanemask_lt());
+                    fix_i[pos] = id - lo;
+                    fix_k[pos] = k;
+                }
+                nfix += __popc(vm);
+                a_in_h = a_in_h || __any_sync(0xFFFFFFFFu, valid && id == sa);
+                __syncwarp();
+            }
+            if (a_own && !a_in_h) {
+                if (lane == 0) {
+                    fix_i[nfix] = sa - lo;
+                    fix_k[nfix] = -1;
+                }
+                nfix += 1;
+            }
+            __syncwarp();
+            for (int e = lane; e < nfix; e += 32) {
+                const int li = fix_i[e];
+                atomicOr(&bmp[li >> 8], 1u << ((li >> 3) & 31));
+            }
+            if (lane == 0) scal_i[3] = nfix;
+        }
+        __syncthreads();
+
+        // ---- 4. exp pass over the unrecorded entries --------------------------
+        const float o_c = m_loc * kscale;
+        float s1 = 0.0f, s2 = 0.0f;
+        for (int j = tid; j < nv; j += NT) {
+            const uint4 w = lds128(buf_s + 16u * j);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float y0 = fmaf(bf_lo(ww[q]), kscale, -o_c);
+                const float y1 = fmaf(bf_hi(ww[q]), kscale, -o_c);
+                const float e0 = ex2(y0), e1 = ex2(y1);
+                s1 += e0;
+                s1 += e1;
+                s2 = fmaf(e0, y0, s2);
+                s2 = fmaf(e1, y1, s2);
+            }
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        if (lane == 0) {
+            red[NW + warp] = s1;
+            red[2 * NW + warp] = s2;
+        }
+        __syncthreads();
+
+        // ---- 5. cluster exchange and row scalars (warp 0) ----------------------
+        if (warp == 0) {
+            if (lane == 0) {
+                float S1 = 0.0f, S2 = 0.0f;
+                for (int w = 0; w < NW; ++w) {
+                    S1 += red[NW + w];
+                    S2 += red[2 * NW + w];
+                }
+                const uint32_t ps = smem_addr(part + static_cast<int>(par) * kMaxCluster + crank);
+                for (int r = 0; r < C; ++r)
+                    st_cluster_v4(map_to_rank(ps, r), __float_as_uint(m_loc), __float_as_uint(S1),
+                                  __float_as_uint(S2), __float_as_uint(rs_prev));
+            }
+            // each lane's release covers its own pushes to the peers
+            const uint32_t xb = xbar0 + 8u * par;
+            for (int r = 0; r < C; ++r) mbar_arrive_cluster(map_to_rank(xb, r));
+            const bool got = mbar_wait_cluster_bounded(xb, xph, kWaitLimitNs);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) {
+                    if (a.status) atomicOr(a.status, SC_STATUS_TIMEOUT_EXCHANGE);
+                    scal_i[4] = 1;
+                }
+            } else {
+                const float4* pp = part + static_cast<int>(par) * kMaxCluster;
+                float m = -INFINITY;
+                for (int r = 0; r < C; ++r) m = fmaxf(m, pp[r].x);
+                const float o = m * kscale;
+                float lT = 0.0f, ET = 0.0f;
+                for (int r = 0; r < C; ++r) {
+                    const float4 pr = pp[r];
+                    if (pr.y > 0.0f) {
+                        const float d = pr.x * kscale - o;
+                        const float f = ex2(d);
+                        lT += pr.y * f;
+                        ET += f * (pr.z + d * pr.y);
+                    }
+                }
+                const float2* xr = xh + static_cast<int>(par) * K_max;
+                float lH = 0.0f, EH = 0.0f, lp_best = -INFINITY;
+                int nval = 0, k_best = 0x7FFFFFFF;
+                uint32_t kfl = 0;
+                for (int k = lane; k < cnt; k += 32) {
+                    const int id = ids_s[k];
+                    if (id < 0 || id >= a.V) {
+                        kfl |= SC_FLAG_BAD_ID;
+                        continue;
+                    }
+                    const float2 x = xr[k];
+                    if (__float_as_uint(x.y) != 1u) {
+                        kfl |= SC_FLAG_DUP_ID;
+                        continue;
+                    }
+                    const float y = fmaf(x.x, kscale, -o);
+                    const float e = ex2(y);
+                    lH += e;
+                    EH = fmaf(e, y, EH);
+                    ++nval;
+                    const float lp = lps_s[k];
+                    if (lp > lp_best) {
+                        lp_best = lp;
+                        k_best = k;
+                    }
+                }
+                lH = warp_sum(lH);
+                EH = warp_sum(EH);
+                nval = warp_sum_i(nval);
+                kfl = warp_or(kfl);
+                // arg-max of the recorded logprobs (lowest k on ties)
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ol = __shfl_xor_sync(0xFFFFFFFFu, lp_best, off);
+                    const int ok = __shfl_xor_sync(0xFFFFFFFFu, k_best, off);
+                    if (ol > lp_best || (ol == lp_best && ok < k_best)) {
+                        lp_best = ol;
+                        k_best = ok;
+                    }
+                }
+                // 1 - Q_H without cancellation: -expm1(l_max) minus the other q's in FP64
+                double qrest = 0.0;
+                for (int k = lane; k < cnt; k += 32) {
+                    const int id = ids_s[k];
+                    if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u || k == k_best) continue;
+                    qrest += static_cast<double>(expf(lps_s[k]));
+                }
+                qrest = warp_sum_d(qrest);
+                double tail_mu_d = 1.0, Q_H_d = 0.0;
+                if (nval > 0) {
+                    tail_mu_d = static_cast<double>(-expm1f(lp_best)) - qrest;
+                    Q_H_d = static_cast<double>(expf(lp_best)) + qrest;
+                }
+                const float tail_mu = static_cast<float>(tail_mu_d);
+                const float l = lT + lH;
+                const float log2l = log2f(l);
+                const float P_H = lH / l;
+                const float tail_pi = lT / l;
+                const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
+                uint32_t flags = rflags | kfl;
+                if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
+                if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
+                const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
+                const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
+                const float ya = fmaf(za[par].x, kscale, -o);
+                const float logp_a = (ya - log2l) * kLn2;
+                float wt = 1.0f, k3 = 0.0f;
+                if (a.rollout) {
+                    const float d = logp_a - __ldg(a.rollout + t);
+                    k3 = expm1f(d) - d;
+                    const float w = expf(d);
+                    if (a.is_mode == SC_IS_TIS) {
+                        if (w > a.tis_max) {
+                            wt = a.tis_max;
+                            flags |= SC_FLAG_IS_TRUNC;
+                        } else {
+                            wt = w;
+                        }
+                    } else if (a.is_mode == SC_IS_MIS) {
+                        if (w >= a.mis_min && w <= a.mis_max) {
+                            wt = w;
+                        } else {
+                            wt = 0.0f;
+                            flags |= SC_FLAG_IS_REJECT;
+                        }
+                    }
+                }
+                const float A = __ldg(a.adv + resp);
+                const float Aw = A * wt;
+                float csum = 0.0f;
+                if (a.centering) {
+                    for (int k = lane; k < cnt; k += 32) {
+                        const int id = ids_s[k];
+                        if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u) continue;
+                        const float lk = fmaf(xr[k].x, kscale, -o) - log2l;  // log2 p_k
+                        const float c = expf(lps_s[k]) - rho * ex2(lk);
+                        csum = fmaf(c, lk * kLn2, csum);
+                    }
+                    csum = warp_sum(csum);
+                }
+                const float loss = -Aw * (logp_a - csum);
+                const float entropy = kLn2 * (log2l - (ET + EH) / l);
+                const float alpha = -a.grad_scale * a.inv_t * Aw;
+                const float beta = -alpha * s;
+                const int nfix = scal_i[3];
+                for (int e = lane; e < nfix; e += 32) {
+                    const int k = fix_k[e];
+                    float g;
+                    if (k >= 0) {
+                        const float p = ex2(fmaf(xr[k].x, kscale, -o) - log2l);
+                        const float mu = a.centering ? fmaf(dsr, p, expf(lps_s[k])) : p;
+                        g = alpha * ((ids_s[k] == sa ? 1.0f : 0.0f) - mu);
+                    } else {
+                        g = alpha * (1.0f - s * ex2(ya - log2l));
+                    }
+                    fix_v[e] = g;
+                }
+                if (lane == 0) {
+                    scal[0] = o + log2l;
+                    scal[1] = beta;
+                    scal_i[4] = 0;
+                    if (crank == 0) {
+                        a.logp[t] = logp_a;
+                        if (a.diag) {
+                            sc_row_diag d;
+                            d.loss = loss;
+                            d.logp_a = logp_a;
+                            d.P_H = P_H;
+                            d.tail_pi = tail_pi;
+                            d.Q_H = static_cast<float>(Q_H_d);
+                            d.tail_mu = tail_mu;
+                            d.rho = rho;
+                            d.s = s;
+                            d.entropy = entropy;
+                            d.k3 = k3;
+                            d.is_weight = wt;
+                            d.row_sum = 0.0f;
+                            d.adv = A;
+                            d.n_valid_k = nval;
+                            d.flags = flags;
+                            d.reserved = 0;
+                            a.diag[t] = d;
+                            if (t_prev >= 0) {
+                                float rsum = 0.0f;
+                                for (int r = 0; r < C; ++r) rsum += pp[r].w;
+                                a.diag[t_prev].row_sum = rsum;
+                            }
+                        }
+                        if ((flags & SC_FLAG_DATA_ERRORS) && a.status) atomicOr(a.status, SC_STATUS_DATA);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        if (scal_i[4]) {
+            abort = true;
+            break;
+        }
+
+        // ---- 6. write pass: g = beta * p, patched at recorded ids and a --------
+        const float bw = scal[0];
+        const float beta = scal[1];
+        const int nfix = scal_i[3];
+        float rs = 0.0f;
+        for (int j = tid; j < nvb; j += NT) {
+            const uint4 w = lds128(buf_s + 16u * j);
+            float g[8];
+            g[0] = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
+            g[1] = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
+            g[2] = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
+            g[3] = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
+            g[4] = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
+            g[5] = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
+            g[6] = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
+            g[7] = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
+            const uint32_t word = bmp[j >> 5];  // same word for the whole warp
+            if (word != 0u && ((word >> (j & 31)) & 1u)) {
+                for (int e = 0; e < nfix; ++e) {
+                    const int li = fix_i[e];
+                    if ((li >> 3) == j) {
+                        const float v = fix_v[e];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if ((li & 7) == q) g[q] = v;
+                    }
+                }
+            }
+            rs += ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
+            st_global_v4_hint(grow + 8 * j, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                              pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]), pol);
+        }
+        if (tail && tid == 0) {
+            for (int q = 0; q < tail; ++q) {
+                const int li = n8 + q;
+                float g = beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
+                for (int e = 0; e < nfix; ++e)
+                    if (fix_i[e] == li) g = fix_v[e];
+                rs += g;
+                grow[li] = f_to_bf_bits(g);
+            }
+        }
+        rs = warp_sum(rs);
+        if (lane == 0) red[3 * NW + warp] = rs;
+        __syncthreads();
+        if (tid == 0) {
+            float tot = 0.0f;
+            for (int w = 0; w < NW; ++w) tot += red[3 * NW + w];
+            rs_prev = tot;
+        }
+        t_prev = t;
+        if (warp == 0)
+            for (int e = lane; e < nfix; e += 32) bmp[fix_i[e] >> 8] = 0u;
+        ++nvalid;
+    }
+
+    // The row sum of the last valid row goes to CTA 0 over DSMEM; the final
+    // cluster barrier also keeps every CTA's shared memory alive until no peer
+    // can still write to it.
+    if (tid == 0 && a.diag && t_prev >= 0 && !abort) {
+        const uint32_t fs = smem_addr(frs + crank);
+        st_cluster_v2(map_to_rank(fs, 0), __float_as_uint(rs_prev), 0u);
+    }
+    cluster_sync_all();
+    if (crank == 0 && tid == 0 && a.diag && t_prev >= 0 && !abort) {
+        float rsum = 0.0f;
+        for (int r = 0; r < C; ++r) rsum += frs[r].x;
+        a.diag[t_prev].row_sum = rsum;
+    }
+}
+
+// ---- host side ----------------------------------------------------------
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+struct Plan {
+    int C, NT, S, ncv;
+    Layout L;
+};
+
+Layout make_layout(int S, int K_max, int NT) {
+    Layout L;
+    int off = round_up(S * 2, 128);
+    auto take = [&](int bytes) {
+        const int o = off;
+        off = round_up(off + bytes, 16);
+        return o;
+    };
+    L.off_bars = take((kMaxChunks + 2) * 8);
+    L.off_part = take(2 * kMaxCluster * 16);
+    L.off_frs = take(kMaxCluster * 8);
+    L.off_za = take(2 * 8);
+    L.off_xh = take(2 * K_max * 8);
+    L.off_ids = take(K_max * 4);
+    L.off_lps = take(K_max * 4);
+    L.off_fixi = take((K_max + 1) * 4);
+    L.off_fixk = take((K_max + 1) * 4);
+    L.off_fixv = take((K_max + 1) * 4);
+    L.off_bmp = take(((S / 8 + 31) / 32) * 4);
+    L.off_red = take(4 * (NT / 32) * 4);
+    L.off_scal = take(8 * 4);
+    L.total = off;
+    return L;
+}
+
+int make_plan(int V, int K_max, int req_cluster, int req_threads, Plan* out) {
+    int C = req_cluster;
+    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128); };
+    if (C <= 0) {
+        C = static_cast<int>((2LL * V + kTargetSliceBytes - 1) / kTargetSliceBytes);
+        C = C < 1 ? 1 : (C > 8 ? 8 : C);
+        // no empty slice: at least 8 entries per CTA
+        while (C > 1 && static_cast<long long>(C - 1) * round_up((V + C - 1) / C, 8) >= V) --C;
+        for (;;) {
+            const int S = round_up((V + C - 1) / C, 8);
+            if (make_layout(S, K_max, threads_for(S)).total <= kMaxSmem || C >= kMaxCluster) break;
+            ++C;
+        }
+    }
+    const int S = round_up((V + C - 1) / C, 8);
+    const int NT = threads_for(S);
+    const Layout L = make_layout(S, K_max, NT);
+    if (L.total > kMaxSmem)
+        return fail(SC_ERR_SHAPE, "V = %d with cluster size %d needs %d bytes of shared memory per CTA",
+                    V, C, L.total);
+    const int nvb = S / 8;
+    int nch = (nvb + kChunkVecTarget - 1) / kChunkVecTarget;
+    nch = nch < 1 ? 1 : (nch > kMaxChunks ? kMaxChunks : nch);
+    out->C = C;
+    out->NT = NT;
+    out->S = S;
+    out->ncv = (nvb + nch - 1) / nch;
+    if (out->ncv < 1) out->ncv = 1;
+    out->L = L;
+    return SC_OK;
+}
+
+using KernelFn = void (*)(KArgs);
+
+KernelFn kernel_for(int NT) {
+    switch (NT) {
+        case 128: return center_kernel<128>;
+        case 256: return center_kernel<256>;
+        case 384: return center_kernel<384>;
+        case 512: return center_kernel<512>;
+        default: return nullptr;
+    }
+}
+
+std::mutex g_plan_mutex;
+std::map<std::tuple<int, int>, int> g_smem_set;                 // (device, NT) -> bytes allowed
+std::map<std::tuple<int, int, int, int>, int> g_max_clusters;  // (device, NT, C, smem)
+
+// Sets the kernel's shared-memory and cluster attributes and returns the
+// number of clusters that can be resident at once.
+int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
+    KernelFn fn = kernel_for(P.NT);
+    if (!fn) return fail(SC_ERR_ARG, "threads = %d is not one of 128, 256, 384, 512", P.NT);
+    std::lock_guard<std::mutex> lock(g_plan_mutex);
+    cudaError_t e;
+    auto key = std::make_tuple(dev, P.NT);
+    auto it = g_smem_set.find(key);
+    if (it == g_smem_set.end() || it->second < P.L.total) {
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+        g_smem_set[key] = kMaxSmem;
+    }
+    auto ckey = std::make_tuple(dev, P.NT, P.C, P.L.total);
+    auto cit = g_max_clusters.find(ckey);
+    if (cit != g_max_clusters.end()) {
+        *max_clusters = cit->second;
+        return SC_OK;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.C, 1, 1);
+    cfg.blockDim = dim3(P.NT, 1, 1);
+    cfg.dynamicSmemBytes = P.L.total;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = P.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(fn), &cfg);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
+    if (n <= 0)
+        return fail(SC_ERR_SHAPE, "a cluster of %d CTAs with %d bytes of shared memory does not fit",
+                    P.C, P.L.total);
+    g_max_clusters[ckey] = n;
+    *max_clusters = n;
+    return SC_OK;
+}
+
+int check_params(int V, const sc_params* p) {
+    if (!p) return fail(SC_ERR_NULL, "params is NULL");
+    if (V < 1 || V > kMaxV) return fail(SC_ERR_SHAPE, "V = %d outside 1..%d", V, kMaxV);
+    if (p->K_max < 0 || p->K_max > kMaxK) return fail(SC_ERR_SHAPE, "K_max = %d outside 0..%d", p->K_max, kMaxK);
+    if (!(p->inv_temperature > 0.0f) || !std::isfinite(p->inv_temperature) || p->inv_temperature > 1e4f)
+        return fail(SC_ERR_ARG, "inv_temperature must be finite and in (0, 1e4]");
+    if (!std::isfinite(p->grad_scale)) return fail(SC_ERR_ARG, "grad_scale must be finite");
+    if (p->is_mode < SC_IS_NONE || p->is_mode > SC_IS_MIS) return fail(SC_ERR_ARG, "is_mode = %d", p->is_mode);
+    if (p->is_mode == SC_IS_TIS && !(p->tis_max > 0.0f && std::isfinite(p->tis_max)))
+        return fail(SC_ERR_ARG, "tis_max must be finite and > 0");
+    if (p->is_mode == SC_IS_MIS &&
+        !(p->mis_min >= 0.0f && p->mis_min <= p->mis_max && std::isfinite(p->mis_max)))
+        return fail(SC_ERR_ARG, "need 0 <= mis_min <= mis_max < inf");
+    if (p->centering != 0 && p->centering != 1) return fail(SC_ERR_ARG, "centering must be 0 or 1");
+    if (p->cluster_size < 0 || p->cluster_size > kMaxCluster)
+        return fail(SC_ERR_ARG, "cluster_size = %d outside 0..%d", p->cluster_size, kMaxCluster);
+    if (p->threads != 0 && !kernel_for(p->threads))
+        return fail(SC_ERR_ARG, "threads = %d is not 0, 128, 256, 384 or 512", p->threads);
+    return SC_OK;
+}
+
+}  // namespace
+}  // namespace sc
+
+extern "C" int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* threads, int* slice,
+                             int* smem_bytes, int* max_clusters) {
+    using namespace sc;
+    int st = check_params(V, p);
+    if (st != SC_OK) return st;
+    Plan P;
+    st = make_plan(V, p->K_max, p->cluster_size, p->threads, &P);
+    if (st != SC_OK) return st;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != SC_OK) return st;
+    int mc = 0;
+    st = prepare_kernel(dev, P, &mc);
+    if (st != SC_OK) return st;
+    if (cluster_size) *cluster_size = P.C;
+    if (threads) *threads = P.NT;
+    if (slice) *slice = P.S;
+    if (smem_bytes) *smem_bytes = P.L.total;
+    if (max_clusters) *max_clusters = mc;
+    return ok();
+}
+
+extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, int V,
+                                          long long logits_stride, const int32_t* rec_ids,
+                                          const float* rec_logprobs, const int32_t* rec_count,
+                                          const int32_t* sampled_id, const float* rollout_logprob,
+                                          const int32_t* row_response, const float* adv, int n_resp,
+                                          const sc_params* p, uint16_t* grad_out, long long grad_stride,
+                                          float* logp_out, sc_row_diag* diag_out, uint32_t* status_dev,
+                                          sc_stream_t stream) {
+    using namespace sc;
+    int st = check_params(V, p);
+    if (st != SC_OK) return st;
+    if (T < 0) return fail(SC_ERR_SHAPE, "T = %lld < 0", T);
+    if (n_resp < 0) return fail(SC_ERR_SHAPE, "n_resp = %d < 0", n_resp);
+    if (logits_stride < V || grad_stride < V)
+        return fail(SC_ERR_SHAPE, "row strides (%lld, %lld) must be >= V = %d", logits_stride, grad_stride, V);
+    if (p->is_mode != SC_IS_NONE && !rollout_logprob)
+        return fail(SC_ERR_NULL, "is_mode tis/mis needs rollout_logprob");
+    if (T == 0) return ok();
+    if (!logits || !sampled_id || !row_response || !grad_out || !logp_out)
+        return fail(SC_ERR_NULL, "logits, sampled_id, row_response, grad_out and logp_out are required");
+    if (n_resp > 0 && !adv) return fail(SC_ERR_NULL, "adv is NULL with n_resp > 0");
+    if (p->K_max > 0 && (!rec_ids || !rec_logprobs))
+        return fail(SC_ERR_NULL, "rec_ids and rec_logprobs are required when K_max > 0");
+    if (!aligned(logits, 16) || !aligned(grad_out, 16))
+        return fail(SC_ERR_ALIGN, "logits and grad_out must be 16-byte aligned");
+    if (logits_stride % 8 != 0 || grad_stride % 8 != 0)
+        return fail(SC_ERR_ALIGN, "row strides must be multiples of 8 elements");
+    if (!aligned(rec_ids, 4) || !aligned(rec_logprobs, 4) || !aligned(rec_count, 4) ||
+        !aligned(sampled_id, 4) || !aligned(rollout_logprob, 4) || !aligned(row_response, 4) ||
+        !aligned(adv, 4) || !aligned(logp_out, 4) || !aligned(diag_out, 16) || !aligned(status_dev, 4))
+        return fail(SC_ERR_ALIGN, "metadata arrays must be 4-byte aligned and diag_out 16-byte aligned");
+    {
+        const char* l0 = reinterpret_cast<const char*>(logits);
+        const char* g0 = reinterpret_cast<const char*>(grad_out);
+        const long long lb = 2LL * ((T - 1) * logits_stride + V);
+        const long long gb = 2LL * ((T - 1) * grad_stride + V);
+        const bool same = (l0 == g0) && (logits_stride == grad_stride);
+        if (!same && l0 < g0 + gb && g0 < l0 + lb)
+            return fail(SC_ERR_ARG, "grad_out overlaps logits other than exactly (in place)");
+    }
+    Plan P;
+    st = make_plan(V, p->K_max, p->cluster_size, p->threads, &P);
+    if (st != SC_OK) return st;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != SC_OK) return st;
+    int mc = 0;
+    st = prepare_kernel(dev, P, &mc);
+    if (st != SC_OK) return st;
+    const long long G = T < mc ? T : mc;
+
+    KArgs ka;
+    std::memset(&ka, 0, sizeof ka);
+    ka.logits = logits;
+    ka.ids = rec_ids;
+    ka.lps = rec_logprobs;
+    ka.cnt = rec_count;
+    ka.sampled = sampled_id;
+    ka.rollout = rollout_logprob;
+    ka.resp = row_response;
+    ka.adv = adv;
+    ka.grad = grad_out;
+    ka.logp = logp_out;
+    ka.diag = diag_out;
+    ka.status = status_dev;
+    ka.T = T;
+    ka.lstride = logits_stride;
+    ka.gstride = grad_stride;
+    ka.V = V;
+    ka.K_max = p->K_max;
+    ka.n_resp = n_resp;
+    ka.is_mode = p->is_mode;
+    ka.centering = p->centering;
+    ka.tis_max = p->tis_max;
+    ka.mis_min = p->mis_min;
+    ka.mis_max = p->mis_max;
+    ka.inv_t = p->inv_temperature;
+    ka.grad_scale = p->grad_scale;
+    ka.C = P.C;
+    ka.S = P.S;
+    ka.ncv = P.ncv;
+    ka.L = P.L;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(G * P.C), 1, 1);
+    cfg.blockDim = dim3(P.NT, 1, 1);
+    cfg.dynamicSmemBytes = P.L.total;
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = P.C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NT), ka);
+    if (e != cudaSuccess) return cuda_fail(e, "center_kernel launch");
+    return ok();
+}
