@@ -1,0 +1,399 @@
+#!/usr/bin/env python3
+"""Benchmark of the score-centering hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: the group
+advantages (sc_group_advantages) and the fused score-centered forward and
+backward (sc_center_forward_backward) over the quick-check batch -- 2 prompts
+x 4 responses x 512 tokens = 4096 rows (lengths U[64, 512], the rest padding),
+V = 151936, K = 128 recorded ids, synthetic inputs from ``synth``.
+
+Prints one JSON line.  `value` is valid (unmasked) tokens per second over all
+ranks with inputs resident in HBM; `e2e` is the same metric through the same
+calls with pinned host buffers copied in and the step's outputs copied back
+inside the timed region; `roofline` relates the fused kernel's algorithmic
+bytes to the measured HBM copy bandwidth; `cpu_baseline` times the FP64 CPU
+oracle on this machine's cores on a bounded sample of the same batch.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch under torch.distributed.run: every rank processes its own
+batch (weak scaling); the only exchange is the global valid-token count,
+all-reduced once per batch to set grad_scale = 1 / N_tokens.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "score-centered tokens/s at V=151936 bf16; HBM GB/s as % of GB300 peak"
+WORKLOAD = "C2"
+WORKLOAD_TEXT = ("quick-check batch: 2 prompts x 4 responses x 512 tokens = 4096 rows, lengths U[64,512] "
+                 "padded, V=151936, K=128, logits N(0,3^2)+Zipf bias, sampler noise N(0,0.05^2)")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["precision_off_policy_gb300/csrc/sc_center.cu", "precision_off_policy_gb300/csrc/sc_device.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "center_kernel_C2_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_traffic(launch_rows: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return float(t["dram_bytes_per_launch"]) * launch_rows / float(t["rows_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def algorithmic_bytes(batch) -> int:
+    """Minimum bytes one launch must move (see the design notes): per valid
+    row the logits read and gradient write (4 V), the recorded head (8 per
+    id), its metadata (row_response, sampled id, rollout logprob, advantage:
+    16) and outputs (log p_a 4, diagnostics 64); per padding row the zero
+    gradient (2 V), row_response and sampled id (8) and outputs (68)."""
+    V = batch["V"]
+    resp = batch["row_response"].cpu().numpy()
+    valid = int((resp >= 0).sum())
+    masked = resp.size - valid
+    cnt = batch["rec_count"]
+    k_total = int(cnt.sum()) if cnt is not None else valid * batch["K"]
+    extra_cnt = 4 * valid if cnt is not None else 0
+    return valid * (4 * V + 16 + 68) + 8 * k_total + extra_cnt + masked * (2 * V + 8 + 68)
+
+
+def cpu_baseline(batch, p, adv, max_rows=None):
+    import oracle
+
+    bn = synth.to_numpy(batch)
+    bn["adv"] = adv
+    T = bn["logits"].shape[0]
+    rows = np.arange(T if max_rows is None else min(T, max_rows))
+    prm = oracle.make_params(inv_temperature=float(np.float32(p.inv_temperature)),
+                             grad_scale=float(np.float32(p.grad_scale)))
+    t0 = time.perf_counter()
+    used = 0
+    for r0 in range(0, rows.size, 512):  # bounded memory: 512 rows of FP64 gradients at a time
+        _, _, _, u = oracle.rows(bn, prm, rows[r0:r0 + 512])
+        used = max(used, u)
+    dt = time.perf_counter() - t0
+    valid = int((bn["row_response"][rows] >= 0).sum())
+    return {"value": valid / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{rows.size} rows of the {WORKLOAD} batch ({valid} valid), one pass, {dt:.2f} s wall"}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus and not (world == 1 and n_gpus == 1):
+        if world == 1:
+            raise SystemExit(f"--gpus {n_gpus} needs torch.distributed.run with {n_gpus} processes")
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    import oracle
+
+    cfg = synth.config(WORKLOAD)
+    rows_per_step = 128
+    batch = make_host_rows(cfg, rows_per_step * 2)
+    adv = oracle.group_advantages(batch["rewards"].numpy(), batch["n_groups"], batch["group_size"], True,
+                                  1e-6).astype(np.float32)
+    bn = synth.to_numpy(batch)
+    bn["adv"] = adv
+    prm = oracle.make_params(grad_scale=1.0)
+    times, valids, used = [], [], 0
+    T = bn["logits"].shape[0]
+    for s in range(args.warmup + args.steps):
+        r0 = (s * rows_per_step) % T
+        rows = np.arange(r0, min(T, r0 + rows_per_step))
+        t0 = time.perf_counter()
+        _, _, _, u = oracle.rows(bn, prm, rows)
+        dt = time.perf_counter() - t0
+        used = max(used, u)
+        if s >= args.warmup:
+            times.append(dt)
+            valids.append(int((bn["row_response"][rows] >= 0).sum()))
+    value = sum(valids) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} {WORKLOAD_TEXT}", "rows_per_step": rows_per_step,
+                   "V": cfg["V"], "K": cfg["K"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows of the {WORKLOAD} batch per step (host-generated)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def make_host_rows(cfg, n):
+    """The first `n` rows of the workload generated on the host (same recipe)."""
+    n_resp = max(cfg["n_per_prompt"], (n + cfg["L_pad"] - 1) // cfg["L_pad"])
+    n_prompts = max(1, (n_resp + cfg["n_per_prompt"] - 1) // cfg["n_per_prompt"])
+    sub = synth.config(cfg, n_prompts=min(n_prompts, cfg["n_prompts"]))
+    return synth.make_batch(sub, device="cpu")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import precision_off_policy_gb300 as sc
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sc.build()
+
+    cfg = synth.config(WORKLOAD, seed=synth.CONFIGS[WORKLOAD]["seed"] + 1000 * rank)
+    batch = synth.make_batch(cfg, device=dev)
+    T, V, K = batch["logits"].shape[0], batch["V"], batch["K"]
+    n_valid = batch["n_valid"]
+    total_valid = torch.tensor([n_valid], dtype=torch.int64, device=dev)
+    if world > 1:
+        dist.all_reduce(total_valid)  # global generated-token count for the token-mean loss
+    grad_scale = float(np.float32(1.0 / float(total_valid.item())))  # int64 -> double -> float
+    p = sc.params(K_max=K, inv_temperature=batch["inv_temperature"], grad_scale=grad_scale)
+    plan = sc.sc_plan_query(V, p)
+
+    stream = torch.cuda.Stream(device=dev)
+    grad = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    diag = torch.empty((T, 16), dtype=torch.int32, device=dev)
+    adv = torch.empty_like(batch["rewards"])
+
+    def step(s):
+        sc.sc_group_advantages(batch["rewards"], batch["n_groups"], batch["group_size"], out=adv, stream=s)
+        sc.sc_center_forward_backward(batch["logits"], batch["rec_ids"], batch["rec_logprobs"], batch["rec_count"],
+                                      batch["sampled"], batch["rollout_logprob"], batch["row_response"], adv, p,
+                                      grad_out=grad, logp_out=logp, diag_out=diag, stream=s)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(stream)
+    stream.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- device-resident timing: events around every fused launch -----------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        start.record(stream)
+        for i in range(args.steps):
+            sc.sc_group_advantages(batch["rewards"], batch["n_groups"], batch["group_size"], out=adv, stream=stream)
+            ev[i][0].record(stream)
+            sc.sc_center_forward_backward(batch["logits"], batch["rec_ids"], batch["rec_logprobs"],
+                                          batch["rec_count"], batch["sampled"], batch["rollout_logprob"],
+                                          batch["row_response"], adv, p, grad_out=grad, logp_out=logp,
+                                          diag_out=diag, stream=stream)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    t_max = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    tok = torch.tensor([n_valid * args.steps], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+        dist.all_reduce(tok)
+    elapsed_ms = float(t_max.item())
+    value = float(tok.item()) / (elapsed_ms / 1e3)
+
+    # ---- end to end: pinned host buffers in, outputs back, every step --------
+    host_in = {k: batch[k].cpu().pin_memory() for k in
+               ["logits", "rec_ids", "rec_logprobs", "sampled", "rollout_logprob", "row_response", "rewards"]}
+    host_grad = torch.empty((T, V), dtype=torch.bfloat16).pin_memory()
+    host_logp = torch.empty(T, dtype=torch.float32).pin_memory()
+    host_diag = torch.empty((T, 16), dtype=torch.int32).pin_memory()
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in (host_grad, host_logp, host_diag))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for k, v in host_in.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            sc.sc_group_advantages(dev_in["rewards"], batch["n_groups"], batch["group_size"], out=adv, stream=stream)
+            sc.sc_center_forward_backward(dev_in["logits"], dev_in["rec_ids"], dev_in["rec_logprobs"], None,
+                                          dev_in["sampled"], dev_in["rollout_logprob"], dev_in["row_response"],
+                                          adv, p, grad_out=grad, logp_out=logp, diag_out=diag, stream=stream)
+            host_grad.copy_(grad, non_blocking=True)
+            host_logp.copy_(logp, non_blocking=True)
+            host_diag.copy_(diag, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = n_valid * world * args.e2e_steps / (float(e2e_ms.item()) / 1e3)
+
+    # ---- roofline of the fused kernel ----------------------------------------
+    alg = algorithmic_bytes(batch)
+    k_avg_ms = statistics.fmean(kernel_ms)
+    achieved = alg / (k_avg_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    traffic = measured_traffic(T)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} {WORKLOAD_TEXT}", "rows": T, "valid_rows": n_valid, "V": V, "K": K,
+                   "io": "bf16 logits in, bf16 gradient out, FP32 arithmetic",
+                   "parallelism": f"dp{world} (rows sharded, no data-path collective)",
+                   "l2": "inputs larger than L2 (1.24 GB of logits per step)",
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
+                     "kernel": "center_kernel", "algorithmic_bytes_per_launch": alg,
+                     "kernel_ms": k_avg_ms},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        adv_or = oracle.group_advantages(batch["rewards"].cpu().numpy(), batch["n_groups"], batch["group_size"],
+                                         True, 1e-6).astype(np.float32)
+        line["cpu_baseline"] = cpu_baseline(batch, p, adv_or)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

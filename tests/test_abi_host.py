@@ -1,0 +1,153 @@
+"""Host-side checks of the C ABI: no GPU needed.
+
+The library must load, export every function `include/sc.h` declares, and
+reject bad arguments on the host -- before any CUDA call -- with the status
+codes the header documents.  Pointer arguments here are fake addresses that
+are never dereferenced: validation fails before anything touches them.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import precision_off_policy_gb300 as sc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sc.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    sc.build()
+    return sc.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(sc_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    assert "sc_group_advantages" in names and "sc_center_forward_backward" in names
+    assert set(names) == set(sc.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_struct_layouts_match_header(L):
+    assert ctypes.sizeof(sc.Params) == 40
+    assert sc.DIAG_DTYPE.itemsize == 64
+    p = sc.Params()
+    assert L.sc_params_default(ctypes.byref(p)) == sc.SC_OK
+    assert (p.K_max, p.is_mode, p.tis_max, p.mis_min, p.mis_max, p.centering) == (128, 0, 2.0, 0.5, 5.0, 1)
+    assert (p.inv_temperature, p.grad_scale, p.cluster_size, p.threads) == (1.0, 1.0, 0, 0)
+    assert L.sc_params_default(None) == sc.SC_ERR_NULL
+    assert L.sc_abi_version() == 100
+    assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
+
+
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
+
+
+def call_center(L, T=4, V=64, lstride=64, gstride=64, logits=FAKE, grad=FAKE * 2, ids=FAKE * 3,
+                lps=FAKE * 4, cnt=None, samp=FAKE * 5, roll=None, resp=FAKE * 6, adv=FAKE * 7, n_resp=2,
+                logp=FAKE * 8, diag=None, status=None, **pk):
+    raw_centering = pk.pop("centering", None)
+    p = sc.params(**{"K_max": 8, **pk})
+    if raw_centering is not None:
+        p.centering = raw_centering  # bypass the binding's bool() to reach the C check
+    return L.sc_center_forward_backward(logits, T, V, lstride, ids, lps, cnt, samp, roll, resp, adv, n_resp,
+                                        ctypes.byref(p), grad, gstride, logp, diag, status, None)
+
+
+def err(L):
+    return L.sc_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(V=0), sc.SC_ERR_SHAPE),
+    (dict(V=(1 << 20) + 1, lstride=(1 << 20) + 8, gstride=(1 << 20) + 8), sc.SC_ERR_SHAPE),
+    (dict(T=-1), sc.SC_ERR_SHAPE),
+    (dict(K_max=1025), sc.SC_ERR_SHAPE),
+    (dict(K_max=-1), sc.SC_ERR_SHAPE),
+    (dict(n_resp=-1), sc.SC_ERR_SHAPE),
+    (dict(lstride=32), sc.SC_ERR_SHAPE),
+    (dict(inv_temperature=0.0), sc.SC_ERR_ARG),
+    (dict(inv_temperature=float("inf")), sc.SC_ERR_ARG),
+    (dict(grad_scale=float("nan")), sc.SC_ERR_ARG),
+    (dict(is_mode=3), sc.SC_ERR_ARG),
+    (dict(is_mode=1, roll=FAKE * 9, tis_max=0.0), sc.SC_ERR_ARG),
+    (dict(is_mode=2, roll=FAKE * 9, mis_min=3.0, mis_max=1.0), sc.SC_ERR_ARG),
+    (dict(is_mode=1), sc.SC_ERR_NULL),
+    (dict(centering=2), sc.SC_ERR_ARG),
+    (dict(cluster_size=17), sc.SC_ERR_ARG),
+    (dict(threads=100), sc.SC_ERR_ARG),
+    (dict(logits=None), sc.SC_ERR_NULL),
+    (dict(grad=None), sc.SC_ERR_NULL),
+    (dict(logp=None), sc.SC_ERR_NULL),
+    (dict(samp=None), sc.SC_ERR_NULL),
+    (dict(resp=None), sc.SC_ERR_NULL),
+    (dict(adv=None), sc.SC_ERR_NULL),
+    (dict(ids=None), sc.SC_ERR_NULL),
+    (dict(logits=FAKE + 2), sc.SC_ERR_ALIGN),
+    (dict(grad=FAKE * 2 + 8), sc.SC_ERR_ALIGN),
+    (dict(lstride=68), sc.SC_ERR_ALIGN),
+    (dict(gstride=66), sc.SC_ERR_ALIGN),
+    (dict(samp=FAKE * 5 + 2), sc.SC_ERR_ALIGN),
+    (dict(diag=FAKE * 10 + 4), sc.SC_ERR_ALIGN),
+    (dict(grad=FAKE + 64), sc.SC_ERR_ARG),                       # partial overlap with logits
+    (dict(grad=FAKE, gstride=72, lstride=64), sc.SC_ERR_ARG),    # same base, different stride
+])
+def test_center_rejects_bad_arguments_on_the_host(L, kw, status):
+    assert call_center(L, **kw) == status, err(L)
+    assert err(L) != ""
+
+
+def test_center_empty_batch_is_a_no_op(L):
+    assert call_center(L, T=0, logits=None, grad=None, samp=None, resp=None, logp=None) == sc.SC_OK
+    assert err(L) == ""
+
+
+def test_center_null_params(L):
+    assert L.sc_center_forward_backward(FAKE, 1, 8, 8, None, None, None, FAKE, None, FAKE, FAKE, 1, None,
+                                        FAKE * 2, 8, FAKE * 3, None, None, None) == sc.SC_ERR_NULL
+
+
+def test_no_gpu_reaches_cuda_not_a_crash(L):
+    # Arguments that pass validation reach the CUDA runtime; without a GPU
+    # that reports an error status instead of crashing.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_center(L) in (sc.SC_ERR_CUDA, sc.SC_ERR_UNSUPPORTED)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, -1, 4, 1, 1e-6, FAKE * 2), sc.SC_ERR_SHAPE),
+    ((FAKE, 2, 0, 1, 1e-6, FAKE * 2), sc.SC_ERR_SHAPE),
+    ((FAKE, 2, 65537, 1, 1e-6, FAKE * 2), sc.SC_ERR_SHAPE),
+    ((FAKE, 2, 4, 1, -1.0, FAKE * 2), sc.SC_ERR_ARG),
+    ((FAKE, 2, 4, 1, float("nan"), FAKE * 2), sc.SC_ERR_ARG),
+    ((None, 2, 4, 1, 1e-6, FAKE * 2), sc.SC_ERR_NULL),
+    ((FAKE, 2, 4, 1, 1e-6, None), sc.SC_ERR_NULL),
+    ((FAKE + 2, 2, 4, 1, 1e-6, FAKE * 2), sc.SC_ERR_ALIGN),
+    ((FAKE, 2, 4, 1, 1e-6, FAKE + 4), sc.SC_ERR_ARG),  # partial overlap
+    ((None, 0, 4, 1, 1e-6, None), sc.SC_OK),            # nothing to do
+])
+def test_group_advantages_host_validation(L, args, status):
+    assert L.sc_group_advantages(*args, None) == status, err(L)
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(sc._build_mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(sc, "_lib", None)
+    with pytest.raises(sc.ScError):
+        sc.lib()
+    monkeypatch.undo()
+    assert sc.lib() is not None

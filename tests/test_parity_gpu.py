@@ -1,0 +1,310 @@
+"""GPU parity: the CUDA library against the FP64 oracle, element by element.
+
+Inputs come from the seeded generator (``synth``); advantages for the fused
+kernel come from the oracle's own group statistics.  Tolerances are those of
+``sc_parity``.  Sizes: the tiny configuration in full, reduced copies of the
+large ones (full vocabulary, fewer rows, several clusters' worth of rows and
+a ragged tail), and the full-size configurations with sampled rows plus
+invariants on every row.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_off_policy_gb300 as sc
+import synth
+from sc_parity import (bits_to_f64, check_rows, diag_rows, grad_bits, host_batch, oracle_adv,
+                       run_gpu, sc_params, ulp_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sc.build()
+    sc.lib()
+
+
+def _full_check(batch, p, what, inplace=False, with_rollout=True, nthreads=0, rows=None):
+    adv = oracle_adv(batch)
+    g, lp, d, status = run_gpu(batch, p, adv, inplace=inplace, with_rollout=with_rollout)
+    T = batch["logits"].shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    bn = host_batch(batch, adv, with_rollout)
+    out = []
+    for r0 in range(0, rows.size, 256):
+        rr = rows[r0:r0 + 256]
+        out.append(check_rows(bn, p, rr, grad_bits(g, rr), lp.cpu().numpy()[rr], diag_rows(d, rr),
+                              nthreads=nthreads, what=what))
+    st = int(status.item())
+    assert st & (sc.SC_STATUS_TIMEOUT_LOAD | sc.SC_STATUS_TIMEOUT_EXCHANGE) == 0, f"{what}: status {st:#x}"
+    return g, lp, d, st
+
+
+# -------------------------------------------------------------------------
+# Group advantages
+
+
+@pytest.mark.parametrize("name", ["C1", "C2", "C3", "C4", "C5"])
+def test_group_advantages_match_oracle(name):
+    cfg = synth.config(name)
+    _, rewards = synth.responses(cfg)
+    n = cfg["n_per_prompt"]
+    a_gpu = sc.sc_group_advantages(rewards.cuda(), rewards.numel() // n, n).cpu().numpy()
+    a_or = oracle.group_advantages(rewards.numpy(), rewards.numel() // n, n, True, 1e-6)
+    np.testing.assert_allclose(a_gpu, a_or, rtol=1e-6, atol=1e-7)
+
+
+def test_group_advantages_fractional_large_and_mean_only():
+    rng = np.random.default_rng(5)
+    r = np.concatenate([rng.random(64), [1.0, 1.001, 1.0, 1.0], [3e30, -3e30, 1e30, -1e30],
+                        [0.25] * 4, rng.standard_normal(37 * 4) * 1e3]).astype(np.float32)
+    ng = r.size // 4
+    for norm in (True, False):
+        a_gpu = sc.sc_group_advantages(torch.from_numpy(r).cuda(), ng, 4, norm).cpu().numpy()
+        a_or = oracle.group_advantages(r, ng, 4, norm, 1e-6)
+        np.testing.assert_allclose(a_gpu, a_or, rtol=1e-6, atol=1e-30)
+    assert np.all(a_gpu[r.size - 37 * 4 - 4:r.size - 37 * 4] == 0)  # the all-equal group
+    # large groups and in-place
+    big = torch.rand(3 * 1000, device="cuda")
+    ref = oracle.group_advantages(big.cpu().numpy(), 3, 1000, True, 1e-6)
+    sc.sc_group_advantages(big, 3, 1000, out=big)
+    np.testing.assert_allclose(big.cpu().numpy(), ref, rtol=1e-6, atol=1e-7)
+
+
+# -------------------------------------------------------------------------
+# The fused kernel
+
+
+def test_c1_tiny_full_parity():
+    batch = synth.make_batch("C1")
+    p = sc_params(batch)
+    _, _, _, st = _full_check(batch, p, "C1")
+    assert st == 0
+
+
+def test_c1_without_rollout_logprob():
+    batch = synth.make_batch("C1")
+    _, _, d, _ = _full_check(batch, sc_params(batch), "C1 no rollout", with_rollout=False)
+    assert np.all(sc.diag_to_numpy(d)["k3"] == 0)
+
+
+@pytest.mark.parametrize("name", ["C2", "C4", "C5"])
+def test_reduced_configs_full_parity(name):
+    # full vocabulary, a few responses: several rows per cluster, padding,
+    # ragged counts and the peaked large-vocabulary rows.
+    over = dict(n_prompts=1, n_per_prompt=4 if name != "C5" else 8, L_pad=24)
+    if name == "C2":
+        over.update(len_lo=5, len_hi=24)
+    batch = synth.make_batch(synth.config(name, **over))
+    _full_check(batch, sc_params(batch), f"{name} reduced")
+
+
+def test_c3_chunk_reduced_full_parity():
+    cfg = synth.config("C3", n_prompts=2, L_pad=40, len_lo=10, len_hi=40, chunk_rows=40 * 4)
+    batch = synth.make_batch(cfg, chunk=1)
+    _full_check(batch, sc_params(batch), "C3 reduced chunk 1")
+
+
+@pytest.mark.parametrize("V", [1, 3, 8, 13, 1000, 4097, 33333])
+def test_ragged_vocabulary_sizes(V):
+    K = min(128, V)
+    cfg = synth.config("C1", V=V, K=K, L_pad=5, sigma=2.5)
+    batch = synth.make_batch(cfg)
+    _full_check(batch, sc_params(batch), f"V={V}")
+
+
+@pytest.mark.parametrize("cluster,threads", [(1, 128), (2, 256), (3, 384), (4, 512), (8, 256), (16, 128)])
+def test_explicit_launch_shapes(cluster, threads):
+    cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=16, len_lo=10, len_hi=16, V=30011)
+    batch = synth.make_batch(cfg)
+    _full_check(batch, sc_params(batch, cluster_size=cluster, threads=threads), f"C={cluster} NT={threads}")
+
+
+@pytest.mark.parametrize("mode", [sc.SC_IS_TIS, sc.SC_IS_MIS])
+@pytest.mark.parametrize("centering", [True, False])
+def test_importance_weighting_modes(mode, centering):
+    # a wider sampler mismatch so that weights leave [0.5, 5] and exceed 2
+    cfg = synth.config("C1", sigma_s=1.5, L_pad=16)
+    batch = synth.make_batch(cfg)
+    p = sc_params(batch, is_mode=mode, centering=centering)
+    adv = oracle_adv(batch)
+    g, lp, d, _ = run_gpu(batch, p, adv)
+    bn = host_batch(batch, adv)
+    # rows whose weight sits at a bound within float rounding decide differently: skip them
+    G, LA, OUT, _ = oracle.rows(bn, oracle.make_params(is_mode=mode, centering=centering), np.arange(len(lp)))
+    w = np.exp(LA - bn["rollout_logprob"].astype(np.float64))
+    bounds = [p.tis_max] if mode == sc.SC_IS_TIS else [p.mis_min, p.mis_max]
+    ok = np.all([np.abs(w - b) > 1e-3 * b for b in bounds], axis=0)
+    rows = np.nonzero(ok)[0]
+    assert rows.size >= len(lp) // 2
+    check_rows(bn, p, rows, grad_bits(g, rows), lp.cpu().numpy()[rows], diag_rows(d, rows),
+               what=f"is_mode={mode} centering={centering}")
+    flags = sc.diag_to_numpy(d)["flags"]
+    bit = sc.FLAG_IS_TRUNC if mode == sc.SC_IS_TIS else sc.FLAG_IS_REJECT
+    assert np.any(flags & bit), "the test inputs should exercise the weight bound"
+
+
+def test_temperature_and_grad_scale():
+    cfg = synth.config("C1", temperature=0.7, L_pad=12)
+    batch = synth.make_batch(cfg)
+    _full_check(batch, sc_params(batch, grad_scale=1.0 / 96.0), "T=0.7 scale=1/96")
+
+
+def test_in_place_equals_out_of_place_bitwise():
+    cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=16, len_lo=8, len_hi=16)
+    batch = synth.make_batch(cfg)
+    p = sc_params(batch)
+    adv = oracle_adv(batch)
+    g1, lp1, d1, _ = run_gpu(batch, p, adv)
+    g2, lp2, d2, _ = run_gpu(batch, p, adv, inplace=True)
+    assert torch.equal(g1.view(torch.int16), g2.view(torch.int16))
+    assert torch.equal(lp1, lp2) and torch.equal(d1, d2)
+
+
+def test_deterministic_across_calls():
+    batch = synth.make_batch(synth.config("C1", L_pad=16))
+    p = sc_params(batch)
+    adv = oracle_adv(batch)
+    r1 = run_gpu(batch, p, adv)
+    r2 = run_gpu(batch, p, adv)
+    for a, b in zip(r1[:3], r2[:3]):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+# -------------------------------------------------------------------------
+# Edge cases
+
+
+def _edit(batch, **kw):
+    b = dict(batch)
+    for k, v in kw.items():
+        b[k] = v
+    return b
+
+
+def test_head_hygiene_duplicates_out_of_range_counts():
+    batch = synth.make_batch(synth.config("C1", L_pad=6))
+    T, K = batch["rec_ids"].shape
+    ids = batch["rec_ids"].clone()
+    ids[0, 5] = ids[0, 2]            # a repeat
+    ids[1, 0] = 5000                 # out of range (V = 1024)
+    ids[2, 7] = -1                   # out of range
+    ids[3, 10:20] = ids[3, 0]        # many repeats
+    ids[4, 1] = batch["sampled"][4]  # the sampled token inside the head
+    count = torch.full((T,), K, dtype=torch.int32)
+    count[5] = 0                     # empty head
+    count[6] = 300                   # out of range: clamped to K
+    count[7] = -4                    # out of range: clamped to 0
+    count[8] = 1
+    b = _edit(batch, rec_ids=ids, rec_count=count)
+    _, _, d, st = _full_check(b, sc_params(b), "head hygiene")
+    f = sc.diag_to_numpy(d)["flags"]
+    assert f[0] & sc.FLAG_DUP_ID and f[1] & sc.FLAG_BAD_ID and f[2] & sc.FLAG_BAD_ID
+    assert f[6] & sc.FLAG_BAD_COUNT and f[7] & sc.FLAG_BAD_COUNT
+    assert st & sc.SC_STATUS_DATA
+
+
+def test_bad_rows_and_all_masked():
+    batch = synth.make_batch(synth.config("C1", L_pad=6))
+    resp = batch["row_response"].clone()
+    samp = batch["sampled"].clone()
+    resp[3] = 99                     # response index beyond n_resp
+    samp[4] = 1024                   # sampled id beyond V
+    samp[5] = -2
+    resp[6:9] = -1                   # padding
+    b = _edit(batch, row_response=resp, sampled=samp)
+    g, lp, d, st = _full_check(b, sc_params(b), "bad rows")
+    assert torch.all(g[3:9] == 0)
+    assert st & sc.SC_STATUS_DATA
+    b2 = _edit(batch, row_response=torch.full_like(resp, -1))
+    g2, lp2, d2, st2 = _full_check(b2, sc_params(b2), "all masked")
+    assert torch.all(g2 == 0) and torch.all(lp2 == 0) and st2 == 0
+
+
+def test_empty_batch_and_empty_head_parameter():
+    batch = synth.make_batch(synth.config("C1", L_pad=4))
+    p = sc_params(batch)
+    z = lambda t: t[:0]
+    g, lp, d = sc.sc_center_forward_backward(
+        z(batch["logits"]).cuda(), z(batch["rec_ids"]).cuda(), z(batch["rec_logprobs"]).cuda(), None,
+        z(batch["sampled"]).cuda(), None, z(batch["row_response"]).cuda(),
+        torch.zeros(8, device="cuda"), p)
+    assert g.shape == (0, 1024)
+    # K_max = 0: no recorded head at all -> plain policy gradient
+    b = _edit(batch, rec_ids=batch["rec_ids"][:, :0].contiguous(), rec_logprobs=batch["rec_logprobs"][:, :0].contiguous())
+    _full_check(b, sc_params(b, K_max=0), "K_max=0")
+
+
+def test_row_stride_larger_than_vocab():
+    batch = synth.make_batch(synth.config("C1", V=1000, L_pad=8))
+    T = batch["logits"].shape[0]
+    wide = torch.zeros((T, 1024), dtype=torch.bfloat16)
+    wide[:, :1000] = batch["logits"]
+    wide = wide.cuda()
+    adv = oracle_adv(batch)
+    p = sc_params(batch)
+    out = torch.full((T, 1016), 7.0, dtype=torch.bfloat16, device="cuda")
+    b = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in batch.items()}
+    sc.sc_center_forward_backward(wide, b["rec_ids"], b["rec_logprobs"], None, b["sampled"],
+                                  b["rollout_logprob"], b["row_response"], torch.as_tensor(adv).cuda(), p,
+                                  V=1000, grad_out=out)
+    ref = run_gpu(batch, p, adv)[0]
+    assert torch.equal(out[:, :1000].view(torch.int16), ref.view(torch.int16))
+    assert torch.all(out[:, 1000:] == 7.0)
+
+
+# -------------------------------------------------------------------------
+# Full-size configurations
+
+
+@pytest.mark.slow
+def test_c2_full_size_every_row():
+    batch = synth.make_batch("C2", device="cuda")
+    _full_check(batch, sc_params(batch), "C2 full")
+
+
+def _invariants(batch, g, d, p):
+    """Properties that hold at any size, checked on every row on the device."""
+    diag = sc.diag_to_numpy(d)
+    valid = batch["row_response"].cpu().numpy() >= 0
+    assert np.all(diag["flags"][~valid] == sc.FLAG_MASKED)
+    A = np.abs(diag["adv"] * diag["is_weight"]) * p.inv_temperature * abs(p.grad_scale) * np.maximum(1, diag["rho"])
+    assert np.all(np.abs(diag["row_sum"]) <= 1e-3 * A + 1e-7), "FP32 row sums"
+    # bf16 output row sums, with half an ulp per element of rounding allowance
+    gs = g.double().sum(dim=1).cpu().numpy()
+    gabs = g.float().abs()
+    e = torch.floor(torch.log2(gabs.clamp_min(2.0**-126)))
+    half_ulp = (0.5 * torch.exp2(e - 7) * (gabs > 0)).double().sum(dim=1).cpu().numpy()
+    assert np.all(np.abs(gs) <= 1e-3 * A + half_ulp + 1e-7), "bf16 row sums"
+    assert np.all(np.isfinite(diag["loss"])) and np.all(diag["P_H"][valid] <= 1.0 + 1e-6)
+    assert np.all(np.abs(diag["P_H"] + diag["tail_pi"] - valid) <= 1e-5)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,chunk", [("C4", 0), ("C5", 0), ("C3", 0), ("C3", 17)])
+def test_full_size_sampled_rows_and_invariants(name, chunk):
+    cfg = synth.config(name)
+    batch = synth.make_batch(cfg, chunk=chunk, device="cuda")
+    T = batch["logits"].shape[0]
+    p = sc_params(batch)
+    adv = oracle_adv(batch)
+    g, lp, d, status = run_gpu(batch, p, adv)
+    assert int(status.item()) & 0x6 == 0
+    rng = np.random.default_rng(zlib.crc32(f"{name}/{chunk}".encode()))
+    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 192, replace=False)]))
+    bn = {k: v for k, v in batch.items()}
+    # only the sampled rows travel to the host for the oracle
+    sub = {k: (v[torch.as_tensor(rows, device=v.device)] if isinstance(v, torch.Tensor) and v.dim() >= 1
+               and v.shape[0] == T else v) for k, v in bn.items()}
+    bh = host_batch(sub, adv)
+    check_rows(bh, p, np.arange(rows.size), grad_bits(g, rows), lp.cpu().numpy()[rows], diag_rows(d, rows),
+               what=f"{name} chunk {chunk} sampled")
+    _invariants(batch, g, d, p)
