@@ -253,6 +253,7 @@ def main():
         return run_reference(args)
 
     import precision_off_policy_gb300 as sc
+    from precision_off_policy_gb300 import dp
 
     world, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -266,10 +267,8 @@ def main():
     batch = synth.make_batch(cfg, device=dev)
     T, V, K = batch["logits"].shape[0], batch["V"], batch["K"]
     n_valid = batch["n_valid"]
-    total_valid = torch.tensor([n_valid], dtype=torch.int64, device=dev)
-    if world > 1:
-        dist.all_reduce(total_valid)  # global generated-token count for the token-mean loss
-    grad_scale = float(np.float32(1.0 / float(total_valid.item())))  # int64 -> double -> float
+    # global generated-token count for the token-mean loss (int64 all-reduce)
+    grad_scale = dp.token_mean_scale(dp.global_valid_tokens(n_valid, device=dev))
     p = sc.params(K_max=K, inv_temperature=batch["inv_temperature"], grad_scale=grad_scale)
     plan = sc.sc_plan_query(V, p)
 

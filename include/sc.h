@@ -95,8 +95,9 @@ typedef struct sc_params {
     float inv_temperature; /* 1 / rollout temperature, finite, > 0               */
     float grad_scale;      /* multiplies every gradient element, e.g. 1 / N_tok */
     int cluster_size;      /* CTAs sharing one row: 0 = automatic, else 1..16   */
-    int threads;           /* threads per CTA: 0 = automatic, else 128, 256,
-                              384 or 512                                        */
+    int threads;           /* compute threads per CTA (one more warp fetches):
+                              0 = automatic, else 128, 256, 384 or 512          */
+    int stages;            /* rows in flight per CTA: 0 = automatic, else 1..4   */
 } sc_params;
 
 /* Per-row diagnostics, 64 bytes.  Masked and error rows hold zeros and their

@@ -68,6 +68,7 @@ class Params(ctypes.Structure):
         ("grad_scale", ctypes.c_float),
         ("cluster_size", ctypes.c_int),
         ("threads", ctypes.c_int),
+        ("stages", ctypes.c_int),
     ]
 
 
@@ -123,11 +124,11 @@ def _check(status: int):
 
 
 def params(K_max=128, is_mode=SC_IS_NONE, tis_max=2.0, mis_min=0.5, mis_max=5.0, centering=True,
-           inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0) -> Params:
+           inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0, stages=0) -> Params:
     """Defaults are the settings table of the docs' "Score Centering" section."""
     return Params(int(K_max), int(is_mode), float(tis_max), float(mis_min), float(mis_max),
                   int(bool(centering)), float(inv_temperature), float(grad_scale), int(cluster_size),
-                  int(threads))
+                  int(threads), int(stages))
 
 
 def _ptr(t):

@@ -10,26 +10,36 @@
 // plus log p_a and per-row diagnostics (the section's K3, entropy, masses).
 //
 // GB300 design.  One row is shared by a cluster of C CTAs; CTA r owns the
-// vocabulary slice [r*S, min((r+1)*S, V)).  Per row and CTA:
-//   1. the slice is copied HBM -> shared memory by the TMA engine (1-D bulk
-//      copies in chunks, each completing on its own mbarrier);
-//   2. max pass on packed bf16 pairs as chunks land;
-//   3. warp 0 gathers the recorded ids that fall in the slice, drops repeats,
-//      pushes their logits to every CTA of the cluster (DSMEM) and overwrites
-//      them in shared memory with -2^100, so that
-//   4. the exp pass over the slice accumulates the unrecorded mass
-//      sum_{v not in H} e^{x_v - m} directly (no 1 - P_H cancellation) and
-//      the entropy term;
-//   5. partials travel to every CTA over DSMEM and an mbarrier with
-//      cluster-scope release/acquire; warp 0 of each CTA then computes the
-//      row scalars (LSE, P_H, Q_H, rho, s, loss, k3, IS weight) redundantly;
-//   6. the write pass recomputes p_v from shared memory and streams
-//      g_v = beta p_v straight to global memory with 16-byte stores and an
-//      evict-first L2 hint; the <= K+1 special entries (recorded ids and the
-//      sampled token) are patched in registers via a per-vector bitmap.
+// vocabulary slice [r*S, min((r+1)*S, V)).  Each CTA is warp-specialised:
+//
+// * a producer warp walks the cluster's rows, writes padding and error rows
+//   (zero gradient) itself, and for every valid row claims a pipeline stage,
+//   fetches the row's metadata (recorded ids and log-probabilities, count,
+//   rollout log-probability, advantage) and starts 1-D bulk copies (TMA
+//   engine) of the CTA's logit slice into that stage's shared memory, in
+//   chunks that each complete on their own mbarrier.  With two or more
+//   stages the next row streams in while the current one is computed.
+// * consumer warps, per valid row:
+//   1. max pass on packed bf16 pairs as chunks land, while consumer warp 0
+//      gathers the recorded ids that fall in the slice, drops repeats,
+//      pushes their logits to every CTA of the cluster and overwrites them in
+//      shared memory with -2^100 (the max is exact either way, because warp 0
+//      contributes the values it overwrites);
+//   2. exp pass over the slice: the unrecorded mass sum_{v not in H}
+//      e^{x_v - m} accumulates directly (no 1 - P_H cancellation), with the
+//      entropy term;
+//   3. exchange: partials go to every CTA of the cluster with st.async
+//      stores that complete as transaction bytes on the receiver's mbarrier
+//      (one expect_tx per CTA and row); warp 0 then computes the row scalars
+//      (LSE, P_H, Q_H, rho, s, loss, k3, importance weight) redundantly in
+//      every CTA;
+//   4. write pass: p_v is recomputed from shared memory and g_v = beta p_v
+//      streams to global memory with 16-byte stores and an evict-first L2
+//      hint; the <= K+1 special entries (recorded ids and the sampled token)
+//      are patched in registers via a per-vector bitmap.
 // Every logit is read from HBM once and every gradient written once.  The
-// grid is persistent: as many clusters as fit, looping over rows.  Every
-// wait is bounded (about 1 s) and reports through the status word.
+// grid is persistent (as many clusters as fit).  Every wait is bounded
+// (about 1 s) and reports through the status word.
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -44,20 +54,30 @@ namespace {
 
 constexpr int kMaxCluster = 16;
 constexpr int kMaxChunks = 16;
+constexpr int kMaxStages = 4;
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;          // 227 KiB of dynamic shared memory per CTA
-constexpr int kTargetSliceBytes = 40960;  // automatic plan: ~40 KiB of logits per CTA
 constexpr int kChunkVecTarget = 256;      // 16-byte vectors per bulk copy (4 KiB)
 constexpr uint16_t kSentinel = 0xF180u;   // bf16 -2^100: marks recorded ids in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+// Per-stage row description written by the producer warp.
+struct RowMeta {
+    long long t;  // row index; -1 ends the consumers' loop
+    int resp, sa, cnt;
+    uint32_t rflags;
+    float A, rl;
+};
 
 struct Layout {
-    int off_bars, off_part, off_frs, off_za, off_xh, off_ids, off_lps, off_fixi, off_fixk, off_fixv,
-        off_bmp, off_red, off_scal, total;
+    int stage_bytes;  // bytes of one stage's logit slice (128-aligned)
+    int off_ids, off_lps, off_meta, off_bars, off_part, off_frs, off_za, off_xh, off_fixi, off_fixk,
+        off_fixv, off_bmp, off_red, off_scal, total;
 };
 
 struct KArgs {
@@ -77,66 +97,58 @@ struct KArgs {
     int V, K_max, n_resp;
     int is_mode, centering;
     float tis_max, mis_min, mis_max, inv_t, grad_scale;
-    int C, S, ncv;
+    int C, S, ncv, NB;
     Layout L;
 };
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    return v;
-}
-__device__ __forceinline__ int warp_sum_i(int v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    return v;
-}
-__device__ __forceinline__ uint32_t warp_or(uint32_t v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
     return v;
 }
 __device__ __forceinline__ uint16_t f_to_bf_bits(float x) {
     return static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu);
 }
+__device__ __forceinline__ void status_or(uint32_t* st, uint32_t bits) {
+    if (st) atomicOr(st, bits);
+}
 
-template <int NT>
-__global__ void __launch_bounds__(NT) center_kernel(const __grid_constant__ KArgs a) {
+// Bars of one stage: [0, kMaxChunks) chunk copies, kMaxChunks full, kMaxChunks+1 empty.
+constexpr int kBarsPerStage = kMaxChunks + 2;
+
+template <int NC>
+__global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int NW = NT / 32;
+    constexpr int NCW = NC / 32;  // consumer warps; warp NCW is the producer
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t crank = cluster_ctarank();
     const uint32_t cid = cluster_id_x();
     const uint32_t ncl = num_clusters_x();
-    const int C = a.C;
-    const int K_max = a.K_max;
+    const int C = a.C, K_max = a.K_max, NB = a.NB;
+    const Layout& L = a.L;
 
-    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);
-    const uint32_t buf_s = smem_addr(smem);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + a.L.off_bars);  // [kMaxChunks + 2]
-    float4* part = reinterpret_cast<float4*>(smem + a.L.off_part);      // [2][kMaxCluster]
-    float2* frs = reinterpret_cast<float2*>(smem + a.L.off_frs);        // [kMaxCluster]
-    float2* za = reinterpret_cast<float2*>(smem + a.L.off_za);          // [2]
-    float2* xh = reinterpret_cast<float2*>(smem + a.L.off_xh);          // [2][K_max]
-    int* ids_s = reinterpret_cast<int*>(smem + a.L.off_ids);            // [K_max]
-    float* lps_s = reinterpret_cast<float*>(smem + a.L.off_lps);        // [K_max]
-    int* fix_i = reinterpret_cast<int*>(smem + a.L.off_fixi);           // [K_max + 1]
-    int* fix_k = reinterpret_cast<int*>(smem + a.L.off_fixk);           // [K_max + 1]
-    float* fix_v = reinterpret_cast<float*>(smem + a.L.off_fixv);       // [K_max + 1]
-    uint32_t* bmp = reinterpret_cast<uint32_t*>(smem + a.L.off_bmp);    // one bit per 8 entries
-    float* red = reinterpret_cast<float*>(smem + a.L.off_red);          // [4][NW]
-    float* scal = reinterpret_cast<float*>(smem + a.L.off_scal);        // [8]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
+    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);      // [NB]
+    int* ids_all = reinterpret_cast<int*>(smem + L.off_ids);            // [NB][K_max]
+    float* lps_all = reinterpret_cast<float*>(smem + L.off_lps);        // [NB][K_max]
+    float4* part = reinterpret_cast<float4*>(smem + L.off_part);        // [2][kMaxCluster]
+    float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);          // [kMaxCluster]
+    float2* za = reinterpret_cast<float2*>(smem + L.off_za);            // [2]
+    float2* xh = reinterpret_cast<float2*>(smem + L.off_xh);            // [2][K_max]
+    int* fix_i = reinterpret_cast<int*>(smem + L.off_fixi);             // [K_max + 1]
+    int* fix_k = reinterpret_cast<int*>(smem + L.off_fixk);             // [K_max + 1]
+    float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);         // [K_max + 1]
+    uint32_t* bmp = reinterpret_cast<uint32_t*>(smem + L.off_bmp);      // one bit per 8 entries
+    float* red = reinterpret_cast<float*>(smem + L.off_red);            // [4][NCW]
+    float* scal = reinterpret_cast<float*>(smem + L.off_scal);          // [8]
     int* scal_i = reinterpret_cast<int*>(scal);
+    auto bar_addr = [&](int stage, int i) { return smem_addr(&bars[stage * kBarsPerStage + i]); };
+    const uint32_t xbar0 = smem_addr(&bars[kMaxStages * kBarsPerStage]);
 
     const int lo = static_cast<int>(crank) * a.S;
     const int hi = min(lo + a.S, a.V);
@@ -144,464 +156,562 @@ __global__ void __launch_bounds__(NT) center_kernel(const __grid_constant__ KArg
     const int n8 = n & ~7, nvb = n8 >> 3, tail = n - n8, nv = nvb + (tail ? 1 : 0);
     const int nchunks = (nvb + a.ncv - 1) / a.ncv;
     const int nwords = (a.S / 8 + 31) / 32;
-    const uint32_t xbar0 = smem_addr(&bars[kMaxChunks]);
+    const float kscale = a.inv_t * kLog2e;
+    const uint64_t pol = l2_policy_evict_first();
 
     if (tid == 0) {
-        for (int i = 0; i < kMaxChunks; ++i) mbar_init(smem_addr(&bars[i]), 1u);
-        // exchange barriers: every lane of warp 0 of every CTA arrives once per row
-        mbar_init(xbar0, 32u * static_cast<uint32_t>(C));
-        mbar_init(xbar0 + 8, 32u * static_cast<uint32_t>(C));
+        for (int st = 0; st < NB; ++st) {
+            for (int i = 0; i < kMaxChunks; ++i) mbar_init(bar_addr(st, i), 1u);
+            mbar_init(bar_addr(st, kMaxChunks), 1u);      // full: producer's arrive
+            mbar_init(bar_addr(st, kMaxChunks + 1), 1u);  // empty: consumers' arrive
+        }
+        mbar_init(xbar0, 1u);  // exchange: own expect_tx arrive + peers' st.async bytes
+        mbar_init(xbar0 + 8, 1u);
         fence_mbar_init_cluster();
     }
-    for (int i = tid; i < nwords; i += NT) bmp[i] = 0u;
-    cluster_sync_all();  // peers' barriers exist before anyone arrives on them
+    for (int i = tid; i < nwords; i += NC + 32) bmp[i] = 0u;
+    cluster_sync_all();  // every CTA's barriers exist before peers signal them
 
-    const uint64_t pol = l2_policy_evict_first();
-    const float kscale = a.inv_t * kLog2e;
-    uint32_t nvalid = 0;
-    float rs_prev = 0.0f;  // thread 0: this CTA's share of the previous valid row's sum
-    long long t_prev = -1;
-    bool abort = false;
+    long long t_last = -1;  // consumers: last valid row (for the final row sum)
+    float rs_last = 0.0f;   // consumer thread 0: this CTA's share of its sum
+    bool aborted = false;
 
-    for (long long t = cid; t < a.T; t += ncl) {
-        const int resp = __ldg(a.resp + t);
-        const int sa = __ldg(a.sampled + t);
-        uint32_t zflags = 0;
-        if (resp < 0)
-            zflags = SC_FLAG_MASKED;
-        else if (resp >= a.n_resp)
-            zflags = SC_FLAG_BAD_RESPONSE;
-        else if (sa < 0 || sa >= a.V)
-            zflags = SC_FLAG_BAD_SAMPLED;
-        uint16_t* grow = a.grad + t * a.gstride + lo;
-        if (zflags) {
-            for (int j = tid; j < nvb; j += NT) st_global_v4_hint(grow + 8 * j, 0u, 0u, 0u, 0u, pol);
-            if (tid < tail) grow[n8 + tid] = 0;
-            if (crank == 0 && tid == 0) {
-                a.logp[t] = 0.0f;
-                if (a.diag) {
-                    sc_row_diag d;
-                    memset(&d, 0, sizeof d);
-                    d.flags = zflags;
-                    a.diag[t] = d;
-                }
-                if ((zflags & SC_FLAG_DATA_ERRORS) && a.status) atomicOr(a.status, SC_STATUS_DATA);
+    if (warp == NCW) {
+        // ================= producer warp =================
+        uint32_t nfill = 0;
+        bool stop = false;
+        for (long long base = cid; base < a.T && !stop; base += 32LL * ncl) {
+            const long long tl = base + static_cast<long long>(lane) * ncl;
+            const bool in = tl < a.T;
+            int resp_l = -1, sa_l = 0;
+            if (in) {
+                resp_l = __ldg(a.resp + tl);
+                sa_l = __ldg(a.sampled + tl);
             }
-            continue;
-        }
-
-        const uint32_t par = nvalid & 1u;
-        const uint32_t lph = nvalid & 1u;
-        const uint32_t xph = (nvalid >> 1) & 1u;
-        const uint16_t* lrow = a.logits + t * a.lstride + lo;
-
-        // ---- 1. bulk copies of the slice, tail by plain loads ----------------
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            for (int i = 0; i < nchunks; ++i) {
-                const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                const uint32_t bar = smem_addr(&bars[i]);
-                mbar_expect_tx(bar, bytes);
-                bulk_load(buf_s + 16u * v0, lrow + 8 * v0, bytes, bar, pol);
+            uint32_t zf = 0;
+            if (in) {
+                if (resp_l < 0)
+                    zf = SC_FLAG_MASKED;
+                else if (resp_l >= a.n_resp)
+                    zf = SC_FLAG_BAD_RESPONSE;
+                else if (sa_l < 0 || sa_l >= a.V)
+                    zf = SC_FLAG_BAD_SAMPLED;
             }
-        }
-        float tmax = -INFINITY;
-        if (tail && tid < 8) {
-            uint16_t h = kSentinel;
-            if (tid < tail) {
-                h = lrow[n8 + tid];
-                tmax = bf_to_f(h);
-            }
-            buf[n8 + tid] = h;
-        }
-        int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
-        uint32_t rflags = 0;
-        if (cnt < 0 || cnt > K_max) {
-            rflags |= SC_FLAG_BAD_COUNT;
-            cnt = cnt < 0 ? 0 : K_max;
-        }
-        const long long kbase = t * static_cast<long long>(K_max);
-        for (int k = tid; k < cnt; k += NT) {
-            ids_s[k] = __ldg(a.ids + kbase + k);
-            lps_s[k] = __ldg(a.lps + kbase + k);
-        }
-
-        // ---- 2. max pass, chunk by chunk as the copies land -------------------
-        uint32_t mx2 = 0xFF80FF80u;  // (-inf, -inf)
-        bool timed_out = false;
-        for (int i = 0; i < nchunks; ++i) {
-            const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-            if (!mbar_wait_bounded(smem_addr(&bars[i]), lph, kWaitLimitNs)) {
-                timed_out = true;
-                break;
-            }
-            for (int j = v0 + tid; j < v1; j += NT) {
-                const uint4 w = lds128(buf_s + 16u * j);
-                mx2 = bmax2(mx2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
-            }
-        }
-        float m_loc = fmaxf(fmaxf(bf_lo(mx2), bf_hi(mx2)), tmax);
-        m_loc = warp_max(m_loc);
-        if (lane == 0) red[warp] = m_loc;
-        if (__syncthreads_or(timed_out)) {
-            if (tid == 0) {
-                if (a.status) atomicOr(a.status, SC_STATUS_TIMEOUT_LOAD);
-                // let copies still in flight land before the CTA stops (bounded again)
-                for (int i = 0; i < nchunks; ++i)
-                    (void)mbar_wait_bounded(smem_addr(&bars[i]), lph, kWaitLimitNs);
-            }
-            abort = true;
-            break;
-        }
-        m_loc = red[0];
-#pragma unroll
-        for (int w = 1; w < NW; ++w) m_loc = fmaxf(m_loc, red[w]);
-
-        // ---- 3. gather the recorded ids of this slice (warp 0) ----------------
-        if (warp == 0) {
-            const bool a_own = sa >= lo && sa < hi;
-            if (a_own && lane == 0) {
-                const float zav = bf_to_f(buf[sa - lo]);
-                const uint32_t za_s = smem_addr(&za[par]);
-                for (int r = 0; r < C; ++r)
-                    st_cluster_v2(map_to_rank(za_s, r), __float_as_uint(zav), 1u);
-            }
-            __syncwarp();
-            int nfix = 0;
-            bool a_in_h = false;
-            const uint32_t xh_s = smem_addr(xh + static_cast<int>(par) * K_max);
-            for (int base = 0; base < cnt; base += 32) {
-                const int k = base + lane;
-                const bool in = k < cnt;
-                const int id = in ? ids_s[k] : -1;
-                const bool owned = in && id >= lo && id < hi;
-                const unsigned same = __match_any_sync(0xFFFFFFFFu, owned ? id : -1 - lane);
-                const bool first = owned && (same & lanemask_lt()) == 0u;
-                const uint16_t h = owned ? buf[id - lo] : static_cast<uint16_t>(0);
-                const bool valid = first && h != kSentinel;
-                __syncwarp();
-                if (valid) buf[id - lo] = kSentinel;
-                if (owned) {
-                    const uint32_t fz = __float_as_uint(bf_to_f(h));
-                    const uint32_t fl = valid ? 1u : 2u;
-                    for (int r = 0; r < C; ++r) st_cluster_v2(map_to_rank(xh_s + 8u * k, r), fz, fl);
-                }
-                const unsigned vm = __ballot_sync(0xFFFFFFFFu, valid);
-                if (valid) {
-                    const int pos = nfix + __popc(vm & lanemask_lt());
-                    fix_i[pos] = id - lo;
-                    fix_k[pos] = k;
-                }
-                nfix += __popc(vm);
-                a_in_h = a_in_h || __any_sync(0xFFFFFFFFu, valid && id == sa);
-                __syncwarp();
-            }
-            if (a_own && !a_in_h) {
-                if (lane == 0) {
-                    fix_i[nfix] = sa - lo;
-                    fix_k[nfix] = -1;
-                }
-                nfix += 1;
-            }
-            __syncwarp();
-            for (int e = lane; e < nfix; e += 32) {
-                const int li = fix_i[e];
-                atomicOr(&bmp[li >> 8], 1u << ((li >> 3) & 31));
-            }
-            if (lane == 0) scal_i[3] = nfix;
-        }
-        __syncthreads();
-
-        // ---- 4. exp pass over the unrecorded entries --------------------------
-        const float o_c = m_loc * kscale;
-        float s1 = 0.0f, s2 = 0.0f;
-        for (int j = tid; j < nv; j += NT) {
-            const uint4 w = lds128(buf_s + 16u * j);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float y0 = fmaf(bf_lo(ww[q]), kscale, -o_c);
-                const float y1 = fmaf(bf_hi(ww[q]), kscale, -o_c);
-                const float e0 = ex2(y0), e1 = ex2(y1);
-                s1 += e0;
-                s1 += e1;
-                s2 = fmaf(e0, y0, s2);
-                s2 = fmaf(e1, y1, s2);
-            }
-        }
-        s1 = warp_sum(s1);
-        s2 = warp_sum(s2);
-        if (lane == 0) {
-            red[NW + warp] = s1;
-            red[2 * NW + warp] = s2;
-        }
-        __syncthreads();
-
-        // ---- 5. cluster exchange and row scalars (warp 0) ----------------------
-        if (warp == 0) {
-            if (lane == 0) {
-                float S1 = 0.0f, S2 = 0.0f;
-                for (int w = 0; w < NW; ++w) {
-                    S1 += red[NW + w];
-                    S2 += red[2 * NW + w];
-                }
-                const uint32_t ps = smem_addr(part + static_cast<int>(par) * kMaxCluster + crank);
-                for (int r = 0; r < C; ++r)
-                    st_cluster_v4(map_to_rank(ps, r), __float_as_uint(m_loc), __float_as_uint(S1),
-                                  __float_as_uint(S2), __float_as_uint(rs_prev));
-            }
-            // each lane's release covers its own pushes to the peers
-            const uint32_t xb = xbar0 + 8u * par;
-            for (int r = 0; r < C; ++r) mbar_arrive_cluster(map_to_rank(xb, r));
-            const bool got = mbar_wait_cluster_bounded(xb, xph, kWaitLimitNs);
-            if (!__all_sync(0xFFFFFFFFu, got)) {
-                if (lane == 0) {
-                    if (a.status) atomicOr(a.status, SC_STATUS_TIMEOUT_EXCHANGE);
-                    scal_i[4] = 1;
-                }
-            } else {
-                const float4* pp = part + static_cast<int>(par) * kMaxCluster;
-                float m = -INFINITY;
-                for (int r = 0; r < C; ++r) m = fmaxf(m, pp[r].x);
-                const float o = m * kscale;
-                float lT = 0.0f, ET = 0.0f;
-                for (int r = 0; r < C; ++r) {
-                    const float4 pr = pp[r];
-                    if (pr.y > 0.0f) {
-                        const float d = pr.x * kscale - o;
-                        const float f = ex2(d);
-                        lT += pr.y * f;
-                        ET += f * (pr.z + d * pr.y);
-                    }
-                }
-                const float2* xr = xh + static_cast<int>(par) * K_max;
-                float lH = 0.0f, EH = 0.0f, lp_best = -INFINITY;
-                int nval = 0, k_best = 0x7FFFFFFF;
-                uint32_t kfl = 0;
-                for (int k = lane; k < cnt; k += 32) {
-                    const int id = ids_s[k];
-                    if (id < 0 || id >= a.V) {
-                        kfl |= SC_FLAG_BAD_ID;
-                        continue;
-                    }
-                    const float2 x = xr[k];
-                    if (__float_as_uint(x.y) != 1u) {
-                        kfl |= SC_FLAG_DUP_ID;
-                        continue;
-                    }
-                    const float y = fmaf(x.x, kscale, -o);
-                    const float e = ex2(y);
-                    lH += e;
-                    EH = fmaf(e, y, EH);
-                    ++nval;
-                    const float lp = lps_s[k];
-                    if (lp > lp_best) {
-                        lp_best = lp;
-                        k_best = k;
-                    }
-                }
-                lH = warp_sum(lH);
-                EH = warp_sum(EH);
-                nval = warp_sum_i(nval);
-                kfl = warp_or(kfl);
-                // arg-max of the recorded logprobs (lowest k on ties)
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ol = __shfl_xor_sync(0xFFFFFFFFu, lp_best, off);
-                    const int ok = __shfl_xor_sync(0xFFFFFFFFu, k_best, off);
-                    if (ol > lp_best || (ol == lp_best && ok < k_best)) {
-                        lp_best = ol;
-                        k_best = ok;
-                    }
-                }
-                // 1 - Q_H without cancellation: -expm1(l_max) minus the other q's in FP64
-                double qrest = 0.0;
-                for (int k = lane; k < cnt; k += 32) {
-                    const int id = ids_s[k];
-                    if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u || k == k_best) continue;
-                    qrest += static_cast<double>(expf(lps_s[k]));
-                }
-                qrest = warp_sum_d(qrest);
-                double tail_mu_d = 1.0, Q_H_d = 0.0;
-                if (nval > 0) {
-                    tail_mu_d = static_cast<double>(-expm1f(lp_best)) - qrest;
-                    Q_H_d = static_cast<double>(expf(lp_best)) + qrest;
-                }
-                const float tail_mu = static_cast<float>(tail_mu_d);
-                const float l = lT + lH;
-                const float log2l = log2f(l);
-                const float P_H = lH / l;
-                const float tail_pi = lT / l;
-                const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
-                uint32_t flags = rflags | kfl;
-                if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
-                if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
-                const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
-                const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
-                const float ya = fmaf(za[par].x, kscale, -o);
-                const float logp_a = (ya - log2l) * kLn2;
-                float wt = 1.0f, k3 = 0.0f;
-                if (a.rollout) {
-                    const float d = logp_a - __ldg(a.rollout + t);
-                    k3 = expm1f(d) - d;
-                    const float w = expf(d);
-                    if (a.is_mode == SC_IS_TIS) {
-                        if (w > a.tis_max) {
-                            wt = a.tis_max;
-                            flags |= SC_FLAG_IS_TRUNC;
-                        } else {
-                            wt = w;
-                        }
-                    } else if (a.is_mode == SC_IS_MIS) {
-                        if (w >= a.mis_min && w <= a.mis_max) {
-                            wt = w;
-                        } else {
-                            wt = 0.0f;
-                            flags |= SC_FLAG_IS_REJECT;
-                        }
-                    }
-                }
-                const float A = __ldg(a.adv + resp);
-                const float Aw = A * wt;
-                float csum = 0.0f;
-                if (a.centering) {
-                    for (int k = lane; k < cnt; k += 32) {
-                        const int id = ids_s[k];
-                        if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u) continue;
-                        const float lk = fmaf(xr[k].x, kscale, -o) - log2l;  // log2 p_k
-                        const float c = expf(lps_s[k]) - rho * ex2(lk);
-                        csum = fmaf(c, lk * kLn2, csum);
-                    }
-                    csum = warp_sum(csum);
-                }
-                const float loss = -Aw * (logp_a - csum);
-                const float entropy = kLn2 * (log2l - (ET + EH) / l);
-                const float alpha = -a.grad_scale * a.inv_t * Aw;
-                const float beta = -alpha * s;
-                const int nfix = scal_i[3];
-                for (int e = lane; e < nfix; e += 32) {
-                    const int k = fix_k[e];
-                    float g;
-                    if (k >= 0) {
-                        const float p = ex2(fmaf(xr[k].x, kscale, -o) - log2l);
-                        const float mu = a.centering ? fmaf(dsr, p, expf(lps_s[k])) : p;
-                        g = alpha * ((ids_s[k] == sa ? 1.0f : 0.0f) - mu);
-                    } else {
-                        g = alpha * (1.0f - s * ex2(ya - log2l));
-                    }
-                    fix_v[e] = g;
-                }
-                if (lane == 0) {
-                    scal[0] = o + log2l;
-                    scal[1] = beta;
-                    scal_i[4] = 0;
-                    if (crank == 0) {
-                        a.logp[t] = logp_a;
+            const unsigned inmask = __ballot_sync(kFull, in);
+            for (int j = 0; j < 32 && ((inmask >> j) & 1u); ++j) {
+                const long long t = base + static_cast<long long>(j) * ncl;
+                const uint32_t zfj = __shfl_sync(kFull, zf, j);
+                const int rj = __shfl_sync(kFull, resp_l, j);
+                const int sj = __shfl_sync(kFull, sa_l, j);
+                if (zfj) {  // padding or error row: zero gradient, no compute
+                    uint16_t* grow = a.grad + t * a.gstride + lo;
+                    for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
+                    if (lane < tail) grow[n8 + lane] = 0;
+                    if (crank == 0 && lane == 0) {
+                        a.logp[t] = 0.0f;
                         if (a.diag) {
                             sc_row_diag d;
-                            d.loss = loss;
-                            d.logp_a = logp_a;
-                            d.P_H = P_H;
-                            d.tail_pi = tail_pi;
-                            d.Q_H = static_cast<float>(Q_H_d);
-                            d.tail_mu = tail_mu;
-                            d.rho = rho;
-                            d.s = s;
-                            d.entropy = entropy;
-                            d.k3 = k3;
-                            d.is_weight = wt;
-                            d.row_sum = 0.0f;
-                            d.adv = A;
-                            d.n_valid_k = nval;
-                            d.flags = flags;
-                            d.reserved = 0;
+                            memset(&d, 0, sizeof d);
+                            d.flags = zfj;
                             a.diag[t] = d;
-                            if (t_prev >= 0) {
-                                float rsum = 0.0f;
-                                for (int r = 0; r < C; ++r) rsum += pp[r].w;
-                                a.diag[t_prev].row_sum = rsum;
+                        }
+                        if (zfj & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+                    }
+                    continue;
+                }
+                const int st = static_cast<int>(nfill % NB);
+                if (nfill >= static_cast<uint32_t>(NB)) {
+                    const uint32_t epar = ((nfill / NB) - 1u) & 1u;
+                    if (!mbar_wait_bounded(bar_addr(st, kMaxChunks + 1), epar, kWaitLimitNs)) {
+                        if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                        stop = true;
+                        break;
+                    }
+                }
+                int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
+                uint32_t rflags = 0;
+                if (cnt < 0 || cnt > K_max) {
+                    rflags = SC_FLAG_BAD_COUNT;
+                    cnt = cnt < 0 ? 0 : K_max;
+                }
+                const long long kb = t * static_cast<long long>(K_max);
+                int* ids_s = ids_all + st * K_max;
+                float* lps_s = lps_all + st * K_max;
+                for (int k = lane; k < cnt; k += 32) {
+                    ids_s[k] = __ldg(a.ids + kb + k);
+                    lps_s[k] = __ldg(a.lps + kb + k);
+                }
+                uint16_t* bufst = reinterpret_cast<uint16_t*>(smem + st * L.stage_bytes);
+                const uint16_t* lrow = a.logits + t * a.lstride + lo;
+                if (tail && lane < 8) bufst[n8 + lane] = lane < tail ? lrow[n8 + lane] : kSentinel;
+                if (lane == 0) {
+                    RowMeta m;
+                    m.t = t;
+                    m.resp = rj;
+                    m.sa = sj;
+                    m.cnt = cnt;
+                    m.rflags = rflags;
+                    m.A = __ldg(a.adv + rj);
+                    m.rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
+                    meta[st] = m;
+                    fence_proxy_async_smem();
+                    const uint32_t bs = smem_addr(bufst);
+                    for (int i = 0; i < nchunks; ++i) {
+                        const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                        const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+                        mbar_expect_tx(bar_addr(st, i), bytes);
+                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, bar_addr(st, i), pol);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(st, kMaxChunks));  // release: meta, ids, tail
+                ++nfill;
+            }
+        }
+        if (!stop) {  // end marker for the consumers
+            const int st = static_cast<int>(nfill % NB);
+            bool ok = true;
+            if (nfill >= static_cast<uint32_t>(NB))
+                ok = mbar_wait_bounded(bar_addr(st, kMaxChunks + 1), ((nfill / NB) - 1u) & 1u, kWaitLimitNs);
+            if (ok) {
+                if (lane == 0) {
+                    meta[st].t = -1;
+                    mbar_arrive(bar_addr(st, kMaxChunks));
+                }
+            } else if (lane == 0) {
+                status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+            }
+        }
+        // copies still in flight land before the CTA can exit (bounded again)
+        if (lane == 0) {
+            const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
+            for (uint32_t f = f0; f < nfill; ++f)
+                for (int i = 0; i < nchunks; ++i)
+                    (void)mbar_wait_bounded(bar_addr(f % NB, i), (f / NB) & 1u, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ================= consumer warps =================
+        uint32_t nproc = 0;
+        float rs_prev = 0.0f;
+        long long t_prev = -1;
+        for (;;) {
+            const int st = static_cast<int>(nproc % NB);
+            const uint32_t fpar = (nproc / NB) & 1u;
+            const bool got = mbar_wait_bounded(bar_addr(st, kMaxChunks), fpar, kWaitLimitNs);
+            if (named_bar_or(NC, !got)) {
+                if (tid == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                aborted = true;
+                break;
+            }
+            const RowMeta m = meta[st];
+            if (m.t < 0) break;
+            const uint32_t par = nproc & 1u;
+            const uint32_t xph = (nproc >> 1) & 1u;
+            const uint32_t xb = xbar0 + 8u * par;
+            uint16_t* buf = reinterpret_cast<uint16_t*>(smem + st * L.stage_bytes);
+            const uint32_t buf_s = smem_addr(buf);
+            const int* ids_s = ids_all + st * K_max;
+            const float* lps_s = lps_all + st * K_max;
+            const int cnt = m.cnt, sa = m.sa;
+            const long long t = m.t;
+
+            // ---- 1. max pass (warps 1..) and recorded-id gather (warp 0) ------
+            float m_loc = -INFINITY;
+            bool timed_out = false;
+            if (warp == 0) {
+                for (int i = 0; i < nchunks && !timed_out; ++i)
+                    timed_out = !mbar_wait_bounded(bar_addr(st, i), fpar, kWaitLimitNs);
+                timed_out = __any_sync(kFull, timed_out);
+                if (!timed_out) {
+                    if (lane < tail) m_loc = bf_to_f(buf[n8 + lane]);
+                    const bool a_own = sa >= lo && sa < hi;
+                    if (a_own && lane == 0) {
+                        const float zav = bf_to_f(buf[sa - lo]);
+                        const uint32_t za_s = smem_addr(&za[par]);
+                        for (int r = 0; r < C; ++r)
+                            st_async_v2(map_to_rank(za_s, r), __float_as_uint(zav), 1u, map_to_rank(xb, r));
+                    }
+                    __syncwarp();
+                    int nfix = 0, n_inrange = 0;
+                    bool a_in_h = false;
+                    const uint32_t xh_s = smem_addr(xh + static_cast<int>(par) * K_max);
+                    for (int base = 0; base < cnt; base += 32) {
+                        const int k = base + lane;
+                        const bool in = k < cnt;
+                        const int id = in ? ids_s[k] : -1;
+                        n_inrange += __popc(__ballot_sync(kFull, in && id >= 0 && id < a.V));
+                        const bool owned = in && id >= lo && id < hi;
+                        const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
+                        const bool first = owned && (same & lanemask_lt()) == 0u;
+                        const uint16_t h = owned ? buf[id - lo] : static_cast<uint16_t>(0);
+                        const bool valid = first && h != kSentinel;
+                        __syncwarp();
+                        if (valid) {
+                            buf[id - lo] = kSentinel;
+                            m_loc = fmaxf(m_loc, bf_to_f(h));
+                        }
+                        if (owned) {
+                            const uint32_t fz = __float_as_uint(bf_to_f(h));
+                            const uint32_t fl = valid ? 1u : 2u;
+                            for (int r = 0; r < C; ++r)
+                                st_async_v2(map_to_rank(xh_s + 8u * k, r), fz, fl, map_to_rank(xb, r));
+                        }
+                        const unsigned vm = __ballot_sync(kFull, valid);
+                        if (valid) {
+                            const int pos = nfix + __popc(vm & lanemask_lt());
+                            fix_i[pos] = id - lo;
+                            fix_k[pos] = k;
+                        }
+                        nfix += __popc(vm);
+                        a_in_h = a_in_h || __any_sync(kFull, valid && id == sa);
+                        __syncwarp();
+                    }
+                    if (a_own && !a_in_h) {
+                        if (lane == 0) {
+                            fix_i[nfix] = sa - lo;
+                            fix_k[nfix] = -1;
+                        }
+                        nfix += 1;
+                    }
+                    // bytes this CTA receives this row: one 8-byte entry per in-range
+                    // recorded id, one 16-byte partial per CTA, and z_a
+                    if (lane == 0)
+                        mbar_expect_tx(xb, static_cast<uint32_t>(8 * n_inrange + 16 * C + 8));
+                    __syncwarp();
+                    for (int e = lane; e < nfix; e += 32) {
+                        const int li = fix_i[e];
+                        atomicOr(&bmp[li >> 8], 1u << ((li >> 3) & 31));
+                    }
+                    if (lane == 0) scal_i[3] = nfix;
+                }
+            } else {
+                uint32_t mx2 = 0xFF80FF80u;  // (-inf, -inf)
+                for (int i = 0; i < nchunks && !timed_out; ++i) {
+                    const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                    if (!mbar_wait_bounded(bar_addr(st, i), fpar, kWaitLimitNs)) {
+                        timed_out = true;
+                        break;
+                    }
+                    for (int j = v0 + tid - 32; j < v1; j += NC - 32) {
+                        const uint4 w = lds128(buf_s + 16u * j);
+                        mx2 = bmax2(mx2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
+                    }
+                }
+                m_loc = fmaxf(bf_lo(mx2), bf_hi(mx2));
+            }
+            m_loc = warp_max(m_loc);
+            if (lane == 0) red[warp] = m_loc;
+            if (named_bar_or(NC, timed_out)) {
+                if (tid == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                aborted = true;
+                break;
+            }
+            m_loc = red[0];
+#pragma unroll
+            for (int w = 1; w < NCW; ++w) m_loc = fmaxf(m_loc, red[w]);
+
+            // ---- 2. exp pass over the unrecorded entries ----------------------
+            const float o_c = m_loc * kscale;
+            float s1 = 0.0f, s2 = 0.0f;
+            for (int j = tid; j < nv; j += NC) {
+                const uint4 w = lds128(buf_s + 16u * j);
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float y0 = fmaf(bf_lo(ww[q]), kscale, -o_c);
+                    const float y1 = fmaf(bf_hi(ww[q]), kscale, -o_c);
+                    const float e0 = ex2(y0), e1 = ex2(y1);
+                    s1 += e0;
+                    s1 += e1;
+                    s2 = fmaf(e0, y0, s2);
+                    s2 = fmaf(e1, y1, s2);
+                }
+            }
+            s1 = warp_sum(s1);
+            s2 = warp_sum(s2);
+            if (lane == 0) {
+                red[NCW + warp] = s1;
+                red[2 * NCW + warp] = s2;
+            }
+            named_bar(NC);
+
+            // ---- 3. cluster exchange and row scalars (warp 0) -------------------
+            if (warp == 0) {
+                if (lane == 0) {
+                    float S1 = 0.0f, S2 = 0.0f;
+                    for (int w = 0; w < NCW; ++w) {
+                        S1 += red[NCW + w];
+                        S2 += red[2 * NCW + w];
+                    }
+                    const uint32_t ps = smem_addr(part + static_cast<int>(par) * kMaxCluster + crank);
+                    for (int r = 0; r < C; ++r)
+                        st_async_v4(map_to_rank(ps, r), __float_as_uint(m_loc), __float_as_uint(S1),
+                                    __float_as_uint(S2), __float_as_uint(rs_prev), map_to_rank(xb, r));
+                }
+                const bool ok = mbar_wait_cluster_bounded(xb, xph, kWaitLimitNs);
+                if (!__all_sync(kFull, ok)) {
+                    if (lane == 0) {
+                        status_or(a.status, SC_STATUS_TIMEOUT_EXCHANGE);
+                        scal_i[4] = 1;
+                    }
+                } else {
+                    const float4* pp = part + static_cast<int>(par) * kMaxCluster;
+                    float mg = -INFINITY;
+                    for (int r = 0; r < C; ++r) mg = fmaxf(mg, pp[r].x);
+                    const float o = mg * kscale;
+                    float lT = 0.0f, ET = 0.0f;
+                    for (int r = 0; r < C; ++r) {
+                        const float4 pr = pp[r];
+                        if (pr.y > 0.0f) {
+                            const float d = pr.x * kscale - o;
+                            const float f = ex2(d);
+                            lT += pr.y * f;
+                            ET += f * (pr.z + d * pr.y);
+                        }
+                    }
+                    const float2* xr = xh + static_cast<int>(par) * K_max;
+                    float lH = 0.0f, EH = 0.0f, lp_best = -INFINITY;
+                    int nval = 0, k_best = 0x7FFFFFFF;
+                    uint32_t kfl = 0;
+                    for (int k = lane; k < cnt; k += 32) {
+                        const int id = ids_s[k];
+                        if (id < 0 || id >= a.V) {
+                            kfl |= SC_FLAG_BAD_ID;
+                            continue;
+                        }
+                        const float2 x = xr[k];
+                        if (__float_as_uint(x.y) != 1u) {
+                            kfl |= SC_FLAG_DUP_ID;
+                            continue;
+                        }
+                        const float y = fmaf(x.x, kscale, -o);
+                        const float e = ex2(y);
+                        lH += e;
+                        EH = fmaf(e, y, EH);
+                        ++nval;
+                        const float lp = lps_s[k];
+                        if (lp > lp_best) {
+                            lp_best = lp;
+                            k_best = k;
+                        }
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        lH += __shfl_xor_sync(kFull, lH, off);
+                        EH += __shfl_xor_sync(kFull, EH, off);
+                        nval += __shfl_xor_sync(kFull, nval, off);
+                        kfl |= __shfl_xor_sync(kFull, kfl, off);
+                        const float ol = __shfl_xor_sync(kFull, lp_best, off);
+                        const int ok2 = __shfl_xor_sync(kFull, k_best, off);
+                        if (ol > lp_best || (ol == lp_best && ok2 < k_best)) {
+                            lp_best = ol;
+                            k_best = ok2;
+                        }
+                    }
+                    // 1 - Q_H without cancellation: -expm1(l_max) minus the other
+                    // recorded probabilities, summed error-free (two-sum) in FP32.
+                    float qh = 0.0f, ql = 0.0f;
+                    for (int k = lane; k < cnt; k += 32) {
+                        const int id = ids_s[k];
+                        if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u || k == k_best) continue;
+                        float sh, se;
+                        two_sum(qh, expf(lps_s[k]), sh, se);
+                        qh = sh;
+                        ql += se;
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float oh = __shfl_xor_sync(kFull, qh, off);
+                        const float ol = __shfl_xor_sync(kFull, ql, off);
+                        float sh, se;
+                        two_sum(qh, oh, sh, se);
+                        qh = sh;
+                        ql = ql + ol + se;
+                    }
+                    float tail_mu = 1.0f, Q_H = 0.0f;
+                    if (nval > 0) {
+                        tail_mu = (-expm1f(lp_best) - qh) - ql;
+                        Q_H = (expf(lp_best) + qh) + ql;
+                    }
+                    const float l = lT + lH;
+                    const float log2l = log2f(l);
+                    const float P_H = lH / l;
+                    const float tail_pi = lT / l;
+                    const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
+                    uint32_t flags = m.rflags | kfl;
+                    if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
+                    if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
+                    const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
+                    const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
+                    const float ya = fmaf(za[par].x, kscale, -o);
+                    const float logp_a = (ya - log2l) * kLn2;
+                    float wt = 1.0f, k3 = 0.0f;
+                    if (a.rollout) {
+                        const float d = logp_a - m.rl;
+                        k3 = expm1f(d) - d;
+                        const float w = expf(d);
+                        if (a.is_mode == SC_IS_TIS) {
+                            if (w > a.tis_max) {
+                                wt = a.tis_max;
+                                flags |= SC_FLAG_IS_TRUNC;
+                            } else {
+                                wt = w;
+                            }
+                        } else if (a.is_mode == SC_IS_MIS) {
+                            if (w >= a.mis_min && w <= a.mis_max) {
+                                wt = w;
+                            } else {
+                                wt = 0.0f;
+                                flags |= SC_FLAG_IS_REJECT;
                             }
                         }
-                        if ((flags & SC_FLAG_DATA_ERRORS) && a.status) atomicOr(a.status, SC_STATUS_DATA);
+                    }
+                    const float A = m.A;
+                    const float Aw = A * wt;
+                    float csum = 0.0f;
+                    if (a.centering) {
+                        for (int k = lane; k < cnt; k += 32) {
+                            const int id = ids_s[k];
+                            if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u) continue;
+                            const float lk = fmaf(xr[k].x, kscale, -o) - log2l;  // log2 p_k
+                            const float c = expf(lps_s[k]) - rho * ex2(lk);
+                            csum = fmaf(c, lk * kLn2, csum);
+                        }
+                        csum = warp_sum(csum);
+                    }
+                    const float loss = -Aw * (logp_a - csum);
+                    const float entropy = kLn2 * (log2l - (ET + EH) / l);
+                    const float alpha = -a.grad_scale * a.inv_t * Aw;
+                    const float beta = -alpha * s;
+                    const int nfix = scal_i[3];
+                    for (int e = lane; e < nfix; e += 32) {
+                        const int k = fix_k[e];
+                        float g;
+                        if (k >= 0) {
+                            const float p = ex2(fmaf(xr[k].x, kscale, -o) - log2l);
+                            const float mu = a.centering ? fmaf(dsr, p, expf(lps_s[k])) : p;
+                            g = alpha * ((ids_s[k] == sa ? 1.0f : 0.0f) - mu);
+                        } else {
+                            g = alpha * (1.0f - s * ex2(ya - log2l));
+                        }
+                        fix_v[e] = g;
+                    }
+                    if (lane == 0) {
+                        scal[0] = o + log2l;
+                        scal[1] = beta;
+                        scal_i[4] = 0;
+                        if (crank == 0) {
+                            a.logp[t] = logp_a;
+                            if (a.diag) {
+                                sc_row_diag d;
+                                d.loss = loss;
+                                d.logp_a = logp_a;
+                                d.P_H = P_H;
+                                d.tail_pi = tail_pi;
+                                d.Q_H = Q_H;
+                                d.tail_mu = tail_mu;
+                                d.rho = rho;
+                                d.s = s;
+                                d.entropy = entropy;
+                                d.k3 = k3;
+                                d.is_weight = wt;
+                                d.row_sum = 0.0f;
+                                d.adv = A;
+                                d.n_valid_k = nval;
+                                d.flags = flags;
+                                d.reserved = 0;
+                                a.diag[t] = d;
+                                if (t_prev >= 0) {  // the previous row's sum rode in with this exchange
+                                    float rsum = 0.0f;
+                                    for (int r = 0; r < C; ++r) rsum += pp[r].w;
+                                    a.diag[t_prev].row_sum = rsum;
+                                }
+                            }
+                            if (flags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+                        }
                     }
                 }
             }
-        }
-        __syncthreads();
-        if (scal_i[4]) {
-            abort = true;
-            break;
-        }
+            named_bar(NC);
+            if (scal_i[4]) {
+                aborted = true;
+                break;
+            }
 
-        // ---- 6. write pass: g = beta * p, patched at recorded ids and a --------
-        const float bw = scal[0];
-        const float beta = scal[1];
-        const int nfix = scal_i[3];
-        float rs = 0.0f;
-        for (int j = tid; j < nvb; j += NT) {
-            const uint4 w = lds128(buf_s + 16u * j);
-            float g[8];
-            g[0] = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
-            g[1] = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
-            g[2] = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
-            g[3] = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
-            g[4] = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
-            g[5] = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
-            g[6] = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
-            g[7] = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
-            const uint32_t word = bmp[j >> 5];  // same word for the whole warp
-            if (word != 0u && ((word >> (j & 31)) & 1u)) {
-                for (int e = 0; e < nfix; ++e) {
-                    const int li = fix_i[e];
-                    if ((li >> 3) == j) {
-                        const float v = fix_v[e];
+            // ---- 4. write pass: g = beta p, patched at recorded ids and a ----------
+            const float bw = scal[0];
+            const float beta = scal[1];
+            const int nfix = scal_i[3];
+            uint16_t* grow = a.grad + t * a.gstride + lo;
+            float rs = 0.0f;
+            for (int j = tid; j < nvb; j += NC) {
+                const uint4 w = lds128(buf_s + 16u * j);
+                float g[8];
+                g[0] = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
+                g[1] = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
+                g[2] = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
+                g[3] = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
+                g[4] = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
+                g[5] = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
+                g[6] = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
+                g[7] = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
+                const uint32_t word = bmp[j >> 5];  // same word for the whole warp
+                if (word != 0u && ((word >> (j & 31)) & 1u)) {
+                    for (int e = 0; e < nfix; ++e) {
+                        const int li = fix_i[e];
+                        if ((li >> 3) == j) {
+                            const float v = fix_v[e];
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            if ((li & 7) == q) g[q] = v;
+                            for (int q = 0; q < 8; ++q)
+                                if ((li & 7) == q) g[q] = v;
+                        }
                     }
                 }
+                rs += ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
+                st_global_v4_hint(grow + 8 * j, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                                  pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]), pol);
             }
-            rs += ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
-            st_global_v4_hint(grow + 8 * j, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
-                              pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]), pol);
-        }
-        if (tail && tid == 0) {
-            for (int q = 0; q < tail; ++q) {
-                const int li = n8 + q;
-                float g = beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
-                for (int e = 0; e < nfix; ++e)
-                    if (fix_i[e] == li) g = fix_v[e];
-                rs += g;
-                grow[li] = f_to_bf_bits(g);
+            if (tail && tid == 0) {
+                for (int q = 0; q < tail; ++q) {
+                    const int li = n8 + q;
+                    float g = beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
+                    for (int e = 0; e < nfix; ++e)
+                        if (fix_i[e] == li) g = fix_v[e];
+                    rs += g;
+                    grow[li] = f_to_bf_bits(g);
+                }
             }
+            rs = warp_sum(rs);
+            if (lane == 0) red[3 * NCW + warp] = rs;
+            named_bar(NC);
+            if (tid == 0) {
+                float tot = 0.0f;
+                for (int w = 0; w < NCW; ++w) tot += red[3 * NCW + w];
+                rs_prev = tot;
+                mbar_arrive(bar_addr(st, kMaxChunks + 1));  // stage free for the producer
+            }
+            if (warp == 0)
+                for (int e = lane; e < nfix; e += 32) bmp[fix_i[e] >> 8] = 0u;
+            t_prev = t;
+            ++nproc;
         }
-        rs = warp_sum(rs);
-        if (lane == 0) red[3 * NW + warp] = rs;
-        __syncthreads();
-        if (tid == 0) {
-            float tot = 0.0f;
-            for (int w = 0; w < NW; ++w) tot += red[3 * NW + w];
-            rs_prev = tot;
-        }
-        t_prev = t;
-        if (warp == 0)
-            for (int e = lane; e < nfix; e += 32) bmp[fix_i[e] >> 8] = 0u;
-        ++nvalid;
+        t_last = t_prev;
+        rs_last = rs_prev;
     }
 
     // The row sum of the last valid row goes to CTA 0 over DSMEM; the final
-    // cluster barrier also keeps every CTA's shared memory alive until no peer
-    // can still write to it.
-    if (tid == 0 && a.diag && t_prev >= 0 && !abort) {
+    // cluster barrier also keeps every CTA's shared memory alive until no
+    // peer can still write to it.
+    if (tid == 0 && a.diag && t_last >= 0 && !aborted) {
         const uint32_t fs = smem_addr(frs + crank);
-        st_cluster_v2(map_to_rank(fs, 0), __float_as_uint(rs_prev), 0u);
+        st_cluster_v2(map_to_rank(fs, 0), __float_as_uint(rs_last), 0u);
     }
     cluster_sync_all();
-    if (crank == 0 && tid == 0 && a.diag && t_prev >= 0 && !abort) {
+    if (crank == 0 && tid == 0 && a.diag && t_last >= 0 && !aborted) {
         float rsum = 0.0f;
         for (int r = 0; r < C; ++r) rsum += frs[r].x;
-        a.diag[t_prev].row_sum = rsum;
+        a.diag[t_last].row_sum = rsum;
     }
 }
 
@@ -610,61 +720,64 @@ __global__ void __launch_bounds__(NT) center_kernel(const __grid_constant__ KArg
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 struct Plan {
-    int C, NT, S, ncv;
+    int C, NC, S, ncv, NB;
     Layout L;
 };
 
-Layout make_layout(int S, int K_max, int NT) {
+Layout make_layout(int S, int K_max, int NC, int NB) {
     Layout L;
-    int off = round_up(S * 2, 128);
+    L.stage_bytes = round_up(S * 2, 128);
+    int off = NB * L.stage_bytes;
     auto take = [&](int bytes) {
         const int o = off;
         off = round_up(off + bytes, 16);
         return o;
     };
-    L.off_bars = take((kMaxChunks + 2) * 8);
+    L.off_ids = take(NB * K_max * 4);
+    L.off_lps = take(NB * K_max * 4);
+    L.off_meta = take(NB * static_cast<int>(sizeof(RowMeta)));
+    L.off_bars = take((kMaxStages * kBarsPerStage + 2) * 8);
     L.off_part = take(2 * kMaxCluster * 16);
     L.off_frs = take(kMaxCluster * 8);
     L.off_za = take(2 * 8);
     L.off_xh = take(2 * K_max * 8);
-    L.off_ids = take(K_max * 4);
-    L.off_lps = take(K_max * 4);
     L.off_fixi = take((K_max + 1) * 4);
     L.off_fixk = take((K_max + 1) * 4);
     L.off_fixv = take((K_max + 1) * 4);
     L.off_bmp = take(((S / 8 + 31) / 32) * 4);
-    L.off_red = take(4 * (NT / 32) * 4);
+    L.off_red = take(4 * (NC / 32) * 4);
     L.off_scal = take(8 * 4);
     L.total = off;
     return L;
 }
 
-int make_plan(int V, int K_max, int req_cluster, int req_threads, Plan* out) {
+// Automatic plan: a vocabulary slice of at most ~19 KiB per CTA (clusters of
+// up to 16 CTAs), two pipeline stages, 256 consumer threads.  For the
+// 151936-entry vocabulary this is 16 CTAs x 9496 entries and about 45 KB of
+// shared memory per CTA.
+int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
+    const int NB = req_stages > 0 ? req_stages : 2;
     int C = req_cluster;
-    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128); };
+    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 2048 ? 256 : 128); };
     if (C <= 0) {
-        C = static_cast<int>((2LL * V + kTargetSliceBytes - 1) / kTargetSliceBytes);
-        C = C < 1 ? 1 : (C > 8 ? 8 : C);
-        // no empty slice: at least 8 entries per CTA
+        C = static_cast<int>((2LL * V + 19455) / 19456);
+        C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
         while (C > 1 && static_cast<long long>(C - 1) * round_up((V + C - 1) / C, 8) >= V) --C;
-        for (;;) {
-            const int S = round_up((V + C - 1) / C, 8);
-            if (make_layout(S, K_max, threads_for(S)).total <= kMaxSmem || C >= kMaxCluster) break;
-            ++C;
-        }
     }
     const int S = round_up((V + C - 1) / C, 8);
-    const int NT = threads_for(S);
-    const Layout L = make_layout(S, K_max, NT);
+    const int NC = threads_for(S);
+    const Layout L = make_layout(S, K_max, NC, NB);
     if (L.total > kMaxSmem)
-        return fail(SC_ERR_SHAPE, "V = %d with cluster size %d needs %d bytes of shared memory per CTA",
-                    V, C, L.total);
+        return fail(SC_ERR_SHAPE,
+                    "V = %d with cluster size %d and %d stages needs %d bytes of shared memory per CTA", V, C,
+                    NB, L.total);
     const int nvb = S / 8;
     int nch = (nvb + kChunkVecTarget - 1) / kChunkVecTarget;
     nch = nch < 1 ? 1 : (nch > kMaxChunks ? kMaxChunks : nch);
     out->C = C;
-    out->NT = NT;
+    out->NC = NC;
     out->S = S;
+    out->NB = NB;
     out->ncv = (nvb + nch - 1) / nch;
     if (out->ncv < 1) out->ncv = 1;
     out->L = L;
@@ -673,8 +786,8 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, Plan* out) {
 
 using KernelFn = void (*)(KArgs);
 
-KernelFn kernel_for(int NT) {
-    switch (NT) {
+KernelFn kernel_for(int NC) {
+    switch (NC) {
         case 128: return center_kernel<128>;
         case 256: return center_kernel<256>;
         case 384: return center_kernel<384>;
@@ -684,28 +797,27 @@ KernelFn kernel_for(int NT) {
 }
 
 std::mutex g_plan_mutex;
-std::map<std::tuple<int, int>, int> g_smem_set;                 // (device, NT) -> bytes allowed
-std::map<std::tuple<int, int, int, int>, int> g_max_clusters;  // (device, NT, C, smem)
+std::map<std::tuple<int, int>, int> g_attr_set;                     // (device, NC)
+std::map<std::tuple<int, int, int, int>, int> g_max_clusters;      // (device, NC, C, smem)
 
 // Sets the kernel's shared-memory and cluster attributes and returns the
 // number of clusters that can be resident at once.
 int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
-    KernelFn fn = kernel_for(P.NT);
-    if (!fn) return fail(SC_ERR_ARG, "threads = %d is not one of 128, 256, 384, 512", P.NT);
+    KernelFn fn = kernel_for(P.NC);
+    if (!fn) return fail(SC_ERR_ARG, "threads = %d is not one of 128, 256, 384, 512", P.NC);
     std::lock_guard<std::mutex> lock(g_plan_mutex);
     cudaError_t e;
-    auto key = std::make_tuple(dev, P.NT);
-    auto it = g_smem_set.find(key);
-    if (it == g_smem_set.end() || it->second < P.L.total) {
+    auto key = std::make_tuple(dev, P.NC);
+    if (g_attr_set.find(key) == g_attr_set.end()) {
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
-        g_smem_set[key] = kMaxSmem;
+        g_attr_set[key] = 1;
     }
-    auto ckey = std::make_tuple(dev, P.NT, P.C, P.L.total);
+    auto ckey = std::make_tuple(dev, P.NC, P.C, P.L.total);
     auto cit = g_max_clusters.find(ckey);
     if (cit != g_max_clusters.end()) {
         *max_clusters = cit->second;
@@ -713,7 +825,7 @@ int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.C, 1, 1);
-    cfg.blockDim = dim3(P.NT, 1, 1);
+    cfg.blockDim = dim3(P.NC + 32, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -736,7 +848,8 @@ int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
 int check_params(int V, const sc_params* p) {
     if (!p) return fail(SC_ERR_NULL, "params is NULL");
     if (V < 1 || V > kMaxV) return fail(SC_ERR_SHAPE, "V = %d outside 1..%d", V, kMaxV);
-    if (p->K_max < 0 || p->K_max > kMaxK) return fail(SC_ERR_SHAPE, "K_max = %d outside 0..%d", p->K_max, kMaxK);
+    if (p->K_max < 0 || p->K_max > kMaxK)
+        return fail(SC_ERR_SHAPE, "K_max = %d outside 0..%d", p->K_max, kMaxK);
     if (!(p->inv_temperature > 0.0f) || !std::isfinite(p->inv_temperature) || p->inv_temperature > 1e4f)
         return fail(SC_ERR_ARG, "inv_temperature must be finite and in (0, 1e4]");
     if (!std::isfinite(p->grad_scale)) return fail(SC_ERR_ARG, "grad_scale must be finite");
@@ -751,6 +864,8 @@ int check_params(int V, const sc_params* p) {
         return fail(SC_ERR_ARG, "cluster_size = %d outside 0..%d", p->cluster_size, kMaxCluster);
     if (p->threads != 0 && !kernel_for(p->threads))
         return fail(SC_ERR_ARG, "threads = %d is not 0, 128, 256, 384 or 512", p->threads);
+    if (p->stages < 0 || p->stages > kMaxStages)
+        return fail(SC_ERR_ARG, "stages = %d outside 0..%d", p->stages, kMaxStages);
     return SC_OK;
 }
 
@@ -763,7 +878,7 @@ extern "C" int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* 
     int st = check_params(V, p);
     if (st != SC_OK) return st;
     Plan P;
-    st = make_plan(V, p->K_max, p->cluster_size, p->threads, &P);
+    st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, &P);
     if (st != SC_OK) return st;
     int dev = 0;
     st = check_device(&dev);
@@ -772,7 +887,7 @@ extern "C" int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* 
     st = prepare_kernel(dev, P, &mc);
     if (st != SC_OK) return st;
     if (cluster_size) *cluster_size = P.C;
-    if (threads) *threads = P.NT;
+    if (threads) *threads = P.NC;
     if (slice) *slice = P.S;
     if (smem_bytes) *smem_bytes = P.L.total;
     if (max_clusters) *max_clusters = mc;
@@ -820,7 +935,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
             return fail(SC_ERR_ARG, "grad_out overlaps logits other than exactly (in place)");
     }
     Plan P;
-    st = make_plan(V, p->K_max, p->cluster_size, p->threads, &P);
+    st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, &P);
     if (st != SC_OK) return st;
     int dev = 0;
     st = check_device(&dev);
@@ -860,11 +975,12 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.C = P.C;
     ka.S = P.S;
     ka.ncv = P.ncv;
+    ka.NB = P.NB;
     ka.L = P.L;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(G * P.C), 1, 1);
-    cfg.blockDim = dim3(P.NT, 1, 1);
+    cfg.blockDim = dim3(P.NC + 32, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
@@ -874,7 +990,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NT), ka);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NC), ka);
     if (e != cudaSuccess) return cuda_fail(e, "center_kernel launch");
     return ok();
 }

@@ -79,6 +79,7 @@ int sc_params_default(sc_params* p) {
     p->grad_scale = 1.0f;
     p->cluster_size = 0;
     p->threads = 0;
+    p->stages = 0;
     return sc::ok();
 }
 

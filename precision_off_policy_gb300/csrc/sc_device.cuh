@@ -188,3 +188,54 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 }
 
 }  // namespace sc
+
+namespace sc {
+
+// Asynchronous stores into a peer CTA's shared memory that complete as
+// transaction bytes on the peer's mbarrier (DSMEM, sm_90+).
+__device__ __forceinline__ void st_async_v2(uint32_t cluster_addr, uint32_t a, uint32_t b,
+                                            uint32_t cluster_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+            cluster_addr),
+        "r"(a), "r"(b), "r"(cluster_bar)
+        : "memory");
+}
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t cluster_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            cluster_addr),
+        "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier 1 over the first `n` threads of the CTA (n a multiple of 32).
+__device__ __forceinline__ void named_bar(int n) {
+    asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
+}
+// Same barrier, returning the OR of `p` over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int n, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, %2, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p)), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Error-free sum of two floats (Knuth's two-sum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+}  // namespace sc

@@ -120,11 +120,13 @@ def test_ragged_vocabulary_sizes(V):
     _full_check(batch, sc_params(batch), f"V={V}")
 
 
-@pytest.mark.parametrize("cluster,threads", [(1, 128), (2, 256), (3, 384), (4, 512), (8, 256), (16, 128)])
-def test_explicit_launch_shapes(cluster, threads):
+@pytest.mark.parametrize("cluster,threads,stages", [(1, 128, 1), (2, 256, 2), (3, 384, 3), (4, 512, 4),
+                                                    (8, 256, 1), (16, 128, 2), (16, 256, 3), (5, 256, 2)])
+def test_explicit_launch_shapes(cluster, threads, stages):
     cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=16, len_lo=10, len_hi=16, V=30011)
     batch = synth.make_batch(cfg)
-    _full_check(batch, sc_params(batch, cluster_size=cluster, threads=threads), f"C={cluster} NT={threads}")
+    _full_check(batch, sc_params(batch, cluster_size=cluster, threads=threads, stages=stages),
+                f"C={cluster} NT={threads} stages={stages}")
 
 
 @pytest.mark.parametrize("mode", [sc.SC_IS_TIS, sc.SC_IS_MIS])
