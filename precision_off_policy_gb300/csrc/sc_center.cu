@@ -21,18 +21,19 @@
 //   stages the next row streams in while the current one is computed.
 // * consumer warps, per valid row:
 //   1. max pass on packed bf16 pairs as chunks land, while consumer warp 0
-//      gathers the recorded ids that fall in the slice, drops repeats,
-//      pushes their logits to every CTA of the cluster and overwrites them in
-//      shared memory with -2^100 (the max is exact either way, because warp 0
-//      contributes the values it overwrites);
-//   2. exp pass over the slice: the unrecorded mass sum_{v not in H}
-//      e^{x_v - m} accumulates directly (no 1 - P_H cancellation), with the
-//      entropy term;
-//   3. exchange: partials go to every CTA of the cluster with st.async
-//      stores that complete as transaction bytes on the receiver's mbarrier
-//      (one expect_tx per CTA and row); warp 0 then computes the row scalars
-//      (LSE, P_H, Q_H, rho, s, loss, k3, importance weight) redundantly in
-//      every CTA;
+//      gathers the recorded ids that fall in the slice, drops repeats and
+//      overwrites them in shared memory with -2^100 (the max is exact either
+//      way, because warp 0 contributes the values it overwrites);
+//   2. warp 0 reduces the recorded ids it owns (mass, entropy term, sum of
+//      q y, the recorded mass as an error-free FP32 pair with its largest
+//      term apart); all warps run the exp pass over the slice, so that the
+//      unrecorded mass sum_{v not in H} e^{x_v - m} accumulates directly (no
+//      1 - P_H cancellation), with the entropy term;
+//   3. exchange: each CTA sends one 64-byte record to every CTA of the
+//      cluster with st.async stores that complete as transaction bytes on
+//      the receiver's mbarrier (one expect_tx per CTA and row); warp 0 then
+//      merges the C records into the row scalars (LSE, P_H, Q_H, rho, s,
+//      loss, k3, importance weight), redundantly in every CTA, in O(C);
 //   4. write pass: p_v is recomputed from shared memory and g_v = beta p_v
 //      streams to global memory with 16-byte stores and an evict-first L2
 //      hint; the <= K+1 special entries (recorded ids and the sampled token)
@@ -76,7 +77,7 @@ struct RowMeta {
 
 struct Layout {
     int stage_bytes;  // bytes of one stage's logit slice (128-aligned)
-    int off_ids, off_lps, off_meta, off_bars, off_part, off_frs, off_za, off_xh, off_fixi, off_fixk,
+    int off_ids, off_lps, off_meta, off_bars, off_part, off_mine, off_frs, off_fixi, off_fixk, off_fixz,
         off_fixv, off_bmp, off_red, off_scal, total;
 };
 
@@ -118,8 +119,68 @@ __device__ __forceinline__ void status_or(uint32_t* st, uint32_t bits) {
     if (st) atomicOr(st, bits);
 }
 
-// Bars of one stage: [0, kMaxChunks) chunk copies, kMaxChunks full, kMaxChunks+1 empty.
-constexpr int kBarsPerStage = kMaxChunks + 2;
+// Barriers of one pipeline stage.  A stage's chunk slots are recycled one by
+// one: the write pass releases chunk i (kChunkFree + i) as soon as every
+// consumer warp is done with it, and the producer starts the next row's copy
+// into that slot right away.
+constexpr int kChunkFull = 0;                  // [kMaxChunks] bulk copy landed (tx bytes)
+constexpr int kChunkFree = kMaxChunks;         // [kMaxChunks] consumer warps done with the chunk
+constexpr int kRowFull = 2 * kMaxChunks;       // producer: metadata, ids and tail written
+constexpr int kMetaFree = 2 * kMaxChunks + 1;  // consumers: metadata and ids no longer read
+constexpr int kRowDone = 2 * kMaxChunks + 2;   // consumers: the whole stage is free
+constexpr int kBarsPerStage = 2 * kMaxChunks + 3;
+
+// One CTA's contribution to a row, exchanged across the cluster (64 bytes).
+// y' values are relative to this CTA's own slice maximum m (y' = (z - m) kscale).
+struct Partial {
+    float m;            // slice maximum of z (-inf for an empty slice)
+    float S1, S2;       // unrecorded entries: sum 2^y', sum 2^y' y'
+    float rs;           // FP32 gradient sum of this slice for the previous valid row
+    float lH, EH;       // recorded ids owned here: sum 2^y', sum 2^y' y'
+    float QY;           // sum q_k y'_k over the owned recorded ids
+    float qo_hi, qo_lo; // sum of q_k over them except the largest one (double-float)
+    float lpmax;        // largest recorded log-probability owned here (-inf if none)
+    int kbest;          // its position k (INT_MAX if none)
+    int nval;           // owned recorded ids used
+    uint32_t flags;     // repeated ids (owner), ids out of range (CTA 0)
+    float ya;           // y' of the sampled token, if this CTA owns it
+    int has_a;
+    int pad;
+};
+static_assert(sizeof(Partial) == 64, "partial record is 64 bytes");
+
+// Largest recorded log-probability with the mass of the others, merged
+// commutatively (ties go to the lower k) so a butterfly gives every lane the
+// same bits.  The others' mass is kept as an unevaluated FP32 pair.
+struct HeadMass {
+    float lp;
+    int k;
+    float oh, ol;
+};
+__device__ __forceinline__ HeadMass head_merge(const HeadMass& a, const HeadMass& b) {
+    const bool b_wins = b.lp > a.lp || (b.lp == a.lp && b.k < a.k);
+    const HeadMass& w = b_wins ? b : a;
+    const HeadMass& l = b_wins ? a : b;
+    HeadMass r;
+    r.lp = w.lp;
+    r.k = w.k;
+    float s, e;
+    two_sum(a.oh, b.oh, s, e);
+    float ol = (a.ol + b.ol) + e;
+    float s2, e2;
+    two_sum(s, expf(l.lp), s2, e2);  // expf(-inf) = 0 for an empty side
+    r.oh = s2;
+    r.ol = ol + e2;
+    return r;
+}
+__device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
+    HeadMass o;
+    o.lp = __shfl_xor_sync(kFull, h.lp, off);
+    o.k = __shfl_xor_sync(kFull, h.k, off);
+    o.oh = __shfl_xor_sync(kFull, h.oh, off);
+    o.ol = __shfl_xor_sync(kFull, h.ol, off);
+    return o;
+}
 
 template <int NC>
 __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__ KArgs a) {
@@ -136,12 +197,12 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
     RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);      // [NB]
     int* ids_all = reinterpret_cast<int*>(smem + L.off_ids);            // [NB][K_max]
     float* lps_all = reinterpret_cast<float*>(smem + L.off_lps);        // [NB][K_max]
-    float4* part = reinterpret_cast<float4*>(smem + L.off_part);        // [2][kMaxCluster]
+    Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);      // [2][kMaxCluster]
+    Partial* mine = reinterpret_cast<Partial*>(smem + L.off_mine);      // staging of this CTA's record
     float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);          // [kMaxCluster]
-    float2* za = reinterpret_cast<float2*>(smem + L.off_za);            // [2]
-    float2* xh = reinterpret_cast<float2*>(smem + L.off_xh);            // [2][K_max]
     int* fix_i = reinterpret_cast<int*>(smem + L.off_fixi);             // [K_max + 1]
     int* fix_k = reinterpret_cast<int*>(smem + L.off_fixk);             // [K_max + 1]
+    float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);         // [K_max + 1]
     float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);         // [K_max + 1]
     uint32_t* bmp = reinterpret_cast<uint32_t*>(smem + L.off_bmp);      // one bit per 8 entries
     float* red = reinterpret_cast<float*>(smem + L.off_red);            // [4][NCW]
@@ -161,9 +222,13 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
 
     if (tid == 0) {
         for (int st = 0; st < NB; ++st) {
-            for (int i = 0; i < kMaxChunks; ++i) mbar_init(bar_addr(st, i), 1u);
-            mbar_init(bar_addr(st, kMaxChunks), 1u);      // full: producer's arrive
-            mbar_init(bar_addr(st, kMaxChunks + 1), 1u);  // empty: consumers' arrive
+            for (int i = 0; i < kMaxChunks; ++i) {
+                mbar_init(bar_addr(st, kChunkFull + i), 1u);
+                mbar_init(bar_addr(st, kChunkFree + i), static_cast<uint32_t>(NCW));
+            }
+            mbar_init(bar_addr(st, kRowFull), 1u);
+            mbar_init(bar_addr(st, kMetaFree), 1u);
+            mbar_init(bar_addr(st, kRowDone), 1u);
         }
         mbar_init(xbar0, 1u);  // exchange: own expect_tx arrive + peers' st.async bytes
         mbar_init(xbar0 + 8, 1u);
@@ -220,13 +285,12 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     continue;
                 }
                 const int st = static_cast<int>(nfill % NB);
-                if (nfill >= static_cast<uint32_t>(NB)) {
-                    const uint32_t epar = ((nfill / NB) - 1u) & 1u;
-                    if (!mbar_wait_bounded(bar_addr(st, kMaxChunks + 1), epar, kWaitLimitNs)) {
-                        if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                        stop = true;
-                        break;
-                    }
+                const bool reuse = nfill >= static_cast<uint32_t>(NB);
+                const uint32_t epar = ((nfill / NB) - 1u) & 1u;  // phase of the stage's previous use
+                if (reuse && !mbar_wait_bounded(bar_addr(st, kMetaFree), epar, kWaitLimitNs)) {
+                    if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                    stop = true;
+                    break;
                 }
                 int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
                 uint32_t rflags = 0;
@@ -243,7 +307,6 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 }
                 uint16_t* bufst = reinterpret_cast<uint16_t*>(smem + st * L.stage_bytes);
                 const uint16_t* lrow = a.logits + t * a.lstride + lo;
-                if (tail && lane < 8) bufst[n8 + lane] = lane < tail ? lrow[n8 + lane] : kSentinel;
                 if (lane == 0) {
                     RowMeta m;
                     m.t = t;
@@ -254,17 +317,36 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     m.A = __ldg(a.adv + rj);
                     m.rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
                     meta[st] = m;
-                    fence_proxy_async_smem();
+                    // chunk by chunk, as the previous row's write pass frees each slot
                     const uint32_t bs = smem_addr(bufst);
-                    for (int i = 0; i < nchunks; ++i) {
+                    for (int i = 0; i < nchunks && !stop; ++i) {
+                        if (reuse && !mbar_wait_bounded(bar_addr(st, kChunkFree + i), epar, kWaitLimitNs)) {
+                            status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                            // the chunks already started must land before the CTA can leave
+                            for (int i2 = 0; i2 < i; ++i2)
+                                (void)mbar_wait_bounded(bar_addr(st, kChunkFull + i2), (nfill / NB) & 1u,
+                                                        kWaitLimitNs);
+                            stop = true;
+                            break;
+                        }
+                        fence_proxy_async_smem();
                         const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
                         const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                        mbar_expect_tx(bar_addr(st, i), bytes);
-                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, bar_addr(st, i), pol);
+                        mbar_expect_tx(bar_addr(st, kChunkFull + i), bytes);
+                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, bar_addr(st, kChunkFull + i), pol);
+                    }
+                    if (!stop && reuse && !mbar_wait_bounded(bar_addr(st, kRowDone), epar, kWaitLimitNs)) {
+                        status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                        stop = true;
                     }
                 }
+                stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
+                if (stop) break;
+                // the tail entries (past the last whole 16-byte vector) by plain loads,
+                // once the previous row is completely done with the stage
+                if (tail && lane < 8) bufst[n8 + lane] = lane < tail ? lrow[n8 + lane] : kSentinel;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_addr(st, kMaxChunks));  // release: meta, ids, tail
+                if (lane == 0) mbar_arrive(bar_addr(st, kRowFull));  // release: meta, ids, tail
                 ++nfill;
             }
         }
@@ -272,11 +354,11 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
             const int st = static_cast<int>(nfill % NB);
             bool ok = true;
             if (nfill >= static_cast<uint32_t>(NB))
-                ok = mbar_wait_bounded(bar_addr(st, kMaxChunks + 1), ((nfill / NB) - 1u) & 1u, kWaitLimitNs);
+                ok = mbar_wait_bounded(bar_addr(st, kRowDone), ((nfill / NB) - 1u) & 1u, kWaitLimitNs);
             if (ok) {
                 if (lane == 0) {
                     meta[st].t = -1;
-                    mbar_arrive(bar_addr(st, kMaxChunks));
+                    mbar_arrive(bar_addr(st, kRowFull));
                 }
             } else if (lane == 0) {
                 status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
@@ -287,7 +369,7 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
             const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
             for (uint32_t f = f0; f < nfill; ++f)
                 for (int i = 0; i < nchunks; ++i)
-                    (void)mbar_wait_bounded(bar_addr(f % NB, i), (f / NB) & 1u, kWaitLimitNs);
+                    (void)mbar_wait_bounded(bar_addr(f % NB, kChunkFull + i), (f / NB) & 1u, kWaitLimitNs);
         }
         __syncwarp();
     } else {
@@ -298,7 +380,7 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
         for (;;) {
             const int st = static_cast<int>(nproc % NB);
             const uint32_t fpar = (nproc / NB) & 1u;
-            const bool got = mbar_wait_bounded(bar_addr(st, kMaxChunks), fpar, kWaitLimitNs);
+            const bool got = mbar_wait_bounded(bar_addr(st, kRowFull), fpar, kWaitLimitNs);
             if (named_bar_or(NC, !got)) {
                 if (tid == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                 aborted = true;
@@ -319,49 +401,41 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
             // ---- 1. max pass (warps 1..) and recorded-id gather (warp 0) ------
             float m_loc = -INFINITY;
             bool timed_out = false;
+            int nfix = 0;           // warp 0
+            uint32_t own_flags = 0; // warp 0
             if (warp == 0) {
                 for (int i = 0; i < nchunks && !timed_out; ++i)
-                    timed_out = !mbar_wait_bounded(bar_addr(st, i), fpar, kWaitLimitNs);
+                    timed_out = !mbar_wait_bounded(bar_addr(st, kChunkFull + i), fpar, kWaitLimitNs);
                 timed_out = __any_sync(kFull, timed_out);
                 if (!timed_out) {
                     if (lane < tail) m_loc = bf_to_f(buf[n8 + lane]);
                     const bool a_own = sa >= lo && sa < hi;
-                    if (a_own && lane == 0) {
-                        const float zav = bf_to_f(buf[sa - lo]);
-                        const uint32_t za_s = smem_addr(&za[par]);
-                        for (int r = 0; r < C; ++r)
-                            st_async_v2(map_to_rank(za_s, r), __float_as_uint(zav), 1u, map_to_rank(xb, r));
-                    }
+                    float zav = 0.0f;
+                    if (a_own) zav = bf_to_f(buf[sa - lo]);  // before any entry is overwritten
                     __syncwarp();
-                    int nfix = 0, n_inrange = 0;
-                    bool a_in_h = false;
-                    const uint32_t xh_s = smem_addr(xh + static_cast<int>(par) * K_max);
+                    bool a_in_h = false, dup = false, bad = false;
                     for (int base = 0; base < cnt; base += 32) {
                         const int k = base + lane;
                         const bool in = k < cnt;
                         const int id = in ? ids_s[k] : -1;
-                        n_inrange += __popc(__ballot_sync(kFull, in && id >= 0 && id < a.V));
+                        bad = bad || (in && (id < 0 || id >= a.V));
                         const bool owned = in && id >= lo && id < hi;
                         const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
                         const bool first = owned && (same & lanemask_lt()) == 0u;
                         const uint16_t h = owned ? buf[id - lo] : static_cast<uint16_t>(0);
                         const bool valid = first && h != kSentinel;
+                        dup = dup || (owned && !valid);
                         __syncwarp();
                         if (valid) {
                             buf[id - lo] = kSentinel;
                             m_loc = fmaxf(m_loc, bf_to_f(h));
-                        }
-                        if (owned) {
-                            const uint32_t fz = __float_as_uint(bf_to_f(h));
-                            const uint32_t fl = valid ? 1u : 2u;
-                            for (int r = 0; r < C; ++r)
-                                st_async_v2(map_to_rank(xh_s + 8u * k, r), fz, fl, map_to_rank(xb, r));
                         }
                         const unsigned vm = __ballot_sync(kFull, valid);
                         if (valid) {
                             const int pos = nfix + __popc(vm & lanemask_lt());
                             fix_i[pos] = id - lo;
                             fix_k[pos] = k;
+                            fix_z[pos] = bf_to_f(h);
                         }
                         nfix += __popc(vm);
                         a_in_h = a_in_h || __any_sync(kFull, valid && id == sa);
@@ -371,13 +445,14 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                         if (lane == 0) {
                             fix_i[nfix] = sa - lo;
                             fix_k[nfix] = -1;
+                            fix_z[nfix] = zav;
                         }
                         nfix += 1;
                     }
-                    // bytes this CTA receives this row: one 8-byte entry per in-range
-                    // recorded id, one 16-byte partial per CTA, and z_a
-                    if (lane == 0)
-                        mbar_expect_tx(xb, static_cast<uint32_t>(8 * n_inrange + 16 * C + 8));
+                    own_flags = (__any_sync(kFull, dup) ? SC_FLAG_DUP_ID : 0u) |
+                                (crank == 0 && __any_sync(kFull, bad) ? SC_FLAG_BAD_ID : 0u);
+                    // bytes this CTA receives for the row: one record from every CTA
+                    if (lane == 0) mbar_expect_tx(xb, static_cast<uint32_t>(sizeof(Partial)) * C);
                     __syncwarp();
                     for (int e = lane; e < nfix; e += 32) {
                         const int li = fix_i[e];
@@ -389,10 +464,11 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 uint32_t mx2 = 0xFF80FF80u;  // (-inf, -inf)
                 for (int i = 0; i < nchunks && !timed_out; ++i) {
                     const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                    if (!mbar_wait_bounded(bar_addr(st, i), fpar, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(bar_addr(st, kChunkFull + i), fpar, kWaitLimitNs)) {
                         timed_out = true;
                         break;
                     }
+#pragma unroll 4
                     for (int j = v0 + tid - 32; j < v1; j += NC - 32) {
                         const uint4 w = lds128(buf_s + 16u * j);
                         mx2 = bmax2(mx2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
@@ -410,10 +486,65 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
             m_loc = red[0];
 #pragma unroll
             for (int w = 1; w < NCW; ++w) m_loc = fmaxf(m_loc, red[w]);
-
-            // ---- 2. exp pass over the unrecorded entries ----------------------
             const float o_c = m_loc * kscale;
-            float s1 = 0.0f, s2 = 0.0f;
+
+            // ---- 2. owned recorded ids (warp 0), then the exp pass (all) --------
+            if (warp == 0) {
+                float lH = 0.0f, EH = 0.0f, QY = 0.0f, ya = 0.0f;
+                int nval = 0, has_a = 0;
+                HeadMass hm{-INFINITY, 0x7FFFFFFF, 0.0f, 0.0f};
+                for (int e = lane; e < nfix; e += 32) {
+                    const int k = fix_k[e];
+                    const float y = fmaf(fix_z[e], kscale, -o_c);
+                    if (k < 0) {  // the sampled token, outside the head
+                        ya = y;
+                        has_a = 1;
+                        continue;
+                    }
+                    if (ids_s[k] == sa) {
+                        ya = y;
+                        has_a = 1;
+                    }
+                    const float ev = ex2(y);
+                    lH += ev;
+                    EH = fmaf(ev, y, EH);
+                    const float lp = lps_s[k];
+                    QY = fmaf(expf(lp), y, QY);
+                    ++nval;
+                    HeadMass one{lp, k, 0.0f, 0.0f};
+                    hm = head_merge(hm, one);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    lH += __shfl_xor_sync(kFull, lH, off);
+                    EH += __shfl_xor_sync(kFull, EH, off);
+                    QY += __shfl_xor_sync(kFull, QY, off);
+                    nval += __shfl_xor_sync(kFull, nval, off);
+                    hm = head_merge(hm, head_shfl(hm, off));
+                }
+                const unsigned am = __ballot_sync(kFull, has_a != 0);
+                if (am) ya = __shfl_sync(kFull, ya, __ffs(am) - 1);
+                if (lane == 0) {
+                    Partial& p = *mine;
+                    p.m = m_loc;
+                    p.rs = rs_prev;
+                    p.lH = lH;
+                    p.EH = EH;
+                    p.QY = QY;
+                    p.qo_hi = hm.oh;
+                    p.qo_lo = hm.ol;
+                    p.lpmax = hm.lp;
+                    p.kbest = hm.k;
+                    p.nval = nval;
+                    p.flags = own_flags;
+                    p.ya = ya;
+                    p.has_a = am ? 1 : 0;
+                    p.pad = 0;
+                }
+            }
+            // four independent accumulator pairs keep the FADD/FFMA chains short
+            float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 2
             for (int j = tid; j < nv; j += NC) {
                 const uint4 w = lds128(buf_s + 16u * j);
                 const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
@@ -422,17 +553,17 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     const float y0 = fmaf(bf_lo(ww[q]), kscale, -o_c);
                     const float y1 = fmaf(bf_hi(ww[q]), kscale, -o_c);
                     const float e0 = ex2(y0), e1 = ex2(y1);
-                    s1 += e0;
-                    s1 += e1;
-                    s2 = fmaf(e0, y0, s2);
-                    s2 = fmaf(e1, y1, s2);
+                    s1[q] += e0 + e1;
+                    s2[q] = fmaf(e0, y0, fmaf(e1, y1, s2[q]));
                 }
             }
-            s1 = warp_sum(s1);
-            s2 = warp_sum(s2);
+            float s1t = (s1[0] + s1[1]) + (s1[2] + s1[3]);
+            float s2t = (s2[0] + s2[1]) + (s2[2] + s2[3]);
+            s1t = warp_sum(s1t);
+            s2t = warp_sum(s2t);
             if (lane == 0) {
-                red[NCW + warp] = s1;
-                red[2 * NCW + warp] = s2;
+                red[NCW + warp] = s1t;
+                red[2 * NCW + warp] = s2t;
             }
             named_bar(NC);
 
@@ -444,10 +575,19 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                         S1 += red[NCW + w];
                         S2 += red[2 * NCW + w];
                     }
-                    const uint32_t ps = smem_addr(part + static_cast<int>(par) * kMaxCluster + crank);
-                    for (int r = 0; r < C; ++r)
-                        st_async_v4(map_to_rank(ps, r), __float_as_uint(m_loc), __float_as_uint(S1),
-                                    __float_as_uint(S2), __float_as_uint(rs_prev), map_to_rank(xb, r));
+                    mine->S1 = S1;
+                    mine->S2 = S2;
+                }
+                __syncwarp();
+                if (lane < C) {  // lane r sends this CTA's record to CTA r
+                    const uint32_t src = smem_addr(mine);
+                    const uint32_t dst = map_to_rank(smem_addr(part + static_cast<int>(par) * kMaxCluster + crank), lane);
+                    const uint32_t rb = map_to_rank(xb, lane);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = lds128(src + 16u * q);
+                        st_async_v4(dst + 16u * q, v.x, v.y, v.z, v.w, rb);
+                    }
                 }
                 const bool ok = mbar_wait_cluster_bounded(xb, xph, kWaitLimitNs);
                 if (!__all_sync(kFull, ok)) {
@@ -456,101 +596,69 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                         scal_i[4] = 1;
                     }
                 } else {
-                    const float4* pp = part + static_cast<int>(par) * kMaxCluster;
-                    float mg = -INFINITY;
-                    for (int r = 0; r < C; ++r) mg = fmaxf(mg, pp[r].x);
+                    // lane r < C holds CTA r's record; the others hold neutral values
+                    const Partial* pp = part + static_cast<int>(par) * kMaxCluster;
+                    Partial P;
+                    if (lane < C) {
+                        P = pp[lane];
+                    } else {
+                        memset(&P, 0, sizeof P);
+                        P.m = -INFINITY;
+                        P.lpmax = -INFINITY;
+                        P.kbest = 0x7FFFFFFF;
+                    }
+                    const float mg = warp_max(P.m);
                     const float o = mg * kscale;
-                    float lT = 0.0f, ET = 0.0f;
-                    for (int r = 0; r < C; ++r) {
-                        const float4 pr = pp[r];
-                        if (pr.y > 0.0f) {
-                            const float d = pr.x * kscale - o;
-                            const float f = ex2(d);
-                            lT += pr.y * f;
-                            ET += f * (pr.z + d * pr.y);
-                        }
+                    const bool live = P.m > -INFINITY;
+                    const float d = live ? P.m * kscale - o : 0.0f;
+                    const float f = live ? ex2(d) : 0.0f;
+                    float lT = f * P.S1;
+                    float ET = f * fmaf(d, P.S1, P.S2);
+                    float lH = f * P.lH;
+                    float EH = f * fmaf(d, P.lH, P.EH);
+                    float QYg = 0.0f, Qc = 0.0f;
+                    if (P.nval > 0) {
+                        Qc = (expf(P.lpmax) + P.qo_hi) + P.qo_lo;
+                        QYg = fmaf(d, Qc, P.QY);
                     }
-                    const float2* xr = xh + static_cast<int>(par) * K_max;
-                    float lH = 0.0f, EH = 0.0f, lp_best = -INFINITY;
-                    int nval = 0, k_best = 0x7FFFFFFF;
-                    uint32_t kfl = 0;
-                    for (int k = lane; k < cnt; k += 32) {
-                        const int id = ids_s[k];
-                        if (id < 0 || id >= a.V) {
-                            kfl |= SC_FLAG_BAD_ID;
-                            continue;
-                        }
-                        const float2 x = xr[k];
-                        if (__float_as_uint(x.y) != 1u) {
-                            kfl |= SC_FLAG_DUP_ID;
-                            continue;
-                        }
-                        const float y = fmaf(x.x, kscale, -o);
-                        const float e = ex2(y);
-                        lH += e;
-                        EH = fmaf(e, y, EH);
-                        ++nval;
-                        const float lp = lps_s[k];
-                        if (lp > lp_best) {
-                            lp_best = lp;
-                            k_best = k;
-                        }
-                    }
+                    float ya = P.has_a ? P.ya + d : 0.0f;
+                    int nval = P.nval;
+                    uint32_t flags = P.flags;
+                    HeadMass hm{P.lpmax, P.kbest, P.qo_hi, P.qo_lo};
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) {
+                        lT += __shfl_xor_sync(kFull, lT, off);
+                        ET += __shfl_xor_sync(kFull, ET, off);
                         lH += __shfl_xor_sync(kFull, lH, off);
                         EH += __shfl_xor_sync(kFull, EH, off);
+                        QYg += __shfl_xor_sync(kFull, QYg, off);
+                        ya += __shfl_xor_sync(kFull, ya, off);
                         nval += __shfl_xor_sync(kFull, nval, off);
-                        kfl |= __shfl_xor_sync(kFull, kfl, off);
-                        const float ol = __shfl_xor_sync(kFull, lp_best, off);
-                        const int ok2 = __shfl_xor_sync(kFull, k_best, off);
-                        if (ol > lp_best || (ol == lp_best && ok2 < k_best)) {
-                            lp_best = ol;
-                            k_best = ok2;
-                        }
+                        flags |= __shfl_xor_sync(kFull, flags, off);
+                        hm = head_merge(hm, head_shfl(hm, off));
                     }
-                    // 1 - Q_H without cancellation: -expm1(l_max) minus the other
-                    // recorded probabilities, summed error-free (two-sum) in FP32.
-                    float qh = 0.0f, ql = 0.0f;
-                    for (int k = lane; k < cnt; k += 32) {
-                        const int id = ids_s[k];
-                        if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u || k == k_best) continue;
-                        float sh, se;
-                        two_sum(qh, expf(lps_s[k]), sh, se);
-                        qh = sh;
-                        ql += se;
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        const float oh = __shfl_xor_sync(kFull, qh, off);
-                        const float ol = __shfl_xor_sync(kFull, ql, off);
-                        float sh, se;
-                        two_sum(qh, oh, sh, se);
-                        qh = sh;
-                        ql = ql + ol + se;
-                    }
+                    // 1 - Q_H without cancellation: -expm1(l_max) minus the others' mass
                     float tail_mu = 1.0f, Q_H = 0.0f;
                     if (nval > 0) {
-                        tail_mu = (-expm1f(lp_best) - qh) - ql;
-                        Q_H = (expf(lp_best) + qh) + ql;
+                        tail_mu = (-expm1f(hm.lp) - hm.oh) - hm.ol;
+                        Q_H = (expf(hm.lp) + hm.oh) + hm.ol;
                     }
                     const float l = lT + lH;
                     const float log2l = log2f(l);
                     const float P_H = lH / l;
                     const float tail_pi = lT / l;
                     const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
-                    uint32_t flags = m.rflags | kfl;
+                    flags |= m.rflags;
                     if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
                     if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
                     const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
                     const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
-                    const float ya = fmaf(za[par].x, kscale, -o);
                     const float logp_a = (ya - log2l) * kLn2;
                     float wt = 1.0f, k3 = 0.0f;
                     if (a.rollout) {
-                        const float d = logp_a - m.rl;
-                        k3 = expm1f(d) - d;
-                        const float w = expf(d);
+                        const float dd = logp_a - m.rl;
+                        k3 = expm1f(dd) - dd;
+                        const float w = expf(dd);
                         if (a.is_mode == SC_IS_TIS) {
                             if (w > a.tis_max) {
                                 wt = a.tis_max;
@@ -569,31 +677,27 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     }
                     const float A = m.A;
                     const float Aw = A * wt;
+                    // sum_H c log p = sum_H q log p - rho sum_H p log p, each from the
+                    // merged sums: log p_k = (y_k - log2 l) ln 2.
                     float csum = 0.0f;
-                    if (a.centering) {
-                        for (int k = lane; k < cnt; k += 32) {
-                            const int id = ids_s[k];
-                            if (id < 0 || id >= a.V || __float_as_uint(xr[k].y) != 1u) continue;
-                            const float lk = fmaf(xr[k].x, kscale, -o) - log2l;  // log2 p_k
-                            const float c = expf(lps_s[k]) - rho * ex2(lk);
-                            csum = fmaf(c, lk * kLn2, csum);
-                        }
-                        csum = warp_sum(csum);
+                    if (a.centering && nval > 0) {
+                        const float qlogp = kLn2 * fmaf(-log2l, Q_H, QYg);
+                        const float plogp = kLn2 * fmaf(-log2l, lH, EH) / l;
+                        csum = fmaf(-rho, plogp, qlogp);
                     }
                     const float loss = -Aw * (logp_a - csum);
                     const float entropy = kLn2 * (log2l - (ET + EH) / l);
                     const float alpha = -a.grad_scale * a.inv_t * Aw;
                     const float beta = -alpha * s;
-                    const int nfix = scal_i[3];
                     for (int e = lane; e < nfix; e += 32) {
                         const int k = fix_k[e];
+                        const float p = ex2(fmaf(fix_z[e], kscale, -o) - log2l);
                         float g;
                         if (k >= 0) {
-                            const float p = ex2(fmaf(xr[k].x, kscale, -o) - log2l);
                             const float mu = a.centering ? fmaf(dsr, p, expf(lps_s[k])) : p;
                             g = alpha * ((ids_s[k] == sa ? 1.0f : 0.0f) - mu);
                         } else {
-                            g = alpha * (1.0f - s * ex2(ya - log2l));
+                            g = alpha * (1.0f - s * p);
                         }
                         fix_v[e] = g;
                     }
@@ -604,27 +708,27 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                         if (crank == 0) {
                             a.logp[t] = logp_a;
                             if (a.diag) {
-                                sc_row_diag d;
-                                d.loss = loss;
-                                d.logp_a = logp_a;
-                                d.P_H = P_H;
-                                d.tail_pi = tail_pi;
-                                d.Q_H = Q_H;
-                                d.tail_mu = tail_mu;
-                                d.rho = rho;
-                                d.s = s;
-                                d.entropy = entropy;
-                                d.k3 = k3;
-                                d.is_weight = wt;
-                                d.row_sum = 0.0f;
-                                d.adv = A;
-                                d.n_valid_k = nval;
-                                d.flags = flags;
-                                d.reserved = 0;
-                                a.diag[t] = d;
+                                sc_row_diag dg;
+                                dg.loss = loss;
+                                dg.logp_a = logp_a;
+                                dg.P_H = P_H;
+                                dg.tail_pi = tail_pi;
+                                dg.Q_H = Q_H;
+                                dg.tail_mu = tail_mu;
+                                dg.rho = rho;
+                                dg.s = s;
+                                dg.entropy = entropy;
+                                dg.k3 = k3;
+                                dg.is_weight = wt;
+                                dg.row_sum = 0.0f;
+                                dg.adv = A;
+                                dg.n_valid_k = nval;
+                                dg.flags = flags;
+                                dg.reserved = 0;
+                                a.diag[t] = dg;
                                 if (t_prev >= 0) {  // the previous row's sum rode in with this exchange
                                     float rsum = 0.0f;
-                                    for (int r = 0; r < C; ++r) rsum += pp[r].w;
+                                    for (int r = 0; r < C; ++r) rsum += pp[r].rs;
                                     a.diag[t_prev].row_sum = rsum;
                                 }
                             }
@@ -638,45 +742,52 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 aborted = true;
                 break;
             }
+            if (tid == 0) mbar_arrive(bar_addr(st, kMetaFree));  // metadata and ids are consumed
 
             // ---- 4. write pass: g = beta p, patched at recorded ids and a ----------
             const float bw = scal[0];
             const float beta = scal[1];
-            const int nfix = scal_i[3];
+            const int nfx = scal_i[3];
             uint16_t* grow = a.grad + t * a.gstride + lo;
             float rs = 0.0f;
-            for (int j = tid; j < nvb; j += NC) {
-                const uint4 w = lds128(buf_s + 16u * j);
-                float g[8];
-                g[0] = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
-                g[1] = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
-                g[2] = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
-                g[3] = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
-                g[4] = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
-                g[5] = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
-                g[6] = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
-                g[7] = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
-                const uint32_t word = bmp[j >> 5];  // same word for the whole warp
-                if (word != 0u && ((word >> (j & 31)) & 1u)) {
-                    for (int e = 0; e < nfix; ++e) {
-                        const int li = fix_i[e];
-                        if ((li >> 3) == j) {
-                            const float v = fix_v[e];
+            for (int i = 0; i < nchunks; ++i) {
+                const int v1 = min((i + 1) * a.ncv, nvb);
+#pragma unroll 2
+                for (int j = i * a.ncv + tid; j < v1; j += NC) {
+                    const uint4 w = lds128(buf_s + 16u * j);
+                    float g[8];
+                    g[0] = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
+                    g[1] = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
+                    g[2] = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
+                    g[3] = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
+                    g[4] = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
+                    g[5] = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
+                    g[6] = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
+                    g[7] = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
+                    const uint32_t word = bmp[j >> 5];  // same word for the whole warp
+                    if (word != 0u && ((word >> (j & 31)) & 1u)) {
+                        for (int e = 0; e < nfx; ++e) {
+                            const int li = fix_i[e];
+                            if ((li >> 3) == j) {
+                                const float v = fix_v[e];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                if ((li & 7) == q) g[q] = v;
+                                for (int q = 0; q < 8; ++q)
+                                    if ((li & 7) == q) g[q] = v;
+                            }
                         }
                     }
+                    rs += ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
+                    st_global_v4_hint(grow + 8 * j, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
+                                      pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]), pol);
                 }
-                rs += ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
-                st_global_v4_hint(grow + 8 * j, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
-                                  pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]), pol);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_addr(st, kChunkFree + i));  // slot i may be refilled
             }
             if (tail && tid == 0) {
                 for (int q = 0; q < tail; ++q) {
                     const int li = n8 + q;
                     float g = beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
-                    for (int e = 0; e < nfix; ++e)
+                    for (int e = 0; e < nfx; ++e)
                         if (fix_i[e] == li) g = fix_v[e];
                     rs += g;
                     grow[li] = f_to_bf_bits(g);
@@ -689,10 +800,10 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 float tot = 0.0f;
                 for (int w = 0; w < NCW; ++w) tot += red[3 * NCW + w];
                 rs_prev = tot;
-                mbar_arrive(bar_addr(st, kMaxChunks + 1));  // stage free for the producer
+                mbar_arrive(bar_addr(st, kRowDone));  // tail entries and the stage are free
             }
             if (warp == 0)
-                for (int e = lane; e < nfix; e += 32) bmp[fix_i[e] >> 8] = 0u;
+                for (int e = lane; e < nfx; e += 32) bmp[fix_i[e] >> 8] = 0u;
             t_prev = t;
             ++nproc;
         }
@@ -737,12 +848,12 @@ Layout make_layout(int S, int K_max, int NC, int NB) {
     L.off_lps = take(NB * K_max * 4);
     L.off_meta = take(NB * static_cast<int>(sizeof(RowMeta)));
     L.off_bars = take((kMaxStages * kBarsPerStage + 2) * 8);
-    L.off_part = take(2 * kMaxCluster * 16);
+    L.off_part = take(2 * kMaxCluster * 64);
+    L.off_mine = take(64);
     L.off_frs = take(kMaxCluster * 8);
-    L.off_za = take(2 * 8);
-    L.off_xh = take(2 * K_max * 8);
     L.off_fixi = take((K_max + 1) * 4);
     L.off_fixk = take((K_max + 1) * 4);
+    L.off_fixz = take((K_max + 1) * 4);
     L.off_fixv = take((K_max + 1) * 4);
     L.off_bmp = take(((S / 8 + 31) / 32) * 4);
     L.off_red = take(4 * (NC / 32) * 4);
@@ -751,16 +862,16 @@ Layout make_layout(int S, int K_max, int NC, int NB) {
     return L;
 }
 
-// Automatic plan: a vocabulary slice of at most ~19 KiB per CTA (clusters of
-// up to 16 CTAs), two pipeline stages, 256 consumer threads.  For the
-// 151936-entry vocabulary this is 16 CTAs x 9496 entries and about 45 KB of
-// shared memory per CTA.
+// Automatic plan: about 40 KiB of logits per CTA (clusters of up to 16
+// CTAs), one pipeline stage (more resident CTAs beat deeper prefetch on
+// GB300, measured), 128 compute threads up to ~20k entries per slice.  For the
+// 151936-entry vocabulary: 8 CTAs x 18992 entries, ~44 KB of shared memory.
 int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
-    const int NB = req_stages > 0 ? req_stages : 2;
+    const int NB = req_stages > 0 ? req_stages : 1;
     int C = req_cluster;
-    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 2048 ? 256 : 128); };
+    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S > 20480 ? 256 : 128); };
     if (C <= 0) {
-        C = static_cast<int>((2LL * V + 19455) / 19456);
+        C = static_cast<int>((2LL * V + 40959) / 40960);
         C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
         while (C > 1 && static_cast<long long>(C - 1) * round_up((V + C - 1) / C, 8) >= V) --C;
     }
@@ -778,8 +889,9 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
     out->NC = NC;
     out->S = S;
     out->NB = NB;
-    out->ncv = (nvb + nch - 1) / nch;
-    if (out->ncv < 1) out->ncv = 1;
+    // a whole number of 32-vector groups per chunk keeps each warp's bitmap word uniform
+    out->ncv = round_up((nvb + nch - 1) / nch, 32);
+    if (out->ncv < 32) out->ncv = 32;
     out->L = L;
     return SC_OK;
 }
