@@ -321,35 +321,57 @@ def main():
     value = float(tok.item()) / (elapsed_ms / 1e3)
 
     # ---- end to end: pinned host buffers in, outputs back, every step --------
+    # Two device buffer sets: step i+1's inputs copy in (copy stream) while
+    # step i computes and copies its gradient, log p_a and diagnostics out
+    # (compute stream), so the two copy directions overlap.
     host_in = {k: batch[k].cpu().pin_memory() for k in
                ["logits", "rec_ids", "rec_logprobs", "sampled", "rollout_logprob", "row_response", "rewards"]}
     host_grad = torch.empty((T, V), dtype=torch.bfloat16).pin_memory()
     host_logp = torch.empty(T, dtype=torch.float32).pin_memory()
     host_diag = torch.empty((T, 16), dtype=torch.int32).pin_memory()
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    del grad
+    torch.cuda.empty_cache()
+    sets = []
+    for _ in range(2):
+        sets.append(dict(inp={k: torch.empty_like(v, device=dev) for k, v in host_in.items()},
+                         grad=torch.empty((T, V), dtype=torch.bfloat16, device=dev),
+                         logp=torch.empty(T, dtype=torch.float32, device=dev),
+                         diag=torch.empty((T, 16), dtype=torch.int32, device=dev),
+                         adv=torch.empty_like(batch["rewards"]),
+                         loaded=torch.cuda.Event(), done=torch.cuda.Event()))
+    copy_stream = torch.cuda.Stream(device=dev)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in (host_grad, host_logp, host_diag))
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for k, v in host_in.items():
-                dev_in[k].copy_(v, non_blocking=True)
-            sc.sc_group_advantages(dev_in["rewards"], batch["n_groups"], batch["group_size"], out=adv, stream=stream)
-            sc.sc_center_forward_backward(dev_in["logits"], dev_in["rec_ids"], dev_in["rec_logprobs"], None,
-                                          dev_in["sampled"], dev_in["rollout_logprob"], dev_in["row_response"],
-                                          adv, p, grad_out=grad, logp_out=logp, diag_out=diag, stream=stream)
-            host_grad.copy_(grad, non_blocking=True)
-            host_logp.copy_(logp, non_blocking=True)
-            host_diag.copy_(diag, non_blocking=True)
+    def e2e_run(n):
+        for i in range(n):
+            bs = sets[i % 2]
+            copy_stream.wait_event(bs["done"])  # the set's previous step has finished with it
+            with torch.cuda.stream(copy_stream):
+                for k, v in host_in.items():
+                    bs["inp"][k].copy_(v, non_blocking=True)
+                bs["loaded"].record(copy_stream)
+            stream.wait_event(bs["loaded"])
+            with torch.cuda.stream(stream):
+                x = bs["inp"]
+                sc.sc_group_advantages(x["rewards"], batch["n_groups"], batch["group_size"], out=bs["adv"],
+                                       stream=stream)
+                sc.sc_center_forward_backward(x["logits"], x["rec_ids"], x["rec_logprobs"], None, x["sampled"],
+                                              x["rollout_logprob"], x["row_response"], bs["adv"], p,
+                                              grad_out=bs["grad"], logp_out=bs["logp"], diag_out=bs["diag"],
+                                              stream=stream)
+                host_grad.copy_(bs["grad"], non_blocking=True)
+                host_logp.copy_(bs["logp"], non_blocking=True)
+                host_diag.copy_(bs["diag"], non_blocking=True)
+                bs["done"].record(stream)
 
-    for _ in range(3):
-        e2e_step()
+    e2e_run(3)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    copy_stream.wait_event(e0)
+    e2e_run(args.e2e_steps)
+    e1.record(stream)  # the compute stream's last step waited for every copy-in
     barrier()
     e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
     if world > 1:

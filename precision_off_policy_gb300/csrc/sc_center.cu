@@ -10,34 +10,35 @@
 // plus log p_a and per-row diagnostics (the section's K3, entropy, masses).
 //
 // GB300 design.  One row is shared by a cluster of C CTAs; CTA r owns the
-// vocabulary slice [r*S, min((r+1)*S, V)).  Each CTA is warp-specialised:
+// vocabulary slice [r*S, min((r+1)*S, V)).  Each CTA is warp-specialised.
 //
-// * a producer warp walks the cluster's rows, writes padding and error rows
-//   (zero gradient) itself, and for every valid row claims a pipeline stage,
-//   fetches the row's metadata (recorded ids and log-probabilities, count,
-//   rollout log-probability, advantage) and starts 1-D bulk copies (TMA
-//   engine) of the CTA's logit slice into that stage's shared memory, in
-//   chunks that each complete on their own mbarrier.  With two or more
-//   stages the next row streams in while the current one is computed.
-// * consumer warps, per valid row:
+// * The producer warp walks the cluster's rows ahead of the consumers.  Per
+//   row it fills a slot of a small metadata ring: the row's scalars and, for
+//   valid rows, the compact list of recorded ids that fall in this CTA's
+//   slice (repeats dropped, q = exp(logprob) precomputed) with a bitmap of the
+//   16-byte vectors that hold them.  It then starts 1-D bulk copies (TMA
+//   engine) of the logit slice into the data stage, 4 KiB chunk by chunk, each
+//   as soon as the previous row's write pass has released that chunk.
+// * The consumer warps, per row of the ring:
+//   0. padding / error rows: write the zero gradient slice and move on;
 //   1. max pass on packed bf16 pairs as chunks land, while consumer warp 0
-//      gathers the recorded ids that fall in the slice, drops repeats and
-//      overwrites them in shared memory with -2^100 (the max is exact either
-//      way, because warp 0 contributes the values it overwrites);
-//   2. warp 0 reduces the recorded ids it owns (mass, entropy term, sum of
+//      reads the owned recorded ids' logits and overwrites them in shared
+//      memory with -2^100 (the max is exact either way: warp 0 contributes
+//      the values it overwrites);
+//   2. warp 0 reduces the owned recorded ids (mass, entropy term, sum of
 //      q y, the recorded mass as an error-free FP32 pair with its largest
-//      term apart); all warps run the exp pass over the slice, so that the
-//      unrecorded mass sum_{v not in H} e^{x_v - m} accumulates directly (no
-//      1 - P_H cancellation), with the entropy term;
+//      term apart) while all warps run the exp pass: the unrecorded mass
+//      sum_{v not in H} e^{x_v - m} accumulates directly (no 1 - P_H
+//      cancellation), with the entropy term;
 //   3. exchange: each CTA sends one 64-byte record to every CTA of the
-//      cluster with st.async stores that complete as transaction bytes on
-//      the receiver's mbarrier (one expect_tx per CTA and row); warp 0 then
-//      merges the C records into the row scalars (LSE, P_H, Q_H, rho, s,
-//      loss, k3, importance weight), redundantly in every CTA, in O(C);
+//      cluster with st.async stores that complete as transaction bytes on the
+//      receiver's mbarrier; warp 0 merges the C records into the row scalars
+//      (LSE, P_H, Q_H, rho, s, loss, k3, importance weight) in O(C), the same
+//      way in every CTA;
 //   4. write pass: p_v is recomputed from shared memory and g_v = beta p_v
 //      streams to global memory with 16-byte stores and an evict-first L2
 //      hint; the <= K+1 special entries (recorded ids and the sampled token)
-//      are patched in registers via a per-vector bitmap.
+//      are patched in registers via the per-vector bitmap.
 // Every logit is read from HBM once and every gradient written once.  The
 // grid is persistent (as many clusters as fit).  Every wait is bounded
 // (about 1 s) and reports through the status word.
@@ -55,7 +56,8 @@ namespace {
 
 constexpr int kMaxCluster = 16;
 constexpr int kMaxChunks = 16;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 4;             // data stages
+constexpr int kMaxMeta = kMaxStages + 1;  // metadata ring slots
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;          // 227 KiB of dynamic shared memory per CTA
@@ -67,18 +69,44 @@ constexpr float kTailFloor = 1e-6f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-// Per-stage row description written by the producer warp.
+// One row as the producer hands it to the consumers.
 struct RowMeta {
-    long long t;  // row index; -1 ends the consumers' loop
-    int resp, sa, cnt;
-    uint32_t rflags;
-    float A, rl;
+    long long t;      // row index; -1 ends the consumers' loop
+    uint32_t zflags;  // nonzero: padding or error row (zero gradient)
+    int sa;           // sampled id
+    int nown;         // recorded ids of this CTA's slice in the compact list
+    int a_li;         // local index of a in this slice, -1 if another CTA owns it
+    uint32_t flags;   // row flags found by the producer (count, repeats, out of range)
+    float A, rl;      // advantage, rollout logprob
+    int pad[3];
 };
+static_assert(sizeof(RowMeta) == 48, "RowMeta layout");
+
+// One CTA's contribution to a row, exchanged across the cluster (64 bytes).
+// y' values are relative to this CTA's own slice maximum m (y' = (z - m) kscale).
+struct Partial {
+    float m;            // slice maximum of z (-inf for an empty slice)
+    float S1, S2;       // unrecorded entries: sum 2^y', sum 2^y' y'
+    float rs;           // FP32 gradient sum of this slice for the previous valid row
+    float lH, EH;       // recorded ids owned here: sum 2^y', sum 2^y' y'
+    float QY;           // sum q_k y'_k over the owned recorded ids
+    float qo_hi, qo_lo; // sum of q_k over them except the largest one (double-float)
+    float qbest;        // the largest q_k owned here (0 if none)
+    int kbest;          // its position k (INT_MAX if none)
+    int nval;           // owned recorded ids used
+    uint32_t flags;     // row flags found by this CTA's producer
+    float ya;           // y' of the sampled token, if this CTA owns it
+    int has_a;
+    float omq;          // 1 - qbest, from its log-probability (-expm1)
+};
+static_assert(sizeof(Partial) == 64, "partial record is 64 bytes");
 
 struct Layout {
-    int stage_bytes;  // bytes of one stage's logit slice (128-aligned)
-    int off_ids, off_lps, off_meta, off_bars, off_part, off_mine, off_frs, off_fixi, off_fixk, off_fixz,
-        off_fixv, off_bmp, off_red, off_scal, total;
+    int stage_bytes;  // bytes of one data stage (128-aligned)
+    int list_cap;     // entries of one owned list (K_max)
+    int nwords;       // bitmap words of one slice
+    int off_meta, off_list_li, off_list_lp, off_list_k, off_bitmap, off_bars, off_part, off_mine, off_frs,
+        off_fixz, off_fixv, off_red, off_scal, total;
 };
 
 struct KArgs {
@@ -98,7 +126,7 @@ struct KArgs {
     int V, K_max, n_resp;
     int is_mode, centering;
     float tis_max, mis_min, mis_max, inv_t, grad_scale;
-    int C, S, ncv, NB;
+    int C, S, ncv, NB, MS;
     Layout L;
 };
 
@@ -119,122 +147,110 @@ __device__ __forceinline__ void status_or(uint32_t* st, uint32_t bits) {
     if (st) atomicOr(st, bits);
 }
 
-// Barriers of one pipeline stage.  A stage's chunk slots are recycled one by
-// one: the write pass releases chunk i (kChunkFree + i) as soon as every
-// consumer warp is done with it, and the producer starts the next row's copy
-// into that slot right away.
-constexpr int kChunkFull = 0;                  // [kMaxChunks] bulk copy landed (tx bytes)
-constexpr int kChunkFree = kMaxChunks;         // [kMaxChunks] consumer warps done with the chunk
-constexpr int kRowFull = 2 * kMaxChunks;       // producer: metadata, ids and tail written
-constexpr int kMetaFree = 2 * kMaxChunks + 1;  // consumers: metadata and ids no longer read
-constexpr int kRowDone = 2 * kMaxChunks + 2;   // consumers: the whole stage is free
-constexpr int kBarsPerStage = 2 * kMaxChunks + 3;
-
-// One CTA's contribution to a row, exchanged across the cluster (64 bytes).
-// y' values are relative to this CTA's own slice maximum m (y' = (z - m) kscale).
-struct Partial {
-    float m;            // slice maximum of z (-inf for an empty slice)
-    float S1, S2;       // unrecorded entries: sum 2^y', sum 2^y' y'
-    float rs;           // FP32 gradient sum of this slice for the previous valid row
-    float lH, EH;       // recorded ids owned here: sum 2^y', sum 2^y' y'
-    float QY;           // sum q_k y'_k over the owned recorded ids
-    float qo_hi, qo_lo; // sum of q_k over them except the largest one (double-float)
-    float lpmax;        // largest recorded log-probability owned here (-inf if none)
-    int kbest;          // its position k (INT_MAX if none)
-    int nval;           // owned recorded ids used
-    uint32_t flags;     // repeated ids (owner), ids out of range (CTA 0)
-    float ya;           // y' of the sampled token, if this CTA owns it
-    int has_a;
-    int pad;
-};
-static_assert(sizeof(Partial) == 64, "partial record is 64 bytes");
-
-// Largest recorded log-probability with the mass of the others, merged
+// Largest recorded probability with the mass of the others, merged
 // commutatively (ties go to the lower k) so a butterfly gives every lane the
 // same bits.  The others' mass is kept as an unevaluated FP32 pair.
 struct HeadMass {
-    float lp;
+    float q;
     int k;
+    float omq;  // 1 - q of the winner, accurate near q = 1
     float oh, ol;
 };
 __device__ __forceinline__ HeadMass head_merge(const HeadMass& a, const HeadMass& b) {
-    const bool b_wins = b.lp > a.lp || (b.lp == a.lp && b.k < a.k);
-    const HeadMass& w = b_wins ? b : a;
-    const HeadMass& l = b_wins ? a : b;
+    const bool b_wins = b.q > a.q || (b.q == a.q && b.k < a.k);
     HeadMass r;
-    r.lp = w.lp;
-    r.k = w.k;
+    r.q = b_wins ? b.q : a.q;
+    r.k = b_wins ? b.k : a.k;
+    r.omq = b_wins ? b.omq : a.omq;
+    const float lq = b_wins ? a.q : b.q;
     float s, e;
     two_sum(a.oh, b.oh, s, e);
-    float ol = (a.ol + b.ol) + e;
+    const float ol = (a.ol + b.ol) + e;
     float s2, e2;
-    two_sum(s, expf(l.lp), s2, e2);  // expf(-inf) = 0 for an empty side
+    two_sum(s, lq, s2, e2);
     r.oh = s2;
     r.ol = ol + e2;
     return r;
 }
 __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
     HeadMass o;
-    o.lp = __shfl_xor_sync(kFull, h.lp, off);
+    o.q = __shfl_xor_sync(kFull, h.q, off);
     o.k = __shfl_xor_sync(kFull, h.k, off);
+    o.omq = __shfl_xor_sync(kFull, h.omq, off);
     o.oh = __shfl_xor_sync(kFull, h.oh, off);
     o.ol = __shfl_xor_sync(kFull, h.ol, off);
     return o;
 }
 
+// Barriers.  Data stage d: kChunkFull + i (copy of chunk i landed, tx bytes),
+// kChunkFree + i (every consumer warp is done with chunk i).  Meta slot s:
+// kMetaFull (producer wrote it), kMetaFree (consumers are done with it).
+constexpr int kChunkFull = 0;
+constexpr int kChunkFree = kMaxChunks;
+constexpr int kBarsPerStage = 2 * kMaxChunks;
+constexpr int kMetaBase = kMaxStages * kBarsPerStage;
+constexpr int kMetaFull = 0;
+constexpr int kMetaFree = 1;
+constexpr int kXBase = kMetaBase + 2 * kMaxMeta;
+constexpr int kNumBars = kXBase + 2;
+
+// Resident CTAs per SM the register allocation must allow (shared memory
+// allows about this many at the automatic plan's slice sizes).
+constexpr int min_blocks(int NC) { return NC <= 128 ? 6 : (NC <= 256 ? 4 : (NC <= 384 ? 3 : 2)); }
+
 template <int NC>
-__global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NCW = NC / 32;  // consumer warps; warp NCW is the producer
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t crank = cluster_ctarank();
     const uint32_t cid = cluster_id_x();
     const uint32_t ncl = num_clusters_x();
-    const int C = a.C, K_max = a.K_max, NB = a.NB;
+    const int C = a.C, K_max = a.K_max, NB = a.NB, MS = a.MS;
     const Layout& L = a.L;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
-    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);      // [NB]
-    int* ids_all = reinterpret_cast<int*>(smem + L.off_ids);            // [NB][K_max]
-    float* lps_all = reinterpret_cast<float*>(smem + L.off_lps);        // [NB][K_max]
-    Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);      // [2][kMaxCluster]
-    Partial* mine = reinterpret_cast<Partial*>(smem + L.off_mine);      // staging of this CTA's record
-    float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);          // [kMaxCluster]
-    int* fix_i = reinterpret_cast<int*>(smem + L.off_fixi);             // [K_max + 1]
-    int* fix_k = reinterpret_cast<int*>(smem + L.off_fixk);             // [K_max + 1]
-    float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);         // [K_max + 1]
-    float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);         // [K_max + 1]
-    uint32_t* bmp = reinterpret_cast<uint32_t*>(smem + L.off_bmp);      // one bit per 8 entries
-    float* red = reinterpret_cast<float*>(smem + L.off_red);            // [4][NCW]
-    float* scal = reinterpret_cast<float*>(smem + L.off_scal);          // [8]
+    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);         // [MS]
+    int* list_li = reinterpret_cast<int*>(smem + L.off_list_li);           // [MS][list_cap]
+    float* list_lp = reinterpret_cast<float*>(smem + L.off_list_lp);       // [MS][list_cap]
+    int* list_k = reinterpret_cast<int*>(smem + L.off_list_k);             // [MS][list_cap]
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [MS][nwords]
+    Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [2][C]
+    Partial* mine = reinterpret_cast<Partial*>(smem + L.off_mine);         // staging of this CTA's record
+    float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);             // [kMaxCluster]
+    float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);            // [list_cap]
+    float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);            // [list_cap]
+    float* red = reinterpret_cast<float*>(smem + L.off_red);               // [4][NCW]
+    float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [8]
     int* scal_i = reinterpret_cast<int*>(scal);
-    auto bar_addr = [&](int stage, int i) { return smem_addr(&bars[stage * kBarsPerStage + i]); };
-    const uint32_t xbar0 = smem_addr(&bars[kMaxStages * kBarsPerStage]);
+    auto data_bar = [&](int d, int i) { return smem_addr(&bars[d * kBarsPerStage + i]); };
+    auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
+    const uint32_t xbar0 = smem_addr(&bars[kXBase]);
 
     const int lo = static_cast<int>(crank) * a.S;
     const int hi = min(lo + a.S, a.V);
     const int n = max(hi - lo, 0);
     const int n8 = n & ~7, nvb = n8 >> 3, tail = n - n8, nv = nvb + (tail ? 1 : 0);
     const int nchunks = (nvb + a.ncv - 1) / a.ncv;
-    const int nwords = (a.S / 8 + 31) / 32;
+    const int cap = L.list_cap, nwords = L.nwords;
     const float kscale = a.inv_t * kLog2e;
     const uint64_t pol = l2_policy_evict_first();
 
     if (tid == 0) {
-        for (int st = 0; st < NB; ++st) {
+        for (int d = 0; d < NB; ++d)
             for (int i = 0; i < kMaxChunks; ++i) {
-                mbar_init(bar_addr(st, kChunkFull + i), 1u);
-                mbar_init(bar_addr(st, kChunkFree + i), static_cast<uint32_t>(NCW));
+                mbar_init(data_bar(d, kChunkFull + i), 1u);
+                mbar_init(data_bar(d, kChunkFree + i), static_cast<uint32_t>(NCW));
             }
-            mbar_init(bar_addr(st, kRowFull), 1u);
-            mbar_init(bar_addr(st, kMetaFree), 1u);
-            mbar_init(bar_addr(st, kRowDone), 1u);
+        for (int s = 0; s < MS; ++s) {
+            mbar_init(meta_bar(s, kMetaFull), 1u);
+            mbar_init(meta_bar(s, kMetaFree), 1u);
         }
         mbar_init(xbar0, 1u);  // exchange: own expect_tx arrive + peers' st.async bytes
         mbar_init(xbar0 + 8, 1u);
         fence_mbar_init_cluster();
     }
-    for (int i = tid; i < nwords; i += NC + 32) bmp[i] = 0u;
+    for (int i = tid; i < MS * nwords; i += NC + 32) bitmap[i] = 0u;
     cluster_sync_all();  // every CTA's barriers exist before peers signal them
 
     long long t_last = -1;  // consumers: last valid row (for the final row sum)
@@ -243,7 +259,7 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
 
     if (warp == NCW) {
         // ================= producer warp =================
-        uint32_t nfill = 0;
+        uint32_t nmeta = 0, ndata = 0;
         bool stop = false;
         for (long long base = cid; base < a.T && !stop; base += 32LL * ncl) {
             const long long tl = base + static_cast<long long>(lane) * ncl;
@@ -268,63 +284,112 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 const uint32_t zfj = __shfl_sync(kFull, zf, j);
                 const int rj = __shfl_sync(kFull, resp_l, j);
                 const int sj = __shfl_sync(kFull, sa_l, j);
-                if (zfj) {  // padding or error row: zero gradient, no compute
-                    uint16_t* grow = a.grad + t * a.gstride + lo;
-                    for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
-                    if (lane < tail) grow[n8 + lane] = 0;
-                    if (crank == 0 && lane == 0) {
-                        a.logp[t] = 0.0f;
-                        if (a.diag) {
-                            sc_row_diag d;
-                            memset(&d, 0, sizeof d);
-                            d.flags = zfj;
-                            a.diag[t] = d;
-                        }
-                        if (zfj & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
-                    }
-                    continue;
-                }
-                const int st = static_cast<int>(nfill % NB);
-                const bool reuse = nfill >= static_cast<uint32_t>(NB);
-                const uint32_t epar = ((nfill / NB) - 1u) & 1u;  // phase of the stage's previous use
-                if (reuse && !mbar_wait_bounded(bar_addr(st, kMetaFree), epar, kWaitLimitNs)) {
+                const int ms = static_cast<int>(nmeta % MS);
+                if (nmeta >= static_cast<uint32_t>(MS) &&
+                    !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nmeta / MS) - 1u) & 1u, kWaitLimitNs)) {
                     if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                     stop = true;
                     break;
                 }
+                RowMeta* mt = meta + ms;
+                if (zfj) {  // padding or error row: the consumers write zeros
+                    if (lane == 0) {
+                        mt->t = t;
+                        mt->zflags = zfj;
+                        mt->sa = sj;
+                        mt->nown = 0;
+                        mt->a_li = -1;
+                        mt->flags = 0;
+                        mt->A = 0.0f;
+                        mt->rl = 0.0f;
+                        mbar_arrive(meta_bar(ms, kMetaFull));
+                    }
+                    ++nmeta;
+                    continue;
+                }
+                // ---- recorded ids of this slice: compact list, repeats dropped ----
+                // (row scalars loaded first so their latency overlaps the list)
+                const float row_A = __ldg(a.adv + rj);
+                const float row_rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
                 int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
-                uint32_t rflags = 0;
+                uint32_t flags = 0;
                 if (cnt < 0 || cnt > K_max) {
-                    rflags = SC_FLAG_BAD_COUNT;
+                    flags |= SC_FLAG_BAD_COUNT;
                     cnt = cnt < 0 ? 0 : K_max;
                 }
+                int* li_s = list_li + ms * cap;
+                float* lp_s = list_lp + ms * cap;
+                int* k_s = list_k + ms * cap;
+                uint32_t* bm = bitmap + ms * nwords;
+                for (int w = lane; w < nwords; w += 32) bm[w] = 0u;  // the slot's previous bits
+                __syncwarp();
                 const long long kb = t * static_cast<long long>(K_max);
-                int* ids_s = ids_all + st * K_max;
-                float* lps_s = lps_all + st * K_max;
-                for (int k = lane; k < cnt; k += 32) {
-                    ids_s[k] = __ldg(a.ids + kb + k);
-                    lps_s[k] = __ldg(a.lps + kb + k);
+                int nown = 0;
+                bool bad = false, dup = false;
+                for (int kb0 = 0; kb0 < cnt; kb0 += 128) {
+                    int idr[4];
+                    float lpr[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {  // four rounds of loads in flight together
+                        const int k = kb0 + 32 * r + lane;
+                        idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
+                        lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int k = kb0 + 32 * r + lane;
+                        const bool kin = k < cnt;
+                        const int id = idr[r];
+                        bad = bad || (kin && (id < 0 || id >= a.V));
+                        const bool owned = kin && id >= lo && id < hi;
+                        const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
+                        bool keep = owned && (same & lanemask_lt()) == 0u;
+                        if (keep)  // repeats of an earlier round
+                            for (int e = 0; e < nown; ++e)
+                                if (li_s[e] == id - lo) {
+                                    keep = false;
+                                    break;
+                                }
+                        dup = dup || (owned && !keep);
+                        const unsigned km = __ballot_sync(kFull, keep);
+                        if (keep) {
+                            const int pos = nown + __popc(km & lanemask_lt());
+                            li_s[pos] = id - lo;
+                            lp_s[pos] = lpr[r];
+                            k_s[pos] = k;
+                            atomicOr(&bm[(id - lo) >> 8], 1u << (((id - lo) >> 3) & 31));
+                        }
+                        nown += __popc(km);
+                        __syncwarp();
+                    }
                 }
-                uint16_t* bufst = reinterpret_cast<uint16_t*>(smem + st * L.stage_bytes);
-                const uint16_t* lrow = a.logits + t * a.lstride + lo;
+                if (__any_sync(kFull, dup)) flags |= SC_FLAG_DUP_ID;
+                if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
+                const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
                 if (lane == 0) {
-                    RowMeta m;
-                    m.t = t;
-                    m.resp = rj;
-                    m.sa = sj;
-                    m.cnt = cnt;
-                    m.rflags = rflags;
-                    m.A = __ldg(a.adv + rj);
-                    m.rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
-                    meta[st] = m;
-                    // chunk by chunk, as the previous row's write pass frees each slot
+                    if (a_li >= 0) atomicOr(&bm[a_li >> 8], 1u << ((a_li >> 3) & 31));
+                    mt->t = t;
+                    mt->zflags = 0;
+                    mt->sa = sj;
+                    mt->nown = nown;
+                    mt->a_li = a_li;
+                    mt->flags = flags;
+                    mt->A = row_A;
+                    mt->rl = row_rl;
+                }
+                // ---- logit slice: chunk by chunk as the stage's slots free up ----
+                if (lane == 0) {
+                    const int ds = static_cast<int>(ndata % NB);
+                    const bool reuse = ndata >= static_cast<uint32_t>(NB);
+                    const uint32_t fpar = ((ndata / NB) - 1u) & 1u;
+                    uint16_t* bufst = reinterpret_cast<uint16_t*>(smem + ds * L.stage_bytes);
+                    const uint16_t* lrow = a.logits + t * a.lstride + lo;
                     const uint32_t bs = smem_addr(bufst);
-                    for (int i = 0; i < nchunks && !stop; ++i) {
-                        if (reuse && !mbar_wait_bounded(bar_addr(st, kChunkFree + i), epar, kWaitLimitNs)) {
+                    for (int i = 0; i < nchunks; ++i) {
+                        if (reuse && !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
                             status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                            // the chunks already started must land before the CTA can leave
-                            for (int i2 = 0; i2 < i; ++i2)
-                                (void)mbar_wait_bounded(bar_addr(st, kChunkFull + i2), (nfill / NB) & 1u,
+                            for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
+                                (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (ndata / NB) & 1u,
                                                         kWaitLimitNs);
                             stop = true;
                             break;
@@ -332,33 +397,27 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                         fence_proxy_async_smem();
                         const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
                         const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                        mbar_expect_tx(bar_addr(st, kChunkFull + i), bytes);
-                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, bar_addr(st, kChunkFull + i), pol);
-                    }
-                    if (!stop && reuse && !mbar_wait_bounded(bar_addr(st, kRowDone), epar, kWaitLimitNs)) {
-                        status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                        stop = true;
+                        mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
+                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol);
                     }
                 }
                 stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
                 if (stop) break;
-                // the tail entries (past the last whole 16-byte vector) by plain loads,
-                // once the previous row is completely done with the stage
-                if (tail && lane < 8) bufst[n8 + lane] = lane < tail ? lrow[n8 + lane] : kSentinel;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_addr(st, kRowFull));  // release: meta, ids, tail
-                ++nfill;
+                if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
+                ++nmeta;
+                ++ndata;
             }
         }
         if (!stop) {  // end marker for the consumers
-            const int st = static_cast<int>(nfill % NB);
+            const int ms = static_cast<int>(nmeta % MS);
             bool ok = true;
-            if (nfill >= static_cast<uint32_t>(NB))
-                ok = mbar_wait_bounded(bar_addr(st, kRowDone), ((nfill / NB) - 1u) & 1u, kWaitLimitNs);
+            if (nmeta >= static_cast<uint32_t>(MS))
+                ok = mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nmeta / MS) - 1u) & 1u, kWaitLimitNs);
             if (ok) {
                 if (lane == 0) {
-                    meta[st].t = -1;
-                    mbar_arrive(bar_addr(st, kRowFull));
+                    meta[ms].t = -1;
+                    mbar_arrive(meta_bar(ms, kMetaFull));
                 }
             } else if (lane == 0) {
                 status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
@@ -366,105 +425,94 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
         }
         // copies still in flight land before the CTA can exit (bounded again)
         if (lane == 0) {
-            const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
-            for (uint32_t f = f0; f < nfill; ++f)
+            const uint32_t f0 = ndata > static_cast<uint32_t>(NB) ? ndata - NB : 0u;
+            for (uint32_t f = f0; f < ndata; ++f)
                 for (int i = 0; i < nchunks; ++i)
-                    (void)mbar_wait_bounded(bar_addr(f % NB, kChunkFull + i), (f / NB) & 1u, kWaitLimitNs);
+                    (void)mbar_wait_bounded(data_bar(f % NB, kChunkFull + i), (f / NB) & 1u, kWaitLimitNs);
         }
         __syncwarp();
     } else {
         // ================= consumer warps =================
-        uint32_t nproc = 0;
+        uint32_t nmeta = 0, ndata = 0;
         float rs_prev = 0.0f;
         long long t_prev = -1;
         for (;;) {
-            const int st = static_cast<int>(nproc % NB);
-            const uint32_t fpar = (nproc / NB) & 1u;
-            const bool got = mbar_wait_bounded(bar_addr(st, kRowFull), fpar, kWaitLimitNs);
+            const int ms = static_cast<int>(nmeta % MS);
+            const bool got = mbar_wait_bounded(meta_bar(ms, kMetaFull), (nmeta / MS) & 1u, kWaitLimitNs);
             if (named_bar_or(NC, !got)) {
                 if (tid == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                 aborted = true;
                 break;
             }
-            const RowMeta m = meta[st];
+            const RowMeta m = meta[ms];
             if (m.t < 0) break;
-            const uint32_t par = nproc & 1u;
-            const uint32_t xph = (nproc >> 1) & 1u;
-            const uint32_t xb = xbar0 + 8u * par;
-            uint16_t* buf = reinterpret_cast<uint16_t*>(smem + st * L.stage_bytes);
-            const uint32_t buf_s = smem_addr(buf);
-            const int* ids_s = ids_all + st * K_max;
-            const float* lps_s = lps_all + st * K_max;
-            const int cnt = m.cnt, sa = m.sa;
             const long long t = m.t;
+            uint16_t* grow = a.grad + t * a.gstride + lo;
+            if (m.zflags) {  // ---- padding or error row: zero gradient ----
+                for (int j = tid; j < nvb; j += NC) st_global_v4_hint(grow + 8 * j, 0u, 0u, 0u, 0u, pol);
+                if (tid < tail) grow[n8 + tid] = 0;
+                if (crank == 0 && tid == 0) {
+                    a.logp[t] = 0.0f;
+                    if (a.diag) {  // zeros and the flags, as four 16-byte stores
+                        float4* dp = reinterpret_cast<float4*>(a.diag + t);
+                        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        dp[0] = z4;
+                        dp[1] = z4;
+                        dp[2] = z4;
+                        dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(m.zflags), 0.0f);
+                    }
+                    if (m.zflags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+                }
+                named_bar(NC);  // every consumer is done with the slot
+                if (tid == 0) mbar_arrive(meta_bar(ms, kMetaFree));
+                ++nmeta;
+                continue;
+            }
+            const int ds = static_cast<int>(ndata % NB);
+            const uint32_t fpar = (ndata / NB) & 1u;
+            const uint32_t par = ndata & 1u;
+            const uint32_t xph = (ndata >> 1) & 1u;
+            const uint32_t xb = xbar0 + 8u * par;
+            uint16_t* buf = reinterpret_cast<uint16_t*>(smem + ds * L.stage_bytes);
+            const uint32_t buf_s = smem_addr(buf);
+            const int* li_s = list_li + ms * cap;
+            const float* lp_s = list_lp + ms * cap;
+            const int* k_s = list_k + ms * cap;
+            const uint32_t* bm = bitmap + ms * nwords;
+            const int nown = m.nown;
 
-            // ---- 1. max pass (warps 1..) and recorded-id gather (warp 0) ------
+            // ---- 1. max pass (warps 1..) and owned recorded ids (warp 0) -------
             float m_loc = -INFINITY;
             bool timed_out = false;
-            int nfix = 0;           // warp 0
-            uint32_t own_flags = 0; // warp 0
+            float zav = 0.0f;  // warp 0: z of the sampled token if owned here
             if (warp == 0) {
+                if (tail) {  // entries past the last whole vector, padded with the sentinel
+                    const uint16_t* lrow = a.logits + t * a.lstride + lo;
+                    if (lane < 8) buf[n8 + lane] = lane < tail ? lrow[n8 + lane] : kSentinel;
+                    __syncwarp();
+                }
                 for (int i = 0; i < nchunks && !timed_out; ++i)
-                    timed_out = !mbar_wait_bounded(bar_addr(st, kChunkFull + i), fpar, kWaitLimitNs);
+                    timed_out = !mbar_wait_bounded(data_bar(ds, kChunkFull + i), fpar, kWaitLimitNs);
                 timed_out = __any_sync(kFull, timed_out);
                 if (!timed_out) {
                     if (lane < tail) m_loc = bf_to_f(buf[n8 + lane]);
-                    const bool a_own = sa >= lo && sa < hi;
-                    float zav = 0.0f;
-                    if (a_own) zav = bf_to_f(buf[sa - lo]);  // before any entry is overwritten
+                    if (m.a_li >= 0) zav = bf_to_f(buf[m.a_li]);  // before any entry is overwritten
                     __syncwarp();
-                    bool a_in_h = false, dup = false, bad = false;
-                    for (int base = 0; base < cnt; base += 32) {
-                        const int k = base + lane;
-                        const bool in = k < cnt;
-                        const int id = in ? ids_s[k] : -1;
-                        bad = bad || (in && (id < 0 || id >= a.V));
-                        const bool owned = in && id >= lo && id < hi;
-                        const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
-                        const bool first = owned && (same & lanemask_lt()) == 0u;
-                        const uint16_t h = owned ? buf[id - lo] : static_cast<uint16_t>(0);
-                        const bool valid = first && h != kSentinel;
-                        dup = dup || (owned && !valid);
-                        __syncwarp();
-                        if (valid) {
-                            buf[id - lo] = kSentinel;
-                            m_loc = fmaxf(m_loc, bf_to_f(h));
-                        }
-                        const unsigned vm = __ballot_sync(kFull, valid);
-                        if (valid) {
-                            const int pos = nfix + __popc(vm & lanemask_lt());
-                            fix_i[pos] = id - lo;
-                            fix_k[pos] = k;
-                            fix_z[pos] = bf_to_f(h);
-                        }
-                        nfix += __popc(vm);
-                        a_in_h = a_in_h || __any_sync(kFull, valid && id == sa);
-                        __syncwarp();
+                    for (int e = lane; e < nown; e += 32) {
+                        const int li = li_s[e];
+                        const float z = bf_to_f(buf[li]);
+                        fix_z[e] = z;
+                        m_loc = fmaxf(m_loc, z);
+                        buf[li] = kSentinel;
                     }
-                    if (a_own && !a_in_h) {
-                        if (lane == 0) {
-                            fix_i[nfix] = sa - lo;
-                            fix_k[nfix] = -1;
-                            fix_z[nfix] = zav;
-                        }
-                        nfix += 1;
-                    }
-                    own_flags = (__any_sync(kFull, dup) ? SC_FLAG_DUP_ID : 0u) |
-                                (crank == 0 && __any_sync(kFull, bad) ? SC_FLAG_BAD_ID : 0u);
                     // bytes this CTA receives for the row: one record from every CTA
                     if (lane == 0) mbar_expect_tx(xb, static_cast<uint32_t>(sizeof(Partial)) * C);
-                    __syncwarp();
-                    for (int e = lane; e < nfix; e += 32) {
-                        const int li = fix_i[e];
-                        atomicOr(&bmp[li >> 8], 1u << ((li >> 3) & 31));
-                    }
-                    if (lane == 0) scal_i[3] = nfix;
                 }
             } else {
                 uint32_t mx2 = 0xFF80FF80u;  // (-inf, -inf)
                 for (int i = 0; i < nchunks && !timed_out; ++i) {
                     const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                    if (!mbar_wait_bounded(bar_addr(st, kChunkFull + i), fpar, kWaitLimitNs)) {
+                    if (!mbar_wait_bounded(data_bar(ds, kChunkFull + i), fpar, kWaitLimitNs)) {
                         timed_out = true;
                         break;
                     }
@@ -490,29 +538,19 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
 
             // ---- 2. owned recorded ids (warp 0), then the exp pass (all) --------
             if (warp == 0) {
-                float lH = 0.0f, EH = 0.0f, QY = 0.0f, ya = 0.0f;
-                int nval = 0, has_a = 0;
-                HeadMass hm{-INFINITY, 0x7FFFFFFF, 0.0f, 0.0f};
-                for (int e = lane; e < nfix; e += 32) {
-                    const int k = fix_k[e];
+                float lH = 0.0f, EH = 0.0f, QY = 0.0f;
+                int nval = 0;
+                HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};
+                for (int e = lane; e < nown; e += 32) {
                     const float y = fmaf(fix_z[e], kscale, -o_c);
-                    if (k < 0) {  // the sampled token, outside the head
-                        ya = y;
-                        has_a = 1;
-                        continue;
-                    }
-                    if (ids_s[k] == sa) {
-                        ya = y;
-                        has_a = 1;
-                    }
                     const float ev = ex2(y);
                     lH += ev;
                     EH = fmaf(ev, y, EH);
-                    const float lp = lps_s[k];
-                    QY = fmaf(expf(lp), y, QY);
+                    const float lp = lp_s[e];
+                    const float q = expf(lp);
+                    QY = fmaf(q, y, QY);
                     ++nval;
-                    HeadMass one{lp, k, 0.0f, 0.0f};
-                    hm = head_merge(hm, one);
+                    hm = head_merge(hm, HeadMass{q, k_s[e], -expm1f(lp), 0.0f, 0.0f});
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
@@ -522,8 +560,6 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     nval += __shfl_xor_sync(kFull, nval, off);
                     hm = head_merge(hm, head_shfl(hm, off));
                 }
-                const unsigned am = __ballot_sync(kFull, has_a != 0);
-                if (am) ya = __shfl_sync(kFull, ya, __ffs(am) - 1);
                 if (lane == 0) {
                     Partial& p = *mine;
                     p.m = m_loc;
@@ -533,32 +569,46 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     p.QY = QY;
                     p.qo_hi = hm.oh;
                     p.qo_lo = hm.ol;
-                    p.lpmax = hm.lp;
+                    p.qbest = hm.q;
                     p.kbest = hm.k;
                     p.nval = nval;
-                    p.flags = own_flags;
-                    p.ya = ya;
-                    p.has_a = am ? 1 : 0;
-                    p.pad = 0;
+                    p.flags = m.flags;
+                    p.ya = m.a_li >= 0 ? fmaf(zav, kscale, -o_c) : 0.0f;
+                    p.has_a = m.a_li >= 0 ? 1 : 0;
+                    p.omq = hm.omq;
                 }
             }
             // four independent accumulator pairs keep the FADD/FFMA chains short
-            float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float s1a = 0.0f, s1b = 0.0f, s1c = 0.0f, s1d = 0.0f;
+            float s2a = 0.0f, s2b = 0.0f, s2c = 0.0f, s2d = 0.0f;
 #pragma unroll 2
             for (int j = tid; j < nv; j += NC) {
                 const uint4 w = lds128(buf_s + 16u * j);
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float y0 = fmaf(bf_lo(ww[q]), kscale, -o_c);
-                    const float y1 = fmaf(bf_hi(ww[q]), kscale, -o_c);
-                    const float e0 = ex2(y0), e1 = ex2(y1);
-                    s1[q] += e0 + e1;
-                    s2[q] = fmaf(e0, y0, fmaf(e1, y1, s2[q]));
-                }
+                float y0 = fmaf(bf_lo(w.x), kscale, -o_c), y1 = fmaf(bf_hi(w.x), kscale, -o_c);
+                float e0 = ex2(y0), e1 = ex2(y1);
+                s1a += e0 + e1;
+                s2a = fmaf(e0, y0, fmaf(e1, y1, s2a));
+                y0 = fmaf(bf_lo(w.y), kscale, -o_c);
+                y1 = fmaf(bf_hi(w.y), kscale, -o_c);
+                e0 = ex2(y0);
+                e1 = ex2(y1);
+                s1b += e0 + e1;
+                s2b = fmaf(e0, y0, fmaf(e1, y1, s2b));
+                y0 = fmaf(bf_lo(w.z), kscale, -o_c);
+                y1 = fmaf(bf_hi(w.z), kscale, -o_c);
+                e0 = ex2(y0);
+                e1 = ex2(y1);
+                s1c += e0 + e1;
+                s2c = fmaf(e0, y0, fmaf(e1, y1, s2c));
+                y0 = fmaf(bf_lo(w.w), kscale, -o_c);
+                y1 = fmaf(bf_hi(w.w), kscale, -o_c);
+                e0 = ex2(y0);
+                e1 = ex2(y1);
+                s1d += e0 + e1;
+                s2d = fmaf(e0, y0, fmaf(e1, y1, s2d));
             }
-            float s1t = (s1[0] + s1[1]) + (s1[2] + s1[3]);
-            float s2t = (s2[0] + s2[1]) + (s2[2] + s2[3]);
+            float s1t = (s1a + s1b) + (s1c + s1d);
+            float s2t = (s2a + s2b) + (s2c + s2d);
             s1t = warp_sum(s1t);
             s2t = warp_sum(s2t);
             if (lane == 0) {
@@ -581,7 +631,7 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 __syncwarp();
                 if (lane < C) {  // lane r sends this CTA's record to CTA r
                     const uint32_t src = smem_addr(mine);
-                    const uint32_t dst = map_to_rank(smem_addr(part + static_cast<int>(par) * kMaxCluster + crank), lane);
+                    const uint32_t dst = map_to_rank(smem_addr(part + static_cast<int>(par) * C + crank), lane);
                     const uint32_t rb = map_to_rank(xb, lane);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -597,16 +647,30 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     }
                 } else {
                     // lane r < C holds CTA r's record; the others hold neutral values
-                    const Partial* pp = part + static_cast<int>(par) * kMaxCluster;
-                    Partial P;
-                    if (lane < C) {
-                        P = pp[lane];
-                    } else {
-                        memset(&P, 0, sizeof P);
-                        P.m = -INFINITY;
-                        P.lpmax = -INFINITY;
-                        P.kbest = 0x7FFFFFFF;
-                    }
+                    const Partial* pp = part + static_cast<int>(par) * C;
+                    const bool have = lane < C;
+                    const uint32_t pa = smem_addr(pp + (have ? lane : 0));
+                    const uint4 r0 = lds128(pa), r1 = lds128(pa + 16u), r2 = lds128(pa + 32u), r3 = lds128(pa + 48u);
+                    struct {
+                        float m, S1, S2, lH, EH, QY, qo_hi, qo_lo, qbest, ya, omq;
+                        int kbest, nval, has_a;
+                        uint32_t flags;
+                    } P;
+                    P.m = have ? __uint_as_float(r0.x) : -INFINITY;
+                    P.S1 = have ? __uint_as_float(r0.y) : 0.0f;
+                    P.S2 = have ? __uint_as_float(r0.z) : 0.0f;
+                    P.lH = have ? __uint_as_float(r1.x) : 0.0f;
+                    P.EH = have ? __uint_as_float(r1.y) : 0.0f;
+                    P.QY = have ? __uint_as_float(r1.z) : 0.0f;
+                    P.qo_hi = have ? __uint_as_float(r1.w) : 0.0f;
+                    P.qo_lo = have ? __uint_as_float(r2.x) : 0.0f;
+                    P.qbest = have ? __uint_as_float(r2.y) : 0.0f;
+                    P.kbest = have ? static_cast<int>(r2.z) : 0x7FFFFFFF;
+                    P.nval = have ? static_cast<int>(r2.w) : 0;
+                    P.flags = have ? r3.x : 0u;
+                    P.ya = have ? __uint_as_float(r3.y) : 0.0f;
+                    P.has_a = have ? static_cast<int>(r3.z) : 0;
+                    P.omq = have ? __uint_as_float(r3.w) : 1.0f;
                     const float mg = warp_max(P.m);
                     const float o = mg * kscale;
                     const bool live = P.m > -INFINITY;
@@ -616,15 +680,12 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     float ET = f * fmaf(d, P.S1, P.S2);
                     float lH = f * P.lH;
                     float EH = f * fmaf(d, P.lH, P.EH);
-                    float QYg = 0.0f, Qc = 0.0f;
-                    if (P.nval > 0) {
-                        Qc = (expf(P.lpmax) + P.qo_hi) + P.qo_lo;
-                        QYg = fmaf(d, Qc, P.QY);
-                    }
+                    float QYg = 0.0f;
+                    if (P.nval > 0) QYg = fmaf(d, (P.qbest + P.qo_hi) + P.qo_lo, P.QY);
                     float ya = P.has_a ? P.ya + d : 0.0f;
                     int nval = P.nval;
                     uint32_t flags = P.flags;
-                    HeadMass hm{P.lpmax, P.kbest, P.qo_hi, P.qo_lo};
+                    HeadMass hm{P.qbest, P.kbest, P.omq, P.qo_hi, P.qo_lo};
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) {
                         lT += __shfl_xor_sync(kFull, lT, off);
@@ -637,18 +698,18 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                         flags |= __shfl_xor_sync(kFull, flags, off);
                         hm = head_merge(hm, head_shfl(hm, off));
                     }
-                    // 1 - Q_H without cancellation: -expm1(l_max) minus the others' mass
+                    // 1 - Q_H without cancellation: (1 - q_max), taken from its
+                    // log-probability, minus the others' mass
                     float tail_mu = 1.0f, Q_H = 0.0f;
                     if (nval > 0) {
-                        tail_mu = (-expm1f(hm.lp) - hm.oh) - hm.ol;
-                        Q_H = (expf(hm.lp) + hm.oh) + hm.ol;
+                        tail_mu = (hm.omq - hm.oh) - hm.ol;
+                        Q_H = (hm.q + hm.oh) + hm.ol;
                     }
                     const float l = lT + lH;
                     const float log2l = log2f(l);
                     const float P_H = lH / l;
                     const float tail_pi = lT / l;
                     const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
-                    flags |= m.rflags;
                     if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
                     if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
                     const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
@@ -689,43 +750,24 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                     const float entropy = kLn2 * (log2l - (ET + EH) / l);
                     const float alpha = -a.grad_scale * a.inv_t * Aw;
                     const float beta = -alpha * s;
-                    for (int e = lane; e < nfix; e += 32) {
-                        const int k = fix_k[e];
+                    for (int e = lane; e < nown; e += 32) {  // gradient at the owned recorded ids
                         const float p = ex2(fmaf(fix_z[e], kscale, -o) - log2l);
-                        float g;
-                        if (k >= 0) {
-                            const float mu = a.centering ? fmaf(dsr, p, expf(lps_s[k])) : p;
-                            g = alpha * ((ids_s[k] == sa ? 1.0f : 0.0f) - mu);
-                        } else {
-                            g = alpha * (1.0f - s * p);
-                        }
-                        fix_v[e] = g;
+                        const float mu = a.centering ? fmaf(dsr, p, expf(lp_s[e])) : p;
+                        fix_v[e] = alpha * ((li_s[e] == m.a_li ? 1.0f : 0.0f) - mu);
                     }
                     if (lane == 0) {
                         scal[0] = o + log2l;
                         scal[1] = beta;
+                        scal[2] = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
                         scal_i[4] = 0;
                         if (crank == 0) {
                             a.logp[t] = logp_a;
-                            if (a.diag) {
-                                sc_row_diag dg;
-                                dg.loss = loss;
-                                dg.logp_a = logp_a;
-                                dg.P_H = P_H;
-                                dg.tail_pi = tail_pi;
-                                dg.Q_H = Q_H;
-                                dg.tail_mu = tail_mu;
-                                dg.rho = rho;
-                                dg.s = s;
-                                dg.entropy = entropy;
-                                dg.k3 = k3;
-                                dg.is_weight = wt;
-                                dg.row_sum = 0.0f;
-                                dg.adv = A;
-                                dg.n_valid_k = nval;
-                                dg.flags = flags;
-                                dg.reserved = 0;
-                                a.diag[t] = dg;
+                            if (a.diag) {  // the record in field order, as four 16-byte stores
+                                float4* dp = reinterpret_cast<float4*>(a.diag + t);
+                                dp[0] = make_float4(loss, logp_a, P_H, tail_pi);
+                                dp[1] = make_float4(Q_H, tail_mu, rho, s);
+                                dp[2] = make_float4(entropy, k3, wt, 0.0f);
+                                dp[3] = make_float4(A, __int_as_float(nval), __uint_as_float(flags), 0.0f);
                                 if (t_prev >= 0) {  // the previous row's sum rode in with this exchange
                                     float rsum = 0.0f;
                                     for (int r = 0; r < C; ++r) rsum += pp[r].rs;
@@ -742,53 +784,67 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 aborted = true;
                 break;
             }
-            if (tid == 0) mbar_arrive(bar_addr(st, kMetaFree));  // metadata and ids are consumed
 
             // ---- 4. write pass: g = beta p, patched at recorded ids and a ----------
             const float bw = scal[0];
             const float beta = scal[1];
-            const int nfx = scal_i[3];
-            uint16_t* grow = a.grad + t * a.gstride + lo;
+            const float g_a_free = scal[2];
+            const int a_li = m.a_li;
+            // Each warp turns a group of 32 vectors into gradients in place in shared
+            // memory and hands the 512-byte group to the TMA engine (bulk store);
+            // a chunk slot goes back to the producer once its stores have read it.
             float rs = 0.0f;
             for (int i = 0; i < nchunks; ++i) {
-                const int v1 = min((i + 1) * a.ncv, nvb);
-#pragma unroll 2
-                for (int j = i * a.ncv + tid; j < v1; j += NC) {
-                    const uint4 w = lds128(buf_s + 16u * j);
-                    float g[8];
-                    g[0] = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
-                    g[1] = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
-                    g[2] = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
-                    g[3] = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
-                    g[4] = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
-                    g[5] = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
-                    g[6] = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
-                    g[7] = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
-                    const uint32_t word = bmp[j >> 5];  // same word for the whole warp
-                    if (word != 0u && ((word >> (j & 31)) & 1u)) {
-                        for (int e = 0; e < nfx; ++e) {
-                            const int li = fix_i[e];
-                            if ((li >> 3) == j) {
-                                const float v = fix_v[e];
-#pragma unroll
-                                for (int q = 0; q < 8; ++q)
-                                    if ((li & 7) == q) g[q] = v;
+                const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                for (int jb = v0 + 32 * warp; jb < v1; jb += NC) {
+                    const int j = jb + lane;
+                    if (j < v1) {
+                        const uint4 w = lds128(buf_s + 16u * j);
+                        float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
+                        float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
+                        float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
+                        float g3 = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
+                        float g4 = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
+                        float g5 = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
+                        float g6 = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
+                        float g7 = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
+                        const uint32_t word = bm[j >> 5];  // same word for the whole warp
+                        if (word != 0u && ((word >> (j & 31)) & 1u)) {
+                            auto patch = [&](int q, float v) {
+                                g0 = q == 0 ? v : g0;
+                                g1 = q == 1 ? v : g1;
+                                g2 = q == 2 ? v : g2;
+                                g3 = q == 3 ? v : g3;
+                                g4 = q == 4 ? v : g4;
+                                g5 = q == 5 ? v : g5;
+                                g6 = q == 6 ? v : g6;
+                                g7 = q == 7 ? v : g7;
+                            };
+                            if ((a_li >> 3) == j) patch(a_li & 7, g_a_free);
+                            for (int e = 0; e < nown; ++e) {
+                                const int li = li_s[e];
+                                if ((li >> 3) == j) patch(li & 7, fix_v[e]);
                             }
                         }
+                        rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
+                        sts128(buf_s + 16u * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
+                               pack_bf16x2(g6, g7));
                     }
-                    rs += ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
-                    st_global_v4_hint(grow + 8 * j, pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]),
-                                      pack_bf16x2(g[4], g[5]), pack_bf16x2(g[6], g[7]), pol);
+                    fence_proxy_async_smem();  // the group's writes are visible to the TMA engine
+                    __syncwarp();
+                    if (lane == 0)
+                        bulk_store(grow + 8 * jb, buf_s + 16u * jb, static_cast<uint32_t>(min(32, v1 - jb)) * 16u, pol);
                 }
+                if (lane == 0) bulk_wait_read<0>();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_addr(st, kChunkFree + i));  // slot i may be refilled
+                if (lane == 0) mbar_arrive(data_bar(ds, kChunkFree + i));  // slot i may be refilled
             }
             if (tail && tid == 0) {
                 for (int q = 0; q < tail; ++q) {
                     const int li = n8 + q;
-                    float g = beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
-                    for (int e = 0; e < nfx; ++e)
-                        if (fix_i[e] == li) g = fix_v[e];
+                    float g = li == a_li ? g_a_free : beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
+                    for (int e = 0; e < nown; ++e)
+                        if (li_s[e] == li) g = fix_v[e];
                     rs += g;
                     grow[li] = f_to_bf_bits(g);
                 }
@@ -800,13 +856,13 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
                 float tot = 0.0f;
                 for (int w = 0; w < NCW; ++w) tot += red[3 * NCW + w];
                 rs_prev = tot;
-                mbar_arrive(bar_addr(st, kRowDone));  // tail entries and the stage are free
+                mbar_arrive(meta_bar(ms, kMetaFree));  // the slot's list and bitmap are free
             }
-            if (warp == 0)
-                for (int e = lane; e < nfx; e += 32) bmp[fix_i[e] >> 8] = 0u;
             t_prev = t;
-            ++nproc;
+            ++nmeta;
+            ++ndata;
         }
+        if (lane == 0) bulk_wait_all();  // this warp's gradient stores have completed
         t_last = t_prev;
         rs_last = rs_prev;
     }
@@ -831,31 +887,32 @@ __global__ void __launch_bounds__(NC + 32) center_kernel(const __grid_constant__
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 struct Plan {
-    int C, NC, S, ncv, NB;
+    int C, NC, S, ncv, NB, MS;
     Layout L;
 };
 
-Layout make_layout(int S, int K_max, int NC, int NB) {
+Layout make_layout(int S, int K_max, int NC, int NB, int MS, int C) {
     Layout L;
     L.stage_bytes = round_up(S * 2, 128);
+    L.list_cap = K_max > 0 ? K_max : 1;
+    L.nwords = (S / 8 + 31) / 32;
     int off = NB * L.stage_bytes;
     auto take = [&](int bytes) {
         const int o = off;
         off = round_up(off + bytes, 16);
         return o;
     };
-    L.off_ids = take(NB * K_max * 4);
-    L.off_lps = take(NB * K_max * 4);
-    L.off_meta = take(NB * static_cast<int>(sizeof(RowMeta)));
-    L.off_bars = take((kMaxStages * kBarsPerStage + 2) * 8);
-    L.off_part = take(2 * kMaxCluster * 64);
-    L.off_mine = take(64);
+    L.off_meta = take(MS * static_cast<int>(sizeof(RowMeta)));
+    L.off_list_li = take(MS * L.list_cap * 4);
+    L.off_list_lp = take(MS * L.list_cap * 4);
+    L.off_list_k = take(MS * L.list_cap * 4);
+    L.off_bitmap = take(MS * L.nwords * 4);
+    L.off_bars = take(kNumBars * 8);
+    L.off_part = take(2 * C * static_cast<int>(sizeof(Partial)));
+    L.off_mine = take(static_cast<int>(sizeof(Partial)));
     L.off_frs = take(kMaxCluster * 8);
-    L.off_fixi = take((K_max + 1) * 4);
-    L.off_fixk = take((K_max + 1) * 4);
-    L.off_fixz = take((K_max + 1) * 4);
-    L.off_fixv = take((K_max + 1) * 4);
-    L.off_bmp = take(((S / 8 + 31) / 32) * 4);
+    L.off_fixz = take(L.list_cap * 4);
+    L.off_fixv = take(L.list_cap * 4);
     L.off_red = take(4 * (NC / 32) * 4);
     L.off_scal = take(8 * 4);
     L.total = off;
@@ -863,13 +920,14 @@ Layout make_layout(int S, int K_max, int NC, int NB) {
 }
 
 // Automatic plan: about 40 KiB of logits per CTA (clusters of up to 16
-// CTAs), one pipeline stage (more resident CTAs beat deeper prefetch on
-// GB300, measured), 128 compute threads up to ~20k entries per slice.  For the
-// 151936-entry vocabulary: 8 CTAs x 18992 entries, ~44 KB of shared memory.
+// CTAs), one data stage whose 4 KiB chunks are recycled as the write pass
+// frees them, a two-slot metadata ring, 256 compute threads (128 for small
+// slices).  For the 151936-entry vocabulary: 8 CTAs x 18992 entries.
 int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
     const int NB = req_stages > 0 ? req_stages : 1;
+    const int MS = NB + 1;
     int C = req_cluster;
-    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S > 20480 ? 256 : 128); };
+    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128); };
     if (C <= 0) {
         C = static_cast<int>((2LL * V + 40959) / 40960);
         C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
@@ -877,7 +935,7 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
     }
     const int S = round_up((V + C - 1) / C, 8);
     const int NC = threads_for(S);
-    const Layout L = make_layout(S, K_max, NC, NB);
+    const Layout L = make_layout(S, K_max, NC, NB, MS, C);
     if (L.total > kMaxSmem)
         return fail(SC_ERR_SHAPE,
                     "V = %d with cluster size %d and %d stages needs %d bytes of shared memory per CTA", V, C,
@@ -889,6 +947,7 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
     out->NC = NC;
     out->S = S;
     out->NB = NB;
+    out->MS = MS;
     // a whole number of 32-vector groups per chunk keeps each warp's bitmap word uniform
     out->ncv = round_up((nvb + nch - 1) / nch, 32);
     if (out->ncv < 32) out->ncv = 32;
@@ -1088,6 +1147,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.S = P.S;
     ka.ncv = P.ncv;
     ka.NB = P.NB;
+    ka.MS = P.MS;
     ka.L = P.L;
 
     cudaLaunchConfig_t cfg = {};
