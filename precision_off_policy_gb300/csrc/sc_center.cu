@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
     const int nchunks = (nvb + a.ncv - 1) / a.ncv;
     const int cap = L.list_cap, nwords = L.nwords;
     const float kscale = a.inv_t * kLog2e;
-    const uint64_t pol = l2_policy_evict_first();
+    const uint64_t pol = l2_policy_evict_first();     // last use: gradient stores, write-pass reads
+    const uint64_t pol_keep = l2_policy_evict_last(); // slice copies, read again by the write pass
 
     if (tid == 0) {
         for (int d = 0; d < NB; ++d)
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                         const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
                         const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
                         mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
-                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol);
+                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
                     }
                 }
                 stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
@@ -616,6 +617,11 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                 red[2 * NCW + warp] = s2t;
             }
             named_bar(NC);
+            // The slice in shared memory has served its two passes: hand it back so
+            // the next row streams in during the exchange and the write pass, which
+            // reads the logits again from L2.
+            if (lane == 0)
+                for (int i = 0; i < nchunks; ++i) mbar_arrive(data_bar(ds, kChunkFree + i));
 
             // ---- 3. cluster exchange and row scalars (warp 0) -------------------
             if (warp == 0) {
@@ -790,59 +796,45 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
             const float beta = scal[1];
             const float g_a_free = scal[2];
             const int a_li = m.a_li;
-            // Each warp turns a group of 32 vectors into gradients in place in shared
-            // memory and hands the 512-byte group to the TMA engine (bulk store);
-            // a chunk slot goes back to the producer once its stores have read it.
+            const uint16_t* lrow = a.logits + t * a.lstride + lo;
             float rs = 0.0f;
-            for (int i = 0; i < nchunks; ++i) {
-                const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                for (int jb = v0 + 32 * warp; jb < v1; jb += NC) {
-                    const int j = jb + lane;
-                    if (j < v1) {
-                        const uint4 w = lds128(buf_s + 16u * j);
-                        float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
-                        float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
-                        float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
-                        float g3 = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
-                        float g4 = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
-                        float g5 = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
-                        float g6 = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
-                        float g7 = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
-                        const uint32_t word = bm[j >> 5];  // same word for the whole warp
-                        if (word != 0u && ((word >> (j & 31)) & 1u)) {
-                            auto patch = [&](int q, float v) {
-                                g0 = q == 0 ? v : g0;
-                                g1 = q == 1 ? v : g1;
-                                g2 = q == 2 ? v : g2;
-                                g3 = q == 3 ? v : g3;
-                                g4 = q == 4 ? v : g4;
-                                g5 = q == 5 ? v : g5;
-                                g6 = q == 6 ? v : g6;
-                                g7 = q == 7 ? v : g7;
-                            };
-                            if ((a_li >> 3) == j) patch(a_li & 7, g_a_free);
-                            for (int e = 0; e < nown; ++e) {
-                                const int li = li_s[e];
-                                if ((li >> 3) == j) patch(li & 7, fix_v[e]);
-                            }
-                        }
-                        rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
-                        sts128(buf_s + 16u * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
-                               pack_bf16x2(g6, g7));
+#pragma unroll 2
+            for (int j = tid; j < nvb; j += NC) {
+                const uint4 w = ldg_v4_hint(lrow + 8 * j, pol);
+                float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
+                float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
+                float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
+                float g3 = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
+                float g4 = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
+                float g5 = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
+                float g6 = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
+                float g7 = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
+                const uint32_t word = bm[j >> 5];  // same word for the whole warp
+                if (word != 0u && ((word >> (j & 31)) & 1u)) {
+                    auto patch = [&](int q, float v) {
+                        g0 = q == 0 ? v : g0;
+                        g1 = q == 1 ? v : g1;
+                        g2 = q == 2 ? v : g2;
+                        g3 = q == 3 ? v : g3;
+                        g4 = q == 4 ? v : g4;
+                        g5 = q == 5 ? v : g5;
+                        g6 = q == 6 ? v : g6;
+                        g7 = q == 7 ? v : g7;
+                    };
+                    if ((a_li >> 3) == j) patch(a_li & 7, g_a_free);
+                    for (int e = 0; e < nown; ++e) {
+                        const int li = li_s[e];
+                        if ((li >> 3) == j) patch(li & 7, fix_v[e]);
                     }
-                    fence_proxy_async_smem();  // the group's writes are visible to the TMA engine
-                    __syncwarp();
-                    if (lane == 0)
-                        bulk_store(grow + 8 * jb, buf_s + 16u * jb, static_cast<uint32_t>(min(32, v1 - jb)) * 16u, pol);
                 }
-                if (lane == 0) bulk_wait_read<0>();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(data_bar(ds, kChunkFree + i));  // slot i may be refilled
+                rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
+                st_global_v4_hint(grow + 8 * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
+                                  pack_bf16x2(g6, g7), pol);
             }
             if (tail && tid == 0) {
                 for (int q = 0; q < tail; ++q) {
                     const int li = n8 + q;
-                    float g = li == a_li ? g_a_free : beta * ex2(fmaf(bf_to_f(buf[li]), kscale, -bw));
+                    float g = li == a_li ? g_a_free : beta * ex2(fmaf(bf_to_f(lrow[li]), kscale, -bw));
                     for (int e = 0; e < nown; ++e)
                         if (li_s[e] == li) g = fix_v[e];
                     rs += g;
@@ -862,7 +854,6 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
             ++nmeta;
             ++ndata;
         }
-        if (lane == 0) bulk_wait_all();  // this warp's gradient stores have completed
         t_last = t_prev;
         rs_last = rs_prev;
     }
