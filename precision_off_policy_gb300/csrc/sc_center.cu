@@ -12,36 +12,32 @@
 // GB300 design.  One row is shared by a cluster of C CTAs; CTA r owns the
 // vocabulary slice [r*S, min((r+1)*S, V)).  Each CTA is warp-specialised.
 //
-// * The producer warp walks the cluster's rows ahead of the consumers.  Per
-//   row it fills a slot of a small metadata ring: the row's scalars and, for
-//   valid rows, the compact list of recorded ids that fall in this CTA's
-//   slice (repeats dropped, q = exp(logprob) precomputed) with a bitmap of the
-//   16-byte vectors that hold them.  It then starts 1-D bulk copies (TMA
-//   engine) of the logit slice into the data stage, 4 KiB chunk by chunk, each
-//   as soon as the previous row's write pass has released that chunk.
-// * The consumer warps, per row of the ring:
-//   0. padding / error rows: write the zero gradient slice and move on;
-//   1. max pass on packed bf16 pairs as chunks land, while consumer warp 0
-//      reads the owned recorded ids' logits and overwrites them in shared
-//      memory with -2^100 (the max is exact either way: warp 0 contributes
-//      the values it overwrites);
-//   2. warp 0 reduces the owned recorded ids (mass, entropy term, sum of
-//      q y, the recorded mass as an error-free FP32 pair with its largest
-//      term apart) while all warps run the exp pass: the unrecorded mass
-//      sum_{v not in H} e^{x_v - m} accumulates directly (no 1 - P_H
-//      cancellation), with the entropy term;
-//   3. exchange: each CTA sends one 64-byte record to every CTA of the
-//      cluster with st.async stores that complete as transaction bytes on the
-//      receiver's mbarrier; warp 0 merges the C records into the row scalars
-//      (LSE, P_H, Q_H, rho, s, loss, k3, importance weight) in O(C), the same
-//      way in every CTA;
-//   4. write pass: p_v is recomputed from shared memory and g_v = beta p_v
-//      streams to global memory with 16-byte stores and an evict-first L2
-//      hint; the <= K+1 special entries (recorded ids and the sampled token)
-//      are patched in registers via the per-vector bitmap.
+// * The producer warp walks the cluster's rows ahead of the others.  It
+//   writes padding and error rows (zero gradient) itself.  For every valid row
+//   it fills a slot of a metadata ring -- the row's scalars and the compact
+//   list of recorded ids that fall in this CTA's slice (repeats dropped), with
+//   a one-bit-per-entry bitmap of them -- and starts 1-D bulk copies (TMA
+//   engine) of the logit slice into shared memory, chunk by chunk, as soon as
+//   the streaming warps have released the buffer.
+// * The streaming warps alternate two passes.  Phase A of row i: one pass
+//   over the slice in shared memory with a running maximum, summing
+//   e^{x_v - m} and its entropy term over the unrecorded entries (recorded ids
+//   are skipped through the bitmap, so the unrecorded mass accumulates
+//   directly, with no 1 - P_H cancellation), then picking up the recorded
+//   ids' logits; the buffer is then released.  Write pass of row i - 1: the
+//   slice again from L2 (the copies are marked evict-last), g_v = beta p_v
+//   stored with 16-byte stores, no special cases.
+// * The scalar warp does the per-row serial work off the streaming path:
+//   it merges the streaming warps' partials into this CTA's 64-byte record,
+//   sends it to every CTA of the cluster with st.async stores that complete
+//   as transaction bytes on the receiver's mbarrier, merges the C records
+//   into the row scalars (LSE, P_H, Q_H, rho, s, loss, k3, importance weight)
+//   -- the same way in every CTA -- while the streaming warps run phase A of
+//   the next row, and after a row's write pass overwrites its <= K+1 special
+//   entries (recorded ids and the sampled token) with their own gradients.
 // Every logit is read from HBM once and every gradient written once.  The
-// grid is persistent (as many clusters as fit).  Every wait is bounded
-// (about 1 s) and reports through the status word.
+// grid is persistent (as many clusters as fit).  Every wait is bounded (about
+// 1 s) and reports through the status word.
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -56,38 +52,39 @@ namespace {
 
 constexpr int kMaxCluster = 16;
 constexpr int kMaxChunks = 16;
-constexpr int kMaxStages = 4;             // data stages
-constexpr int kMaxMeta = kMaxStages + 1;  // metadata ring slots
+constexpr int kMaxStages = 4;  // data stages
+constexpr int kMetaSlots = 4;  // metadata ring: rows in the write pass, in phase A, and two prefetched
+constexpr int kXBufs = 4;      // exchange buffers (peers may run ahead by a row)
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
-constexpr int kMaxSmem = 232448;          // 227 KiB of dynamic shared memory per CTA
-constexpr int kChunkVecTarget = 256;      // 16-byte vectors per bulk copy (4 KiB)
-constexpr uint16_t kSentinel = 0xF180u;   // bf16 -2^100: marks recorded ids in shared memory
+constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
+constexpr int kChunkVecTarget = 256;    // 16-byte vectors per bulk copy (4 KiB)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr uint32_t kSleepProducerNs = 128;  // polling interval of the producer's waits
+constexpr uint32_t kSleepScalarNs = 32;     // polling interval of the scalar warp's waits
+constexpr uint32_t kSleepStreamNs = 32;     // polling interval of the streaming warps' waits
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-// One row as the producer hands it to the consumers.
+// One valid row as the producer hands it to the consumers.
 struct RowMeta {
-    long long t;      // row index; -1 ends the consumers' loop
-    uint32_t zflags;  // nonzero: padding or error row (zero gradient)
-    int sa;           // sampled id
-    int nown;         // recorded ids of this CTA's slice in the compact list
-    int a_li;         // local index of a in this slice, -1 if another CTA owns it
-    uint32_t flags;   // row flags found by the producer (count, repeats, out of range)
-    float A, rl;      // advantage, rollout logprob
-    int pad[3];
+    long long t;     // row index; -1 ends the consumers' loop
+    int sa;          // sampled id
+    int nown;        // recorded ids of this CTA's slice in the compact list
+    int a_li;        // local index of a in this slice, -1 if another CTA owns it
+    uint32_t flags;  // row flags found by the producer (count, repeats, out of range)
+    float A, rl;     // advantage, rollout logprob
 };
-static_assert(sizeof(RowMeta) == 48, "RowMeta layout");
+static_assert(sizeof(RowMeta) == 32, "RowMeta layout");
 
 // One CTA's contribution to a row, exchanged across the cluster (64 bytes).
 // y' values are relative to this CTA's own slice maximum m (y' = (z - m) kscale).
 struct Partial {
     float m;            // slice maximum of z (-inf for an empty slice)
     float S1, S2;       // unrecorded entries: sum 2^y', sum 2^y' y'
-    float rs;           // FP32 gradient sum of this slice for the previous valid row
+    float rs;           // FP32 gradient sum of this slice for the row two rows back
     float lH, EH;       // recorded ids owned here: sum 2^y', sum 2^y' y'
     float QY;           // sum q_k y'_k over the owned recorded ids
     float qo_hi, qo_lo; // sum of q_k over them except the largest one (double-float)
@@ -104,9 +101,9 @@ static_assert(sizeof(Partial) == 64, "partial record is 64 bytes");
 struct Layout {
     int stage_bytes;  // bytes of one data stage (128-aligned)
     int list_cap;     // entries of one owned list (K_max)
-    int nwords;       // bitmap words of one slice
+    int nwords;       // bitmap words of one slice (one bit per entry)
     int off_meta, off_list_li, off_list_lp, off_list_k, off_bitmap, off_bars, off_part, off_mine, off_frs,
-        off_fixz, off_fixv, off_red, off_scal, total;
+        off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, total;
 };
 
 struct KArgs {
@@ -126,7 +123,7 @@ struct KArgs {
     int V, K_max, n_resp;
     int is_mode, centering;
     float tis_max, mis_min, mis_max, inv_t, grad_scale;
-    int C, S, ncv, NB, MS;
+    int C, S, ncv, NB;
     Layout L;
 };
 
@@ -147,9 +144,41 @@ __device__ __forceinline__ void status_or(uint32_t* st, uint32_t bits) {
     if (st) atomicOr(st, bits);
 }
 
+// Running (max, sum 2^y, sum 2^y y) triples, y relative to max * kscale.
+// Merging rescales both sides to the larger maximum; an empty side (m = -inf)
+// contributes nothing.  The merge is commutative, so a butterfly leaves every
+// lane with the same bits.
+struct Mass {
+    float m, s1, s2;
+};
+__device__ __forceinline__ Mass mass_merge(const Mass& a, const Mass& b, float kscale) {
+    const float m = fmaxf(a.m, b.m);
+    Mass r;
+    r.m = m;
+    r.s1 = 0.0f;
+    r.s2 = 0.0f;
+    if (a.m > -INFINITY) {
+        const float d = (a.m - m) * kscale;
+        const float f = ex2(d);
+        r.s1 = f * a.s1;
+        r.s2 = f * fmaf(d, a.s1, a.s2);
+    }
+    if (b.m > -INFINITY) {
+        const float d = (b.m - m) * kscale;
+        const float f = ex2(d);
+        r.s1 = fmaf(f, b.s1, r.s1);
+        r.s2 = fmaf(f, fmaf(d, b.s1, b.s2), r.s2);
+    }
+    return r;
+}
+__device__ __forceinline__ Mass mass_shfl(const Mass& x, int off) {
+    return Mass{__shfl_xor_sync(kFull, x.m, off), __shfl_xor_sync(kFull, x.s1, off),
+                __shfl_xor_sync(kFull, x.s2, off)};
+}
+
 // Largest recorded probability with the mass of the others, merged
-// commutatively (ties go to the lower k) so a butterfly gives every lane the
-// same bits.  The others' mass is kept as an unevaluated FP32 pair.
+// commutatively (ties go to the lower k).  The others' mass is kept as an
+// unevaluated FP32 pair.
 struct HeadMass {
     float q;
     int k;
@@ -183,59 +212,68 @@ __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
 }
 
 // Barriers.  Data stage d: kChunkFull + i (copy of chunk i landed, tx bytes),
-// kChunkFree + i (every consumer warp is done with chunk i).  Meta slot s:
-// kMetaFull (producer wrote it), kMetaFree (consumers are done with it).
+// kChunkFree + i (every streaming warp is done with chunk i).  Meta slot s:
+// kMetaFull (producer wrote it), kMetaFree (its row is written).  Exchange
+// buffer x: a row's records (own expect_tx arrive + peers' bytes).  kADone[p]:
+// every streaming warp finished phase A of a row of parity p (and so the write
+// pass of the row two before it).  kSReady[p]: the row scalars of a row of
+// parity p are published.
 constexpr int kChunkFull = 0;
 constexpr int kChunkFree = kMaxChunks;
 constexpr int kBarsPerStage = 2 * kMaxChunks;
 constexpr int kMetaBase = kMaxStages * kBarsPerStage;
 constexpr int kMetaFull = 0;
 constexpr int kMetaFree = 1;
-constexpr int kXBase = kMetaBase + 2 * kMaxMeta;
-constexpr int kNumBars = kXBase + 2;
+constexpr int kXBase = kMetaBase + 2 * kMetaSlots;
+constexpr int kADone = kXBase + kXBufs;
+constexpr int kSReady = kADone + 2;
+constexpr int kNumBars = kSReady + 2;
 
-// Resident CTAs per SM the register allocation must allow (shared memory
-// allows about this many at the automatic plan's slice sizes).
-constexpr int min_blocks(int NC) { return NC <= 128 ? 6 : (NC <= 256 ? 4 : (NC <= 384 ? 3 : 2)); }
+// Resident CTAs per SM the register allocation must allow.
+constexpr int min_blocks(int NC) { return NC <= 128 ? 6 : (NC <= 256 ? 3 : 2); }
 
 template <int NC>
-__global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int NCW = NC / 32;  // consumer warps; warp NCW is the producer
+    constexpr int NCW = NC / 32;  // streaming warps; warp NCW: row scalars; warp NCW + 1: producer
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t crank = cluster_ctarank();
     const uint32_t cid = cluster_id_x();
     const uint32_t ncl = num_clusters_x();
-    const int C = a.C, K_max = a.K_max, NB = a.NB, MS = a.MS;
+    const int C = a.C, K_max = a.K_max, NB = a.NB;
     const Layout& L = a.L;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
-    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);         // [MS]
-    int* list_li = reinterpret_cast<int*>(smem + L.off_list_li);           // [MS][list_cap]
-    float* list_lp = reinterpret_cast<float*>(smem + L.off_list_lp);       // [MS][list_cap]
-    int* list_k = reinterpret_cast<int*>(smem + L.off_list_k);             // [MS][list_cap]
-    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [MS][nwords]
-    Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [2][C]
+    RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);         // [kMetaSlots]
+    int* list_li = reinterpret_cast<int*>(smem + L.off_list_li);           // [kMetaSlots][cap]
+    float* list_lp = reinterpret_cast<float*>(smem + L.off_list_lp);       // [kMetaSlots][cap]
+    int* list_k = reinterpret_cast<int*>(smem + L.off_list_k);             // [kMetaSlots][cap]
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [kMetaSlots][nwords]
+    Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [kXBufs][C]
     Partial* mine = reinterpret_cast<Partial*>(smem + L.off_mine);         // staging of this CTA's record
     float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);             // [kMaxCluster]
-    float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);            // [list_cap]
-    float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);            // [list_cap]
-    float* red = reinterpret_cast<float*>(smem + L.off_red);               // [4][NCW]
-    float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [8]
-    int* scal_i = reinterpret_cast<int*>(scal);
+    float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);            // [2][cap] recorded logits
+    float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);            // [2][cap] their gradients
+    float* zav = reinterpret_cast<float*>(smem + L.off_zav);               // [2] logit of a
+    float* red = reinterpret_cast<float*>(smem + L.off_red);               // [2][3][NCW] warp partials
+    float* rsw = reinterpret_cast<float*>(smem + L.off_rsw);               // [2][NCW] warp row sums
+    float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [2][4] row scalars
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_flag);
     auto data_bar = [&](int d, int i) { return smem_addr(&bars[d * kBarsPerStage + i]); };
     auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
-    const uint32_t xbar0 = smem_addr(&bars[kXBase]);
+    auto xbar = [&](int x) { return smem_addr(&bars[kXBase + x]); };
+    auto adone = [&](int p) { return smem_addr(&bars[kADone + p]); };
+    auto sready = [&](int p) { return smem_addr(&bars[kSReady + p]); };
 
     const int lo = static_cast<int>(crank) * a.S;
     const int hi = min(lo + a.S, a.V);
     const int n = max(hi - lo, 0);
-    const int n8 = n & ~7, nvb = n8 >> 3, tail = n - n8, nv = nvb + (tail ? 1 : 0);
+    const int n8 = n & ~7, nvb = n8 >> 3, tail = n - n8;
     const int nchunks = (nvb + a.ncv - 1) / a.ncv;
     const int cap = L.list_cap, nwords = L.nwords;
     const float kscale = a.inv_t * kLog2e;
-    const uint64_t pol = l2_policy_evict_first();     // last use: gradient stores, write-pass reads
-    const uint64_t pol_keep = l2_policy_evict_last(); // slice copies, read again by the write pass
+    const uint64_t pol = l2_policy_evict_first();      // last use: gradient stores, write-pass reads
+    const uint64_t pol_keep = l2_policy_evict_last();  // slice copies, read again by the write pass
 
     if (tid == 0) {
         for (int d = 0; d < NB; ++d)
@@ -243,24 +281,62 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                 mbar_init(data_bar(d, kChunkFull + i), 1u);
                 mbar_init(data_bar(d, kChunkFree + i), static_cast<uint32_t>(NCW));
             }
-        for (int s = 0; s < MS; ++s) {
+        for (int s = 0; s < kMetaSlots; ++s) {
             mbar_init(meta_bar(s, kMetaFull), 1u);
             mbar_init(meta_bar(s, kMetaFree), 1u);
+            meta[s].nown = 0;
         }
-        mbar_init(xbar0, 1u);  // exchange: own expect_tx arrive + peers' st.async bytes
-        mbar_init(xbar0 + 8, 1u);
+        for (int x = 0; x < kXBufs; ++x) mbar_init(xbar(x), 1u);
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(adone(p), static_cast<uint32_t>(NCW));
+            mbar_init(sready(p), 1u);
+        }
+        for (int r = 0; r < kMaxCluster; ++r) frs[r] = make_float2(0.0f, 0.0f);
+        *abort_flag = 0;
         fence_mbar_init_cluster();
     }
-    for (int i = tid; i < MS * nwords; i += NC + 32) bitmap[i] = 0u;
+    for (int i = tid; i < kMetaSlots * nwords; i += NC + 64) bitmap[i] = 0u;
     cluster_sync_all();  // every CTA's barriers exist before peers signal them
 
-    long long t_last = -1;  // consumers: last valid row (for the final row sum)
-    float rs_last = 0.0f;   // consumer thread 0: this CTA's share of its sum
-    bool aborted = false;
+    // Any role that gives up raises the flag; the others see it at their next
+    // row and leave too (their waits are bounded in any case).
+    auto give_up = [&](uint32_t bits) {
+        if (lane == 0) {
+            status_or(a.status, bits);
+            *abort_flag = 1;
+        }
+    };
+    auto flag_up = [&]() { return __any_sync(kFull, *abort_flag != 0); };
 
-    if (warp == NCW) {
+    // scalar warp state kept for the final row-sum flush
+    bool clean_end = false;
+    uint32_t nrows = 0;
+    float fin_rs2 = 0.0f, fin_rs1 = 0.0f;
+    long long t_m1 = -1, t_m2 = -1;  // row indices of the two rows before the current one
+    float corr_m1 = 0.0f, corr_m2 = 0.0f;  // their row-sum corrections for the patched entries
+
+    // The write pass stores g = beta p everywhere; once it is done with row r,
+    // the scalar warp overwrites the recorded ids and a with their own values.
+    auto patch_row = [&](uint32_t r, long long t) {
+        const int sl = static_cast<int>(r % kMetaSlots);
+        const int q = static_cast<int>(r & 1u);
+        const int* li = list_li + sl * cap;
+        const float* fv = fix_v + q * cap;
+        const int nown = meta[sl].nown, a_li = meta[sl].a_li;
+        uint16_t* grow = a.grad + t * a.gstride + lo;
+        bool a_rec = false;
+        for (int e = lane; e < nown; e += 32) {
+            const int l = li[e];
+            a_rec = a_rec || l == a_li;
+            grow[l] = f_to_bf_bits(fv[e]);
+        }
+        a_rec = __any_sync(kFull, a_rec);
+        if (lane == 0 && a_li >= 0 && !a_rec) grow[a_li] = f_to_bf_bits(scal[4 * q + 2]);
+    };
+
+    if (warp == NCW + 1) {
         // ================= producer warp =================
-        uint32_t nmeta = 0, ndata = 0;
+        uint32_t nfill = 0;
         bool stop = false;
         for (long long base = cid; base < a.T && !stop; base += 32LL * ncl) {
             const long long tl = base + static_cast<long long>(lane) * ncl;
@@ -281,32 +357,39 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
             }
             const unsigned inmask = __ballot_sync(kFull, in);
             for (int j = 0; j < 32 && ((inmask >> j) & 1u); ++j) {
+                if (flag_up()) {
+                    stop = true;
+                    break;
+                }
                 const long long t = base + static_cast<long long>(j) * ncl;
                 const uint32_t zfj = __shfl_sync(kFull, zf, j);
                 const int rj = __shfl_sync(kFull, resp_l, j);
                 const int sj = __shfl_sync(kFull, sa_l, j);
-                const int ms = static_cast<int>(nmeta % MS);
-                if (nmeta >= static_cast<uint32_t>(MS) &&
-                    !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nmeta / MS) - 1u) & 1u, kWaitLimitNs)) {
+                if (zfj) {  // padding or error row: zero gradient, no compute
+                    uint16_t* grow = a.grad + t * a.gstride + lo;
+                    for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
+                    if (lane < tail) grow[n8 + lane] = 0;
+                    if (crank == 0 && lane == 0) {
+                        a.logp[t] = 0.0f;
+                        if (a.diag) {  // zeros and the flags, as four 16-byte stores
+                            float4* dp = reinterpret_cast<float4*>(a.diag + t);
+                            const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                            dp[0] = z4;
+                            dp[1] = z4;
+                            dp[2] = z4;
+                            dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(zfj), 0.0f);
+                        }
+                        if (zfj & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+                    }
+                    continue;
+                }
+                const int ms = static_cast<int>(nfill % kMetaSlots);
+                if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
+                    !mbar_wait_sleepy(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs,
+                                      kSleepProducerNs)) {
                     if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                     stop = true;
                     break;
-                }
-                RowMeta* mt = meta + ms;
-                if (zfj) {  // padding or error row: the consumers write zeros
-                    if (lane == 0) {
-                        mt->t = t;
-                        mt->zflags = zfj;
-                        mt->sa = sj;
-                        mt->nown = 0;
-                        mt->a_li = -1;
-                        mt->flags = 0;
-                        mt->A = 0.0f;
-                        mt->rl = 0.0f;
-                        mbar_arrive(meta_bar(ms, kMetaFull));
-                    }
-                    ++nmeta;
-                    continue;
                 }
                 // ---- recorded ids of this slice: compact list, repeats dropped ----
                 // (row scalars loaded first so their latency overlaps the list)
@@ -322,7 +405,10 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                 float* lp_s = list_lp + ms * cap;
                 int* k_s = list_k + ms * cap;
                 uint32_t* bm = bitmap + ms * nwords;
-                for (int w = lane; w < nwords; w += 32) bm[w] = 0u;  // the slot's previous bits
+                {  // clear the bits of the slot's previous row (whole words: they are all its own)
+                    const int old = meta[ms].nown;
+                    for (int e = lane; e < old; e += 32) bm[li_s[e] >> 5] = 0u;
+                }
                 __syncwarp();
                 const long long kb = t * static_cast<long long>(K_max);
                 int nown = 0;
@@ -358,7 +444,7 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                             li_s[pos] = id - lo;
                             lp_s[pos] = lpr[r];
                             k_s[pos] = k;
-                            atomicOr(&bm[(id - lo) >> 8], 1u << (((id - lo) >> 3) & 31));
+                            atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
                         }
                         nown += __popc(km);
                         __syncwarp();
@@ -368,9 +454,8 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                 if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
                 const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
                 if (lane == 0) {
-                    if (a_li >= 0) atomicOr(&bm[a_li >> 8], 1u << ((a_li >> 3) & 31));
+                    RowMeta* mt = meta + ms;
                     mt->t = t;
-                    mt->zflags = 0;
                     mt->sa = sj;
                     mt->nown = nown;
                     mt->a_li = a_li;
@@ -380,17 +465,17 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                 }
                 // ---- logit slice: chunk by chunk as the stage's slots free up ----
                 if (lane == 0) {
-                    const int ds = static_cast<int>(ndata % NB);
-                    const bool reuse = ndata >= static_cast<uint32_t>(NB);
-                    const uint32_t fpar = ((ndata / NB) - 1u) & 1u;
-                    uint16_t* bufst = reinterpret_cast<uint16_t*>(smem + ds * L.stage_bytes);
+                    const int ds = static_cast<int>(nfill % NB);
+                    const bool reuse = nfill >= static_cast<uint32_t>(NB);
+                    const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
                     const uint16_t* lrow = a.logits + t * a.lstride + lo;
-                    const uint32_t bs = smem_addr(bufst);
+                    const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
                     for (int i = 0; i < nchunks; ++i) {
-                        if (reuse && !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
+                        if (reuse &&
+                            !mbar_wait_sleepy(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs, kSleepProducerNs)) {
                             status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                             for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
-                                (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (ndata / NB) & 1u,
+                                (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
                                                         kWaitLimitNs);
                             stop = true;
                             break;
@@ -406,15 +491,15 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                 if (stop) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
-                ++nmeta;
-                ++ndata;
+                ++nfill;
             }
         }
         if (!stop) {  // end marker for the consumers
-            const int ms = static_cast<int>(nmeta % MS);
+            const int ms = static_cast<int>(nfill % kMetaSlots);
             bool ok = true;
-            if (nmeta >= static_cast<uint32_t>(MS))
-                ok = mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nmeta / MS) - 1u) & 1u, kWaitLimitNs);
+            if (nfill >= static_cast<uint32_t>(kMetaSlots))
+                ok = mbar_wait_sleepy(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs,
+                                      kSleepProducerNs);
             if (ok) {
                 if (lane == 0) {
                     meta[ms].t = -1;
@@ -426,124 +511,64 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
         }
         // copies still in flight land before the CTA can exit (bounded again)
         if (lane == 0) {
-            const uint32_t f0 = ndata > static_cast<uint32_t>(NB) ? ndata - NB : 0u;
-            for (uint32_t f = f0; f < ndata; ++f)
+            const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
+            for (uint32_t f = f0; f < nfill; ++f)
                 for (int i = 0; i < nchunks; ++i)
                     (void)mbar_wait_bounded(data_bar(f % NB, kChunkFull + i), (f / NB) & 1u, kWaitLimitNs);
         }
         __syncwarp();
-    } else {
-        // ================= consumer warps =================
-        uint32_t nmeta = 0, ndata = 0;
-        float rs_prev = 0.0f;
-        long long t_prev = -1;
-        for (;;) {
-            const int ms = static_cast<int>(nmeta % MS);
-            const bool got = mbar_wait_bounded(meta_bar(ms, kMetaFull), (nmeta / MS) & 1u, kWaitLimitNs);
-            if (named_bar_or(NC, !got)) {
-                if (tid == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                aborted = true;
+    } else if (warp == NCW) {
+        // ================= scalar warp: records, exchange, row scalars =================
+        for (uint32_t j = 0;; ++j) {
+            if (flag_up()) break;
+            const int p = static_cast<int>(j & 1u);
+            const bool got = mbar_wait_sleepy(adone(p), (j >> 1) & 1u, kWaitLimitNs, kSleepScalarNs);
+            if (!__all_sync(kFull, got)) {
+                give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
             }
+            const int ms = static_cast<int>(j % kMetaSlots);
             const RowMeta m = meta[ms];
-            if (m.t < 0) break;
-            const long long t = m.t;
-            uint16_t* grow = a.grad + t * a.gstride + lo;
-            if (m.zflags) {  // ---- padding or error row: zero gradient ----
-                for (int j = tid; j < nvb; j += NC) st_global_v4_hint(grow + 8 * j, 0u, 0u, 0u, 0u, pol);
-                if (tid < tail) grow[n8 + tid] = 0;
-                if (crank == 0 && tid == 0) {
-                    a.logp[t] = 0.0f;
-                    if (a.diag) {  // zeros and the flags, as four 16-byte stores
-                        float4* dp = reinterpret_cast<float4*>(a.diag + t);
-                        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        dp[0] = z4;
-                        dp[1] = z4;
-                        dp[2] = z4;
-                        dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(m.zflags), 0.0f);
-                    }
-                    if (m.zflags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
-                }
-                named_bar(NC);  // every consumer is done with the slot
-                if (tid == 0) mbar_arrive(meta_bar(ms, kMetaFree));
-                ++nmeta;
-                continue;
+            // The write pass of row j - 2 ended before phase A of row j in every
+            // streaming warp: its special entries can be patched, its row sum is
+            // complete and its slot can be refilled.
+            float rs2 = 0.0f;
+            if (j >= 2) {
+                patch_row(j - 2, t_m2);
+                rs2 = warp_sum(lane < NCW ? rsw[((j - 2) & 1u) * NCW + lane] : 0.0f) + corr_m2;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(meta_bar(static_cast<int>((j - 2) % kMetaSlots), kMetaFree));
             }
-            const int ds = static_cast<int>(ndata % NB);
-            const uint32_t fpar = (ndata / NB) & 1u;
-            const uint32_t par = ndata & 1u;
-            const uint32_t xph = (ndata >> 1) & 1u;
-            const uint32_t xb = xbar0 + 8u * par;
-            uint16_t* buf = reinterpret_cast<uint16_t*>(smem + ds * L.stage_bytes);
-            const uint32_t buf_s = smem_addr(buf);
+            if (m.t < 0) {  // end of the stream: the last two rows' sums go to CTA 0 below
+                fin_rs2 = rs2;
+                if (j >= 1) {
+                    patch_row(j - 1, t_m1);
+                    fin_rs1 = warp_sum(lane < NCW ? rsw[((j - 1) & 1u) * NCW + lane] : 0.0f) + corr_m1;
+                }
+                nrows = j;
+                clean_end = true;
+                break;
+            }
+            const int xi = static_cast<int>(j & 3u);
             const int* li_s = list_li + ms * cap;
             const float* lp_s = list_lp + ms * cap;
             const int* k_s = list_k + ms * cap;
-            const uint32_t* bm = bitmap + ms * nwords;
-            const int nown = m.nown;
-
-            // ---- 1. max pass (warps 1..) and owned recorded ids (warp 0) -------
-            float m_loc = -INFINITY;
-            bool timed_out = false;
-            float zav = 0.0f;  // warp 0: z of the sampled token if owned here
-            if (warp == 0) {
-                if (tail) {  // entries past the last whole vector, padded with the sentinel
-                    const uint16_t* lrow = a.logits + t * a.lstride + lo;
-                    if (lane < 8) buf[n8 + lane] = lane < tail ? lrow[n8 + lane] : kSentinel;
-                    __syncwarp();
-                }
-                for (int i = 0; i < nchunks && !timed_out; ++i)
-                    timed_out = !mbar_wait_bounded(data_bar(ds, kChunkFull + i), fpar, kWaitLimitNs);
-                timed_out = __any_sync(kFull, timed_out);
-                if (!timed_out) {
-                    if (lane < tail) m_loc = bf_to_f(buf[n8 + lane]);
-                    if (m.a_li >= 0) zav = bf_to_f(buf[m.a_li]);  // before any entry is overwritten
-                    __syncwarp();
-                    for (int e = lane; e < nown; e += 32) {
-                        const int li = li_s[e];
-                        const float z = bf_to_f(buf[li]);
-                        fix_z[e] = z;
-                        m_loc = fmaxf(m_loc, z);
-                        buf[li] = kSentinel;
-                    }
-                    // bytes this CTA receives for the row: one record from every CTA
-                    if (lane == 0) mbar_expect_tx(xb, static_cast<uint32_t>(sizeof(Partial)) * C);
-                }
-            } else {
-                uint32_t mx2 = 0xFF80FF80u;  // (-inf, -inf)
-                for (int i = 0; i < nchunks && !timed_out; ++i) {
-                    const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                    if (!mbar_wait_bounded(data_bar(ds, kChunkFull + i), fpar, kWaitLimitNs)) {
-                        timed_out = true;
-                        break;
-                    }
-#pragma unroll 4
-                    for (int j = v0 + tid - 32; j < v1; j += NC - 32) {
-                        const uint4 w = lds128(buf_s + 16u * j);
-                        mx2 = bmax2(mx2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
-                    }
-                }
-                m_loc = fmaxf(bf_lo(mx2), bf_hi(mx2));
-            }
-            m_loc = warp_max(m_loc);
-            if (lane == 0) red[warp] = m_loc;
-            if (named_bar_or(NC, timed_out)) {
-                if (tid == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                aborted = true;
-                break;
-            }
-            m_loc = red[0];
+            const float* fz = fix_z + p * cap;
+            const int nown = m.nown, a_li = m.a_li;
+            if (lane == 0) mbar_expect_tx(xbar(xi), static_cast<uint32_t>(sizeof(Partial)) * C);
+            // ---- this CTA's record of row j ----
+            {
+                const float* rp = red + p * 3 * NCW;
+                Mass cm = lane < NCW ? Mass{rp[lane], rp[NCW + lane], rp[2 * NCW + lane]}
+                                     : Mass{-INFINITY, 0.0f, 0.0f};
 #pragma unroll
-            for (int w = 1; w < NCW; ++w) m_loc = fmaxf(m_loc, red[w]);
-            const float o_c = m_loc * kscale;
-
-            // ---- 2. owned recorded ids (warp 0), then the exp pass (all) --------
-            if (warp == 0) {
+                for (int off = 16; off > 0; off >>= 1) cm = mass_merge(cm, mass_shfl(cm, off), kscale);
+                const float o_c = cm.m * kscale;
                 float lH = 0.0f, EH = 0.0f, QY = 0.0f;
                 int nval = 0;
                 HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};
                 for (int e = lane; e < nown; e += 32) {
-                    const float y = fmaf(fix_z[e], kscale, -o_c);
+                    const float y = fmaf(fz[e], kscale, -o_c);
                     const float ev = ex2(y);
                     lH += ev;
                     EH = fmaf(ev, y, EH);
@@ -562,314 +587,405 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
                     hm = head_merge(hm, head_shfl(hm, off));
                 }
                 if (lane == 0) {
-                    Partial& p = *mine;
-                    p.m = m_loc;
-                    p.rs = rs_prev;
-                    p.lH = lH;
-                    p.EH = EH;
-                    p.QY = QY;
-                    p.qo_hi = hm.oh;
-                    p.qo_lo = hm.ol;
-                    p.qbest = hm.q;
-                    p.kbest = hm.k;
-                    p.nval = nval;
-                    p.flags = m.flags;
-                    p.ya = m.a_li >= 0 ? fmaf(zav, kscale, -o_c) : 0.0f;
-                    p.has_a = m.a_li >= 0 ? 1 : 0;
-                    p.omq = hm.omq;
-                }
-            }
-            // four independent accumulator pairs keep the FADD/FFMA chains short
-            float s1a = 0.0f, s1b = 0.0f, s1c = 0.0f, s1d = 0.0f;
-            float s2a = 0.0f, s2b = 0.0f, s2c = 0.0f, s2d = 0.0f;
-#pragma unroll 2
-            for (int j = tid; j < nv; j += NC) {
-                const uint4 w = lds128(buf_s + 16u * j);
-                float y0 = fmaf(bf_lo(w.x), kscale, -o_c), y1 = fmaf(bf_hi(w.x), kscale, -o_c);
-                float e0 = ex2(y0), e1 = ex2(y1);
-                s1a += e0 + e1;
-                s2a = fmaf(e0, y0, fmaf(e1, y1, s2a));
-                y0 = fmaf(bf_lo(w.y), kscale, -o_c);
-                y1 = fmaf(bf_hi(w.y), kscale, -o_c);
-                e0 = ex2(y0);
-                e1 = ex2(y1);
-                s1b += e0 + e1;
-                s2b = fmaf(e0, y0, fmaf(e1, y1, s2b));
-                y0 = fmaf(bf_lo(w.z), kscale, -o_c);
-                y1 = fmaf(bf_hi(w.z), kscale, -o_c);
-                e0 = ex2(y0);
-                e1 = ex2(y1);
-                s1c += e0 + e1;
-                s2c = fmaf(e0, y0, fmaf(e1, y1, s2c));
-                y0 = fmaf(bf_lo(w.w), kscale, -o_c);
-                y1 = fmaf(bf_hi(w.w), kscale, -o_c);
-                e0 = ex2(y0);
-                e1 = ex2(y1);
-                s1d += e0 + e1;
-                s2d = fmaf(e0, y0, fmaf(e1, y1, s2d));
-            }
-            float s1t = (s1a + s1b) + (s1c + s1d);
-            float s2t = (s2a + s2b) + (s2c + s2d);
-            s1t = warp_sum(s1t);
-            s2t = warp_sum(s2t);
-            if (lane == 0) {
-                red[NCW + warp] = s1t;
-                red[2 * NCW + warp] = s2t;
-            }
-            named_bar(NC);
-            // The slice in shared memory has served its two passes: hand it back so
-            // the next row streams in during the exchange and the write pass, which
-            // reads the logits again from L2.
-            if (lane == 0)
-                for (int i = 0; i < nchunks; ++i) mbar_arrive(data_bar(ds, kChunkFree + i));
-
-            // ---- 3. cluster exchange and row scalars (warp 0) -------------------
-            if (warp == 0) {
-                if (lane == 0) {
-                    float S1 = 0.0f, S2 = 0.0f;
-                    for (int w = 0; w < NCW; ++w) {
-                        S1 += red[NCW + w];
-                        S2 += red[2 * NCW + w];
-                    }
-                    mine->S1 = S1;
-                    mine->S2 = S2;
+                    Partial& r = *mine;
+                    r.m = cm.m;
+                    r.S1 = cm.s1;
+                    r.S2 = cm.s2;
+                    r.rs = rs2;
+                    r.lH = lH;
+                    r.EH = EH;
+                    r.QY = QY;
+                    r.qo_hi = hm.oh;
+                    r.qo_lo = hm.ol;
+                    r.qbest = hm.q;
+                    r.kbest = hm.k;
+                    r.nval = nval;
+                    r.flags = m.flags;
+                    r.ya = a_li >= 0 ? fmaf(zav[p], kscale, -o_c) : 0.0f;
+                    r.has_a = a_li >= 0 ? 1 : 0;
+                    r.omq = hm.omq;
                 }
                 __syncwarp();
-                if (lane < C) {  // lane r sends this CTA's record to CTA r
+                if (lane < C) {  // lane r sends the record to CTA r
                     const uint32_t src = smem_addr(mine);
-                    const uint32_t dst = map_to_rank(smem_addr(part + static_cast<int>(par) * C + crank), lane);
-                    const uint32_t rb = map_to_rank(xb, lane);
+                    const uint32_t dst = map_to_rank(smem_addr(part + xi * C + static_cast<int>(crank)), lane);
+                    const uint32_t rb = map_to_rank(xbar(xi), lane);
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const uint4 v = lds128(src + 16u * q);
                         st_async_v4(dst + 16u * q, v.x, v.y, v.z, v.w, rb);
                     }
                 }
-                const bool ok = mbar_wait_cluster_bounded(xb, xph, kWaitLimitNs);
-                if (!__all_sync(kFull, ok)) {
-                    if (lane == 0) {
-                        status_or(a.status, SC_STATUS_TIMEOUT_EXCHANGE);
-                        scal_i[4] = 1;
-                    }
-                } else {
-                    // lane r < C holds CTA r's record; the others hold neutral values
-                    const Partial* pp = part + static_cast<int>(par) * C;
-                    const bool have = lane < C;
-                    const uint32_t pa = smem_addr(pp + (have ? lane : 0));
-                    const uint4 r0 = lds128(pa), r1 = lds128(pa + 16u), r2 = lds128(pa + 32u), r3 = lds128(pa + 48u);
-                    struct {
-                        float m, S1, S2, lH, EH, QY, qo_hi, qo_lo, qbest, ya, omq;
-                        int kbest, nval, has_a;
-                        uint32_t flags;
-                    } P;
-                    P.m = have ? __uint_as_float(r0.x) : -INFINITY;
-                    P.S1 = have ? __uint_as_float(r0.y) : 0.0f;
-                    P.S2 = have ? __uint_as_float(r0.z) : 0.0f;
-                    P.lH = have ? __uint_as_float(r1.x) : 0.0f;
-                    P.EH = have ? __uint_as_float(r1.y) : 0.0f;
-                    P.QY = have ? __uint_as_float(r1.z) : 0.0f;
-                    P.qo_hi = have ? __uint_as_float(r1.w) : 0.0f;
-                    P.qo_lo = have ? __uint_as_float(r2.x) : 0.0f;
-                    P.qbest = have ? __uint_as_float(r2.y) : 0.0f;
-                    P.kbest = have ? static_cast<int>(r2.z) : 0x7FFFFFFF;
-                    P.nval = have ? static_cast<int>(r2.w) : 0;
-                    P.flags = have ? r3.x : 0u;
-                    P.ya = have ? __uint_as_float(r3.y) : 0.0f;
-                    P.has_a = have ? static_cast<int>(r3.z) : 0;
-                    P.omq = have ? __uint_as_float(r3.w) : 1.0f;
-                    const float mg = warp_max(P.m);
-                    const float o = mg * kscale;
-                    const bool live = P.m > -INFINITY;
-                    const float d = live ? P.m * kscale - o : 0.0f;
-                    const float f = live ? ex2(d) : 0.0f;
-                    float lT = f * P.S1;
-                    float ET = f * fmaf(d, P.S1, P.S2);
-                    float lH = f * P.lH;
-                    float EH = f * fmaf(d, P.lH, P.EH);
-                    float QYg = 0.0f;
-                    if (P.nval > 0) QYg = fmaf(d, (P.qbest + P.qo_hi) + P.qo_lo, P.QY);
-                    float ya = P.has_a ? P.ya + d : 0.0f;
-                    int nval = P.nval;
-                    uint32_t flags = P.flags;
-                    HeadMass hm{P.qbest, P.kbest, P.omq, P.qo_hi, P.qo_lo};
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        lT += __shfl_xor_sync(kFull, lT, off);
-                        ET += __shfl_xor_sync(kFull, ET, off);
-                        lH += __shfl_xor_sync(kFull, lH, off);
-                        EH += __shfl_xor_sync(kFull, EH, off);
-                        QYg += __shfl_xor_sync(kFull, QYg, off);
-                        ya += __shfl_xor_sync(kFull, ya, off);
-                        nval += __shfl_xor_sync(kFull, nval, off);
-                        flags |= __shfl_xor_sync(kFull, flags, off);
-                        hm = head_merge(hm, head_shfl(hm, off));
-                    }
-                    // 1 - Q_H without cancellation: (1 - q_max), taken from its
-                    // log-probability, minus the others' mass
-                    float tail_mu = 1.0f, Q_H = 0.0f;
-                    if (nval > 0) {
-                        tail_mu = (hm.omq - hm.oh) - hm.ol;
-                        Q_H = (hm.q + hm.oh) + hm.ol;
-                    }
-                    const float l = lT + lH;
-                    const float log2l = log2f(l);
-                    const float P_H = lH / l;
-                    const float tail_pi = lT / l;
-                    const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
-                    if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
-                    if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
-                    const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
-                    const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
-                    const float logp_a = (ya - log2l) * kLn2;
-                    float wt = 1.0f, k3 = 0.0f;
-                    if (a.rollout) {
-                        const float dd = logp_a - m.rl;
-                        k3 = expm1f(dd) - dd;
-                        const float w = expf(dd);
-                        if (a.is_mode == SC_IS_TIS) {
-                            if (w > a.tis_max) {
-                                wt = a.tis_max;
-                                flags |= SC_FLAG_IS_TRUNC;
-                            } else {
-                                wt = w;
-                            }
-                        } else if (a.is_mode == SC_IS_MIS) {
-                            if (w >= a.mis_min && w <= a.mis_max) {
-                                wt = w;
-                            } else {
-                                wt = 0.0f;
-                                flags |= SC_FLAG_IS_REJECT;
-                            }
-                        }
-                    }
-                    const float A = m.A;
-                    const float Aw = A * wt;
-                    // sum_H c log p = sum_H q log p - rho sum_H p log p, each from the
-                    // merged sums: log p_k = (y_k - log2 l) ln 2.
-                    float csum = 0.0f;
-                    if (a.centering && nval > 0) {
-                        const float qlogp = kLn2 * fmaf(-log2l, Q_H, QYg);
-                        const float plogp = kLn2 * fmaf(-log2l, lH, EH) / l;
-                        csum = fmaf(-rho, plogp, qlogp);
-                    }
-                    const float loss = -Aw * (logp_a - csum);
-                    const float entropy = kLn2 * (log2l - (ET + EH) / l);
-                    const float alpha = -a.grad_scale * a.inv_t * Aw;
-                    const float beta = -alpha * s;
-                    for (int e = lane; e < nown; e += 32) {  // gradient at the owned recorded ids
-                        const float p = ex2(fmaf(fix_z[e], kscale, -o) - log2l);
-                        const float mu = a.centering ? fmaf(dsr, p, expf(lp_s[e])) : p;
-                        fix_v[e] = alpha * ((li_s[e] == m.a_li ? 1.0f : 0.0f) - mu);
-                    }
-                    if (lane == 0) {
-                        scal[0] = o + log2l;
-                        scal[1] = beta;
-                        scal[2] = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
-                        scal_i[4] = 0;
-                        if (crank == 0) {
-                            a.logp[t] = logp_a;
-                            if (a.diag) {  // the record in field order, as four 16-byte stores
-                                float4* dp = reinterpret_cast<float4*>(a.diag + t);
-                                dp[0] = make_float4(loss, logp_a, P_H, tail_pi);
-                                dp[1] = make_float4(Q_H, tail_mu, rho, s);
-                                dp[2] = make_float4(entropy, k3, wt, 0.0f);
-                                dp[3] = make_float4(A, __int_as_float(nval), __uint_as_float(flags), 0.0f);
-                                if (t_prev >= 0) {  // the previous row's sum rode in with this exchange
-                                    float rsum = 0.0f;
-                                    for (int r = 0; r < C; ++r) rsum += pp[r].rs;
-                                    a.diag[t_prev].row_sum = rsum;
-                                }
-                            }
-                            if (flags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
-                        }
-                    }
-                }
             }
-            named_bar(NC);
-            if (scal_i[4]) {
-                aborted = true;
+            // ---- all C records of row j: the row scalars ----
+            const bool ok = mbar_wait_cluster_sleepy(xbar(xi), (j >> 2) & 1u, kWaitLimitNs, kSleepScalarNs);
+            if (!__all_sync(kFull, ok)) {
+                give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                 break;
             }
-
-            // ---- 4. write pass: g = beta p, patched at recorded ids and a ----------
-            const float bw = scal[0];
-            const float beta = scal[1];
-            const float g_a_free = scal[2];
-            const int a_li = m.a_li;
-            const uint16_t* lrow = a.logits + t * a.lstride + lo;
-            float rs = 0.0f;
-#pragma unroll 2
-            for (int j = tid; j < nvb; j += NC) {
-                const uint4 w = ldg_v4_hint(lrow + 8 * j, pol);
-                float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
-                float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
-                float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
-                float g3 = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
-                float g4 = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
-                float g5 = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
-                float g6 = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
-                float g7 = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
-                const uint32_t word = bm[j >> 5];  // same word for the whole warp
-                if (word != 0u && ((word >> (j & 31)) & 1u)) {
-                    auto patch = [&](int q, float v) {
-                        g0 = q == 0 ? v : g0;
-                        g1 = q == 1 ? v : g1;
-                        g2 = q == 2 ? v : g2;
-                        g3 = q == 3 ? v : g3;
-                        g4 = q == 4 ? v : g4;
-                        g5 = q == 5 ? v : g5;
-                        g6 = q == 6 ? v : g6;
-                        g7 = q == 7 ? v : g7;
-                    };
-                    if ((a_li >> 3) == j) patch(a_li & 7, g_a_free);
-                    for (int e = 0; e < nown; ++e) {
-                        const int li = li_s[e];
-                        if ((li >> 3) == j) patch(li & 7, fix_v[e]);
+            {
+                // lane r < C holds CTA r's record; the others hold neutral values
+                const Partial* pp = part + xi * C;
+                const bool have = lane < C;
+                const uint32_t pa = smem_addr(pp + (have ? lane : 0));
+                const uint4 r0 = lds128(pa), r1 = lds128(pa + 16u), r2 = lds128(pa + 32u), r3 = lds128(pa + 48u);
+                const float Pm = have ? __uint_as_float(r0.x) : -INFINITY;
+                const float mg = warp_max(Pm);
+                const float o = mg * kscale;
+                const bool live = Pm > -INFINITY;
+                const float d = live ? Pm * kscale - o : 0.0f;
+                const float f = live ? ex2(d) : 0.0f;
+                const float PS1 = have ? __uint_as_float(r0.y) : 0.0f;
+                const float PS2 = have ? __uint_as_float(r0.z) : 0.0f;
+                const float Prs = have ? __uint_as_float(r0.w) : 0.0f;
+                const float PlH = have ? __uint_as_float(r1.x) : 0.0f;
+                const float PEH = have ? __uint_as_float(r1.y) : 0.0f;
+                const float PQY = have ? __uint_as_float(r1.z) : 0.0f;
+                const int Pnval = have ? static_cast<int>(r2.w) : 0;
+                float lT = f * PS1;
+                float ET = f * fmaf(d, PS1, PS2);
+                float lH = f * PlH;
+                float EH = f * fmaf(d, PlH, PEH);
+                float QYg = 0.0f;
+                if (Pnval > 0) {
+                    const float Qc = (__uint_as_float(r2.y) + __uint_as_float(r1.w)) + __uint_as_float(r2.x);
+                    QYg = fmaf(d, Qc, PQY);
+                }
+                float ya = (have && r3.z) ? __uint_as_float(r3.y) + d : 0.0f;
+                float rsum = Prs;
+                int nval = Pnval;
+                uint32_t flags = have ? r3.x : 0u;
+                HeadMass hm{have ? __uint_as_float(r2.y) : 0.0f, have ? static_cast<int>(r2.z) : 0x7FFFFFFF,
+                            have ? __uint_as_float(r3.w) : 1.0f, have ? __uint_as_float(r1.w) : 0.0f,
+                            have ? __uint_as_float(r2.x) : 0.0f};
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    lT += __shfl_xor_sync(kFull, lT, off);
+                    ET += __shfl_xor_sync(kFull, ET, off);
+                    lH += __shfl_xor_sync(kFull, lH, off);
+                    EH += __shfl_xor_sync(kFull, EH, off);
+                    QYg += __shfl_xor_sync(kFull, QYg, off);
+                    ya += __shfl_xor_sync(kFull, ya, off);
+                    rsum += __shfl_xor_sync(kFull, rsum, off);
+                    nval += __shfl_xor_sync(kFull, nval, off);
+                    flags |= __shfl_xor_sync(kFull, flags, off);
+                    hm = head_merge(hm, head_shfl(hm, off));
+                }
+                // 1 - Q_H without cancellation: (1 - q_max), taken from its
+                // log-probability, minus the others' mass
+                float tail_mu = 1.0f, Q_H = 0.0f;
+                if (nval > 0) {
+                    tail_mu = (hm.omq - hm.oh) - hm.ol;
+                    Q_H = (hm.q + hm.oh) + hm.ol;
+                }
+                const float l = lT + lH;
+                const float log2l = log2f(l);
+                const float P_H = lH / l;
+                const float tail_pi = lT / l;
+                const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
+                if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
+                if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
+                const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
+                const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
+                const float logp_a = (ya - log2l) * kLn2;
+                float wt = 1.0f, k3 = 0.0f;
+                if (a.rollout) {
+                    const float dd = logp_a - m.rl;
+                    k3 = expm1f(dd) - dd;
+                    const float w = expf(dd);
+                    if (a.is_mode == SC_IS_TIS) {
+                        if (w > a.tis_max) {
+                            wt = a.tis_max;
+                            flags |= SC_FLAG_IS_TRUNC;
+                        } else {
+                            wt = w;
+                        }
+                    } else if (a.is_mode == SC_IS_MIS) {
+                        if (w >= a.mis_min && w <= a.mis_max) {
+                            wt = w;
+                        } else {
+                            wt = 0.0f;
+                            flags |= SC_FLAG_IS_REJECT;
+                        }
                     }
                 }
-                rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
-                st_global_v4_hint(grow + 8 * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
-                                  pack_bf16x2(g6, g7), pol);
+                const float A = m.A;
+                const float Aw = A * wt;
+                // sum_H c log p = sum_H q log p - rho sum_H p log p, each from the
+                // merged sums: log p_k = (y_k - log2 l) ln 2.
+                float csum = 0.0f;
+                if (a.centering && nval > 0) {
+                    const float qlogp = kLn2 * fmaf(-log2l, Q_H, QYg);
+                    const float plogp = kLn2 * fmaf(-log2l, lH, EH) / l;
+                    csum = fmaf(-rho, plogp, qlogp);
+                }
+                const float loss = -Aw * (logp_a - csum);
+                const float entropy = kLn2 * (log2l - (ET + EH) / l);
+                const float alpha = -a.grad_scale * a.inv_t * Aw;
+                const float beta = -alpha * s;
+                const float bw = o + log2l;
+                const float g_a_free = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
+                // gradient at the owned recorded ids, and how far it is from the
+                // beta p the write pass stores there (the row sum's correction)
+                float* fv = fix_v + p * cap;
+                float corr = 0.0f;
+                bool a_rec = false;
+                for (int e = lane; e < nown; e += 32) {
+                    const float pe = ex2(fmaf(fz[e], kscale, -o) - log2l);
+                    const float mu = a.centering ? fmaf(dsr, pe, expf(lp_s[e])) : pe;
+                    const bool is_a = li_s[e] == a_li;
+                    const float g = alpha * ((is_a ? 1.0f : 0.0f) - mu);
+                    fv[e] = g;
+                    corr += g - beta * ex2(fmaf(fz[e], kscale, -bw));
+                    a_rec = a_rec || is_a;
+                }
+                corr = warp_sum(corr);
+                if (a_li >= 0 && !__any_sync(kFull, a_rec))
+                    corr += g_a_free - beta * ex2(fmaf(zav[p], kscale, -bw));
+                corr_m2 = corr_m1;
+                corr_m1 = corr;
+                if (lane == 0) {
+                    float* sc = scal + 4 * p;
+                    sc[0] = bw;
+                    sc[1] = beta;
+                    sc[2] = g_a_free;
+                    if (crank == 0) {
+                        a.logp[m.t] = logp_a;
+                        if (a.diag) {  // the record in field order, as four 16-byte stores
+                            float4* dp = reinterpret_cast<float4*>(a.diag + m.t);
+                            dp[0] = make_float4(loss, logp_a, P_H, tail_pi);
+                            dp[1] = make_float4(Q_H, tail_mu, rho, s);
+                            dp[2] = make_float4(entropy, k3, wt, 0.0f);
+                            dp[3] = make_float4(A, __int_as_float(nval), __uint_as_float(flags), 0.0f);
+                            // the records of row j carried the row sums of row j - 2
+                            if (j >= 2) a.diag[t_m2].row_sum = rsum;
+                        }
+                        if (flags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready(p));
             }
-            if (tail && tid == 0) {
-                for (int q = 0; q < tail; ++q) {
-                    const int li = n8 + q;
-                    float g = li == a_li ? g_a_free : beta * ex2(fmaf(bf_to_f(lrow[li]), kscale, -bw));
-                    for (int e = 0; e < nown; ++e)
-                        if (li_s[e] == li) g = fix_v[e];
-                    rs += g;
-                    grow[li] = f_to_bf_bits(g);
+            t_m2 = t_m1;
+            t_m1 = m.t;
+        }
+    } else {
+        // ================= streaming warps: phase A of row i, write pass of row i - 1 =================
+        for (uint32_t i = 0;; ++i) {
+            if (flag_up()) break;
+            const int ms = static_cast<int>(i % kMetaSlots);
+            const bool got =
+                mbar_wait_sleepy(meta_bar(ms, kMetaFull), (i / kMetaSlots) & 1u, kWaitLimitNs, kSleepStreamNs);
+            if (!__all_sync(kFull, got)) {
+                give_up(SC_STATUS_TIMEOUT_LOAD);
+                break;
+            }
+            const RowMeta m = meta[ms];
+            const bool have_cur = m.t >= 0;
+            if (have_cur) {
+                // ------------- phase A: one pass over the slice in shared memory -------------
+                const int p = static_cast<int>(i & 1u);
+                const int ds = static_cast<int>(i % NB);
+                const uint32_t fpar = (i / NB) & 1u;
+                const uint32_t buf_s = smem_addr(smem + ds * L.stage_bytes);
+                const int* li_s = list_li + ms * cap;
+                const uint32_t* bm = bitmap + ms * nwords;
+                const int nown = m.nown, a_li = m.a_li;
+                // running maximum and the sums over the unrecorded entries (vectors
+                // holding a recorded id take the rare per-entry path)
+                float mt = -INFINITY;
+                float s1a = 0.0f, s1b = 0.0f, s1c = 0.0f, s1d = 0.0f;
+                float s2a = 0.0f, s2b = 0.0f, s2c = 0.0f, s2d = 0.0f;
+                bool timed_out = false;
+                for (int c = 0; c < nchunks; ++c) {
+                    if (!mbar_wait_sleepy(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs, kSleepStreamNs)) {
+                        timed_out = true;
+                        break;
+                    }
+                    const int v1 = min((c + 1) * a.ncv, nvb);
+#pragma unroll 2
+                    for (int j = c * a.ncv + tid; j < v1; j += NC) {
+                        const uint4 w = lds128(buf_s + 16u * j);
+                        const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+                        const float vm = fmaxf(bf_lo(mx), bf_hi(mx));
+                        if (vm > mt) {  // new running maximum: rescale the sums
+                            if (mt > -INFINITY) {
+                                const float d = (mt - vm) * kscale;
+                                const float f = ex2(d);
+                                s2a = f * fmaf(d, s1a, s2a);
+                                s2b = f * fmaf(d, s1b, s2b);
+                                s2c = f * fmaf(d, s1c, s2c);
+                                s2d = f * fmaf(d, s1d, s2d);
+                                s1a *= f;
+                                s1b *= f;
+                                s1c *= f;
+                                s1d *= f;
+                            }
+                            mt = vm;
+                        }
+                        const float o = mt * kscale;
+                        const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                        if (rbits == 0u) {
+                            float y0 = fmaf(bf_lo(w.x), kscale, -o), y1 = fmaf(bf_hi(w.x), kscale, -o);
+                            float e0 = ex2(y0), e1 = ex2(y1);
+                            s1a += e0 + e1;
+                            s2a = fmaf(e0, y0, fmaf(e1, y1, s2a));
+                            y0 = fmaf(bf_lo(w.y), kscale, -o);
+                            y1 = fmaf(bf_hi(w.y), kscale, -o);
+                            e0 = ex2(y0);
+                            e1 = ex2(y1);
+                            s1b += e0 + e1;
+                            s2b = fmaf(e0, y0, fmaf(e1, y1, s2b));
+                            y0 = fmaf(bf_lo(w.z), kscale, -o);
+                            y1 = fmaf(bf_hi(w.z), kscale, -o);
+                            e0 = ex2(y0);
+                            e1 = ex2(y1);
+                            s1c += e0 + e1;
+                            s2c = fmaf(e0, y0, fmaf(e1, y1, s2c));
+                            y0 = fmaf(bf_lo(w.w), kscale, -o);
+                            y1 = fmaf(bf_hi(w.w), kscale, -o);
+                            e0 = ex2(y0);
+                            e1 = ex2(y1);
+                            s1d += e0 + e1;
+                            s2d = fmaf(e0, y0, fmaf(e1, y1, s2d));
+                        } else {
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float z = (q & 1) ? bf_hi(ww[q >> 1]) : bf_lo(ww[q >> 1]);
+                                if (!((rbits >> q) & 1u)) {
+                                    const float y = fmaf(z, kscale, -o);
+                                    const float e = ex2(y);
+                                    s1a += e;
+                                    s2a = fmaf(e, y, s2a);
+                                }
+                            }
+                        }
+                    }
+                }
+                if (tail && tid == 0 && !timed_out) {  // entries past the last whole vector
+                    const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                    for (int q = 0; q < tail; ++q) {
+                        const float z = bf_to_f(lrow[n8 + q]);
+                        const int li = n8 + q;
+                        if (z > mt) {
+                            if (mt > -INFINITY) {
+                                const float d = (mt - z) * kscale;
+                                const float f = ex2(d);
+                                s2a = f * fmaf(d, s1a, s2a);
+                                s2b = f * fmaf(d, s1b, s2b);
+                                s2c = f * fmaf(d, s1c, s2c);
+                                s2d = f * fmaf(d, s1d, s2d);
+                                s1a *= f;
+                                s1b *= f;
+                                s1c *= f;
+                                s1d *= f;
+                            }
+                            mt = z;
+                        }
+                        if (!((bm[li >> 5] >> (li & 31)) & 1u)) {
+                            const float y = fmaf(z, kscale, -mt * kscale);
+                            const float e = ex2(y);
+                            s1a += e;
+                            s2a = fmaf(e, y, s2a);
+                        }
+                    }
+                }
+                if (__any_sync(kFull, timed_out)) {
+                    give_up(SC_STATUS_TIMEOUT_LOAD);
+                    break;
+                }
+                {  // the recorded ids' logits and a's (every chunk has landed for this thread)
+                    const uint16_t* buf = reinterpret_cast<const uint16_t*>(smem + ds * L.stage_bytes);
+                    const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                    float* fz = fix_z + p * cap;
+                    for (int e = tid; e < nown; e += NC) {
+                        const int li = li_s[e];
+                        fz[e] = bf_to_f(li < n8 ? buf[li] : lrow[li]);
+                    }
+                    if (tid == NC - 1 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? buf[a_li] : lrow[a_li]);
+                }
+                Mass ms_acc{mt, (s1a + s1b) + (s1c + s1d), (s2a + s2b) + (s2c + s2d)};
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) ms_acc = mass_merge(ms_acc, mass_shfl(ms_acc, off), kscale);
+                if (lane == 0) {
+                    float* rp = red + p * 3 * NCW;
+                    rp[warp] = ms_acc.m;
+                    rp[NCW + warp] = ms_acc.s1;
+                    rp[2 * NCW + warp] = ms_acc.s2;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(adone(p));
+                    // the slice has served its pass: the next row may stream in
+                    for (int c = 0; c < nchunks; ++c) mbar_arrive(data_bar(ds, kChunkFree + c));
                 }
             }
-            rs = warp_sum(rs);
-            if (lane == 0) red[3 * NCW + warp] = rs;
-            named_bar(NC);
-            if (tid == 0) {
-                float tot = 0.0f;
-                for (int w = 0; w < NCW; ++w) tot += red[3 * NCW + w];
-                rs_prev = tot;
-                mbar_arrive(meta_bar(ms, kMetaFree));  // the slot's list and bitmap are free
+            if (i > 0) {
+                // ---- write pass of row i - 1: the slice again from L2, g = beta p (the
+                // special entries are patched by the scalar warp afterwards) ----
+                const uint32_t ip = i - 1;
+                const int pp = static_cast<int>(ip & 1u);
+                const int msp = static_cast<int>(ip % kMetaSlots);
+                const RowMeta mp = meta[msp];
+                const uint16_t* lrow = a.logits + mp.t * a.lstride + lo;
+                uint16_t* grow = a.grad + mp.t * a.gstride + lo;
+                const bool ready = mbar_wait_sleepy(sready(pp), (ip >> 1) & 1u, kWaitLimitNs, kSleepStreamNs);
+                if (!__all_sync(kFull, ready)) {
+                    give_up(SC_STATUS_TIMEOUT_EXCHANGE);
+                    break;
+                }
+                const float bw = scal[4 * pp + 0];
+                const float beta = scal[4 * pp + 1];
+                float rs = 0.0f;
+#pragma unroll 2
+                for (int j = tid; j < nvb; j += NC) {
+                    const uint4 w = ldg_v4_hint(lrow + 8 * j, pol);
+                    const float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
+                    const float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
+                    const float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
+                    const float g3 = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
+                    const float g4 = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
+                    const float g5 = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
+                    const float g6 = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
+                    const float g7 = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
+                    rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
+                    st_global_v4_hint(grow + 8 * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
+                                      pack_bf16x2(g6, g7), pol);
+                }
+                if (tail && tid == 0) {
+                    for (int q = 0; q < tail; ++q) {
+                        const int li = n8 + q;
+                        const float g = beta * ex2(fmaf(bf_to_f(lrow[li]), kscale, -bw));
+                        rs += g;
+                        grow[li] = f_to_bf_bits(g);
+                    }
+                }
+                rs = warp_sum(rs);
+                if (lane == 0) rsw[pp * NCW + warp] = rs;
             }
-            t_prev = t;
-            ++nmeta;
-            ++ndata;
+            if (!have_cur) {  // end of the stream: every row of this warp is written
+                __syncwarp();
+                if (lane == 0) mbar_arrive(adone(static_cast<int>(i & 1u)));
+                break;
+            }
         }
-        t_last = t_prev;
-        rs_last = rs_prev;
     }
 
-    // The row sum of the last valid row goes to CTA 0 over DSMEM; the final
-    // cluster barrier also keeps every CTA's shared memory alive until no
-    // peer can still write to it.
-    if (tid == 0 && a.diag && t_last >= 0 && !aborted) {
-        const uint32_t fs = smem_addr(frs + crank);
-        st_cluster_v2(map_to_rank(fs, 0), __float_as_uint(rs_last), 0u);
-    }
+    // The row sums of the last two rows go to CTA 0 over DSMEM (the earlier
+    // ones rode with later records); the final cluster barrier also keeps
+    // every CTA's shared memory alive until no peer can still write to it.
+    if (warp == NCW && lane == 0 && a.diag && clean_end)
+        st_cluster_v2(map_to_rank(smem_addr(frs + crank), 0), __float_as_uint(fin_rs2), __float_as_uint(fin_rs1));
     cluster_sync_all();
-    if (crank == 0 && tid == 0 && a.diag && t_last >= 0 && !aborted) {
-        float rsum = 0.0f;
-        for (int r = 0; r < C; ++r) rsum += frs[r].x;
-        a.diag[t_last].row_sum = rsum;
+    if (crank == 0 && warp == NCW && lane == 0 && a.diag && clean_end) {
+        float s2 = 0.0f, s1 = 0.0f;
+        for (int r = 0; r < C; ++r) {
+            s2 += frs[r].x;
+            s1 += frs[r].y;
+        }
+        if (nrows >= 2) a.diag[t_m2].row_sum = s2;
+        if (nrows >= 1) a.diag[t_m1].row_sum = s1;
     }
 }
 
@@ -878,45 +994,47 @@ __global__ void __launch_bounds__(NC + 32, min_blocks(NC)) center_kernel(const _
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 struct Plan {
-    int C, NC, S, ncv, NB, MS;
+    int C, NC, S, ncv, NB;
     Layout L;
 };
 
-Layout make_layout(int S, int K_max, int NC, int NB, int MS, int C) {
+Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     Layout L;
     L.stage_bytes = round_up(S * 2, 128);
     L.list_cap = K_max > 0 ? K_max : 1;
-    L.nwords = (S / 8 + 31) / 32;
+    L.nwords = (S + 31) / 32;
     int off = NB * L.stage_bytes;
     auto take = [&](int bytes) {
         const int o = off;
         off = round_up(off + bytes, 16);
         return o;
     };
-    L.off_meta = take(MS * static_cast<int>(sizeof(RowMeta)));
-    L.off_list_li = take(MS * L.list_cap * 4);
-    L.off_list_lp = take(MS * L.list_cap * 4);
-    L.off_list_k = take(MS * L.list_cap * 4);
-    L.off_bitmap = take(MS * L.nwords * 4);
+    L.off_meta = take(kMetaSlots * static_cast<int>(sizeof(RowMeta)));
+    L.off_list_li = take(kMetaSlots * L.list_cap * 4);
+    L.off_list_lp = take(kMetaSlots * L.list_cap * 4);
+    L.off_list_k = take(kMetaSlots * L.list_cap * 4);
+    L.off_bitmap = take(kMetaSlots * L.nwords * 4);
     L.off_bars = take(kNumBars * 8);
-    L.off_part = take(2 * C * static_cast<int>(sizeof(Partial)));
+    L.off_part = take(kXBufs * C * static_cast<int>(sizeof(Partial)));
     L.off_mine = take(static_cast<int>(sizeof(Partial)));
     L.off_frs = take(kMaxCluster * 8);
-    L.off_fixz = take(L.list_cap * 4);
-    L.off_fixv = take(L.list_cap * 4);
-    L.off_red = take(4 * (NC / 32) * 4);
-    L.off_scal = take(8 * 4);
+    L.off_fixz = take(2 * L.list_cap * 4);
+    L.off_fixv = take(2 * L.list_cap * 4);
+    L.off_zav = take(2 * 4);
+    L.off_red = take(2 * 3 * (NC / 32) * 4);
+    L.off_rsw = take(2 * (NC / 32) * 4);
+    L.off_scal = take(2 * 4 * 4);
+    L.off_flag = take(4);
     L.total = off;
     return L;
 }
 
 // Automatic plan: about 40 KiB of logits per CTA (clusters of up to 16
-// CTAs), one data stage whose 4 KiB chunks are recycled as the write pass
-// frees them, a two-slot metadata ring, 256 compute threads (128 for small
+// CTAs), one data stage that the next row refills while the write pass of
+// the previous row runs from L2, 256 compute threads (128 for small
 // slices).  For the 151936-entry vocabulary: 8 CTAs x 18992 entries.
 int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
     const int NB = req_stages > 0 ? req_stages : 1;
-    const int MS = NB + 1;
     int C = req_cluster;
     auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128); };
     if (C <= 0) {
@@ -926,22 +1044,21 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
     }
     const int S = round_up((V + C - 1) / C, 8);
     const int NC = threads_for(S);
-    const Layout L = make_layout(S, K_max, NC, NB, MS, C);
+    const Layout L = make_layout(S, K_max, NC, NB, C);
     if (L.total > kMaxSmem)
         return fail(SC_ERR_SHAPE,
                     "V = %d with cluster size %d and %d stages needs %d bytes of shared memory per CTA", V, C,
                     NB, L.total);
     const int nvb = S / 8;
-    int nch = (nvb + kChunkVecTarget - 1) / kChunkVecTarget;
-    nch = nch < 1 ? 1 : (nch > kMaxChunks ? kMaxChunks : nch);
     out->C = C;
     out->NC = NC;
     out->S = S;
     out->NB = NB;
-    out->MS = MS;
-    // a whole number of 32-vector groups per chunk keeps each warp's bitmap word uniform
-    out->ncv = round_up((nvb + nch - 1) / nch, 32);
-    if (out->ncv < 32) out->ncv = 32;
+    // chunks of a whole number of passes of the compute threads (every thread
+    // has the same share of each chunk), at most kMaxChunks of them
+    int ncv = NC * (kChunkVecTarget / NC > 1 ? kChunkVecTarget / NC : 1);
+    if ((nvb + ncv - 1) / ncv > kMaxChunks) ncv = round_up((nvb + kMaxChunks - 1) / kMaxChunks, NC);
+    out->ncv = ncv;
     out->L = L;
     return SC_OK;
 }
@@ -987,7 +1104,7 @@ int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.C, 1, 1);
-    cfg.blockDim = dim3(P.NC + 32, 1, 1);
+    cfg.blockDim = dim3(P.NC + 64, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1138,12 +1255,11 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.S = P.S;
     ka.ncv = P.ncv;
     ka.NB = P.NB;
-    ka.MS = P.MS;
     ka.L = P.L;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(G * P.C), 1, 1);
-    cfg.blockDim = dim3(P.NC + 32, 1, 1);
+    cfg.blockDim = dim3(P.NC + 64, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];

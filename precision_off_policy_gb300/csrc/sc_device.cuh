@@ -118,6 +118,29 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
     }
 }
 
+// Bounded waits for waiters off the critical path: between polls the warp
+// sleeps, leaving its issue slots to the warps that do the streaming work.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                 uint32_t sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+__device__ __forceinline__ bool mbar_wait_cluster_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                         uint32_t sleep_ns) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // ---- bulk copies (TMA engine, 1-D) ------------------------------------
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
