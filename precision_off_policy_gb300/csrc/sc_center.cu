@@ -63,9 +63,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
-constexpr uint32_t kSleepProducerNs = 128;  // polling interval of the producer's waits
-constexpr uint32_t kSleepScalarNs = 32;     // polling interval of the scalar warp's waits
-constexpr uint32_t kSleepStreamNs = 32;     // polling interval of the streaming warps' waits
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 // One valid row as the producer hands it to the consumers.
@@ -385,8 +382,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 }
                 const int ms = static_cast<int>(nfill % kMetaSlots);
                 if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
-                    !mbar_wait_sleepy(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs,
-                                      kSleepProducerNs)) {
+                    !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs)) {
                     if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                     stop = true;
                     break;
@@ -472,7 +468,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
                     for (int i = 0; i < nchunks; ++i) {
                         if (reuse &&
-                            !mbar_wait_sleepy(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs, kSleepProducerNs)) {
+                            !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
                             status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                             for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
                                 (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
@@ -498,8 +494,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
             const int ms = static_cast<int>(nfill % kMetaSlots);
             bool ok = true;
             if (nfill >= static_cast<uint32_t>(kMetaSlots))
-                ok = mbar_wait_sleepy(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs,
-                                      kSleepProducerNs);
+                ok = mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs);
             if (ok) {
                 if (lane == 0) {
                     meta[ms].t = -1;
@@ -522,7 +517,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
         for (uint32_t j = 0;; ++j) {
             if (flag_up()) break;
             const int p = static_cast<int>(j & 1u);
-            const bool got = mbar_wait_sleepy(adone(p), (j >> 1) & 1u, kWaitLimitNs, kSleepScalarNs);
+            const bool got = mbar_wait_bounded(adone(p), (j >> 1) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, got)) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
@@ -563,6 +558,11 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                                      : Mass{-INFINITY, 0.0f, 0.0f};
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) cm = mass_merge(cm, mass_shfl(cm, off), kscale);
+                {  // the owned recorded logits may lie above the streaming offset
+                    float zmax = -INFINITY;
+                    for (int e = lane; e < nown; e += 32) zmax = fmaxf(zmax, fz[e]);
+                    cm = mass_merge(cm, Mass{warp_max(zmax), 0.0f, 0.0f}, kscale);
+                }
                 const float o_c = cm.m * kscale;
                 float lH = 0.0f, EH = 0.0f, QY = 0.0f;
                 int nval = 0;
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 }
             }
             // ---- all C records of row j: the row scalars ----
-            const bool ok = mbar_wait_cluster_sleepy(xbar(xi), (j >> 2) & 1u, kWaitLimitNs, kSleepScalarNs);
+            const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j >> 2) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, ok)) {
                 give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                 break;
@@ -775,7 +775,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
             if (flag_up()) break;
             const int ms = static_cast<int>(i % kMetaSlots);
             const bool got =
-                mbar_wait_sleepy(meta_bar(ms, kMetaFull), (i / kMetaSlots) & 1u, kWaitLimitNs, kSleepStreamNs);
+                mbar_wait_bounded(meta_bar(ms, kMetaFull), (i / kMetaSlots) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, got)) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
@@ -791,14 +791,29 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const int* li_s = list_li + ms * cap;
                 const uint32_t* bm = bitmap + ms * nwords;
                 const int nown = m.nown, a_li = m.a_li;
-                // running maximum and the sums over the unrecorded entries (vectors
-                // holding a recorded id take the rare per-entry path)
-                float mt = -INFINITY;
+                // The exponent offset is the largest logit among the warp's first
+                // vectors, fixed for the whole pass: no running maximum to keep up
+                // to date.  Entries far above it would overflow 2^y, so a thread whose
+                // sums come out too large or not finite redoes its own vectors
+                // exactly (its maximum first).  Vectors holding a recorded id take
+                // the rare per-entry path.
+                bool timed_out = false;
+                float mz = -INFINITY;
+                if (nchunks > 0) {
+                    timed_out = !mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, kWaitLimitNs);
+                    if (!timed_out && tid < nvb) {
+                        const uint4 w = lds128(buf_s + 16u * tid);
+                        const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+                        mz = fmaxf(bf_lo(mx), bf_hi(mx));
+                    }
+                }
+                mz = warp_max(mz);
+                const bool fast = mz > -INFINITY;
+                const float o = fast ? mz * kscale : 0.0f;
                 float s1a = 0.0f, s1b = 0.0f, s1c = 0.0f, s1d = 0.0f;
                 float s2a = 0.0f, s2b = 0.0f, s2c = 0.0f, s2d = 0.0f;
-                bool timed_out = false;
-                for (int c = 0; c < nchunks; ++c) {
-                    if (!mbar_wait_sleepy(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs, kSleepStreamNs)) {
+                for (int c = 0; c < nchunks && !timed_out; ++c) {
+                    if (!mbar_wait_bounded(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs)) {
                         timed_out = true;
                         break;
                     }
@@ -806,24 +821,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
 #pragma unroll 2
                     for (int j = c * a.ncv + tid; j < v1; j += NC) {
                         const uint4 w = lds128(buf_s + 16u * j);
-                        const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-                        const float vm = fmaxf(bf_lo(mx), bf_hi(mx));
-                        if (vm > mt) {  // new running maximum: rescale the sums
-                            if (mt > -INFINITY) {
-                                const float d = (mt - vm) * kscale;
-                                const float f = ex2(d);
-                                s2a = f * fmaf(d, s1a, s2a);
-                                s2b = f * fmaf(d, s1b, s2b);
-                                s2c = f * fmaf(d, s1c, s2c);
-                                s2d = f * fmaf(d, s1d, s2d);
-                                s1a *= f;
-                                s1b *= f;
-                                s1c *= f;
-                                s1d *= f;
-                            }
-                            mt = vm;
-                        }
-                        const float o = mt * kscale;
                         const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
                         if (rbits == 0u) {
                             float y0 = fmaf(bf_lo(w.x), kscale, -o), y1 = fmaf(bf_hi(w.x), kscale, -o);
@@ -863,32 +860,43 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         }
                     }
                 }
+                Mass ms_acc{mz, (s1a + s1b) + (s1c + s1d), (s2a + s2b) + (s2c + s2d)};
+                if (!timed_out && !(fast && ms_acc.s1 <= 0x1p100f && fabsf(ms_acc.s2) <= 0x1p110f)) {
+                    // exact: this thread's maximum, then its sums relative to it (also
+                    // the path of -inf logits, whose 0 * -inf made the fast sums NaN)
+                    float mx = -INFINITY;
+                    for (int j = tid; j < nvb; j += NC) {
+                        const uint4 w = lds128(buf_s + 16u * j);
+                        const uint32_t m2 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+                        mx = fmaxf(mx, fmaxf(bf_lo(m2), bf_hi(m2)));
+                    }
+                    float s1 = 0.0f, s2 = 0.0f;
+                    if (mx > -INFINITY) {
+                        const float ox = mx * kscale;
+                        for (int j = tid; j < nvb; j += NC) {
+                            const uint4 w = lds128(buf_s + 16u * j);
+                            const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                if ((rbits >> q) & 1u) continue;
+                                // (clamped so that a -inf logit adds 0, not 0 * -inf)
+                                const float y = fmaxf(
+                                    fmaf((q & 1) ? bf_hi(ww[q >> 1]) : bf_lo(ww[q >> 1]), kscale, -ox), -1024.0f);
+                                const float e = ex2(y);
+                                s1 += e;
+                                s2 = fmaf(e, y, s2);
+                            }
+                        }
+                    }
+                    ms_acc = Mass{mx, s1, s2};
+                }
                 if (tail && tid == 0 && !timed_out) {  // entries past the last whole vector
                     const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
                     for (int q = 0; q < tail; ++q) {
-                        const float z = bf_to_f(lrow[n8 + q]);
                         const int li = n8 + q;
-                        if (z > mt) {
-                            if (mt > -INFINITY) {
-                                const float d = (mt - z) * kscale;
-                                const float f = ex2(d);
-                                s2a = f * fmaf(d, s1a, s2a);
-                                s2b = f * fmaf(d, s1b, s2b);
-                                s2c = f * fmaf(d, s1c, s2c);
-                                s2d = f * fmaf(d, s1d, s2d);
-                                s1a *= f;
-                                s1b *= f;
-                                s1c *= f;
-                                s1d *= f;
-                            }
-                            mt = z;
-                        }
-                        if (!((bm[li >> 5] >> (li & 31)) & 1u)) {
-                            const float y = fmaf(z, kscale, -mt * kscale);
-                            const float e = ex2(y);
-                            s1a += e;
-                            s2a = fmaf(e, y, s2a);
-                        }
+                        if (!((bm[li >> 5] >> (li & 31)) & 1u))
+                            ms_acc = mass_merge(ms_acc, Mass{bf_to_f(lrow[li]), 1.0f, 0.0f}, kscale);
                     }
                 }
                 if (__any_sync(kFull, timed_out)) {
@@ -905,7 +913,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     }
                     if (tid == NC - 1 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? buf[a_li] : lrow[a_li]);
                 }
-                Mass ms_acc{mt, (s1a + s1b) + (s1c + s1d), (s2a + s2b) + (s2c + s2d)};
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) ms_acc = mass_merge(ms_acc, mass_shfl(ms_acc, off), kscale);
                 if (lane == 0) {
@@ -930,7 +937,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const RowMeta mp = meta[msp];
                 const uint16_t* lrow = a.logits + mp.t * a.lstride + lo;
                 uint16_t* grow = a.grad + mp.t * a.gstride + lo;
-                const bool ready = mbar_wait_sleepy(sready(pp), (ip >> 1) & 1u, kWaitLimitNs, kSleepStreamNs);
+                const bool ready = mbar_wait_bounded(sready(pp), (ip >> 1) & 1u, kWaitLimitNs);
                 if (!__all_sync(kFull, ready)) {
                     give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                     break;

@@ -97,13 +97,39 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware until the phase completes or `hint_ns` passes, so a
+// waiting warp takes no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded waits: give up after `limit_ns` of wall time and return false.
+constexpr uint32_t kSuspendHintNs = 100000;  // longest single hardware suspension
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
@@ -112,31 +138,7 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
-    }
-}
-
-// Bounded waits for waiters off the critical path: between polls the warp
-// sleeps, leaving its issue slots to the warps that do the streaming work.
-__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                 uint32_t sleep_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        __nanosleep(sleep_ns);
-        if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > limit_ns) return false;
-    }
-}
-__device__ __forceinline__ bool mbar_wait_cluster_sleepy(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                         uint32_t sleep_ns) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        __nanosleep(sleep_ns);
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (mbar_try_wait_cluster_hint(bar, parity, kSuspendHintNs)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }

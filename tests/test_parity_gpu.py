@@ -245,6 +245,39 @@ def test_empty_batch_and_empty_head_parameter():
     _full_check(b, sc_params(b, K_max=0), "K_max=0")
 
 
+def _unprotected(batch):
+    """Mask of the entries that are neither recorded ids nor the sampled token."""
+    T, V = batch["logits"].shape
+    keep = torch.ones(T, V, dtype=torch.bool)
+    ids = batch["rec_ids"].long()
+    ok = (ids >= 0) & (ids < V)
+    keep.scatter_(1, torch.where(ok, ids, torch.zeros_like(ids)), False)
+    keep[torch.arange(T), batch["sampled"].long()] = False
+    return keep
+
+
+@pytest.mark.parametrize("cluster,threads", [(0, 0), (2, 128)])
+def test_wide_dynamic_range_and_infinite_logits(cluster, threads):
+    """Entries far above the exponent offset a warp takes from its first vectors
+    (2^y would overflow), -inf entries (0 * -inf), and warps whose first vectors
+    are all -inf: each takes the exact per-thread path and must still match."""
+    batch = synth.make_batch(synth.config("C1", V=8192, L_pad=8))
+    z = batch["logits"].float().clone()
+    free = _unprotected(batch)
+    row0 = torch.zeros_like(free[0])
+    row0[6000:6003] = True                     # row 0: three entries at +120
+    z[0, row0 & free[0]] = 120.0
+    row3 = torch.zeros_like(free[3])
+    row3[4000:4100] = True                     # row 3: a block at +90
+    z[3, row3 & free[3]] = 90.0
+    neg = torch.zeros_like(free)
+    neg[1, 100:200] = True                     # row 1: scattered -inf
+    neg[2, :2048] = True                       # row 2: the first 2048 entries -inf
+    z[neg & free] = float("-inf")
+    b = _edit(batch, logits=z.to(torch.bfloat16))
+    _full_check(b, sc_params(b, cluster_size=cluster, threads=threads), f"dynamic range {cluster},{threads}")
+
+
 def test_row_stride_larger_than_vocab():
     batch = synth.make_batch(synth.config("C1", V=1000, L_pad=8))
     T = batch["logits"].shape[0]
