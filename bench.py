@@ -46,7 +46,7 @@ WORKLOAD_TEXT = ("quick-check batch: 2 prompts x 4 responses x 512 tokens = 4096
                  "padded, V=151936, K=128, logits N(0,3^2)+Zipf bias, sampler noise N(0,0.05^2)")
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["precision_off_policy_gb300/csrc/sc_center.cu", "precision_off_policy_gb300/csrc/sc_device.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "center_kernel_C2_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "center_kernel_C2_traffic.txt")
 
 
 def kernel_source_hash() -> str:
@@ -67,16 +67,24 @@ def hbm_peak():
 
 
 def measured_traffic(launch_rows: int):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+    """DRAM bytes per launch from the committed ncu summary (`key: value`
+    lines), if it was taken on the current kernel source; else None."""
+    t = {}
     try:
         with open(TRAFFIC_FILE) as f:
-            t = json.load(f)
-    except (OSError, ValueError):
+            for line in f:
+                if line.startswith("#") or ":" not in line:
+                    continue
+                k, v = line.split(":", 1)
+                t[k.strip()] = v.strip()
+    except OSError:
         return None
     if t.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return float(t["dram_bytes_per_launch"]) * launch_rows / float(t["rows_per_launch"])
+    try:
+        return float(t["dram_bytes_per_launch"]) * launch_rows / float(t["rows_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 class ClockSampler:

@@ -924,8 +924,10 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(adone(p));
-                    // the slice has served its pass: the next row may stream in
-                    for (int c = 0; c < nchunks; ++c) mbar_arrive(data_bar(ds, kChunkFree + c));
+                    // one stage: the slice has served its pass, the next row may stream
+                    // in (the write pass reads it again from L2)
+                    if (NB == 1)
+                        for (int c = 0; c < nchunks; ++c) mbar_arrive(data_bar(ds, kChunkFree + c));
                 }
             }
             if (i > 0) {
@@ -945,9 +947,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const float bw = scal[4 * pp + 0];
                 const float beta = scal[4 * pp + 1];
                 float rs = 0.0f;
-#pragma unroll 2
-                for (int j = tid; j < nvb; j += NC) {
-                    const uint4 w = ldg_v4_hint(lrow + 8 * j, pol);
+                auto emit = [&](int j, const uint4& w) {  // 8 gradients from 8 logits
                     const float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
                     const float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
                     const float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
@@ -959,6 +959,22 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
                     st_global_v4_hint(grow + 8 * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
                                       pack_bf16x2(g6, g7), pol);
+                };
+                if (NB > 1) {
+                    // the slice is still in its stage: read it there and hand each
+                    // chunk back to the producer as soon as this warp is done with it
+                    const int dsp = static_cast<int>(ip % NB);
+                    const uint32_t bufp = smem_addr(smem + dsp * L.stage_bytes);
+                    for (int c = 0; c < nchunks; ++c) {
+                        const int v1 = min((c + 1) * a.ncv, nvb);
+#pragma unroll 2
+                        for (int j = c * a.ncv + tid; j < v1; j += NC) emit(j, lds128(bufp + 16u * j));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(data_bar(dsp, kChunkFree + c));
+                    }
+                } else {
+#pragma unroll 2
+                    for (int j = tid; j < nvb; j += NC) emit(j, ldg_v4_hint(lrow + 8 * j, pol));
                 }
                 if (tail && tid == 0) {
                     for (int q = 0; q < tail; ++q) {
@@ -1036,16 +1052,19 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     return L;
 }
 
-// Automatic plan: about 40 KiB of logits per CTA (clusters of up to 16
+// Automatic plan: about 80 KiB of logits per CTA (clusters of up to 16
 // CTAs), one data stage that the next row refills while the write pass of
-// the previous row runs from L2, 256 compute threads (128 for small
-// slices).  For the 151936-entry vocabulary: 8 CTAs x 18992 entries.
+// the previous row runs from L2, 512 compute threads (256 or 128 for small
+// slices).  For the 151936-entry vocabulary: 4 CTAs x 37984 entries, two
+// CTAs per SM.
 int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
     const int NB = req_stages > 0 ? req_stages : 1;
     int C = req_cluster;
-    auto threads_for = [&](int S) { return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128); };
+    auto threads_for = [&](int S) {
+        return req_threads > 0 ? req_threads : (S >= 24576 ? 512 : (S >= 8192 ? 256 : 128));
+    };
     if (C <= 0) {
-        C = static_cast<int>((2LL * V + 40959) / 40960);
+        C = static_cast<int>((2LL * V + 81919) / 81920);
         C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
         while (C > 1 && static_cast<long long>(C - 1) * round_up((V + C - 1) / C, 8) >= V) --C;
     }
