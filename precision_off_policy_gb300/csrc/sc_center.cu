@@ -58,7 +58,7 @@ constexpr int kXBufs = 4;      // exchange buffers (peers may run ahead by a row
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
-constexpr int kChunkVecTarget = 256;    // 16-byte vectors per bulk copy (4 KiB)
+constexpr int kChunkVecTarget = 1024;   // 16-byte vectors per bulk copy (16 KiB)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
@@ -791,18 +791,20 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const int* li_s = list_li + ms * cap;
                 const uint32_t* bm = bitmap + ms * nwords;
                 const int nown = m.nown, a_li = m.a_li;
-                // The exponent offset is the largest logit among the warp's first
-                // vectors, fixed for the whole pass: no running maximum to keep up
-                // to date.  Entries far above it would overflow 2^y, so a thread whose
-                // sums come out too large or not finite redoes its own vectors
-                // exactly (its maximum first).  Vectors holding a recorded id take
-                // the rare per-entry path.
+                // The exponent offset is the largest logit among the slice's first 32
+                // vectors -- every warp reads the same ones and reduces them the same
+                // way, so the whole CTA shares it without a barrier -- fixed for the
+                // whole pass: no running maximum to keep up to date, and the warp's
+                // sums add up plainly.  Entries far above it would overflow 2^y, so a
+                // thread whose sums come out too large or not finite redoes its own
+                // vectors exactly (its maximum first).  Vectors holding a recorded id
+                // take the rare per-entry path.
                 bool timed_out = false;
                 float mz = -INFINITY;
                 if (nchunks > 0) {
                     timed_out = !mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, kWaitLimitNs);
-                    if (!timed_out && tid < nvb) {
-                        const uint4 w = lds128(buf_s + 16u * tid);
+                    if (!timed_out && lane < nvb) {
+                        const uint4 w = lds128(buf_s + 16u * lane);
                         const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
                         mz = fmaxf(bf_lo(mx), bf_hi(mx));
                     }
@@ -860,8 +862,21 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         }
                     }
                 }
+                if (tail && tid == 0 && !timed_out) {  // entries past the last whole vector
+                    const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                    for (int q = 0; q < tail; ++q) {
+                        const int li = n8 + q;
+                        if (!((bm[li >> 5] >> (li & 31)) & 1u)) {
+                            const float y = fmaf(bf_to_f(lrow[li]), kscale, -o);
+                            const float e = ex2(y);
+                            s1a += e;
+                            s2a = fmaf(e, y, s2a);
+                        }
+                    }
+                }
                 Mass ms_acc{mz, (s1a + s1b) + (s1c + s1d), (s2a + s2b) + (s2c + s2d)};
-                if (!timed_out && !(fast && ms_acc.s1 <= 0x1p100f && fabsf(ms_acc.s2) <= 0x1p110f)) {
+                const bool ok = fast && ms_acc.s1 <= 0x1p100f && fabsf(ms_acc.s2) <= 0x1p110f;
+                if (!timed_out && !ok) {
                     // exact: this thread's maximum, then its sums relative to it (also
                     // the path of -inf logits, whose 0 * -inf made the fast sums NaN)
                     float mx = -INFINITY;
@@ -890,13 +905,13 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         }
                     }
                     ms_acc = Mass{mx, s1, s2};
-                }
-                if (tail && tid == 0 && !timed_out) {  // entries past the last whole vector
-                    const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
-                    for (int q = 0; q < tail; ++q) {
-                        const int li = n8 + q;
-                        if (!((bm[li >> 5] >> (li & 31)) & 1u))
-                            ms_acc = mass_merge(ms_acc, Mass{bf_to_f(lrow[li]), 1.0f, 0.0f}, kscale);
+                    if (tail && tid == 0) {  // the tail again, relative to this maximum
+                        const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                        for (int q = 0; q < tail; ++q) {
+                            const int li = n8 + q;
+                            if (!((bm[li >> 5] >> (li & 31)) & 1u))
+                                ms_acc = mass_merge(ms_acc, Mass{bf_to_f(lrow[li]), 1.0f, 0.0f}, kscale);
+                        }
                     }
                 }
                 if (__any_sync(kFull, timed_out)) {
@@ -913,8 +928,14 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     }
                     if (tid == NC - 1 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? buf[a_li] : lrow[a_li]);
                 }
+                if (__all_sync(kFull, ok)) {  // one offset for the whole warp: plain sums
+                    ms_acc.s1 = warp_sum(ms_acc.s1);
+                    ms_acc.s2 = warp_sum(ms_acc.s2);
+                } else {
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) ms_acc = mass_merge(ms_acc, mass_shfl(ms_acc, off), kscale);
+                    for (int off = 16; off > 0; off >>= 1)
+                        ms_acc = mass_merge(ms_acc, mass_shfl(ms_acc, off), kscale);
+                }
                 if (lane == 0) {
                     float* rp = red + p * 3 * NCW;
                     rp[warp] = ms_acc.m;
