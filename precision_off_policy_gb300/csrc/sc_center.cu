@@ -812,8 +812,10 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 mz = warp_max(mz);
                 const bool fast = mz > -INFINITY;
                 const float o = fast ? mz * kscale : 0.0f;
-                float s1a = 0.0f, s1b = 0.0f, s1c = 0.0f, s1d = 0.0f;
-                float s2a = 0.0f, s2b = 0.0f, s2c = 0.0f, s2d = 0.0f;
+                // packed pairs: sum 2^y and sum 2^y y over the unrecorded entries
+                const f2_t K2 = f2_pack(kscale, kscale), NO2 = f2_pack(-o, -o);
+                f2_t S1a = 0ull, S1b = 0ull, S2a = 0ull, S2b = 0ull;
+                float s1x = 0.0f, s2x = 0.0f;  // entries taken one by one
                 for (int c = 0; c < nchunks && !timed_out; ++c) {
                     if (!mbar_wait_bounded(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs)) {
                         timed_out = true;
@@ -825,28 +827,22 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         const uint4 w = lds128(buf_s + 16u * j);
                         const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
                         if (rbits == 0u) {
-                            float y0 = fmaf(bf_lo(w.x), kscale, -o), y1 = fmaf(bf_hi(w.x), kscale, -o);
-                            float e0 = ex2(y0), e1 = ex2(y1);
-                            s1a += e0 + e1;
-                            s2a = fmaf(e0, y0, fmaf(e1, y1, s2a));
-                            y0 = fmaf(bf_lo(w.y), kscale, -o);
-                            y1 = fmaf(bf_hi(w.y), kscale, -o);
-                            e0 = ex2(y0);
-                            e1 = ex2(y1);
-                            s1b += e0 + e1;
-                            s2b = fmaf(e0, y0, fmaf(e1, y1, s2b));
-                            y0 = fmaf(bf_lo(w.z), kscale, -o);
-                            y1 = fmaf(bf_hi(w.z), kscale, -o);
-                            e0 = ex2(y0);
-                            e1 = ex2(y1);
-                            s1c += e0 + e1;
-                            s2c = fmaf(e0, y0, fmaf(e1, y1, s2c));
-                            y0 = fmaf(bf_lo(w.w), kscale, -o);
-                            y1 = fmaf(bf_hi(w.w), kscale, -o);
-                            e0 = ex2(y0);
-                            e1 = ex2(y1);
-                            s1d += e0 + e1;
-                            s2d = fmaf(e0, y0, fmaf(e1, y1, s2d));
+                            f2_t y = f2_fma(bf2_to_f2(w.x), K2, NO2);
+                            f2_t e = f2_ex2(y);
+                            S1a = f2_add(S1a, e);
+                            S2a = f2_fma(e, y, S2a);
+                            y = f2_fma(bf2_to_f2(w.y), K2, NO2);
+                            e = f2_ex2(y);
+                            S1b = f2_add(S1b, e);
+                            S2b = f2_fma(e, y, S2b);
+                            y = f2_fma(bf2_to_f2(w.z), K2, NO2);
+                            e = f2_ex2(y);
+                            S1a = f2_add(S1a, e);
+                            S2a = f2_fma(e, y, S2a);
+                            y = f2_fma(bf2_to_f2(w.w), K2, NO2);
+                            e = f2_ex2(y);
+                            S1b = f2_add(S1b, e);
+                            S2b = f2_fma(e, y, S2b);
                         } else {
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -855,8 +851,8 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                                 if (!((rbits >> q) & 1u)) {
                                     const float y = fmaf(z, kscale, -o);
                                     const float e = ex2(y);
-                                    s1a += e;
-                                    s2a = fmaf(e, y, s2a);
+                                    s1x += e;
+                                    s2x = fmaf(e, y, s2x);
                                 }
                             }
                         }
@@ -869,12 +865,13 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         if (!((bm[li >> 5] >> (li & 31)) & 1u)) {
                             const float y = fmaf(bf_to_f(lrow[li]), kscale, -o);
                             const float e = ex2(y);
-                            s1a += e;
-                            s2a = fmaf(e, y, s2a);
+                            s1x += e;
+                            s2x = fmaf(e, y, s2x);
                         }
                     }
                 }
-                Mass ms_acc{mz, (s1a + s1b) + (s1c + s1d), (s2a + s2b) + (s2c + s2d)};
+                const f2_t S1 = f2_add(S1a, S1b), S2 = f2_add(S2a, S2b);
+                Mass ms_acc{mz, (f2_lo(S1) + f2_hi(S1)) + s1x, (f2_lo(S2) + f2_hi(S2)) + s2x};
                 const bool ok = fast && ms_acc.s1 <= 0x1p100f && fabsf(ms_acc.s2) <= 0x1p110f;
                 if (!timed_out && !ok) {
                     // exact: this thread's maximum, then its sums relative to it (also
@@ -968,18 +965,16 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const float bw = scal[4 * pp + 0];
                 const float beta = scal[4 * pp + 1];
                 float rs = 0.0f;
-                auto emit = [&](int j, const uint4& w) {  // 8 gradients from 8 logits
-                    const float g0 = beta * ex2(fmaf(bf_lo(w.x), kscale, -bw));
-                    const float g1 = beta * ex2(fmaf(bf_hi(w.x), kscale, -bw));
-                    const float g2 = beta * ex2(fmaf(bf_lo(w.y), kscale, -bw));
-                    const float g3 = beta * ex2(fmaf(bf_hi(w.y), kscale, -bw));
-                    const float g4 = beta * ex2(fmaf(bf_lo(w.z), kscale, -bw));
-                    const float g5 = beta * ex2(fmaf(bf_hi(w.z), kscale, -bw));
-                    const float g6 = beta * ex2(fmaf(bf_lo(w.w), kscale, -bw));
-                    const float g7 = beta * ex2(fmaf(bf_hi(w.w), kscale, -bw));
-                    rs += ((g0 + g1) + (g2 + g3)) + ((g4 + g5) + (g6 + g7));
-                    st_global_v4_hint(grow + 8 * j, pack_bf16x2(g0, g1), pack_bf16x2(g2, g3), pack_bf16x2(g4, g5),
-                                      pack_bf16x2(g6, g7), pol);
+                const f2_t K2 = f2_pack(kscale, kscale), NBW2 = f2_pack(-bw, -bw), BETA2 = f2_pack(beta, beta);
+                f2_t RS = 0ull;
+                auto emit = [&](int j, const uint4& w) {  // 8 gradients from 8 logits, in packed pairs
+                    const f2_t g0 = f2_mul(f2_ex2(f2_fma(bf2_to_f2(w.x), K2, NBW2)), BETA2);
+                    const f2_t g1 = f2_mul(f2_ex2(f2_fma(bf2_to_f2(w.y), K2, NBW2)), BETA2);
+                    const f2_t g2 = f2_mul(f2_ex2(f2_fma(bf2_to_f2(w.z), K2, NBW2)), BETA2);
+                    const f2_t g3 = f2_mul(f2_ex2(f2_fma(bf2_to_f2(w.w), K2, NBW2)), BETA2);
+                    RS = f2_add(RS, f2_add(f2_add(g0, g1), f2_add(g2, g3)));
+                    st_global_v4_hint(grow + 8 * j, pack_bf16x2(f2_lo(g0), f2_hi(g0)), pack_bf16x2(f2_lo(g1), f2_hi(g1)),
+                                      pack_bf16x2(f2_lo(g2), f2_hi(g2)), pack_bf16x2(f2_lo(g3), f2_hi(g3)), pol);
                 };
                 if (NB > 1) {
                     // the slice is still in its stage: read it there and hand each
@@ -1005,7 +1000,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         grow[li] = f_to_bf_bits(g);
                     }
                 }
-                rs = warp_sum(rs);
+                rs = warp_sum(rs + (f2_lo(RS) + f2_hi(RS)));
                 if (lane == 0) rsw[pp * NCW + warp] = rs;
             }
             if (!have_cur) {  // end of the stream: every row of this warp is written

@@ -188,6 +188,39 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Two FP32 values in one 64-bit register pair (lo, hi) for the packed FP32
+// instructions of sm_100+ (add/mul/fma .f32x2): each lane rounds exactly as
+// the scalar instruction does, at half the issue cost.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(f2_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(f2_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// A packed bf16 pair (lo in bits 0..15) widened to two FP32 values.
+__device__ __forceinline__ f2_t bf2_to_f2(uint32_t w) {
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// 2^x lane-wise (MUFU, one instruction per lane).
+__device__ __forceinline__ f2_t f2_ex2(f2_t y) { return f2_pack(ex2(f2_lo(y)), ex2(f2_hi(y))); }
+
 // Lane-wise maximum of two packed bf16 pairs.
 __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     uint32_t d;
