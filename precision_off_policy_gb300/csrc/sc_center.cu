@@ -73,8 +73,14 @@ struct RowMeta {
     int a_li;        // local index of a in this slice, -1 if another CTA owns it
     uint32_t flags;  // row flags found by the producer (count, repeats, out of range)
     float A, rl;     // advantage, rollout logprob
+    // this slice's recorded ids, from their log-probabilities alone
+    float qbest;     // the largest q (0 if none)
+    float omq;       // 1 - qbest, from its log-probability
+    float oh, ol;    // the sum of the other q (double-float)
+    int kbest;       // position k of qbest (INT_MAX if none)
+    int pad[3];
 };
-static_assert(sizeof(RowMeta) == 32, "RowMeta layout");
+static_assert(sizeof(RowMeta) == 64, "RowMeta layout");
 
 // One CTA's contribution to a row, exchanged across the cluster (64 bytes).
 // y' values are relative to this CTA's own slice maximum m (y' = (z - m) kscale).
@@ -99,7 +105,7 @@ struct Layout {
     int stage_bytes;  // bytes of one data stage (128-aligned)
     int list_cap;     // entries of one owned list (K_max)
     int nwords;       // bitmap words of one slice (one bit per entry)
-    int off_meta, off_list_li, off_list_lp, off_list_k, off_bitmap, off_bars, off_part, off_mine, off_frs,
+    int off_meta, off_list_li, off_list_q, off_bitmap, off_bars, off_part, off_mine, off_frs,
         off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, total;
 };
 
@@ -243,8 +249,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.off_bars);
     RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);         // [kMetaSlots]
     int* list_li = reinterpret_cast<int*>(smem + L.off_list_li);           // [kMetaSlots][cap]
-    float* list_lp = reinterpret_cast<float*>(smem + L.off_list_lp);       // [kMetaSlots][cap]
-    int* list_k = reinterpret_cast<int*>(smem + L.off_list_k);             // [kMetaSlots][cap]
+    float* list_q = reinterpret_cast<float*>(smem + L.off_list_q);         // [kMetaSlots][cap] q = e^lp
     uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [kMetaSlots][nwords]
     Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [kXBufs][C]
     Partial* mine = reinterpret_cast<Partial*>(smem + L.off_mine);         // staging of this CTA's record
@@ -398,8 +403,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     cnt = cnt < 0 ? 0 : K_max;
                 }
                 int* li_s = list_li + ms * cap;
-                float* lp_s = list_lp + ms * cap;
-                int* k_s = list_k + ms * cap;
+                float* q_s = list_q + ms * cap;
                 uint32_t* bm = bitmap + ms * nwords;
                 {  // clear the bits of the slot's previous row (whole words: they are all its own)
                     const int old = meta[ms].nown;
@@ -409,6 +413,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const long long kb = t * static_cast<long long>(K_max);
                 int nown = 0;
                 bool bad = false, dup = false;
+                HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};  // the kept ids' q, merged
                 for (int kb0 = 0; kb0 < cnt; kb0 += 128) {
                     int idr[4];
                     float lpr[4];
@@ -437,15 +442,18 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         const unsigned km = __ballot_sync(kFull, keep);
                         if (keep) {
                             const int pos = nown + __popc(km & lanemask_lt());
+                            const float q = expf(lpr[r]);
                             li_s[pos] = id - lo;
-                            lp_s[pos] = lpr[r];
-                            k_s[pos] = k;
+                            q_s[pos] = q;
+                            hm = head_merge(hm, HeadMass{q, k, -expm1f(lpr[r]), 0.0f, 0.0f});
                             atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
                         }
                         nown += __popc(km);
                         __syncwarp();
                     }
                 }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) hm = head_merge(hm, head_shfl(hm, off));
                 if (__any_sync(kFull, dup)) flags |= SC_FLAG_DUP_ID;
                 if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
                 const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
@@ -458,7 +466,17 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     mt->flags = flags;
                     mt->A = row_A;
                     mt->rl = row_rl;
+                    mt->qbest = hm.q;
+                    mt->omq = hm.omq;
+                    mt->oh = hm.oh;
+                    mt->ol = hm.ol;
+                    mt->kbest = hm.k;
                 }
+                // The slot is published before the copies start: the consumers wait
+                // for each chunk on its own barrier, so they can start as soon as the
+                // first chunk lands.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
                 // ---- logit slice: chunk by chunk as the stage's slots free up ----
                 if (lane == 0) {
                     const int ds = static_cast<int>(nfill % NB);
@@ -485,8 +503,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 }
                 stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
                 if (stop) break;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
                 ++nfill;
             }
         }
@@ -546,8 +562,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
             }
             const int xi = static_cast<int>(j & 3u);
             const int* li_s = list_li + ms * cap;
-            const float* lp_s = list_lp + ms * cap;
-            const int* k_s = list_k + ms * cap;
+            const float* q_s = list_q + ms * cap;
             const float* fz = fix_z + p * cap;
             const int nown = m.nown, a_li = m.a_li;
             if (lane == 0) mbar_expect_tx(xbar(xi), static_cast<uint32_t>(sizeof(Partial)) * C);
@@ -555,9 +570,15 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
             {
                 const float* rp = red + p * 3 * NCW;
                 Mass cm = lane < NCW ? Mass{rp[lane], rp[NCW + lane], rp[2 * NCW + lane]}
-                                     : Mass{-INFINITY, 0.0f, 0.0f};
+                                     : Mass{rp[0], 0.0f, 0.0f};
+                if (__all_sync(kFull, cm.m == rp[0])) {  // one offset in every warp: plain sums
+                    cm.s1 = warp_sum(cm.s1);
+                    cm.s2 = warp_sum(cm.s2);
+                } else {
+                    if (lane >= NCW) cm.m = -INFINITY;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) cm = mass_merge(cm, mass_shfl(cm, off), kscale);
+                    for (int off = 16; off > 0; off >>= 1) cm = mass_merge(cm, mass_shfl(cm, off), kscale);
+                }
                 {  // the owned recorded logits may lie above the streaming offset
                     float zmax = -INFINITY;
                     for (int e = lane; e < nown; e += 32) zmax = fmaxf(zmax, fz[e]);
@@ -565,26 +586,18 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 }
                 const float o_c = cm.m * kscale;
                 float lH = 0.0f, EH = 0.0f, QY = 0.0f;
-                int nval = 0;
-                HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};
                 for (int e = lane; e < nown; e += 32) {
                     const float y = fmaf(fz[e], kscale, -o_c);
                     const float ev = ex2(y);
                     lH += ev;
                     EH = fmaf(ev, y, EH);
-                    const float lp = lp_s[e];
-                    const float q = expf(lp);
-                    QY = fmaf(q, y, QY);
-                    ++nval;
-                    hm = head_merge(hm, HeadMass{q, k_s[e], -expm1f(lp), 0.0f, 0.0f});
+                    QY = fmaf(q_s[e], y, QY);
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     lH += __shfl_xor_sync(kFull, lH, off);
                     EH += __shfl_xor_sync(kFull, EH, off);
                     QY += __shfl_xor_sync(kFull, QY, off);
-                    nval += __shfl_xor_sync(kFull, nval, off);
-                    hm = head_merge(hm, head_shfl(hm, off));
                 }
                 if (lane == 0) {
                     Partial& r = *mine;
@@ -595,15 +608,15 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     r.lH = lH;
                     r.EH = EH;
                     r.QY = QY;
-                    r.qo_hi = hm.oh;
-                    r.qo_lo = hm.ol;
-                    r.qbest = hm.q;
-                    r.kbest = hm.k;
-                    r.nval = nval;
+                    r.qo_hi = m.oh;
+                    r.qo_lo = m.ol;
+                    r.qbest = m.qbest;
+                    r.kbest = m.kbest;
+                    r.nval = nown;
                     r.flags = m.flags;
                     r.ya = a_li >= 0 ? fmaf(zav[p], kscale, -o_c) : 0.0f;
                     r.has_a = a_li >= 0 ? 1 : 0;
-                    r.omq = hm.omq;
+                    r.omq = m.omq;
                 }
                 __syncwarp();
                 if (lane < C) {  // lane r sends the record to CTA r
@@ -732,7 +745,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 bool a_rec = false;
                 for (int e = lane; e < nown; e += 32) {
                     const float pe = ex2(fmaf(fz[e], kscale, -o) - log2l);
-                    const float mu = a.centering ? fmaf(dsr, pe, expf(lp_s[e])) : pe;
+                    const float mu = a.centering ? fmaf(dsr, pe, q_s[e]) : pe;
                     const bool is_a = li_s[e] == a_li;
                     const float g = alpha * ((is_a ? 1.0f : 0.0f) - mu);
                     fv[e] = g;
@@ -1050,8 +1063,7 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     };
     L.off_meta = take(kMetaSlots * static_cast<int>(sizeof(RowMeta)));
     L.off_list_li = take(kMetaSlots * L.list_cap * 4);
-    L.off_list_lp = take(kMetaSlots * L.list_cap * 4);
-    L.off_list_k = take(kMetaSlots * L.list_cap * 4);
+    L.off_list_q = take(kMetaSlots * L.list_cap * 4);
     L.off_bitmap = take(kMetaSlots * L.nwords * 4);
     L.off_bars = take(kNumBars * 8);
     L.off_part = take(kXBufs * C * static_cast<int>(sizeof(Partial)));
