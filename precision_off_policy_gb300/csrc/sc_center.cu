@@ -691,39 +691,50 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     tail_mu = (hm.omq - hm.oh) - hm.ol;
                     Q_H = (hm.q + hm.oh) + hm.ol;
                 }
+                // First what the write pass needs (bw, beta), published at once;
+                // the diagnostics and the recorded ids' own gradients after.
                 const float l = lT + lH;
                 const float log2l = log2f(l);
                 const float P_H = lH / l;
                 const float tail_pi = lT / l;
                 const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
-                if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
-                if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
                 const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
-                const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
                 const float logp_a = (ya - log2l) * kLn2;
-                float wt = 1.0f, k3 = 0.0f;
-                if (a.rollout) {
-                    const float dd = logp_a - m.rl;
-                    k3 = expm1f(dd) - dd;
+                const float dd = a.rollout ? logp_a - m.rl : 0.0f;
+                float wt = 1.0f;
+                if (a.is_mode == SC_IS_TIS) {
                     const float w = expf(dd);
-                    if (a.is_mode == SC_IS_TIS) {
-                        if (w > a.tis_max) {
-                            wt = a.tis_max;
-                            flags |= SC_FLAG_IS_TRUNC;
-                        } else {
-                            wt = w;
-                        }
-                    } else if (a.is_mode == SC_IS_MIS) {
-                        if (w >= a.mis_min && w <= a.mis_max) {
-                            wt = w;
-                        } else {
-                            wt = 0.0f;
-                            flags |= SC_FLAG_IS_REJECT;
-                        }
+                    if (w > a.tis_max) {
+                        wt = a.tis_max;
+                        flags |= SC_FLAG_IS_TRUNC;
+                    } else {
+                        wt = w;
+                    }
+                } else if (a.is_mode == SC_IS_MIS) {
+                    const float w = expf(dd);
+                    if (w >= a.mis_min && w <= a.mis_max) {
+                        wt = w;
+                    } else {
+                        wt = 0.0f;
+                        flags |= SC_FLAG_IS_REJECT;
                     }
                 }
                 const float A = m.A;
                 const float Aw = A * wt;
+                const float alpha = -a.grad_scale * a.inv_t * Aw;
+                const float beta = -alpha * s;
+                const float bw = o + log2l;
+                if (lane == 0) {
+                    scal[4 * p + 0] = bw;
+                    scal[4 * p + 1] = beta;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sready(p));
+
+                if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
+                if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
+                const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
+                const float k3 = a.rollout ? expm1f(dd) - dd : 0.0f;
                 // sum_H c log p = sum_H q log p - rho sum_H p log p, each from the
                 // merged sums: log p_k = (y_k - log2 l) ln 2.
                 float csum = 0.0f;
@@ -734,9 +745,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 }
                 const float loss = -Aw * (logp_a - csum);
                 const float entropy = kLn2 * (log2l - (ET + EH) / l);
-                const float alpha = -a.grad_scale * a.inv_t * Aw;
-                const float beta = -alpha * s;
-                const float bw = o + log2l;
                 const float g_a_free = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
                 // gradient at the owned recorded ids, and how far it is from the
                 // beta p the write pass stores there (the row sum's correction)
@@ -758,10 +766,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 corr_m2 = corr_m1;
                 corr_m1 = corr;
                 if (lane == 0) {
-                    float* sc = scal + 4 * p;
-                    sc[0] = bw;
-                    sc[1] = beta;
-                    sc[2] = g_a_free;
+                    scal[4 * p + 2] = g_a_free;  // read back by this warp when it patches the row
                     if (crank == 0) {
                         a.logp[m.t] = logp_a;
                         if (a.diag) {  // the record in field order, as four 16-byte stores
@@ -776,8 +781,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         if (flags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sready(p));
             }
             t_m2 = t_m1;
             t_m1 = m.t;
@@ -970,6 +973,12 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const RowMeta mp = meta[msp];
                 const uint16_t* lrow = a.logits + mp.t * a.lstride + lo;
                 uint16_t* grow = a.grad + mp.t * a.gstride + lo;
+                // the first L2 reads go out before the row scalars are known
+                uint4 wa = make_uint4(0u, 0u, 0u, 0u), wb = wa;
+                if (NB == 1) {
+                    if (tid < nvb) wa = ldg_v4_hint(lrow + 8 * tid, pol);
+                    if (tid + NC < nvb) wb = ldg_v4_hint(lrow + 8 * (tid + NC), pol);
+                }
                 const bool ready = mbar_wait_bounded(sready(pp), (ip >> 1) & 1u, kWaitLimitNs);
                 if (!__all_sync(kFull, ready)) {
                     give_up(SC_STATUS_TIMEOUT_EXCHANGE);
@@ -1002,8 +1011,14 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                         if (lane == 0) mbar_arrive(data_bar(dsp, kChunkFree + c));
                     }
                 } else {
-#pragma unroll 2
-                    for (int j = tid; j < nvb; j += NC) emit(j, ldg_v4_hint(lrow + 8 * j, pol));
+                    // two vectors in flight ahead of the two being written
+                    for (int j = tid; j < nvb; j += 2 * NC) {
+                        const uint4 w0 = wa, w1 = wb;
+                        if (j + 2 * NC < nvb) wa = ldg_v4_hint(lrow + 8 * (j + 2 * NC), pol);
+                        if (j + 3 * NC < nvb) wb = ldg_v4_hint(lrow + 8 * (j + 3 * NC), pol);
+                        emit(j, w0);
+                        if (j + NC < nvb) emit(j + NC, w1);
+                    }
                 }
                 if (tail && tid == 0) {
                     for (int q = 0; q < tail; ++q) {
