@@ -36,8 +36,9 @@ FLAG_CLAMP_PI = 0x40
 FLAG_CLAMP_MU = 0x80
 FLAG_IS_TRUNC = 0x100
 FLAG_IS_REJECT = 0x200
+FLAG_CLIPPED = 0x400
 
-IS_NONE, IS_TIS, IS_MIS = 0, 1, 2
+IS_NONE, IS_TIS, IS_MIS, IS_CLIP = 0, 1, 2, 3
 
 
 class Params(ctypes.Structure):
@@ -49,6 +50,8 @@ class Params(ctypes.Structure):
         ("centering", ctypes.c_int),
         ("inv_temperature", ctypes.c_double),
         ("grad_scale", ctypes.c_double),
+        ("clip_low", ctypes.c_double),
+        ("clip_high", ctypes.c_double),
     ]
 
 
@@ -114,6 +117,9 @@ def lib():
             L.sco_group_advantages.restype = ctypes.c_int
             L.sco_group_advantages.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_double, ctypes.c_void_p]
+            L.sco_rollout_mean_advantages.restype = ctypes.c_int
+            L.sco_rollout_mean_advantages.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong,
+                                                      ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
             L.sco_row.restype = ctypes.c_uint
             L.sco_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
@@ -139,10 +145,12 @@ def _ptr(a):
 
 
 def make_params(is_mode=IS_NONE, tis_max=2.0, mis_min=0.5, mis_max=5.0, centering=True,
-                inv_temperature=1.0, grad_scale=1.0) -> Params:
-    """Defaults are the settings table of the docs' "Score Centering" section."""
+                inv_temperature=1.0, grad_scale=1.0, clip_low=0.2, clip_high=0.3) -> Params:
+    """Defaults are the settings table of the docs' "Score Centering" section
+    and, for the clipped GRPO baseline (is_mode 3), the clip widths of the
+    page's `grpo` preset."""
     return Params(int(is_mode), float(tis_max), float(mis_min), float(mis_max), int(bool(centering)),
-                  float(inv_temperature), float(grad_scale))
+                  float(inv_temperature), float(grad_scale), float(clip_low), float(clip_high))
 
 
 def bf16_to_double(bits) -> np.ndarray:
@@ -171,6 +179,21 @@ def group_advantages(rewards, n_groups: int, group_size: int, normalize_std: boo
     if rc != 0:
         raise ValueError("sco_group_advantages rejected its arguments")
     return out
+
+
+def rollout_mean_advantages(adv, row_response, n_resp: int):
+    """Per-rollout mean loss: (adv[r] / valid tokens of response r, counts)."""
+    a = np.ascontiguousarray(adv, dtype=np.float64)
+    rr = np.ascontiguousarray(row_response, dtype=np.int32)
+    counts = np.zeros(n_resp, dtype=np.int64)
+    out = np.zeros(n_resp, dtype=np.float64)
+    if a.size != n_resp:
+        raise ValueError("adv must have n_resp entries")
+    rc = lib().sco_rollout_mean_advantages(_ptr(a), _ptr(rr) if rr.size else None, rr.size, n_resp,
+                                           _ptr(counts), _ptr(out))
+    if rc != 0:
+        raise ValueError("sco_rollout_mean_advantages rejected its arguments")
+    return out, counts
 
 
 def row(z_bits, ids, logprobs, a: int, A: float, params: Params | None = None,

@@ -46,6 +46,16 @@
  *   - is_mode tis weights the token by min(w, tis_max); is_mode mis weights
  *     it by w inside [mis_min, mis_max] and by 0 outside; w = exp(d).
  *   - centering = 0 drops the centering term (c = 0, s = 1).
+ *   - is_mode 3 is the clipped GRPO baseline of the page's "Training" section
+ *     (the `grpo` preset: clipped objective, lower/upper clip widths 0.2/0.3,
+ *     per-rollout mean loss): with the ratio w = exp(d) and its clipped copy
+ *     w_c = clamp(w, 1 - clip_low, 1 + clip_high), the token loss is
+ *     -min(w A, w_c A).  Its gradient is that of -A w, i.e. the policy
+ *     gradient weighted by w, wherever the unclipped term is the minimum, and
+ *     zero where the clipped one is (flag CLIPPED).  It has no centering term:
+ *     the mode is defined with centering = 0 only.  The per-rollout mean is
+ *     sco_rollout_mean_advantages below: each response's advantage divided
+ *     by its number of valid tokens (0 for a response without any).
  */
 #include <math.h>
 #include <pthread.h>
@@ -65,13 +75,15 @@
 #define SCO_FLAG_CLAMP_MU 0x80u     /* 1 - Q_H < 1e-6: numerator clamped      */
 #define SCO_FLAG_IS_TRUNC 0x100u    /* tis: weight truncated at tis_max       */
 #define SCO_FLAG_IS_REJECT 0x200u   /* mis: weight outside the interval -> 0  */
+#define SCO_FLAG_CLIPPED 0x400u     /* clipped GRPO: the clipped term is the minimum */
 
 typedef struct {
-    int is_mode; /* 0 none, 1 tis, 2 mis */
+    int is_mode; /* 0 none, 1 tis, 2 mis, 3 clipped GRPO */
     double tis_max, mis_min, mis_max;
     int centering; /* 1: score centering on, 0: plain importance-weighted PG */
     double inv_temperature;
     double grad_scale;
+    double clip_low, clip_high; /* clipped GRPO: ratio kept in [1 - low, 1 + high] */
 } sco_params;
 
 typedef struct {
@@ -168,6 +180,21 @@ int sco_group_advantages(const float* rewards, int n_groups, int group_size, int
     return 0;
 }
 
+/* Per-rollout mean: each response's advantage divided by its number of
+ * valid tokens (rows whose response index is r), 0 for a response with none;
+ * the counts are returned too.  Returns 0, or -1 on bad arguments. */
+int sco_rollout_mean_advantages(const double* adv, const int32_t* row_response, long long T, int n_resp,
+                                long long* counts, double* adv_out) {
+    if (T < 0 || n_resp < 0) return -1;
+    if (n_resp > 0 && (!adv || !counts || !adv_out)) return -1;
+    if (T > 0 && !row_response) return -1;
+    for (int r = 0; r < n_resp; ++r) counts[r] = 0;
+    for (long long t = 0; t < T; ++t)
+        if (row_response[t] >= 0 && row_response[t] < n_resp) ++counts[row_response[t]];
+    for (int r = 0; r < n_resp; ++r) adv_out[r] = counts[r] > 0 ? adv[r] / (double)counts[r] : 0.0;
+    return 0;
+}
+
 /* ---- one token row --------------------------------------------------- */
 
 /* Score-centered forward/backward for one unmasked row.
@@ -241,6 +268,16 @@ static unsigned sco_row_impl(const uint16_t* z, int V, const int32_t* ids, const
     if (p->is_mode == 1) {
         wt = w < p->tis_max ? w : p->tis_max;
         if (w > p->tis_max) flags |= SCO_FLAG_IS_TRUNC;
+    } else if (p->is_mode == 3) {
+        /* -min(w A, w_c A): the gradient is -A w where the unclipped term is
+         * the minimum (equal terms included), 0 where the clipped one is */
+        double wc = w < 1.0 - p->clip_low ? 1.0 - p->clip_low : (w > 1.0 + p->clip_high ? 1.0 + p->clip_high : w);
+        if (wc == w || w * A < wc * A) {
+            wt = w;
+        } else {
+            wt = 0.0;
+            flags |= SCO_FLAG_CLIPPED;
+        }
     } else if (p->is_mode == 2) {
         if (w >= p->mis_min && w <= p->mis_max)
             wt = w;
@@ -260,6 +297,10 @@ static unsigned sco_row_impl(const uint16_t* z, int V, const int32_t* ids, const
                 centered += c * logp[v];
             }
     double loss = -A_eff * (logp[a] - centered);
+    if (p->is_mode == 3) {
+        double wc = w < 1.0 - p->clip_low ? 1.0 - p->clip_low : (w > 1.0 + p->clip_high ? 1.0 + p->clip_high : w);
+        loss = -fmin(w * A, wc * A);
+    }
 
     /* Gradient: g_v = scale * (1/T) * (-A) * ([v==a] - s p_v - [v in H] c_v). */
     double coef = p->grad_scale * invT * (-A_eff);
@@ -302,6 +343,7 @@ unsigned sco_row(const uint16_t* z, int V, const int32_t* ids, const float* lp, 
                  sco_row_out* out) {
     if (!z || V <= 0 || !p || !grad || !out || count < 0 || (count > 0 && (!ids || !lp)))
         return ~0u;
+    if (p->is_mode == 3 && p->centering) return ~0u; /* the clipped objective has no centering */
     int* in_h = (int*)malloc(sizeof(int) * (size_t)V);
     double* logp = (double*)malloc(sizeof(double) * (size_t)V);
     if (!in_h || !logp) {
@@ -399,6 +441,7 @@ int sco_rows(const uint16_t* logits, long long T, int V, long long row_stride, c
              const sco_params* p, const long long* rows, long long n_rows, double* grad,
              double* logp_a, sco_row_out* out, int nthreads) {
     if (V <= 0 || T < 0 || row_stride < V || K_max < 0 || !p || n_rows < 0) return -1;
+    if (p->is_mode == 3 && p->centering) return -1;
     if (n_rows == 0) return 0;
     if (!logits || !sampled || !row_response || !adv || !rows || !grad || !logp_a || !out) return -1;
     if (K_max > 0 && (!rec_ids || !rec_logprobs)) return -1;

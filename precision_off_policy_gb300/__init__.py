@@ -27,6 +27,7 @@ from . import build as _build_mod
 __all__ = [
     "build", "lib", "ScError", "Params", "params", "DIAG_DTYPE", "DIAG_FIELDS",
     "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
+    "ScoreCenteredLoss", "score_centered_loss",
     "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS",
 ]
 
@@ -243,3 +244,42 @@ def sc_plan_query(V: int, p: Params) -> dict:
 def diag_to_numpy(diag: torch.Tensor) -> np.ndarray:
     """int32 [T, 16] diagnostics tensor -> numpy structured array [T]."""
     return diag.detach().cpu().contiguous().numpy().view(DIAG_DTYPE).reshape(-1)
+
+
+class ScoreCenteredLoss(torch.autograd.Function):
+    """Autograd wrapper of :func:`sc_center_forward_backward`.
+
+    The forward pass is one library launch: it produces the per-row losses and
+    the finished gradient with respect to the logits, which is saved.  The
+    returned loss is ``grad_scale * sum_t loss_t`` (a token mean when
+    grad_scale = 1 / N_tokens), whose gradient is exactly the saved one; the
+    backward pass returns it scaled by the incoming gradient.  Besides the
+    launch, torch only sums the T row losses and, when the incoming gradient is
+    not 1, scales the saved gradient.  Outputs: (loss, logp [T], diag int32
+    [T, 16]); the last two carry no gradient.
+    """
+
+    @staticmethod
+    def forward(ctx, logits, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response, adv,
+                p, stream=None):
+        T = logits.shape[0]
+        diag = torch.empty((T, 16), dtype=torch.int32, device=logits.device)
+        grad, logp, diag = sc_center_forward_backward(
+            logits.detach(), rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response, adv, p,
+            diag_out=diag, stream=stream)
+        ctx.save_for_backward(grad)
+        loss = diag.view(torch.float32)[:, 0].sum() * float(np.float32(p.grad_scale))
+        ctx.mark_non_differentiable(logp, diag)
+        return loss, logp, diag
+
+    @staticmethod
+    def backward(ctx, g_loss, g_logp, g_diag):
+        (grad,) = ctx.saved_tensors
+        return (grad * g_loss.to(grad.dtype),) + (None,) * 9
+
+
+def score_centered_loss(logits, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response, adv,
+                        p, stream=None):
+    """Differentiable score-centered loss (see :class:`ScoreCenteredLoss`)."""
+    return ScoreCenteredLoss.apply(logits, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob,
+                                   row_response, adv, p, stream)

@@ -549,3 +549,75 @@ def test_batch_masks_padding_and_flags_bad_rows():
                             A=float(batch["adv"][batch["row_response"][t]]))
         np.testing.assert_array_equal(g[t], g1)
         assert out["loss"][t] == o1["loss"]
+
+
+# --------------------------------------------------------------------------
+# Clipped GRPO baseline (the `grpo` preset of the docs page's "Training"
+# section: clipped objective, clip widths 0.2 / 0.3, per-rollout mean loss).
+
+
+def _clip_case(rng, V, w_target, A, inv_t=1.0, lo=0.2, hi=0.3):
+    z = _random_row(rng, V, 2.0)
+    a = int(rng.integers(V))
+    zf = bf16_values(z)
+    lpa = log_softmax(zf * inv_t)[a]
+    old = float(np.float32(lpa - np.log(w_target)))
+    prm = oracle.make_params(is_mode=oracle.IS_CLIP, centering=False, inv_temperature=inv_t,
+                             clip_low=lo, clip_high=hi)
+    g, o = oracle.row(z, [], [], a=a, A=A, params=prm, rollout_logprob=old)
+    return z, zf, a, old, g, o
+
+
+@pytest.mark.parametrize("w_target,A,active", [
+    (1.0, 1.3, True), (1.1, -0.8, True),        # inside the clip range: the ratio's gradient
+    (1.6, 1.3, False), (0.5, -0.8, False),      # clipped term is the minimum: no gradient
+    (0.5, 1.3, True), (1.6, -0.8, True),        # unclipped term is the minimum: gradient flows
+])
+def test_clipped_grpo_gradient_matches_central_differences(w_target, A, active):
+    rng = np.random.default_rng(int(w_target * 100) + (7 if A > 0 else 11))
+    V, inv_t, lo, hi = 20, 1.25, 0.2, 0.3
+    z, zf, a, old, g, o = _clip_case(rng, V, w_target, A, inv_t, lo, hi)
+
+    def loss(zz):
+        w = np.exp(log_softmax(zz * inv_t)[a] - old)
+        return -min(w * A, min(max(w, 1 - lo), 1 + hi) * A)
+
+    np.testing.assert_allclose(loss(zf), o["loss"], rtol=1e-12)
+    assert bool(o["flags"] & oracle.FLAG_CLIPPED) == (not active)
+    h = 1e-6
+    fd = np.array([(loss(zf + h * np.eye(V)[v]) - loss(zf - h * np.eye(V)[v])) / (2 * h) for v in range(V)])
+    np.testing.assert_allclose(g, fd, rtol=1e-6, atol=1e-8)
+    if not active:
+        assert np.all(g == 0.0) and o["is_weight"] == 0.0
+
+
+def test_clipped_grpo_at_unit_ratio_is_the_plain_policy_gradient():
+    rng = np.random.default_rng(5)
+    V, A, inv_t = 37, -1.1, 1 / 0.7
+    z, zf, a, old, g, o = _clip_case(rng, V, 1.0, A, inv_t)
+    # ratio 1 (up to the FP32 rounding of the old log-probability)
+    w = np.exp(log_softmax(zf * inv_t)[a] - old)
+    p = softmax(zf * inv_t)
+    ref = inv_t * (-A * w) * (np.eye(V)[a] - p)
+    np.testing.assert_allclose(g, ref, rtol=1e-12, atol=1e-15)
+    assert abs(o["loss"] + A * w) <= 1e-12
+    assert abs(g.sum()) <= 1e-12
+
+
+def test_clipped_grpo_rejects_centering():
+    rng = np.random.default_rng(6)
+    z = _random_row(rng, 8, 1.0)
+    prm = oracle.make_params(is_mode=oracle.IS_CLIP, centering=True)
+    with pytest.raises(ValueError):
+        oracle.row(z, [], [], a=0, A=1.0, params=prm, rollout_logprob=-1.0)
+
+
+def test_rollout_mean_advantages_hand_counts():
+    adv = np.array([1.5, -0.5, -0.5, -0.5, 2.0])
+    rr = np.array([0, 0, 0, 1, -1, 3, 3, 3, 3, 1, 7, -1], dtype=np.int32)  # 7 is out of range
+    out, counts = oracle.rollout_mean_advantages(adv, rr, 5)
+    assert counts.tolist() == [3, 2, 0, 4, 0]
+    np.testing.assert_array_equal(out, [0.5, -0.25, 0.0, -0.125, 0.0])
+    # agrees with a bincount over the valid response indices
+    ok = (rr >= 0) & (rr < 5)
+    assert counts.tolist() == np.bincount(rr[ok], minlength=5).tolist()

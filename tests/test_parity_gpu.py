@@ -245,6 +245,25 @@ def test_empty_batch_and_empty_head_parameter():
     _full_check(b, sc_params(b, K_max=0), "K_max=0")
 
 
+def test_autograd_wrapper_matches_direct_call():
+    batch = synth.make_batch(synth.config("C1", L_pad=8))
+    p = sc_params(batch, grad_scale=1.0 / 64.0)
+    adv = torch.from_numpy(oracle_adv(batch)).cuda()
+    b = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in batch.items()}
+    logits = b["logits"].clone().requires_grad_(True)
+    loss, logp, diag = sc.score_centered_loss(logits, b["rec_ids"], b["rec_logprobs"], b["rec_count"], b["sampled"],
+                                              b["rollout_logprob"], b["row_response"], adv, p)
+    (2.0 * loss).backward()
+    g, lp, d = sc.sc_center_forward_backward(b["logits"], b["rec_ids"], b["rec_logprobs"], b["rec_count"],
+                                             b["sampled"], b["rollout_logprob"], b["row_response"], adv, p,
+                                             diag_out=torch.empty((64, 16), dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(logits.grad, g * 2.0)
+    assert torch.equal(logp, lp) and torch.equal(diag, d)
+    rows = sc.diag_to_numpy(d)["loss"].astype(np.float64)
+    assert abs(float(loss) - rows.sum() / 64.0) <= 1e-5 * max(1.0, abs(rows.sum() / 64.0))
+
+
 def _unprotected(batch):
     """Mask of the entries that are neither recorded ids nor the sampled token."""
     T, V = batch["logits"].shape
