@@ -71,23 +71,33 @@ typedef struct CUstream_st* sc_stream_t;
 #define SC_FLAG_CLAMP_MU 0x80u     /* 1 - Q_H < 1e-6: numerator clamped          */
 #define SC_FLAG_IS_TRUNC 0x100u    /* tis: weight truncated at tis_max           */
 #define SC_FLAG_IS_REJECT 0x200u   /* mis: weight outside [mis_min, mis_max]     */
+#define SC_FLAG_CLIPPED 0x400u     /* clip: the clipped term is the minimum       */
 #define SC_FLAG_DATA_ERRORS (SC_FLAG_BAD_ID | SC_FLAG_DUP_ID | SC_FLAG_BAD_SAMPLED | \
                              SC_FLAG_BAD_COUNT | SC_FLAG_BAD_RESPONSE)
 
 /* Importance weighting modes: the `is_mode` setting (none / tis / mis) of the
  * settings table in the docs' "Score Centering" section.  w = exp(log p_a -
  * rollout logprob).  tis weights the token by min(w, tis_max); mis weights it
- * by w inside [mis_min, mis_max] and by 0 outside. */
+ * by w inside [mis_min, mis_max] and by 0 outside.
+ * SC_IS_CLIP is the clipped GRPO baseline of the page's "Training" section
+ * (`grpo` preset): token loss -min(w A, clamp(w, 1 - clip_low, 1 + clip_high) A)
+ * with rollout_logprob holding the old policy's log-probability; the gradient
+ * is the policy gradient weighted by w where the unclipped term is the
+ * minimum and 0 where the clipped one is (SC_FLAG_CLIPPED).  It requires
+ * centering = 0.  Its per-rollout mean loss comes from the advantages of
+ * sc_rollout_mean_advantages. */
 #define SC_IS_NONE 0
 #define SC_IS_TIS 1
 #define SC_IS_MIS 2
+#define SC_IS_CLIP 3
 
 /* Parameters of sc_center_forward_backward.  Defaults (sc_params_default):
  * the docs' settings table -- K = 128, is_mode none, tis_max 2.0,
- * mis_min 0.5, mis_max 5.0, centering on -- at temperature 1, scale 1. */
+ * mis_min 0.5, mis_max 5.0, centering on -- at temperature 1, scale 1, and
+ * the `grpo` preset's clip widths 0.2 / 0.3. */
 typedef struct sc_params {
     int K_max;             /* row length of rec_ids / rec_logprobs, 0..1024     */
-    int is_mode;           /* SC_IS_NONE, SC_IS_TIS or SC_IS_MIS                 */
+    int is_mode;           /* SC_IS_NONE, SC_IS_TIS, SC_IS_MIS or SC_IS_CLIP     */
     float tis_max;         /* > 0                                               */
     float mis_min;         /* 0 <= mis_min <= mis_max                            */
     float mis_max;
@@ -98,6 +108,8 @@ typedef struct sc_params {
     int threads;           /* compute threads per CTA (one more warp fetches):
                               0 = automatic, else 128, 256, 384 or 512          */
     int stages;            /* rows in flight per CTA: 0 = automatic, else 1..4   */
+    float clip_low;        /* SC_IS_CLIP: ratio floor 1 - clip_low, 0 <= low < 1 */
+    float clip_high;       /* SC_IS_CLIP: ratio ceiling 1 + clip_high, >= 0      */
 } sc_params;
 
 /* Per-row diagnostics, 64 bytes.  Masked and error rows hold zeros and their
@@ -149,14 +161,32 @@ int sc_group_advantages(const float* rewards, int n_groups, int group_size, int 
                         float eps, float* adv_out, sc_stream_t stream);
 
 /*
+ * Per-rollout mean loss (the `grpo` preset of the docs page's "Training"
+ * section): each response's advantage divided by its number of valid tokens,
+ * so that grad_scale = 1 / n_resp then averages per-rollout token means.
+ *
+ * adv          : FP32 [n_resp] advantages (device).
+ * row_response : int32 [T] response index of each row; rows with an index
+ *                outside [0, n_resp) count for no response.
+ * counts_out   : int32 [n_resp] valid tokens per response (device, written).
+ * adv_out      : FP32 [n_resp] adv[r] / counts[r], 0 where counts[r] == 0;
+ *                may equal adv.
+ * Asynchronous on `stream` (two kernels and a memset; nothing allocated).
+ * Errors: SC_ERR_NULL, SC_ERR_SHAPE (T or n_resp negative), SC_ERR_ALIGN,
+ * SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
+ */
+int sc_rollout_mean_advantages(const float* adv, const int32_t* row_response, long long T, int n_resp,
+                               int32_t* counts_out, float* adv_out, sc_stream_t stream);
+
+/*
  * Score-centered forward and backward over T token rows (docs "Score
  * Centering" page, section "Score Centering"; one fused kernel).
  *
  * logits          : bf16 [T, logits_stride], the first V entries of each row
  *                   are the trainer's raw logits; 16-byte aligned,
- *                   logits_stride % 8 == 0, logits_stride >= V.  Finite
- *                   values above -2^100 (the value -2^100 is reserved inside
- *                   the kernel).
+ *                   logits_stride % 8 == 0, logits_stride >= V.  Any
+ *                   values: -inf entries carry no mass (a NaN makes the
+ *                   row's results NaN).
  * rec_ids         : int32 [T, K_max] recorded candidate ids (top-K of the
  *                   sampler); entries past rec_count[t] are ignored.
  * rec_logprobs    : FP32 [T, K_max] their sampler log-probabilities, in

@@ -28,11 +28,11 @@ __all__ = [
     "build", "lib", "ScError", "Params", "params", "DIAG_DTYPE", "DIAG_FIELDS",
     "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
     "ScoreCenteredLoss", "score_centered_loss",
-    "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS",
+    "sc_rollout_mean_advantages", "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS", "SC_IS_CLIP",
 ]
 
 SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
-SC_IS_NONE, SC_IS_TIS, SC_IS_MIS = 0, 1, 2
+SC_IS_NONE, SC_IS_TIS, SC_IS_MIS, SC_IS_CLIP = 0, 1, 2, 3
 SC_STATUS_DATA, SC_STATUS_TIMEOUT_LOAD, SC_STATUS_TIMEOUT_EXCHANGE = 0x1, 0x2, 0x4
 
 FLAG_MASKED = 0x1
@@ -45,10 +45,12 @@ FLAG_CLAMP_PI = 0x40
 FLAG_CLAMP_MU = 0x80
 FLAG_IS_TRUNC = 0x100
 FLAG_IS_REJECT = 0x200
+FLAG_CLIPPED = 0x400
 
 # Symbols declared in include/sc.h.
-EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_center_forward_backward",
-           "sc_plan_query", "sc_status_string", "sc_last_error", "sc_abi_version"]
+EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_rollout_mean_advantages",
+           "sc_center_forward_backward", "sc_plan_query", "sc_status_string", "sc_last_error",
+           "sc_abi_version"]
 
 
 class ScError(RuntimeError):
@@ -70,6 +72,8 @@ class Params(ctypes.Structure):
         ("cluster_size", ctypes.c_int),
         ("threads", ctypes.c_int),
         ("stages", ctypes.c_int),
+        ("clip_low", ctypes.c_float),
+        ("clip_high", ctypes.c_float),
     ]
 
 
@@ -103,6 +107,8 @@ def lib():
             L.sc_params_default.restype = i32
             L.sc_group_advantages.argtypes = [vp, i32, i32, i32, f32, vp, vp]
             L.sc_group_advantages.restype = i32
+            L.sc_rollout_mean_advantages.argtypes = [vp, vp, i64, i32, vp, vp, vp]
+            L.sc_rollout_mean_advantages.restype = i32
             L.sc_center_forward_backward.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                                      ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
             L.sc_center_forward_backward.restype = i32
@@ -125,11 +131,13 @@ def _check(status: int):
 
 
 def params(K_max=128, is_mode=SC_IS_NONE, tis_max=2.0, mis_min=0.5, mis_max=5.0, centering=True,
-           inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0, stages=0) -> Params:
-    """Defaults are the settings table of the docs' "Score Centering" section."""
+           inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0, stages=0, clip_low=0.2,
+           clip_high=0.3) -> Params:
+    """Defaults are the settings table of the docs' "Score Centering" section
+    and the clip widths of the page's `grpo` preset."""
     return Params(int(K_max), int(is_mode), float(tis_max), float(mis_min), float(mis_max),
                   int(bool(centering)), float(inv_temperature), float(grad_scale), int(cluster_size),
-                  int(threads), int(stages))
+                  int(threads), int(stages), float(clip_low), float(clip_high))
 
 
 def _ptr(t):
@@ -176,6 +184,31 @@ def sc_group_advantages(rewards: torch.Tensor, n_groups: int, group_size: int,
     _check(lib().sc_group_advantages(_ptr(rewards), int(n_groups), int(group_size),
                                      int(bool(normalize_std)), float(eps), _ptr(out), _stream(stream)))
     return out
+
+
+def sc_rollout_mean_advantages(adv: torch.Tensor, row_response: torch.Tensor, out: torch.Tensor | None = None,
+                               counts: torch.Tensor | None = None, stream=None):
+    """Per-rollout mean: adv[r] / (valid tokens of response r), 0 if none.
+
+    adv float32 [n_resp], row_response int32 [T] on the same CUDA device.
+    Returns (adv_out, counts int32 [n_resp]); ``out`` may be ``adv``.
+    """
+    dev = adv.device
+    _need(adv, "adv", torch.float32, dev, 1)
+    _need(row_response, "row_response", torch.int32, dev, 1)
+    n = adv.numel()
+    out = torch.empty_like(adv) if out is None else out
+    counts = torch.empty(n, dtype=torch.int32, device=dev) if counts is None else counts
+    _need(out, "out", torch.float32, dev, 1)
+    _need(counts, "counts", torch.int32, dev, 1)
+    for name, t in [("adv", adv), ("row_response", row_response), ("out", out), ("counts", counts)]:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if out.numel() != n or counts.numel() != n:
+        raise ValueError("out and counts must have n_resp entries")
+    _check(lib().sc_rollout_mean_advantages(_ptr(adv), _ptr(row_response), int(row_response.numel()), int(n),
+                                            _ptr(counts), _ptr(out), _stream(stream)))
+    return out, counts
 
 
 def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | None,

@@ -1,4 +1,5 @@
-// sc_advantages.cu -- GRPO group advantages (one warp per group).
+// sc_advantages.cu -- GRPO group advantages (one warp per group) and the
+// per-rollout mean of the clipped GRPO baseline (advantage / valid tokens).
 //
 // Follows the "Training" section of the Agent Lightning "Score Centering"
 // docs page (rollout-level advantages with group standard-deviation
@@ -68,6 +69,31 @@ __global__ void __launch_bounds__(32) group_adv_kernel(const float* rewards, int
     }
 }
 
+// Valid tokens per response: rows of one response are mostly consecutive, so
+// the lanes of a warp that share a response index add their count once.
+__global__ void response_count_kernel(const int32_t* row_response, long long T, int n_resp, int32_t* counts) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long t0 = static_cast<long long>(blockIdx.x) * blockDim.x; t0 < T; t0 += stride) {
+        const long long t = t0 + threadIdx.x;
+        const int r = t < T ? row_response[t] : -1;
+        const bool valid = r >= 0 && r < n_resp;
+        const unsigned active = __ballot_sync(0xFFFFFFFFu, valid);
+        if (valid) {
+            const unsigned same = __match_any_sync(active, r);
+            const int lane = threadIdx.x & 31;
+            if ((same & ((1u << lane) - 1u)) == 0u) atomicAdd(counts + r, __popc(same));
+        }
+    }
+}
+
+__global__ void rollout_mean_kernel(const float* adv, const int32_t* counts, int n_resp, float* out) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < n_resp) {
+        const int c = counts[r];
+        out[r] = c > 0 ? adv[r] / static_cast<float>(c) : 0.0f;
+    }
+}
+
 }  // namespace
 }  // namespace sc
 
@@ -94,5 +120,34 @@ extern "C" int sc_group_advantages(const float* rewards, int n_groups, int group
         rewards, group_size, normalize_std ? 1 : 0, eps, adv_out);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "group_adv_kernel launch");
+    return ok();
+}
+
+extern "C" int sc_rollout_mean_advantages(const float* adv, const int32_t* row_response, long long T, int n_resp,
+                                          int32_t* counts_out, float* adv_out, sc_stream_t stream) {
+    using namespace sc;
+    if (T < 0) return fail(SC_ERR_SHAPE, "T = %lld < 0", T);
+    if (n_resp < 0) return fail(SC_ERR_SHAPE, "n_resp = %d < 0", n_resp);
+    if (n_resp == 0) return ok();
+    if (!adv || !counts_out || !adv_out) return fail(SC_ERR_NULL, "adv, counts_out and adv_out are required");
+    if (T > 0 && !row_response) return fail(SC_ERR_NULL, "row_response is NULL with T > 0");
+    if (!aligned(adv, 4) || !aligned(row_response, 4) || !aligned(counts_out, 4) || !aligned(adv_out, 4))
+        return fail(SC_ERR_ALIGN, "arrays must be 4-byte aligned");
+    int dev = 0;
+    int st = check_device(&dev);
+    if (st != SC_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(counts_out, 0, sizeof(int32_t) * static_cast<size_t>(n_resp), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counts)");
+    if (T > 0) {
+        const long long want = (T + 255) / 256;
+        const int blocks = static_cast<int>(want < 1024 ? want : 1024);
+        response_count_kernel<<<blocks, 256, 0, s>>>(row_response, T, n_resp, counts_out);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "response_count_kernel launch");
+    }
+    rollout_mean_kernel<<<(n_resp + 255) / 256, 256, 0, s>>>(adv, counts_out, n_resp, adv_out);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "rollout_mean_kernel launch");
     return ok();
 }

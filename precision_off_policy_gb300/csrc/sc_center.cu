@@ -125,7 +125,7 @@ struct KArgs {
     long long T, lstride, gstride;
     int V, K_max, n_resp;
     int is_mode, centering;
-    float tis_max, mis_min, mis_max, inv_t, grad_scale;
+    float tis_max, mis_min, mis_max, inv_t, grad_scale, clip_lo, clip_hi;
     int C, S, ncv, NB;
     Layout L;
 };
@@ -701,25 +701,30 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
                 const float logp_a = (ya - log2l) * kLn2;
                 const float dd = a.rollout ? logp_a - m.rl : 0.0f;
-                float wt = 1.0f;
+                // importance weight: w = exp(d) clipped, truncated or masked by mode
+                const float A = m.A;
+                const float w = a.is_mode != SC_IS_NONE ? expf(dd) : 1.0f;
+                float wt = w;
+                float wc = w;  // clipped GRPO: the clipped ratio
                 if (a.is_mode == SC_IS_TIS) {
-                    const float w = expf(dd);
                     if (w > a.tis_max) {
                         wt = a.tis_max;
                         flags |= SC_FLAG_IS_TRUNC;
-                    } else {
-                        wt = w;
                     }
                 } else if (a.is_mode == SC_IS_MIS) {
-                    const float w = expf(dd);
-                    if (w >= a.mis_min && w <= a.mis_max) {
-                        wt = w;
-                    } else {
+                    if (!(w >= a.mis_min && w <= a.mis_max)) {
                         wt = 0.0f;
                         flags |= SC_FLAG_IS_REJECT;
                     }
+                } else if (a.is_mode == SC_IS_CLIP) {
+                    // -min(w A, w_c A): the ratio's gradient where the unclipped
+                    // term is the minimum, none where the clipped one is
+                    wc = fminf(fmaxf(w, a.clip_lo), a.clip_hi);
+                    if (!(wc == w || w * A < wc * A)) {
+                        wt = 0.0f;
+                        flags |= SC_FLAG_CLIPPED;
+                    }
                 }
-                const float A = m.A;
                 const float Aw = A * wt;
                 const float alpha = -a.grad_scale * a.inv_t * Aw;
                 const float beta = -alpha * s;
@@ -743,7 +748,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     const float plogp = kLn2 * fmaf(-log2l, lH, EH) / l;
                     csum = fmaf(-rho, plogp, qlogp);
                 }
-                const float loss = -Aw * (logp_a - csum);
+                const float loss = a.is_mode == SC_IS_CLIP ? -fminf(w * A, wc * A) : -Aw * (logp_a - csum);
                 const float entropy = kLn2 * (log2l - (ET + EH) / l);
                 const float g_a_free = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
                 // gradient at the owned recorded ids, and how far it is from the
@@ -1201,7 +1206,12 @@ int check_params(int V, const sc_params* p) {
     if (!(p->inv_temperature > 0.0f) || !std::isfinite(p->inv_temperature) || p->inv_temperature > 1e4f)
         return fail(SC_ERR_ARG, "inv_temperature must be finite and in (0, 1e4]");
     if (!std::isfinite(p->grad_scale)) return fail(SC_ERR_ARG, "grad_scale must be finite");
-    if (p->is_mode < SC_IS_NONE || p->is_mode > SC_IS_MIS) return fail(SC_ERR_ARG, "is_mode = %d", p->is_mode);
+    if (p->is_mode < SC_IS_NONE || p->is_mode > SC_IS_CLIP) return fail(SC_ERR_ARG, "is_mode = %d", p->is_mode);
+    if (p->is_mode == SC_IS_CLIP) {
+        if (p->centering) return fail(SC_ERR_ARG, "is_mode clip is defined with centering = 0");
+        if (!(p->clip_low >= 0.0f && p->clip_low < 1.0f) || !(p->clip_high >= 0.0f) || !std::isfinite(p->clip_high))
+            return fail(SC_ERR_ARG, "need 0 <= clip_low < 1 and finite clip_high >= 0");
+    }
     if (p->is_mode == SC_IS_TIS && !(p->tis_max > 0.0f && std::isfinite(p->tis_max)))
         return fail(SC_ERR_ARG, "tis_max must be finite and > 0");
     if (p->is_mode == SC_IS_MIS &&
@@ -1320,6 +1330,8 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.mis_max = p->mis_max;
     ka.inv_t = p->inv_temperature;
     ka.grad_scale = p->grad_scale;
+    ka.clip_lo = 1.0f - p->clip_low;
+    ka.clip_hi = 1.0f + p->clip_high;
     ka.C = P.C;
     ka.S = P.S;
     ka.ncv = P.ncv;

@@ -80,6 +80,8 @@ int sc_params_default(sc_params* p) {
     p->cluster_size = 0;
     p->threads = 0;
     p->stages = 0;
+    p->clip_low = 0.2f;
+    p->clip_high = 0.3f;
     return sc::ok();
 }
 
@@ -98,6 +100,6 @@ const char* sc_status_string(int status) {
 
 const char* sc_last_error(void) { return sc::last_error_text(); }
 
-int sc_abi_version(void) { return 100; }
+int sc_abi_version(void) { return 101; }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ import precision_off_policy_gb300 as sc
 import synth
 
 CLAMP_BITS = oracle.FLAG_CLAMP_PI | oracle.FLAG_CLAMP_MU
-IS_BITS = oracle.FLAG_IS_TRUNC | oracle.FLAG_IS_REJECT
+IS_BITS = oracle.FLAG_IS_TRUNC | oracle.FLAG_IS_REJECT | oracle.FLAG_CLIPPED
 
 
 def ulp_bf16(x):
@@ -56,7 +56,8 @@ def oracle_params(p: sc.Params):
     # The library takes its scalars in FP32; the oracle takes the same values.
     return oracle.make_params(is_mode=p.is_mode, tis_max=p.tis_max, mis_min=p.mis_min, mis_max=p.mis_max,
                               centering=bool(p.centering), inv_temperature=float(np.float32(p.inv_temperature)),
-                              grad_scale=float(np.float32(p.grad_scale)))
+                              grad_scale=float(np.float32(p.grad_scale)), clip_low=p.clip_low,
+                              clip_high=p.clip_high)
 
 
 def run_gpu(batch, p, adv: np.ndarray, inplace=False, with_rollout=True, stream=None):

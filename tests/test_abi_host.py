@@ -41,14 +41,14 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_struct_layouts_match_header(L):
-    assert ctypes.sizeof(sc.Params) == 44
+    assert ctypes.sizeof(sc.Params) == 52
     assert sc.DIAG_DTYPE.itemsize == 64
     p = sc.Params()
     assert L.sc_params_default(ctypes.byref(p)) == sc.SC_OK
     assert (p.K_max, p.is_mode, p.tis_max, p.mis_min, p.mis_max, p.centering) == (128, 0, 2.0, 0.5, 5.0, 1)
     assert (p.inv_temperature, p.grad_scale, p.cluster_size, p.threads, p.stages) == (1.0, 1.0, 0, 0, 0)
     assert L.sc_params_default(None) == sc.SC_ERR_NULL
-    assert L.sc_abi_version() == 100
+    assert L.sc_abi_version() == 101
     assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
 
 
@@ -81,7 +81,12 @@ def err(L):
     (dict(inv_temperature=0.0), sc.SC_ERR_ARG),
     (dict(inv_temperature=float("inf")), sc.SC_ERR_ARG),
     (dict(grad_scale=float("nan")), sc.SC_ERR_ARG),
-    (dict(is_mode=3), sc.SC_ERR_ARG),
+    (dict(is_mode=4), sc.SC_ERR_ARG),
+    (dict(is_mode=3, roll=FAKE * 9), sc.SC_ERR_ARG),                              # clip needs centering 0
+    (dict(is_mode=3, roll=FAKE * 9, centering=0, clip_low=1.0), sc.SC_ERR_ARG),
+    (dict(is_mode=3, roll=FAKE * 9, centering=0, clip_high=-0.1), sc.SC_ERR_ARG),
+    (dict(is_mode=3, roll=FAKE * 9, centering=0, clip_high=float("inf")), sc.SC_ERR_ARG),
+    (dict(is_mode=3, centering=0), sc.SC_ERR_NULL),                                # clip needs the old logprob
     (dict(is_mode=1, roll=FAKE * 9, tis_max=0.0), sc.SC_ERR_ARG),
     (dict(is_mode=2, roll=FAKE * 9, mis_min=3.0, mis_max=1.0), sc.SC_ERR_ARG),
     (dict(is_mode=1), sc.SC_ERR_NULL),
@@ -152,3 +157,21 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
         sc.lib()
     monkeypatch.undo()
     assert sc.lib() is not None
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE * 2, -1, 4, FAKE * 3, FAKE * 4), sc.SC_ERR_SHAPE),
+    ((FAKE, FAKE * 2, 8, -1, FAKE * 3, FAKE * 4), sc.SC_ERR_SHAPE),
+    ((None, FAKE * 2, 8, 4, FAKE * 3, FAKE * 4), sc.SC_ERR_NULL),
+    ((FAKE, None, 8, 4, FAKE * 3, FAKE * 4), sc.SC_ERR_NULL),
+    ((FAKE, FAKE * 2, 8, 4, None, FAKE * 4), sc.SC_ERR_NULL),
+    ((FAKE, FAKE * 2, 8, 4, FAKE * 3, None), sc.SC_ERR_NULL),
+    ((FAKE + 2, FAKE * 2, 8, 4, FAKE * 3, FAKE * 4), sc.SC_ERR_ALIGN),
+    ((FAKE, FAKE * 2 + 1, 8, 4, FAKE * 3, FAKE * 4), sc.SC_ERR_ALIGN),
+])
+def test_rollout_mean_rejects_bad_arguments_on_the_host(L, args, status):
+    assert L.sc_rollout_mean_advantages(*args, None) == status, err(L)
+
+
+def test_rollout_mean_no_responses_is_a_no_op(L):
+    assert L.sc_rollout_mean_advantages(None, None, 8, 0, None, None, None) == sc.SC_OK

@@ -18,7 +18,7 @@ import oracle
 import precision_off_policy_gb300 as sc
 import synth
 from sc_parity import (bits_to_f64, check_rows, diag_rows, grad_bits, host_batch, oracle_adv,
-                       run_gpu, sc_params, ulp_bf16)
+                       oracle_params, run_gpu, sc_params, ulp_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -153,6 +153,54 @@ def test_importance_weighting_modes(mode, centering):
     assert np.any(flags & bit), "the test inputs should exercise the weight bound"
 
 
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_clipped_grpo_mode(sign):
+    """The clipped GRPO baseline: a wide sampler mismatch spreads the ratio
+    across both clip bounds; the advantages are the per-rollout means."""
+    cfg = synth.config("C1", sigma_s=1.5, L_pad=16)
+    batch = synth.make_batch(cfg)
+    p = sc_params(batch, is_mode=sc.SC_IS_CLIP, centering=False, grad_scale=1.0 / 8)
+    adv = (sign * np.abs(oracle_adv(batch)) + 0.25 * sign).astype(np.float32)  # one sign per run
+    g, lp, d, _ = run_gpu(batch, p, adv)
+    bn = host_batch(batch, adv)
+    G, LA, OUT, _ = oracle.rows(bn, oracle_params(p), np.arange(len(lp)))
+    w = np.exp(LA - bn["rollout_logprob"].astype(np.float64))
+    ok = np.all([np.abs(w - b) > 1e-3 * b for b in [1.0 - 0.2, 1.0 + 0.3]], axis=0)
+    rows = np.nonzero(ok)[0]
+    assert rows.size >= len(lp) // 2
+    check_rows(bn, p, rows, grad_bits(g, rows), lp.cpu().numpy()[rows], diag_rows(d, rows), what=f"clip A{sign:+}")
+    flags = sc.diag_to_numpy(d)["flags"][rows]
+    np.testing.assert_array_equal(flags & sc.FLAG_CLIPPED, OUT["flags"][rows] & oracle.FLAG_CLIPPED)
+    assert np.any(flags & sc.FLAG_CLIPPED), "some rows should have the clipped term as the minimum"
+    assert np.any((flags & sc.FLAG_CLIPPED) == 0) and np.any(~((w > 0.8) & (w < 1.3))[rows] & ((flags & sc.FLAG_CLIPPED) == 0)), \
+        "some rows outside the clip range should keep their gradient"
+    gr = g.float().cpu().numpy()[rows]
+    assert np.all(gr[(flags & sc.FLAG_CLIPPED) != 0] == 0)
+
+
+def test_rollout_mean_advantages_match_oracle():
+    for name in ["C1", "C2", "C5"]:
+        cfg = synth.config(name)
+        lengths, rewards = synth.responses(cfg)
+        L = cfg["L_pad"]
+        n_resp = rewards.numel()
+        rows = torch.arange(n_resp * L)
+        rr = torch.where((rows % L) < lengths[rows // L], rows // L, torch.full_like(rows, -1)).to(torch.int32)
+        rr[5] = n_resp + 3  # an out-of-range index counts for nobody
+        adv = oracle.group_advantages(rewards.numpy(), n_resp // cfg["n_per_prompt"], cfg["n_per_prompt"])
+        adv32 = adv.astype(np.float32)
+        out, counts = sc.sc_rollout_mean_advantages(torch.from_numpy(adv32).cuda(), rr.cuda())
+        ref, rc = oracle.rollout_mean_advantages(adv32.astype(np.float64), rr.numpy(), n_resp)
+        assert counts.cpu().numpy().tolist() == rc.tolist(), name
+        np.testing.assert_array_equal(out.cpu().numpy(), ref.astype(np.float32), err_msg=name)
+    # in place, and an empty batch of rows
+    a = torch.tensor([2.0, -1.0], device="cuda")
+    out, counts = sc.sc_rollout_mean_advantages(a, torch.tensor([0, 0, 1, 0], dtype=torch.int32, device="cuda"), out=a)
+    assert a.cpu().tolist() == [float(np.float32(2.0) / np.float32(3.0)), -1.0]
+    out, counts = sc.sc_rollout_mean_advantages(a, torch.zeros(0, dtype=torch.int32, device="cuda"))
+    assert out.cpu().tolist() == [0.0, 0.0] and counts.cpu().tolist() == [0, 0]
+
+
 def test_temperature_and_grad_scale():
     cfg = synth.config("C1", temperature=0.7, L_pad=12)
     batch = synth.make_batch(cfg)
@@ -261,7 +309,7 @@ def test_autograd_wrapper_matches_direct_call():
     assert torch.equal(logits.grad, g * 2.0)
     assert torch.equal(logp, lp) and torch.equal(diag, d)
     rows = sc.diag_to_numpy(d)["loss"].astype(np.float64)
-    assert abs(float(loss) - rows.sum() / 64.0) <= 1e-5 * max(1.0, abs(rows.sum() / 64.0))
+    assert abs(float(loss.detach()) - rows.sum() / 64.0) <= 1e-5 * max(1.0, abs(rows.sum() / 64.0))
 
 
 def _unprotected(batch):
