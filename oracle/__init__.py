@@ -120,6 +120,10 @@ def lib():
             L.sco_rollout_mean_advantages.restype = ctypes.c_int
             L.sco_rollout_mean_advantages.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong,
                                                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+            L.sco_topk_capture.restype = ctypes.c_int
+            L.sco_topk_capture.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_longlong,
+                                           ctypes.c_double, ctypes.c_int, ctypes.c_double, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p]
             L.sco_row.restype = ctypes.c_uint
             L.sco_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
@@ -194,6 +198,23 @@ def rollout_mean_advantages(adv, row_response, n_resp: int):
     if rc != 0:
         raise ValueError("sco_rollout_mean_advantages rejected its arguments")
     return out, counts
+
+
+def topk_capture(logits, K: int, inv_temperature: float = 1.0, top_p: float = 1.0):
+    """Sampler-side capture of the top-K behaviour probabilities (FP32 logits
+    [T, V]).  Returns (ids int32 [T, K], logprobs float32 [T, K], count int32 [T])."""
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    if z.ndim != 2:
+        raise ValueError("logits must be [T, V]")
+    T, V = z.shape
+    ids = np.zeros((T, K), dtype=np.int32)
+    lp = np.zeros((T, K), dtype=np.float32)
+    cnt = np.zeros(T, dtype=np.int32)
+    rc = lib().sco_topk_capture(_ptr(z), T, V, V, float(inv_temperature), int(K), float(top_p), _ptr(ids),
+                                _ptr(lp), _ptr(cnt))
+    if rc != 0:
+        raise ValueError("sco_topk_capture rejected its arguments")
+    return ids, lp, cnt
 
 
 def row(z_bits, ids, logprobs, a: int, A: float, params: Params | None = None,

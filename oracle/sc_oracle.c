@@ -493,3 +493,70 @@ int sco_rows(const uint16_t* logits, long long T, int V, long long row_stride, c
 
 int sco_row_out_size(void) { return (int)sizeof(sco_row_out); }
 int sco_params_size(void) { return (int)sizeof(sco_params); }
+
+/* ---- sampler-side top-K capture ---------------------------------------- */
+
+/* What the sampler records per generated position (docs page "Score
+ * Centering", section "Score Centering": the top K behaviour probabilities
+ * of the sampling call, with their original normalisation).  The behaviour
+ * distribution is mu = softmax(z * inv_t) over the V sampler logits z, or,
+ * with top_p < 1, that distribution restricted to its nucleus -- the
+ * smallest prefix of the entries sorted by probability whose preceding mass
+ * is below top_p -- and renormalised.  Entries are sorted by z, larger
+ * first, equal values by lower id.  Row t gets count = min(K, V, nucleus
+ * size) ids and log mu values; the entries past the count hold id -1 and 0.
+ * Plain definition: a full sort of the row, FP64 sums in sorted order. */
+typedef struct {
+    float z;
+    int id;
+} sco_entry;
+
+static int sco_entry_cmp(const void* pa, const void* pb) {
+    const sco_entry* a = (const sco_entry*)pa;
+    const sco_entry* b = (const sco_entry*)pb;
+    if (a->z > b->z) return -1;
+    if (a->z < b->z) return 1;
+    return (a->id > b->id) - (a->id < b->id);
+}
+
+int sco_topk_capture(const float* logits, long long T, int V, long long row_stride, double inv_t, int K,
+                     double top_p, int32_t* ids_out, float* lp_out, int32_t* count_out) {
+    if (T < 0 || V <= 0 || row_stride < V || K < 0 || !(inv_t > 0.0) || !(top_p > 0.0 && top_p <= 1.0))
+        return -1;
+    if (T == 0 || K == 0) return 0;
+    if (!logits || !ids_out || !lp_out) return -1;
+    sco_entry* e = (sco_entry*)malloc(sizeof(sco_entry) * (size_t)V);
+    if (!e) return -1;
+    for (long long t = 0; t < T; ++t) {
+        const float* z = logits + t * row_stride;
+        for (int v = 0; v < V; ++v) {
+            e[v].z = z[v];
+            e[v].id = v;
+        }
+        qsort(e, (size_t)V, sizeof(sco_entry), sco_entry_cmp);
+        /* log-sum-exp of the tempered logits, in sorted order */
+        double m = (double)e[0].z * inv_t, l = 0.0;
+        for (int i = 0; i < V; ++i) l += exp((double)e[i].z * inv_t - m);
+        double lse = m + log(l);
+        long long n_keep = V;
+        double lognuc = 0.0;
+        if (top_p < 1.0) {
+            double cum = 0.0;
+            long long i = 0;
+            while (i < V && cum < top_p) {
+                cum += exp((double)e[i].z * inv_t - lse);
+                ++i;
+            }
+            n_keep = i;
+            lognuc = log(cum);
+        }
+        int cnt = (int)(n_keep < K ? n_keep : K);
+        for (int k = 0; k < K; ++k) {
+            ids_out[t * K + k] = k < cnt ? e[k].id : -1;
+            lp_out[t * K + k] = k < cnt ? (float)((double)e[k].z * inv_t - lse - lognuc) : 0.0f;
+        }
+        if (count_out) count_out[t] = cnt;
+    }
+    free(e);
+    return 0;
+}

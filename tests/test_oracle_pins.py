@@ -621,3 +621,78 @@ def test_rollout_mean_advantages_hand_counts():
     # agrees with a bincount over the valid response indices
     ok = (rr >= 0) & (rr < 5)
     assert counts.tolist() == np.bincount(rr[ok], minlength=5).tolist()
+
+
+# --------------------------------------------------------------------------
+# Sampler-side top-K capture (the top K behaviour probabilities recorded per
+# generated position, docs page "Score Centering").
+
+
+def test_topk_capture_hand_worked_nucleus():
+    # p = [1/2, 1/4, 1/8, 1/8]; top_p 0.7: the mass before entry 1 is 1/2 < 0.7 and
+    # before entry 2 it is 3/4 >= 0.7, so the nucleus is {0, 1} with mass 3/4.
+    z = np.log(np.array([[4.0, 2.0, 1.0, 1.0]])).astype(np.float32)
+    ids, lp, cnt = oracle.topk_capture(z, 3, 1.0, 0.7)
+    assert ids.tolist() == [[0, 1, -1]] and cnt.tolist() == [2]
+    np.testing.assert_allclose(lp[0, :2], np.log([2 / 3, 1 / 3]), rtol=1e-6)
+    ids, lp, cnt = oracle.topk_capture(z, 3, 1.0, 1.0)
+    assert ids.tolist() == [[0, 1, 2]] and cnt.tolist() == [3]  # the tie 2/3 goes to the lower id
+    np.testing.assert_allclose(lp[0], np.log([0.5, 0.25, 0.125]), rtol=1e-6)
+
+
+def test_topk_capture_equal_logits_and_short_rows():
+    z = np.full((2, 300), 1.25, dtype=np.float32)
+    ids, lp, cnt = oracle.topk_capture(z, 128)
+    assert np.all(ids == np.arange(128)) and np.all(cnt == 128)
+    np.testing.assert_allclose(lp, -np.log(300.0), rtol=1e-6)
+    ids, lp, cnt = oracle.topk_capture(z[:, :5], 8)  # K > V: every id, then padding
+    assert ids[0].tolist() == [0, 1, 2, 3, 4, -1, -1, -1] and cnt.tolist() == [5, 5]
+
+
+def test_topk_capture_geometric_closed_form():
+    # z_v = -v ln 2 at inv_t = 1: p_v = 2^-v / S with S = 2 (1 - 2^-V)
+    V, K = 60, 16
+    z = (-np.arange(V) * np.log(2.0)).astype(np.float32)[None, :]
+    S = 2.0 * (1.0 - 2.0 ** -V)
+    zz = z[0].astype(np.float64)
+    ids, lp, cnt = oracle.topk_capture(z, K)
+    assert ids[0].tolist() == list(range(K))
+    np.testing.assert_allclose(lp[0], zz[:K] - np.log(np.exp(zz).sum()), rtol=1e-6)
+    np.testing.assert_allclose(lp[0], -np.arange(K) * np.log(2.0) - np.log(S), rtol=1e-5)
+    # top_p 0.9: the mass before entry n is (1 - 2^-n) / (1 - 2^-V); it first reaches 0.9 at n = 4
+    ids, lp, cnt = oracle.topk_capture(z, K, 1.0, 0.9)
+    assert cnt.tolist() == [4] and ids[0, :4].tolist() == [0, 1, 2, 3]
+    nuc = (1.0 - 2.0 ** -4) / (1.0 - 2.0 ** -V)
+    np.testing.assert_allclose(lp[0, :4], -np.arange(4) * np.log(2.0) - np.log(S) - np.log(nuc), rtol=1e-5)
+
+
+@pytest.mark.parametrize("inv_t,top_p", [(1.0, 1.0), (1 / 0.7, 1.0), (1 / 0.7, 0.95), (2.0, 0.5)])
+def test_topk_capture_selection_invariants(inv_t, top_p):
+    rng = np.random.default_rng(int(inv_t * 10 + top_p * 100))
+    T, V, K = 6, 2000, 64
+    z = (rng.standard_normal((T, V)) * 3.0).astype(np.float32)
+    z[:, 100:140] = z[:, 99:100]  # a run of equal values
+    ids, lp, cnt = oracle.topk_capture(z, K, inv_t, top_p)
+    for t in range(T):
+        c = cnt[t]
+        sel = ids[t, :c]
+        assert np.all(ids[t, c:] == -1) and len(set(sel.tolist())) == c
+        rest = np.setdiff1d(np.arange(V), sel)
+        # every selected value is at least every unselected one; among equal values the lower ids win
+        assert z[t, sel].min() >= z[t, rest].max()
+        edge = z[t, sel].min()
+        assert np.all(rest[z[t, rest] == edge] > sel[z[t, sel] == edge].max())
+        # sorted by value, larger first
+        assert np.all(np.diff(z[t, sel].astype(np.float64)) <= 0)
+        ls = log_softmax(z[t].astype(np.float64) * inv_t)
+        if top_p == 1.0:
+            assert c == K
+            np.testing.assert_allclose(lp[t, :c], ls[sel], rtol=1e-6, atol=1e-6)
+        else:
+            # brute force: the nucleus is the shortest sorted prefix whose preceding mass is below top_p
+            order = np.lexsort((np.arange(V), -z[t].astype(np.float64)))
+            before = np.concatenate([[0.0], np.cumsum(np.exp(ls[order]))[:-1]])
+            n_keep = int((before < top_p).sum())
+            assert c == min(K, n_keep)
+            nuc = np.exp(ls[order[:n_keep]]).sum()
+            np.testing.assert_allclose(lp[t, :c], ls[sel] - np.log(nuc), rtol=1e-6, atol=1e-6)
