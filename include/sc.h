@@ -134,6 +134,33 @@ typedef struct sc_row_diag {
     uint32_t reserved;
 } sc_row_diag;
 
+/*
+ * Sampler-side capture of the top K behaviour probabilities (docs page
+ * "Score Centering", section "Score Centering": each generated position
+ * records the top K probabilities of the sampling call, with their original
+ * normalisation).  The behaviour distribution is mu = softmax(z * inv_t)
+ * over the V sampler logits, or, with top_p < 1, that distribution
+ * restricted to its nucleus -- the shortest prefix of the entries sorted by
+ * probability whose preceding mass is below top_p -- and renormalised.
+ * Entries are ordered by z, larger first, equal values by lower id.
+ *
+ * logits       : FP32 [T, logits_stride] sampler logits (device), 16-byte
+ *                aligned, logits_stride % 4 == 0, >= V; each row holds at
+ *                least one finite value (-inf entries carry no mass).
+ * ids_out      : int32 [T, K] the recorded ids, row t at t * K; entries past
+ *                the row's count hold -1.
+ * logprobs_out : FP32 [T, K] log mu of those ids (0 past the count).
+ * count_out    : int32 [T] min(K, V, nucleus size), or NULL.
+ * K            : 1..1024.  inv_temperature finite > 0.  top_p in (0, 1].
+ * Asynchronous on `stream`; nothing is allocated.  Sums are taken in 2^-40
+ * fixed point, so results do not depend on the order of the additions.
+ * Errors: SC_ERR_SHAPE (T < 0, V outside 1..2^24, K, stride), SC_ERR_ARG,
+ * SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
+ */
+int sc_topk_capture(const float* logits, long long T, int V, long long logits_stride, float inv_temperature,
+                    int K, float top_p, int32_t* ids_out, float* logprobs_out, int32_t* count_out,
+                    sc_stream_t stream);
+
 /* Fills *p with the defaults above.  Returns SC_OK or SC_ERR_NULL. */
 int sc_params_default(sc_params* p);
 

@@ -28,7 +28,7 @@ __all__ = [
     "build", "lib", "ScError", "Params", "params", "DIAG_DTYPE", "DIAG_FIELDS",
     "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
     "ScoreCenteredLoss", "score_centered_loss",
-    "sc_rollout_mean_advantages", "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS", "SC_IS_CLIP",
+    "sc_rollout_mean_advantages", "sc_topk_capture", "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS", "SC_IS_CLIP",
 ]
 
 SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
@@ -48,7 +48,7 @@ FLAG_IS_REJECT = 0x200
 FLAG_CLIPPED = 0x400
 
 # Symbols declared in include/sc.h.
-EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_rollout_mean_advantages",
+EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_rollout_mean_advantages", "sc_topk_capture",
            "sc_center_forward_backward", "sc_plan_query", "sc_status_string", "sc_last_error",
            "sc_abi_version"]
 
@@ -109,6 +109,8 @@ def lib():
             L.sc_group_advantages.restype = i32
             L.sc_rollout_mean_advantages.argtypes = [vp, vp, i64, i32, vp, vp, vp]
             L.sc_rollout_mean_advantages.restype = i32
+            L.sc_topk_capture.argtypes = [vp, i64, i32, i64, f32, i32, f32, vp, vp, vp, vp]
+            L.sc_topk_capture.restype = i32
             L.sc_center_forward_backward.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                                      ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
             L.sc_center_forward_backward.restype = i32
@@ -209,6 +211,35 @@ def sc_rollout_mean_advantages(adv: torch.Tensor, row_response: torch.Tensor, ou
     _check(lib().sc_rollout_mean_advantages(_ptr(adv), _ptr(row_response), int(row_response.numel()), int(n),
                                             _ptr(counts), _ptr(out), _stream(stream)))
     return out, counts
+
+
+def sc_topk_capture(logits: torch.Tensor, K: int, inv_temperature: float = 1.0, top_p: float = 1.0,
+                    ids_out: torch.Tensor | None = None, logprobs_out: torch.Tensor | None = None,
+                    count_out: torch.Tensor | None = None, V: int | None = None, stream=None):
+    """Sampler-side top-K capture.  logits: FP32 [T, >=V] on a CUDA device with
+    contiguous rows.  Returns (ids int32 [T, K], logprobs float32 [T, K],
+    count int32 [T])."""
+    dev = logits.device
+    if dev.type != "cuda":
+        raise ValueError("logits must be on a CUDA device")
+    _need(logits, "logits", torch.float32, dev, 2)
+    T = logits.shape[0]
+    V = logits.shape[1] if V is None else int(V)
+    K = int(K)
+    ids_out = torch.empty((T, K), dtype=torch.int32, device=dev) if ids_out is None else ids_out
+    logprobs_out = torch.empty((T, K), dtype=torch.float32, device=dev) if logprobs_out is None else logprobs_out
+    count_out = torch.empty(T, dtype=torch.int32, device=dev) if count_out is None else count_out
+    _need(ids_out, "ids_out", torch.int32, dev, 2)
+    _need(logprobs_out, "logprobs_out", torch.float32, dev, 2)
+    _need(count_out, "count_out", torch.int32, dev, 1)
+    for name, t in [("ids_out", ids_out), ("logprobs_out", logprobs_out), ("count_out", count_out)]:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if T == 0:
+        return ids_out, logprobs_out, count_out
+    _check(lib().sc_topk_capture(_ptr(logits), T, V, _rows(logits, "logits"), float(inv_temperature), K,
+                                 float(top_p), _ptr(ids_out), _ptr(logprobs_out), _ptr(count_out), _stream(stream)))
+    return ids_out, logprobs_out, count_out
 
 
 def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | None,

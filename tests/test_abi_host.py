@@ -175,3 +175,30 @@ def test_rollout_mean_rejects_bad_arguments_on_the_host(L, args, status):
 
 def test_rollout_mean_no_responses_is_a_no_op(L):
     assert L.sc_rollout_mean_advantages(None, None, 8, 0, None, None, None) == sc.SC_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=-1), sc.SC_ERR_SHAPE),
+    (dict(V=0), sc.SC_ERR_SHAPE),
+    (dict(K=0), sc.SC_ERR_SHAPE),
+    (dict(K=1025), sc.SC_ERR_SHAPE),
+    (dict(stride=60), sc.SC_ERR_SHAPE),
+    (dict(inv_t=0.0), sc.SC_ERR_ARG),
+    (dict(top_p=0.0), sc.SC_ERR_ARG),
+    (dict(top_p=1.5), sc.SC_ERR_ARG),
+    (dict(logits=None), sc.SC_ERR_NULL),
+    (dict(ids=None), sc.SC_ERR_NULL),
+    (dict(lps=None), sc.SC_ERR_NULL),
+    (dict(logits=FAKE + 4), sc.SC_ERR_ALIGN),
+    (dict(stride=66), sc.SC_ERR_ALIGN),
+    (dict(cnt=FAKE * 4 + 2), sc.SC_ERR_ALIGN),
+])
+def test_topk_capture_rejects_bad_arguments_on_the_host(L, kw, status):
+    a = dict(logits=FAKE, T=3, V=64, stride=64, inv_t=1.0, K=8, top_p=1.0, ids=FAKE * 2, lps=FAKE * 3, cnt=None)
+    a.update(kw)
+    assert L.sc_topk_capture(a["logits"], a["T"], a["V"], a["stride"], a["inv_t"], a["K"], a["top_p"], a["ids"],
+                             a["lps"], a["cnt"], None) == status, err(L)
+
+
+def test_topk_capture_empty_batch_is_a_no_op(L):
+    assert L.sc_topk_capture(None, 0, 64, 64, 1.0, 8, 1.0, None, None, None, None) == sc.SC_OK
