@@ -313,9 +313,9 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
     // scalar warp state kept for the final row-sum flush
     bool clean_end = false;
     uint32_t nrows = 0;
-    float fin_rs2 = 0.0f, fin_rs1 = 0.0f;
-    long long t_m1 = -1, t_m2 = -1;  // row indices of the two rows before the current one
-    float corr_m1 = 0.0f, corr_m2 = 0.0f;  // their row-sum corrections for the patched entries
+    float fin_rs1 = 0.0f;
+    long long t_m1 = -1;    // row index of the row before the current one
+    float corr_m1 = 0.0f;   // its row-sum correction for the patched entries
 
     // The write pass stores g = beta p everywhere; once it is done with row r,
     // the scalar warp overwrites the recorded ids and a with their own values.
@@ -533,6 +533,36 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
         for (uint32_t j = 0;; ++j) {
             if (flag_up()) break;
             const int p = static_cast<int>(j & 1u);
+            {
+                // While the streaming warps run phase A of row j, gather the logits
+                // of its recorded ids and of a from global memory (the slice's copies
+                // have brought them into L2 or have them in flight).
+                const int msg = static_cast<int>(j % kMetaSlots);
+                const bool mready = mbar_wait_bounded(meta_bar(msg, kMetaFull), (j / kMetaSlots) & 1u, kWaitLimitNs);
+                if (!__all_sync(kFull, mready)) {
+                    give_up(SC_STATUS_TIMEOUT_LOAD);
+                    break;
+                }
+                const long long tg = meta[msg].t;
+                if (tg >= 0) {
+                    const int ng = meta[msg].nown, ag = meta[msg].a_li;
+                    const uint16_t* lrow = a.logits + tg * a.lstride + lo;
+                    const int* lig = list_li + msg * cap;
+                    float* fz = fix_z + p * cap;
+                    int idx[4];
+                    uint16_t zr[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) idx[r] = lane + 32 * r < ng ? lig[lane + 32 * r] : -1;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) zr[r] = idx[r] >= 0 ? lrow[idx[r]] : static_cast<uint16_t>(0);
+                    const uint16_t za = (lane == 0 && ag >= 0) ? lrow[ag] : static_cast<uint16_t>(0);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        if (idx[r] >= 0) fz[lane + 32 * r] = bf_to_f(zr[r]);
+                    for (int e = lane + 128; e < ng; e += 32) fz[e] = bf_to_f(lrow[lig[e]]);
+                    if (lane == 0 && ag >= 0) zav[p] = bf_to_f(za);
+                }
+            }
             const bool got = mbar_wait_bounded(adone(p), (j >> 1) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, got)) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
@@ -540,22 +570,22 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
             }
             const int ms = static_cast<int>(j % kMetaSlots);
             const RowMeta m = meta[ms];
-            // The write pass of row j - 2 ended before phase A of row j in every
-            // streaming warp: its special entries can be patched, its row sum is
-            // complete and its slot can be refilled.
-            float rs2 = 0.0f;
-            if (j >= 2) {
-                patch_row(j - 2, t_m2);
-                rs2 = warp_sum(lane < NCW ? rsw[((j - 2) & 1u) * NCW + lane] : 0.0f) + corr_m2;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(meta_bar(static_cast<int>((j - 2) % kMetaSlots), kMetaFree));
-            }
-            if (m.t < 0) {  // end of the stream: the last two rows' sums go to CTA 0 below
-                fin_rs2 = rs2;
+            // The write pass of row j - 1 ended before phase A of row j in every
+            // streaming warp: its row sum is complete (it rides with this row's
+            // record), and its special entries can be patched once the record is
+            // on its way.
+            float rs1 = 0.0f;
+            if (j >= 1) rs1 = warp_sum(lane < NCW ? rsw[((j - 1) & 1u) * NCW + lane] : 0.0f) + corr_m1;
+            auto finish_prev = [&]() {
                 if (j >= 1) {
                     patch_row(j - 1, t_m1);
-                    fin_rs1 = warp_sum(lane < NCW ? rsw[((j - 1) & 1u) * NCW + lane] : 0.0f) + corr_m1;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(meta_bar(static_cast<int>((j - 1) % kMetaSlots), kMetaFree));
                 }
+            };
+            if (m.t < 0) {  // end of the stream: the last row's sum goes to CTA 0 below
+                finish_prev();
+                fin_rs1 = rs1;
                 nrows = j;
                 clean_end = true;
                 break;
@@ -604,7 +634,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     r.m = cm.m;
                     r.S1 = cm.s1;
                     r.S2 = cm.s2;
-                    r.rs = rs2;
+                    r.rs = rs1;
                     r.lH = lH;
                     r.EH = EH;
                     r.QY = QY;
@@ -630,6 +660,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     }
                 }
             }
+            finish_prev();  // while the peers' records are on their way
             // ---- all C records of row j: the row scalars ----
             const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j >> 2) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, ok)) {
@@ -768,7 +799,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 corr = warp_sum(corr);
                 if (a_li >= 0 && !__any_sync(kFull, a_rec))
                     corr += g_a_free - beta * ex2(fmaf(zav[p], kscale, -bw));
-                corr_m2 = corr_m1;
                 corr_m1 = corr;
                 if (lane == 0) {
                     scal[4 * p + 2] = g_a_free;  // read back by this warp when it patches the row
@@ -780,18 +810,17 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                             dp[1] = make_float4(Q_H, tail_mu, rho, s);
                             dp[2] = make_float4(entropy, k3, wt, 0.0f);
                             dp[3] = make_float4(A, __int_as_float(nval), __uint_as_float(flags), 0.0f);
-                            // the records of row j carried the row sums of row j - 2
-                            if (j >= 2) a.diag[t_m2].row_sum = rsum;
+                            // the records of row j carried the row sums of row j - 1
+                            if (j >= 1) a.diag[t_m1].row_sum = rsum;
                         }
                         if (flags & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
                     }
                 }
             }
-            t_m2 = t_m1;
             t_m1 = m.t;
         }
     } else {
-        // ================= streaming warps: phase A of row i, write pass of row i - 1 =================
+        // ================= streaming warps: phase A of row i, then its write pass =================
         for (uint32_t i = 0;; ++i) {
             if (flag_up()) break;
             const int ms = static_cast<int>(i % kMetaSlots);
@@ -802,16 +831,18 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 break;
             }
             const RowMeta m = meta[ms];
-            const bool have_cur = m.t >= 0;
-            if (have_cur) {
+            if (m.t < 0) {  // end of the stream: every row of this warp is written
+                __syncwarp();
+                if (lane == 0) mbar_arrive(adone(static_cast<int>(i & 1u)));
+                break;
+            }
+            const int p = static_cast<int>(i & 1u);
+            {
                 // ------------- phase A: one pass over the slice in shared memory -------------
-                const int p = static_cast<int>(i & 1u);
                 const int ds = static_cast<int>(i % NB);
                 const uint32_t fpar = (i / NB) & 1u;
                 const uint32_t buf_s = smem_addr(smem + ds * L.stage_bytes);
-                const int* li_s = list_li + ms * cap;
                 const uint32_t* bm = bitmap + ms * nwords;
-                const int nown = m.nown, a_li = m.a_li;
                 // The exponent offset is the largest logit among the slice's first 32
                 // vectors -- every warp reads the same ones and reduces them the same
                 // way, so the whole CTA shares it without a barrier -- fixed for the
@@ -821,9 +852,11 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 // vectors exactly (its maximum first).  Vectors holding a recorded id
                 // take the rare per-entry path.
                 bool timed_out = false;
+                // Nothing reads the slice from shared memory after the pass (the
+                // scalar warp gathers the recorded ids' logits from global memory).
                 float mz = -INFINITY;
-                if (nchunks > 0) {
-                    timed_out = !mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, kWaitLimitNs);
+                if (nchunks > 0) {  // (waits decided warp-wide)
+                    timed_out = !__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, kWaitLimitNs));
                     if (!timed_out && lane < nvb) {
                         const uint4 w = lds128(buf_s + 16u * lane);
                         const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
@@ -838,7 +871,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 f2_t S1a = 0ull, S1b = 0ull, S2a = 0ull, S2b = 0ull;
                 float s1x = 0.0f, s2x = 0.0f;  // entries taken one by one
                 for (int c = 0; c < nchunks && !timed_out; ++c) {
-                    if (!mbar_wait_bounded(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs)) {
+                    if (!__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs))) {
                         timed_out = true;
                         break;
                     }
@@ -897,9 +930,11 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 if (!timed_out && !ok) {
                     // exact: this thread's maximum, then its sums relative to it (also
                     // the path of -inf logits, whose 0 * -inf made the fast sums NaN)
+                    // (from global memory: the shared-memory slice may already be refilled)
+                    const uint4* grow4 = reinterpret_cast<const uint4*>(a.logits + m.t * a.lstride + lo);
                     float mx = -INFINITY;
                     for (int j = tid; j < nvb; j += NC) {
-                        const uint4 w = lds128(buf_s + 16u * j);
+                        const uint4 w = grow4[j];
                         const uint32_t m2 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
                         mx = fmaxf(mx, fmaxf(bf_lo(m2), bf_hi(m2)));
                     }
@@ -907,7 +942,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     if (mx > -INFINITY) {
                         const float ox = mx * kscale;
                         for (int j = tid; j < nvb; j += NC) {
-                            const uint4 w = lds128(buf_s + 16u * j);
+                            const uint4 w = grow4[j];
                             const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -936,16 +971,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     give_up(SC_STATUS_TIMEOUT_LOAD);
                     break;
                 }
-                {  // the recorded ids' logits and a's (every chunk has landed for this thread)
-                    const uint16_t* buf = reinterpret_cast<const uint16_t*>(smem + ds * L.stage_bytes);
-                    const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
-                    float* fz = fix_z + p * cap;
-                    for (int e = tid; e < nown; e += NC) {
-                        const int li = li_s[e];
-                        fz[e] = bf_to_f(li < n8 ? buf[li] : lrow[li]);
-                    }
-                    if (tid == NC - 1 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? buf[a_li] : lrow[a_li]);
-                }
                 if (__all_sync(kFull, ok)) {  // one offset for the whole warp: plain sums
                     ms_acc.s1 = warp_sum(ms_acc.s1);
                     ms_acc.s2 = warp_sum(ms_acc.s2);
@@ -963,21 +988,21 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(adone(p));
-                    // one stage: the slice has served its pass, the next row may stream
-                    // in (the write pass reads it again from L2)
+                    // one stage: the slice has served its pass and the next row may
+                    // stream in; the write pass reads it again from L2, soon enough
+                    // (right after the exchange) that it is still there
                     if (NB == 1)
                         for (int c = 0; c < nchunks; ++c) mbar_arrive(data_bar(ds, kChunkFree + c));
                 }
             }
-            if (i > 0) {
-                // ---- write pass of row i - 1: the slice again from L2, g = beta p (the
-                // special entries are patched by the scalar warp afterwards) ----
-                const uint32_t ip = i - 1;
-                const int pp = static_cast<int>(ip & 1u);
-                const int msp = static_cast<int>(ip % kMetaSlots);
-                const RowMeta mp = meta[msp];
-                const uint16_t* lrow = a.logits + mp.t * a.lstride + lo;
-                uint16_t* grow = a.grad + mp.t * a.gstride + lo;
+            {
+                // ---- write pass of row i, once the cluster has its row scalars: g = beta p
+                // (the special entries are patched by the scalar warp afterwards), the
+                // slice read again from L2 (one stage) or from its stage ----
+                const uint32_t ip = i;
+                const int pp = p;
+                const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                uint16_t* grow = a.grad + m.t * a.gstride + lo;
                 // the first L2 reads go out before the row scalars are known
                 uint4 wa = make_uint4(0u, 0u, 0u, 0u), wb = wa;
                 if (NB == 1) {
@@ -1036,11 +1061,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 rs = warp_sum(rs + (f2_lo(RS) + f2_hi(RS)));
                 if (lane == 0) rsw[pp * NCW + warp] = rs;
             }
-            if (!have_cur) {  // end of the stream: every row of this warp is written
-                __syncwarp();
-                if (lane == 0) mbar_arrive(adone(static_cast<int>(i & 1u)));
-                break;
-            }
         }
     }
 
@@ -1048,15 +1068,11 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
     // ones rode with later records); the final cluster barrier also keeps
     // every CTA's shared memory alive until no peer can still write to it.
     if (warp == NCW && lane == 0 && a.diag && clean_end)
-        st_cluster_v2(map_to_rank(smem_addr(frs + crank), 0), __float_as_uint(fin_rs2), __float_as_uint(fin_rs1));
+        st_cluster_v2(map_to_rank(smem_addr(frs + crank), 0), __float_as_uint(fin_rs1), 0u);
     cluster_sync_all();
     if (crank == 0 && warp == NCW && lane == 0 && a.diag && clean_end) {
-        float s2 = 0.0f, s1 = 0.0f;
-        for (int r = 0; r < C; ++r) {
-            s2 += frs[r].x;
-            s1 += frs[r].y;
-        }
-        if (nrows >= 2) a.diag[t_m2].row_sum = s2;
+        float s1 = 0.0f;
+        for (int r = 0; r < C; ++r) s1 += frs[r].x;
         if (nrows >= 1) a.diag[t_m1].row_sum = s1;
     }
 }
