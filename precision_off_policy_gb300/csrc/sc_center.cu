@@ -19,22 +19,24 @@
 //   a one-bit-per-entry bitmap of them -- and starts 1-D bulk copies (TMA
 //   engine) of the logit slice into shared memory, chunk by chunk, as soon as
 //   the streaming warps have released the buffer.
-// * The streaming warps alternate two passes.  Phase A of row i: one pass
-//   over the slice in shared memory with a running maximum, summing
-//   e^{x_v - m} and its entropy term over the unrecorded entries (recorded ids
-//   are skipped through the bitmap, so the unrecorded mass accumulates
-//   directly, with no 1 - P_H cancellation), then picking up the recorded
-//   ids' logits; the buffer is then released.  Write pass of row i - 1: the
-//   slice again from L2 (the copies are marked evict-last), g_v = beta p_v
-//   stored with 16-byte stores, no special cases.
-// * The scalar warp does the per-row serial work off the streaming path:
-//   it merges the streaming warps' partials into this CTA's 64-byte record,
-//   sends it to every CTA of the cluster with st.async stores that complete
-//   as transaction bytes on the receiver's mbarrier, merges the C records
-//   into the row scalars (LSE, P_H, Q_H, rho, s, loss, k3, importance weight)
-//   -- the same way in every CTA -- while the streaming warps run phase A of
-//   the next row, and after a row's write pass overwrites its <= K+1 special
-//   entries (recorded ids and the sampled token) with their own gradients.
+// * The streaming warps take each row through two passes over the slice in
+//   shared memory.  Phase A: with one exponent offset (the largest logit of the
+//   slice's first vectors), sum 2^y and its entropy term over the unrecorded
+//   entries (recorded ids are skipped through the bitmap, so the unrecorded
+//   mass accumulates directly, with no 1 - P_H cancellation).  Then, once the
+//   cluster has the row scalars, the write pass: g_v = beta p_v with 16-byte
+//   stores and no special cases, handing every chunk back to the producer as
+//   soon as it is written, so the next row streams into the stage while this
+//   one is written.
+// * The scalar warp does the per-row serial work off the streaming path.
+//   While phase A runs it picks up the recorded ids' logits from the slice and
+//   sums them relative to the pass's offset; when phase A ends it merges the
+//   streaming warps' partials into this CTA's 64-byte record and sends it to
+//   every CTA of the cluster with st.async stores that complete as transaction
+//   bytes on the receiver's mbarrier, patches the previous row's special
+//   entries (recorded ids and the sampled token) with their own gradients,
+//   and merges the C records into the row scalars (LSE, P_H, Q_H, rho, s,
+//   loss, k3, importance weight) the same way in every CTA.
 // Every logit is read from HBM once and every gradient written once.  The
 // grid is persistent (as many clusters as fit).  Every wait is bounded (about
 // 1 s) and reports through the status word.
@@ -105,7 +107,7 @@ struct Layout {
     int stage_bytes;  // bytes of one data stage (128-aligned)
     int list_cap;     // entries of one owned list (K_max)
     int nwords;       // bitmap words of one slice (one bit per entry)
-    int off_meta, off_list_li, off_list_q, off_bitmap, off_bars, off_part, off_mine, off_frs,
+    int off_meta, off_list_li, off_list_q, off_bitmap, off_bars, off_part, off_frs,
         off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, total;
 };
 
@@ -252,7 +254,6 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
     float* list_q = reinterpret_cast<float*>(smem + L.off_list_q);         // [kMetaSlots][cap] q = e^lp
     uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [kMetaSlots][nwords]
     Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [kXBufs][C]
-    Partial* mine = reinterpret_cast<Partial*>(smem + L.off_mine);         // staging of this CTA's record
     float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);             // [kMaxCluster]
     float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);            // [2][cap] recorded logits
     float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);            // [2][cap] their gradients
@@ -275,7 +276,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
     const int cap = L.list_cap, nwords = L.nwords;
     const float kscale = a.inv_t * kLog2e;
     const uint64_t pol = l2_policy_evict_first();      // last use: gradient stores, write-pass reads
-    const uint64_t pol_keep = l2_policy_evict_last();  // slice copies, read again by the write pass
+    const uint64_t pol_keep = l2_policy_evict_normal();  // slice copies (measured: evict-first is slower)
 
     if (tid == 0) {
         for (int d = 0; d < NB; ++d)
@@ -533,43 +534,80 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
         for (uint32_t j = 0;; ++j) {
             if (flag_up()) break;
             const int p = static_cast<int>(j & 1u);
-            {
-                // While the streaming warps run phase A of row j, gather the logits
-                // of its recorded ids and of a from global memory (the slice's copies
-                // have brought them into L2 or have them in flight).
-                const int msg = static_cast<int>(j % kMetaSlots);
-                const bool mready = mbar_wait_bounded(meta_bar(msg, kMetaFull), (j / kMetaSlots) & 1u, kWaitLimitNs);
-                if (!__all_sync(kFull, mready)) {
+            const int ms = static_cast<int>(j % kMetaSlots);
+            // ---- while the streaming warps run phase A of row j: everything that
+            // needs only the slice -- the streaming offset (the same largest logit of
+            // the first vectors), the recorded ids' and a's logits, and the recorded
+            // ids' sums relative to the larger of that offset and their own maximum ----
+            if (!__all_sync(kFull, mbar_wait_bounded(meta_bar(ms, kMetaFull), (j / kMetaSlots) & 1u, kWaitLimitNs))) {
+                give_up(SC_STATUS_TIMEOUT_LOAD);
+                break;
+            }
+            const RowMeta m = meta[ms];
+            const int* li_s = list_li + ms * cap;
+            const float* q_s = list_q + ms * cap;
+            const float* fz = fix_z + p * cap;
+            const int nown = m.nown, a_li = m.a_li;
+            float zmax = -INFINITY, Mo = -INFINITY, lH = 0.0f, EH = 0.0f, QY = 0.0f;
+            auto head_sums = [&](float o_c) {  // owned recorded ids relative to o_c
+                lH = 0.0f;
+                EH = 0.0f;
+                QY = 0.0f;
+                for (int e = lane; e < nown; e += 32) {
+                    const float y = fmaf(fz[e], kscale, -o_c);
+                    const float ev = ex2(y);
+                    lH += ev;
+                    EH = fmaf(ev, y, EH);
+                    QY = fmaf(q_s[e], y, QY);
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    lH += __shfl_xor_sync(kFull, lH, off);
+                    EH += __shfl_xor_sync(kFull, EH, off);
+                    QY += __shfl_xor_sync(kFull, QY, off);
+                }
+            };
+            if (m.t >= 0) {
+                // The chunk waits also make the bulk copies' data visible to this warp.
+                const int ds = static_cast<int>(j % NB);
+                bool landed = true;
+                for (int c = 0; c < nchunks; ++c)
+                    landed = landed && mbar_wait_bounded(data_bar(ds, kChunkFull + c), (j / NB) & 1u, kWaitLimitNs);
+                if (!__all_sync(kFull, landed)) {
                     give_up(SC_STATUS_TIMEOUT_LOAD);
                     break;
                 }
-                const long long tg = meta[msg].t;
-                if (tg >= 0) {
-                    const int ng = meta[msg].nown, ag = meta[msg].a_li;
-                    const uint16_t* lrow = a.logits + tg * a.lstride + lo;
-                    const int* lig = list_li + msg * cap;
-                    float* fz = fix_z + p * cap;
-                    int idx[4];
-                    uint16_t zr[4];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) idx[r] = lane + 32 * r < ng ? lig[lane + 32 * r] : -1;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) zr[r] = idx[r] >= 0 ? lrow[idx[r]] : static_cast<uint16_t>(0);
-                    const uint16_t za = (lane == 0 && ag >= 0) ? lrow[ag] : static_cast<uint16_t>(0);
-#pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        if (idx[r] >= 0) fz[lane + 32 * r] = bf_to_f(zr[r]);
-                    for (int e = lane + 128; e < ng; e += 32) fz[e] = bf_to_f(lrow[lig[e]]);
-                    if (lane == 0 && ag >= 0) zav[p] = bf_to_f(za);
+                const unsigned char* sb = smem + ds * L.stage_bytes;
+                float mz = -INFINITY;
+                if (nchunks > 0 && lane < nvb) {
+                    const uint4 w = lds128(smem_addr(sb) + 16u * lane);
+                    const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
+                    mz = fmaxf(bf_lo(mx), bf_hi(mx));
                 }
+                mz = warp_max(mz);
+                // logits of the owned recorded ids and of a: from the stage, past the
+                // last whole vector from global memory
+                const uint16_t* sb16 = reinterpret_cast<const uint16_t*>(sb);
+                const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                float* fzw = fix_z + p * cap;
+                for (int e = lane; e < nown; e += 32) {
+                    const int li = li_s[e];
+                    const float z = bf_to_f(li < n8 ? sb16[li] : lrow[li]);
+                    fzw[e] = z;
+                    zmax = fmaxf(zmax, z);
+                }
+                zmax = warp_max(zmax);
+                if (lane == 0 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? sb16[a_li] : lrow[a_li]);
+                __syncwarp();
+                Mo = fmaxf(mz, zmax);
+                if (Mo > -INFINITY) head_sums(Mo * kscale);
             }
+            // ---- phase A of row j is done ----
             const bool got = mbar_wait_bounded(adone(p), (j >> 1) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, got)) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
             }
-            const int ms = static_cast<int>(j % kMetaSlots);
-            const RowMeta m = meta[ms];
             // The write pass of row j - 1 ended before phase A of row j in every
             // streaming warp: its row sum is complete (it rides with this row's
             // record), and its special entries can be patched once the record is
@@ -591,12 +629,8 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 break;
             }
             const int xi = static_cast<int>(j & 3u);
-            const int* li_s = list_li + ms * cap;
-            const float* q_s = list_q + ms * cap;
-            const float* fz = fix_z + p * cap;
-            const int nown = m.nown, a_li = m.a_li;
             if (lane == 0) mbar_expect_tx(xbar(xi), static_cast<uint32_t>(sizeof(Partial)) * C);
-            // ---- this CTA's record of row j ----
+            // ---- this CTA's record of row j, sent from registers ----
             {
                 const float* rp = red + p * 3 * NCW;
                 Mass cm = lane < NCW ? Mass{rp[lane], rp[NCW + lane], rp[2 * NCW + lane]}
@@ -609,55 +643,22 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) cm = mass_merge(cm, mass_shfl(cm, off), kscale);
                 }
-                {  // the owned recorded logits may lie above the streaming offset
-                    float zmax = -INFINITY;
-                    for (int e = lane; e < nown; e += 32) zmax = fmaxf(zmax, fz[e]);
-                    cm = mass_merge(cm, Mass{warp_max(zmax), 0.0f, 0.0f}, kscale);
-                }
+                // the owned recorded logits may lie above the streaming offset
+                cm = mass_merge(cm, Mass{zmax, 0.0f, 0.0f}, kscale);
+                if (cm.m != Mo) head_sums(cm.m * kscale);  // (an exact pass moved the offset)
                 const float o_c = cm.m * kscale;
-                float lH = 0.0f, EH = 0.0f, QY = 0.0f;
-                for (int e = lane; e < nown; e += 32) {
-                    const float y = fmaf(fz[e], kscale, -o_c);
-                    const float ev = ex2(y);
-                    lH += ev;
-                    EH = fmaf(ev, y, EH);
-                    QY = fmaf(q_s[e], y, QY);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    lH += __shfl_xor_sync(kFull, lH, off);
-                    EH += __shfl_xor_sync(kFull, EH, off);
-                    QY += __shfl_xor_sync(kFull, QY, off);
-                }
-                if (lane == 0) {
-                    Partial& r = *mine;
-                    r.m = cm.m;
-                    r.S1 = cm.s1;
-                    r.S2 = cm.s2;
-                    r.rs = rs1;
-                    r.lH = lH;
-                    r.EH = EH;
-                    r.QY = QY;
-                    r.qo_hi = m.oh;
-                    r.qo_lo = m.ol;
-                    r.qbest = m.qbest;
-                    r.kbest = m.kbest;
-                    r.nval = nown;
-                    r.flags = m.flags;
-                    r.ya = a_li >= 0 ? fmaf(zav[p], kscale, -o_c) : 0.0f;
-                    r.has_a = a_li >= 0 ? 1 : 0;
-                    r.omq = m.omq;
-                }
-                __syncwarp();
                 if (lane < C) {  // lane r sends the record to CTA r
-                    const uint32_t src = smem_addr(mine);
                     const uint32_t dst = map_to_rank(smem_addr(part + xi * C + static_cast<int>(crank)), lane);
                     const uint32_t rb = map_to_rank(xbar(xi), lane);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 v = lds128(src + 16u * q);
-                        st_async_v4(dst + 16u * q, v.x, v.y, v.z, v.w, rb);
-                    }
+                    const float ya = a_li >= 0 ? fmaf(zav[p], kscale, -o_c) : 0.0f;
+                    st_async_v4(dst, __float_as_uint(cm.m), __float_as_uint(cm.s1), __float_as_uint(cm.s2),
+                                __float_as_uint(rs1), rb);
+                    st_async_v4(dst + 16u, __float_as_uint(lH), __float_as_uint(EH), __float_as_uint(QY),
+                                __float_as_uint(m.oh), rb);
+                    st_async_v4(dst + 32u, __float_as_uint(m.ol), __float_as_uint(m.qbest),
+                                static_cast<uint32_t>(m.kbest), static_cast<uint32_t>(nown), rb);
+                    st_async_v4(dst + 48u, m.flags, __float_as_uint(ya), a_li >= 0 ? 1u : 0u,
+                                __float_as_uint(m.omq), rb);
                 }
             }
             finish_prev();  // while the peers' records are on their way
@@ -837,11 +838,11 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                 break;
             }
             const int p = static_cast<int>(i & 1u);
+            const int ds = static_cast<int>(i % NB);  // the row's data stage
+            const uint32_t buf_s = smem_addr(smem + ds * L.stage_bytes);
             {
                 // ------------- phase A: one pass over the slice in shared memory -------------
-                const int ds = static_cast<int>(i % NB);
                 const uint32_t fpar = (i / NB) & 1u;
-                const uint32_t buf_s = smem_addr(smem + ds * L.stage_bytes);
                 const uint32_t* bm = bitmap + ms * nwords;
                 // The exponent offset is the largest logit among the slice's first 32
                 // vectors -- every warp reads the same ones and reduces them the same
@@ -986,29 +987,18 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     rp[2 * NCW + warp] = ms_acc.s2;
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(adone(p));
-                    // one stage: the slice has served its pass and the next row may
-                    // stream in; the write pass reads it again from L2, soon enough
-                    // (right after the exchange) that it is still there
-                    if (NB == 1)
-                        for (int c = 0; c < nchunks; ++c) mbar_arrive(data_bar(ds, kChunkFree + c));
-                }
+                if (lane == 0) mbar_arrive(adone(p));
             }
             {
                 // ---- write pass of row i, once the cluster has its row scalars: g = beta p
                 // (the special entries are patched by the scalar warp afterwards), the
-                // slice read again from L2 (one stage) or from its stage ----
+                // slice read from its stage, every chunk handed back to the producer
+                // as soon as this warp is done with it (the next row streams into it
+                // while this one is written) ----
                 const uint32_t ip = i;
                 const int pp = p;
                 const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
                 uint16_t* grow = a.grad + m.t * a.gstride + lo;
-                // the first L2 reads go out before the row scalars are known
-                uint4 wa = make_uint4(0u, 0u, 0u, 0u), wb = wa;
-                if (NB == 1) {
-                    if (tid < nvb) wa = ldg_v4_hint(lrow + 8 * tid, pol);
-                    if (tid + NC < nvb) wb = ldg_v4_hint(lrow + 8 * (tid + NC), pol);
-                }
                 const bool ready = mbar_wait_bounded(sready(pp), (ip >> 1) & 1u, kWaitLimitNs);
                 if (!__all_sync(kFull, ready)) {
                     give_up(SC_STATUS_TIMEOUT_EXCHANGE);
@@ -1028,27 +1018,12 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
                     st_global_v4_hint(grow + 8 * j, pack_bf16x2(f2_lo(g0), f2_hi(g0)), pack_bf16x2(f2_lo(g1), f2_hi(g1)),
                                       pack_bf16x2(f2_lo(g2), f2_hi(g2)), pack_bf16x2(f2_lo(g3), f2_hi(g3)), pol);
                 };
-                if (NB > 1) {
-                    // the slice is still in its stage: read it there and hand each
-                    // chunk back to the producer as soon as this warp is done with it
-                    const int dsp = static_cast<int>(ip % NB);
-                    const uint32_t bufp = smem_addr(smem + dsp * L.stage_bytes);
-                    for (int c = 0; c < nchunks; ++c) {
-                        const int v1 = min((c + 1) * a.ncv, nvb);
+                for (int c = 0; c < nchunks; ++c) {
+                    const int v1 = min((c + 1) * a.ncv, nvb);
 #pragma unroll 2
-                        for (int j = c * a.ncv + tid; j < v1; j += NC) emit(j, lds128(bufp + 16u * j));
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(data_bar(dsp, kChunkFree + c));
-                    }
-                } else {
-                    // two vectors in flight ahead of the two being written
-                    for (int j = tid; j < nvb; j += 2 * NC) {
-                        const uint4 w0 = wa, w1 = wb;
-                        if (j + 2 * NC < nvb) wa = ldg_v4_hint(lrow + 8 * (j + 2 * NC), pol);
-                        if (j + 3 * NC < nvb) wb = ldg_v4_hint(lrow + 8 * (j + 3 * NC), pol);
-                        emit(j, w0);
-                        if (j + NC < nvb) emit(j + NC, w1);
-                    }
+                    for (int j = c * a.ncv + tid; j < v1; j += NC) emit(j, lds128(buf_s + 16u * j));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(data_bar(ds, kChunkFree + c));
                 }
                 if (tail && tid == 0) {
                     for (int q = 0; q < tail; ++q) {
@@ -1103,7 +1078,6 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     L.off_bitmap = take(kMetaSlots * L.nwords * 4);
     L.off_bars = take(kNumBars * 8);
     L.off_part = take(kXBufs * C * static_cast<int>(sizeof(Partial)));
-    L.off_mine = take(static_cast<int>(sizeof(Partial)));
     L.off_frs = take(kMaxCluster * 8);
     L.off_fixz = take(2 * L.list_cap * 4);
     L.off_fixv = take(2 * L.list_cap * 4);
@@ -1117,15 +1091,14 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
 }
 
 // Automatic plan: about 80 KiB of logits per CTA (clusters of up to 16
-// CTAs), one data stage that the next row refills while the write pass of
-// the previous row runs from L2, 512 compute threads (256 or 128 for small
-// slices).  For the 151936-entry vocabulary: 4 CTAs x 37984 entries, two
-// CTAs per SM.
+// CTAs), one data stage that the write pass hands back chunk by chunk to the
+// next row's copies, 256 streaming threads (128 for small slices).  For the
+// 151936-entry vocabulary: 4 CTAs x 37984 entries, two CTAs per SM.
 int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
     const int NB = req_stages > 0 ? req_stages : 1;
     int C = req_cluster;
     auto threads_for = [&](int S) {
-        return req_threads > 0 ? req_threads : (S >= 24576 ? 512 : (S >= 8192 ? 256 : 128));
+        return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128);
     };
     if (C <= 0) {
         C = static_cast<int>((2LL * V + 81919) / 81920);
