@@ -61,6 +61,7 @@ constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
 constexpr int kChunkVecTarget = 1024;   // 16-byte vectors per bulk copy (16 KiB)
+constexpr int kWalkRows = 256;          // rows per batch of the producer's walk
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
@@ -108,7 +109,7 @@ struct Layout {
     int list_cap;     // entries of one owned list (K_max)
     int nwords;       // bitmap words of one slice (one bit per entry)
     int off_meta, off_list_li, off_list_q, off_bitmap, off_bars, off_part, off_frs,
-        off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, total;
+        off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, off_walk, off_pos, total;
 };
 
 struct KArgs {
@@ -235,12 +236,12 @@ constexpr int kSReady = kADone + 2;
 constexpr int kNumBars = kSReady + 2;
 
 // Resident CTAs per SM the register allocation must allow.
-constexpr int min_blocks(int NC) { return NC <= 128 ? 6 : (NC <= 256 ? 3 : 2); }
+constexpr int min_blocks(int NC) { return NC <= 128 ? 4 : 2; }
 
 template <int NC>
-__global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int NCW = NC / 32;  // streaming warps; warp NCW: row scalars; warp NCW + 1: producer
+    constexpr int NCW = NC / 32;  // streaming warps; warp NCW: row scalars; NCW + 1: producer; NCW + 2: zero rows
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t crank = cluster_ctarank();
     const uint32_t cid = cluster_id_x();
@@ -262,6 +263,8 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
     float* rsw = reinterpret_cast<float*>(smem + L.off_rsw);               // [2][NCW] warp row sums
     float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [2][4] row scalars
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_flag);
+    int* walk_all = reinterpret_cast<int*>(smem + L.off_walk);             // [2 warps][2][kWalkRows] response indices
+    volatile long long* prod_pos = reinterpret_cast<volatile long long*>(smem + L.off_pos);  // producer's walk position
     auto data_bar = [&](int d, int i) { return smem_addr(&bars[d * kBarsPerStage + i]); };
     auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
     auto xbar = [&](int x) { return smem_addr(&bars[kXBase + x]); };
@@ -296,9 +299,10 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
         }
         for (int r = 0; r < kMaxCluster; ++r) frs[r] = make_float2(0.0f, 0.0f);
         *abort_flag = 0;
+        *prod_pos = 0;
         fence_mbar_init_cluster();
     }
-    for (int i = tid; i < kMetaSlots * nwords; i += NC + 64) bitmap[i] = 0u;
+    for (int i = tid; i < kMetaSlots * nwords; i += NC + 96) bitmap[i] = 0u;
     cluster_sync_all();  // every CTA's barriers exist before peers signal them
 
     // Any role that gives up raises the flag; the others see it at their next
@@ -337,177 +341,230 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
         if (lane == 0 && a_li >= 0 && !a_rec) grow[a_li] = f_to_bf_bits(scal[4 * q + 2]);
     };
 
-    if (warp == NCW + 1) {
-        // ================= producer warp =================
+    if (warp >= NCW + 1) {
+        // ================= producer warp (rows with a response) and zero warp (padding rows) =================
+        // Both walk all rows in the same order (as every CTA of the cluster does):
+        // the producer takes every ncl-th row with a response index in range,
+        // the zero warp, counted separately, every ncl-th padding row.  Every
+        // cluster gets the same number of rows of each kind, within one,
+        // however the padding falls, and the zero rows' stores never hold up
+        // the producer.  The response indices are fetched a batch of kWalkRows
+        // ahead (loads in flight while the batch before is dealt) into a
+        // two-batch buffer of the warp's own.
+        const bool zero_warp = warp == NCW + 2;
+        int* walk = walk_all + (zero_warp ? 2 * kWalkRows : 0);
         uint32_t nfill = 0;
         bool stop = false;
-        for (long long base = cid; base < a.T && !stop; base += 32LL * ncl) {
-            const long long tl = base + static_cast<long long>(lane) * ncl;
-            const bool in = tl < a.T;
-            int resp_l = -1, sa_l = 0;
-            if (in) {
-                resp_l = __ldg(a.resp + tl);
-                sa_l = __ldg(a.sampled + tl);
-            }
-            uint32_t zf = 0;
-            if (in) {
-                if (resp_l < 0)
-                    zf = SC_FLAG_MASKED;
-                else if (resp_l >= a.n_resp)
-                    zf = SC_FLAG_BAD_RESPONSE;
-                else if (sa_l < 0 || sa_l >= a.V)
-                    zf = SC_FLAG_BAD_SAMPLED;
-            }
-            const unsigned inmask = __ballot_sync(kFull, in);
-            for (int j = 0; j < 32 && ((inmask >> j) & 1u); ++j) {
-                if (flag_up()) {
-                    stop = true;
-                    break;
-                }
-                const long long t = base + static_cast<long long>(j) * ncl;
-                const uint32_t zfj = __shfl_sync(kFull, zf, j);
-                const int rj = __shfl_sync(kFull, resp_l, j);
-                const int sj = __shfl_sync(kFull, sa_l, j);
-                if (zfj) {  // padding or error row: zero gradient, no compute
-                    uint16_t* grow = a.grad + t * a.gstride + lo;
-                    for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
-                    if (lane < tail) grow[n8 + lane] = 0;
-                    if (crank == 0 && lane == 0) {
-                        a.logp[t] = 0.0f;
-                        if (a.diag) {  // zeros and the flags, as four 16-byte stores
-                            float4* dp = reinterpret_cast<float4*>(a.diag + t);
-                            const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                            dp[0] = z4;
-                            dp[1] = z4;
-                            dp[2] = z4;
-                            dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(zfj), 0.0f);
-                        }
-                        if (zfj & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
-                    }
-                    continue;
-                }
-                const int ms = static_cast<int>(nfill % kMetaSlots);
-                if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
-                    !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs)) {
-                    if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                    stop = true;
-                    break;
-                }
-                // ---- recorded ids of this slice: compact list, repeats dropped ----
-                // (row scalars loaded first so their latency overlaps the list)
-                const float row_A = __ldg(a.adv + rj);
-                const float row_rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
-                int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
-                uint32_t flags = 0;
-                if (cnt < 0 || cnt > K_max) {
-                    flags |= SC_FLAG_BAD_COUNT;
-                    cnt = cnt < 0 ? 0 : K_max;
-                }
-                int* li_s = list_li + ms * cap;
-                float* q_s = list_q + ms * cap;
-                uint32_t* bm = bitmap + ms * nwords;
-                {  // clear the bits of the slot's previous row (whole words: they are all its own)
-                    const int old = meta[ms].nown;
-                    for (int e = lane; e < old; e += 32) bm[li_s[e] >> 5] = 0u;
-                }
-                __syncwarp();
-                const long long kb = t * static_cast<long long>(K_max);
-                int nown = 0;
-                bool bad = false, dup = false;
-                HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};  // the kept ids' q, merged
-                for (int kb0 = 0; kb0 < cnt; kb0 += 128) {
-                    int idr[4];
-                    float lpr[4];
+        uint32_t seen_full = 0, seen_pad = 0;
+        int pre[kWalkRows / 32];
+        auto fetch = [&](long long b0) {
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {  // four rounds of loads in flight together
-                        const int k = kb0 + 32 * r + lane;
-                        idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
-                        lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
-                    }
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int k = kb0 + 32 * r + lane;
-                        const bool kin = k < cnt;
-                        const int id = idr[r];
-                        bad = bad || (kin && (id < 0 || id >= a.V));
-                        const bool owned = kin && id >= lo && id < hi;
-                        const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
-                        bool keep = owned && (same & lanemask_lt()) == 0u;
-                        if (keep)  // repeats of an earlier round
-                            for (int e = 0; e < nown; ++e)
-                                if (li_s[e] == id - lo) {
-                                    keep = false;
-                                    break;
-                                }
-                        dup = dup || (owned && !keep);
-                        const unsigned km = __ballot_sync(kFull, keep);
-                        if (keep) {
-                            const int pos = nown + __popc(km & lanemask_lt());
-                            const float q = expf(lpr[r]);
-                            li_s[pos] = id - lo;
-                            q_s[pos] = q;
-                            hm = head_merge(hm, HeadMass{q, k, -expm1f(lpr[r]), 0.0f, 0.0f});
-                            atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
-                        }
-                        nown += __popc(km);
-                        __syncwarp();
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) hm = head_merge(hm, head_shfl(hm, off));
-                if (__any_sync(kFull, dup)) flags |= SC_FLAG_DUP_ID;
-                if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
-                const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
-                if (lane == 0) {
-                    RowMeta* mt = meta + ms;
-                    mt->t = t;
-                    mt->sa = sj;
-                    mt->nown = nown;
-                    mt->a_li = a_li;
-                    mt->flags = flags;
-                    mt->A = row_A;
-                    mt->rl = row_rl;
-                    mt->qbest = hm.q;
-                    mt->omq = hm.omq;
-                    mt->oh = hm.oh;
-                    mt->ol = hm.ol;
-                    mt->kbest = hm.k;
-                }
-                // The slot is published before the copies start: the consumers wait
-                // for each chunk on its own barrier, so they can start as soon as the
-                // first chunk lands.
-                __syncwarp();
-                if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
-                // ---- logit slice: chunk by chunk as the stage's slots free up ----
-                if (lane == 0) {
-                    const int ds = static_cast<int>(nfill % NB);
-                    const bool reuse = nfill >= static_cast<uint32_t>(NB);
-                    const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
-                    const uint16_t* lrow = a.logits + t * a.lstride + lo;
-                    const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
-                    for (int i = 0; i < nchunks; ++i) {
-                        if (reuse &&
-                            !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
-                            status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                            for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
-                                (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
-                                                        kWaitLimitNs);
-                            stop = true;
-                            break;
-                        }
-                        fence_proxy_async_smem();
-                        const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                        const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                        mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
-                        bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
-                    }
-                }
-                stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
-                if (stop) break;
-                ++nfill;
+            for (int k = 0; k < kWalkRows / 32; ++k) {
+                const long long tk = b0 + 32 * k + lane;
+                pre[k] = tk < a.T ? __ldg(a.resp + tk) : -1;
             }
+        };
+        auto stash = [&](int buf) {
+#pragma unroll
+            for (int k = 0; k < kWalkRows / 32; ++k) walk[buf * kWalkRows + 32 * k + lane] = pre[k];
+            __syncwarp();
+        };
+        fetch(0);
+        stash(0);
+        for (long long wb = 0; wb < a.T && !stop; wb += kWalkRows) {
+            const int wbi = static_cast<int>((wb / kWalkRows) & 1);
+            if (wb + kWalkRows < a.T) fetch(wb + kWalkRows);
+            for (int g = 0; g < kWalkRows / 32 && !stop; ++g) {
+                const long long base = wb + 32 * g;
+                if (base >= a.T) break;
+                const long long tl = base + lane;
+                const bool in = tl < a.T;
+                const int resp_l = walk[wbi * kWalkRows + 32 * g + lane];
+                const bool full = in && resp_l >= 0 && resp_l < a.n_resp;
+                const bool pad = in && !full;
+                const uint32_t fm = __ballot_sync(kFull, full), pm = __ballot_sync(kFull, pad);
+                const uint32_t before = lanemask_lt();
+                const bool take = zero_warp ? pad && (seen_pad + __popc(pm & before)) % ncl == cid
+                                            : full && (seen_full + __popc(fm & before)) % ncl == cid;
+                seen_full += __popc(fm);
+                seen_pad += __popc(pm);
+                int sa_l = 0;
+                uint32_t zf = 0;
+                if (take) {
+                    if (resp_l < 0) {
+                        zf = SC_FLAG_MASKED;
+                    } else if (resp_l >= a.n_resp) {
+                        zf = SC_FLAG_BAD_RESPONSE;
+                    } else {
+                        sa_l = __ldg(a.sampled + tl);
+                        if (sa_l < 0 || sa_l >= a.V) zf = SC_FLAG_BAD_SAMPLED;
+                    }
+                }
+                for (uint32_t tm = __ballot_sync(kFull, take); tm != 0u; tm &= tm - 1u) {
+                    if (flag_up()) {
+                        stop = true;
+                        break;
+                    }
+                    const int j = __ffs(tm) - 1;
+                    const long long t = base + j;
+                    const uint32_t zfj = __shfl_sync(kFull, zf, j);
+                    const int rj = __shfl_sync(kFull, resp_l, j);
+                    const int sj = __shfl_sync(kFull, sa_l, j);
+                    if (zfj) {  // padding or error row: zero gradient, no compute
+                        if (zero_warp) {
+                            // Paced by the producer: a zero row is written once the producer
+                            // has passed it, so zero rows keep to the order of the row stream
+                            // (filling the bandwidth the pipeline leaves) without ever holding
+                            // up the producer.  The wait is bounded; on expiry it just writes.
+                            if (*prod_pos <= t) {
+                                const uint64_t t0 = global_timer_ns();
+                                while (*prod_pos <= t && global_timer_ns() - t0 < kWaitLimitNs) __nanosleep(256);
+                            }
+                            __syncwarp();
+                        }
+                        uint16_t* grow = a.grad + t * a.gstride + lo;
+                        for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
+                        if (lane < tail) grow[n8 + lane] = 0;
+                        if (crank == 0 && lane == 0) {
+                            a.logp[t] = 0.0f;
+                            if (a.diag) {  // zeros and the flags, as four 16-byte stores
+                                float4* dp = reinterpret_cast<float4*>(a.diag + t);
+                                const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                                dp[0] = z4;
+                                dp[1] = z4;
+                                dp[2] = z4;
+                                dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(zfj), 0.0f);
+                            }
+                            if (zfj & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+                        }
+                        continue;
+                    }
+                    const int ms = static_cast<int>(nfill % kMetaSlots);
+                    if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
+                        !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs)) {
+                        if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                        stop = true;
+                        break;
+                    }
+                    // ---- recorded ids of this slice: compact list, repeats dropped ----
+                    // (row scalars loaded first so their latency overlaps the list)
+                    const float row_A = __ldg(a.adv + rj);
+                    const float row_rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
+                    int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
+                    uint32_t flags = 0;
+                    if (cnt < 0 || cnt > K_max) {
+                        flags |= SC_FLAG_BAD_COUNT;
+                        cnt = cnt < 0 ? 0 : K_max;
+                    }
+                    int* li_s = list_li + ms * cap;
+                    float* q_s = list_q + ms * cap;
+                    uint32_t* bm = bitmap + ms * nwords;
+                    {  // clear the bits of the slot's previous row (whole words: they are all its own)
+                        const int old = meta[ms].nown;
+                        for (int e = lane; e < old; e += 32) bm[li_s[e] >> 5] = 0u;
+                    }
+                    __syncwarp();
+                    const long long kb = t * static_cast<long long>(K_max);
+                    int nown = 0;
+                    bool bad = false, dup = false;
+                    HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};  // the kept ids' q, merged
+                    for (int kb0 = 0; kb0 < cnt; kb0 += 128) {
+                        int idr[4];
+                        float lpr[4];
+    #pragma unroll
+                        for (int r = 0; r < 4; ++r) {  // four rounds of loads in flight together
+                            const int k = kb0 + 32 * r + lane;
+                            idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
+                            lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
+                        }
+    #pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int k = kb0 + 32 * r + lane;
+                            const bool kin = k < cnt;
+                            const int id = idr[r];
+                            bad = bad || (kin && (id < 0 || id >= a.V));
+                            const bool owned = kin && id >= lo && id < hi;
+                            const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
+                            bool keep = owned && (same & lanemask_lt()) == 0u;
+                            if (keep)  // repeats of an earlier round
+                                for (int e = 0; e < nown; ++e)
+                                    if (li_s[e] == id - lo) {
+                                        keep = false;
+                                        break;
+                                    }
+                            dup = dup || (owned && !keep);
+                            const unsigned km = __ballot_sync(kFull, keep);
+                            if (keep) {
+                                const int pos = nown + __popc(km & lanemask_lt());
+                                const float q = expf(lpr[r]);
+                                li_s[pos] = id - lo;
+                                q_s[pos] = q;
+                                hm = head_merge(hm, HeadMass{q, k, -expm1f(lpr[r]), 0.0f, 0.0f});
+                                atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
+                            }
+                            nown += __popc(km);
+                            __syncwarp();
+                        }
+                    }
+    #pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) hm = head_merge(hm, head_shfl(hm, off));
+                    if (__any_sync(kFull, dup)) flags |= SC_FLAG_DUP_ID;
+                    if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
+                    const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
+                    if (lane == 0) {
+                        RowMeta* mt = meta + ms;
+                        mt->t = t;
+                        mt->sa = sj;
+                        mt->nown = nown;
+                        mt->a_li = a_li;
+                        mt->flags = flags;
+                        mt->A = row_A;
+                        mt->rl = row_rl;
+                        mt->qbest = hm.q;
+                        mt->omq = hm.omq;
+                        mt->oh = hm.oh;
+                        mt->ol = hm.ol;
+                        mt->kbest = hm.k;
+                    }
+                    // The slot is published before the copies start: the consumers wait
+                    // for each chunk on its own barrier, so they can start as soon as the
+                    // first chunk lands.
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
+                    // ---- logit slice: chunk by chunk as the stage's slots free up ----
+                    if (lane == 0) {
+                        const int ds = static_cast<int>(nfill % NB);
+                        const bool reuse = nfill >= static_cast<uint32_t>(NB);
+                        const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
+                        const uint16_t* lrow = a.logits + t * a.lstride + lo;
+                        const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
+                        for (int i = 0; i < nchunks; ++i) {
+                            if (reuse &&
+                                !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
+                                status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                                for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
+                                    (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
+                                                            kWaitLimitNs);
+                                stop = true;
+                                break;
+                            }
+                            fence_proxy_async_smem();
+                            const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                            const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+                            mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
+                            bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
+                        }
+                    }
+                    stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
+                    if (stop) break;
+                    ++nfill;
+                    if (lane == 0) *prod_pos = t + 1;
+                }
+            }
+            if (!stop && wb + kWalkRows < a.T) stash(wbi ^ 1);
         }
-        if (!stop) {  // end marker for the consumers
+        if (!zero_warp && lane == 0) *prod_pos = 0x7FFFFFFFFFFFFFFFLL;  // the zero warp may finish
+        if (!stop && !zero_warp) {  // end marker for the consumers
             const int ms = static_cast<int>(nfill % kMetaSlots);
             bool ok = true;
             if (nfill >= static_cast<uint32_t>(kMetaSlots))
@@ -522,7 +579,7 @@ __global__ void __launch_bounds__(NC + 64, min_blocks(NC)) center_kernel(const _
             }
         }
         // copies still in flight land before the CTA can exit (bounded again)
-        if (lane == 0) {
+        if (lane == 0 && !zero_warp) {
             const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
             for (uint32_t f = f0; f < nfill; ++f)
                 for (int i = 0; i < nchunks; ++i)
@@ -1086,6 +1143,8 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     L.off_rsw = take(2 * (NC / 32) * 4);
     L.off_scal = take(2 * 4 * 4);
     L.off_flag = take(4);
+    L.off_walk = take(2 * 2 * kWalkRows * 4);
+    L.off_pos = take(8);
     L.total = off;
     return L;
 }
@@ -1167,7 +1226,7 @@ int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.C, 1, 1);
-    cfg.blockDim = dim3(P.NC + 64, 1, 1);
+    cfg.blockDim = dim3(P.NC + 96, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1329,7 +1388,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(G * P.C), 1, 1);
-    cfg.blockDim = dim3(P.NC + 64, 1, 1);
+    cfg.blockDim = dim3(P.NC + 96, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
