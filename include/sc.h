@@ -22,7 +22,8 @@
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates no memory; it keeps only a small per-process cache of launch
- *     plans.
+ *     plans.  The fused call takes a small caller-owned workspace (see
+ *     SC_WORKSPACE_BYTES).
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     Argument errors are detected on the host before anything is launched
  *     and returned as a status code; nothing is written in that case.
@@ -234,20 +235,30 @@ int sc_rollout_mean_advantages(const float* adv, const int32_t* row_response, lo
  * diag_out        : sc_row_diag [T] or NULL.
  * status_dev      : one device uint32 or NULL; SC_STATUS_* bits are OR-ed
  *                   into it (the caller clears it).
+ * workspace       : SC_WORKSPACE_BYTES of device memory, 16-byte aligned,
+ *                   all zero before its first use.  It holds the counter from
+ *                   which the launch hands rows out to its thread-block
+ *                   clusters at run time (the clusters that run ahead take
+ *                   more rows), and the launch leaves it zero again when it
+ *                   completes, so consecutive calls on one stream can share
+ *                   one workspace.  Calls that may run at the same time (other
+ *                   streams) need workspaces of their own; after a launch that
+ *                   did not complete (a CUDA error), zero it again.
  * Recorded ids outside [0, V) are ignored, and a repeated id is ignored
  * after its first occurrence; both set row flags.
  * Errors: SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE (T < 0, V < 1,
  * V > 1048576, K_max outside 0..1024, n_resp < 0, strides < V), SC_ERR_ARG
  * (bad parameter values or overlap), SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
- * T == 0 is a no-op.
+ * T == 0 is a no-op (the workspace is not touched).
  */
+#define SC_WORKSPACE_BYTES 64
 int sc_center_forward_backward(const uint16_t* logits, long long T, int V, long long logits_stride,
                                const int32_t* rec_ids, const float* rec_logprobs,
                                const int32_t* rec_count, const int32_t* sampled_id,
                                const float* rollout_logprob, const int32_t* row_response,
                                const float* adv, int n_resp, const sc_params* p, uint16_t* grad_out,
                                long long grad_stride, float* logp_out, sc_row_diag* diag_out,
-                               uint32_t* status_dev, sc_stream_t stream);
+                               uint32_t* status_dev, void* workspace, sc_stream_t stream);
 
 /* Launch plan the library would use for a vocabulary of V and these
  * parameters on the current device (no launch).  Any output pointer may be

@@ -29,6 +29,7 @@ __all__ = [
     "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
     "ScoreCenteredLoss", "score_centered_loss",
     "sc_rollout_mean_advantages", "sc_topk_capture", "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS", "SC_IS_CLIP",
+    "WORKSPACE_BYTES", "workspace", "reset_workspaces",
 ]
 
 SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
@@ -112,7 +113,7 @@ def lib():
             L.sc_topk_capture.argtypes = [vp, i64, i32, i64, f32, i32, f32, vp, vp, vp, vp]
             L.sc_topk_capture.restype = i32
             L.sc_center_forward_backward.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
-                                                     ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
+                                                     ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp, vp]
             L.sc_center_forward_backward.restype = i32
             L.sc_plan_query.argtypes = [i32, ctypes.POINTER(Params)] + [ctypes.POINTER(i32)] * 5
             L.sc_plan_query.restype = i32
@@ -242,6 +243,34 @@ def sc_topk_capture(logits: torch.Tensor, K: int, inv_temperature: float = 1.0, 
     return ids_out, logprobs_out, count_out
 
 
+WORKSPACE_BYTES = 64  # SC_WORKSPACE_BYTES
+_workspaces = {}
+
+
+def workspace(device, stream=None) -> torch.Tensor:
+    """The binding's workspace for calls on (device, stream): 64 zeroed bytes,
+    created on first use.  Calls on one stream run one after another, so they
+    share it; another stream gets its own."""
+    dev = torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    key = (dev.index, int(stream.cuda_stream))
+    with _lock:
+        ws = _workspaces.get(key)
+        if ws is None:
+            ws = torch.zeros(WORKSPACE_BYTES // 8, dtype=torch.int64, device=dev)
+            _workspaces[key] = ws
+    return ws
+
+
+def reset_workspaces() -> None:
+    """Zero every workspace the binding holds (needed only after a launch that
+    did not complete, e.g. a CUDA error)."""
+    with _lock:
+        for ws in _workspaces.values():
+            ws.zero_()
+
+
 def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | None,
                                rec_logprobs: torch.Tensor | None, rec_count: torch.Tensor | None,
                                sampled_id: torch.Tensor, rollout_logprob: torch.Tensor | None,
@@ -249,7 +278,8 @@ def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | Non
                                V: int | None = None, grad_out: torch.Tensor | None = None,
                                logp_out: torch.Tensor | None = None,
                                diag_out: torch.Tensor | None = None,
-                               status: torch.Tensor | None = None, stream=None):
+                               status: torch.Tensor | None = None, stream=None,
+                               workspace_buf: torch.Tensor | None = None):
     """Score-centered forward/backward.
 
     logits: bf16 [T, >=V] on a CUDA device with contiguous rows; rec_ids int32
@@ -257,7 +287,9 @@ def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | Non
     sampled_id, row_response int32 [T]; rollout_logprob float32 [T] or None;
     adv float32 [n_resp].  grad_out may be ``logits`` (in place).  diag_out,
     when given, is an int32 [T, 16] tensor (64-byte records, see
-    :func:`diag_to_numpy`); status an int32 [1] tensor.
+    :func:`diag_to_numpy`); status an int32 [1] tensor.  workspace_buf: 64
+    zeroed bytes on the device (SC_WORKSPACE_BYTES in the C header); by
+    default the binding's own for this device and stream (:func:`workspace`).
     Returns (grad_out, logp_out, diag_out).
     """
     dev = logits.device
@@ -290,11 +322,16 @@ def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | Non
         _need(status, "status", torch.int32, dev, 1)
     if T == 0:
         return grad_out, logp_out, diag_out
+    if workspace_buf is None:
+        workspace_buf = workspace(dev, stream)
+    elif workspace_buf.device != dev or workspace_buf.numel() * workspace_buf.element_size() < WORKSPACE_BYTES:
+        raise ValueError(f"workspace_buf must hold {WORKSPACE_BYTES} bytes on {dev}")
     _check(lib().sc_center_forward_backward(
         _ptr(logits), T, V, _rows(logits, "logits"), _ptr(rec_ids) if K_max else None,
         _ptr(rec_logprobs) if K_max else None, _ptr(rec_count), _ptr(sampled_id), _ptr(rollout_logprob),
         _ptr(row_response), _ptr(adv), int(adv.numel()), ctypes.byref(p), _ptr(grad_out),
-        _rows(grad_out, "grad_out"), _ptr(logp_out), _ptr(diag_out), _ptr(status), _stream(stream)))
+        _rows(grad_out, "grad_out"), _ptr(logp_out), _ptr(diag_out), _ptr(status), _ptr(workspace_buf),
+        _stream(stream)))
     return grad_out, logp_out, diag_out
 
 

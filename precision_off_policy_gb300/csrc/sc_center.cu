@@ -61,7 +61,9 @@ constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
 constexpr int kChunkVecTarget = 1024;   // 16-byte vectors per bulk copy (16 KiB)
-constexpr int kWalkRows = 256;          // rows per batch of the producer's walk
+constexpr int kGrab = 8;                // grab ring: rows CTA 0 may hand out ahead of its peers
+constexpr int kZq = 16;                 // zero queue: zero rows the producer may queue ahead
+constexpr long long kDynamicShare = 4;  // 1 / (share of the rows handed out at run time)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
@@ -109,7 +111,7 @@ struct Layout {
     int list_cap;     // entries of one owned list (K_max)
     int nwords;       // bitmap words of one slice (one bit per entry)
     int off_meta, off_list_li, off_list_q, off_bitmap, off_bars, off_part, off_frs,
-        off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, off_walk, off_pos, total;
+        off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, off_grab, off_zq, off_zqf, total;
 };
 
 struct KArgs {
@@ -125,6 +127,8 @@ struct KArgs {
     float* logp;
     sc_row_diag* diag;
     uint32_t* status;
+    unsigned long long* ws;  // [0]: rows handed out after T_static, [1]: CTAs that have finished
+    long long T_static;      // rows dealt round robin before the hand-out starts (a multiple of the clusters)
     long long T, lstride, gstride;
     int V, K_max, n_resp;
     int is_mode, centering;
@@ -222,8 +226,10 @@ __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
 // kMetaFull (producer wrote it), kMetaFree (its row is written).  Exchange
 // buffer x: a row's records (own expect_tx arrive + peers' bytes).  kADone[p]:
 // every streaming warp finished phase A of a row of parity p (and so the write
-// pass of the row two before it).  kSReady[p]: the row scalars of a row of
-// parity p are published.
+// pass of the row before it).  kSReady[p]: the row scalars of a row of parity p
+// are published.  Grab ring slot g: kGrabFull (the row index from CTA 0 landed,
+// tx bytes), kGrabFree (in CTA 0: every CTA of the cluster has read it).  Zero
+// queue slot z: kZqFull (producer wrote it), kZqFree (the zero warp took it).
 constexpr int kChunkFull = 0;
 constexpr int kChunkFree = kMaxChunks;
 constexpr int kBarsPerStage = 2 * kMaxChunks;
@@ -233,7 +239,9 @@ constexpr int kMetaFree = 1;
 constexpr int kXBase = kMetaBase + 2 * kMetaSlots;
 constexpr int kADone = kXBase + kXBufs;
 constexpr int kSReady = kADone + 2;
-constexpr int kNumBars = kSReady + 2;
+constexpr int kGrabBase = kSReady + 2;
+constexpr int kZqBase = kGrabBase + 2 * kGrab;
+constexpr int kNumBars = kZqBase + 2 * kZq;
 
 // Resident CTAs per SM the register allocation must allow.
 constexpr int min_blocks(int NC) { return NC <= 128 ? 4 : 2; }
@@ -263,13 +271,18 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     float* rsw = reinterpret_cast<float*>(smem + L.off_rsw);               // [2][NCW] warp row sums
     float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [2][4] row scalars
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_flag);
-    int* walk_all = reinterpret_cast<int*>(smem + L.off_walk);             // [2 warps][2][kWalkRows] response indices
-    volatile long long* prod_pos = reinterpret_cast<volatile long long*>(smem + L.off_pos);  // producer's walk position
+    long long* grab_ring = reinterpret_cast<long long*>(smem + L.off_grab);  // [kGrab] row indices from CTA 0
+    long long* zq_t = reinterpret_cast<long long*>(smem + L.off_zq);        // [kZq] zero rows
+    uint32_t* zq_f = reinterpret_cast<uint32_t*>(smem + L.off_zqf);         // [kZq] their flags
     auto data_bar = [&](int d, int i) { return smem_addr(&bars[d * kBarsPerStage + i]); };
     auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
     auto xbar = [&](int x) { return smem_addr(&bars[kXBase + x]); };
     auto adone = [&](int p) { return smem_addr(&bars[kADone + p]); };
     auto sready = [&](int p) { return smem_addr(&bars[kSReady + p]); };
+    auto grab_full = [&](int g) { return smem_addr(&bars[kGrabBase + 2 * g]); };
+    auto grab_free = [&](int g) { return smem_addr(&bars[kGrabBase + 2 * g + 1]); };
+    auto zq_full = [&](int z) { return smem_addr(&bars[kZqBase + 2 * z]); };
+    auto zq_free = [&](int z) { return smem_addr(&bars[kZqBase + 2 * z + 1]); };
 
     const int lo = static_cast<int>(crank) * a.S;
     const int hi = min(lo + a.S, a.V);
@@ -297,9 +310,16 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             mbar_init(adone(p), static_cast<uint32_t>(NCW));
             mbar_init(sready(p), 1u);
         }
+        for (int g = 0; g < kGrab; ++g) {
+            mbar_init(grab_full(g), 1u);
+            mbar_init(grab_free(g), static_cast<uint32_t>(C));
+        }
+        for (int z = 0; z < kZq; ++z) {
+            mbar_init(zq_full(z), 1u);
+            mbar_init(zq_free(z), 1u);
+        }
         for (int r = 0; r < kMaxCluster; ++r) frs[r] = make_float2(0.0f, 0.0f);
         *abort_flag = 0;
-        *prod_pos = 0;
         fence_mbar_init_cluster();
     }
     for (int i = tid; i < kMetaSlots * nwords; i += NC + 96) bitmap[i] = 0u;
@@ -341,230 +361,225 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         if (lane == 0 && a_li >= 0 && !a_rec) grow[a_li] = f_to_bf_bits(scal[4 * q + 2]);
     };
 
-    if (warp >= NCW + 1) {
-        // ================= producer warp (rows with a response) and zero warp (padding rows) =================
-        // Both walk all rows in the same order (as every CTA of the cluster does):
-        // the producer takes every ncl-th row with a response index in range,
-        // the zero warp, counted separately, every ncl-th padding row.  Every
-        // cluster gets the same number of rows of each kind, within one,
-        // however the padding falls, and the zero rows' stores never hold up
-        // the producer.  The response indices are fetched a batch of kWalkRows
-        // ahead (loads in flight while the batch before is dealt) into a
-        // two-batch buffer of the warp's own.
-        const bool zero_warp = warp == NCW + 2;
-        int* walk = walk_all + (zero_warp ? 2 * kWalkRows : 0);
-        uint32_t nfill = 0;
+    if (warp == NCW + 1) {
+        // ================= producer warp =================
+        // Rows [0, T_static) are dealt round robin (row cid + k * ncl).  The rest
+        // are handed out at run time: CTA 0 of the cluster takes the next one
+        // from the launch's counter (workspace; the following take is always in
+        // flight) and sends it to every CTA of the cluster through a grab ring in
+        // their shared memory, so the clusters that have run ahead take more of
+        // the last rows and all finish together.  Rows with a response get the
+        // full pass (metadata slot, slice copies); zero rows (padding, bad
+        // response or sampled id) go to the zero warp's queue, so their stores
+        // never hold up the producer.
+        uint32_t nfill = 0, ng = 0, nz = 0;
         bool stop = false;
-        uint32_t seen_full = 0, seen_pad = 0;
-        int pre[kWalkRows / 32];
-        auto fetch = [&](long long b0) {
-#pragma unroll
-            for (int k = 0; k < kWalkRows / 32; ++k) {
-                const long long tk = b0 + 32 * k + lane;
-                pre[k] = tk < a.T ? __ldg(a.resp + tk) : -1;
+        long long t_static = cid;
+        unsigned long long pend = 0;  // CTA 0, lane 0: the counter value of the take in flight
+        bool pending = false;
+        for (;;) {
+            if (flag_up()) {
+                stop = true;
+                break;
             }
-        };
-        auto stash = [&](int buf) {
-#pragma unroll
-            for (int k = 0; k < kWalkRows / 32; ++k) walk[buf * kWalkRows + 32 * k + lane] = pre[k];
-            __syncwarp();
-        };
-        fetch(0);
-        stash(0);
-        for (long long wb = 0; wb < a.T && !stop; wb += kWalkRows) {
-            const int wbi = static_cast<int>((wb / kWalkRows) & 1);
-            if (wb + kWalkRows < a.T) fetch(wb + kWalkRows);
-            for (int g = 0; g < kWalkRows / 32 && !stop; ++g) {
-                const long long base = wb + 32 * g;
-                if (base >= a.T) break;
-                const long long tl = base + lane;
-                const bool in = tl < a.T;
-                const int resp_l = walk[wbi * kWalkRows + 32 * g + lane];
-                const bool full = in && resp_l >= 0 && resp_l < a.n_resp;
-                const bool pad = in && !full;
-                const uint32_t fm = __ballot_sync(kFull, full), pm = __ballot_sync(kFull, pad);
-                const uint32_t before = lanemask_lt();
-                const bool take = zero_warp ? pad && (seen_pad + __popc(pm & before)) % ncl == cid
-                                            : full && (seen_full + __popc(fm & before)) % ncl == cid;
-                seen_full += __popc(fm);
-                seen_pad += __popc(pm);
-                int sa_l = 0;
-                uint32_t zf = 0;
-                if (take) {
-                    if (resp_l < 0) {
-                        zf = SC_FLAG_MASKED;
-                    } else if (resp_l >= a.n_resp) {
-                        zf = SC_FLAG_BAD_RESPONSE;
-                    } else {
-                        sa_l = __ldg(a.sampled + tl);
-                        if (sa_l < 0 || sa_l >= a.V) zf = SC_FLAG_BAD_SAMPLED;
+            long long t;
+            if (t_static < a.T_static) {
+                t = t_static;
+                t_static += ncl;
+            } else {
+                const int g = static_cast<int>(ng % kGrab);
+                if (crank == 0) {
+                    // every CTA has read this slot's previous row (bounded wait)
+                    bool ok = true;
+                    if (ng >= static_cast<uint32_t>(kGrab))
+                        ok = mbar_wait_cluster_bounded(grab_free(g), ((ng / kGrab) - 1u) & 1u, kWaitLimitNs);
+                    if (!__all_sync(kFull, ok)) {
+                        give_up(SC_STATUS_TIMEOUT_LOAD);
+                        stop = true;
+                        break;
                     }
+                    unsigned long long tg = 0;
+                    if (lane == 0) {
+                        tg = static_cast<unsigned long long>(a.T_static) + (pending ? pend : atomicAdd(a.ws, 1ull));
+                        pending = tg < static_cast<unsigned long long>(a.T);
+                        if (pending) pend = atomicAdd(a.ws, 1ull);  // the next take, in flight
+                    }
+                    tg = __shfl_sync(kFull, tg, 0);
+                    if (lane < C)
+                        st_async_v2(map_to_rank(smem_addr(grab_ring + g), lane), static_cast<uint32_t>(tg),
+                                    static_cast<uint32_t>(tg >> 32), map_to_rank(grab_full(g), lane));
                 }
-                for (uint32_t tm = __ballot_sync(kFull, take); tm != 0u; tm &= tm - 1u) {
-                    if (flag_up()) {
-                        stop = true;
-                        break;
-                    }
-                    const int j = __ffs(tm) - 1;
-                    const long long t = base + j;
-                    const uint32_t zfj = __shfl_sync(kFull, zf, j);
-                    const int rj = __shfl_sync(kFull, resp_l, j);
-                    const int sj = __shfl_sync(kFull, sa_l, j);
-                    if (zfj) {  // padding or error row: zero gradient, no compute
-                        if (zero_warp) {
-                            // Paced by the producer: a zero row is written once the producer
-                            // has passed it, so zero rows keep to the order of the row stream
-                            // (filling the bandwidth the pipeline leaves) without ever holding
-                            // up the producer.  The wait is bounded; on expiry it just writes.
-                            if (*prod_pos <= t) {
-                                const uint64_t t0 = global_timer_ns();
-                                while (*prod_pos <= t && global_timer_ns() - t0 < kWaitLimitNs) __nanosleep(256);
-                            }
-                            __syncwarp();
-                        }
-                        uint16_t* grow = a.grad + t * a.gstride + lo;
-                        for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
-                        if (lane < tail) grow[n8 + lane] = 0;
-                        if (crank == 0 && lane == 0) {
-                            a.logp[t] = 0.0f;
-                            if (a.diag) {  // zeros and the flags, as four 16-byte stores
-                                float4* dp = reinterpret_cast<float4*>(a.diag + t);
-                                const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                                dp[0] = z4;
-                                dp[1] = z4;
-                                dp[2] = z4;
-                                dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(zfj), 0.0f);
-                            }
-                            if (zfj & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
-                        }
-                        continue;
-                    }
-                    const int ms = static_cast<int>(nfill % kMetaSlots);
-                    if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
-                        !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs)) {
-                        if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                        stop = true;
-                        break;
-                    }
-                    // ---- recorded ids of this slice: compact list, repeats dropped ----
-                    // (row scalars loaded first so their latency overlaps the list)
-                    const float row_A = __ldg(a.adv + rj);
-                    const float row_rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
-                    int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
-                    uint32_t flags = 0;
-                    if (cnt < 0 || cnt > K_max) {
-                        flags |= SC_FLAG_BAD_COUNT;
-                        cnt = cnt < 0 ? 0 : K_max;
-                    }
-                    int* li_s = list_li + ms * cap;
-                    float* q_s = list_q + ms * cap;
-                    uint32_t* bm = bitmap + ms * nwords;
-                    {  // clear the bits of the slot's previous row (whole words: they are all its own)
-                        const int old = meta[ms].nown;
-                        for (int e = lane; e < old; e += 32) bm[li_s[e] >> 5] = 0u;
-                    }
-                    __syncwarp();
-                    const long long kb = t * static_cast<long long>(K_max);
-                    int nown = 0;
-                    bool bad = false, dup = false;
-                    HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};  // the kept ids' q, merged
-                    for (int kb0 = 0; kb0 < cnt; kb0 += 128) {
-                        int idr[4];
-                        float lpr[4];
-    #pragma unroll
-                        for (int r = 0; r < 4; ++r) {  // four rounds of loads in flight together
-                            const int k = kb0 + 32 * r + lane;
-                            idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
-                            lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
-                        }
-    #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const int k = kb0 + 32 * r + lane;
-                            const bool kin = k < cnt;
-                            const int id = idr[r];
-                            bad = bad || (kin && (id < 0 || id >= a.V));
-                            const bool owned = kin && id >= lo && id < hi;
-                            const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
-                            bool keep = owned && (same & lanemask_lt()) == 0u;
-                            if (keep)  // repeats of an earlier round
-                                for (int e = 0; e < nown; ++e)
-                                    if (li_s[e] == id - lo) {
-                                        keep = false;
-                                        break;
-                                    }
-                            dup = dup || (owned && !keep);
-                            const unsigned km = __ballot_sync(kFull, keep);
-                            if (keep) {
-                                const int pos = nown + __popc(km & lanemask_lt());
-                                const float q = expf(lpr[r]);
-                                li_s[pos] = id - lo;
-                                q_s[pos] = q;
-                                hm = head_merge(hm, HeadMass{q, k, -expm1f(lpr[r]), 0.0f, 0.0f});
-                                atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
-                            }
-                            nown += __popc(km);
-                            __syncwarp();
-                        }
-                    }
-    #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) hm = head_merge(hm, head_shfl(hm, off));
-                    if (__any_sync(kFull, dup)) flags |= SC_FLAG_DUP_ID;
-                    if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
-                    const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
-                    if (lane == 0) {
-                        RowMeta* mt = meta + ms;
-                        mt->t = t;
-                        mt->sa = sj;
-                        mt->nown = nown;
-                        mt->a_li = a_li;
-                        mt->flags = flags;
-                        mt->A = row_A;
-                        mt->rl = row_rl;
-                        mt->qbest = hm.q;
-                        mt->omq = hm.omq;
-                        mt->oh = hm.oh;
-                        mt->ol = hm.ol;
-                        mt->kbest = hm.k;
-                    }
-                    // The slot is published before the copies start: the consumers wait
-                    // for each chunk on its own barrier, so they can start as soon as the
-                    // first chunk lands.
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
-                    // ---- logit slice: chunk by chunk as the stage's slots free up ----
-                    if (lane == 0) {
-                        const int ds = static_cast<int>(nfill % NB);
-                        const bool reuse = nfill >= static_cast<uint32_t>(NB);
-                        const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
-                        const uint16_t* lrow = a.logits + t * a.lstride + lo;
-                        const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
-                        for (int i = 0; i < nchunks; ++i) {
-                            if (reuse &&
-                                !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
-                                status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                                for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
-                                    (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
-                                                            kWaitLimitNs);
-                                stop = true;
+                if (lane == 0) mbar_expect_tx(grab_full(g), 8u);
+                if (!__all_sync(kFull, mbar_wait_cluster_bounded(grab_full(g), (ng / kGrab) & 1u, kWaitLimitNs))) {
+                    give_up(SC_STATUS_TIMEOUT_LOAD);
+                    stop = true;
+                    break;
+                }
+                const unsigned long long tu = static_cast<unsigned long long>(grab_ring[g]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_rank(grab_free(g), 0));  // slot read
+                ++ng;
+                if (tu >= static_cast<unsigned long long>(a.T)) break;  // no rows left
+                t = static_cast<long long>(tu);
+            }
+            const int rj = __ldg(a.resp + t);
+            int sj = 0;
+            uint32_t zf = 0;
+            if (rj < 0) {
+                zf = SC_FLAG_MASKED;
+            } else if (rj >= a.n_resp) {
+                zf = SC_FLAG_BAD_RESPONSE;
+            } else {
+                sj = __ldg(a.sampled + t);
+                if (sj < 0 || sj >= a.V) zf = SC_FLAG_BAD_SAMPLED;
+            }
+            if (zf) {  // zero row: to the zero warp's queue
+                const int z = static_cast<int>(nz % kZq);
+                if (nz >= static_cast<uint32_t>(kZq) &&
+                    !__all_sync(kFull, mbar_wait_bounded(zq_free(z), ((nz / kZq) - 1u) & 1u, kWaitLimitNs))) {
+                    give_up(SC_STATUS_TIMEOUT_LOAD);
+                    stop = true;
+                    break;
+                }
+                if (lane == 0) {
+                    zq_t[z] = t;
+                    zq_f[z] = zf;
+                    mbar_arrive(zq_full(z));  // release: the slot
+                }
+                ++nz;
+                continue;
+            }
+            const int ms = static_cast<int>(nfill % kMetaSlots);
+            if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
+                !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs)) {
+                if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                stop = true;
+                break;
+            }
+            // ---- recorded ids of this slice: compact list, repeats dropped ----
+            // (row scalars loaded first so their latency overlaps the list)
+            const float row_A = __ldg(a.adv + rj);
+            const float row_rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
+            int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
+            uint32_t flags = 0;
+            if (cnt < 0 || cnt > K_max) {
+                flags |= SC_FLAG_BAD_COUNT;
+                cnt = cnt < 0 ? 0 : K_max;
+            }
+            int* li_s = list_li + ms * cap;
+            float* q_s = list_q + ms * cap;
+            uint32_t* bm = bitmap + ms * nwords;
+            {  // clear the bits of the slot's previous row (whole words: they are all its own)
+                const int old = meta[ms].nown;
+                for (int e = lane; e < old; e += 32) bm[li_s[e] >> 5] = 0u;
+            }
+            __syncwarp();
+            const long long kb = t * static_cast<long long>(K_max);
+            int nown = 0;
+            bool bad = false, dup = false;
+            HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};  // the kept ids' q, merged
+            for (int kb0 = 0; kb0 < cnt; kb0 += 128) {
+                int idr[4];
+                float lpr[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {  // four rounds of loads in flight together
+                    const int k = kb0 + 32 * r + lane;
+                    idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
+                    lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int k = kb0 + 32 * r + lane;
+                    const bool kin = k < cnt;
+                    const int id = idr[r];
+                    bad = bad || (kin && (id < 0 || id >= a.V));
+                    const bool owned = kin && id >= lo && id < hi;
+                    const unsigned same = __match_any_sync(kFull, owned ? id : -1 - lane);
+                    bool keep = owned && (same & lanemask_lt()) == 0u;
+                    if (keep)  // repeats of an earlier round
+                        for (int e = 0; e < nown; ++e)
+                            if (li_s[e] == id - lo) {
+                                keep = false;
                                 break;
                             }
-                            fence_proxy_async_smem();
-                            const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                            const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                            mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
-                            bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
-                        }
+                    dup = dup || (owned && !keep);
+                    const unsigned km = __ballot_sync(kFull, keep);
+                    if (keep) {
+                        const int pos = nown + __popc(km & lanemask_lt());
+                        const float q = expf(lpr[r]);
+                        li_s[pos] = id - lo;
+                        q_s[pos] = q;
+                        hm = head_merge(hm, HeadMass{q, k, -expm1f(lpr[r]), 0.0f, 0.0f});
+                        atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
                     }
-                    stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
-                    if (stop) break;
-                    ++nfill;
-                    if (lane == 0) *prod_pos = t + 1;
+                    nown += __popc(km);
+                    __syncwarp();
                 }
             }
-            if (!stop && wb + kWalkRows < a.T) stash(wbi ^ 1);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) hm = head_merge(hm, head_shfl(hm, off));
+            if (__any_sync(kFull, dup)) flags |= SC_FLAG_DUP_ID;
+            if (crank == 0 && __any_sync(kFull, bad)) flags |= SC_FLAG_BAD_ID;
+            const int a_li = (sj >= lo && sj < hi) ? sj - lo : -1;
+            if (lane == 0) {
+                RowMeta* mt = meta + ms;
+                mt->t = t;
+                mt->sa = sj;
+                mt->nown = nown;
+                mt->a_li = a_li;
+                mt->flags = flags;
+                mt->A = row_A;
+                mt->rl = row_rl;
+                mt->qbest = hm.q;
+                mt->omq = hm.omq;
+                mt->oh = hm.oh;
+                mt->ol = hm.ol;
+                mt->kbest = hm.k;
+            }
+            // The slot is published before the copies start: the consumers wait
+            // for each chunk on its own barrier, so they can start as soon as the
+            // first chunk lands.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
+            // ---- logit slice: chunk by chunk as the stage's slots free up ----
+            if (lane == 0) {
+                const int ds = static_cast<int>(nfill % NB);
+                const bool reuse = nfill >= static_cast<uint32_t>(NB);
+                const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
+                const uint16_t* lrow = a.logits + t * a.lstride + lo;
+                const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
+                for (int i = 0; i < nchunks; ++i) {
+                    if (reuse &&
+                        !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
+                        status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
+                        for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
+                            (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
+                                                    kWaitLimitNs);
+                        stop = true;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                    const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+                    mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
+                    bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
+                }
+            }
+            stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
+            if (stop) break;
+            ++nfill;
         }
-        if (!zero_warp && lane == 0) *prod_pos = 0x7FFFFFFFFFFFFFFFLL;  // the zero warp may finish
-        if (!stop && !zero_warp) {  // end marker for the consumers
+        {  // end marker for the zero warp (it leaves on its own if the queue stalls)
+            const int z = static_cast<int>(nz % kZq);
+            bool ok = true;
+            if (nz >= static_cast<uint32_t>(kZq))
+                ok = mbar_wait_bounded(zq_free(z), ((nz / kZq) - 1u) & 1u, kWaitLimitNs);
+            if (__all_sync(kFull, ok) && lane == 0) {
+                zq_t[z] = -1;
+                mbar_arrive(zq_full(z));
+            }
+        }
+        if (!stop) {  // end marker for the consumers
             const int ms = static_cast<int>(nfill % kMetaSlots);
             bool ok = true;
             if (nfill >= static_cast<uint32_t>(kMetaSlots))
@@ -579,13 +594,43 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             }
         }
         // copies still in flight land before the CTA can exit (bounded again)
-        if (lane == 0 && !zero_warp) {
+        if (lane == 0) {
             const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
             for (uint32_t f = f0; f < nfill; ++f)
                 for (int i = 0; i < nchunks; ++i)
                     (void)mbar_wait_bounded(data_bar(f % NB, kChunkFull + i), (f / NB) & 1u, kWaitLimitNs);
         }
         __syncwarp();
+    } else if (warp == NCW + 2) {
+        // ================= zero warp: zero rows from the producer's queue =================
+        for (uint32_t iz = 0;; ++iz) {
+            const int z = static_cast<int>(iz % kZq);
+            if (!__all_sync(kFull, mbar_wait_bounded(zq_full(z), (iz / kZq) & 1u, kWaitLimitNs))) {
+                give_up(SC_STATUS_TIMEOUT_LOAD);
+                break;
+            }
+            const long long t = zq_t[z];
+            const uint32_t zf = zq_f[z];
+            __syncwarp();
+            if (t < 0) break;
+            uint16_t* grow = a.grad + t * a.gstride + lo;
+            for (int v = lane; v < nvb; v += 32) st_global_v4_hint(grow + 8 * v, 0u, 0u, 0u, 0u, pol);
+            if (lane < tail) grow[n8 + lane] = 0;
+            if (crank == 0 && lane == 0) {
+                a.logp[t] = 0.0f;
+                if (a.diag) {  // zeros and the flags, as four 16-byte stores
+                    float4* dp = reinterpret_cast<float4*>(a.diag + t);
+                    const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    dp[0] = z4;
+                    dp[1] = z4;
+                    dp[2] = z4;
+                    dp[3] = make_float4(0.0f, 0.0f, __uint_as_float(zf), 0.0f);
+                }
+                if (zf & SC_FLAG_DATA_ERRORS) status_or(a.status, SC_STATUS_DATA);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(zq_free(z));
+        }
     } else if (warp == NCW) {
         // ================= scalar warp: records, exchange, row scalars =================
         for (uint32_t j = 0;; ++j) {
@@ -754,7 +799,6 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     QYg = fmaf(d, Qc, PQY);
                 }
                 float ya = (have && r3.z) ? __uint_as_float(r3.y) + d : 0.0f;
-                float rsum = Prs;
                 int nval = Pnval;
                 uint32_t flags = have ? r3.x : 0u;
                 HeadMass hm{have ? __uint_as_float(r2.y) : 0.0f, have ? static_cast<int>(r2.z) : 0x7FFFFFFF,
@@ -768,11 +812,15 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     EH += __shfl_xor_sync(kFull, EH, off);
                     QYg += __shfl_xor_sync(kFull, QYg, off);
                     ya += __shfl_xor_sync(kFull, ya, off);
-                    rsum += __shfl_xor_sync(kFull, rsum, off);
                     nval += __shfl_xor_sync(kFull, nval, off);
                     flags |= __shfl_xor_sync(kFull, flags, off);
                     hm = head_merge(hm, head_shfl(hm, off));
                 }
+                // the previous row's sum, in CTA order (as the end-of-stream flush
+                // adds the last row's), so a row's sum does not depend on which
+                // of the two paths finished it
+                float rsum = 0.0f;
+                for (int r = 0; r < C; ++r) rsum += __shfl_sync(kFull, Prs, r);
                 // 1 - Q_H without cancellation: (1 - q_max), taken from its
                 // log-probability, minus the others' mass
                 float tail_mu = 1.0f, Q_H = 0.0f;
@@ -1107,6 +1155,16 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         for (int r = 0; r < C; ++r) s1 += frs[r].x;
         if (nrows >= 1) a.diag[t_m1].row_sum = s1;
     }
+    // The last CTA to finish leaves the workspace zeroed for the next launch
+    // (every CTA is past its last row hand-out by now).
+    if (tid == 0) {
+        __threadfence();
+        const unsigned long long done = atomicAdd(a.ws + 1, 1ull);
+        if (done == static_cast<unsigned long long>(gridDim.x) - 1ull) {
+            atomicExch(a.ws, 0ull);
+            atomicExch(a.ws + 1, 0ull);
+        }
+    }
 }
 
 // ---- host side ----------------------------------------------------------
@@ -1143,8 +1201,9 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     L.off_rsw = take(2 * (NC / 32) * 4);
     L.off_scal = take(2 * 4 * 4);
     L.off_flag = take(4);
-    L.off_walk = take(2 * 2 * kWalkRows * 4);
-    L.off_pos = take(8);
+    L.off_grab = take(kGrab * 8);
+    L.off_zq = take(kZq * 8);
+    L.off_zqf = take(kZq * 4);
     L.total = off;
     return L;
 }
@@ -1307,7 +1366,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
                                           const int32_t* row_response, const float* adv, int n_resp,
                                           const sc_params* p, uint16_t* grad_out, long long grad_stride,
                                           float* logp_out, sc_row_diag* diag_out, uint32_t* status_dev,
-                                          sc_stream_t stream) {
+                                          void* workspace, sc_stream_t stream) {
     using namespace sc;
     int st = check_params(V, p);
     if (st != SC_OK) return st;
@@ -1318,8 +1377,8 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     if (p->is_mode != SC_IS_NONE && !rollout_logprob)
         return fail(SC_ERR_NULL, "is_mode tis/mis needs rollout_logprob");
     if (T == 0) return ok();
-    if (!logits || !sampled_id || !row_response || !grad_out || !logp_out)
-        return fail(SC_ERR_NULL, "logits, sampled_id, row_response, grad_out and logp_out are required");
+    if (!logits || !sampled_id || !row_response || !grad_out || !logp_out || !workspace)
+        return fail(SC_ERR_NULL, "logits, sampled_id, row_response, grad_out, logp_out and workspace are required");
     if (n_resp > 0 && !adv) return fail(SC_ERR_NULL, "adv is NULL with n_resp > 0");
     if (p->K_max > 0 && (!rec_ids || !rec_logprobs))
         return fail(SC_ERR_NULL, "rec_ids and rec_logprobs are required when K_max > 0");
@@ -1329,8 +1388,9 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
         return fail(SC_ERR_ALIGN, "row strides must be multiples of 8 elements");
     if (!aligned(rec_ids, 4) || !aligned(rec_logprobs, 4) || !aligned(rec_count, 4) ||
         !aligned(sampled_id, 4) || !aligned(rollout_logprob, 4) || !aligned(row_response, 4) ||
-        !aligned(adv, 4) || !aligned(logp_out, 4) || !aligned(diag_out, 16) || !aligned(status_dev, 4))
-        return fail(SC_ERR_ALIGN, "metadata arrays must be 4-byte aligned and diag_out 16-byte aligned");
+        !aligned(adv, 4) || !aligned(logp_out, 4) || !aligned(diag_out, 16) || !aligned(status_dev, 4) ||
+        !aligned(workspace, 16))
+        return fail(SC_ERR_ALIGN, "metadata arrays must be 4-byte aligned, diag_out and workspace 16-byte aligned");
     {
         const char* l0 = reinterpret_cast<const char*>(logits);
         const char* g0 = reinterpret_cast<const char*>(grad_out);
@@ -1350,6 +1410,9 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     st = prepare_kernel(dev, P, &mc);
     if (st != SC_OK) return st;
     const long long G = T < mc ? T : mc;
+    // About the last quarter of the rows are handed out at run time (the rest,
+    // rounded down to a multiple of the clusters, are dealt round robin).
+    const long long T_static = (T - (T + kDynamicShare - 1) / kDynamicShare) / G * G;
 
     KArgs ka;
     std::memset(&ka, 0, sizeof ka);
@@ -1365,6 +1428,8 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.logp = logp_out;
     ka.diag = diag_out;
     ka.status = status_dev;
+    ka.ws = static_cast<unsigned long long*>(workspace);
+    ka.T_static = T_static;
     ka.T = T;
     ka.lstride = logits_stride;
     ka.gstride = grad_stride;

@@ -48,7 +48,7 @@ def test_struct_layouts_match_header(L):
     assert (p.K_max, p.is_mode, p.tis_max, p.mis_min, p.mis_max, p.centering) == (128, 0, 2.0, 0.5, 5.0, 1)
     assert (p.inv_temperature, p.grad_scale, p.cluster_size, p.threads, p.stages) == (1.0, 1.0, 0, 0, 0)
     assert L.sc_params_default(None) == sc.SC_ERR_NULL
-    assert L.sc_abi_version() == 101
+    assert L.sc_abi_version() == 102
     assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
 
 
@@ -57,13 +57,13 @@ FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced
 
 def call_center(L, T=4, V=64, lstride=64, gstride=64, logits=FAKE, grad=FAKE * 2, ids=FAKE * 3,
                 lps=FAKE * 4, cnt=None, samp=FAKE * 5, roll=None, resp=FAKE * 6, adv=FAKE * 7, n_resp=2,
-                logp=FAKE * 8, diag=None, status=None, **pk):
+                logp=FAKE * 8, diag=None, status=None, ws=FAKE * 11, **pk):
     raw_centering = pk.pop("centering", None)
     p = sc.params(**{"K_max": 8, **pk})
     if raw_centering is not None:
         p.centering = raw_centering  # bypass the binding's bool() to reach the C check
     return L.sc_center_forward_backward(logits, T, V, lstride, ids, lps, cnt, samp, roll, resp, adv, n_resp,
-                                        ctypes.byref(p), grad, gstride, logp, diag, status, None)
+                                        ctypes.byref(p), grad, gstride, logp, diag, status, ws, None)
 
 
 def err(L):
@@ -101,6 +101,8 @@ def err(L):
     (dict(resp=None), sc.SC_ERR_NULL),
     (dict(adv=None), sc.SC_ERR_NULL),
     (dict(ids=None), sc.SC_ERR_NULL),
+    (dict(ws=None), sc.SC_ERR_NULL),
+    (dict(ws=FAKE * 11 + 8), sc.SC_ERR_ALIGN),
     (dict(logits=FAKE + 2), sc.SC_ERR_ALIGN),
     (dict(grad=FAKE * 2 + 8), sc.SC_ERR_ALIGN),
     (dict(lstride=68), sc.SC_ERR_ALIGN),
@@ -116,13 +118,13 @@ def test_center_rejects_bad_arguments_on_the_host(L, kw, status):
 
 
 def test_center_empty_batch_is_a_no_op(L):
-    assert call_center(L, T=0, logits=None, grad=None, samp=None, resp=None, logp=None) == sc.SC_OK
+    assert call_center(L, T=0, logits=None, grad=None, samp=None, resp=None, logp=None, ws=None) == sc.SC_OK
     assert err(L) == ""
 
 
 def test_center_null_params(L):
     assert L.sc_center_forward_backward(FAKE, 1, 8, 8, None, None, None, FAKE, None, FAKE, FAKE, 1, None,
-                                        FAKE * 2, 8, FAKE * 3, None, None, None) == sc.SC_ERR_NULL
+                                        FAKE * 2, 8, FAKE * 3, None, None, FAKE * 4, None) == sc.SC_ERR_NULL
 
 
 def test_no_gpu_reaches_cuda_not_a_crash(L):

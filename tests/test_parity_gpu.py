@@ -229,6 +229,23 @@ def test_deterministic_across_calls():
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
 
 
+def test_run_time_row_hand_out_is_deterministic_and_leaves_the_workspace_zero():
+    # 1024 rows over the persistent grid: the first rows are dealt round robin,
+    # the last quarter handed out at run time, so which cluster takes which
+    # row changes from call to call; every output must not.
+    cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=512, len_lo=64, len_hi=512)
+    batch = synth.make_batch(cfg)
+    p = sc_params(batch)
+    adv = oracle_adv(batch)
+    runs = [run_gpu(batch, p, adv) for _ in range(3)]
+    for r in runs[1:]:
+        assert torch.equal(runs[0][0].view(torch.int16), r[0].view(torch.int16))
+        assert torch.equal(runs[0][1], r[1]) and torch.equal(runs[0][2], r[2])
+        assert int(r[3].item()) == 0
+    ws = sc.workspace(torch.device("cuda"))
+    assert int(ws.abs().sum().item()) == 0
+
+
 # -------------------------------------------------------------------------
 # Edge cases
 
