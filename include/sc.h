@@ -260,6 +260,42 @@ int sc_center_forward_backward(const uint16_t* logits, long long T, int V, long 
                                long long grad_stride, float* logp_out, sc_row_diag* diag_out,
                                uint32_t* status_dev, void* workspace, sc_stream_t stream);
 
+/*
+ * The same call for callers that cannot allocate device memory.  (The docs
+ * pages have no counterpart: this is a property of the library, not of the
+ * method.)
+ *
+ * Some callers receive their input and output buffers and nothing else -- a
+ * plugin inside another framework whose memory planner has already placed
+ * every buffer, or an embedded runtime that reserves all of its device memory
+ * up front -- so they cannot provide the workspace above.  This entry point
+ * takes the same arguments as sc_center_forward_backward except the
+ * workspace, and computes the same outputs.  It allocates nothing: its
+ * workspace is a fixed 256-byte array inside the library, held in device
+ * memory on every GPU that loads the library until the process exits.
+ *   - The first call on a device looks up that array's device address on
+ *     the current device (cudaGetSymbolAddress); make that first call before
+ *     any stream capture.
+ *   - Every call clears the workspace on `stream` before its launch, so a
+ *     failed earlier call does not leave it dirty.
+ *   - All calls share the one array: calls whose launches may overlap on the
+ *     GPU (different streams without ordering between them) race on it and
+ *     give wrong results.  Serialise them, or use sc_center_forward_backward
+ *     with a workspace per stream.
+ *   - The workspace a call needs does not depend on T, V or K_max; a call
+ *     would be refused (SC_ERR_SHAPE) only if SC_WORKSPACE_BYTES exceeded the
+ *     array's 256 bytes.
+ * Errors: as sc_center_forward_backward; on an argument error nothing but the
+ * library's own array is written.
+ */
+int sc_center_forward_backward_noalloc(const uint16_t* logits, long long T, int V, long long logits_stride,
+                                       const int32_t* rec_ids, const float* rec_logprobs,
+                                       const int32_t* rec_count, const int32_t* sampled_id,
+                                       const float* rollout_logprob, const int32_t* row_response,
+                                       const float* adv, int n_resp, const sc_params* p, uint16_t* grad_out,
+                                       long long grad_stride, float* logp_out, sc_row_diag* diag_out,
+                                       uint32_t* status_dev, sc_stream_t stream);
+
 /* Launch plan the library would use for a vocabulary of V and these
  * parameters on the current device (no launch).  Any output pointer may be
  * NULL.  cluster_size: CTAs per row; threads: per CTA; slice: vocabulary

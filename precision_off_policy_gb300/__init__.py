@@ -50,8 +50,8 @@ FLAG_CLIPPED = 0x400
 
 # Symbols declared in include/sc.h.
 EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_rollout_mean_advantages", "sc_topk_capture",
-           "sc_center_forward_backward", "sc_plan_query", "sc_status_string", "sc_last_error",
-           "sc_abi_version"]
+           "sc_center_forward_backward", "sc_center_forward_backward_noalloc", "sc_plan_query",
+           "sc_status_string", "sc_last_error", "sc_abi_version"]
 
 
 class ScError(RuntimeError):
@@ -115,6 +115,9 @@ def lib():
             L.sc_center_forward_backward.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                                      ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp, vp]
             L.sc_center_forward_backward.restype = i32
+            L.sc_center_forward_backward_noalloc.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                             ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
+            L.sc_center_forward_backward_noalloc.restype = i32
             L.sc_plan_query.argtypes = [i32, ctypes.POINTER(Params)] + [ctypes.POINTER(i32)] * 5
             L.sc_plan_query.restype = i32
             L.sc_status_string.argtypes = [i32]

@@ -1467,3 +1467,70 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     if (e != cudaSuccess) return cuda_fail(e, "center_kernel launch");
     return ok();
 }
+
+// ---- the same call for callers that cannot allocate -----------------------
+//
+// Some callers are handed their input and output buffers and nothing else --
+// for instance a plugin running inside another framework whose memory planner
+// has already placed every buffer, or an embedded runtime that reserves all of
+// its device memory at start-up -- and have no way to obtain the small
+// workspace sc_center_forward_backward needs.  This variant keeps that
+// workspace in the library itself: a fixed array in device memory, present on
+// every GPU that loads the library until the process exits.
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+// Room for the workspace of one call (SC_WORKSPACE_BYTES); every call shares it.
+static __device__ __align__(256) unsigned char g_center_scratch[256];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kNoAllocMaxDevices] = {};  // device address of g_center_scratch, per device
+
+}  // namespace
+
+extern "C" int sc_center_forward_backward_noalloc(const uint16_t* logits, long long T, int V,
+                                                  long long logits_stride, const int32_t* rec_ids,
+                                                  const float* rec_logprobs, const int32_t* rec_count,
+                                                  const int32_t* sampled_id, const float* rollout_logprob,
+                                                  const int32_t* row_response, const float* adv, int n_resp,
+                                                  const sc_params* p, uint16_t* grad_out, long long grad_stride,
+                                                  float* logp_out, sc_row_diag* diag_out, uint32_t* status_dev,
+                                                  sc_stream_t stream) {
+    using namespace sc;
+    // The scratch a call needs does not depend on T, V or K_max; the check
+    // below refuses the call only if the workspace ever outgrew the array.
+    if (SC_WORKSPACE_BYTES > static_cast<int>(sizeof(g_center_scratch)))
+        return fail(SC_ERR_SHAPE, "the workspace (%d bytes) exceeds the library's scratch array (%d bytes)",
+                    SC_WORKSPACE_BYTES, static_cast<int>(sizeof(g_center_scratch)));
+    if (T == 0) return sc_center_forward_backward(logits, T, V, logits_stride, rec_ids, rec_logprobs, rec_count,
+                                                  sampled_id, rollout_logprob, row_response, adv, n_resp, p,
+                                                  grad_out, grad_stride, logp_out, diag_out, status_dev,
+                                                  nullptr, stream);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return fail(SC_ERR_UNSUPPORTED, "device %d is beyond the %d devices this entry point serves", dev,
+                    kNoAllocMaxDevices);
+    void* scratch = nullptr;
+    {
+        // First call on a device: look up the array's device address there (the
+        // array's name in host code is only a stand-in for it).
+        std::lock_guard<std::mutex> lock(g_scratch_mutex);
+        if (!g_scratch_ptr[dev]) {
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_center_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+            g_scratch_ptr[dev] = ptr;
+        }
+        scratch = g_scratch_ptr[dev];
+    }
+    // The row counter must start at zero: clear it in stream order (the array
+    // keeps whatever the previous call, or a failed one, left in it).
+    e = cudaMemsetAsync(scratch, 0, SC_WORKSPACE_BYTES, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch)");
+    return sc_center_forward_backward(logits, T, V, logits_stride, rec_ids, rec_logprobs, rec_count, sampled_id,
+                                      rollout_logprob, row_response, adv, n_resp, p, grad_out, grad_stride, logp_out,
+                                      diag_out, status_dev, scratch, stream);
+}
