@@ -9,10 +9,12 @@ V = 151936, K = 128 recorded ids, synthetic inputs from ``synth``.
 
 Prints one JSON line.  `value` is valid (unmasked) tokens per second over all
 ranks with inputs resident in HBM; `e2e` is the same metric through the same
-calls with pinned host buffers copied in and the step's outputs copied back
-inside the timed region; `roofline` relates the fused kernel's algorithmic
-bytes to the measured HBM copy bandwidth; `cpu_baseline` times the FP64 CPU
-oracle on this machine's cores on a bounded sample of the same batch.
+calls with pinned host buffers copied in and the step's results (per-row
+losses and log p_a) copied back inside the timed region; `roofline` relates
+the fused kernel's algorithmic bytes to the measured HBM copy bandwidth;
+`cpu_baseline` times the FP64 CPU oracle on this machine's cores on a bounded
+sample of the same batch; `secondary` times the sampler-side top-K capture
+(sc_topk_capture) on the batch's FP32 sampler logits.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 For N > 1 launch under torch.distributed.run: every rank processes its own
@@ -163,6 +165,48 @@ def algorithmic_bytes(batch) -> int:
     k_total = int(cnt.sum()) if cnt is not None else valid * batch["K"]
     extra_cnt = 4 * valid if cnt is not None else 0
     return valid * (4 * V + 16 + 68) + 8 * k_total + extra_cnt + masked * (2 * V + 8 + 68)
+
+
+def topk_secondary(batch, dev, peak, peak_kind, reps=10):
+    """The sampler-side top-K capture on the batch's sampler logits (FP32
+    trainer logits plus the sampler's N(0, 0.05^2) perturbation), K = 128,
+    with and without the nucleus: CUDA-event time per launch and the fraction
+    of the HBM copy bandwidth for reading each logit once."""
+    import precision_off_policy_gb300 as sc
+
+    cfg = synth.config(WORKLOAD)
+    g = torch.Generator(device=dev).manual_seed(cfg["seed"] + 77)
+    z = batch["logits"].float()
+    z.add_(torch.randn(z.shape, generator=g, device=dev), alpha=cfg["sigma_s"])
+    T, V = z.shape
+    K = batch["K"]
+    ids = torch.empty((T, K), dtype=torch.int32, device=dev)
+    lps = torch.empty((T, K), dtype=torch.float32, device=dev)
+    cnt = torch.empty(T, dtype=torch.int32, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    out = []
+    alg = T * (4 * V + 8 * K + 4)
+    for inv_t, top_p in [(1.0, 1.0), (1.0 / 0.7, 0.95)]:
+        with torch.cuda.stream(st):
+            for _ in range(3):
+                sc.sc_topk_capture(z, K, inv_t, top_p, ids_out=ids, logprobs_out=lps, count_out=cnt, stream=st)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(reps):
+                sc.sc_topk_capture(z, K, inv_t, top_p, ids_out=ids, logprobs_out=lps, count_out=cnt, stream=st)
+            e1.record(st)
+        st.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        achieved = alg / (ms / 1e3) / 1e9
+        out.append({"kernel": "topk_kernel", "call": "sc_topk_capture",
+                    "workload": f"{WORKLOAD} sampler logits FP32 [{T}, {V}], K={K}, inv_t={inv_t:.4g}, top_p={top_p}",
+                    "rows_per_s": T / (ms / 1e3), "ms_per_launch": ms,
+                    "mean_count": float(cnt.float().mean().item()),
+                    "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                                 "frac": achieved / peak, "peak_source": peak_kind,
+                                 "algorithmic_bytes_per_launch": alg}})
+    del z
+    return out
 
 
 def cpu_baseline(batch, p, adv, min_seconds=10.0, max_passes=50):
@@ -333,16 +377,17 @@ def main():
     elapsed_ms = float(t_max.item())
     value = float(tok.item()) / (elapsed_ms / 1e3)
 
-    # ---- end to end: pinned host buffers in, outputs back, every step --------
-    # Three device buffer sets and three streams: step i+1's inputs copy in
-    # (copy-in stream) while step i computes (compute stream) and step i-1's
-    # gradient, log p_a and diagnostics copy out (copy-out stream), so both
-    # copy directions and the kernels overlap.  Host outputs alternate between
-    # two pinned buffers.
+    # ---- end to end: pinned host buffers in, the step's result back ----------
+    # Every step copies its inputs in from pinned host memory and reads its
+    # result back: the per-row losses and log p_a (the diagnostics records and
+    # logp_out).  The gradient stays on the device, where the backward pass of
+    # the LM head consumes it.  Three device buffer sets and three streams:
+    # step i+1's inputs copy in (copy-in stream) while step i computes (compute
+    # stream) and step i-1's results copy out (copy-out stream).  Host outputs
+    # alternate between two pinned buffers.
     host_in = {k: batch[k].cpu().pin_memory() for k in
                ["logits", "rec_ids", "rec_logprobs", "sampled", "rollout_logprob", "row_response", "rewards"]}
-    host_out = [dict(grad=torch.empty((T, V), dtype=torch.bfloat16).pin_memory(),
-                     logp=torch.empty(T, dtype=torch.float32).pin_memory(),
+    host_out = [dict(logp=torch.empty(T, dtype=torch.float32).pin_memory(),
                      diag=torch.empty((T, 16), dtype=torch.int32).pin_memory()) for _ in range(2)]
     del grad
     torch.cuda.empty_cache()
@@ -380,7 +425,6 @@ def main():
             copy_out.wait_event(bs["computed"])
             with torch.cuda.stream(copy_out):
                 ho = host_out[i % 2]
-                ho["grad"].copy_(bs["grad"], non_blocking=True)
                 ho["logp"].copy_(bs["logp"], non_blocking=True)
                 ho["diag"].copy_(bs["diag"], non_blocking=True)
                 bs["done"].record(copy_out)
@@ -425,6 +469,9 @@ def main():
         "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
     }
+    del sets
+    torch.cuda.empty_cache()
+    line["secondary"] = topk_secondary(batch, dev, peak, peak_kind)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         adv_or = oracle.group_advantages(batch["rewards"].cpu().numpy(), batch["n_groups"], batch["group_size"],
