@@ -27,6 +27,7 @@
 #include <map>
 #include <mutex>
 
+#include "sc_device.cuh"
 #include "sc_internal.h"
 
 namespace sc {
@@ -98,6 +99,11 @@ struct Shared {
     unsigned long long cand[kCap];      // (key << 32) | ~id, sorted descending
     unsigned long long top[kMaxTopK];   // the selected entries, sorted
     unsigned long long scan[kNT / 32];  // block scan scratch
+    float fred[kNT / 32];               // block maximum; block sums (high parts)
+    float flo[kNT / 32];                // block sums (low parts)
+    double dS, dlse;                    // the row's normaliser and log-sum-exp
+    int cross;                          // first candidate at which the nucleus mass is reached
+    double pnuc;                        // the nucleus mass there
     unsigned long long s_fixed;         // the row's normaliser, fixed point
     uint32_t maxkey;
     int ncand;
@@ -157,19 +163,35 @@ __device__ void find_from_top(Shared& sh, const T* vals, int nbins, double targe
     __syncthreads();
 }
 
-// Every entry of the row, 16-byte loads, f(z, id).
+// Every entry of the row, f(z, id): 16-byte loads, kUnroll of them in flight
+// per thread before any is used (every caller's f is order-independent).
+constexpr int kUnroll = 4;
 template <typename F>
 __device__ __forceinline__ void for_each_entry(const float* row, int V, F&& f) {
     const int nv4 = V >> 2;
     const float4* r4 = reinterpret_cast<const float4*>(row);
-    for (int i = threadIdx.x; i < nv4; i += kNT) {
+    int i = threadIdx.x;
+    for (; i + (kUnroll - 1) * kNT < nv4; i += kUnroll * kNT) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(r4 + i + u * kNT);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = 4 * (i + u * kNT);
+            f(v[u].x, b);
+            f(v[u].y, b + 1);
+            f(v[u].z, b + 2);
+            f(v[u].w, b + 3);
+        }
+    }
+    for (; i < nv4; i += kNT) {
         const float4 v = __ldg(r4 + i);
         f(v.x, 4 * i);
         f(v.y, 4 * i + 1);
         f(v.z, 4 * i + 2);
         f(v.w, 4 * i + 3);
     }
-    for (int i = (nv4 << 2) + static_cast<int>(threadIdx.x); i < V; i += kNT) f(__ldg(row + i), i);
+    for (int j = (nv4 << 2) + static_cast<int>(threadIdx.x); j < V; j += kNT) f(__ldg(row + j), j);
 }
 
 __device__ __forceinline__ unsigned long long pack_entry(uint32_t key, int id) {
@@ -454,16 +476,16 @@ __device__ void find_from_top_f(Shared& sh, const float* vals, double target) {
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_constant__ TopkArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+// The exact path for one row: radix selection over the whole row (two or more
+// passes over it), for any row the one-pass path below cannot finish.
+__device__ void exact_row(Shared& sh, const TopkArgs& a, long long t) {
     unsigned long long* top = sh.top;
     const int tid = threadIdx.x;
     const int V = a.V;
     const int Kp = min(a.K, V);
     const float kt = a.inv_t * kLog2e;
     const bool use_p = a.top_p < 1.0f;
-    for (long long t = blockIdx.x; t < a.T; t += gridDim.x) {
+    {
         const float* row = a.logits + t * a.stride;
         // ---- pass 1: the maximum and the top digit's histogram
         for (int i = tid; i < kBins; i += kNT) sh.hist0[i] = 0u;
@@ -486,16 +508,13 @@ __global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_const
         const bool coll0 = rabove + sh.hist0[rbin] <= static_cast<unsigned long long>(kCap);
         const uint32_t lowkey = static_cast<uint32_t>(rbin) << 20;
 
-        // ---- pass 2: the normaliser, the masses of the top digit, the candidates
-        for (int i = tid; i < kBins; i += kNT) sh.mhf[i] = 0.0f;
+        // ---- pass 2: the normaliser and the candidates
         if (tid == 0) sh.ncand = 0;
         __syncthreads();
         unsigned long long s = 0ull;
         for_each_entry(row, V, [&](float z, int id) {
             const uint32_t k = key_of(z);
-            const float e = rel_mass(z, mz, kt);
-            s += to_fixed(e);
-            if (use_p) atomicAdd(&sh.mhf[k >> 20], e);
+            s += fixed_q(z, mz, kt);
             if (coll0 && k >= lowkey) {
                 const int pos = atomicAdd(&sh.ncand, 1);
                 if (pos < kCap) sh.cand[pos] = pack_entry(k, id);
@@ -542,8 +561,13 @@ __global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_const
                 P = sh.found_above;
                 __syncthreads();
             } else {
-                // it ends further down: the FP32 mass histogram of pass 2 points
-                // to the bin, the exact search confirms it
+                // it ends further down (rows flatter than the selection): the FP32
+                // mass histogram of the top digit, taken only now, points to the
+                // bin, the exact search confirms it
+                for (int i = tid; i < kBins; i += kNT) sh.mhf[i] = 0.0f;
+                __syncthreads();
+                for_each_entry(row, V, [&](float z, int) { atomicAdd(&sh.mhf[key_of(z) >> 20], rel_mass(z, mz, kt)); });
+                __syncthreads();
                 find_from_top_f(sh, sh.mhf, thr);
                 int bp = sh.found_bin;
                 if (bp < 0) bp = rbin;
@@ -570,6 +594,261 @@ __global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_const
         if (tid == 0 && a.counts) a.counts[t] = count;
         __syncthreads();
     }
+}
+
+constexpr int kNW = kNT / 32;
+constexpr int kSampRun = 32;    // vectors per sampled run (one warp load)
+constexpr int kSampEvery = 16;  // one run in kSampEvery is sampled
+
+// A sum kept as an unevaluated FP32 pair hi + lo, added without error
+// (two-sum): the same bits in every lane whatever the order of the operands.
+struct Pair {
+    float hi, lo;
+};
+__device__ __forceinline__ Pair pair_add(Pair a, Pair b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    return Pair{s, (a.lo + b.lo) + e};
+}
+__device__ __forceinline__ Pair pair_shfl_xor(Pair v, int o) {
+    return Pair{__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
+}
+// Sum of the threads' pairs over the block in a fixed order.
+__device__ Pair block_sum_pair(Shared& sh, Pair v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = pair_add(v, pair_shfl_xor(v, o));
+    if (lane == 0) {
+        sh.fred[warp] = v.hi;
+        sh.flo[warp] = v.lo;
+    }
+    __syncthreads();
+    Pair r{0.0f, 0.0f};
+    for (int w = 0; w < kNW; ++w) r = pair_add(r, Pair{sh.fred[w], sh.flo[w]});
+    __syncthreads();
+    return r;
+}
+__device__ float block_max_f(Shared& sh, float v) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    if (lane == 0) sh.fred[warp] = v;
+    __syncthreads();
+    float r = -INFINITY;
+    for (int w = 0; w < kNW; ++w) r = fmaxf(r, sh.fred[w]);
+    __syncthreads();
+    return r;
+}
+// Bitonic sort of kNT keys, larger first (one per thread).
+__device__ void sort_keys_desc(uint32_t* k) {
+    const int i = threadIdx.x;
+    for (int size = 2; size <= kNT; size <<= 1)
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const int l = i ^ j;
+            if (l > i) {
+                const uint32_t x = k[i], y = k[l];
+                if (((i & size) == 0) ? (x < y) : (x > y)) {
+                    k[i] = y;
+                    k[l] = x;
+                }
+            }
+            __syncthreads();
+        }
+}
+
+// The one-pass path for one row.  A sample (every kSampEvery-th run of
+// vectors) gives each thread a maximum; the largest of those maxima is the
+// exponent offset, and the `rank`-th largest the candidate threshold, placed
+// so that about 3 K entries of the row reach it.  One pass over the row then
+// sums 2^(z kt - offset kt) per thread (compensated, in a fixed order; a
+// thread that meets an entry above the offset moves its own offset up) and
+// collects every entry at or above the threshold.  The candidates are sorted;
+// the top K and, with top_p < 1, the nucleus come from them.  Returns false --
+// outputs untouched, the same decision in every thread -- when the row needs
+// the exact path: too few or too many candidates, a nucleus that reaches below
+// them, entries that are not finite, or K above kCap / 4.
+__device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
+    const float* row = a.logits + t * a.stride;
+    const int V = a.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Kp = min(a.K, V);
+    if (4 * Kp > kCap) return false;
+    const float kt = a.inv_t * kLog2e;
+    const int nv4 = V >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+
+    // ---- the threshold and the offset from the sample
+    float tau = -INFINITY;  // candidates: z >= tau (-inf: every entry)
+    float o = -INFINITY;    // exponent offset of the sums
+    if (V > kCap) {
+        const int nruns = nv4 / kSampRun;
+        float smax = -INFINITY;
+        for (int r = warp * kSampEvery; r < nruns; r += kNW * kSampEvery) {
+            const float4 v = __ldg(r4 + r * kSampRun + lane);
+            smax = fmaxf(smax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        }
+        sh.hist[tid] = key_of(smax);
+        __syncthreads();
+        sort_keys_desc(sh.hist);
+        const int rank = max(8, (3 * Kp + kSampEvery - 1) / kSampEvery);
+        tau = float_of(sh.hist[rank - 1]);
+        o = float_of(sh.hist[0]);
+        __syncthreads();
+        if (!isfinite(o)) return false;
+    }
+
+    // ---- one pass: the sums and the candidates
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    // (z - m) is formed first and then scaled, so the terms nearest the
+    // offset -- the ones that dominate the sum -- carry no rounding of the offset
+    float m = o;                      // this thread's offset
+    float s = 0.0f, c = 0.0f;         // compensated sum of 2^((z - m) kt)
+    const f2_t KT2 = f2_pack(kt, kt);
+    auto raise = [&](float m_new) {   // an entry above this thread's offset
+        if (m > -INFINITY) {
+            const float f = ex2((m - m_new) * kt);
+            s *= f;
+            c *= f;
+        }
+        m = m_new;
+    };
+    auto add = [&](float e) {
+        const float y = e - c;
+        const float u = s + y;
+        c = (u - s) - y;
+        s = u;
+    };
+    auto collect1 = [&](float z, int id) {
+        if (z >= tau) {
+            const int pos = atomicAdd(&sh.ncand, 1);
+            if (pos < kCap) sh.cand[pos] = pack_entry(key_of(z), id);
+        }
+    };
+    auto take4 = [&](const float4& v, int id0) {
+        const float m4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+        if (m4 > m) raise(m4);
+        if (m > -INFINITY) {
+            const f2_t NM = f2_pack(-m, -m);
+            const f2_t e01 = f2_ex2(f2_mul(f2_add(f2_pack(v.x, v.y), NM), KT2));
+            const f2_t e23 = f2_ex2(f2_mul(f2_add(f2_pack(v.z, v.w), NM), KT2));
+            const f2_t e = f2_add(e01, e23);
+            add(f2_lo(e) + f2_hi(e));
+        }
+        if (m4 >= tau) {
+            collect1(v.x, id0);
+            collect1(v.y, id0 + 1);
+            collect1(v.z, id0 + 2);
+            collect1(v.w, id0 + 3);
+        }
+    };
+    {
+        int i = tid;
+        for (; i + (kUnroll - 1) * kNT < nv4; i += kUnroll * kNT) {
+            float4 v[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(r4 + i + u * kNT);
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) take4(v[u], 4 * (i + u * kNT));
+        }
+        for (; i < nv4; i += kNT) take4(__ldg(r4 + i), 4 * i);
+        for (int j = (nv4 << 2) + tid; j < V; j += kNT) {
+            const float z = __ldg(row + j);
+            if (z > m) raise(z);
+            if (m > -INFINITY) add(ex2((z - m) * kt));
+            collect1(z, j);
+        }
+    }
+    // ---- the normaliser: every thread's sum moved to the row maximum M
+    // (threads already there untouched), summed without error in a fixed order
+    const float M = block_max_f(sh, m);
+    float part = s - c;
+    if (!(m > -INFINITY)) part = 0.0f;
+    else if (m != M) part *= ex2((m - M) * kt);
+    const Pair tot = block_sum_pair(sh, Pair{part, 0.0f});
+    if (tid == 0) {
+        const double S = (double)tot.hi + (double)tot.lo;
+        sh.dS = S;
+        sh.dlse = (double)M * a.inv_t + log(S);
+    }
+    __syncthreads();
+    const double S = sh.dS, lse = sh.dlse;
+    const int nc = sh.ncand;
+    if (!isfinite(M) || !(S > 0.0) || !isfinite(S) || !isfinite(lse) || nc < Kp || nc > kCap) return false;
+    sort_desc(sh, nc);
+
+    // ---- the nucleus: one warp walks the sorted candidates with error-free
+    // FP32 running sums
+    int count = Kp;
+    double log_nuc = 0.0;
+    if (a.top_p < 1.0f) {
+        if (warp == 0) {
+            const double thr = (double)a.top_p * S;
+            const float t_hi = (float)thr, t_lo = (float)(thr - (double)t_hi);
+            const int per = (nc + 31) / 32;
+            const int i0 = lane * per, i1 = min(nc, i0 + per);
+            auto mass = [&](int i) { return ex2((float_of(static_cast<uint32_t>(sh.cand[i] >> 32)) - M) * kt); };
+            Pair loc{0.0f, 0.0f};
+            for (int i = i0; i < i1; ++i) loc = pair_add(loc, Pair{mass(i), 0.0f});
+            // exclusive scan of the lanes' pairs, in lane order
+            Pair inc = loc;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const Pair y{__shfl_up_sync(0xFFFFFFFFu, inc.hi, d), __shfl_up_sync(0xFFFFFFFFu, inc.lo, d)};
+                if (lane >= d) inc = pair_add(y, inc);
+            }
+            const Pair all{__shfl_sync(0xFFFFFFFFu, inc.hi, 31), __shfl_sync(0xFFFFFFFFu, inc.lo, 31)};
+            Pair run{__shfl_up_sync(0xFFFFFFFFu, inc.hi, 1), __shfl_up_sync(0xFFFFFFFFu, inc.lo, 1)};
+            if (lane == 0) run = Pair{0.0f, 0.0f};
+            // first candidate whose preceding mass reaches thr
+            int mine = nc + 1;
+            for (int i = i0; i < i1; ++i) {
+                if ((run.hi - t_hi) + (run.lo - t_lo) >= 0.0f) {
+                    mine = i;
+                    break;
+                }
+                run = pair_add(run, Pair{mass(i), 0.0f});
+            }
+            int cross = mine;
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) cross = min(cross, __shfl_xor_sync(0xFFFFFFFFu, cross, o2));
+            if (lane == 0) {
+                sh.cross = cross;
+                if (cross > nc) sh.pnuc = (all.hi - t_hi) + (all.lo - t_lo) >= 0.0f ? (double)all.hi + (double)all.lo : -1.0;
+            }
+            if (mine == cross && cross <= nc) sh.pnuc = (double)run.hi + (double)run.lo;
+        }
+        __syncthreads();
+        const int cross = sh.cross;
+        const double P = sh.pnuc;
+        __syncthreads();
+        if (!(P > 0.0)) return false;  // the nucleus reaches below the candidates
+        count = min(Kp, cross <= nc ? cross : nc);
+        log_nuc = log(P / S);
+    }
+
+    // ---- outputs
+    int32_t* ids = a.ids + t * a.K;
+    float* lps = a.lps + t * a.K;
+    for (int i = tid; i < a.K; i += kNT) {
+        if (i < count) {
+            const uint32_t key = static_cast<uint32_t>(sh.cand[i] >> 32);
+            ids[i] = static_cast<int>(~static_cast<uint32_t>(sh.cand[i]));
+            lps[i] = static_cast<float>(static_cast<double>(float_of(key)) * a.inv_t - lse - log_nuc);
+        } else {
+            ids[i] = -1;
+            lps[i] = 0.0f;
+        }
+    }
+    if (tid == 0 && a.counts) a.counts[t] = count;
+    __syncthreads();
+    return true;
+}
+
+__global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_constant__ TopkArgs a) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
+    for (long long t = blockIdx.x; t < a.T; t += gridDim.x)
+        if (!fast_row(sh, a, t)) exact_row(sh, a, t);
 }
 
 }  // namespace
