@@ -735,11 +735,19 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             // ---- this CTA's record of row j, sent from registers ----
             {
                 const float* rp = red + p * 3 * NCW;
+                // one offset in every warp (the usual case): plain sums in warp
+                // order, read by every lane
+                bool same = true;
+                float q1 = 0.0f, q2 = 0.0f;
+                for (int w = 0; w < NCW; ++w) {
+                    same = same && rp[w] == rp[0];
+                    q1 += rp[NCW + w];
+                    q2 += rp[2 * NCW + w];
+                }
                 Mass cm = lane < NCW ? Mass{rp[lane], rp[NCW + lane], rp[2 * NCW + lane]}
                                      : Mass{rp[0], 0.0f, 0.0f};
-                if (__all_sync(kFull, cm.m == rp[0])) {  // one offset in every warp: plain sums
-                    cm.s1 = warp_sum(cm.s1);
-                    cm.s2 = warp_sum(cm.s2);
+                if (same) {
+                    cm = Mass{rp[0], q1, q2};
                 } else {
                     if (lane >= NCW) cm.m = -INFINITY;
 #pragma unroll
@@ -763,7 +771,6 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                                 __float_as_uint(m.omq), rb);
                 }
             }
-            finish_prev();  // while the peers' records are on their way
             // ---- all C records of row j: the row scalars ----
             const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j >> 2) & 1u, kWaitLimitNs);
             if (!__all_sync(kFull, ok)) {
@@ -771,56 +778,44 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 break;
             }
             {
-                // lane r < C holds CTA r's record; the others hold neutral values
+                // Every lane reads the C records (broadcast loads) and merges them
+                // in CTA order: the same bits in every lane, no shuffles.  The
+                // previous row's sum is added in the same order as the
+                // end-of-stream flush adds the last row's, so a row's sum does not
+                // depend on which of the two paths finished it.
                 const Partial* pp = part + xi * C;
-                const bool have = lane < C;
-                const uint32_t pa = smem_addr(pp + (have ? lane : 0));
-                const uint4 r0 = lds128(pa), r1 = lds128(pa + 16u), r2 = lds128(pa + 32u), r3 = lds128(pa + 48u);
-                const float Pm = have ? __uint_as_float(r0.x) : -INFINITY;
-                const float mg = warp_max(Pm);
+                float mg = -INFINITY;
+                for (int r = 0; r < C; ++r) mg = fmaxf(mg, pp[r].m);
                 const float o = mg * kscale;
-                const bool live = Pm > -INFINITY;
-                const float d = live ? Pm * kscale - o : 0.0f;
-                const float f = live ? ex2(d) : 0.0f;
-                const float PS1 = have ? __uint_as_float(r0.y) : 0.0f;
-                const float PS2 = have ? __uint_as_float(r0.z) : 0.0f;
-                const float Prs = have ? __uint_as_float(r0.w) : 0.0f;
-                const float PlH = have ? __uint_as_float(r1.x) : 0.0f;
-                const float PEH = have ? __uint_as_float(r1.y) : 0.0f;
-                const float PQY = have ? __uint_as_float(r1.z) : 0.0f;
-                const int Pnval = have ? static_cast<int>(r2.w) : 0;
-                float lT = f * PS1;
-                float ET = f * fmaf(d, PS1, PS2);
-                float lH = f * PlH;
-                float EH = f * fmaf(d, PlH, PEH);
-                float QYg = 0.0f;
-                if (Pnval > 0) {
-                    const float Qc = (__uint_as_float(r2.y) + __uint_as_float(r1.w)) + __uint_as_float(r2.x);
-                    QYg = fmaf(d, Qc, PQY);
+                float lT = 0.0f, ET = 0.0f, lH = 0.0f, EH = 0.0f, QYg = 0.0f, ya = 0.0f, rsum = 0.0f;
+                int nval = 0;
+                uint32_t flags = 0u;
+                HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};
+                for (int r = 0; r < C; ++r) {
+                    const uint32_t pa = smem_addr(pp + r);
+                    const uint4 r0 = lds128(pa), r1 = lds128(pa + 16u), r2 = lds128(pa + 32u), r3 = lds128(pa + 48u);
+                    const float Pm = __uint_as_float(r0.x);
+                    const bool live = Pm > -INFINITY;
+                    const float d = live ? Pm * kscale - o : 0.0f;
+                    const float f = live ? ex2(d) : 0.0f;
+                    const float PS1 = __uint_as_float(r0.y), PS2 = __uint_as_float(r0.z);
+                    const float PlH = __uint_as_float(r1.x), PEH = __uint_as_float(r1.y);
+                    const int Pnval = static_cast<int>(r2.w);
+                    lT = fmaf(f, PS1, lT);
+                    ET = fmaf(f, fmaf(d, PS1, PS2), ET);
+                    lH = fmaf(f, PlH, lH);
+                    EH = fmaf(f, fmaf(d, PlH, PEH), EH);
+                    if (Pnval > 0) {
+                        const float Qc = (__uint_as_float(r2.y) + __uint_as_float(r1.w)) + __uint_as_float(r2.x);
+                        QYg += fmaf(d, Qc, __uint_as_float(r1.z));
+                    }
+                    if (r3.z) ya += __uint_as_float(r3.y) + d;
+                    rsum += __uint_as_float(r0.w);
+                    nval += Pnval;
+                    flags |= r3.x;
+                    hm = head_merge(hm, HeadMass{__uint_as_float(r2.y), static_cast<int>(r2.z), __uint_as_float(r3.w),
+                                                 __uint_as_float(r1.w), __uint_as_float(r2.x)});
                 }
-                float ya = (have && r3.z) ? __uint_as_float(r3.y) + d : 0.0f;
-                int nval = Pnval;
-                uint32_t flags = have ? r3.x : 0u;
-                HeadMass hm{have ? __uint_as_float(r2.y) : 0.0f, have ? static_cast<int>(r2.z) : 0x7FFFFFFF,
-                            have ? __uint_as_float(r3.w) : 1.0f, have ? __uint_as_float(r1.w) : 0.0f,
-                            have ? __uint_as_float(r2.x) : 0.0f};
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    lT += __shfl_xor_sync(kFull, lT, off);
-                    ET += __shfl_xor_sync(kFull, ET, off);
-                    lH += __shfl_xor_sync(kFull, lH, off);
-                    EH += __shfl_xor_sync(kFull, EH, off);
-                    QYg += __shfl_xor_sync(kFull, QYg, off);
-                    ya += __shfl_xor_sync(kFull, ya, off);
-                    nval += __shfl_xor_sync(kFull, nval, off);
-                    flags |= __shfl_xor_sync(kFull, flags, off);
-                    hm = head_merge(hm, head_shfl(hm, off));
-                }
-                // the previous row's sum, in CTA order (as the end-of-stream flush
-                // adds the last row's), so a row's sum does not depend on which
-                // of the two paths finished it
-                float rsum = 0.0f;
-                for (int r = 0; r < C; ++r) rsum += __shfl_sync(kFull, Prs, r);
                 // 1 - Q_H without cancellation: (1 - q_max), taken from its
                 // log-probability, minus the others' mass
                 float tail_mu = 1.0f, Q_H = 0.0f;
@@ -872,6 +867,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sready(p));
+                finish_prev();  // the previous row's special entries, off the critical path
 
                 if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
                 if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
