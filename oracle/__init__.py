@@ -114,6 +114,8 @@ def lib():
             L.sco_bf16_to_double.argtypes = [ctypes.c_uint16]
             L.sco_double_to_bf16_rne.restype = ctypes.c_uint16
             L.sco_double_to_bf16_rne.argtypes = [ctypes.c_double]
+            L.sco_round_bf16_n.restype = None
+            L.sco_round_bf16_n.argtypes = [ctypes.c_void_p, ctypes.c_longlong, ctypes.c_void_p]
             L.sco_group_advantages.restype = ctypes.c_int
             L.sco_group_advantages.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_double, ctypes.c_void_p]
@@ -273,3 +275,39 @@ def rows(batch: dict, params: Params, row_idx=None, nthreads: int = 0):
     if used < 0:
         raise ValueError("sco_rows rejected its arguments")
     return g, la, out, used
+
+
+def bf16_round_array(x) -> np.ndarray:
+    """Every entry of x rounded to bf16 (ties to even); uint16 bit patterns, same shape."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(a.shape, dtype=np.uint16)
+    lib().sco_round_bf16_n(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def lmhead_rows(hidden_bits, w_bits, batch: dict, params: Params, nthreads: int = 0):
+    """The LM head followed by score centering, for a BF16 trainer.
+
+    The trainer's logits are z = bf16(H W^T): H [T, d] and W [V, d] are bf16
+    values, their products summed in FP64 and rounded once to bf16 (ties to
+    even).  Every row then gets the score-centered gradient g of the row
+    oracle (``rows``), and the gradients of the batch loss
+    grad_scale * sum_t loss_t with respect to the LM head's inputs follow from
+    z's linearity: dH = g W and dW = g^T H, in FP64 from the unrounded g.
+
+    hidden_bits: uint16 [T, d]; w_bits: uint16 [V, d]; batch: the keys of
+    ``rows`` except logits (V taken from w_bits).
+    Returns (dH [T, d], dW [V, d], logp_a [T], out [T], z_bits [T, V]).
+    """
+    Hb = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
+    Wb = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    if Hb.ndim != 2 or Wb.ndim != 2 or Hb.shape[1] != Wb.shape[1]:
+        raise ValueError("hidden must be [T, d] and w [V, d] with the same d")
+    H = bf16_to_double(Hb)
+    W = bf16_to_double(Wb)
+    z_bits = bf16_round_array(H @ W.T)
+    b = dict(batch)
+    b["logits"] = z_bits
+    b["V"] = Wb.shape[0]
+    g, la, out, _ = rows(b, params, None, nthreads)
+    return g @ W, g.T @ H, la, out, z_bits

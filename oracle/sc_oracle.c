@@ -491,6 +491,11 @@ int sco_rows(const uint16_t* logits, long long T, int V, long long row_stride, c
     return failed ? -1 : started;
 }
 
+/* Every entry of x rounded to bf16 (ties to even), as bit patterns. */
+void sco_round_bf16_n(const double* x, long long n, uint16_t* out) {
+    for (long long i = 0; i < n; ++i) out[i] = sco_double_to_bf16_rne(x[i]);
+}
+
 int sco_row_out_size(void) { return (int)sizeof(sco_row_out); }
 int sco_params_size(void) { return (int)sizeof(sco_params); }
 

@@ -696,3 +696,97 @@ def test_topk_capture_selection_invariants(inv_t, top_p):
             assert c == min(K, n_keep)
             nuc = np.exp(ls[order[:n_keep]]).sum()
             np.testing.assert_allclose(lp[t, :c], ls[sel] - np.log(nuc), rtol=1e-6, atol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# The LM head followed by score centering (z = bf16(H W^T); dH = g W, dW = g^T H).
+
+
+def _lmhead_case(rng, T=4, d=5, V=12, K=3, inv_t=1.0):
+    # small integers: z = H W^T is an integer of a few bits, exact in bf16
+    H = rng.integers(-2, 3, size=(T, d)).astype(np.float64)
+    W = rng.integers(-2, 3, size=(V, d)).astype(np.float64)
+    ids = np.stack([rng.choice(V, K, replace=False) for _ in range(T)]).astype(np.int32)
+    lp = np.log(rng.dirichlet(np.ones(K), size=T) * 0.8).astype(np.float32)
+    sampled = rng.integers(0, V, size=T).astype(np.int32)
+    resp = np.array([0, 1, -1, 1][:T], dtype=np.int32)
+    adv = np.array([0.9, -1.3], dtype=np.float32)
+    batch = dict(rec_ids=ids, rec_logprobs=lp, rec_count=None, sampled=sampled, rollout_logprob=None,
+                 row_response=resp, adv=adv)
+    return H, W, batch
+
+
+@pytest.mark.parametrize("inv_t,seed", [(1.0, 41), (1 / 0.7, 42)])
+def test_lmhead_gradients_match_central_differences(inv_t, seed):
+    rng = np.random.default_rng(seed)
+    H, W, batch = _lmhead_case(rng, inv_t=inv_t)
+    scale = 0.25
+    prm = oracle.make_params(inv_temperature=inv_t, grad_scale=scale)
+    dH, dW, la, out, zb = oracle.lmhead_rows(bf16_bits(H), bf16_bits(W), batch, prm)
+    assert np.array_equal(bf16_values(zb), H @ W.T)  # exact here: the rounding is the identity
+    T = H.shape[0]
+    # the batch loss with every row's stop-gradient constants c held at the base point
+    consts = []
+    for t in range(T):
+        if batch["row_response"][t] < 0:
+            consts.append(None)
+            continue
+        p0 = softmax((H[t] @ W.T) * inv_t)
+        ids = batch["rec_ids"][t]
+        c = np.exp(batch["rec_logprobs"][t].astype(np.float64)) - out["rho"][t] * p0[ids]
+        consts.append((ids, c, int(batch["sampled"][t]), float(batch["adv"][batch["row_response"][t]])))
+
+    def loss(HH, WW):
+        tot = 0.0
+        for t, k in enumerate(consts):
+            if k is None:
+                continue
+            ids, c, a, A = k
+            l = log_softmax((HH[t] @ WW.T) * inv_t)
+            tot += -A * (l[a] - np.dot(c, l[ids]))
+        return scale * tot
+
+    np.testing.assert_allclose(loss(H, W), scale * out["loss"].sum(), rtol=1e-12)
+    h = 1e-6
+    fdH = np.zeros_like(H)
+    for i in np.ndindex(H.shape):
+        e = np.zeros_like(H)
+        e[i] = h
+        fdH[i] = (loss(H + e, W) - loss(H - e, W)) / (2 * h)
+    fdW = np.zeros_like(W)
+    for i in np.ndindex(W.shape):
+        e = np.zeros_like(W)
+        e[i] = h
+        fdW[i] = (loss(H, W + e) - loss(H, W - e)) / (2 * h)
+    np.testing.assert_allclose(dH, fdH, rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dW, fdW, rtol=1e-6, atol=1e-8)
+    assert np.all(dH[2] == 0)  # the padding row contributes nothing
+
+
+def test_lmhead_with_identity_head_reduces_to_the_row_oracle():
+    # W = I (V = d): z = bf16(H), dH is the rows' gradient itself and dW = g^T H.
+    rng = np.random.default_rng(43)
+    T, d, K = 6, 40, 8
+    Hb = bf16_bits(rng.standard_normal((T, d)) * 2.0)
+    Wb = bf16_bits(np.eye(d))
+    ids = np.stack([rng.choice(d, K, replace=False) for _ in range(T)]).astype(np.int32)
+    lp = np.log(rng.dirichlet(np.ones(K), size=T) * 0.9).astype(np.float32)
+    batch = dict(rec_ids=ids, rec_logprobs=lp, rec_count=None, sampled=rng.integers(0, d, T).astype(np.int32),
+                 rollout_logprob=None, row_response=np.array([0, 0, 1, 1, -1, 0], np.int32),
+                 adv=np.array([1.1, -0.4], np.float32))
+    prm = oracle.make_params()
+    dH, dW, la, out, zb = oracle.lmhead_rows(Hb, Wb, batch, prm)
+    assert np.array_equal(zb, Hb)
+    g, la2, out2, _ = oracle.rows(dict(batch, logits=Hb, V=d), prm)
+    np.testing.assert_array_equal(dH, g)
+    np.testing.assert_allclose(dW, g.T @ bf16_values(Hb), rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(la, la2)
+
+
+def test_bf16_round_array_matches_the_scalar_rounding():
+    rng = np.random.default_rng(44)
+    x = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-6, 6, 2000), [0.0, -0.0, 1.0 + 2.0**-8]])
+    got = oracle.bf16_round_array(x)
+    ref = np.array([oracle.bf16_bits(float(v)) for v in x], dtype=np.uint16)
+    np.testing.assert_array_equal(got, ref)
+    assert got[-1] == 0x3F80  # the tie 1 + 2^-8 rounds to even (1.0)
