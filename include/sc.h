@@ -38,6 +38,7 @@
 #ifndef SC_H
 #define SC_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -295,6 +296,43 @@ int sc_center_forward_backward_noalloc(const uint16_t* logits, long long T, int 
                                        const float* adv, int n_resp, const sc_params* p, uint16_t* grad_out,
                                        long long grad_stride, float* logp_out, sc_row_diag* diag_out,
                                        uint32_t* status_dev, sc_stream_t stream);
+
+/*
+ * The LM head followed by score centering, in row blocks (the next step of
+ * the path: the trainer's logits come from its LM head, z = H W^T).
+ *
+ * hidden      : bf16 [T, d] hidden states H, rows contiguous (d % 8 == 0),
+ *               16-byte aligned.
+ * w           : bf16 [V, d] the LM head W, 16-byte aligned.
+ * rec_ids ... p : as sc_center_forward_backward, for the T rows.
+ * block_rows  : rows per block; only one [block_rows, V] block of logits is
+ *               ever held (in the workspace).
+ * dhidden     : bf16 [T, d], written: dH = g W, g the score-centered gradient
+ *               of grad_scale * sum(loss) with respect to z.
+ * dw          : FP32 [V, d], written (not accumulated across calls):
+ *               dW = g^T H.
+ * logp_out, diag_out, status_dev : as sc_center_forward_backward.
+ * workspace   : sc_lmhead_workspace_bytes(block_rows, V) bytes of device
+ *               memory, 256-byte aligned; its first SC_WORKSPACE_BYTES must
+ *               be zero before the first call (they are left zero, as for
+ *               sc_center_forward_backward).  It holds cuBLASLt's scratch and
+ *               the block of logits.  Calls that may run at the same time
+ *               need workspaces of their own.
+ * Per block: z_b = H_b W^T (cuBLASLt, FP32 accumulation, bf16 logits), the
+ * fused score-centering kernel in place, dH_b = g_b W and dW += g_b^T H_b
+ * (cuBLASLt, FP32 accumulation); all asynchronous on `stream`.
+ * Errors: as sc_center_forward_backward, plus SC_ERR_SHAPE (d not a multiple
+ * of 8, block_rows < 1, workspace too small), SC_ERR_CUDA for a cuBLASLt
+ * failure (its status in the message).  T == 0 is a no-op.
+ */
+size_t sc_lmhead_workspace_bytes(long long block_rows, int V);
+int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t* w, long long T, int d, int V,
+                               const int32_t* rec_ids, const float* rec_logprobs, const int32_t* rec_count,
+                               const int32_t* sampled_id, const float* rollout_logprob,
+                               const int32_t* row_response, const float* adv, int n_resp, const sc_params* p,
+                               long long block_rows, uint16_t* dhidden, float* dw, float* logp_out,
+                               sc_row_diag* diag_out, uint32_t* status_dev, void* workspace,
+                               size_t workspace_bytes, sc_stream_t stream);
 
 /* Launch plan the library would use for a vocabulary of V and these
  * parameters on the current device (no launch).  Any output pointer may be

@@ -29,7 +29,7 @@ __all__ = [
     "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
     "ScoreCenteredLoss", "score_centered_loss",
     "sc_rollout_mean_advantages", "sc_topk_capture", "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS", "SC_IS_CLIP",
-    "WORKSPACE_BYTES", "workspace", "reset_workspaces",
+    "WORKSPACE_BYTES", "workspace", "reset_workspaces", "sc_lmhead_forward_backward",
 ]
 
 SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
@@ -50,7 +50,8 @@ FLAG_CLIPPED = 0x400
 
 # Symbols declared in include/sc.h.
 EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_rollout_mean_advantages", "sc_topk_capture",
-           "sc_center_forward_backward", "sc_center_forward_backward_noalloc", "sc_plan_query",
+           "sc_center_forward_backward", "sc_center_forward_backward_noalloc", "sc_lmhead_workspace_bytes",
+           "sc_lmhead_forward_backward", "sc_plan_query",
            "sc_status_string", "sc_last_error", "sc_abi_version"]
 
 
@@ -118,6 +119,12 @@ def lib():
             L.sc_center_forward_backward_noalloc.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                                              ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
             L.sc_center_forward_backward_noalloc.restype = i32
+            L.sc_lmhead_workspace_bytes.argtypes = [i64, i32]
+            L.sc_lmhead_workspace_bytes.restype = ctypes.c_size_t
+            L.sc_lmhead_forward_backward.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                     ctypes.POINTER(Params), i64, vp, vp, vp, vp, vp, vp,
+                                                     ctypes.c_size_t, vp]
+            L.sc_lmhead_forward_backward.restype = i32
             L.sc_plan_query.argtypes = [i32, ctypes.POINTER(Params)] + [ctypes.POINTER(i32)] * 5
             L.sc_plan_query.restype = i32
             L.sc_status_string.argtypes = [i32]
@@ -387,3 +394,70 @@ def score_centered_loss(logits, rec_ids, rec_logprobs, rec_count, sampled_id, ro
     """Differentiable score-centered loss (see :class:`ScoreCenteredLoss`)."""
     return ScoreCenteredLoss.apply(logits, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob,
                                    row_response, adv, p, stream)
+
+
+_lmhead_workspaces = {}
+
+
+def sc_lmhead_forward_backward(hidden: torch.Tensor, w: torch.Tensor, rec_ids, rec_logprobs, rec_count,
+                               sampled_id, rollout_logprob, row_response, adv, p: Params, block_rows: int = 1024,
+                               dhidden: torch.Tensor | None = None, dw: torch.Tensor | None = None,
+                               logp_out: torch.Tensor | None = None, diag_out: torch.Tensor | None = None,
+                               status: torch.Tensor | None = None, stream=None,
+                               workspace_buf: torch.Tensor | None = None):
+    """The LM head followed by score centering: z = H W^T in row blocks, the
+    fused kernel on each block, dH = g W and dW = g^T H.
+
+    hidden bf16 [T, d], w bf16 [V, d] (contiguous, d % 8 == 0); the other
+    inputs as :func:`sc_center_forward_backward`.  Returns (dhidden bf16
+    [T, d], dw float32 [V, d], logp_out, diag_out).  workspace_buf: a uint8
+    tensor of sc_lmhead_workspace_bytes(block_rows, V) zero-initialised
+    bytes; by default the binding's own for this device, stream and size.
+    """
+    dev = hidden.device
+    if dev.type != "cuda":
+        raise ValueError("hidden must be on a CUDA device")
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(w, "w", torch.bfloat16, dev, 2)
+    if not hidden.is_contiguous() or not w.is_contiguous():
+        raise ValueError("hidden and w must be contiguous")
+    T, d = hidden.shape
+    V = w.shape[0]
+    if w.shape[1] != d:
+        raise ValueError("w must be [V, d] with the hidden size d")
+    K_max = int(p.K_max)
+    for name, t, dt, nd in [("rec_ids", rec_ids, torch.int32, 2), ("rec_logprobs", rec_logprobs, torch.float32, 2),
+                            ("rec_count", rec_count, torch.int32, 1), ("sampled_id", sampled_id, torch.int32, 1),
+                            ("rollout_logprob", rollout_logprob, torch.float32, 1),
+                            ("row_response", row_response, torch.int32, 1), ("adv", adv, torch.float32, 1)]:
+        _need(t, name, dt, dev, nd)
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    dhidden = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if dhidden is None else dhidden
+    dw = torch.empty((V, d), dtype=torch.float32, device=dev) if dw is None else dw
+    logp_out = torch.empty(T, dtype=torch.float32, device=dev) if logp_out is None else logp_out
+    _need(dhidden, "dhidden", torch.bfloat16, dev, 2)
+    _need(dw, "dw", torch.float32, dev, 2)
+    _need(logp_out, "logp_out", torch.float32, dev, 1)
+    if diag_out is not None:
+        _need(diag_out, "diag_out", torch.int32, dev, 2)
+    if T == 0:
+        return dhidden, dw, logp_out, diag_out
+    L = lib()
+    need = int(L.sc_lmhead_workspace_bytes(min(int(block_rows), T), V))
+    if workspace_buf is None:
+        s_obj = torch.cuda.current_stream(dev) if stream is None else stream
+        key = (dev.index, int(s_obj.cuda_stream), need)
+        with _lock:
+            workspace_buf = _lmhead_workspaces.get(key)
+            if workspace_buf is None:
+                workspace_buf = torch.zeros(need, dtype=torch.uint8, device=dev)
+                _lmhead_workspaces[key] = workspace_buf
+    if workspace_buf.device != dev or workspace_buf.numel() * workspace_buf.element_size() < need:
+        raise ValueError(f"workspace_buf must hold {need} bytes on {dev}")
+    _check(L.sc_lmhead_forward_backward(
+        _ptr(hidden), _ptr(w), T, d, V, _ptr(rec_ids) if K_max else None, _ptr(rec_logprobs) if K_max else None,
+        _ptr(rec_count), _ptr(sampled_id), _ptr(rollout_logprob), _ptr(row_response), _ptr(adv), int(adv.numel()),
+        ctypes.byref(p), int(block_rows), _ptr(dhidden), _ptr(dw), _ptr(logp_out), _ptr(diag_out), _ptr(status),
+        _ptr(workspace_buf), int(workspace_buf.numel() * workspace_buf.element_size()), _stream(stream)))
+    return dhidden, dw, logp_out, diag_out

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libsc_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
-SOURCES = ["sc_center.cu", "sc_topk.cu", "sc_advantages.cu", "sc_common.cu"]
+SOURCES = ["sc_center.cu", "sc_topk.cu", "sc_lmhead.cu", "sc_advantages.cu", "sc_common.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -74,7 +74,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(log)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
-            "-Xlinker", f"-rpath={os.path.join(cuda, 'lib64')}"]
+            "-lcublasLt", "-Xlinker", f"-rpath={os.path.join(cuda, 'lib64')}"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -242,3 +242,50 @@ def to_numpy(batch: dict) -> dict:
         else:
             out[k] = v
     return out
+
+
+def lmhead_batch(T: int, d: int, V: int, K: int = 128, seed: int = 7, dyadic: bool = True, sigma_s: float = 0.05,
+                 n_resp: int = 4, pad_frac: float = 0.2) -> dict:
+    """Inputs of the LM head followed by score centering (CPU tensors).
+
+    hidden bf16 [T, d] and w bf16 [V, d].  With `dyadic`, hidden lies on a
+    1/8 grid in [-1, 1] and w on a 1/16 grid in [-1, 1], so every product and
+    every sum of d <= 2048 of them is exact in FP32: the trainer's logits
+    H W^T need no rounding before their single rounding to bf16.  Otherwise
+    both are N(0, 1) scaled so the logits have a standard deviation near 3.
+    The sampler's view: FP32 logits H W^T (computed here in FP32 on the CPU,
+    as a sampler would) plus N(0, sigma_s^2) noise; the recorded ids are its
+    top-K with FP32 log-probabilities, the sampled token is drawn from it.
+    The last rows of every response are padding (about pad_frac of them).
+    """
+    g = torch.Generator().manual_seed(seed)
+    if dyadic:
+        H = torch.randint(-8, 9, (T, d), generator=g).float() / 8.0
+        W = torch.randint(-16, 17, (V, d), generator=g).float() / 16.0
+        W = W * (3.0 / (math.sqrt(d) * 0.6))
+        W = torch.round(W * 16.0) / 16.0  # back on the 1/16 grid
+        W = W.clamp(-1.0, 1.0)
+    else:
+        H = torch.randn(T, d, generator=g)
+        W = torch.randn(V, d, generator=g) * (3.0 / math.sqrt(d))
+    hidden = H.to(torch.bfloat16)
+    w = W.to(torch.bfloat16)
+    z = hidden.float() @ w.float().T
+    zs = z + torch.randn(z.shape, generator=g) * sigma_s
+    mu = torch.softmax(zs, dim=1)
+    Kp = min(K, V)
+    top = torch.topk(mu, Kp, dim=1)
+    rec_ids = top.indices.to(torch.int32)
+    rec_lp = torch.log(top.values).to(torch.float32)
+    gum = -torch.log(-torch.log(torch.rand(zs.shape, generator=g).clamp_min(1e-20)))
+    sampled = torch.argmax(torch.log(mu.clamp_min(1e-38)) + gum, dim=1).to(torch.int32)
+    rl = torch.log(mu.gather(1, sampled.long()[:, None])[:, 0]).to(torch.float32)
+    per = max(1, T // n_resp)
+    resp = torch.arange(T, dtype=torch.int32) // per
+    resp = torch.clamp(resp, max=n_resp - 1)
+    pos = torch.arange(T) - resp.long() * per
+    resp = torch.where(pos >= int(round(per * (1 - pad_frac))), torch.full_like(resp, -1), resp)
+    rewards = (torch.rand(n_resp, generator=g) < 0.5).float()
+    return dict(hidden=hidden, w=w, rec_ids=rec_ids, rec_logprobs=rec_lp, rec_count=None, sampled=sampled,
+                rollout_logprob=rl, row_response=resp, rewards=rewards, n_groups=1, group_size=n_resp, K=Kp, V=V,
+                inv_temperature=1.0)

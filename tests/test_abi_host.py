@@ -26,7 +26,7 @@ def L():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*)\s+(sc_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(sc_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_documented_entry_points():
@@ -204,3 +204,42 @@ def test_topk_capture_rejects_bad_arguments_on_the_host(L, kw, status):
 
 def test_topk_capture_empty_batch_is_a_no_op(L):
     assert L.sc_topk_capture(None, 0, 64, 64, 1.0, 8, 1.0, None, None, None, None) == sc.SC_OK
+
+
+def call_lmhead(L, T=4, d=64, V=100, hidden=FAKE, w=FAKE * 2, ids=FAKE * 3, lps=FAKE * 4, samp=FAKE * 5,
+                resp=FAKE * 6, adv=FAKE * 7, dh=FAKE * 8, dw=FAKE * 9, logp=FAKE * 10, ws=FAKE * 256,
+                ws_bytes=None, block_rows=2, **pk):
+    p = sc.params(**{"K_max": 8, **pk})
+    if ws_bytes is None:
+        ws_bytes = L.sc_lmhead_workspace_bytes(min(block_rows, T) if block_rows > 0 else 1, V)
+    return L.sc_lmhead_forward_backward(hidden, w, T, d, V, ids, lps, None, samp, None, resp, adv, 2,
+                                        ctypes.byref(p), block_rows, dh, dw, logp, None, None, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=60), sc.SC_ERR_SHAPE),
+    (dict(d=0), sc.SC_ERR_SHAPE),
+    (dict(V=0), sc.SC_ERR_SHAPE),
+    (dict(T=-1), sc.SC_ERR_SHAPE),
+    (dict(block_rows=0), sc.SC_ERR_SHAPE),
+    (dict(K_max=2000), sc.SC_ERR_SHAPE),
+    (dict(inv_temperature=0.0), sc.SC_ERR_ARG),
+    (dict(hidden=None), sc.SC_ERR_NULL),
+    (dict(dw=None), sc.SC_ERR_NULL),
+    (dict(ws=None), sc.SC_ERR_NULL),
+    (dict(logp=None), sc.SC_ERR_NULL),
+    (dict(ids=None), sc.SC_ERR_NULL),
+    (dict(hidden=FAKE + 8), sc.SC_ERR_ALIGN),
+    (dict(ws=FAKE * 256 + 16), sc.SC_ERR_ALIGN),
+    (dict(ws_bytes=1024), sc.SC_ERR_SHAPE),
+])
+def test_lmhead_rejects_bad_arguments_on_the_host(L, kw, status):
+    assert call_lmhead(L, **kw) == status, err(L)
+
+
+def test_lmhead_workspace_size(L):
+    assert L.sc_lmhead_workspace_bytes(0, 100) == 0
+    small = L.sc_lmhead_workspace_bytes(1, 100)
+    big = L.sc_lmhead_workspace_bytes(1024, 151936)
+    # the block of logits (rows padded to a multiple of 8 entries) on top of a fixed part
+    assert big - small == 1024 * 151936 * 2 - 256 and big % 256 == 0
