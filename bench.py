@@ -209,6 +209,59 @@ def topk_secondary(batch, dev, peak, peak_kind, reps=10):
     return out
 
 
+def bf16_peak():
+    """Measured dense bf16 TFLOP/s (the sustained figure: the call below runs
+    for tens of milliseconds back to back)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (sustained)"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback (sustained)"
+
+
+def lmhead_secondary(batch, adv, dev, d=4096, block_rows=1024, reps=5):
+    """The LM head followed by score centering on the batch's 4096 rows:
+    random bf16 hidden states [T, d] and head [V, d] (logits of standard
+    deviation near 3), the batch's recorded ids, sampled tokens and responses.
+    Three GEMMs of 2 T d V flops each per call (logits, dH, dW)."""
+    import precision_off_policy_gb300 as sc
+
+    T, V, K = batch["logits"].shape[0], batch["V"], batch["K"]
+    g = torch.Generator(device=dev).manual_seed(4242)
+    hidden = torch.randn((T, d), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((V, d), generator=g, device=dev) * (3.0 / d ** 0.5)).to(torch.bfloat16)
+    dh = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((V, d), dtype=torch.float32, device=dev)
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    p = sc.params(K_max=K, grad_scale=1.0 / max(1, batch["n_valid"]))
+    st = torch.cuda.Stream(device=dev)
+
+    def call():
+        sc.sc_lmhead_forward_backward(hidden, w, batch["rec_ids"], batch["rec_logprobs"], batch["rec_count"],
+                                      batch["sampled"], batch["rollout_logprob"], batch["row_response"], adv, p,
+                                      block_rows=block_rows, dhidden=dh, dw=dw, logp_out=logp, stream=st)
+
+    with torch.cuda.stream(st):
+        for _ in range(2):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            call()
+        e1.record(st)
+    st.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = 3 * 2.0 * T * d * V
+    peak, kind = bf16_peak()
+    achieved = flops / (ms / 1e3) / 1e12
+    del hidden, w, dh, dw
+    return {"kernel": "cuBLASLt GEMMs + center_kernel", "call": "sc_lmhead_forward_backward",
+            "workload": f"{WORKLOAD} rows: T={T}, d={d}, V={V}, K={K}, blocks of {block_rows} rows",
+            "ms_per_call": ms, "tokens_per_s": batch["n_valid"] / (ms / 1e3),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": kind, "flops_per_call": flops}}
+
+
 def cpu_baseline(batch, p, adv, min_seconds=10.0, max_passes=50):
     """The FP64 oracle over the whole batch on all host cores, repeated until
     about `min_seconds` of wall time have been spent (a stable figure)."""
@@ -472,6 +525,8 @@ def main():
     del sets
     torch.cuda.empty_cache()
     line["secondary"] = topk_secondary(batch, dev, peak, peak_kind)
+    line["secondary"].append(lmhead_secondary(batch, adv, dev))
+    torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         adv_or = oracle.group_advantages(batch["rewards"].cpu().numpy(), batch["n_groups"], batch["group_size"],
