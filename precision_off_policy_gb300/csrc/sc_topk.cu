@@ -9,8 +9,16 @@
 // renormalised.  Entries are ordered by z, larger first, equal values by
 // lower id.  Each row gets count = min(K, V, nucleus size) ids and log mu.
 //
-// GB300 design: one CTA per row (persistent grid), radix selection on an
-// order-preserving 32-bit key of z in digits of 12, 12 and 8 bits.
+// GB300 design: a persistent grid of 512-thread CTAs, each split into two
+// 256-thread groups that take rows independently (named barriers), so that one
+// group's per-row sorting and reductions overlap the other's streaming.
+// One-pass path (almost every row): a 1/16 sample sets the exponent offset and
+// a candidate threshold; one pass over the row sums the softmax normaliser
+// (compensated, fixed order) and collects the entries above the threshold;
+// the candidates are sorted and give the top K and the nucleus (see fast_row).
+// Exact path (rows the one-pass path cannot finish, taken by the whole CTA
+// between rounds): radix selection on an order-preserving 32-bit key of z in
+// digits of 12, 12 and 8 bits.
 //   pass 1  row maximum and the 4096-bin histogram of the top digit;
 //   pass 2  the softmax normaliser in 2^-40 fixed point (integer sums, so
 //           the result does not depend on the order of the additions), the
@@ -99,11 +107,6 @@ struct Shared {
     unsigned long long cand[kCap];      // (key << 32) | ~id, sorted descending
     unsigned long long top[kMaxTopK];   // the selected entries, sorted
     unsigned long long scan[kNT / 32];  // block scan scratch
-    float fred[kNT / 32];               // block maximum; block sums (high parts)
-    float flo[kNT / 32];                // block sums (low parts)
-    double dS, dlse;                    // the row's normaliser and log-sum-exp
-    int cross;                          // first candidate at which the nucleus mass is reached
-    double pnuc;                        // the nucleus mass there
     unsigned long long s_fixed;         // the row's normaliser, fixed point
     uint32_t maxkey;
     int ncand;
@@ -596,9 +599,44 @@ __device__ void exact_row(Shared& sh, const TopkArgs& a, long long t) {
     }
 }
 
-constexpr int kNW = kNT / 32;
-constexpr int kSampRun = 32;    // vectors per sampled run (one warp load)
-constexpr int kSampEvery = 16;  // one run in kSampEvery is sampled
+constexpr int kGroups = 2;            // independent thread groups of a CTA on the one-pass path (<= 4)
+constexpr int kGT = kNT / kGroups;    // threads per group
+constexpr int kGW = kGT / 32;         // warps per group
+constexpr int kSampRun = 32;          // vectors per sampled run (one warp load)
+constexpr int kSampEvery = 16;        // one run in kSampEvery is sampled
+constexpr int kRound = 32;            // rows per group between the CTA's exact-path rounds
+
+// A thread group's view: its threads, its named barrier, its shared state.
+struct GroupShared {
+    uint32_t keys[kGT];                 // the sample maxima, sorted
+    unsigned long long cand[kCap];      // (key << 32) | ~id
+    float fred[kGW], flo[kGW];          // group maximum / sums of pairs
+    double dS, dlse;
+    double pnuc;
+    int ncand, cross;
+};
+struct KernelShared {
+    union {
+        Shared exact;                   // the exact path: the whole CTA, between rounds
+        GroupShared grp[kGroups];       // the one-pass path: one per group
+    } u;
+    int ndefer;
+    long long defer[kGroups * kRound];  // rows of this round left to the exact path
+};
+
+struct Group {
+    int id, tid, lane, warp;
+    // named barriers 1.. kGroups (0 is the CTA's), as immediates so that only
+    // those are reserved
+    __device__ void sync() const {
+        switch (id) {
+            case 0: asm volatile("bar.sync 1, %0;" ::"n"(kGT) : "memory"); break;
+            case 1: asm volatile("bar.sync 2, %0;" ::"n"(kGT) : "memory"); break;
+            case 2: asm volatile("bar.sync 3, %0;" ::"n"(kGT) : "memory"); break;
+            default: asm volatile("bar.sync 4, %0;" ::"n"(kGT) : "memory"); break;
+        }
+    }
+};
 
 // A sum kept as an unevaluated FP32 pair hi + lo, added without error
 // (two-sum): the same bits in every lane whatever the order of the operands.
@@ -613,63 +651,91 @@ __device__ __forceinline__ Pair pair_add(Pair a, Pair b) {
 __device__ __forceinline__ Pair pair_shfl_xor(Pair v, int o) {
     return Pair{__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
 }
-// Sum of the threads' pairs over the block in a fixed order.
-__device__ Pair block_sum_pair(Shared& sh, Pair v) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Sum of the group's pairs in a fixed order.
+__device__ Pair group_sum_pair(GroupShared& gs, const Group& G, Pair v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = pair_add(v, pair_shfl_xor(v, o));
-    if (lane == 0) {
-        sh.fred[warp] = v.hi;
-        sh.flo[warp] = v.lo;
+    if (G.lane == 0) {
+        gs.fred[G.warp] = v.hi;
+        gs.flo[G.warp] = v.lo;
     }
-    __syncthreads();
+    G.sync();
     Pair r{0.0f, 0.0f};
-    for (int w = 0; w < kNW; ++w) r = pair_add(r, Pair{sh.fred[w], sh.flo[w]});
-    __syncthreads();
+    for (int w = 0; w < kGW; ++w) r = pair_add(r, Pair{gs.fred[w], gs.flo[w]});
+    G.sync();
     return r;
 }
-__device__ float block_max_f(Shared& sh, float v) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ float group_max_f(GroupShared& gs, const Group& G, float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-    if (lane == 0) sh.fred[warp] = v;
-    __syncthreads();
+    if (G.lane == 0) gs.fred[G.warp] = v;
+    G.sync();
     float r = -INFINITY;
-    for (int w = 0; w < kNW; ++w) r = fmaxf(r, sh.fred[w]);
-    __syncthreads();
+    for (int w = 0; w < kGW; ++w) r = fmaxf(r, gs.fred[w]);
+    G.sync();
     return r;
 }
-// Bitonic sort of kNT keys, larger first (one per thread).
-__device__ void sort_keys_desc(uint32_t* k) {
-    const int i = threadIdx.x;
-    for (int size = 2; size <= kNT; size <<= 1)
+// Bitonic sort of the group's kGT keys, larger first (one per thread): the
+// steps within a warp by shuffles, the others through shared memory.
+__device__ void group_sort_keys_desc(GroupShared& gs, const Group& G, uint32_t key) {
+    const int i = G.tid;
+    uint32_t x = key;
+    for (int size = 2; size <= kGT; size <<= 1)
         for (int j = size >> 1; j > 0; j >>= 1) {
-            const int l = i ^ j;
-            if (l > i) {
-                const uint32_t x = k[i], y = k[l];
-                if (((i & size) == 0) ? (x < y) : (x > y)) {
-                    k[i] = y;
-                    k[l] = x;
+            const bool desc = (i & size) == 0;  // this pair's block sorts larger first
+            uint32_t y;
+            if (j < 32) {
+                y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+            } else {
+                gs.keys[i] = x;
+                G.sync();
+                y = gs.keys[i ^ j];
+                G.sync();
+            }
+            const bool lower = (i & j) == 0;  // i is the first of its pair
+            const uint32_t hi = max(x, y), lo = min(x, y);
+            x = (lower == desc) ? hi : lo;
+        }
+    gs.keys[i] = x;
+    G.sync();
+}
+// Bitonic sort of cand[0, n), larger first (n <= kCap), by the group.
+__device__ void group_sort_desc(GroupShared& gs, const Group& G, int n) {
+    int m = 1;
+    while (m < n) m <<= 1;
+    for (int i = n + G.tid; i < m; i += kGT) gs.cand[i] = 0ull;
+    G.sync();
+    for (int k = 2; k <= m; k <<= 1)
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = G.tid; i < m; i += kGT) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const unsigned long long x = gs.cand[i], y = gs.cand[l];
+                    if (((i & k) == 0) ? (x < y) : (x > y)) {
+                        gs.cand[i] = y;
+                        gs.cand[l] = x;
+                    }
                 }
             }
-            __syncthreads();
+            G.sync();
         }
 }
 
-// The one-pass path for one row.  A sample (every kSampEvery-th run of
-// vectors) gives each thread a maximum; the largest of those maxima is the
-// exponent offset, and the `rank`-th largest the candidate threshold, placed
-// so that about 3 K entries of the row reach it.  One pass over the row then
-// sums 2^(z kt - offset kt) per thread (compensated, in a fixed order; a
-// thread that meets an entry above the offset moves its own offset up) and
-// collects every entry at or above the threshold.  The candidates are sorted;
-// the top K and, with top_p < 1, the nucleus come from them.  Returns false --
-// outputs untouched, the same decision in every thread -- when the row needs
-// the exact path: too few or too many candidates, a nucleus that reaches below
-// them, entries that are not finite, or K above kCap / 4.
-__device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
+// The one-pass path for one row, run by one thread group.  A sample (every
+// kSampEvery-th run of vectors) gives each thread a maximum; the largest of
+// those maxima is the exponent offset, and the `rank`-th largest the candidate
+// threshold, placed so that about 3 K entries of the row reach it.  One pass
+// over the row then sums 2^((z - m) kt) per thread (compensated, in a fixed
+// order; a thread that meets an entry above its offset m moves m up) and
+// collects every entry at or above the threshold.  The candidates are
+// sorted; the top K and, with top_p < 1, the nucleus come from them.  Returns
+// false -- outputs untouched, the same decision in every thread of the group
+// -- when the row needs the exact path: too few or too many candidates, a
+// nucleus that reaches below them, entries that are not finite, or K above
+// kCap / 4.
+__device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, long long t) {
     const float* row = a.logits + t * a.stride;
-    const int V = a.V, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int V = a.V, tid = G.tid, lane = G.lane, warp = G.warp;
     const int Kp = min(a.K, V);
     if (4 * Kp > kCap) return false;
     const float kt = a.inv_t * kLog2e;
@@ -682,23 +748,21 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
     if (V > kCap) {
         const int nruns = nv4 / kSampRun;
         float smax = -INFINITY;
-        for (int r = warp * kSampEvery; r < nruns; r += kNW * kSampEvery) {
+        for (int r = warp * kSampEvery; r < nruns; r += kGW * kSampEvery) {
             const float4 v = __ldg(r4 + r * kSampRun + lane);
             smax = fmaxf(smax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
         }
-        sh.hist[tid] = key_of(smax);
-        __syncthreads();
-        sort_keys_desc(sh.hist);
-        const int rank = max(8, (3 * Kp + kSampEvery - 1) / kSampEvery);
-        tau = float_of(sh.hist[rank - 1]);
-        o = float_of(sh.hist[0]);
-        __syncthreads();
+        group_sort_keys_desc(gs, G, key_of(smax));
+        const int rank = min(kGT, max(8, (3 * Kp + kSampEvery - 1) / kSampEvery));
+        tau = float_of(gs.keys[rank - 1]);
+        o = float_of(gs.keys[0]);
+        G.sync();
         if (!isfinite(o)) return false;
     }
 
     // ---- one pass: the sums and the candidates
-    if (tid == 0) sh.ncand = 0;
-    __syncthreads();
+    if (tid == 0) gs.ncand = 0;
+    G.sync();
     // (z - m) is formed first and then scaled, so the terms nearest the
     // offset -- the ones that dominate the sum -- carry no rounding of the offset
     float m = o;                      // this thread's offset
@@ -720,8 +784,8 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
     };
     auto collect1 = [&](float z, int id) {
         if (z >= tau) {
-            const int pos = atomicAdd(&sh.ncand, 1);
-            if (pos < kCap) sh.cand[pos] = pack_entry(key_of(z), id);
+            const int pos = atomicAdd(&gs.ncand, 1);
+            if (pos < kCap) gs.cand[pos] = pack_entry(key_of(z), id);
         }
     };
     auto take4 = [&](const float4& v, int id0) {
@@ -743,15 +807,15 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
     };
     {
         int i = tid;
-        for (; i + (kUnroll - 1) * kNT < nv4; i += kUnroll * kNT) {
+        for (; i + (kUnroll - 1) * kGT < nv4; i += kUnroll * kGT) {
             float4 v[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(r4 + i + u * kNT);
+            for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(r4 + i + u * kGT);
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) take4(v[u], 4 * (i + u * kNT));
+            for (int u = 0; u < kUnroll; ++u) take4(v[u], 4 * (i + u * kGT));
         }
-        for (; i < nv4; i += kNT) take4(__ldg(r4 + i), 4 * i);
-        for (int j = (nv4 << 2) + tid; j < V; j += kNT) {
+        for (; i < nv4; i += kGT) take4(__ldg(r4 + i), 4 * i);
+        for (int j = (nv4 << 2) + tid; j < V; j += kGT) {
             const float z = __ldg(row + j);
             if (z > m) raise(z);
             if (m > -INFINITY) add(ex2((z - m) * kt));
@@ -760,21 +824,21 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
     }
     // ---- the normaliser: every thread's sum moved to the row maximum M
     // (threads already there untouched), summed without error in a fixed order
-    const float M = block_max_f(sh, m);
+    const float M = group_max_f(gs, G, m);
     float part = s - c;
     if (!(m > -INFINITY)) part = 0.0f;
     else if (m != M) part *= ex2((m - M) * kt);
-    const Pair tot = block_sum_pair(sh, Pair{part, 0.0f});
+    const Pair tot = group_sum_pair(gs, G, Pair{part, 0.0f});
     if (tid == 0) {
         const double S = (double)tot.hi + (double)tot.lo;
-        sh.dS = S;
-        sh.dlse = (double)M * a.inv_t + log(S);
+        gs.dS = S;
+        gs.dlse = (double)M * a.inv_t + log(S);
     }
-    __syncthreads();
-    const double S = sh.dS, lse = sh.dlse;
-    const int nc = sh.ncand;
+    G.sync();
+    const double S = gs.dS, lse = gs.dlse;
+    const int nc = gs.ncand;
     if (!isfinite(M) || !(S > 0.0) || !isfinite(S) || !isfinite(lse) || nc < Kp || nc > kCap) return false;
-    sort_desc(sh, nc);
+    group_sort_desc(gs, G, nc);
 
     // ---- the nucleus: one warp walks the sorted candidates with error-free
     // FP32 running sums
@@ -786,7 +850,7 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
             const float t_hi = (float)thr, t_lo = (float)(thr - (double)t_hi);
             const int per = (nc + 31) / 32;
             const int i0 = lane * per, i1 = min(nc, i0 + per);
-            auto mass = [&](int i) { return ex2((float_of(static_cast<uint32_t>(sh.cand[i] >> 32)) - M) * kt); };
+            auto mass = [&](int i) { return ex2((float_of(static_cast<uint32_t>(gs.cand[i] >> 32)) - M) * kt); };
             Pair loc{0.0f, 0.0f};
             for (int i = i0; i < i1; ++i) loc = pair_add(loc, Pair{mass(i), 0.0f});
             // exclusive scan of the lanes' pairs, in lane order
@@ -812,15 +876,15 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
 #pragma unroll
             for (int o2 = 16; o2 > 0; o2 >>= 1) cross = min(cross, __shfl_xor_sync(0xFFFFFFFFu, cross, o2));
             if (lane == 0) {
-                sh.cross = cross;
-                if (cross > nc) sh.pnuc = (all.hi - t_hi) + (all.lo - t_lo) >= 0.0f ? (double)all.hi + (double)all.lo : -1.0;
+                gs.cross = cross;
+                if (cross > nc) gs.pnuc = (all.hi - t_hi) + (all.lo - t_lo) >= 0.0f ? (double)all.hi + (double)all.lo : -1.0;
             }
-            if (mine == cross && cross <= nc) sh.pnuc = (double)run.hi + (double)run.lo;
+            if (mine == cross && cross <= nc) gs.pnuc = (double)run.hi + (double)run.lo;
         }
-        __syncthreads();
-        const int cross = sh.cross;
-        const double P = sh.pnuc;
-        __syncthreads();
+        G.sync();
+        const int cross = gs.cross;
+        const double P = gs.pnuc;
+        G.sync();
         if (!(P > 0.0)) return false;  // the nucleus reaches below the candidates
         count = min(Kp, cross <= nc ? cross : nc);
         log_nuc = log(P / S);
@@ -829,10 +893,10 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
     // ---- outputs
     int32_t* ids = a.ids + t * a.K;
     float* lps = a.lps + t * a.K;
-    for (int i = tid; i < a.K; i += kNT) {
+    for (int i = tid; i < a.K; i += kGT) {
         if (i < count) {
-            const uint32_t key = static_cast<uint32_t>(sh.cand[i] >> 32);
-            ids[i] = static_cast<int>(~static_cast<uint32_t>(sh.cand[i]));
+            const uint32_t key = static_cast<uint32_t>(gs.cand[i] >> 32);
+            ids[i] = static_cast<int>(~static_cast<uint32_t>(gs.cand[i]));
             lps[i] = static_cast<float>(static_cast<double>(float_of(key)) * a.inv_t - lse - log_nuc);
         } else {
             ids[i] = -1;
@@ -840,15 +904,39 @@ __device__ bool fast_row(Shared& sh, const TopkArgs& a, long long t) {
         }
     }
     if (tid == 0 && a.counts) a.counts[t] = count;
-    __syncthreads();
+    G.sync();
     return true;
 }
 
+// Rows are dealt to the thread groups round robin (group b * kGroups + g of
+// the grid takes rows b * kGroups + g + k * groups).  Each group takes its
+// rows on the one-pass path; a row it cannot finish waits for the end of the
+// round, when the whole CTA takes the deferred rows on the exact path.
 __global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_constant__ TopkArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
-    for (long long t = blockIdx.x; t < a.T; t += gridDim.x)
-        if (!fast_row(sh, a, t)) exact_row(sh, a, t);
+    KernelShared& ks = *reinterpret_cast<KernelShared*>(smem_raw);
+    const Group G{static_cast<int>(threadIdx.x) / kGT, static_cast<int>(threadIdx.x) % kGT,
+                  static_cast<int>(threadIdx.x) & 31, (static_cast<int>(threadIdx.x) % kGT) >> 5};
+    const long long ngroups = static_cast<long long>(gridDim.x) * kGroups;
+    const long long first = static_cast<long long>(blockIdx.x) * kGroups;  // this CTA's first group
+    // rounds: as many as the CTA's first group has rows (the others have at most as many)
+    const long long rows0 = first < a.T ? (a.T - first + ngroups - 1) / ngroups : 0;
+    if (threadIdx.x == 0) ks.ndefer = 0;
+    __syncthreads();
+    for (long long k0 = 0; k0 < rows0; k0 += kRound) {
+        const long long k1 = min(rows0, k0 + kRound);
+        for (long long k = k0; k < k1; ++k) {
+            const long long t = first + G.id + k * ngroups;
+            if (t >= a.T) break;
+            if (!fast_row(ks.u.grp[G.id], G, a, t) && G.tid == 0) ks.defer[atomicAdd(&ks.ndefer, 1)] = t;
+        }
+        __syncthreads();
+        const int nd = ks.ndefer;
+        for (int q = 0; q < nd; ++q) exact_row(ks.u.exact, a, ks.defer[q]);
+        __syncthreads();
+        if (threadIdx.x == 0) ks.ndefer = 0;
+        __syncthreads();
+    }
 }
 
 }  // namespace
@@ -883,10 +971,10 @@ extern "C" int sc_topk_capture(const float* logits, long long T, int V, long lon
         if (it == grid_for.end()) {
             cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(topk_capture_kernel),
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(sizeof(Shared)));
+                                                 static_cast<int>(sizeof(KernelShared)));
             if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(topk smem)");
             int per_sm = 0, sms = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_capture_kernel, kNT, sizeof(Shared));
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_capture_kernel, kNT, sizeof(KernelShared));
             if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
             e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
@@ -908,7 +996,7 @@ extern "C" int sc_topk_capture(const float* logits, long long T, int V, long lon
     ka.lps = logprobs_out;
     ka.counts = count_out;
     const long long g = T < grid ? T : grid;
-    topk_capture_kernel<<<static_cast<unsigned>(g), kNT, sizeof(Shared), reinterpret_cast<cudaStream_t>(stream)>>>(ka);
+    topk_capture_kernel<<<static_cast<unsigned>(g), kNT, sizeof(KernelShared), reinterpret_cast<cudaStream_t>(stream)>>>(ka);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "topk_capture_kernel launch");
     return ok();
