@@ -33,9 +33,6 @@ __device__ __forceinline__ void cluster_sync_all() {
         "barrier.cluster.arrive.release.aligned;\n\t"
         "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
     uint32_t r;
@@ -45,13 +42,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
     asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-                 "r"(c), "r"(d)
-                 : "memory");
-}
-
 // ---- mbarriers --------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -245,10 +235,6 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-}  // namespace sc
-
-namespace sc {
-
 // Asynchronous stores into a peer CTA's shared memory that complete as
 // transaction bytes on the peer's mbarrier (DSMEM, sm_90+).
 __device__ __forceinline__ void st_async_v2(uint32_t cluster_addr, uint32_t a, uint32_t b,
@@ -271,24 +257,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Named barrier 1 over the first `n` threads of the CTA (n a multiple of 32).
-__device__ __forceinline__ void named_bar(int n) {
-    asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory");
-}
-// Same barrier, returning the OR of `p` over the participating threads.
-__device__ __forceinline__ bool named_bar_or(int n, bool p) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, %2, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(p)), "r"(n)
-        : "memory");
-    return r != 0;
-}
-
 // Error-free sum of two floats (Knuth's two-sum): s + e == a + b exactly.
 __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
@@ -296,51 +264,10 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-}  // namespace sc
-
-namespace sc {
-
-// shared -> global bulk copy (TMA engine), one bulk group per call.  src and
-// dst 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst), "r"(src),
-        "r"(bytes), "l"(policy)
-        : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Waits until at most N committed bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-// Waits until every committed bulk group has completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
-
-}  // namespace sc
-
-namespace sc {
-
 __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-// 16-byte global load through the non-coherent path, no L1 allocation, with an L2 eviction hint.
-__device__ __forceinline__ uint4 ldg_v4_hint(const void* ptr, uint64_t policy) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr), "l"(policy));
-    return v;
 }
 
 }  // namespace sc
