@@ -246,6 +246,43 @@ def test_run_time_row_hand_out_is_deterministic_and_leaves_the_workspace_zero():
     assert int(ws.abs().sum().item()) == 0
 
 
+def test_concurrent_streams_with_their_own_workspaces():
+    # Two launches at once on two streams (the binding gives each stream its
+    # own workspace, so their run-time row counters do not meet): each result
+    # equals the same call run alone.
+    dev = torch.device("cuda")
+    cfg_a = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=512, len_lo=64, len_hi=512)
+    cfg_b = synth.config("C4", n_prompts=1, n_per_prompt=2, L_pad=256)
+    outs = {}
+    for name, cfg in (("a", cfg_a), ("b", cfg_b)):
+        b = synth.make_batch(cfg)
+        adv = torch.as_tensor(oracle_adv(b), device=dev)
+        x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in b.items()}
+        outs[name] = (x, adv, sc_params(b))
+    alone = {}
+    for name, (x, adv, p) in outs.items():
+        g, lp, _ = sc.sc_center_forward_backward(x["logits"], x["rec_ids"], x["rec_logprobs"], x["rec_count"],
+                                                 x["sampled"], x["rollout_logprob"], x["row_response"], adv, p)
+        torch.cuda.synchronize()
+        alone[name] = (g.clone(), lp.clone())
+    streams = {"a": torch.cuda.Stream(), "b": torch.cuda.Stream()}
+    res = {}
+    for _ in range(3):
+        for name, (x, adv, p) in outs.items():
+            s = streams[name]
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                res[name] = sc.sc_center_forward_backward(
+                    x["logits"], x["rec_ids"], x["rec_logprobs"], x["rec_count"], x["sampled"], x["rollout_logprob"],
+                    x["row_response"], adv, p, stream=s)
+        torch.cuda.synchronize()
+        for name in outs:
+            assert torch.equal(res[name][0].view(torch.int16), alone[name][0].view(torch.int16)), name
+            assert torch.equal(res[name][1], alone[name][1]), name
+    for s in streams.values():
+        assert int(sc.workspace(dev, s).abs().sum().item()) == 0
+
+
 # -------------------------------------------------------------------------
 # Edge cases
 
