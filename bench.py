@@ -404,24 +404,34 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    # ---- device-resident timing: events around every fused launch -----------
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # ---- device-resident timing ----------------------------------------------
+    # The fused kernel is launched with programmatic stream serialisation: its
+    # shared-memory set-up overlaps the previous kernel's tail.  An event
+    # recorded between two kernels ends that overlap, so the fused launch is
+    # bracketed by events on every EVENT_EVERY-th step only; its duration is
+    # the mean over those launches (which lose their own overlap: a slightly
+    # long, conservative figure), and `value` is the whole timed region.
+    EVENT_EVERY = 8
+    timed = [i for i in range(args.steps) if i % EVENT_EVERY == 0]
+    ev = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for i in timed}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         barrier()
         start.record(stream)
         for i in range(args.steps):
             sc.sc_group_advantages(batch["rewards"], batch["n_groups"], batch["group_size"], out=adv, stream=stream)
-            ev[i][0].record(stream)
+            if i in ev:
+                ev[i][0].record(stream)
             sc.sc_center_forward_backward(batch["logits"], batch["rec_ids"], batch["rec_logprobs"],
                                           batch["rec_count"], batch["sampled"], batch["rollout_logprob"],
                                           batch["row_response"], adv, p, grad_out=grad, logp_out=logp,
                                           diag_out=diag, stream=stream)
-            ev[i][1].record(stream)
+            if i in ev:
+                ev[i][1].record(stream)
         stop.record(stream)
         barrier()
     elapsed_ms = start.elapsed_time(stop)
-    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    kernel_ms = [a.elapsed_time(b) for a, b in ev.values()]
     t_max = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
     tok = torch.tensor([n_valid * args.steps], dtype=torch.float64, device=dev)
     if world > 1:
@@ -516,7 +526,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_kind,
                      "kernel": "center_kernel", "algorithmic_bytes_per_launch": alg,
-                     "kernel_ms": k_avg_ms},
+                     "kernel_ms": k_avg_ms, "timed_launches": len(kernel_ms)},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps},
         "gpu_launches": 2 * args.steps,

@@ -36,6 +36,9 @@ __device__ __forceinline__ float warp_max_f32(float v) {
 // Grid: one 32-thread block per group.
 __global__ void __launch_bounds__(32) group_adv_kernel(const float* rewards, int group_size,
                                                        int normalize_std, float eps, float* adv) {
+    // the next kernel in the stream (the fused call, which waits for this grid
+    // before it reads the advantages) may start its set-up now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x;
     const long long base = static_cast<long long>(blockIdx.x) * group_size;
     const float* r = rewards + base;

@@ -323,6 +323,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         fence_mbar_init_cluster();
     }
     for (int i = tid; i < kMetaSlots * nwords; i += NC + 96) bitmap[i] = 0u;
+    // Launched with programmatic stream serialisation: everything above touches
+    // only shared memory and may overlap the previous kernel in the stream; no
+    // global input is read before that kernel has completed.
+    grid_dependency_wait();
     cluster_sync_all();  // every CTA's barriers exist before peers signal them
 
     // Any role that gives up raises the flag; the others see it at their next
@@ -1452,13 +1456,17 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     cfg.blockDim = dim3(P.NC + 96, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = P.C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the kernel's shared-memory set-up may overlap the previous kernel's tail
+    // (the kernel waits for it before reading any input)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NC), ka);
     if (e != cudaSuccess) return cuda_fail(e, "center_kernel launch");
     return ok();
