@@ -231,7 +231,7 @@ def test_deterministic_across_calls():
 
 def test_run_time_row_hand_out_is_deterministic_and_leaves_the_workspace_zero():
     # 1024 rows over the persistent grid: the first rows are dealt round robin,
-    # the last quarter handed out at run time, so which cluster takes which
+    # the last rows handed out at run time, so which cluster takes which
     # row changes from call to call; every output must not.
     cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=512, len_lo=64, len_hi=512)
     batch = synth.make_batch(cfg)
