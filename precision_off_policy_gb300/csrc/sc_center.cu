@@ -60,7 +60,7 @@ constexpr int kXBufs = 4;      // exchange buffers (peers may run ahead by a row
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
-constexpr int kChunkVecTarget = 1024;   // 16-byte vectors per bulk copy (16 KiB)
+constexpr int kChunkVecTarget = 2048;   // 16-byte vectors per bulk copy (32 KiB; measured best of 8-128 KiB)
 constexpr int kGrab = 8;                // grab ring: rows CTA 0 may hand out ahead of its peers
 constexpr int kZq = 16;                 // zero queue: zero rows the producer may queue ahead
 constexpr long long kDynamicShare = 8;  // 1 / (share of the rows handed out at run time; measured best of 3..20)
