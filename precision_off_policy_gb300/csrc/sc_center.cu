@@ -60,6 +60,7 @@ constexpr int kXBufs = 4;      // exchange buffers (peers may run ahead by a row
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
+constexpr int kTwoPerSmBytes = 114688;  // dynamic shared memory that still fits two CTAs on an SM
 constexpr int kChunkVecTarget = 2048;   // 16-byte vectors per bulk copy (32 KiB; measured best of 8-128 KiB)
 constexpr int kGrab = 8;                // grab ring: rows CTA 0 may hand out ahead of its peers
 constexpr int kZq = 16;                 // zero queue: zero rows the producer may queue ahead
@@ -1036,11 +1037,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (!timed_out && !ok) {
                     // exact: this thread's maximum, then its sums relative to it (also
                     // the path of -inf logits, whose 0 * -inf made the fast sums NaN)
-                    // (from global memory: the shared-memory slice may already be refilled)
-                    const uint4* grow4 = reinterpret_cast<const uint4*>(a.logits + m.t * a.lstride + lo);
+                    // (from the slice in its stage, which stays there until the write pass)
                     float mx = -INFINITY;
                     for (int j = tid; j < nvb; j += NC) {
-                        const uint4 w = grow4[j];
+                        const uint4 w = lds128(buf_s + 16u * j);
                         const uint32_t m2 = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
                         mx = fmaxf(mx, fmaxf(bf_lo(m2), bf_hi(m2)));
                     }
@@ -1048,7 +1048,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     if (mx > -INFINITY) {
                         const float ox = mx * kscale;
                         for (int j = tid; j < nvb; j += NC) {
-                            const uint4 w = grow4[j];
+                            const uint4 w = lds128(buf_s + 16u * j);
                             const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -1208,10 +1208,10 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     return L;
 }
 
-// Automatic plan: about 80 KiB of logits per CTA (clusters of up to 16
-// CTAs), one data stage that the write pass hands back chunk by chunk to the
+// Automatic plan: the smallest cluster (up to 16 CTAs) whose CTAs fit two to
+// an SM, one data stage that the write pass hands back chunk by chunk to the
 // next row's copies, 256 streaming threads (128 for small slices).  For the
-// 151936-entry vocabulary: 4 CTAs x 37984 entries, two CTAs per SM.
+// 151936-entry vocabulary: 4 CTAs x 37984 entries; for 248320: 6 x 41392.
 int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
     const int NB = req_stages > 0 ? req_stages : 1;
     int C = req_cluster;
@@ -1219,8 +1219,16 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
         return req_threads > 0 ? req_threads : (S >= 8192 ? 256 : 128);
     };
     if (C <= 0) {
-        C = static_cast<int>((2LL * V + 81919) / 81920);
-        C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
+        // the smallest cluster whose CTAs fit two to an SM (the most bytes per
+        // CTA that still leaves another CTA to cover each one's row exchange)
+        C = kMaxCluster;
+        for (int c = 1; c <= kMaxCluster; ++c) {
+            const int Sc = round_up((V + c - 1) / c, 8);
+            if (make_layout(Sc, K_max, threads_for(Sc), NB, c).total <= kTwoPerSmBytes) {
+                C = c;
+                break;
+            }
+        }
         while (C > 1 && static_cast<long long>(C - 1) * round_up((V + C - 1) / C, 8) >= V) --C;
     }
     const int S = round_up((V + C - 1) / C, 8);
