@@ -105,10 +105,12 @@ def build(force: bool = False) -> str:
 
 
 def lib():
+    """The loaded oracle.  ``SC_ORACLE_LIB`` names another compiled copy to load
+    instead (the mutation tests point it at copies with a planted mistake)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
+            path = os.environ.get("SC_ORACLE_LIB") or build()
             L = ctypes.CDLL(path)
             L.sco_bf16_to_double.restype = ctypes.c_double
             L.sco_bf16_to_double.argtypes = [ctypes.c_uint16]

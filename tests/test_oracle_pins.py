@@ -572,6 +572,9 @@ def _clip_case(rng, V, w_target, A, inv_t=1.0, lo=0.2, hi=0.3):
     (1.0, 1.3, True), (1.1, -0.8, True),        # inside the clip range: the ratio's gradient
     (1.6, 1.3, False), (0.5, -0.8, False),      # clipped term is the minimum: no gradient
     (0.5, 1.3, True), (1.6, -0.8, True),        # unclipped term is the minimum: gradient flows
+    # between the widths (1 - 0.3 < w < 1 - 0.2, 1 + 0.2 < w < 1 + 0.3): the
+    # lower width 0.2 clips 0.75, the upper width 0.3 keeps 1.25 inside
+    (0.75, -0.8, False), (1.25, 1.3, True),
 ])
 def test_clipped_grpo_gradient_matches_central_differences(w_target, A, active):
     rng = np.random.default_rng(int(w_target * 100) + (7 if A > 0 else 11))
