@@ -51,11 +51,42 @@ KERNEL_SOURCES = ["precision_off_policy_gb300/csrc/sc_center.cu", "precision_off
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "center_kernel_C2_traffic.txt")
 
 
+def strip_c_comments(text: str) -> str:
+    """C/C++ source without its comments (newlines inside block comments kept);
+    string and character literals are copied as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            j = n if j < 0 else j + 2
+            out.append("\n" * text.count("\n", i, j))
+            i = j
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the fused kernel's code: its sources without comments, blank
+    lines and trailing blanks, so that editing a comment does not change the
+    kernel the committed counters were taken on."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            lines = (ln.rstrip() for ln in strip_c_comments(f.read()).split("\n"))
+        h.update("\n".join(ln for ln in lines if ln).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
 
 
@@ -152,17 +183,22 @@ class ClockSampler:
 
 
 def algorithmic_bytes(batch) -> int:
-    """Minimum bytes one launch must move (see the design notes): per valid
-    row the logits read and gradient write (4 V), the recorded head (8 per
-    id), its metadata (row_response, sampled id, rollout logprob, advantage:
-    16) and outputs (log p_a 4, diagnostics 64); per padding row the zero
-    gradient (2 V), row_response and sampled id (8) and outputs (68)."""
+    """Minimum bytes one launch must move: per valid row the logits read and
+    gradient write (4 V), the recorded head (8 per id used: its count clamped
+    to [0, K], 4 more for the count itself), its metadata (row_response,
+    sampled id, rollout logprob, advantage: 16) and outputs (log p_a 4,
+    diagnostics 64); per padding row the zero gradient (2 V), row_response and
+    sampled id (8) and outputs (68)."""
     V = batch["V"]
     resp = batch["row_response"].cpu().numpy()
     valid = int((resp >= 0).sum())
     masked = resp.size - valid
     cnt = batch["rec_count"]
-    k_total = int(cnt.sum()) if cnt is not None else valid * batch["K"]
+    if cnt is not None:
+        c = np.asarray(cnt.cpu().numpy() if hasattr(cnt, "cpu") else cnt)
+        k_total = int(np.clip(c[resp >= 0], 0, batch["K"]).sum())
+    else:
+        k_total = valid * batch["K"]
     extra_cnt = 4 * valid if cnt is not None else 0
     return valid * (4 * V + 16 + 68) + 8 * k_total + extra_cnt + masked * (2 * V + 8 + 68)
 

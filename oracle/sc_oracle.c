@@ -35,8 +35,7 @@
  * obtained from d log p_u / d x_v = [u == v] - p_v with c held constant
  * (stop-gradient).  Every gradient row therefore sums to zero.
  *
- * Readings where the pages are silent (each one is listed in the design
- * notes):
+ * Readings where the pages are silent:
  *   - std is the unbiased (n - 1) sample std; eps is added to it; a group
  *     whose rewards are all equal has A = 0; a group of one has A = 0.
  *   - a recorded id outside [0, V) is ignored and flagged; a repeated id is

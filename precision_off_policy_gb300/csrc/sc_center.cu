@@ -959,8 +959,8 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 // vectors exactly (its maximum first).  Vectors holding a recorded id
                 // take the rare per-entry path.
                 bool timed_out = false;
-                // Nothing reads the slice from shared memory after the pass (the
-                // scalar warp gathers the recorded ids' logits from global memory).
+                // The slice stays in its stage after the pass: the write pass reads
+                // it again, and the scalar warp took the recorded ids' logits from it.
                 float mz = -INFINITY;
                 if (nchunks > 0) {  // (waits decided warp-wide)
                     timed_out = !__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, kWaitLimitNs));
