@@ -11,7 +11,7 @@ exchange.  Two things span ranks:
   groups.
 
 Token counts stay integers until the final division, which is done in double
-precision ("avoids rounding token counts", devotd.net release note, section 4).
+precision (the devotd.net release note, section 4, keeps token counts unrounded).
 """
 
 from __future__ import annotations

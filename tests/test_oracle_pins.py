@@ -346,8 +346,9 @@ def test_row_sums_vanish_with_and_without_clamps():
 
 
 def test_unclamped_mu_hat_is_q_on_head_and_proportional_to_p_elsewhere():
-    # Docs: "The unrecorded behavior tail is approximated as proportional to
-    # the current policy": mu_hat = q on H and rho * p off H, total mass 1.
+    # The docs page models the behaviour mass outside the recorded ids as the
+    # current policy scaled to that mass: mu_hat = q on H and rho * p off H,
+    # total mass 1.
     rng = np.random.default_rng(32)
     V, K = 500, 50
     z = _random_row(rng, V, 2.0)
