@@ -136,6 +136,31 @@ def test_no_gpu_reaches_cuda_not_a_crash(L):
     assert call_center(L) in (sc.SC_ERR_CUDA, sc.SC_ERR_UNSUPPORTED)
 
 
+def call_center_noalloc(L, **kw):
+    """The allocation-free entry point with call_center's arguments (no workspace)."""
+    kw = dict(kw)
+    kw.pop("ws", None)
+    T, V = kw.pop("T", 4), kw.pop("V", 8)
+    p = sc.params(K_max=8)
+    return L.sc_center_forward_backward_noalloc(kw.get("logits", FAKE), T, V, 8, FAKE * 5, FAKE * 6, None,
+                                                kw.get("samp", FAKE * 7), None, kw.get("resp", FAKE * 10),
+                                                FAKE * 12, 2, ctypes.byref(p), kw.get("grad", FAKE * 2), 8,
+                                                kw.get("logp", FAKE * 8), None, None, None)
+
+
+def test_noalloc_empty_batch_is_a_no_op(L):
+    assert call_center_noalloc(L, T=0, logits=None, grad=None, samp=None, resp=None, logp=None) == sc.SC_OK
+    assert err(L) == ""
+
+
+def test_noalloc_without_a_gpu_reports_a_status(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_center_noalloc(L) in (sc.SC_ERR_CUDA, sc.SC_ERR_UNSUPPORTED)
+    assert err(L) != ""
+
+
 @pytest.mark.parametrize("args,status", [
     ((FAKE, -1, 4, 1, 1e-6, FAKE * 2), sc.SC_ERR_SHAPE),
     ((FAKE, 2, 0, 1, 1e-6, FAKE * 2), sc.SC_ERR_SHAPE),
