@@ -176,6 +176,64 @@ def _need(t, name, dtype, dev, ndim=None):
         raise ValueError(f"{name} must have {ndim} dimensions")
 
 
+def _check_rows(T, **named):
+    """Each given per-row tensor is 1-D with T entries."""
+    for name, t in named.items():
+        if t is not None and (t.dim() != 1 or t.shape[0] != T):
+            raise ValueError(f"{name} must have T = {T} entries, got shape {tuple(t.shape)}")
+
+
+def _check_row_inputs(T, K_max, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response,
+                      logp_out, diag_out, status):
+    """The per-row inputs and outputs shared by the fused call and the LM head
+    hold what the kernels read or write (the C ABI takes plain pointers, so a
+    short buffer is refused here, before any launch)."""
+    if K_max > 0:
+        for name, t in (("rec_ids", rec_ids), ("rec_logprobs", rec_logprobs)):
+            if t is None or tuple(t.shape) != (T, K_max):
+                raise ValueError(f"{name} must be [T, K_max] = [{T}, {K_max}]")
+    _check_rows(T, rec_count=rec_count, sampled_id=sampled_id, rollout_logprob=rollout_logprob,
+                row_response=row_response, logp_out=logp_out)
+    if diag_out is not None and (tuple(diag_out.shape) != (T, 16) or not diag_out.is_contiguous()):
+        raise ValueError("diag_out must be a contiguous int32 [T, 16] tensor")
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold one int32")
+
+
+def _check_center_buffers(T, V, K_max, logits, grad_out, rec_ids, rec_logprobs, rec_count, sampled_id,
+                          rollout_logprob, row_response, logp_out, diag_out, status):
+    """Shapes of the fused call's buffers: logits and grad_out rows hold at
+    least V entries, grad_out has T rows, the per-row tensors T entries."""
+    if logits.shape[1] < V:
+        raise ValueError(f"logits rows hold {logits.shape[1]} entries, fewer than V = {V}")
+    if grad_out.shape[0] != T or grad_out.shape[1] < V:
+        raise ValueError(f"grad_out must be [T = {T}, >= V = {V}], got {tuple(grad_out.shape)}")
+    _check_row_inputs(T, K_max, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response,
+                      logp_out, diag_out, status)
+
+
+def _check_topk_buffers(T, V, K, logits, ids_out, logprobs_out, count_out):
+    """Shapes of the top-K capture's buffers."""
+    if logits.shape[1] < V:
+        raise ValueError(f"logits rows hold {logits.shape[1]} entries, fewer than V = {V}")
+    for name, t in (("ids_out", ids_out), ("logprobs_out", logprobs_out)):
+        if tuple(t.shape) != (T, K):
+            raise ValueError(f"{name} must be [T, K] = [{T}, {K}], got {tuple(t.shape)}")
+    _check_rows(T, count_out=count_out)
+
+
+def _check_lmhead_buffers(T, d, V, K_max, dhidden, dw, rec_ids, rec_logprobs, rec_count, sampled_id,
+                          rollout_logprob, row_response, logp_out, diag_out, status):
+    """Shapes of the LM head call's buffers: dhidden [T, d] and dw [V, d],
+    contiguous, and the per-row tensors as for the fused call."""
+    if tuple(dhidden.shape) != (T, d) or not dhidden.is_contiguous():
+        raise ValueError(f"dhidden must be a contiguous [T, d] = [{T}, {d}] tensor")
+    if tuple(dw.shape) != (V, d) or not dw.is_contiguous():
+        raise ValueError(f"dw must be a contiguous [V, d] = [{V}, {d}] tensor")
+    _check_row_inputs(T, K_max, rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response,
+                      logp_out, diag_out, status)
+
+
 def _rows(t, name):
     """Row stride of a 2-D tensor whose rows are contiguous."""
     if t.stride(1) != 1:
@@ -188,12 +246,16 @@ def sc_group_advantages(rewards: torch.Tensor, n_groups: int, group_size: int,
                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """FP32 rewards [n_groups * group_size] (device) -> FP32 advantages."""
     dev = rewards.device
+    if dev.type != "cuda":
+        raise ValueError("rewards must be on a CUDA device")
     _need(rewards, "rewards", torch.float32, dev)
     if not rewards.is_contiguous() or rewards.numel() != n_groups * group_size:
         raise ValueError("rewards must be contiguous with n_groups * group_size entries")
     if out is None:
         out = torch.empty_like(rewards)
     _need(out, "out", torch.float32, dev)
+    if out.numel() != rewards.numel() or not out.is_contiguous():
+        raise ValueError("out must be contiguous with as many entries as rewards")
     _check(lib().sc_group_advantages(_ptr(rewards), int(n_groups), int(group_size),
                                      int(bool(normalize_std)), float(eps), _ptr(out), _stream(stream)))
     return out
@@ -207,6 +269,8 @@ def sc_rollout_mean_advantages(adv: torch.Tensor, row_response: torch.Tensor, ou
     Returns (adv_out, counts int32 [n_resp]); ``out`` may be ``adv``.
     """
     dev = adv.device
+    if dev.type != "cuda":
+        raise ValueError("adv must be on a CUDA device")
     _need(adv, "adv", torch.float32, dev, 1)
     _need(row_response, "row_response", torch.int32, dev, 1)
     n = adv.numel()
@@ -246,6 +310,7 @@ def sc_topk_capture(logits: torch.Tensor, K: int, inv_temperature: float = 1.0, 
     for name, t in [("ids_out", ids_out), ("logprobs_out", logprobs_out), ("count_out", count_out)]:
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
+    _check_topk_buffers(T, V, K, logits, ids_out, logprobs_out, count_out)
     if T == 0:
         return ids_out, logprobs_out, count_out
     _check(lib().sc_topk_capture(_ptr(logits), T, V, _rows(logits, "logits"), float(inv_temperature), K,
@@ -316,20 +381,16 @@ def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | Non
         _need(t, name, dt, dev, nd)
         if t is not None and not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
-    if K_max > 0 and (rec_ids.shape != (T, K_max) or rec_logprobs.shape != (T, K_max)):
-        raise ValueError("rec_ids / rec_logprobs must be [T, K_max]")
     if grad_out is None:
         grad_out = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
     _need(grad_out, "grad_out", torch.bfloat16, dev, 2)
     if logp_out is None:
         logp_out = torch.empty(T, dtype=torch.float32, device=dev)
     _need(logp_out, "logp_out", torch.float32, dev, 1)
-    if diag_out is not None:
-        _need(diag_out, "diag_out", torch.int32, dev, 2)
-        if diag_out.shape != (T, 16) or not diag_out.is_contiguous():
-            raise ValueError("diag_out must be a contiguous int32 [T, 16] tensor")
-    if status is not None:
-        _need(status, "status", torch.int32, dev, 1)
+    _need(diag_out, "diag_out", torch.int32, dev, 2)
+    _need(status, "status", torch.int32, dev, 1)
+    _check_center_buffers(T, V, K_max, logits, grad_out, rec_ids, rec_logprobs, rec_count, sampled_id,
+                          rollout_logprob, row_response, logp_out, diag_out, status)
     if T == 0:
         return grad_out, logp_out, diag_out
     if workspace_buf is None:
@@ -439,8 +500,10 @@ def sc_lmhead_forward_backward(hidden: torch.Tensor, w: torch.Tensor, rec_ids, r
     _need(dhidden, "dhidden", torch.bfloat16, dev, 2)
     _need(dw, "dw", torch.float32, dev, 2)
     _need(logp_out, "logp_out", torch.float32, dev, 1)
-    if diag_out is not None:
-        _need(diag_out, "diag_out", torch.int32, dev, 2)
+    _need(diag_out, "diag_out", torch.int32, dev, 2)
+    _need(status, "status", torch.int32, dev, 1)
+    _check_lmhead_buffers(T, d, V, K_max, dhidden, dw, rec_ids, rec_logprobs, rec_count, sampled_id,
+                          rollout_logprob, row_response, logp_out, diag_out, status)
     if T == 0:
         return dhidden, dw, logp_out, diag_out
     L = lib()
