@@ -21,9 +21,11 @@
  *
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
- *     allocates no memory; it keeps only a small per-process cache of launch
- *     plans.  The fused call takes a small caller-owned workspace (see
- *     SC_WORKSPACE_BYTES).
+ *     allocates no memory at run time.  It keeps a small per-process cache of
+ *     launch plans (for the LM head also cuBLASLt handles and matmul plans)
+ *     and one 256-byte static device array per GPU, which only
+ *     sc_center_forward_backward_noalloc uses.  The fused call takes a small
+ *     caller-owned workspace (see SC_WORKSPACE_BYTES).
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     Argument errors are detected on the host before anything is launched
  *     and returned as a status code; nothing is written in that case.
@@ -107,7 +109,8 @@ typedef struct sc_params {
     float inv_temperature; /* 1 / rollout temperature, finite, > 0               */
     float grad_scale;      /* multiplies every gradient element, e.g. 1 / N_tok */
     int cluster_size;      /* CTAs sharing one row: 0 = automatic, else 1..16   */
-    int threads;           /* compute threads per CTA (one more warp fetches):
+    int threads;           /* streaming threads per CTA (plus three warps: row
+                              scalars, bulk copies, zero rows):
                               0 = automatic, else 128, 256, 384 or 512          */
     int stages;            /* rows in flight per CTA: 0 = automatic, else 1..4   */
     float clip_low;        /* SC_IS_CLIP: ratio floor 1 - clip_low, 0 <= low < 1 */
@@ -154,8 +157,10 @@ typedef struct sc_row_diag {
  * logprobs_out : FP32 [T, K] log mu of those ids (0 past the count).
  * count_out    : int32 [T] min(K, V, nucleus size), or NULL.
  * K            : 1..1024.  inv_temperature finite > 0.  top_p in (0, 1].
- * Asynchronous on `stream`; nothing is allocated.  Sums are taken in 2^-40
- * fixed point, so results do not depend on the order of the additions.
+ * Asynchronous on `stream`; nothing is allocated.  Every sum is taken in a
+ * fixed order (compensated FP32 on the one-pass path that almost every row
+ * takes, 2^-40 fixed point on the exact path for the rest), so the results
+ * do not depend on how the rows are scheduled.
  * Errors: SC_ERR_SHAPE (T < 0, V outside 1..2^24, K, stride), SC_ERR_ARG,
  * SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
  */
