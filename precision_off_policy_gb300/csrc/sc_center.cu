@@ -12,9 +12,12 @@
 // GB300 design.  One row is shared by a cluster of C CTAs; CTA r owns the
 // vocabulary slice [r*S, min((r+1)*S, V)).  Each CTA is warp-specialised.
 //
-// * The producer warp walks the cluster's rows ahead of the others.  It
-//   writes padding and error rows (zero gradient) itself.  For every valid row
-//   it fills a slot of a metadata ring -- the row's scalars and the compact
+// * The producer warp walks the cluster's rows ahead of the others: the first
+//   seven eighths of the rows dealt round robin, the rest handed out at run
+//   time from a counter in the caller's workspace (CTA 0 takes each row and
+//   passes its index to its peers through their shared memory).  Padding and
+//   error rows go to the zero warp's queue.  For every valid row it fills a
+//   slot of a metadata ring -- the row's scalars and the compact
 //   list of recorded ids that fall in this CTA's slice (repeats dropped), with
 //   a one-bit-per-entry bitmap of them -- and starts 1-D bulk copies (TMA
 //   engine) of the logit slice into shared memory, chunk by chunk, as soon as
@@ -37,6 +40,8 @@
 //   entries (recorded ids and the sampled token) with their own gradients,
 //   and merges the C records into the row scalars (LSE, P_H, Q_H, rho, s,
 //   loss, k3, importance weight) the same way in every CTA.
+// * The zero warp writes the queued zero rows (padding and error rows) and
+//   their log p_a and diagnostics, so the producer never waits on them.
 // Every logit is read from HBM once and every gradient written once.  The
 // grid is persistent (as many clusters as fit).  Every wait is bounded (about
 // 1 s) and reports through the status word.
