@@ -5,8 +5,6 @@ committed DRAM traffic figure."""
 import os
 import shutil
 
-import numpy as np
-import pytest
 import torch
 
 import bench

@@ -17,8 +17,8 @@ import torch
 import oracle
 import precision_off_policy_gb300 as sc
 import synth
-from sc_parity import (bits_to_f64, check_rows, diag_rows, grad_bits, host_batch, oracle_adv,
-                       oracle_params, run_gpu, sc_params, ulp_bf16)
+from sc_parity import (check_rows, diag_rows, grad_bits, host_batch, oracle_adv, oracle_params, run_gpu,
+                       sc_params)
 
 pytestmark = pytest.mark.gpu
 
