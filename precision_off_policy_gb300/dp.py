@@ -3,8 +3,8 @@
 Rows are independent, so the path shards over rows with no data-path
 exchange.  Two things span ranks:
 
-* the loss is a mean over the generated tokens of the whole step ("global
-  generated-token reduction", docs "Score Centering" section), so every rank
+* the loss is a mean over every generated token of the whole step (the
+  docs' "Score Centering" section reduces over all of them), so every rank
   needs the global count of valid rows: one int64 all-reduce per batch;
 * advantages are normalised within a group of responses to one prompt, so a
   shard boundary must not cut a group: :func:`shard_groups` splits whole
