@@ -128,3 +128,57 @@ def test_pins_reject_planted_mistake(outcomes, name):
     rc, out = outcomes[name]
     # exit 1: the pins ran and at least one failed (a crash would be < 0)
     assert rc == 1, f"mutant '{name}' was not caught by the pins (exit {rc}):\n{out}"
+
+
+# The LM head's oracle is Python (oracle.lmhead_rows): its mutants are planted
+# in a copy of that function's source, swapped into the oracle module for one
+# test, and its two pins (finite differences, the identity head) run directly.
+LMHEAD_MUTANTS = {
+    "dH from the bf16-rounded gradient": ("return g @ W, g.T @ H,",
+                                          "return bf16_to_double(bf16_round_array(g)) @ W, g.T @ H,"),
+    "dW from the bf16-rounded gradient": ("return g @ W, g.T @ H,",
+                                          "return g @ W, bf16_to_double(bf16_round_array(g)).T @ H,"),
+    "grad_scale applied twice to dH": ("return g @ W, g.T @ H,", "return params.grad_scale * (g @ W), g.T @ H,"),
+    "logits truncated to bf16": ("z_bits = bf16_round_array(H @ W.T)",
+                                 "z_bits = ((H @ W.T).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)"),
+    "dW transposed": ("return g @ W, g.T @ H,", "return g @ W, (g.T @ H).T,"),
+}
+
+
+@pytest.mark.parametrize("name", list(LMHEAD_MUTANTS))
+def test_lmhead_pins_reject_planted_mistake(name, monkeypatch):
+    import inspect
+
+    import oracle
+    import test_oracle_pins as pins
+
+    old, new = LMHEAD_MUTANTS[name]
+    src = inspect.getsource(oracle.lmhead_rows)
+    assert src.count(old) == 1, name
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(oracle, "lmhead_rows", ns["lmhead_rows"])
+    caught = 0
+    for pin in (lambda: pins.test_lmhead_gradients_match_central_differences(1.0, 41),
+                lambda: pins.test_lmhead_gradients_match_central_differences(1 / 0.7, 42),
+                pins.test_lmhead_with_identity_head_reduces_to_the_row_oracle,
+                pins.test_lmhead_logits_are_the_rounded_fp64_products):
+        try:
+            pin()
+        except Exception:  # an assertion, or a shape mismatch the mutant causes
+            caught += 1
+    assert caught >= 1, f"LM-head mutant '{name}' passed every pin"
+
+
+def test_lmhead_unmutated_copy_passes_its_pins(monkeypatch):
+    import inspect
+
+    import oracle
+    import test_oracle_pins as pins
+
+    ns = dict(vars(oracle))
+    exec(compile(inspect.getsource(oracle.lmhead_rows), "<copy>", "exec"), ns)
+    monkeypatch.setattr(oracle, "lmhead_rows", ns["lmhead_rows"])
+    pins.test_lmhead_gradients_match_central_differences(1.0, 41)
+    pins.test_lmhead_with_identity_head_reduces_to_the_row_oracle()
+    pins.test_lmhead_logits_are_the_rounded_fp64_products()

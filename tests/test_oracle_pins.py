@@ -787,6 +787,26 @@ def test_lmhead_with_identity_head_reduces_to_the_row_oracle():
     np.testing.assert_array_equal(la, la2)
 
 
+def test_lmhead_logits_are_the_rounded_fp64_products():
+    # Non-dyadic inputs: each logit is the FP64 product H W^T (exact here: 24
+    # products of bf16 values need far fewer than 53 bits) rounded once by the
+    # scalar bf16 rounding pinned above; some entries round up in magnitude, so
+    # truncation would differ there.
+    rng = np.random.default_rng(45)
+    T, d, V, K = 5, 24, 40, 4
+    Hb = bf16_bits(rng.standard_normal((T, d)))
+    Wb = bf16_bits(rng.standard_normal((V, d)) * 0.3)
+    batch = dict(rec_ids=np.stack([rng.choice(V, K, replace=False) for _ in range(T)]).astype(np.int32),
+                 rec_logprobs=np.log(rng.dirichlet(np.ones(K), size=T) * 0.8).astype(np.float32), rec_count=None,
+                 sampled=rng.integers(0, V, T).astype(np.int32), rollout_logprob=None,
+                 row_response=np.array([0, 0, 1, 1, -1], np.int32), adv=np.array([0.7, -1.2], np.float32))
+    _, _, _, _, zb = oracle.lmhead_rows(Hb, Wb, batch, oracle.make_params())
+    prod = bf16_values(Hb) @ bf16_values(Wb).T
+    expected = np.array([oracle.bf16_bits(float(x)) for x in prod.ravel()], dtype=np.uint16).reshape(T, V)
+    np.testing.assert_array_equal(zb, expected)
+    assert np.any(np.abs(bf16_values(expected)) > np.abs(prod))
+
+
 def test_bf16_round_array_matches_the_scalar_rounding():
     rng = np.random.default_rng(44)
     x = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-6, 6, 2000), [0.0, -0.0, 1.0 + 2.0**-8]])
