@@ -6,7 +6,9 @@ swapped operand), compiles it with gcc into a temporary directory and runs
 the pin file ``test_oracle_pins.py`` against it in a child process, with
 ``SC_ORACLE_LIB`` pointing the oracle loader at the copy.  Every mutant must
 make at least one pin fail; an unmutated copy built the same way must pass
-them all, which shows that the children really load the copies.  The
+them all, which shows that the children really load the copies.  The LM
+head's oracle, written in Python, gets its mutants in-process instead (a
+mutated copy of the function swapped into the module for one test).  The
 committed oracle is never modified, and nothing here runs the CUDA library.
 """
 
