@@ -131,6 +131,15 @@ def test_explicit_launch_shapes(cluster, threads, stages, flags):
                 f"C={cluster} NT={threads} stages={stages} flags={flags}")
 
 
+@pytest.mark.parametrize("flags", [0, sc.SC_FLAGS_VECTOR])
+def test_largest_vocabulary_and_head(flags):
+    # the largest sizes the call accepts: V = 2^20 (clusters of 16 CTAs) and
+    # K_max = 1024 recorded ids per row
+    cfg = synth.config("C1", V=1 << 20, K=1024, L_pad=3, sigma=2.5)
+    batch = synth.make_batch(cfg)
+    _full_check(batch, sc_params(batch, flag_layout=flags), f"V=2^20 K=1024 flags={flags}")
+
+
 def test_automatic_flag_layout_follows_residency():
     # per-entry flags at 151936 entries (4 CTAs x 74 clusters beat 3 x 97);
     # per-vector flags at 248320 (5 x 58 beat 6 x 46): the plan with more CTAs
