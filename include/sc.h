@@ -115,7 +115,23 @@ typedef struct sc_params {
     int stages;            /* rows in flight per CTA: 0 = automatic, else 1..4   */
     float clip_low;        /* SC_IS_CLIP: ratio floor 1 - clip_low, 0 <= low < 1 */
     float clip_high;       /* SC_IS_CLIP: ratio ceiling 1 + clip_high, >= 0      */
+    int flag_layout;       /* how a CTA marks the recorded ids of its slice in
+                              shared memory: 0 = automatic, SC_FLAGS_ENTRY or
+                              SC_FLAGS_VECTOR                                   */
 } sc_params;
+
+/* Recorded-id flag layouts (sc_params.flag_layout).  SC_FLAGS_ENTRY keeps one
+ * bit per vocabulary entry of the slice: the fastest lookup.  SC_FLAGS_VECTOR
+ * keeps one bit per 8-entry vector plus, for the few flagged vectors, their
+ * 8-bit entry masks in vector order behind a per-word count of the flags
+ * before it: 15-20 KB less shared memory per CTA at the large vocabularies,
+ * so that a smaller cluster still fits two CTAs to an SM, for two more
+ * dependent shared-memory loads on a flagged vector.  The automatic choice
+ * takes, under each layout, the smallest cluster whose CTAs fit two to an SM
+ * and keeps the one with more CTAs resident on the GPU (SC_FLAGS_ENTRY on a
+ * tie). */
+#define SC_FLAGS_ENTRY 1
+#define SC_FLAGS_VECTOR 2
 
 /* Per-row diagnostics, 64 bytes.  Masked and error rows hold zeros and their
  * flags.  loss is the unscaled token loss; the batch loss whose gradient is
@@ -343,10 +359,11 @@ int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t* w, long l
  * parameters on the current device (no launch).  Any output pointer may be
  * NULL.  cluster_size: CTAs per row; threads: per CTA; slice: vocabulary
  * entries per CTA; smem_bytes: dynamic shared memory per CTA;
- * max_clusters: clusters resident at once (the persistent grid size).
+ * max_clusters: clusters resident at once (the persistent grid size);
+ * flag_layout: SC_FLAGS_ENTRY or SC_FLAGS_VECTOR.
  * Errors: as sc_center_forward_backward for V, K_max and p. */
 int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* threads, int* slice,
-                  int* smem_bytes, int* max_clusters);
+                  int* smem_bytes, int* max_clusters, int* flag_layout);
 
 /* Short text for a status code. */
 const char* sc_status_string(int status);

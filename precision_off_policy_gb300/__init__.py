@@ -34,6 +34,7 @@ __all__ = [
 
 SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
 SC_IS_NONE, SC_IS_TIS, SC_IS_MIS, SC_IS_CLIP = 0, 1, 2, 3
+SC_FLAGS_ENTRY, SC_FLAGS_VECTOR = 1, 2  # recorded-id flag layouts (0 = automatic)
 SC_STATUS_DATA, SC_STATUS_TIMEOUT_LOAD, SC_STATUS_TIMEOUT_EXCHANGE = 0x1, 0x2, 0x4
 
 FLAG_MASKED = 0x1
@@ -76,6 +77,7 @@ class Params(ctypes.Structure):
         ("stages", ctypes.c_int),
         ("clip_low", ctypes.c_float),
         ("clip_high", ctypes.c_float),
+        ("flag_layout", ctypes.c_int),
     ]
 
 
@@ -125,7 +127,7 @@ def lib():
                                                      ctypes.POINTER(Params), i64, vp, vp, vp, vp, vp, vp,
                                                      ctypes.c_size_t, vp]
             L.sc_lmhead_forward_backward.restype = i32
-            L.sc_plan_query.argtypes = [i32, ctypes.POINTER(Params)] + [ctypes.POINTER(i32)] * 5
+            L.sc_plan_query.argtypes = [i32, ctypes.POINTER(Params)] + [ctypes.POINTER(i32)] * 6
             L.sc_plan_query.restype = i32
             L.sc_status_string.argtypes = [i32]
             L.sc_status_string.restype = ctypes.c_char_p
@@ -145,12 +147,12 @@ def _check(status: int):
 
 def params(K_max=128, is_mode=SC_IS_NONE, tis_max=2.0, mis_min=0.5, mis_max=5.0, centering=True,
            inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0, stages=0, clip_low=0.2,
-           clip_high=0.3) -> Params:
+           clip_high=0.3, flag_layout=0) -> Params:
     """Defaults are the settings table of the docs' "Score Centering" section
     and the clip widths of the page's `grpo` preset."""
     return Params(int(K_max), int(is_mode), float(tis_max), float(mis_min), float(mis_max),
                   int(bool(centering)), float(inv_temperature), float(grad_scale), int(cluster_size),
-                  int(threads), int(stages), float(clip_low), float(clip_high))
+                  int(threads), int(stages), float(clip_low), float(clip_high), int(flag_layout))
 
 
 def _ptr(t):
@@ -408,9 +410,10 @@ def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | Non
 
 def sc_plan_query(V: int, p: Params) -> dict:
     """The launch plan the library uses for V on the current device."""
-    out = [ctypes.c_int(0) for _ in range(5)]
+    out = [ctypes.c_int(0) for _ in range(6)]
     _check(lib().sc_plan_query(int(V), ctypes.byref(p), *[ctypes.byref(o) for o in out]))
-    return dict(zip(["cluster_size", "threads", "slice", "smem_bytes", "max_clusters"], [o.value for o in out]))
+    return dict(zip(["cluster_size", "threads", "slice", "smem_bytes", "max_clusters", "flag_layout"],
+                    [o.value for o in out]))
 
 
 def diag_to_numpy(diag: torch.Tensor) -> np.ndarray:

@@ -19,13 +19,14 @@
 //   error rows go to the zero warp's queue.  For every valid row it fills a
 //   slot of a metadata ring -- the row's scalars and the compact
 //   list of recorded ids that fall in this CTA's slice (repeats dropped), with
-//   a one-bit-per-entry bitmap of them -- and starts 1-D bulk copies (TMA
+//   flags marking them (one bit per entry, or one bit per 8-entry vector with
+//   the flagged vectors' masks) -- and starts 1-D bulk copies (TMA
 //   engine) of the logit slice into shared memory, chunk by chunk, as soon as
 //   the streaming warps have released the buffer.
 // * The streaming warps take each row through two passes over the slice in
 //   shared memory.  Phase A: with one exponent offset (the largest logit of the
 //   slice's first vectors), sum 2^y and its entropy term over the unrecorded
-//   entries (recorded ids are skipped through the bitmap, so the unrecorded
+//   entries (recorded ids are skipped through the flags, so the unrecorded
 //   mass accumulates directly, with no 1 - P_H cancellation).  Then, once the
 //   cluster has the row scalars, the write pass: g_v = beta p_v with 16-byte
 //   stores and no special cases, handing every chunk back to the producer as
@@ -115,8 +116,9 @@ static_assert(sizeof(Partial) == 64, "partial record is 64 bytes");
 struct Layout {
     int stage_bytes;  // bytes of one data stage (128-aligned)
     int list_cap;     // entries of one owned list (K_max)
-    int nwords;       // bitmap words of one slice (one bit per entry)
-    int off_meta, off_list_li, off_list_q, off_bitmap, off_bars, off_part, off_frs,
+    int nwords;       // flag words of one slice (a bit per entry, or per 8-entry vector)
+    int mwords;       // mask words of one slot (per-vector flags: four 8-bit masks a word)
+    int off_meta, off_list_li, off_list_q, off_bitmap, off_vpre, off_vmask, off_bars, off_part, off_frs,
         off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, off_grab, off_zq, off_zqf, total;
 };
 
@@ -252,7 +254,9 @@ constexpr int kNumBars = kZqBase + 2 * kZq;
 // Resident CTAs per SM the register allocation must allow.
 constexpr int min_blocks(int NC) { return NC <= 128 ? 4 : 2; }
 
-template <int NC>
+// VF: recorded-id flags one bit per 8-entry vector (with the flagged vectors'
+// masks) instead of one bit per entry.
+template <int NC, bool VF>
 __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int NCW = NC / 32;  // streaming warps; warp NCW: row scalars; NCW + 1: producer; NCW + 2: zero rows
@@ -267,7 +271,9 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     RowMeta* meta = reinterpret_cast<RowMeta*>(smem + L.off_meta);         // [kMetaSlots]
     int* list_li = reinterpret_cast<int*>(smem + L.off_list_li);           // [kMetaSlots][cap]
     float* list_q = reinterpret_cast<float*>(smem + L.off_list_q);         // [kMetaSlots][cap] q = e^lp
-    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [kMetaSlots][nwords]
+    uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [kMetaSlots][nwords] flags
+    uint16_t* vpre = reinterpret_cast<uint16_t*>(smem + L.off_vpre);        // VF: [kMetaSlots][nwords]
+    uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + L.off_vmask);      // VF: [kMetaSlots][mwords]
     Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [kXBufs][C]
     float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);             // [kMaxCluster]
     float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);            // [2][cap] recorded logits
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     const int n = max(hi - lo, 0);
     const int n8 = n & ~7, nvb = n8 >> 3, tail = n - n8;
     const int nchunks = (nvb + a.ncv - 1) / a.ncv;
-    const int cap = L.list_cap, nwords = L.nwords;
+    const int cap = L.list_cap, nwords = L.nwords, mwords = L.mwords;
     const float kscale = a.inv_t * kLog2e;
     const uint64_t pol = l2_policy_evict_first();      // last use: gradient stores, write-pass reads
     const uint64_t pol_keep = l2_policy_evict_normal();  // slice copies (measured: evict-first is slower)
@@ -479,9 +485,13 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             int* li_s = list_li + ms * cap;
             float* q_s = list_q + ms * cap;
             uint32_t* bm = bitmap + ms * nwords;
-            {  // clear the bits of the slot's previous row (whole words: they are all its own)
+            uint16_t* pre = vpre + ms * nwords;
+            uint32_t* mk = vmask + ms * mwords;
+            {  // clear the flags of the slot's previous row (whole words: they are all its own)
                 const int old = meta[ms].nown;
-                for (int e = lane; e < old; e += 32) bm[li_s[e] >> 5] = 0u;
+                for (int e = lane; e < old; e += 32) bm[li_s[e] >> (VF ? 8 : 5)] = 0u;
+                if constexpr (VF)
+                    for (int w = lane; w < mwords; w += 32) mk[w] = 0u;
             }
             __syncwarp();
             const long long kb = t * static_cast<long long>(K_max);
@@ -520,9 +530,42 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                         li_s[pos] = id - lo;
                         q_s[pos] = q;
                         hm = head_merge(hm, HeadMass{q, k, -expm1f(lpr[r]), 0.0f, 0.0f});
-                        atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
+                        if constexpr (VF)
+                            atomicOr(&bm[(id - lo) >> 8], 1u << (((id - lo) >> 3) & 31));
+                        else
+                            atomicOr(&bm[(id - lo) >> 5], 1u << ((id - lo) & 31));
                     }
                     nown += __popc(km);
+                    __syncwarp();
+                }
+            }
+            if constexpr (VF) {
+                if (nown > 0) {
+                    // rank of each flagged vector among the slice's flagged vectors, in
+                    // vector order: per flag word, the flags of the words before it
+                    // (each lane counts a run of consecutive words, one warp scan)
+                    const int wb = (nwords + 31) >> 5;
+                    const int w0 = min(lane * wb, nwords), w1 = min(w0 + wb, nwords);
+                    int nf = 0;
+                    for (int w = w0; w < w1; ++w) nf += __popc(bm[w]);
+                    int inc = nf;
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const int y = __shfl_up_sync(kFull, inc, d);
+                        if (lane >= d) inc += y;
+                    }
+                    int run = inc - nf;
+                    for (int w = w0; w < w1; ++w) {
+                        pre[w] = static_cast<uint16_t>(run);
+                        run += __popc(bm[w]);
+                    }
+                    __syncwarp();
+                    // each recorded entry's bit in its vector's mask (ranks < nown <= cap)
+                    for (int e = lane; e < nown; e += 32) {
+                        const int x = li_s[e], v = x >> 3;
+                        const int r = pre[v >> 5] + __popc(bm[v >> 5] & ((1u << (v & 31)) - 1u));
+                        atomicOr(&mk[r >> 2], (1u << (x & 7)) << (8 * (r & 3)));
+                    }
                     __syncwarp();
                 }
             }
@@ -955,6 +998,21 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 // ------------- phase A: one pass over the slice in shared memory -------------
                 const uint32_t fpar = (i / NB) & 1u;
                 const uint32_t* bm = bitmap + ms * nwords;
+                const uint16_t* pre = vpre + ms * nwords;
+                const uint32_t* mk = vmask + ms * mwords;
+                // VF: the recorded entries (8 bits) of a flagged vector j, fw its flag word
+                auto rec_mask = [&](int j, uint32_t fw) {
+                    const int r = pre[j >> 5] + __popc(fw & ((1u << (j & 31)) - 1u));
+                    return (mk[r >> 2] >> (8 * (r & 3))) & 0xFFu;
+                };
+                auto rec_bits = [&](int j) -> uint32_t {  // the recorded entries of any vector j
+                    if constexpr (VF) {
+                        const uint32_t fw = bm[j >> 5];
+                        return ((fw >> (j & 31)) & 1u) ? rec_mask(j, fw) : 0u;
+                    } else {
+                        return (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                    }
+                };
                 // The exponent offset is the largest logit among the slice's first 32
                 // vectors -- every warp reads the same ones and reduces them the same
                 // way, so the whole CTA shares it without a barrier -- fixed for the
@@ -991,7 +1049,13 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
 #pragma unroll 2
                     for (int j = c * a.ncv + tid; j < v1; j += NC) {
                         const uint4 w = lds128(buf_s + 16u * j);
-                        const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                        uint32_t rbits, fw = 0u;
+                        if constexpr (VF) {
+                            fw = bm[j >> 5];
+                            rbits = (fw >> (j & 31)) & 1u;  // nonzero: look up the mask below
+                        } else {
+                            rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                        }
                         if (rbits == 0u) {
                             f2_t y = f2_fma(bf2_to_f2(w.x), K2, NO2);
                             f2_t e = f2_ex2(y);
@@ -1010,6 +1074,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                             S1b = f2_add(S1b, e);
                             S2b = f2_fma(e, y, S2b);
                         } else {
+                            if constexpr (VF) rbits = rec_mask(j, fw);
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
@@ -1026,9 +1091,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 }
                 if (tail && tid == 0 && !timed_out) {  // entries past the last whole vector
                     const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                    const uint32_t tb = rec_bits(nvb);
                     for (int q = 0; q < tail; ++q) {
                         const int li = n8 + q;
-                        if (!((bm[li >> 5] >> (li & 31)) & 1u)) {
+                        if (!((tb >> q) & 1u)) {
                             const float y = fmaf(bf_to_f(lrow[li]), kscale, -o);
                             const float e = ex2(y);
                             s1x += e;
@@ -1054,7 +1120,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                         const float ox = mx * kscale;
                         for (int j = tid; j < nvb; j += NC) {
                             const uint4 w = lds128(buf_s + 16u * j);
-                            const uint32_t rbits = (bm[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+                            const uint32_t rbits = rec_bits(j);
                             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
@@ -1071,9 +1137,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     ms_acc = Mass{mx, s1, s2};
                     if (tail && tid == 0) {  // the tail again, relative to this maximum
                         const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
+                        const uint32_t tb = rec_bits(nvb);
                         for (int q = 0; q < tail; ++q) {
                             const int li = n8 + q;
-                            if (!((bm[li >> 5] >> (li & 31)) & 1u))
+                            if (!((tb >> q) & 1u))
                                 ms_acc = mass_merge(ms_acc, Mass{bf_to_f(lrow[li]), 1.0f, 0.0f}, kscale);
                         }
                     }
@@ -1178,14 +1245,16 @@ inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 struct Plan {
     int C, NC, S, ncv, NB;
+    bool VF;  // recorded-id flags per 8-entry vector (else per entry)
     Layout L;
 };
 
-Layout make_layout(int S, int K_max, int NC, int NB, int C) {
+Layout make_layout(int S, int K_max, int NC, int NB, int C, bool vf) {
     Layout L;
     L.stage_bytes = round_up(S * 2, 128);
     L.list_cap = K_max > 0 ? K_max : 1;
-    L.nwords = (S + 31) / 32;
+    L.nwords = vf ? (S / 8 + 31) / 32 : (S + 31) / 32;
+    L.mwords = vf ? (L.list_cap + 3) / 4 : 0;
     int off = NB * L.stage_bytes;
     auto take = [&](int bytes) {
         const int o = off;
@@ -1196,6 +1265,8 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     L.off_list_li = take(kMetaSlots * L.list_cap * 4);
     L.off_list_q = take(kMetaSlots * L.list_cap * 4);
     L.off_bitmap = take(kMetaSlots * L.nwords * 4);
+    L.off_vpre = take(vf ? kMetaSlots * L.nwords * 2 : 0);
+    L.off_vmask = take(kMetaSlots * L.mwords * 4);
     L.off_bars = take(kNumBars * 8);
     L.off_part = take(kXBufs * C * static_cast<int>(sizeof(Partial)));
     L.off_frs = take(kMaxCluster * 8);
@@ -1213,11 +1284,11 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C) {
     return L;
 }
 
-// Automatic plan: the smallest cluster (up to 16 CTAs) whose CTAs fit two to
-// an SM, one data stage that the write pass hands back chunk by chunk to the
-// next row's copies, 256 streaming threads (128 for small slices).  For the
-// 151936-entry vocabulary: 4 CTAs x 37984 entries; for 248320: 6 x 41392.
-int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, Plan* out) {
+// A plan under one flag layout.  Automatic cluster size: the smallest cluster
+// (up to 16 CTAs) whose CTAs fit two to an SM; one data stage that the write
+// pass hands back chunk by chunk to the next row's copies; 256 streaming
+// threads (128 for small slices).
+int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages, bool vf, Plan* out) {
     const int NB = req_stages > 0 ? req_stages : 1;
     int C = req_cluster;
     auto threads_for = [&](int S) {
@@ -1229,7 +1300,7 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
         C = kMaxCluster;
         for (int c = 1; c <= kMaxCluster; ++c) {
             const int Sc = round_up((V + c - 1) / c, 8);
-            if (make_layout(Sc, K_max, threads_for(Sc), NB, c).total <= kTwoPerSmBytes) {
+            if (make_layout(Sc, K_max, threads_for(Sc), NB, c, vf).total <= kTwoPerSmBytes) {
                 C = c;
                 break;
             }
@@ -1238,7 +1309,7 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
     }
     const int S = round_up((V + C - 1) / C, 8);
     const int NC = threads_for(S);
-    const Layout L = make_layout(S, K_max, NC, NB, C);
+    const Layout L = make_layout(S, K_max, NC, NB, C, vf);
     if (L.total > kMaxSmem)
         return fail(SC_ERR_SHAPE,
                     "V = %d with cluster size %d and %d stages needs %d bytes of shared memory per CTA", V, C,
@@ -1248,6 +1319,7 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
     out->NC = NC;
     out->S = S;
     out->NB = NB;
+    out->VF = vf;
     // chunks of a whole number of passes of the compute threads (every thread
     // has the same share of each chunk), at most kMaxChunks of them
     int ncv = NC * (kChunkVecTarget / NC > 1 ? kChunkVecTarget / NC : 1);
@@ -1259,28 +1331,28 @@ int make_plan(int V, int K_max, int req_cluster, int req_threads, int req_stages
 
 using KernelFn = void (*)(KArgs);
 
-KernelFn kernel_for(int NC) {
+KernelFn kernel_for(int NC, bool vf) {
     switch (NC) {
-        case 128: return center_kernel<128>;
-        case 256: return center_kernel<256>;
-        case 384: return center_kernel<384>;
-        case 512: return center_kernel<512>;
+        case 128: return vf ? center_kernel<128, true> : center_kernel<128, false>;
+        case 256: return vf ? center_kernel<256, true> : center_kernel<256, false>;
+        case 384: return vf ? center_kernel<384, true> : center_kernel<384, false>;
+        case 512: return vf ? center_kernel<512, true> : center_kernel<512, false>;
         default: return nullptr;
     }
 }
 
 std::mutex g_plan_mutex;
-std::map<std::tuple<int, int>, int> g_attr_set;                     // (device, NC)
-std::map<std::tuple<int, int, int, int>, int> g_max_clusters;      // (device, NC, C, smem)
+std::map<std::tuple<int, int, bool>, int> g_attr_set;                     // (device, NC, VF)
+std::map<std::tuple<int, int, bool, int, int>, int> g_max_clusters;      // (device, NC, VF, C, smem)
 
 // Sets the kernel's shared-memory and cluster attributes and returns the
 // number of clusters that can be resident at once.
 int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
-    KernelFn fn = kernel_for(P.NC);
+    KernelFn fn = kernel_for(P.NC, P.VF);
     if (!fn) return fail(SC_ERR_ARG, "threads = %d is not one of 128, 256, 384, 512", P.NC);
     std::lock_guard<std::mutex> lock(g_plan_mutex);
     cudaError_t e;
-    auto key = std::make_tuple(dev, P.NC);
+    auto key = std::make_tuple(dev, P.NC, P.VF);
     if (g_attr_set.find(key) == g_attr_set.end()) {
         e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
@@ -1290,7 +1362,7 @@ int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
         g_attr_set[key] = 1;
     }
-    auto ckey = std::make_tuple(dev, P.NC, P.C, P.L.total);
+    auto ckey = std::make_tuple(dev, P.NC, P.VF, P.C, P.L.total);
     auto cit = g_max_clusters.find(ckey);
     if (cit != g_max_clusters.end()) {
         *max_clusters = cit->second;
@@ -1340,35 +1412,70 @@ int check_params(int V, const sc_params* p) {
     if (p->centering != 0 && p->centering != 1) return fail(SC_ERR_ARG, "centering must be 0 or 1");
     if (p->cluster_size < 0 || p->cluster_size > kMaxCluster)
         return fail(SC_ERR_ARG, "cluster_size = %d outside 0..%d", p->cluster_size, kMaxCluster);
-    if (p->threads != 0 && !kernel_for(p->threads))
+    if (p->threads != 0 && !kernel_for(p->threads, false))
         return fail(SC_ERR_ARG, "threads = %d is not 0, 128, 256, 384 or 512", p->threads);
     if (p->stages < 0 || p->stages > kMaxStages)
         return fail(SC_ERR_ARG, "stages = %d outside 0..%d", p->stages, kMaxStages);
+    if (p->flag_layout < 0 || p->flag_layout > SC_FLAGS_VECTOR)
+        return fail(SC_ERR_ARG, "flag_layout = %d is not 0, %d or %d", p->flag_layout, SC_FLAGS_ENTRY,
+                    SC_FLAGS_VECTOR);
     return SC_OK;
+}
+
+// The plan for V and p on device dev, with its resident clusters.  A given
+// flag layout, or a given cluster size, is kept (a given cluster size alone
+// takes per-entry flags).  Otherwise each layout gets its smallest cluster
+// that fits two CTAs to an SM, and the plan with more CTAs resident on the
+// GPU wins, per-entry flags on a tie: per-vector flags free 15-20 KB of shared
+// memory, which matters only where it lets a smaller cluster fill the SMs
+// better (measured: 248320 entries, 5 CTAs x 58 clusters against 6 x 46, 6 %
+// faster; at 151936 entries 3 x 97 against 4 x 74 was 13 % slower).
+int plan_for(int dev, int V, const sc_params* p, Plan* P, int* mc) {
+    if (p->flag_layout != 0 || p->cluster_size > 0) {
+        int st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, p->flag_layout == SC_FLAGS_VECTOR, P);
+        if (st != SC_OK) return st;
+        return prepare_kernel(dev, *P, mc);
+    }
+    Plan pe, pv;
+    int me = 0, mv = 0;
+    int st = make_plan(V, p->K_max, 0, p->threads, p->stages, false, &pe);
+    if (st != SC_OK) return st;
+    st = prepare_kernel(dev, pe, &me);
+    if (st != SC_OK) return st;
+    *P = pe;
+    *mc = me;
+    if (make_plan(V, p->K_max, 0, p->threads, p->stages, true, &pv) == SC_OK && pv.C < pe.C &&
+        prepare_kernel(dev, pv, &mv) == SC_OK && static_cast<long long>(mv) * pv.C > static_cast<long long>(me) * pe.C) {
+        *P = pv;
+        *mc = mv;
+    }
+    return ok();
 }
 
 }  // namespace
 }  // namespace sc
 
 extern "C" int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* threads, int* slice,
-                             int* smem_bytes, int* max_clusters) {
+                             int* smem_bytes, int* max_clusters, int* flag_layout) {
     using namespace sc;
     int st = check_params(V, p);
     if (st != SC_OK) return st;
     Plan P;
-    st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, &P);
+    // the shape checks of the requested (or per-entry automatic) plan need no device
+    st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, p->flag_layout == SC_FLAGS_VECTOR, &P);
     if (st != SC_OK) return st;
     int dev = 0;
     st = check_device(&dev);
     if (st != SC_OK) return st;
     int mc = 0;
-    st = prepare_kernel(dev, P, &mc);
+    st = plan_for(dev, V, p, &P, &mc);
     if (st != SC_OK) return st;
     if (cluster_size) *cluster_size = P.C;
     if (threads) *threads = P.NC;
     if (slice) *slice = P.S;
     if (smem_bytes) *smem_bytes = P.L.total;
     if (max_clusters) *max_clusters = mc;
+    if (flag_layout) *flag_layout = P.VF ? SC_FLAGS_VECTOR : SC_FLAGS_ENTRY;
     return ok();
 }
 
@@ -1414,13 +1521,14 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
             return fail(SC_ERR_ARG, "grad_out overlaps logits other than exactly (in place)");
     }
     Plan P;
-    st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, &P);
+    // the shape checks of the requested (or per-entry automatic) plan need no device
+    st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, p->flag_layout == SC_FLAGS_VECTOR, &P);
     if (st != SC_OK) return st;
     int dev = 0;
     st = check_device(&dev);
     if (st != SC_OK) return st;
     int mc = 0;
-    st = prepare_kernel(dev, P, &mc);
+    st = plan_for(dev, V, p, &P, &mc);
     if (st != SC_OK) return st;
     const long long G = T < mc ? T : mc;
     // About the last eighth of the rows are handed out at run time (the rest,
@@ -1480,7 +1588,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NC), ka);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NC, P.VF), ka);
     if (e != cudaSuccess) return cuda_fail(e, "center_kernel launch");
     return ok();
 }

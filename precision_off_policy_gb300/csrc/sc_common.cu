@@ -82,6 +82,7 @@ int sc_params_default(sc_params* p) {
     p->stages = 0;
     p->clip_low = 0.2f;
     p->clip_high = 0.3f;
+    p->flag_layout = 0;
     return sc::ok();
 }
 
@@ -100,6 +101,6 @@ const char* sc_status_string(int status) {
 
 const char* sc_last_error(void) { return sc::last_error_text(); }
 
-int sc_abi_version(void) { return 102; }
+int sc_abi_version(void) { return 103; }
 
 }  // extern "C"

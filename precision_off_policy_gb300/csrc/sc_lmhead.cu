@@ -143,7 +143,7 @@ extern "C" int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t
     if (V < 1 || V > (1 << 20)) return fail(SC_ERR_SHAPE, "V = %d outside 1..2^20", V);
     if (block_rows < 1) return fail(SC_ERR_SHAPE, "block_rows = %lld < 1", block_rows);
     {   // the score-centering parameters and V, checked before anything is launched
-        const int pst = sc_plan_query(V, p, nullptr, nullptr, nullptr, nullptr, nullptr);
+        const int pst = sc_plan_query(V, p, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
         if (pst != SC_OK && pst != SC_ERR_CUDA && pst != SC_ERR_UNSUPPORTED) return pst;
     }
     if (T == 0) return ok();

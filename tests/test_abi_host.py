@@ -41,14 +41,15 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_struct_layouts_match_header(L):
-    assert ctypes.sizeof(sc.Params) == 52
+    assert ctypes.sizeof(sc.Params) == 56
     assert sc.DIAG_DTYPE.itemsize == 64
     p = sc.Params()
     assert L.sc_params_default(ctypes.byref(p)) == sc.SC_OK
     assert (p.K_max, p.is_mode, p.tis_max, p.mis_min, p.mis_max, p.centering) == (128, 0, 2.0, 0.5, 5.0, 1)
     assert (p.inv_temperature, p.grad_scale, p.cluster_size, p.threads, p.stages) == (1.0, 1.0, 0, 0, 0)
+    assert (p.clip_low, p.clip_high, p.flag_layout) == (pytest.approx(0.2), pytest.approx(0.3), 0)
     assert L.sc_params_default(None) == sc.SC_ERR_NULL
-    assert L.sc_abi_version() == 102
+    assert L.sc_abi_version() == 103
     assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
 
 
@@ -94,6 +95,8 @@ def err(L):
     (dict(cluster_size=17), sc.SC_ERR_ARG),
     (dict(threads=100), sc.SC_ERR_ARG),
     (dict(stages=5), sc.SC_ERR_ARG),
+    (dict(flag_layout=3), sc.SC_ERR_ARG),
+    (dict(flag_layout=-1), sc.SC_ERR_ARG),
     (dict(logits=None), sc.SC_ERR_NULL),
     (dict(grad=None), sc.SC_ERR_NULL),
     (dict(logp=None), sc.SC_ERR_NULL),

@@ -112,21 +112,43 @@ def test_c3_chunk_reduced_full_parity():
     _full_check(batch, sc_params(batch), "C3 reduced chunk 1")
 
 
+@pytest.mark.parametrize("flags", [0, sc.SC_FLAGS_VECTOR])
 @pytest.mark.parametrize("V", [1, 3, 8, 13, 1000, 4097, 33333])
-def test_ragged_vocabulary_sizes(V):
+def test_ragged_vocabulary_sizes(V, flags):
     K = min(128, V)
     cfg = synth.config("C1", V=V, K=K, L_pad=5, sigma=2.5)
     batch = synth.make_batch(cfg)
-    _full_check(batch, sc_params(batch), f"V={V}")
+    _full_check(batch, sc_params(batch, flag_layout=flags), f"V={V} flags={flags}")
 
 
+@pytest.mark.parametrize("flags", [sc.SC_FLAGS_ENTRY, sc.SC_FLAGS_VECTOR])
 @pytest.mark.parametrize("cluster,threads,stages", [(1, 128, 1), (2, 256, 2), (3, 384, 3), (4, 512, 4),
                                                     (8, 256, 1), (16, 128, 2), (16, 256, 3), (5, 256, 2)])
-def test_explicit_launch_shapes(cluster, threads, stages):
+def test_explicit_launch_shapes(cluster, threads, stages, flags):
     cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=16, len_lo=10, len_hi=16, V=30011)
     batch = synth.make_batch(cfg)
-    _full_check(batch, sc_params(batch, cluster_size=cluster, threads=threads, stages=stages),
-                f"C={cluster} NT={threads} stages={stages}")
+    _full_check(batch, sc_params(batch, cluster_size=cluster, threads=threads, stages=stages, flag_layout=flags),
+                f"C={cluster} NT={threads} stages={stages} flags={flags}")
+
+
+@pytest.mark.parametrize("flags", [0, sc.SC_FLAGS_VECTOR])
+def test_largest_vocabulary_and_head(flags):
+    # the largest sizes the call accepts: V = 2^20 (clusters of 16 CTAs) and
+    # K_max = 1024 recorded ids per row
+    cfg = synth.config("C1", V=1 << 20, K=1024, L_pad=3, sigma=2.5)
+    batch = synth.make_batch(cfg)
+    _full_check(batch, sc_params(batch, flag_layout=flags), f"V=2^20 K=1024 flags={flags}")
+
+
+def test_automatic_flag_layout_follows_residency():
+    # per-entry flags at 151936 entries (4 CTAs x 74 clusters beat 3 x 97);
+    # per-vector flags at 248320 (5 x 58 beat 6 x 46): the plan with more CTAs
+    p = sc.params(K_max=128)
+    q1, q2 = sc.sc_plan_query(151936, p), sc.sc_plan_query(248320, p)
+    assert q1["flag_layout"] == sc.SC_FLAGS_ENTRY and q1["cluster_size"] == 4, q1
+    assert q2["flag_layout"] == sc.SC_FLAGS_VECTOR and q2["cluster_size"] == 5, q2
+    assert q2["cluster_size"] * q2["max_clusters"] > 6 * sc.sc_plan_query(248320, sc.params(
+        K_max=128, cluster_size=6))["max_clusters"]
 
 
 @pytest.mark.parametrize("mode", [sc.SC_IS_TIS, sc.SC_IS_MIS])
@@ -377,8 +399,8 @@ def _unprotected(batch):
     return keep
 
 
-@pytest.mark.parametrize("cluster,threads", [(0, 0), (2, 128)])
-def test_wide_dynamic_range_and_infinite_logits(cluster, threads):
+@pytest.mark.parametrize("cluster,threads,flags", [(0, 0, 0), (2, 128, 0), (0, 0, 2), (2, 128, 2)])
+def test_wide_dynamic_range_and_infinite_logits(cluster, threads, flags):
     """Entries far above the exponent offset a warp takes from its first vectors
     (2^y would overflow), -inf entries (0 * -inf), and warps whose first vectors
     are all -inf: each takes the exact per-thread path and must still match."""
@@ -396,7 +418,8 @@ def test_wide_dynamic_range_and_infinite_logits(cluster, threads):
     neg[2, :2048] = True                       # row 2: the first 2048 entries -inf
     z[neg & free] = float("-inf")
     b = _edit(batch, logits=z.to(torch.bfloat16))
-    _full_check(b, sc_params(b, cluster_size=cluster, threads=threads), f"dynamic range {cluster},{threads}")
+    _full_check(b, sc_params(b, cluster_size=cluster, threads=threads, flag_layout=flags),
+                f"dynamic range {cluster},{threads} flags={flags}")
 
 
 def test_row_stride_larger_than_vocab():
