@@ -612,7 +612,7 @@ struct GroupShared {
     unsigned long long cand[kCap];      // (key << 32) | ~id
     float fred[kGW], flo[kGW];          // group maximum / sums of pairs
     double dS, dlse;
-    double pnuc;
+    double pnuc, lnuc;  // the nucleus mass and log(nucleus mass / normaliser)
     int ncand, cross;
 };
 struct KernelShared {
@@ -880,14 +880,18 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
                 if (cross > nc) gs.pnuc = (all.hi - t_hi) + (all.lo - t_lo) >= 0.0f ? (double)all.hi + (double)all.lo : -1.0;
             }
             if (mine == cross && cross <= nc) gs.pnuc = (double)run.hi + (double)run.lo;
+            __syncwarp();
+            // the one FP64 logarithm of the nucleus, in one thread (GB300's FP64
+            // rate is a small fraction of its FP32 rate)
+            if (lane == 0) gs.lnuc = gs.pnuc > 0.0 ? log(gs.pnuc / S) : 0.0;
         }
         G.sync();
         const int cross = gs.cross;
         const double P = gs.pnuc;
+        log_nuc = gs.lnuc;
         G.sync();
         if (!(P > 0.0)) return false;  // the nucleus reaches below the candidates
         count = min(Kp, cross <= nc ? cross : nc);
-        log_nuc = log(P / S);
     }
 
     // ---- outputs
