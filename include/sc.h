@@ -118,6 +118,18 @@ typedef struct sc_params {
     int flag_layout;       /* how a CTA marks the recorded ids of its slice in
                               shared memory: 0 = automatic, SC_FLAGS_ENTRY or
                               SC_FLAGS_VECTOR                                   */
+    int wait_limit_us;     /* how long any wait inside the kernel (a bulk copy,
+                              a peer's record, a hand-off between its warps)
+                              may take before the launch gives up and sets
+                              SC_STATUS_TIMEOUT_*: 0 = 1 s, else 1..60000000 us.
+                              The final wait for bulk copies in flight before
+                              a CTA exits always allows 1 s.                    */
+    int test_stall;        /* test hook, 0 in normal use.  1: every CTA leaves
+                              out the bulk copy of the first chunk of its first
+                              row, so the waits for it run out: the launch ends
+                              early with SC_STATUS_TIMEOUT_LOAD and its outputs
+                              are incomplete, with no fault and the context
+                              usable.  It exercises the failure path.           */
 } sc_params;
 
 /* Recorded-id flag layouts (sc_params.flag_layout).  SC_FLAGS_ENTRY keeps one
@@ -154,6 +166,24 @@ typedef struct sc_row_diag {
     uint32_t flags;    /* SC_FLAG_* bits                                        */
     uint32_t reserved;
 } sc_row_diag;
+
+/*
+ * The batch loss of a fused call: grad_scale * sum_t diag[t].loss, the docs'
+ * global generated-token reduction ("Score Centering" page, section
+ * "Training": the loss summed over every generated token of the batch and
+ * divided by their number) when grad_scale = 1 / N_tokens.  Its gradient with
+ * respect to the logits is the grad_out of the same call.
+ *
+ * diag     : sc_row_diag [T] written by sc_center_forward_backward (device,
+ *            16-byte aligned); masked and error rows hold loss 0.
+ * loss_out : one FP32 value (device), written.
+ * The sum runs in one fixed order (FP64 partial sums over rows t = i mod 512,
+ * then a pairwise tree), rounded to FP32 once, so repeated calls give the
+ * same bits.  T == 0 writes 0.  Asynchronous on `stream`.
+ * Errors: SC_ERR_SHAPE (T < 0), SC_ERR_NULL, SC_ERR_ARG (grad_scale not
+ * finite), SC_ERR_ALIGN, SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
+ */
+int sc_batch_loss(const sc_row_diag* diag, long long T, float grad_scale, float* loss_out, sc_stream_t stream);
 
 /*
  * Sampler-side capture of the top K behaviour probabilities (docs page
@@ -346,6 +376,33 @@ int sc_center_forward_backward_noalloc(const uint16_t* logits, long long T, int 
  * of 8, block_rows < 1, workspace too small), SC_ERR_CUDA for a cuBLASLt
  * failure (its status in the message).  T == 0 is a no-op.
  */
+/*
+ * Dense bf16 GEMM on the tensor cores: the LM head's three products
+ * (z = H W^T, dH = g W, dW = g^T H) run on it.
+ *
+ *     C[M, N] = A[M, K] . B[K, N]    (FP32 accumulation)
+ *
+ * A       : bf16, a_layout 0: stored [M][K] (K contiguous, row stride lda);
+ *           a_layout 1: stored [K][M] (M contiguous, row stride lda).
+ * B       : bf16, b_layout 0: stored [N][K] (row stride ldb); b_layout 1:
+ *           stored [K][N].
+ * C       : row-major [M][N], row stride ldc; c_mode SC_GEMM_BF16 writes bf16
+ *           (round to nearest even), SC_GEMM_FP32 writes FP32, SC_GEMM_FP32_ADD
+ *           adds the FP32 product to what C holds.
+ * All pointers device, 16-byte aligned; row strides multiples of 16 bytes
+ * and at least the row length.  Sizes 1..2^31.  status_dev (nullable): a
+ * device word into which SC_STATUS_TIMEOUT_LOAD is OR-ed if a wait inside
+ * the kernel ran out.  Asynchronous on `stream`; nothing is allocated.
+ * Errors: SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG,
+ * SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
+ */
+#define SC_GEMM_BF16 0
+#define SC_GEMM_FP32 1
+#define SC_GEMM_FP32_ADD 2
+int sc_gemm_bf16(const uint16_t* A, long long lda, int a_layout, const uint16_t* B, long long ldb, int b_layout,
+                 void* C, long long ldc, int c_mode, long long M, long long N, long long K, uint32_t* status_dev,
+                 sc_stream_t stream);
+
 size_t sc_lmhead_workspace_bytes(long long block_rows, int V);
 int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t* w, long long T, int d, int V,
                                const int32_t* rec_ids, const float* rec_logprobs, const int32_t* rec_count,

@@ -29,7 +29,8 @@ __all__ = [
     "sc_group_advantages", "sc_center_forward_backward", "sc_plan_query", "diag_to_numpy",
     "ScoreCenteredLoss", "score_centered_loss",
     "sc_rollout_mean_advantages", "sc_topk_capture", "SC_IS_NONE", "SC_IS_TIS", "SC_IS_MIS", "SC_IS_CLIP",
-    "WORKSPACE_BYTES", "workspace", "reset_workspaces", "sc_lmhead_forward_backward",
+    "WORKSPACE_BYTES", "workspace", "reset_workspaces", "sc_lmhead_forward_backward", "sc_batch_loss",
+    "sc_gemm_bf16", "GEMM_BF16", "GEMM_FP32", "GEMM_FP32_ADD",
 ]
 
 SC_OK, SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_SHAPE, SC_ERR_ARG, SC_ERR_CUDA, SC_ERR_UNSUPPORTED = range(7)
@@ -50,7 +51,7 @@ FLAG_IS_REJECT = 0x200
 FLAG_CLIPPED = 0x400
 
 # Symbols declared in include/sc.h.
-EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_rollout_mean_advantages", "sc_topk_capture",
+EXPORTS = ["sc_params_default", "sc_group_advantages", "sc_batch_loss", "sc_gemm_bf16", "sc_rollout_mean_advantages", "sc_topk_capture",
            "sc_center_forward_backward", "sc_center_forward_backward_noalloc", "sc_lmhead_workspace_bytes",
            "sc_lmhead_forward_backward", "sc_plan_query",
            "sc_status_string", "sc_last_error", "sc_abi_version"]
@@ -78,6 +79,8 @@ class Params(ctypes.Structure):
         ("clip_low", ctypes.c_float),
         ("clip_high", ctypes.c_float),
         ("flag_layout", ctypes.c_int),
+        ("wait_limit_us", ctypes.c_int),
+        ("test_stall", ctypes.c_int),
     ]
 
 
@@ -111,6 +114,10 @@ def lib():
             L.sc_params_default.restype = i32
             L.sc_group_advantages.argtypes = [vp, i32, i32, i32, f32, vp, vp]
             L.sc_group_advantages.restype = i32
+            L.sc_batch_loss.argtypes = [vp, i64, f32, vp, vp]
+            L.sc_batch_loss.restype = i32
+            L.sc_gemm_bf16.argtypes = [vp, i64, i32, vp, i64, i32, vp, i64, i32, i64, i64, i64, vp, vp]
+            L.sc_gemm_bf16.restype = i32
             L.sc_rollout_mean_advantages.argtypes = [vp, vp, i64, i32, vp, vp, vp]
             L.sc_rollout_mean_advantages.restype = i32
             L.sc_topk_capture.argtypes = [vp, i64, i32, i64, f32, i32, f32, vp, vp, vp, vp]
@@ -147,12 +154,15 @@ def _check(status: int):
 
 def params(K_max=128, is_mode=SC_IS_NONE, tis_max=2.0, mis_min=0.5, mis_max=5.0, centering=True,
            inv_temperature=1.0, grad_scale=1.0, cluster_size=0, threads=0, stages=0, clip_low=0.2,
-           clip_high=0.3, flag_layout=0) -> Params:
+           clip_high=0.3, flag_layout=0, wait_limit_us=0, test_stall=0) -> Params:
     """Defaults are the settings table of the docs' "Score Centering" section
-    and the clip widths of the page's `grpo` preset."""
+    and the clip widths of the page's `grpo` preset.  wait_limit_us: how long
+    a wait inside the fused kernel may take before the launch gives up (0 =
+    1 s); test_stall: the test hook of the C header (0 in normal use)."""
     return Params(int(K_max), int(is_mode), float(tis_max), float(mis_min), float(mis_max),
                   int(bool(centering)), float(inv_temperature), float(grad_scale), int(cluster_size),
-                  int(threads), int(stages), float(clip_low), float(clip_high), int(flag_layout))
+                  int(threads), int(stages), float(clip_low), float(clip_high), int(flag_layout),
+                  int(wait_limit_us), int(test_stall))
 
 
 def _ptr(t):
@@ -335,7 +345,10 @@ def workspace(device, stream=None) -> torch.Tensor:
     with _lock:
         ws = _workspaces.get(key)
         if ws is None:
-            ws = torch.zeros(WORKSPACE_BYTES // 8, dtype=torch.int64, device=dev)
+            # allocated and zeroed on the stream the calls run on, so that the
+            # zero fill is ordered before the first launch that uses it
+            with torch.cuda.stream(stream):
+                ws = torch.zeros(WORKSPACE_BYTES // 8, dtype=torch.int64, device=dev)
             _workspaces[key] = ws
     return ws
 
@@ -344,8 +357,9 @@ def reset_workspaces() -> None:
     """Zero every workspace the binding holds (needed only after a launch that
     did not complete, e.g. a CUDA error)."""
     with _lock:
-        for ws in _workspaces.values():
-            ws.zero_()
+        for (dev_index, stream_ptr), ws in _workspaces.items():
+            with torch.cuda.stream(torch.cuda.ExternalStream(stream_ptr, device=torch.device("cuda", dev_index))):
+                ws.zero_()
 
 
 def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | None,
@@ -408,6 +422,54 @@ def sc_center_forward_backward(logits: torch.Tensor, rec_ids: torch.Tensor | Non
     return grad_out, logp_out, diag_out
 
 
+def sc_batch_loss(diag: torch.Tensor, grad_scale: float, out: torch.Tensor | None = None, stream=None):
+    """grad_scale * sum of the rows' losses of a fused call's diagnostics
+    (int32 [T, 16] on a CUDA device), summed by the library in a fixed order.
+    Returns a float32 [1] device tensor (``out`` when given)."""
+    dev = diag.device
+    if dev.type != "cuda":
+        raise ValueError("diag must be on a CUDA device")
+    _need(diag, "diag", torch.int32, dev, 2)
+    if diag.shape[1] != 16 or not diag.is_contiguous():
+        raise ValueError("diag must be a contiguous int32 [T, 16] tensor")
+    out = torch.empty(1, dtype=torch.float32, device=dev) if out is None else out
+    _need(out, "out", torch.float32, dev)
+    if out.numel() < 1:
+        raise ValueError("out must hold one float32")
+    _check(lib().sc_batch_loss(_ptr(diag), int(diag.shape[0]), float(grad_scale), _ptr(out), _stream(stream)))
+    return out
+
+
+GEMM_BF16, GEMM_FP32, GEMM_FP32_ADD = 0, 1, 2
+
+
+def sc_gemm_bf16(a: torch.Tensor, b: torch.Tensor, c: torch.Tensor, a_kmajor: bool = True, b_kmajor: bool = True,
+                 c_mode: int = GEMM_BF16, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """C = A . B on the tensor cores (the LM head's products).
+
+    a: bf16, [M, K] when ``a_kmajor`` else [K, M]; b: bf16, [N, K] when
+    ``b_kmajor`` else [K, N]; rows contiguous.  c: row-major [M, N], bf16
+    (GEMM_BF16) or float32 (GEMM_FP32: written; GEMM_FP32_ADD: C += A . B).
+    """
+    dev = a.device
+    if dev.type != "cuda":
+        raise ValueError("a must be on a CUDA device")
+    _need(a, "a", torch.bfloat16, dev, 2)
+    _need(b, "b", torch.bfloat16, dev, 2)
+    _need(c, "c", torch.bfloat16 if c_mode == GEMM_BF16 else torch.float32, dev, 2)
+    _need(status, "status", torch.int32, dev, 1)
+    M, K = (a.shape[0], a.shape[1]) if a_kmajor else (a.shape[1], a.shape[0])
+    N, Kb = (b.shape[0], b.shape[1]) if b_kmajor else (b.shape[1], b.shape[0])
+    if Kb != K:
+        raise ValueError(f"inner sizes differ: {K} and {Kb}")
+    if tuple(c.shape[:1]) != (M,) or c.shape[1] < N:
+        raise ValueError(f"c must be [M = {M}, >= N = {N}]")
+    _check(lib().sc_gemm_bf16(_ptr(a), _rows(a, "a"), 0 if a_kmajor else 1, _ptr(b), _rows(b, "b"),
+                              0 if b_kmajor else 1, _ptr(c), _rows(c, "c"), int(c_mode), M, N, K, _ptr(status),
+                              _stream(stream)))
+    return c
+
+
 def sc_plan_query(V: int, p: Params) -> dict:
     """The launch plan the library uses for V on the current device."""
     out = [ctypes.c_int(0) for _ in range(6)]
@@ -427,10 +489,10 @@ class ScoreCenteredLoss(torch.autograd.Function):
     The forward pass is one library launch: it produces the per-row losses and
     the finished gradient with respect to the logits, which is saved.  The
     returned loss is ``grad_scale * sum_t loss_t`` (a token mean when
-    grad_scale = 1 / N_tokens), whose gradient is exactly the saved one; the
-    backward pass returns it scaled by the incoming gradient.  Besides the
-    launch, torch only sums the T row losses and, when the incoming gradient is
-    not 1, scales the saved gradient.  Outputs: (loss, logp [T], diag int32
+    grad_scale = 1 / N_tokens), summed by the library (:func:`sc_batch_loss`),
+    whose gradient is exactly the saved one; the backward pass returns it
+    scaled by the incoming gradient (torch's one multiplication, when the
+    incoming gradient is not 1).  Outputs: (loss, logp [T], diag int32
     [T, 16]); the last two carry no gradient.
     """
 
@@ -443,7 +505,7 @@ class ScoreCenteredLoss(torch.autograd.Function):
             logits.detach(), rec_ids, rec_logprobs, rec_count, sampled_id, rollout_logprob, row_response, adv, p,
             diag_out=diag, stream=stream)
         ctx.save_for_backward(grad)
-        loss = diag.view(torch.float32)[:, 0].sum() * float(np.float32(p.grad_scale))
+        loss = sc_batch_loss(diag, float(np.float32(p.grad_scale)), stream=stream).reshape(())
         ctx.mark_non_differentiable(logp, diag)
         return loss, logp, diag
 
@@ -517,7 +579,8 @@ def sc_lmhead_forward_backward(hidden: torch.Tensor, w: torch.Tensor, rec_ids, r
         with _lock:
             workspace_buf = _lmhead_workspaces.get(key)
             if workspace_buf is None:
-                workspace_buf = torch.zeros(need, dtype=torch.uint8, device=dev)
+                with torch.cuda.stream(s_obj):  # zero fill ordered before the first call on s_obj
+                    workspace_buf = torch.zeros(need, dtype=torch.uint8, device=dev)
                 _lmhead_workspaces[key] = workspace_buf
     if workspace_buf.device != dev or workspace_buf.numel() * workspace_buf.element_size() < need:
         raise ValueError(f"workspace_buf must hold {need} bytes on {dev}")

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libsc_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
-SOURCES = ["sc_center.cu", "sc_topk.cu", "sc_lmhead.cu", "sc_advantages.cu", "sc_common.cu"]
+SOURCES = ["sc_center.cu", "sc_topk.cu", "sc_lmhead.cu", "sc_gemm.cu", "sc_advantages.cu", "sc_common.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

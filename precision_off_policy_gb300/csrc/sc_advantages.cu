@@ -1,5 +1,6 @@
-// sc_advantages.cu -- GRPO group advantages (one warp per group) and the
-// per-rollout mean of the clipped GRPO baseline (advantage / valid tokens).
+// sc_advantages.cu -- GRPO group advantages (one warp per group), the
+// per-rollout mean of the clipped GRPO baseline (advantage / valid tokens),
+// and the batch loss grad_scale * sum_t loss_t of the fused call.
 //
 // Follows the "Training" section of the Agent Lightning "Score Centering"
 // docs page (rollout-level advantages with group standard-deviation
@@ -97,8 +98,47 @@ __global__ void rollout_mean_kernel(const float* adv, const int32_t* counts, int
     }
 }
 
+// The batch loss: grad_scale * sum of the rows' token losses (the first field
+// of each 64-byte diagnostics record), the docs' global generated-token
+// reduction when grad_scale = 1 / N_tokens.  One CTA, so the order of the
+// additions is fixed: thread i sums rows i, i + 512, ... in FP64, then a
+// pairwise tree over the 512 partial sums; one rounding to FP32 at the end.
+constexpr int kLossThreads = 512;
+__global__ void __launch_bounds__(kLossThreads) batch_loss_kernel(const float* diag_words, long long T,
+                                                                  float grad_scale, float* out) {
+    __shared__ double part[kLossThreads];
+    double s = 0.0;
+    for (long long t = threadIdx.x; t < T; t += kLossThreads) s += static_cast<double>(diag_words[16 * t]);
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int h = kLossThreads / 2; h > 0; h >>= 1) {
+        if (static_cast<int>(threadIdx.x) < h) part[threadIdx.x] += part[threadIdx.x + h];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *out = static_cast<float>(static_cast<double>(grad_scale) * part[0]);
+}
+
 }  // namespace
 }  // namespace sc
+
+extern "C" int sc_batch_loss(const sc_row_diag* diag, long long T, float grad_scale, float* loss_out,
+                             sc_stream_t stream) {
+    using namespace sc;
+    if (T < 0) return fail(SC_ERR_SHAPE, "T = %lld < 0", T);
+    if (!loss_out) return fail(SC_ERR_NULL, "loss_out is NULL");
+    if (T > 0 && !diag) return fail(SC_ERR_NULL, "diag is NULL with T > 0");
+    if (!std::isfinite(grad_scale)) return fail(SC_ERR_ARG, "grad_scale must be finite");
+    if (!aligned(diag, 16) || !aligned(loss_out, 4))
+        return fail(SC_ERR_ALIGN, "diag must be 16-byte aligned, loss_out 4-byte aligned");
+    int dev = 0;
+    int st = check_device(&dev);
+    if (st != SC_OK) return st;
+    batch_loss_kernel<<<1, kLossThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float*>(diag), T, grad_scale, loss_out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "batch_loss_kernel launch");
+    return ok();
+}
 
 extern "C" int sc_group_advantages(const float* rewards, int n_groups, int group_size,
                                    int normalize_std, float eps, float* adv_out, sc_stream_t stream) {

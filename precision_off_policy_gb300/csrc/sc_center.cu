@@ -74,7 +74,8 @@ constexpr long long kDynamicShare = 8;  // 1 / (share of the rows handed out at 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTailFloor = 1e-6f;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // default limit of a bounded wait
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // bulk copies in flight before a CTA leaves
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 // One valid row as the producer hands it to the consumers.
@@ -141,6 +142,8 @@ struct KArgs {
     int V, K_max, n_resp;
     int is_mode, centering;
     float tis_max, mis_min, mis_max, inv_t, grad_scale, clip_lo, clip_hi;
+    unsigned long long wait_ns;  // limit of every bounded wait but the final drains of bulk copies
+    int stall;                   // test hook: the first bulk copy of each CTA is left out
     int C, S, ncv, NB;
     Layout L;
 };
@@ -303,6 +306,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     const int nchunks = (nvb + a.ncv - 1) / a.ncv;
     const int cap = L.list_cap, nwords = L.nwords, mwords = L.mwords;
     const float kscale = a.inv_t * kLog2e;
+    const unsigned long long wait_ns = a.wait_ns;
     const uint64_t pol = l2_policy_evict_first();      // last use: gradient stores, write-pass reads
     const uint64_t pol_keep = l2_policy_evict_normal();  // slice copies (measured: evict-first is slower)
 
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     // every CTA has read this slot's previous row (bounded wait)
                     bool ok = true;
                     if (ng >= static_cast<uint32_t>(kGrab))
-                        ok = mbar_wait_cluster_bounded(grab_free(g), ((ng / kGrab) - 1u) & 1u, kWaitLimitNs);
+                        ok = mbar_wait_cluster_bounded(grab_free(g), ((ng / kGrab) - 1u) & 1u, wait_ns);
                     if (!__all_sync(kFull, ok)) {
                         give_up(SC_STATUS_TIMEOUT_LOAD);
                         stop = true;
@@ -426,7 +430,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                                     static_cast<uint32_t>(tg >> 32), map_to_rank(grab_full(g), lane));
                 }
                 if (lane == 0) mbar_expect_tx(grab_full(g), 8u);
-                if (!__all_sync(kFull, mbar_wait_cluster_bounded(grab_full(g), (ng / kGrab) & 1u, kWaitLimitNs))) {
+                if (!__all_sync(kFull, mbar_wait_cluster_bounded(grab_full(g), (ng / kGrab) & 1u, wait_ns))) {
                     give_up(SC_STATUS_TIMEOUT_LOAD);
                     stop = true;
                     break;
@@ -452,7 +456,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             if (zf) {  // zero row: to the zero warp's queue
                 const int z = static_cast<int>(nz % kZq);
                 if (nz >= static_cast<uint32_t>(kZq) &&
-                    !__all_sync(kFull, mbar_wait_bounded(zq_free(z), ((nz / kZq) - 1u) & 1u, kWaitLimitNs))) {
+                    !__all_sync(kFull, mbar_wait_bounded(zq_free(z), ((nz / kZq) - 1u) & 1u, wait_ns))) {
                     give_up(SC_STATUS_TIMEOUT_LOAD);
                     stop = true;
                     break;
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             }
             const int ms = static_cast<int>(nfill % kMetaSlots);
             if (nfill >= static_cast<uint32_t>(kMetaSlots) &&
-                !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs)) {
+                !mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, wait_ns)) {
                 if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                 stop = true;
                 break;
@@ -603,14 +607,17 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
                 for (int i = 0; i < nchunks; ++i) {
                     if (reuse &&
-                        !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, kWaitLimitNs)) {
+                        !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, wait_ns)) {
                         status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                         for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
                             (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
-                                                    kWaitLimitNs);
+                                                    kDrainLimitNs);
                         stop = true;
                         break;
                     }
+                    // test hook: the first chunk of the first row is never copied,
+                    // so every wait for it runs out (the failure path, with no fault)
+                    if (a.stall && nfill == 0u && i == 0) continue;
                     fence_proxy_async_smem();
                     const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
                     const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
@@ -626,7 +633,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             const int z = static_cast<int>(nz % kZq);
             bool ok = true;
             if (nz >= static_cast<uint32_t>(kZq))
-                ok = mbar_wait_bounded(zq_free(z), ((nz / kZq) - 1u) & 1u, kWaitLimitNs);
+                ok = mbar_wait_bounded(zq_free(z), ((nz / kZq) - 1u) & 1u, wait_ns);
             if (__all_sync(kFull, ok) && lane == 0) {
                 zq_t[z] = -1;
                 mbar_arrive(zq_full(z));
@@ -636,7 +643,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             const int ms = static_cast<int>(nfill % kMetaSlots);
             bool ok = true;
             if (nfill >= static_cast<uint32_t>(kMetaSlots))
-                ok = mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, kWaitLimitNs);
+                ok = mbar_wait_bounded(meta_bar(ms, kMetaFree), ((nfill / kMetaSlots) - 1u) & 1u, wait_ns);
             if (ok) {
                 if (lane == 0) {
                     meta[ms].t = -1;
@@ -651,14 +658,15 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             const uint32_t f0 = nfill > static_cast<uint32_t>(NB) ? nfill - NB : 0u;
             for (uint32_t f = f0; f < nfill; ++f)
                 for (int i = 0; i < nchunks; ++i)
-                    (void)mbar_wait_bounded(data_bar(f % NB, kChunkFull + i), (f / NB) & 1u, kWaitLimitNs);
+                    if (!(a.stall && f == 0u && i == 0))  // (the copy the test hook left out)
+                        (void)mbar_wait_bounded(data_bar(f % NB, kChunkFull + i), (f / NB) & 1u, kDrainLimitNs);
         }
         __syncwarp();
     } else if (warp == NCW + 2) {
         // ================= zero warp: zero rows from the producer's queue =================
         for (uint32_t iz = 0;; ++iz) {
             const int z = static_cast<int>(iz % kZq);
-            if (!__all_sync(kFull, mbar_wait_bounded(zq_full(z), (iz / kZq) & 1u, kWaitLimitNs))) {
+            if (!__all_sync(kFull, mbar_wait_bounded(zq_full(z), (iz / kZq) & 1u, wait_ns))) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
             }
@@ -694,7 +702,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             // needs only the slice -- the streaming offset (the same largest logit of
             // the first vectors), the recorded ids' and a's logits, and the recorded
             // ids' sums relative to the larger of that offset and their own maximum ----
-            if (!__all_sync(kFull, mbar_wait_bounded(meta_bar(ms, kMetaFull), (j / kMetaSlots) & 1u, kWaitLimitNs))) {
+            if (!__all_sync(kFull, mbar_wait_bounded(meta_bar(ms, kMetaFull), (j / kMetaSlots) & 1u, wait_ns))) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
             }
@@ -727,7 +735,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 const int ds = static_cast<int>(j % NB);
                 bool landed = true;
                 for (int c = 0; c < nchunks; ++c)
-                    landed = landed && mbar_wait_bounded(data_bar(ds, kChunkFull + c), (j / NB) & 1u, kWaitLimitNs);
+                    landed = landed && mbar_wait_bounded(data_bar(ds, kChunkFull + c), (j / NB) & 1u, wait_ns);
                 if (!__all_sync(kFull, landed)) {
                     give_up(SC_STATUS_TIMEOUT_LOAD);
                     break;
@@ -758,7 +766,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (Mo > -INFINITY) head_sums(Mo * kscale);
             }
             // ---- phase A of row j is done ----
-            const bool got = mbar_wait_bounded(adone(p), (j >> 1) & 1u, kWaitLimitNs);
+            const bool got = mbar_wait_bounded(adone(p), (j >> 1) & 1u, wait_ns);
             if (!__all_sync(kFull, got)) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
@@ -825,7 +833,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 }
             }
             // ---- all C records of row j: the row scalars ----
-            const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j >> 2) & 1u, kWaitLimitNs);
+            const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j >> 2) & 1u, wait_ns);
             if (!__all_sync(kFull, ok)) {
                 give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                 break;
@@ -980,7 +988,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             if (flag_up()) break;
             const int ms = static_cast<int>(i % kMetaSlots);
             const bool got =
-                mbar_wait_bounded(meta_bar(ms, kMetaFull), (i / kMetaSlots) & 1u, kWaitLimitNs);
+                mbar_wait_bounded(meta_bar(ms, kMetaFull), (i / kMetaSlots) & 1u, wait_ns);
             if (!__all_sync(kFull, got)) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
@@ -1026,7 +1034,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 // it again, and the scalar warp took the recorded ids' logits from it.
                 float mz = -INFINITY;
                 if (nchunks > 0) {  // (waits decided warp-wide)
-                    timed_out = !__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, kWaitLimitNs));
+                    timed_out = !__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull), fpar, wait_ns));
                     if (!timed_out && lane < nvb) {
                         const uint4 w = lds128(buf_s + 16u * lane);
                         const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
@@ -1041,7 +1049,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 f2_t S1a = 0ull, S1b = 0ull, S2a = 0ull, S2b = 0ull;
                 float s1x = 0.0f, s2x = 0.0f;  // entries taken one by one
                 for (int c = 0; c < nchunks && !timed_out; ++c) {
-                    if (!__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull + c), fpar, kWaitLimitNs))) {
+                    if (!__all_sync(kFull, mbar_wait_bounded(data_bar(ds, kChunkFull + c), fpar, wait_ns))) {
                         timed_out = true;
                         break;
                     }
@@ -1176,7 +1184,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 const int pp = p;
                 const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
                 uint16_t* grow = a.grad + m.t * a.gstride + lo;
-                const bool ready = mbar_wait_bounded(sready(pp), (ip >> 1) & 1u, kWaitLimitNs);
+                const bool ready = mbar_wait_bounded(sready(pp), (ip >> 1) & 1u, wait_ns);
                 if (!__all_sync(kFull, ready)) {
                     give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                     break;
@@ -1416,6 +1424,9 @@ int check_params(int V, const sc_params* p) {
         return fail(SC_ERR_ARG, "threads = %d is not 0, 128, 256, 384 or 512", p->threads);
     if (p->stages < 0 || p->stages > kMaxStages)
         return fail(SC_ERR_ARG, "stages = %d outside 0..%d", p->stages, kMaxStages);
+    if (p->wait_limit_us < 0 || p->wait_limit_us > 60000000)
+        return fail(SC_ERR_ARG, "wait_limit_us = %d outside 0..60000000", p->wait_limit_us);
+    if (p->test_stall != 0 && p->test_stall != 1) return fail(SC_ERR_ARG, "test_stall must be 0 or 1");
     if (p->flag_layout < 0 || p->flag_layout > SC_FLAGS_VECTOR)
         return fail(SC_ERR_ARG, "flag_layout = %d is not 0, %d or %d", p->flag_layout, SC_FLAGS_ENTRY,
                     SC_FLAGS_VECTOR);
@@ -1479,15 +1490,24 @@ extern "C" int sc_plan_query(int V, const sc_params* p, int* cluster_size, int* 
     return ok();
 }
 
-extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, int V,
-                                          long long logits_stride, const int32_t* rec_ids,
-                                          const float* rec_logprobs, const int32_t* rec_count,
-                                          const int32_t* sampled_id, const float* rollout_logprob,
-                                          const int32_t* row_response, const float* adv, int n_resp,
-                                          const sc_params* p, uint16_t* grad_out, long long grad_stride,
-                                          float* logp_out, sc_row_diag* diag_out, uint32_t* status_dev,
-                                          void* workspace, sc_stream_t stream) {
-    using namespace sc;
+namespace sc {
+namespace {
+
+// A checked call of the fused kernel, ready to launch once it has a workspace.
+struct CenterLaunch {
+    KArgs ka;
+    Plan P;
+    long long G;  // clusters in the grid
+};
+
+// Every host-side check of sc_center_forward_backward (the workspace pointer
+// only when `need_ws`) and the launch plan; writes nothing on the device.
+int center_prepare(const uint16_t* logits, long long T, int V, long long logits_stride, const int32_t* rec_ids,
+                   const float* rec_logprobs, const int32_t* rec_count, const int32_t* sampled_id,
+                   const float* rollout_logprob, const int32_t* row_response, const float* adv, int n_resp,
+                   const sc_params* p, uint16_t* grad_out, long long grad_stride, float* logp_out,
+                   sc_row_diag* diag_out, uint32_t* status_dev, const void* workspace, bool need_ws,
+                   CenterLaunch* out) {
     int st = check_params(V, p);
     if (st != SC_OK) return st;
     if (T < 0) return fail(SC_ERR_SHAPE, "T = %lld < 0", T);
@@ -1496,8 +1516,8 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
         return fail(SC_ERR_SHAPE, "row strides (%lld, %lld) must be >= V = %d", logits_stride, grad_stride, V);
     if (p->is_mode != SC_IS_NONE && !rollout_logprob)
         return fail(SC_ERR_NULL, "is_mode tis/mis needs rollout_logprob");
-    if (T == 0) return ok();
-    if (!logits || !sampled_id || !row_response || !grad_out || !logp_out || !workspace)
+    if (T == 0) return SC_OK;
+    if (!logits || !sampled_id || !row_response || !grad_out || !logp_out || (need_ws && !workspace))
         return fail(SC_ERR_NULL, "logits, sampled_id, row_response, grad_out, logp_out and workspace are required");
     if (n_resp > 0 && !adv) return fail(SC_ERR_NULL, "adv is NULL with n_resp > 0");
     if (p->K_max > 0 && (!rec_ids || !rec_logprobs))
@@ -1520,7 +1540,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
         if (!same && l0 < g0 + gb && g0 < l0 + lb)
             return fail(SC_ERR_ARG, "grad_out overlaps logits other than exactly (in place)");
     }
-    Plan P;
+    Plan& P = out->P;
     // the shape checks of the requested (or per-entry automatic) plan need no device
     st = make_plan(V, p->K_max, p->cluster_size, p->threads, p->stages, p->flag_layout == SC_FLAGS_VECTOR, &P);
     if (st != SC_OK) return st;
@@ -1531,11 +1551,12 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     st = plan_for(dev, V, p, &P, &mc);
     if (st != SC_OK) return st;
     const long long G = T < mc ? T : mc;
+    out->G = G;
     // About the last eighth of the rows are handed out at run time (the rest,
     // rounded down to a multiple of the clusters, are dealt round robin).
     const long long T_static = (T - (T + kDynamicShare - 1) / kDynamicShare) / G * G;
 
-    KArgs ka;
+    KArgs& ka = out->ka;
     std::memset(&ka, 0, sizeof ka);
     ka.logits = logits;
     ka.ids = rec_ids;
@@ -1549,7 +1570,7 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.logp = logp_out;
     ka.diag = diag_out;
     ka.status = status_dev;
-    ka.ws = static_cast<unsigned long long*>(workspace);
+    ka.ws = nullptr;
     ka.T_static = T_static;
     ka.T = T;
     ka.lstride = logits_stride;
@@ -1566,17 +1587,24 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     ka.grad_scale = p->grad_scale;
     ka.clip_lo = 1.0f - p->clip_low;
     ka.clip_hi = 1.0f + p->clip_high;
+    ka.wait_ns = p->wait_limit_us > 0 ? 1000ull * static_cast<unsigned long long>(p->wait_limit_us) : kWaitLimitNs;
+    ka.stall = p->test_stall;
     ka.C = P.C;
     ka.S = P.S;
     ka.ncv = P.ncv;
     ka.NB = P.NB;
     ka.L = P.L;
+    return SC_OK;
+}
 
+int center_launch(CenterLaunch& cl, void* workspace, cudaStream_t stream) {
+    const Plan& P = cl.P;
+    cl.ka.ws = static_cast<unsigned long long*>(workspace);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(G * P.C), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(cl.G * P.C), 1, 1);
     cfg.blockDim = dim3(P.NC + 96, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
-    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = P.C;
@@ -1588,9 +1616,30 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NC, P.VF), ka);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(P.NC, P.VF), cl.ka);
     if (e != cudaSuccess) return cuda_fail(e, "center_kernel launch");
     return ok();
+}
+
+}  // namespace
+}  // namespace sc
+
+extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, int V,
+                                          long long logits_stride, const int32_t* rec_ids,
+                                          const float* rec_logprobs, const int32_t* rec_count,
+                                          const int32_t* sampled_id, const float* rollout_logprob,
+                                          const int32_t* row_response, const float* adv, int n_resp,
+                                          const sc_params* p, uint16_t* grad_out, long long grad_stride,
+                                          float* logp_out, sc_row_diag* diag_out, uint32_t* status_dev,
+                                          void* workspace, sc_stream_t stream) {
+    using namespace sc;
+    CenterLaunch cl;
+    const int st = center_prepare(logits, T, V, logits_stride, rec_ids, rec_logprobs, rec_count, sampled_id,
+                                  rollout_logprob, row_response, adv, n_resp, p, grad_out, grad_stride, logp_out,
+                                  diag_out, status_dev, workspace, true, &cl);
+    if (st != SC_OK) return st;
+    if (T == 0) return ok();
+    return center_launch(cl, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---- the same call for callers that cannot allocate -----------------------
@@ -1605,12 +1654,8 @@ extern "C" int sc_center_forward_backward(const uint16_t* logits, long long T, i
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
 // Room for the workspace of one call (SC_WORKSPACE_BYTES); every call shares it.
 static __device__ __align__(256) unsigned char g_center_scratch[256];
-
-std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kNoAllocMaxDevices] = {};  // device address of g_center_scratch, per device
 
 }  // namespace
 
@@ -1628,34 +1673,22 @@ extern "C" int sc_center_forward_backward_noalloc(const uint16_t* logits, long l
     if (SC_WORKSPACE_BYTES > static_cast<int>(sizeof(g_center_scratch)))
         return fail(SC_ERR_SHAPE, "the workspace (%d bytes) exceeds the library's scratch array (%d bytes)",
                     SC_WORKSPACE_BYTES, static_cast<int>(sizeof(g_center_scratch)));
-    if (T == 0) return sc_center_forward_backward(logits, T, V, logits_stride, rec_ids, rec_logprobs, rec_count,
-                                                  sampled_id, rollout_logprob, row_response, adv, n_resp, p,
-                                                  grad_out, grad_stride, logp_out, diag_out, status_dev,
-                                                  nullptr, stream);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kNoAllocMaxDevices)
-        return fail(SC_ERR_UNSUPPORTED, "device %d is beyond the %d devices this entry point serves", dev,
-                    kNoAllocMaxDevices);
+    // every argument is checked before the array is touched
+    CenterLaunch cl;
+    const int st = center_prepare(logits, T, V, logits_stride, rec_ids, rec_logprobs, rec_count, sampled_id,
+                                  rollout_logprob, row_response, adv, n_resp, p, grad_out, grad_stride, logp_out,
+                                  diag_out, status_dev, nullptr, false, &cl);
+    if (st != SC_OK) return st;
+    if (T == 0) return ok();
+    // The array's device address on the current device (the array's name in
+    // host code is only a stand-in for it).  Looked up on every call: it is a
+    // table lookup after the first, and stays right if the module was reloaded.
     void* scratch = nullptr;
-    {
-        // First call on a device: look up the array's device address there (the
-        // array's name in host code is only a stand-in for it).
-        std::lock_guard<std::mutex> lock(g_scratch_mutex);
-        if (!g_scratch_ptr[dev]) {
-            void* ptr = nullptr;
-            e = cudaGetSymbolAddress(&ptr, g_center_scratch);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-            g_scratch_ptr[dev] = ptr;
-        }
-        scratch = g_scratch_ptr[dev];
-    }
+    cudaError_t e = cudaGetSymbolAddress(&scratch, g_center_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
     // The row counter must start at zero: clear it in stream order (the array
     // keeps whatever the previous call, or a failed one, left in it).
     e = cudaMemsetAsync(scratch, 0, SC_WORKSPACE_BYTES, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch)");
-    return sc_center_forward_backward(logits, T, V, logits_stride, rec_ids, rec_logprobs, rec_count, sampled_id,
-                                      rollout_logprob, row_response, adv, n_resp, p, grad_out, grad_stride, logp_out,
-                                      diag_out, status_dev, scratch, stream);
+    return center_launch(cl, scratch, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -83,6 +83,8 @@ int sc_params_default(sc_params* p) {
     p->clip_low = 0.2f;
     p->clip_high = 0.3f;
     p->flag_layout = 0;
+    p->wait_limit_us = 0;
+    p->test_stall = 0;
     return sc::ok();
 }
 
@@ -101,6 +103,6 @@ const char* sc_status_string(int status) {
 
 const char* sc_last_error(void) { return sc::last_error_text(); }
 
-int sc_abi_version(void) { return 103; }
+int sc_abi_version(void) { return 104; }
 
 }  // extern "C"

@@ -1,0 +1,499 @@
+// sc_gemm.cu -- dense bf16 GEMM on the fifth-generation tensor cores (tcgen05),
+// the building block of the LM head's three products (z = H W^T, dH = g W,
+// dW = g^T H).
+//
+//   C[M, N] = A[M, K] . B[K, N]      (FP32 accumulation in tensor memory)
+//
+// A is stored either K-major ([M][K], K contiguous) or M-major ([K][M]); B
+// either K-major ([N][K]) or N-major ([K][N]).  C is row-major [M][N] and is
+// written as bf16 (round to nearest even), as FP32, or added in FP32 to what C
+// already holds (a reduce-add performed by the TMA engine in L2).
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+// * warp 0, one thread: the TMA producer.  For every K step of 64 it loads
+//   the A tile (128 x 64) and the B tile (256 x 64) into one of four
+//   shared-memory stages with 2-D tensor copies in the 128-byte swizzled
+//   layout the tensor cores read, and signals the stage's mbarrier with the
+//   bytes in flight.
+// * warp 1: allocates the 512 tensor-memory columns (two 128 x 256 FP32
+//   accumulators); one thread issues the tcgen05.mma instructions (four of
+//   K = 16 per stage) and commits each stage back to the producer and each
+//   finished accumulator to the epilogue.
+// * warps 2-5: the epilogue.  Each warp owns 32 accumulator rows (the
+//   tensor-memory lanes its warp index selects); it reads 32 or 64 columns at
+//   a time with tcgen05.ld, converts them, writes them to a swizzled 4 KiB
+//   staging buffer and stores (or reduce-adds) them with a TMA tensor store,
+//   double-buffered, and hands the accumulator back as soon as it is read, so
+//   the next tile's MMAs overlap this tile's stores.
+// Every wait is bounded (about 1 s of %globaltimer); on expiry the kernel
+// sets a status bit, stops issuing work, lets the copies and MMAs it started
+// complete and frees its tensor memory before it returns.
+#include <cuda.h>
+
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "sc_device.cuh"
+#include "sc_internal.h"
+
+namespace sc {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;             // 16 KiB
+constexpr int kBBytes = BN * BK * 2;             // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;   // 48 KiB
+constexpr int kEpiBuf = 32 * 128;                // one warp's staging buffer: 32 rows x 128 B
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer, MMA, four epilogue warps
+constexpr int kTmemCols = 512;                   // two accumulators of BN FP32 columns
+constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * 2 * kEpiBuf;
+constexpr int kSmemBars = 256;
+constexpr int kSmemTotal = kSmemData + kSmemBars + 1024;  // + alignment slack
+constexpr unsigned long long kWaitNs = 1000000000ull;
+constexpr uint32_t kStatusTimeout = 0x2u;         // SC_STATUS_TIMEOUT_LOAD
+
+static_assert(kSmemTotal <= 232448, "shared memory per CTA");
+
+struct GemmArgs {
+    long long M, N, K;
+    int num_m, num_n, k_steps;
+    long long tiles;
+    int a_mn, b_mn;   // operand majorness: 0 K-major, 1 M- / N-major
+    int c_mode;       // 0 bf16 store, 1 FP32 store, 2 FP32 reduce-add
+    int m_fastest;    // tile order: consecutive tiles share their B tile (1) or their A tile (0)
+    uint32_t idesc;   // tcgen05 instruction descriptor
+    uint32_t* status;
+};
+
+// ---- tcgen05 / TMA tensor helpers -------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most one committed store group may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// D[tmem] (+)= A[smem] . B[smem], kind::f16 (bf16 inputs, FP32 accumulator).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+// 32 consecutive FP32 columns of this warp's 32 lanes: one row per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Shared-memory matrix descriptor of a tile in the 128-byte swizzled layout
+// (start, leading and stride byte offsets in 16-byte units; version 1;
+// layout type 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Descriptor of the K = 16 slice kk (0..3) of a stage's operand tile.
+// K-major: rows of 64 elements (128 B), 8-row groups 1024 B apart; the slice
+// starts 32 B further along the row.  M-/N-major: 64-element blocks of the
+// M (N) extent 8 KiB apart (one TMA box of 64 K rows each), 8-row groups of K
+// 1024 B apart; the slice starts 16 rows (2 KiB) further down.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, int kk) {
+    return mn_major ? smem_desc(base + 2048u * kk, 8192u, 1024u) : smem_desc(base + 32u * kk, 16u, 1024u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUtensorMap tmA,
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // the swizzled layouts repeat every 1024 B
+    unsigned char* sbase = smem_raw + (base - raw);
+    const uint32_t stage0 = base;
+    const uint32_t epi0 = base + kStages * kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + kSmemData);
+    // bars: full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
+    auto full = [&](int s) { return smem_addr(&bars[s]); };
+    auto empty = [&](int s) { return smem_addr(&bars[kStages + s]); };
+    auto acc_full = [&](int a) { return smem_addr(&bars[2 * kStages + a]); };
+    auto acc_empty = [&](int a) { return smem_addr(&bars[2 * kStages + 2 + a]); };
+    const uint32_t drain = smem_addr(&bars[2 * kStages + 4]);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + kSmemData + 128);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + kSmemData + 136);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full(s), 1u);
+            mbar_init(empty(s), 1u);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full(a), 1u);
+            mbar_init(acc_empty(a), static_cast<uint32_t>(kEpiWarps));
+        }
+        mbar_init(drain, 1u);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto give_up = [&]() {
+        if (g.status) atomicOr(g.status, kStatusTimeout);
+        *abort_flag = 1;
+    };
+    auto tile_coords = [&](long long t, int& mt, int& nt) {
+        if (g.m_fastest) {
+            mt = static_cast<int>(t % g.num_m);
+            nt = static_cast<int>(t / g.num_m);
+        } else {
+            nt = static_cast<int>(t % g.num_n);
+            mt = static_cast<int>(t / g.num_n);
+        }
+    };
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            uint32_t it = 0;  // stages issued
+            for (long long t = blockIdx.x; t < g.tiles && !*abort_flag; t += gridDim.x) {
+                int mt, nt;
+                tile_coords(t, mt, nt);
+                const int m0 = mt * BM, n0 = nt * BN;
+                for (int ks = 0; ks < g.k_steps; ++ks, ++it) {
+                    const int s = static_cast<int>(it % kStages);
+                    if (it >= static_cast<uint32_t>(kStages) &&
+                        !mbar_wait_bounded(empty(s), ((it / kStages) - 1u) & 1u, kWaitNs)) {
+                        give_up();
+                        break;
+                    }
+                    const uint32_t sa = stage0 + s * kStageBytes, sb = sa + kABytes;
+                    mbar_expect_tx(full(s), static_cast<uint32_t>(kStageBytes));
+                    const int k0 = ks * BK;
+                    if (g.a_mn) {
+                        tma_load_2d(sa, &tmA, m0, k0, full(s));
+                        tma_load_2d(sa + 8192u, &tmA, m0 + 64, k0, full(s));
+                    } else {
+                        tma_load_2d(sa, &tmA, k0, m0, full(s));
+                    }
+                    if (g.b_mn) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) tma_load_2d(sb + 8192u * j, &tmB, n0 + 64 * j, k0, full(s));
+                    } else {
+                        tma_load_2d(sb, &tmB, k0, n0, full(s));
+                    }
+                }
+            }
+            // copies in flight land before the CTA can leave
+            const uint32_t first = it > static_cast<uint32_t>(kStages) ? it - kStages : 0u;
+            for (uint32_t j = first; j < it; ++j)
+                (void)mbar_wait_bounded(full(static_cast<int>(j % kStages)), (j / kStages) & 1u, kWaitNs);
+        }
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            uint32_t it = 0, lt = 0;  // stages consumed, local tiles
+            bool ok = true;
+            for (long long t = blockIdx.x; t < g.tiles && ok && !*abort_flag; t += gridDim.x, ++lt) {
+                const int acc = static_cast<int>(lt & 1u);
+                if (lt >= 2u && !mbar_wait_bounded(acc_empty(acc), ((lt >> 1) - 1u) & 1u, kWaitNs)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
+                for (int ks = 0; ks < g.k_steps; ++ks, ++it) {
+                    const int s = static_cast<int>(it % kStages);
+                    if (!mbar_wait_bounded(full(s), (it / kStages) & 1u, kWaitNs)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = stage0 + s * kStageBytes, sb = sa + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc_mma(d, operand_desc(sa, g.a_mn, kk), operand_desc(sb, g.b_mn, kk), g.idesc,
+                               (ks | kk) != 0 ? 1u : 0u);
+                    tc_commit(empty(s));  // the stage is free once these MMAs have read it
+                }
+                if (ok) tc_commit(acc_full(acc));
+            }
+            // every MMA issued has completed before the tensor memory is freed
+            tc_commit(drain);
+            (void)mbar_wait_bounded(drain, 0u, kWaitNs);
+        }
+    } else {
+        // ================= epilogue: tensor memory -> global =================
+        const int q = warp & 3;  // tensor-memory lanes 32q .. 32q + 31
+        const uint32_t buf0 = epi0 + static_cast<uint32_t>((warp - 2) * 2 * kEpiBuf);
+        const int cols = g.c_mode == 0 ? 64 : 32;  // columns per 128-byte staging row
+        const int nchunks = BN / cols;
+        uint32_t lt = 0, nst = 0;
+        for (long long t = blockIdx.x; t < g.tiles; t += gridDim.x, ++lt) {
+            const int acc = static_cast<int>(lt & 1u);
+            // (the decision to leave is taken warp-wide: the loads below are .sync.aligned)
+            const bool got = mbar_wait_bounded(acc_full(acc), (lt >> 1) & 1u, kWaitNs);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                if (lane == 0) give_up();
+                break;
+            }
+            tc_fence_after();
+            int mt, nt;
+            tile_coords(t, mt, nt);
+            const long long r0 = static_cast<long long>(mt) * BM + 32 * q;
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * BN);
+            for (int c = 0; c < nchunks; ++c) {
+                const long long c0 = static_cast<long long>(nt) * BN + c * cols;
+                if (r0 >= g.M || c0 >= g.N) break;  // (chunks are in column order)
+                uint32_t v[64];
+                uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                tmem_ld32(tbase + static_cast<uint32_t>(c * cols), lo);
+                if (cols == 64) tmem_ld32(tbase + static_cast<uint32_t>(c * cols + 32), hi);
+                tmem_ld_wait();
+                const uint32_t buf = buf0 + static_cast<uint32_t>((nst & 1u) * kEpiBuf);
+                if (lane == 0) bulk_wait_read_le1();  // the store that used this buffer has read it
+                __syncwarp();
+                const uint32_t row = buf + 128u * lane;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t w0, w1, w2, w3;
+                    if (cols == 64) {  // eight bf16 per 16-byte chunk, round to nearest even
+                        w0 = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                        w1 = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                        w2 = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                        w3 = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                    } else {
+                        w0 = v[4 * j + 0];
+                        w1 = v[4 * j + 1];
+                        w2 = v[4 * j + 2];
+                        w3 = v[4 * j + 3];
+                    }
+                    sts128(row + 16u * static_cast<uint32_t>(j ^ (lane & 7)), w0, w1, w2, w3);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    if (g.c_mode == 2)
+                        tma_reduce_add_2d(&tmC, static_cast<int>(c0), static_cast<int>(r0), buf);
+                    else
+                        tma_store_2d(&tmC, static_cast<int>(c0), static_cast<int>(r0), buf);
+                    bulk_commit_group();
+                }
+                ++nst;
+            }
+            // the accumulator is read: the MMAs of a later tile may use it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(acc));
+        }
+        if (lane == 0) bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_gemm_mutex;
+EncodeTiledFn g_encode = nullptr;
+std::map<int, int> g_gemm_attr;  // device -> attributes set
+std::map<int, int> g_sm_count;   // device -> SMs
+
+int encoder(EncodeTiledFn* out) {
+    std::lock_guard<std::mutex> lock(g_gemm_mutex);
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+        if (q != cudaDriverEntryPointSuccess || !fn)
+            return fail(SC_ERR_UNSUPPORTED, "the driver has no cuTensorMapEncodeTiled");
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = g_encode;
+    return SC_OK;
+}
+
+// 2-D tensor map of a row-major matrix [rows][cols] (cols contiguous, row
+// stride `ld` elements), boxes of box_cols x box_rows, 128-byte swizzle.
+int make_map(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, CUtensorMapDataType dt, int esize,
+             long long rows, long long cols, long long ld, int box_cols, int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * static_cast<cuuint64_t>(esize)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(SC_ERR_ARG, "cuTensorMapEncodeTiled failed (%d) for a %lld x %lld matrix, row stride %lld",
+                    static_cast<int>(r), rows, cols, ld);
+    return SC_OK;
+}
+
+// tcgen05 instruction descriptor, kind::f16: FP32 accumulator, bf16 A and B,
+// operand majorness, N / 8 and M / 16.
+uint32_t instr_desc(int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+           (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+}  // namespace
+
+int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, long long ldb, int b_mn, void* C,
+              long long ldc, int c_mode, long long M, long long N, long long K, int m_fastest, uint32_t* status,
+              cudaStream_t stream) {
+    if (M < 1 || N < 1 || K < 1) return fail(SC_ERR_SHAPE, "GEMM sizes M=%lld N=%lld K=%lld must be >= 1", M, N, K);
+    if (M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31))
+        return fail(SC_ERR_SHAPE, "GEMM sizes must be below 2^31");
+    if (c_mode < 0 || c_mode > 2) return fail(SC_ERR_ARG, "c_mode = %d", c_mode);
+    if (!A || !B || !C) return fail(SC_ERR_NULL, "A, B and C are required");
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(status, 4))
+        return fail(SC_ERR_ALIGN, "A, B and C must be 16-byte aligned");
+    const int cesize = c_mode == 0 ? 2 : 4;
+    if (lda % 8 || ldb % 8 || (ldc * cesize) % 16)
+        return fail(SC_ERR_ALIGN, "row strides must be multiples of 16 bytes");
+    if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N)
+        return fail(SC_ERR_SHAPE, "a row stride is shorter than its row");
+    EncodeTiledFn enc = nullptr;
+    int st = encoder(&enc);
+    if (st != SC_OK) return st;
+    CUtensorMap ta, tb, tc;
+    st = a_mn ? make_map(enc, &ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, M, lda, 64, 64)
+              : make_map(enc, &ta, A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, K, lda, 64, BM);
+    if (st != SC_OK) return st;
+    st = b_mn ? make_map(enc, &tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, ldb, 64, 64)
+              : make_map(enc, &tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, ldb, 64, BN);
+    if (st != SC_OK) return st;
+    st = c_mode == 0 ? make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, ldc, 64, 32)
+                     : make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32, 32);
+    if (st != SC_OK) return st;
+    int dev = 0;
+    st = check_device(&dev);
+    if (st != SC_OK) return st;
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_gemm_mutex);
+        if (!g_gemm_attr.count(dev)) {
+            const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(gemm_kernel),
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm smem)");
+            int n = 0;
+            const cudaError_t e2 = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            if (e2 != cudaSuccess) return cuda_fail(e2, "cudaDeviceGetAttribute(SMs)");
+            g_sm_count[dev] = n;
+            g_gemm_attr[dev] = 1;
+        }
+        sms = g_sm_count[dev];
+    }
+    GemmArgs ga;
+    std::memset(&ga, 0, sizeof ga);
+    ga.M = M;
+    ga.N = N;
+    ga.K = K;
+    ga.num_m = static_cast<int>((M + BM - 1) / BM);
+    ga.num_n = static_cast<int>((N + BN - 1) / BN);
+    ga.k_steps = static_cast<int>((K + BK - 1) / BK);
+    ga.tiles = static_cast<long long>(ga.num_m) * ga.num_n;
+    ga.a_mn = a_mn ? 1 : 0;
+    ga.b_mn = b_mn ? 1 : 0;
+    ga.c_mode = c_mode;
+    ga.m_fastest = m_fastest ? 1 : 0;
+    ga.idesc = instr_desc(ga.a_mn, ga.b_mn);
+    ga.status = status;
+    const long long grid = ga.tiles < sms ? ga.tiles : sms;
+    gemm_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemTotal, stream>>>(ga, ta, tb, tc);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "gemm_kernel launch");
+    return SC_OK;
+}
+
+}  // namespace sc
+
+extern "C" int sc_gemm_bf16(const uint16_t* A, long long lda, int a_layout, const uint16_t* B, long long ldb,
+                            int b_layout, void* C, long long ldc, int c_mode, long long M, long long N, long long K,
+                            uint32_t* status_dev, sc_stream_t stream) {
+    using namespace sc;
+    if (a_layout != 0 && a_layout != 1) return fail(SC_ERR_ARG, "a_layout = %d", a_layout);
+    if (b_layout != 0 && b_layout != 1) return fail(SC_ERR_ARG, "b_layout = %d", b_layout);
+    const int st = gemm_bf16(A, lda, a_layout, B, ldb, b_layout, C, ldc, c_mode, M, N, K, 1, status_dev,
+                             reinterpret_cast<cudaStream_t>(stream));
+    if (st != SC_OK) return st;
+    return ok();
+}

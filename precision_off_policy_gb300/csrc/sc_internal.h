@@ -19,6 +19,15 @@ int cuda_fail(cudaError_t e, const char* what);
 // Caches the answer per device.  Returns SC_OK or an error status.
 int check_device(int* device_out);
 
+// C[M, N] = A . B on the tensor cores (sc_gemm.cu): A [M][K] (a_mn = 0) or
+// [K][M] (a_mn = 1), B [N][K] (b_mn = 0) or [K][N] (b_mn = 1), bf16; C
+// row-major, c_mode 0 bf16, 1 FP32, 2 FP32 added to C.  m_fastest orders the
+// output tiles so that consecutive ones share B's tile (1) or A's (0).
+// Checks its arguments; returns SC_OK or an error status (no message reset).
+int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, long long ldb, int b_mn, void* C,
+              long long ldc, int c_mode, long long M, long long N, long long K, int m_fastest, uint32_t* status,
+              cudaStream_t stream);
+
 inline bool aligned(const void* p, unsigned a) {
     return (reinterpret_cast<unsigned long long>(p) % a) == 0;
 }

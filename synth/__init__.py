@@ -27,6 +27,11 @@ of the five workload configurations:
   recorded count per row is U{1..128} (capped by the nucleus size); 5% of
   sampled tokens are drawn outside the recorded ids; rewards {0, 1} with one
   all-ones and one all-zeros group.
+* C2R the quick-check batch where the trainer's policy sits on the sampler's
+  recorded ids: after the sampler's top-K is recorded, the trainer logits of
+  the recorded ids are raised by U[10, 30] per row (then rounded to bf16),
+  so the trainer's unrecorded mass falls to about e^-10 .. e^-30 while the
+  sampler's stays where it was.
 
 The sampler distribution mu is softmax((trainer logits + noise) / T_s) in
 FP32; the recorded ids are mu's top-K with FP32 log mu (their sum stays
@@ -44,7 +49,7 @@ BASE = dict(
     n_prompts=2, n_per_prompt=4, L_pad=8, len_lo=None, len_hi=None, V=1024, K=128,
     logits="normal", sigma=2.0, zipf=0.0, sigma_s=0.05, temperature=1.0, top_p=1.0,
     k_uniform=False, p_outside=0.0, p_reward=0.5, force_zero_frac=0.0, force_equal_groups=0,
-    chunk_rows=None, seed=1,
+    chunk_rows=None, head_boost=None, seed=1,
 )
 
 CONFIGS = {
@@ -58,6 +63,11 @@ CONFIGS = {
     "C5": dict(BASE, n_prompts=8, n_per_prompt=8, L_pad=1024, V=151936, sigma=3.0, zipf=1.1,
                temperature=0.7, top_p=0.95, k_uniform=True, p_outside=0.05, force_equal_groups=2,
                seed=5),
+    # The quick-check batch with a trainer that has moved almost all of its
+    # mass onto the sampler's recorded ids: 1 - P_H far below 1e-6 on most
+    # rows while the sampler's own tail 1 - Q_H stays large.
+    "C2R": dict(BASE, L_pad=512, len_lo=64, len_hi=512, V=151936, sigma=3.0, zipf=1.1, p_reward=0.3,
+                head_boost=(10.0, 30.0), seed=12),
 }
 
 
@@ -204,6 +214,14 @@ def make_batch(cfg, chunk: int = 0, device="cpu", row_block: int = 1024) -> dict
             rec_count[b0:b1] = cnt.to(torch.int32)
         else:
             cnt = torch.full((nb,), K, device=device)
+        if cfg["head_boost"] is not None:
+            # the trainer's logits of the recorded ids raised by a per-row amount
+            lo_b, hi_b = cfg["head_boost"]
+            boost = lo_b + (hi_b - lo_b) * torch.rand(nb, generator=g, device=device)
+            pos = (torch.arange(K, device=device)[None, :] < cnt[:, None]).float()
+            zb = z.float().scatter_add_(1, top_id, pos * boost[:, None])
+            logits[b0:b1] = zb.to(torch.bfloat16)
+            del zb, pos
         if cfg["p_outside"] > 0:
             in_head = torch.zeros(nb, V, dtype=torch.bool, device=device)
             pos = torch.arange(K, device=device)[None, :] < cnt[:, None]

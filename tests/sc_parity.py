@@ -6,10 +6,10 @@ gives none):
 * gradient elements: |g_gpu - g_oracle| <= 1 bf16 ulp of g_oracle + 1e-7
   (times |grad_scale| when a scale other than 1 is used);
 * log p_a: |delta| <= 1e-4;
-* row sums: the FP32 sum of the kernel's gradient row before rounding is
-  within 1e-3 |A| (scaled) of zero; the bf16 output row sums to within
-  1e-3 |A| plus half an ulp per element (rounding alone can exceed the bare
-  bound on flat rows);
+* row sums: the bf16 output row sums to within 1e-3 |A| (scaled) plus half
+  an ulp per element (rounding alone can exceed the bare bound on flat
+  rows); the kernel's FP32 sum before rounding to within 1e-3 |A| max(1,
+  rho), a bound on FP32 rounding derived in `fp32_row_sum_bound`;
 * diagnostics: relative 1e-4 with small absolute floors, as listed in
   `check_diag`.
 
@@ -156,12 +156,50 @@ def check_diag(d: np.ndarray, o: np.ndarray, p: sc.Params, what: str, d_or=None)
     np.testing.assert_allclose(dv["is_weight"], ov["is_weight"], rtol=1e-3, atol=1e-7, err_msg=f"{what}: is_weight")
 
 
+def fp32_row_sum_bound(o: np.ndarray, p: sc.Params) -> np.ndarray:
+    """Bound on the kernel's FP32 row sum (diag field `row_sum`).
+
+    The kernel forms it as the sum of the values its write pass stores,
+    beta p_v on every entry, plus, for the recorded ids and the sampled token,
+    the difference between their own gradient and beta p_v.  Those terms add
+    up to at most |a| (s + 1 + Q_H + rho P_H) <= 5 |a| max(1, rho) in absolute
+    value (a = grad_scale A_w / T, s <= 1 + rho), and FP32 rounding of the
+    terms (each exponent argument rounded once, at most 2^-24 |y| with |y| <=
+    64 in the bits that matter) and of the summation tree (at most a few
+    hundred additions deep for any launch plan) stays below 400 * 2^-24 of
+    that sum: under 1.2e-4 |a| max(1, rho).  The check uses 1e-3 |a|
+    max(1, rho).  When rho >> 1 (the trainer's tail mass clamped at 1e-6)
+    beta = -a s is of order a rho and the cancellation between the write
+    pass's sum and the corrections is real; the bf16 output itself holds the
+    patched values and needs no rho (see check_row_sums)."""
+    a = np.abs(o["adv"] * o["is_weight"]) * abs(float(np.float32(p.grad_scale))) * float(np.float32(p.inv_temperature))
+    return 1e-3 * a * np.maximum(1.0, o["rho"]) + 1e-7
+
+
+def bf16_row_sum_allowance(g: np.ndarray) -> np.ndarray:
+    """Half a bf16 ulp per nonzero element: the most round-to-nearest-even can
+    move a row's sum."""
+    return 0.5 * ulp_bf16(g).sum(axis=1) * (np.abs(g) > 0).any(axis=1)
+
+
 def check_row_sums(g: np.ndarray, d: np.ndarray, o: np.ndarray, p: sc.Params, what: str):
-    coef = np.abs(o["adv"] * o["is_weight"]) * abs(float(np.float32(p.grad_scale))) * float(np.float32(p.inv_temperature))
-    coef = coef * np.maximum(1.0, o["rho"])
-    assert np.all(np.abs(d["row_sum"]) <= 1e-3 * coef + 1e-7), f"{what}: FP32 row sum"
-    half_ulp = 0.5 * ulp_bf16(g).sum(axis=1) * (np.abs(g) > 0).any(axis=1)
-    assert np.all(np.abs(g.sum(axis=1)) <= 1e-3 * coef + half_ulp + 1e-7), f"{what}: bf16 row sum"
+    """Every gradient row sums to zero.  The FP32 row sum the kernel reports is
+    held to fp32_row_sum_bound; the bf16 output row to the target 1e-3 |a|
+    (a = grad_scale A_w / T) plus the rounding allowance, with no rho factor:
+    its entries sum to at most 4 |a| in absolute value in every regime."""
+    assert np.all(np.abs(d["row_sum"]) <= fp32_row_sum_bound(o, p)), f"{what}: FP32 row sum"
+    a = np.abs(o["adv"] * o["is_weight"]) * abs(float(np.float32(p.grad_scale))) * float(np.float32(p.inv_temperature))
+    assert np.all(np.abs(g.sum(axis=1)) <= 1e-3 * a + bf16_row_sum_allowance(g) + 1e-7), f"{what}: bf16 row sum"
+
+
+def bare_row_sum_fraction(g: np.ndarray, o: np.ndarray, p: sc.Params) -> float:
+    """Fraction of the rows with a nonzero advantage whose bf16 output sums to
+    within the bare 1e-3 |a|, with no rounding allowance."""
+    a = np.abs(o["adv"] * o["is_weight"]) * abs(float(np.float32(p.grad_scale))) * float(np.float32(p.inv_temperature))
+    live = a > 0
+    if not live.any():
+        return 1.0
+    return float(np.mean(np.abs(g.sum(axis=1))[live] <= 1e-3 * a[live]))
 
 
 def grad_bits(g: torch.Tensor, rows) -> np.ndarray:

@@ -41,15 +41,16 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_struct_layouts_match_header(L):
-    assert ctypes.sizeof(sc.Params) == 56
+    assert ctypes.sizeof(sc.Params) == 64
     assert sc.DIAG_DTYPE.itemsize == 64
     p = sc.Params()
     assert L.sc_params_default(ctypes.byref(p)) == sc.SC_OK
     assert (p.K_max, p.is_mode, p.tis_max, p.mis_min, p.mis_max, p.centering) == (128, 0, 2.0, 0.5, 5.0, 1)
     assert (p.inv_temperature, p.grad_scale, p.cluster_size, p.threads, p.stages) == (1.0, 1.0, 0, 0, 0)
     assert (p.clip_low, p.clip_high, p.flag_layout) == (pytest.approx(0.2), pytest.approx(0.3), 0)
+    assert (p.wait_limit_us, p.test_stall) == (0, 0)
     assert L.sc_params_default(None) == sc.SC_ERR_NULL
-    assert L.sc_abi_version() == 103
+    assert L.sc_abi_version() == 104
     assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
 
 
@@ -97,6 +98,9 @@ def err(L):
     (dict(stages=5), sc.SC_ERR_ARG),
     (dict(flag_layout=3), sc.SC_ERR_ARG),
     (dict(flag_layout=-1), sc.SC_ERR_ARG),
+    (dict(wait_limit_us=-1), sc.SC_ERR_ARG),
+    (dict(wait_limit_us=60000001), sc.SC_ERR_ARG),
+    (dict(test_stall=2), sc.SC_ERR_ARG),
     (dict(logits=None), sc.SC_ERR_NULL),
     (dict(grad=None), sc.SC_ERR_NULL),
     (dict(logp=None), sc.SC_ERR_NULL),
@@ -154,6 +158,19 @@ def call_center_noalloc(L, **kw):
 def test_noalloc_empty_batch_is_a_no_op(L):
     assert call_center_noalloc(L, T=0, logits=None, grad=None, samp=None, resp=None, logp=None) == sc.SC_OK
     assert err(L) == ""
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(logits=FAKE + 2), sc.SC_ERR_ALIGN),
+    (dict(samp=None), sc.SC_ERR_NULL),
+    (dict(grad=None), sc.SC_ERR_NULL),
+    (dict(V=0), sc.SC_ERR_SHAPE),
+])
+def test_noalloc_checks_its_arguments_before_anything_else(L, kw, status):
+    # the same host-side checks as the regular call, before the library's
+    # array is looked up or cleared (these fail even without a GPU)
+    assert call_center_noalloc(L, **kw) == status, err(L)
+    assert err(L) != ""
 
 
 def test_noalloc_without_a_gpu_reports_a_status(L):
@@ -271,3 +288,15 @@ def test_lmhead_workspace_size(L):
     big = L.sc_lmhead_workspace_bytes(1024, 151936)
     # the block of logits (rows padded to a multiple of 8 entries) on top of a fixed part
     assert big - small == 1024 * 151936 * 2 - 256 and big % 256 == 0
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, -1, 1.0, FAKE * 2), sc.SC_ERR_SHAPE),
+    ((FAKE, 4, 1.0, None), sc.SC_ERR_NULL),
+    ((None, 4, 1.0, FAKE * 2), sc.SC_ERR_NULL),
+    ((FAKE, 4, float("inf"), FAKE * 2), sc.SC_ERR_ARG),
+    ((FAKE + 4, 4, 1.0, FAKE * 2), sc.SC_ERR_ALIGN),
+    ((FAKE, 4, 1.0, FAKE * 2 + 2), sc.SC_ERR_ALIGN),
+])
+def test_batch_loss_rejects_bad_arguments_on_the_host(L, args, status):
+    assert L.sc_batch_loss(*args, None) == status, err(L)

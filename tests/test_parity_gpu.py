@@ -451,20 +451,25 @@ def test_c2_full_size_every_row():
 
 
 def _invariants(batch, g, d, p):
-    """Properties that hold at any size, checked on every row on the device."""
+    """Properties that hold at any size, checked on every row on the device.
+    Returns the fraction of rows with a nonzero advantage whose bf16 output
+    meets the bare row-sum bound 1e-3 |a| with no rounding allowance."""
     diag = sc.diag_to_numpy(d)
     valid = batch["row_response"].cpu().numpy() >= 0
     assert np.all(diag["flags"][~valid] == sc.FLAG_MASKED)
-    A = np.abs(diag["adv"] * diag["is_weight"]) * p.inv_temperature * abs(p.grad_scale) * np.maximum(1, diag["rho"])
-    assert np.all(np.abs(diag["row_sum"]) <= 1e-3 * A + 1e-7), "FP32 row sums"
+    a = np.abs(diag["adv"] * diag["is_weight"]) * p.inv_temperature * abs(p.grad_scale)
+    # the kernel's FP32 row sums: the derived FP32 rounding bound (sc_parity.fp32_row_sum_bound)
+    assert np.all(np.abs(diag["row_sum"]) <= 1e-3 * a * np.maximum(1, diag["rho"]) + 1e-7), "FP32 row sums"
     # bf16 output row sums, with half an ulp per element of rounding allowance
     gs = g.double().sum(dim=1).cpu().numpy()
     gabs = g.float().abs()
     e = torch.floor(torch.log2(gabs.clamp_min(2.0**-126)))
     half_ulp = (0.5 * torch.exp2(e - 7) * (gabs > 0)).double().sum(dim=1).cpu().numpy()
-    assert np.all(np.abs(gs) <= 1e-3 * A + half_ulp + 1e-7), "bf16 row sums"
+    assert np.all(np.abs(gs) <= 1e-3 * a + half_ulp + 1e-7), "bf16 row sums"
     assert np.all(np.isfinite(diag["loss"])) and np.all(diag["P_H"][valid] <= 1.0 + 1e-6)
     assert np.all(np.abs(diag["P_H"] + diag["tail_pi"] - valid) <= 1e-5)
+    live = a > 0
+    return float(np.mean(np.abs(gs)[live] <= 1e-3 * a[live])) if live.any() else 1.0
 
 
 @pytest.mark.slow
@@ -486,4 +491,128 @@ def test_full_size_sampled_rows_and_invariants(name, chunk):
     bh = host_batch(sub, adv)
     check_rows(bh, p, np.arange(rows.size), grad_bits(g, rows), lp.cpu().numpy()[rows], diag_rows(d, rows),
                what=f"{name} chunk {chunk} sampled")
-    _invariants(batch, g, d, p)
+    bare = _invariants(batch, g, d, p)
+    print(f"{name} chunk {chunk}: {bare:.3f} of the rows meet the bare bf16 row-sum bound")
+
+
+# -------------------------------------------------------------------------
+# The clamped-denominator regime: the trainer's mass sits on the recorded ids
+# (1 - P_H below 1e-6, clamped) while the sampler's tail 1 - Q_H stays large,
+# so rho = max(1 - Q_H, 1e-6) / 1e-6 reaches 1e4 .. 1e6 and the unrecorded
+# entries get mu_hat = s p with s of the same order.
+
+
+def _clamp_regime_asserts(diag, valid):
+    f = diag["flags"][valid]
+    rho = diag["rho"][valid]
+    clamped = (f & sc.FLAG_CLAMP_PI) != 0
+    assert clamped.mean() >= 0.5, f"only {clamped.mean():.2f} of the rows clamp 1 - P_H"
+    assert not np.any(f & sc.FLAG_CLAMP_MU), "the sampler's tail should stay above 1e-6"
+    # rho = max(1 - Q_H, 1e-6) / 1e-6 on a clamped row: 1e3 and more wherever the
+    # sampler leaves more than 1e-3 of its mass outside the recorded ids
+    big = rho[clamped] >= 1e3
+    assert big.mean() >= 0.9, f"only {big.mean():.2f} of the clamped rows reach rho >= 1e3"
+    assert np.median(rho[clamped]) >= 1e4, f"median rho of clamped rows {np.median(rho[clamped])}"
+    return clamped.mean(), float(np.median(rho))
+
+
+def test_clamped_denominator_reduced_full_parity():
+    cfg = synth.config("C2R", n_prompts=1, n_per_prompt=4, L_pad=24, len_lo=5, len_hi=24)
+    batch = synth.make_batch(cfg)
+    _, _, d, _ = _full_check(batch, sc_params(batch), "rho >> 1 reduced")
+    frac, med = _clamp_regime_asserts(sc.diag_to_numpy(d), batch["row_response"].numpy() >= 0)
+    print(f"rho >> 1 reduced: {frac:.2f} of the rows clamped, median rho {med:.3g}")
+
+
+@pytest.mark.slow
+def test_clamped_denominator_full_size_sampled_rows_and_invariants():
+    batch = synth.make_batch("C2R", device="cuda")
+    T = batch["logits"].shape[0]
+    p = sc_params(batch)
+    adv = oracle_adv(batch)
+    g, lp, d, status = run_gpu(batch, p, adv)
+    assert int(status.item()) & 0x6 == 0
+    valid = batch["row_response"].cpu().numpy() >= 0
+    frac, med = _clamp_regime_asserts(sc.diag_to_numpy(d), valid)
+    rng = np.random.default_rng(zlib.crc32(b"C2R"))
+    vrows = np.nonzero(valid)[0]
+    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(vrows, 192, replace=False)]))
+    sub = {k: (v[torch.as_tensor(rows, device=v.device)] if isinstance(v, torch.Tensor) and v.dim() >= 1
+               and v.shape[0] == T else v) for k, v in batch.items()}
+    check_rows(host_batch(sub, adv), p, np.arange(rows.size), grad_bits(g, rows), lp.cpu().numpy()[rows],
+               diag_rows(d, rows), what="rho >> 1 full size sampled")
+    bare = _invariants(batch, g, d, p)
+    print(f"rho >> 1 full size: {frac:.2f} of the rows clamped, median rho {med:.3g}, "
+          f"{bare:.3f} meet the bare bf16 row-sum bound")
+
+
+# -------------------------------------------------------------------------
+# Failure path: a wait that runs out.  The test hook (`test_stall`) makes every
+# CTA leave out the bulk copy of its first row's first chunk, so the waits for
+# it can never complete: the launch must give up after `wait_limit_us`, set
+# SC_STATUS_TIMEOUT_LOAD, let its other copies land, leave the workspace zero
+# and return with the context usable.  Nothing faults, traps or spins forever.
+
+
+@pytest.mark.parametrize("cluster,threads,stages", [(0, 0, 0), (8, 128, 2)])
+def test_a_wait_that_runs_out_sets_the_status_and_the_next_call_is_clean(cluster, threads, stages):
+    dev = torch.device("cuda")
+    cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=512, len_lo=64, len_hi=512)
+    batch = synth.make_batch(cfg)
+    adv = oracle_adv(batch)
+    shape = dict(cluster_size=cluster, threads=threads, stages=stages)
+    g_ok, lp_ok, d_ok, st_ok = run_gpu(batch, sc_params(batch, **shape), adv)
+    assert int(st_ok.item()) == 0
+    p_stall = sc_params(batch, wait_limit_us=2000, test_stall=1, **shape)
+    _, _, _, st = run_gpu(batch, p_stall, adv)  # synchronises: a CUDA error would raise here
+    assert int(st.item()) & sc.SC_STATUS_TIMEOUT_LOAD, f"status {int(st.item()):#x}"
+    ws = sc.workspace(dev)
+    assert int(ws.abs().sum().item()) == 0, "the workspace is left zero after a launch that gave up"
+    # the same context runs a normal call cleanly afterwards
+    g2, lp2, d2, st2 = run_gpu(batch, sc_params(batch, **shape), adv)
+    assert int(st2.item()) == 0
+    assert torch.equal(g2.view(torch.int16), g_ok.view(torch.int16))
+    assert torch.equal(lp2, lp_ok) and torch.equal(d2, d_ok)
+    assert int(ws.abs().sum().item()) == 0
+
+
+def test_binding_on_a_stream_that_is_not_current():
+    # The binding's workspace for a stream is zero-filled on that stream, so the
+    # first launch on a fresh, non-current stream sees it zeroed.
+    dev = torch.device("cuda")
+    cfg = synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=512, len_lo=64, len_hi=512)
+    batch = synth.make_batch(cfg)
+    adv = oracle_adv(batch)
+    p = sc_params(batch)
+    g_ref, lp_ref, d_ref, _ = run_gpu(batch, p, adv)
+    for _ in range(2):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        x = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in batch.items()}
+        advd = torch.as_tensor(adv, device=dev)
+        diag = torch.zeros((x["logits"].shape[0], 16), dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+        g, lp, d = sc.sc_center_forward_backward(x["logits"], x["rec_ids"], x["rec_logprobs"], x["rec_count"],
+                                                 x["sampled"], x["rollout_logprob"], x["row_response"], advd, p,
+                                                 diag_out=diag, stream=s)
+        s.synchronize()
+        assert torch.equal(g.view(torch.int16), g_ref.view(torch.int16))
+        assert torch.equal(lp, lp_ref) and torch.equal(d, d_ref)
+        assert int(sc.workspace(dev, s).abs().sum().item()) == 0
+
+
+def test_batch_loss_is_the_scaled_sum_of_the_row_losses():
+    """sc_batch_loss: grad_scale * sum of the rows' losses in a fixed order,
+    one FP32 rounding; the same bits on every call; 0 for no rows."""
+    batch = synth.make_batch(synth.config("C2", n_prompts=1, n_per_prompt=2, L_pad=512, len_lo=64, len_hi=512))
+    p = sc_params(batch, grad_scale=1.0 / 997.0)
+    adv = oracle_adv(batch)
+    _, _, d, _ = run_gpu(batch, p, adv)
+    rows = sc.diag_to_numpy(d)["loss"].astype(np.float64)
+    want = float(np.float32(p.grad_scale)) * rows.sum()
+    got = [float(sc.sc_batch_loss(d, p.grad_scale).item()) for _ in range(3)]
+    assert got[0] == got[1] == got[2]
+    # FP64 partial sums: the only rounding that matters is the final one to FP32
+    assert abs(got[0] - want) <= 2.0 ** -23 * abs(want) + 1e-30
+    empty = sc.sc_batch_loss(torch.zeros((0, 16), dtype=torch.int32, device="cuda"), 1.0)
+    assert float(empty.item()) == 0.0
