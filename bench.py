@@ -347,11 +347,14 @@ def bf16_peak():
         return 1700.0, "fallback (sustained)"
 
 
-def lmhead_secondary(batch, adv, dev, d=4096, block_rows=1024, reps=5):
+def lmhead_secondary(batch, adv, dev, d=4096, reps=5):
     """The LM head followed by score centering on the batch's 4096 rows:
     random bf16 hidden states [T, d] and head [V, d] (logits of standard
     deviation near 3), the batch's recorded ids, sampled tokens and responses.
-    Three GEMMs of 2 T d V flops each per call (logits, dH, dW)."""
+    Three products of 2 T d V flops each per call (logits, dH, dW), all on the
+    library's tensor-core GEMM.  Timed as one block of all T rows and as
+    blocks of 1024 (dW then added to by the later blocks); each product also
+    timed alone at the one-block shapes."""
     import precision_off_policy_gb300 as sc
 
     T, V, K = batch["logits"].shape[0], batch["V"], batch["K"]
@@ -363,31 +366,50 @@ def lmhead_secondary(batch, adv, dev, d=4096, block_rows=1024, reps=5):
     logp = torch.empty(T, dtype=torch.float32, device=dev)
     p = sc.params(K_max=K, grad_scale=1.0 / max(1, batch["n_valid"]))
     st = torch.cuda.Stream(device=dev)
-
-    def call():
-        sc.sc_lmhead_forward_backward(hidden, w, batch["rec_ids"], batch["rec_logprobs"], batch["rec_count"],
-                                      batch["sampled"], batch["rollout_logprob"], batch["row_response"], adv, p,
-                                      block_rows=block_rows, dhidden=dh, dw=dw, logp_out=logp, stream=st)
-
-    with torch.cuda.stream(st):
-        for _ in range(2):
-            call()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(st)
-        for _ in range(reps):
-            call()
-        e1.record(st)
-    st.synchronize()
-    ms = e0.elapsed_time(e1) / reps
-    flops = 3 * 2.0 * T * d * V
     peak, kind = bf16_peak()
-    achieved = flops / (ms / 1e3) / 1e12
-    del hidden, w, dh, dw
-    return {"kernel": "cuBLASLt GEMMs + center_kernel", "call": "sc_lmhead_forward_backward",
-            "workload": f"{WORKLOAD} rows: T={T}, d={d}, V={V}, K={K}, blocks of {block_rows} rows",
-            "ms_per_call": ms, "tokens_per_s": batch["n_valid"] / (ms / 1e3),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": kind, "flops_per_call": flops}}
+    flops = 3 * 2.0 * T * d * V
+
+    def timed(fn, n):
+        with torch.cuda.stream(st):
+            for _ in range(2):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            for _ in range(n):
+                fn()
+            e1.record(st)
+        st.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    out = []
+    for block_rows in (T, 1024):
+        def call():
+            sc.sc_lmhead_forward_backward(hidden, w, batch["rec_ids"], batch["rec_logprobs"], batch["rec_count"],
+                                          batch["sampled"], batch["rollout_logprob"], batch["row_response"], adv, p,
+                                          block_rows=block_rows, dhidden=dh, dw=dw, logp_out=logp, stream=st)
+        ms = timed(call, reps)
+        achieved = flops / (ms / 1e3) / 1e12
+        out.append({"kernel": "gemm_kernel (tcgen05) x 3 + center_kernel", "call": "sc_lmhead_forward_backward",
+                    "workload": f"{WORKLOAD} rows: T={T}, d={d}, V={V}, K={K}, blocks of {block_rows} rows",
+                    "ms_per_call": ms, "tokens_per_s": batch["n_valid"] / (ms / 1e3),
+                    "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": achieved / peak, "peak_source": kind, "flops_per_call": flops}})
+    # each product alone (one block of T rows): z = H W^T, dH = g W, dW = g^T H
+    z = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+    gemms = {"z = H W^T (A, B K-major; bf16 out)": lambda: sc.sc_gemm_bf16(hidden, w, z, True, True, sc.GEMM_BF16,
+                                                                           stream=st),
+             "dH = g W (B N-major; bf16 out)": lambda: sc.sc_gemm_bf16(z, w, dh, True, False, sc.GEMM_BF16, stream=st),
+             "dW = g^T H (A M-major, B N-major; FP32 out)": lambda: sc.sc_gemm_bf16(z, hidden, dw, False, False,
+                                                                                    sc.GEMM_FP32, stream=st)}
+    for name, fn in gemms.items():
+        ms = timed(fn, reps)
+        achieved = 2.0 * T * d * V / (ms / 1e3) / 1e12
+        out.append({"kernel": "gemm_kernel (tcgen05)", "call": "sc_gemm_bf16", "workload": f"{name}: T={T}, d={d}, V={V}",
+                    "ms_per_call": ms, "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                                                    "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": kind,
+                                                    "flops_per_call": 2.0 * T * d * V}})
+    del hidden, w, dh, dw, z
+    return out
 
 
 def cpu_baseline(batch, p, adv, min_seconds=10.0, max_passes=50):
@@ -682,7 +704,7 @@ def main():
     del sets
     torch.cuda.empty_cache()
     line["secondary"] = topk_secondary(batch, dev, peak, peak_kind)
-    line["secondary"].append(lmhead_secondary(batch, adv, dev))
+    line["secondary"].extend(lmhead_secondary(batch, adv, dev))
     torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle

@@ -22,8 +22,7 @@
  * Conventions for every entry point:
  *   - All data pointers are DEVICE pointers owned by the caller.  The library
  *     allocates no memory at run time.  It keeps a small per-process cache of
- *     launch plans (for the LM head also cuBLASLt handles and matmul plans)
- *     and one 256-byte static device array per GPU, which only
+ *     launch plans and one 256-byte static device array per GPU, which only
  *     sc_center_forward_backward_noalloc uses.  The fused call takes a small
  *     caller-owned workspace (see SC_WORKSPACE_BYTES).
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
@@ -366,15 +365,15 @@ int sc_center_forward_backward_noalloc(const uint16_t* logits, long long T, int 
  * workspace   : sc_lmhead_workspace_bytes(block_rows, V) bytes of device
  *               memory, 256-byte aligned; its first SC_WORKSPACE_BYTES must
  *               be zero before the first call (they are left zero, as for
- *               sc_center_forward_backward).  It holds cuBLASLt's scratch and
- *               the block of logits.  Calls that may run at the same time
- *               need workspaces of their own.
- * Per block: z_b = H_b W^T (cuBLASLt, FP32 accumulation, bf16 logits), the
- * fused score-centering kernel in place, dH_b = g_b W and dW += g_b^T H_b
- * (cuBLASLt, FP32 accumulation); all asynchronous on `stream`.
+ *               sc_center_forward_backward).  It holds the block of logits
+ *               (bf16 [block_rows, V rounded up to 8]).  Calls that may run
+ *               at the same time need workspaces of their own.
+ * Per block: z_b = H_b W^T (sc_gemm_bf16: FP32 accumulation, bf16 logits),
+ * the fused score-centering kernel in place, dH_b = g_b W and dW (+)= g_b^T
+ * H_b (sc_gemm_bf16, FP32 accumulation; dW stored by the first block and
+ * added to by the others); all asynchronous on `stream`.
  * Errors: as sc_center_forward_backward, plus SC_ERR_SHAPE (d not a multiple
- * of 8, block_rows < 1, workspace too small), SC_ERR_CUDA for a cuBLASLt
- * failure (its status in the message).  T == 0 is a no-op.
+ * of 8, block_rows < 1, workspace too small).  T == 0 is a no-op.
  */
 /*
  * Dense bf16 GEMM on the tensor cores: the LM head's three products

@@ -287,7 +287,7 @@ def bf16_round_array(x) -> np.ndarray:
     return out
 
 
-def lmhead_rows(hidden_bits, w_bits, batch: dict, params: Params, nthreads: int = 0):
+def lmhead_rows(hidden_bits, w_bits, batch: dict, params: Params, nthreads: int = 0, dw_rows=None):
     """The LM head followed by score centering, for a BF16 trainer.
 
     The trainer's logits are z = bf16(H W^T): H [T, d] and W [V, d] are bf16
@@ -298,8 +298,11 @@ def lmhead_rows(hidden_bits, w_bits, batch: dict, params: Params, nthreads: int 
     z's linearity: dH = g W and dW = g^T H, in FP64 from the unrounded g.
 
     hidden_bits: uint16 [T, d]; w_bits: uint16 [V, d]; batch: the keys of
-    ``rows`` except logits (V taken from w_bits).
-    Returns (dH [T, d], dW [V, d], logp_a [T], out [T], z_bits [T, V]).
+    ``rows`` except logits (V taken from w_bits).  dw_rows: indices of the
+    rows of dW to return (all when None; a full FP64 dW at V = 151936 and
+    d = 4096 takes 5 GB).
+    Returns (dH [T, d], dW [len(dw_rows) or V, d], logp_a [T], out [T],
+    z_bits [T, V]).
     """
     Hb = np.ascontiguousarray(hidden_bits, dtype=np.uint16)
     Wb = np.ascontiguousarray(w_bits, dtype=np.uint16)
@@ -312,4 +315,5 @@ def lmhead_rows(hidden_bits, w_bits, batch: dict, params: Params, nthreads: int 
     b["logits"] = z_bits
     b["V"] = Wb.shape[0]
     g, la, out, _ = rows(b, params, None, nthreads)
-    return g @ W, g.T @ H, la, out, z_bits
+    gw = g if dw_rows is None else g[:, np.asarray(dw_rows, dtype=np.int64)]
+    return g @ W, gw.T @ H, la, out, z_bits

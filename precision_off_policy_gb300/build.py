@@ -74,7 +74,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(log)
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
-            "-lcublasLt", "-Xlinker", f"-rpath={os.path.join(cuda, 'lib64')}"]
+            "-Xlinker", f"-rpath={os.path.join(cuda, 'lib64')}"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -60,6 +60,9 @@ static_assert(kSmemTotal <= 232448, "shared memory per CTA");
 
 struct GemmArgs {
     long long M, N, K;
+    long long N_full;  // columns written by tensor stores: N rounded down to whole 16-byte units
+    void* C;           // C itself, for the columns past N_full (plain stores)
+    long long ldc;
     int num_m, num_n, k_steps;
     long long tiles;
     int a_mn, b_mn;   // operand majorness: 0 K-major, 1 M- / N-major
@@ -310,12 +313,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < nchunks; ++c) {
                 const long long c0 = static_cast<long long>(nt) * BN + c * cols;
                 if (r0 >= g.M || c0 >= g.N) break;  // (chunks are in column order)
+                // A tensor store writes whole 16-byte units of a row, so only the
+                // columns before N_full go through it; the few past it (N not a
+                // multiple of 16 bytes) are stored one by one below.
                 uint32_t v[64];
                 uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
                 uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
                 tmem_ld32(tbase + static_cast<uint32_t>(c * cols), lo);
                 if (cols == 64) tmem_ld32(tbase + static_cast<uint32_t>(c * cols + 32), hi);
                 tmem_ld_wait();
+                if (c0 + cols > g.N_full) {
+                    // columns [max(c0, N_full), N) of this thread's row, one by one
+                    const long long row = r0 + lane;
+                    if (row < g.M) {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) {
+                            const long long col = c0 + j;
+                            if (j < cols && col >= g.N_full && col < g.N) {
+                                if (g.c_mode == 0) {
+                                    uint16_t* cp = static_cast<uint16_t*>(g.C) + row * g.ldc + col;
+                                    *cp = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(v[j]), 0.0f) & 0xFFFFu);
+                                } else if (g.c_mode == 1) {
+                                    static_cast<float*>(g.C)[row * g.ldc + col] = __uint_as_float(v[j]);
+                                } else {
+                                    atomicAdd(static_cast<float*>(g.C) + row * g.ldc + col, __uint_as_float(v[j]));
+                                }
+                            }
+                        }
+                    }
+                    if (c0 >= g.N_full) continue;  // nothing of this chunk for the tensor store
+                }
                 const uint32_t buf = buf0 + static_cast<uint32_t>((nst & 1u) * kEpiBuf);
                 if (lane == 0) bulk_wait_read_le1();  // the store that used this buffer has read it
                 __syncwarp();
@@ -441,8 +468,11 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     st = b_mn ? make_map(enc, &tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, ldb, 64, 64)
               : make_map(enc, &tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, ldb, 64, BN);
     if (st != SC_OK) return st;
-    st = c_mode == 0 ? make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, ldc, 64, 32)
-                     : make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, ldc, 32, 32);
+    const long long per16 = 16 / cesize;              // elements in a 16-byte unit
+    const long long n_full = N / per16 * per16;        // columns the tensor stores cover
+    const long long n_map = n_full > 0 ? n_full : per16;  // (a map needs a nonzero extent; unused then)
+    st = c_mode == 0 ? make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, n_map, ldc, 64, 32)
+                     : make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, n_map, ldc, 32, 32);
     if (st != SC_OK) return st;
     int dev = 0;
     st = check_device(&dev);
@@ -467,6 +497,9 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     ga.M = M;
     ga.N = N;
     ga.K = K;
+    ga.N_full = n_full;
+    ga.C = C;
+    ga.ldc = ldc;
     ga.num_m = static_cast<int>((M + BM - 1) / BM);
     ga.num_n = static_cast<int>((N + BN - 1) / BN);
     ga.k_steps = static_cast<int>((K + BK - 1) / BK);

@@ -276,7 +276,7 @@ def call_lmhead(L, T=4, d=64, V=100, hidden=FAKE, w=FAKE * 2, ids=FAKE * 3, lps=
     (dict(ids=None), sc.SC_ERR_NULL),
     (dict(hidden=FAKE + 8), sc.SC_ERR_ALIGN),
     (dict(ws=FAKE * 256 + 16), sc.SC_ERR_ALIGN),
-    (dict(ws_bytes=1024), sc.SC_ERR_SHAPE),
+    (dict(ws_bytes=256 + 2 * 104 * 2 - 1), sc.SC_ERR_SHAPE),   # short of two rows of logits
 ])
 def test_lmhead_rejects_bad_arguments_on_the_host(L, kw, status):
     assert call_lmhead(L, **kw) == status, err(L)

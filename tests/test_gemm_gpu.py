@@ -34,16 +34,28 @@ def _dyadic(shape, denom, lim, gen):
     return (k.double() / denom)
 
 
+def _padded(x, dtype, fill=0.0):
+    """x on the device in rows padded past a 16-byte boundary (the tensor
+    copies' row alignment) by 16 more bytes, as a view of its first columns;
+    the padding holds `fill`."""
+    rows, cols = x.shape
+    per = 16 // torch.empty((), dtype=dtype).element_size()
+    buf = torch.full((rows, (cols + per - 1) // per * per + per), fill, dtype=dtype)
+    buf[:, :cols] = x.to(dtype)
+    return buf.cuda()[:, :cols]
+
+
 def _run(M, N, K, a_kmajor, b_kmajor, c_mode, seed=0):
     gen = torch.Generator().manual_seed(seed + 1000 * M + N + 7 * K)
     A = _dyadic((M, K), 8, 8, gen)          # exact in bf16
     B = _dyadic((K, N), 64, 64, gen)
-    a = (A if a_kmajor else A.T.contiguous()).to(torch.bfloat16).cuda()
-    b = (B.T.contiguous() if b_kmajor else B).to(torch.bfloat16).cuda()
+    a = _padded(A if a_kmajor else A.T, torch.bfloat16, 3.0)
+    b = _padded(B.T if b_kmajor else B, torch.bfloat16, 3.0)
     exact = (A.numpy() @ B.numpy())          # FP64: exact for these inputs
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     if c_mode == sc.GEMM_BF16:
-        c = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
+        c = _padded(torch.zeros(M, N), torch.bfloat16, 7.0)
+        c.fill_(7.0)
         sc.sc_gemm_bf16(a, b, c, a_kmajor, b_kmajor, c_mode, status=status)
         want = torch.from_numpy(exact).float().to(torch.bfloat16)
         got = c.cpu()
@@ -51,11 +63,13 @@ def _run(M, N, K, a_kmajor, b_kmajor, c_mode, seed=0):
             f"bf16 mismatch: {(got.float() - want.float()).abs().max()}"
     else:
         c0 = _dyadic((M, N), 4, 8, gen)
-        c = (c0.float() if c_mode == sc.GEMM_FP32_ADD else torch.full((M, N), 7.0)).cuda()
+        c = _padded(c0 if c_mode == sc.GEMM_FP32_ADD else torch.full((M, N), 7.0), torch.float32, 7.0)
         sc.sc_gemm_bf16(a, b, c, a_kmajor, b_kmajor, c_mode, status=status)
         want = exact + (c0.numpy() if c_mode == sc.GEMM_FP32_ADD else 0.0)
         got = c.cpu().double().numpy()
         assert np.array_equal(got, want), f"FP32 mismatch: {np.abs(got - want).max()}"
+    pad = c.as_strided((M, c.stride(0)), (c.stride(0), 1))[:, N:]
+    assert torch.all(pad == 7.0), "the row padding past N is not written"
     torch.cuda.synchronize()
     assert int(status.item()) == 0
 

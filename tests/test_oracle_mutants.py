@@ -136,14 +136,14 @@ def test_pins_reject_planted_mistake(outcomes, name):
 # in a copy of that function's source, swapped into the oracle module for one
 # test, and its two pins (finite differences, the identity head) run directly.
 LMHEAD_MUTANTS = {
-    "dH from the bf16-rounded gradient": ("return g @ W, g.T @ H,",
-                                          "return bf16_to_double(bf16_round_array(g)) @ W, g.T @ H,"),
-    "dW from the bf16-rounded gradient": ("return g @ W, g.T @ H,",
-                                          "return g @ W, bf16_to_double(bf16_round_array(g)).T @ H,"),
-    "grad_scale applied twice to dH": ("return g @ W, g.T @ H,", "return params.grad_scale * (g @ W), g.T @ H,"),
+    "dH from the bf16-rounded gradient": ("return g @ W, gw.T @ H,",
+                                          "return bf16_to_double(bf16_round_array(g)) @ W, gw.T @ H,"),
+    "dW from the bf16-rounded gradient": ("return g @ W, gw.T @ H,",
+                                          "return g @ W, bf16_to_double(bf16_round_array(gw)).T @ H,"),
+    "grad_scale applied twice to dH": ("return g @ W, gw.T @ H,", "return params.grad_scale * (g @ W), gw.T @ H,"),
     "logits truncated to bf16": ("z_bits = bf16_round_array(H @ W.T)",
                                  "z_bits = ((H @ W.T).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)"),
-    "dW transposed": ("return g @ W, g.T @ H,", "return g @ W, (g.T @ H).T,"),
+    "dW transposed": ("return g @ W, gw.T @ H,", "return g @ W, (gw.T @ H).T,"),
 }
 
 
