@@ -201,17 +201,27 @@ int sc_batch_loss(const sc_row_diag* diag, long long T, float grad_scale, float*
  *                the row's count hold -1.
  * logprobs_out : FP32 [T, K] log mu of those ids (0 past the count).
  * count_out    : int32 [T] min(K, V, nucleus size), or NULL.
+ * workspace    : SC_WORKSPACE_BYTES of device memory, 16-byte aligned, zero
+ *                before its first use, or NULL.  With it, the rows after each
+ *                thread group's first are handed out at run time from a
+ *                counter there (rows whose nucleus reaches far below the top
+ *                entries cost more passes, and the groups that drew them take
+ *                fewer rows); the launch leaves it zero again when it
+ *                completes.  It may be the workspace of the fused call on the
+ *                same stream (the two use different words of it).  NULL: every
+ *                row dealt at launch.
  * K            : 1..1024.  inv_temperature finite > 0.  top_p in (0, 1].
  * Asynchronous on `stream`; nothing is allocated.  Every sum is taken in a
  * fixed order (compensated FP32 on the one-pass path that almost every row
- * takes, 2^-40 fixed point on the exact path for the rest), so the results
- * do not depend on how the rows are scheduled.
+ * takes, 2^-40 fixed point where the nucleus reaches below the top entries
+ * and on the exact path), so the results do not depend on how the rows are
+ * scheduled.
  * Errors: SC_ERR_SHAPE (T < 0, V outside 1..2^24, K, stride), SC_ERR_ARG,
  * SC_ERR_NULL, SC_ERR_ALIGN, SC_ERR_UNSUPPORTED, SC_ERR_CUDA.
  */
 int sc_topk_capture(const float* logits, long long T, int V, long long logits_stride, float inv_temperature,
                     int K, float top_p, int32_t* ids_out, float* logprobs_out, int32_t* count_out,
-                    sc_stream_t stream);
+                    void* workspace, sc_stream_t stream);
 
 /* Fills *p with the defaults above.  Returns SC_OK or SC_ERR_NULL. */
 int sc_params_default(sc_params* p);

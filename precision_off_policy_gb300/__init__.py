@@ -120,7 +120,7 @@ def lib():
             L.sc_gemm_bf16.restype = i32
             L.sc_rollout_mean_advantages.argtypes = [vp, vp, i64, i32, vp, vp, vp]
             L.sc_rollout_mean_advantages.restype = i32
-            L.sc_topk_capture.argtypes = [vp, i64, i32, i64, f32, i32, f32, vp, vp, vp, vp]
+            L.sc_topk_capture.argtypes = [vp, i64, i32, i64, f32, i32, f32, vp, vp, vp, vp, vp]
             L.sc_topk_capture.restype = i32
             L.sc_center_forward_backward.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                                      ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp, vp]
@@ -302,10 +302,13 @@ def sc_rollout_mean_advantages(adv: torch.Tensor, row_response: torch.Tensor, ou
 
 def sc_topk_capture(logits: torch.Tensor, K: int, inv_temperature: float = 1.0, top_p: float = 1.0,
                     ids_out: torch.Tensor | None = None, logprobs_out: torch.Tensor | None = None,
-                    count_out: torch.Tensor | None = None, V: int | None = None, stream=None):
+                    count_out: torch.Tensor | None = None, V: int | None = None, stream=None,
+                    workspace_buf: torch.Tensor | None = None, dynamic: bool = True):
     """Sampler-side top-K capture.  logits: FP32 [T, >=V] on a CUDA device with
     contiguous rows.  Returns (ids int32 [T, K], logprobs float32 [T, K],
-    count int32 [T])."""
+    count int32 [T]).  With ``dynamic`` the last rows are handed out at run
+    time through the binding's workspace for this device and stream (or
+    ``workspace_buf``); without, every row is dealt at launch."""
     dev = logits.device
     if dev.type != "cuda":
         raise ValueError("logits must be on a CUDA device")
@@ -325,8 +328,14 @@ def sc_topk_capture(logits: torch.Tensor, K: int, inv_temperature: float = 1.0, 
     _check_topk_buffers(T, V, K, logits, ids_out, logprobs_out, count_out)
     if T == 0:
         return ids_out, logprobs_out, count_out
+    ws = None
+    if dynamic:
+        ws = workspace(dev, stream) if workspace_buf is None else workspace_buf
+        if ws.device != dev or ws.numel() * ws.element_size() < WORKSPACE_BYTES:
+            raise ValueError(f"workspace_buf must hold {WORKSPACE_BYTES} bytes on {dev}")
     _check(lib().sc_topk_capture(_ptr(logits), T, V, _rows(logits, "logits"), float(inv_temperature), K,
-                                 float(top_p), _ptr(ids_out), _ptr(logprobs_out), _ptr(count_out), _stream(stream)))
+                                 float(top_p), _ptr(ids_out), _ptr(logprobs_out), _ptr(count_out), _ptr(ws),
+                                 _stream(stream)))
     return ids_out, logprobs_out, count_out
 
 

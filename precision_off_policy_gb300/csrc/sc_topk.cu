@@ -56,6 +56,8 @@ struct TopkArgs {
     int32_t* ids;
     float* lps;
     int32_t* counts;
+    unsigned long long* ws;  // run-time hand-out: [2] rows taken past T_static, [3] CTAs finished (or NULL)
+    long long T_static;      // rows dealt round robin to the thread groups (all of them without ws)
 };
 
 // Order-preserving key: a larger float gives a larger key (-0 counts as +0).
@@ -93,6 +95,16 @@ __device__ __forceinline__ unsigned long long to_fixed(float e) {
 }
 __device__ __forceinline__ unsigned long long fixed_q(float z, float mz, float kt) { return to_fixed(rel_mass(z, mz, kt)); }
 
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int mask) {
+    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), mask);
+    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), mask);
+    return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
+__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), src);
+    return (static_cast<unsigned long long>(hi) << 32) | lo;
+}
 __device__ __forceinline__ unsigned long long shfl_up_u64(unsigned long long v, int d) {
     const uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), d);
     const uint32_t hi = __shfl_up_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), d);
@@ -605,15 +617,20 @@ constexpr int kGW = kGT / 32;         // warps per group
 constexpr int kSampRun = 32;          // vectors per sampled run (one warp load)
 constexpr int kSampEvery = 16;        // one run in kSampEvery is sampled
 constexpr int kRound = 32;            // rows per group between the CTA's exact-path rounds
+constexpr int kNucRes = 64;           // nucleus histogram: bins per binary order of magnitude of mass
+constexpr int kNucBins = 40 * kNucRes;  // down to 2^-40 of the row maximum's mass (the fixed-point unit)
 
 // A thread group's view: its threads, its named barrier, its shared state.
 struct GroupShared {
     uint32_t keys[kGT];                 // the sample maxima, sorted
     unsigned long long cand[kCap];      // (key << 32) | ~id
+    float mh[kNucBins];                 // wide nucleus: mass of the entries below tau per bin (FP32, a guide)
+    unsigned long long u64red[kGW];     // group sums of 64-bit integers
     float fred[kGW], flo[kGW];          // group maximum / sums of pairs
     double dS, dlse;
     double pnuc, lnuc;  // the nucleus mass and log(nucleus mass / normaliser)
-    int ncand, cross;
+    unsigned long long above;           // wide nucleus: fixed-point mass before the crossing bin
+    int ncand, cross, nbin, bstar;
 };
 struct KernelShared {
     union {
@@ -622,6 +639,8 @@ struct KernelShared {
     } u;
     int ndefer;
     long long defer[kGroups * kRound];  // rows of this round left to the exact path
+    long long take[kGroups];            // a group's row from the run-time hand-out
+    int gdone[kGroups];                 // a group has no rows left
 };
 
 struct Group {
@@ -699,26 +718,365 @@ __device__ void group_sort_keys_desc(GroupShared& gs, const Group& G, uint32_t k
     gs.keys[i] = x;
     G.sync();
 }
-// Bitonic sort of cand[0, n), larger first (n <= kCap), by the group.
-__device__ void group_sort_desc(GroupShared& gs, const Group& G, int n) {
-    int m = 1;
-    while (m < n) m <<= 1;
-    for (int i = n + G.tid; i < m; i += kGT) gs.cand[i] = 0ull;
+// Bitonic sort of c[0, m) (m = kGT E, a power of two), larger first, by the
+// group: thread t holds entries [t E, t E + E) in registers; the stages whose
+// partner lies in the same thread compare in registers, those within the warp
+// exchange by shuffles, and only the stages across warps (six for any E) go
+// through shared memory, each with two group barriers.  E <= 4 (up to 1024
+// entries) keeps every entry in registers.
+template <int E>
+__device__ void group_bitonic_regs(unsigned long long* c, const Group& G) {
+    constexpr int m = kGT * E;
+    unsigned long long x[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) x[e] = c[G.tid * E + e];
+    G.sync();  // every thread has its entries before any stage writes c
+    for (int k = 2; k <= m; k <<= 1) {
+        // the stages whose partner is in another thread (j >= E) ...
+        for (int j = k >> 1; j >= E; j >>= 1) {
+            if (j < 32 * E) {
+                const int lj = j / E;  // partner lane
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = G.tid * E + e;
+                    const unsigned long long y = shfl_xor_u64(x[e], lj);
+                    const bool lower = (i & j) == 0, desc = (i & k) == 0;
+                    x[e] = (lower == desc) ? (x[e] > y ? x[e] : y) : (x[e] < y ? x[e] : y);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) c[G.tid * E + e] = x[e];
+                G.sync();
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int i = G.tid * E + e;
+                    const unsigned long long y = c[i ^ j];
+                    const bool lower = (i & j) == 0, desc = (i & k) == 0;
+                    x[e] = (lower == desc) ? (x[e] > y ? x[e] : y) : (x[e] < y ? x[e] : y);
+                }
+                G.sync();
+            }
+        }
+        // ... then those within the thread's own entries (compile-time indices)
+#pragma unroll
+        for (int jj = E / 2; jj > 0; jj >>= 1) {
+            if (jj <= (k >> 1)) {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int f = e ^ jj;
+                    if (f > e) {
+                        const int i = G.tid * E + e;
+                        const bool desc = (i & k) == 0;
+                        const unsigned long long a0 = x[e], b0 = x[f];
+                        if (desc ? (a0 < b0) : (a0 > b0)) {
+                            x[e] = b0;
+                            x[f] = a0;
+                        }
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) c[G.tid * E + e] = x[e];
     G.sync();
+}
+
+// Bitonic sort of cand[off, off + n), larger first, by the group (off + the
+// padded length must stay within kCap: the caller checks).  Padding entries
+// are 0, below every real entry.
+__device__ void group_sort_desc_at(GroupShared& gs, const Group& G, int off, int n) {
+    int m = kGT;
+    while (m < n) m <<= 1;
+    unsigned long long* c = gs.cand + off;
+    for (int i = n + G.tid; i < m; i += kGT) c[i] = 0ull;
+    G.sync();
+    switch (m / kGT) {
+        case 1: group_bitonic_regs<1>(c, G); return;
+        case 2: group_bitonic_regs<2>(c, G); return;
+        case 4: group_bitonic_regs<4>(c, G); return;
+        default: break;
+    }
+    // more than 1024 entries (rare): every stage through shared memory
     for (int k = 2; k <= m; k <<= 1)
         for (int j = k >> 1; j > 0; j >>= 1) {
             for (int i = G.tid; i < m; i += kGT) {
                 const int l = i ^ j;
                 if (l > i) {
-                    const unsigned long long x = gs.cand[i], y = gs.cand[l];
+                    const unsigned long long x = c[i], y = c[l];
                     if (((i & k) == 0) ? (x < y) : (x > y)) {
-                        gs.cand[i] = y;
-                        gs.cand[l] = x;
+                        c[i] = y;
+                        c[l] = x;
                     }
                 }
             }
             G.sync();
         }
+}
+__device__ void group_sort_desc(GroupShared& gs, const Group& G, int n) { group_sort_desc_at(gs, G, 0, n); }
+
+// Exclusive prefix sum of 64-bit integers over the group's threads, in
+// thread order; *total gets the sum of all.
+__device__ unsigned long long group_exclusive_scan_u64(GroupShared& gs, const Group& G, unsigned long long v,
+                                                       unsigned long long* total) {
+    unsigned long long x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const unsigned long long y = shfl_up_u64(x, d);
+        if (G.lane >= d) x += y;
+    }
+    if (G.lane == 31) gs.u64red[G.warp] = x;
+    G.sync();
+    unsigned long long before = 0, all = 0;
+    for (int w = 0; w < kGW; ++w) {
+        const unsigned long long t = gs.u64red[w];
+        if (w < G.warp) before += t;
+        all += t;
+    }
+    G.sync();
+    if (total) *total = all;
+    return before + x - v;
+}
+
+// Every entry of the row, f(z, id), by the group's threads (16-byte loads,
+// kUnroll of them in flight per thread).
+template <typename F>
+__device__ __forceinline__ void group_for_each_entry(const Group& G, const float* row, int V, F&& f) {
+    const int nv4 = V >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    int i = G.tid;
+    for (; i + (kUnroll - 1) * kGT < nv4; i += kUnroll * kGT) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(r4 + i + u * kGT);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int b = 4 * (i + u * kGT);
+            f(v[u].x, b);
+            f(v[u].y, b + 1);
+            f(v[u].z, b + 2);
+            f(v[u].w, b + 3);
+        }
+    }
+    for (; i < nv4; i += kGT) {
+        const float4 v = __ldg(r4 + i);
+        f(v.x, 4 * i);
+        f(v.y, 4 * i + 1);
+        f(v.z, 4 * i + 2);
+        f(v.w, 4 * i + 3);
+    }
+    for (int j = (nv4 << 2) + G.tid; j < V; j += kGT) f(__ldg(row + j), j);
+}
+
+
+// The nucleus bin of an entry below the candidate threshold: how many 1/64
+// binary orders of magnitude its mass lies below the row maximum's (the same
+// expression in both passes, so both put an entry in the same bin).
+__device__ __forceinline__ int nucleus_bin(float z, float M, float kt64) {
+    // floor of a nonnegative x < 2^23 by one add rounded toward zero: the
+    // integer part lands in the low mantissa bits of 2^23 + x
+    const float x = fminf((M - z) * kt64, 4194304.0f);
+    return __float_as_int(__fadd_rz(x, 8388608.0f)) - 0x4B000000;
+}
+
+// The nucleus reaches below the candidates (the entries with z >= tau, sorted
+// in cand[0, nc)): more passes over the row give its exact mass in 2^-40 fixed
+// point (the normaliser S is the one-pass sum).  Pass 2: below tau, every
+// entry's FP32 mass 2^((z - M) kt) goes into a histogram on bins of 1/64 of a
+// binary order of magnitude, which only guides the search: the bin where the
+// running mass
+// (candidates first, then the bins from the top) reaches top_p S should hold
+// the crossing.  Pass 3 sums the exact fixed-point mass of every entry above
+// that bin and collects the bin's entries behind the candidates; one warp
+// walks them, sorted, to the first entry whose preceding mass reaches top_p S,
+// and the nucleus mass is the running sum there.  When the FP32 guide pointed
+// one bin off (the exact mass above the bin already reaches the threshold, or
+// the bin's entries do not), pass 3 repeats on the neighbouring bin.  Returns
+// false (the row goes to the exact path) when a bin's entries do not fit the
+// buffer, the crossing is not found in a few bins, or the fixed-point sums put
+// it among the candidates after all (a near tie).
+__device__ bool wide_nucleus(GroupShared& gs, const Group& G, const TopkArgs& a, const float* row, float M, float tau,
+                             int nc, double S, double* log_nuc) {
+    const int V = a.V;
+    const float kt = a.inv_t * kLog2e;
+    const float kt64 = kt * static_cast<float>(kNucRes);
+    for (int b = G.tid; b < kNucBins; b += kGT) gs.mh[b] = 0.0f;
+    G.sync();
+    // ---- pass 2: the FP32 mass histogram below tau
+    group_for_each_entry(G, row, V, [&](float z, int) {
+        if (z < tau) {
+            const int b = nucleus_bin(z, M, kt64);
+            if (b < kNucBins) atomicAdd(&gs.mh[b], rel_mass(z, M, kt));
+        }
+    });
+    G.sync();
+    // the normaliser in fixed-point units (2^-40 of the row maximum's mass),
+    // from the one-pass sum
+    const double S_fix = S * kFix;
+    // the candidates' fixed-point mass
+    unsigned long long pc = 0ull;
+    for (int i = G.tid; i < nc; i += kGT) pc += fixed_q(float_of(static_cast<uint32_t>(gs.cand[i] >> 32)), M, kt);
+    unsigned long long P_cand = 0ull;
+    (void)group_exclusive_scan_u64(gs, G, pc, &P_cand);
+    const double thr = static_cast<double>(a.top_p) * S_fix;
+    if (!(static_cast<double>(P_cand) < thr)) return false;  // a near tie at the end of the candidates
+    // ---- the guide: the bin where the FP32 running mass crosses thr (thread i
+    // owns bins [i per, (i + 1) per))
+    constexpr int per = (kNucBins + kGT - 1) / kGT;
+    const int b0 = G.tid * per;
+    double local = 0.0;
+    for (int j = 0; j < per; ++j)
+        if (b0 + j < kNucBins) local += static_cast<double>(gs.mh[b0 + j]) * kFix;
+    if (G.tid == 0) gs.bstar = kNucBins - 1;
+    // (the FP32 masses only choose where to look: a plain double scan)
+    double run = static_cast<double>(P_cand);
+    {
+        double x = local;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const double y = __shfl_up_sync(0xFFFFFFFFu, x, d);
+            if (G.lane >= d) x += y;
+        }
+        if (G.lane == 31) gs.u64red[G.warp] = static_cast<unsigned long long>(__double_as_longlong(x));
+        G.sync();
+        double before = 0.0;
+        for (int w = 0; w < G.warp; ++w) before += __longlong_as_double(static_cast<long long>(gs.u64red[w]));
+        G.sync();
+        run += before + x - local;
+    }
+    for (int j = 0; j < per; ++j) {
+        const int b = b0 + j;
+        if (b >= kNucBins) break;
+        const double v = static_cast<double>(gs.mh[b]) * kFix;
+        if (run < thr && thr <= run + v) gs.bstar = b;
+        run += v;
+    }
+    G.sync();
+    int bstar = gs.bstar;
+    G.sync();
+    for (int tries = 0; tries < 4; ++tries) {
+        // ---- pass 3: the exact mass above bin bstar, and its entries
+        if (G.tid == 0) gs.nbin = 0;
+        G.sync();
+        unsigned long long hi = 0ull;
+        group_for_each_entry(G, row, V, [&](float z, int id) {
+            if (z < tau) {
+                const int b = nucleus_bin(z, M, kt64);
+                if (b < bstar) {
+                    hi += fixed_q(z, M, kt);
+                } else if (b == bstar) {
+                    const int pos = atomicAdd(&gs.nbin, 1);
+                    if (nc + pos < kCap) gs.cand[nc + pos] = pack_entry(key_of(z), id);
+                }
+            }
+        });
+        unsigned long long above_hist = 0ull;
+        (void)group_exclusive_scan_u64(gs, G, hi, &above_hist);
+        const unsigned long long above = P_cand + above_hist;
+        const int nb = gs.nbin;
+        G.sync();
+        if (static_cast<double>(above) >= thr) {  // the crossing lies in a bin above
+            if (bstar == 0) return false;
+            --bstar;
+            continue;
+        }
+        int m = 1;
+        while (m < nb) m <<= 1;
+        if (nc + m > kCap) return false;
+        if (nb > 0) group_sort_desc_at(gs, G, nc, nb);
+        // ---- the walk: one warp, lane-contiguous chunks, running sums in fixed point
+        if (G.warp == 0) {
+            const int lane = G.lane;
+            const int chunk = (nb + 31) / 32;
+            const int i0 = nc + lane * chunk, i1 = min(nc + nb, i0 + chunk);
+            auto q_of = [&](int i) { return fixed_q(float_of(static_cast<uint32_t>(gs.cand[i] >> 32)), M, kt); };
+            unsigned long long loc = 0ull;
+            for (int i = i0; i < i1; ++i) loc += q_of(i);
+            unsigned long long inc = loc;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const unsigned long long y = shfl_up_u64(inc, d);
+                if (lane >= d) inc += y;
+            }
+            unsigned long long r = above + inc - loc;  // mass before this lane's first entry
+            unsigned long long P = ~0ull;
+            for (int i = i0; i < i1; ++i) {
+                if (static_cast<double>(r) >= thr) {
+                    P = r;
+                    break;
+                }
+                r += q_of(i);
+            }
+            // the first lane (in entry order) that found the crossing holds it;
+            // if none did, the bin's entries end before it (total below thr)
+            const unsigned found = __ballot_sync(0xFFFFFFFFu, P != ~0ull);
+            const int src = found ? __ffs(found) - 1 : 31;
+            const unsigned long long Pf = shfl_u64(found ? P : inc, src);
+            if (lane == 0) {
+                const unsigned long long end = above + Pf;  // (when not found: the bin's end)
+                if (found) {
+                    gs.pnuc = static_cast<double>(Pf);
+                    gs.lnuc = log(static_cast<double>(Pf) / S_fix);
+                } else if (static_cast<double>(end) >= thr) {
+                    // the first entry of the next bin crosses: the nucleus ends with this bin
+                    gs.pnuc = static_cast<double>(end);
+                    gs.lnuc = log(static_cast<double>(end) / S_fix);
+                } else {
+                    gs.pnuc = -1.0;  // the crossing lies in a bin below
+                }
+            }
+        }
+        G.sync();
+        const double P = gs.pnuc;
+        *log_nuc = gs.lnuc;
+        G.sync();
+        if (P > 0.0) return true;
+        if (bstar + 1 >= kNucBins) return false;
+        ++bstar;
+    }
+    return false;
+}
+
+// One warp walks the sorted entries cand[beg, beg + n) with error-free FP32
+// running sums that start at `base`, for the first entry whose preceding mass
+// reaches thr = (t_hi + t_lo): 32 entries at a time (one per lane, an
+// inclusive warp scan of their masses), stopping at the block that holds it.
+// gs.cross gets its index relative to beg (n + 1 if none); gs.pnuc the
+// nucleus mass: the running sum there, or the entries' total when it reaches
+// thr only after the last of them, or -1 when the nucleus reaches past them.
+__device__ void warp_walk(GroupShared& gs, int lane, int beg, int n, Pair base, float t_hi, float t_lo, float M,
+                          float kt) {
+    Pair run = base;
+    int cross = n + 1;
+    double P = -1.0;
+    for (int b0 = 0; b0 < n; b0 += 32) {
+        const int i = b0 + lane;
+        const float q = i < n ? ex2((float_of(static_cast<uint32_t>(gs.cand[beg + i] >> 32)) - M) * kt) : 0.0f;
+        Pair inc{q, 0.0f};
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const Pair y{__shfl_up_sync(0xFFFFFFFFu, inc.hi, d), __shfl_up_sync(0xFFFFFFFFu, inc.lo, d)};
+            if (lane >= d) inc = pair_add(y, inc);
+        }
+        Pair ex{__shfl_up_sync(0xFFFFFFFFu, inc.hi, 1), __shfl_up_sync(0xFFFFFFFFu, inc.lo, 1)};
+        if (lane == 0) ex = Pair{0.0f, 0.0f};
+        const Pair pre = pair_add(run, ex);  // mass before entry i
+        const bool hit = i < n && (pre.hi - t_hi) + (pre.lo - t_lo) >= 0.0f;
+        const unsigned hits = __ballot_sync(0xFFFFFFFFu, hit);
+        if (hits) {
+            const int src = __ffs(hits) - 1;
+            cross = b0 + src;
+            P = __shfl_sync(0xFFFFFFFFu, (double)pre.hi + (double)pre.lo, src);
+            break;
+        }
+        run = pair_add(run, Pair{__shfl_sync(0xFFFFFFFFu, inc.hi, 31), __shfl_sync(0xFFFFFFFFu, inc.lo, 31)});
+    }
+    if (cross > n && (run.hi - t_hi) + (run.lo - t_lo) >= 0.0f) P = (double)run.hi + (double)run.lo;
+    if (lane == 0) {
+        gs.cross = cross;
+        gs.pnuc = P;
+    }
+    __syncwarp();
 }
 
 // The one-pass path for one row, run by one thread group.  A sample (every
@@ -737,7 +1095,8 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
     const float* row = a.logits + t * a.stride;
     const int V = a.V, tid = G.tid, lane = G.lane, warp = G.warp;
     const int Kp = min(a.K, V);
-    if (4 * Kp > kCap) return false;
+    const bool use_p = a.top_p < 1.0f;
+    if ((use_p ? 6 : 4) * Kp > kCap) return false;
     const float kt = a.inv_t * kLog2e;
     const int nv4 = V >> 2;
     const float4* r4 = reinterpret_cast<const float4*>(row);
@@ -753,7 +1112,10 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
             smax = fmaxf(smax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
         }
         group_sort_keys_desc(gs, G, key_of(smax));
-        const int rank = min(kGT, max(8, (3 * Kp + kSampEvery - 1) / kSampEvery));
+        // about 3 K entries reach the threshold, 4 K with top_p < 1 (so that
+        // most nuclei end among them at the usual temperatures)
+        const int depth = use_p ? 4 : 3;
+        const int rank = min(kGT, max(8, (depth * Kp + kSampEvery - 1) / kSampEvery));
         tau = float_of(gs.keys[rank - 1]);
         o = float_of(gs.keys[0]);
         G.sync();
@@ -841,57 +1203,30 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
     group_sort_desc(gs, G, nc);
 
     // ---- the nucleus: one warp walks the sorted candidates with error-free
-    // FP32 running sums
+    // FP32 running sums; past them, the wide-nucleus passes
     int count = Kp;
     double log_nuc = 0.0;
-    if (a.top_p < 1.0f) {
-        if (warp == 0) {
-            const double thr = (double)a.top_p * S;
-            const float t_hi = (float)thr, t_lo = (float)(thr - (double)t_hi);
-            const int per = (nc + 31) / 32;
-            const int i0 = lane * per, i1 = min(nc, i0 + per);
-            auto mass = [&](int i) { return ex2((float_of(static_cast<uint32_t>(gs.cand[i] >> 32)) - M) * kt); };
-            Pair loc{0.0f, 0.0f};
-            for (int i = i0; i < i1; ++i) loc = pair_add(loc, Pair{mass(i), 0.0f});
-            // exclusive scan of the lanes' pairs, in lane order
-            Pair inc = loc;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const Pair y{__shfl_up_sync(0xFFFFFFFFu, inc.hi, d), __shfl_up_sync(0xFFFFFFFFu, inc.lo, d)};
-                if (lane >= d) inc = pair_add(y, inc);
-            }
-            const Pair all{__shfl_sync(0xFFFFFFFFu, inc.hi, 31), __shfl_sync(0xFFFFFFFFu, inc.lo, 31)};
-            Pair run{__shfl_up_sync(0xFFFFFFFFu, inc.hi, 1), __shfl_up_sync(0xFFFFFFFFu, inc.lo, 1)};
-            if (lane == 0) run = Pair{0.0f, 0.0f};
-            // first candidate whose preceding mass reaches thr
-            int mine = nc + 1;
-            for (int i = i0; i < i1; ++i) {
-                if ((run.hi - t_hi) + (run.lo - t_lo) >= 0.0f) {
-                    mine = i;
-                    break;
-                }
-                run = pair_add(run, Pair{mass(i), 0.0f});
-            }
-            int cross = mine;
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) cross = min(cross, __shfl_xor_sync(0xFFFFFFFFu, cross, o2));
-            if (lane == 0) {
-                gs.cross = cross;
-                if (cross > nc) gs.pnuc = (all.hi - t_hi) + (all.lo - t_lo) >= 0.0f ? (double)all.hi + (double)all.lo : -1.0;
-            }
-            if (mine == cross && cross <= nc) gs.pnuc = (double)run.hi + (double)run.lo;
-            __syncwarp();
-            // the one FP64 logarithm of the nucleus, in one thread (GB300's FP64
-            // rate is a small fraction of its FP32 rate)
-            if (lane == 0) gs.lnuc = gs.pnuc > 0.0 ? log(gs.pnuc / S) : 0.0;
-        }
+    if (use_p) {
+        const double thr = (double)a.top_p * S;
+        const float t_hi = (float)thr, t_lo = (float)(thr - (double)t_hi);
+        if (warp == 0) warp_walk(gs, lane, 0, nc, Pair{0.0f, 0.0f}, t_hi, t_lo, M, kt);
         G.sync();
         const int cross = gs.cross;
         const double P = gs.pnuc;
-        log_nuc = gs.lnuc;
         G.sync();
-        if (!(P > 0.0)) return false;  // the nucleus reaches below the candidates
-        count = min(Kp, cross <= nc ? cross : nc);
+        if (P > 0.0) count = min(Kp, cross <= nc ? cross : nc);
+        if (P > 0.0) {
+            // the one FP64 logarithm, in one thread (GB300's FP64 rate is a
+            // small fraction of its FP32 rate)
+            if (tid == 0) gs.lnuc = log(P / S);
+            G.sync();
+            log_nuc = gs.lnuc;
+            G.sync();
+        } else {
+            // every candidate (and so the top K) is in the nucleus
+            if (!wide_nucleus(gs, G, a, row, M, tau, nc, S, &log_nuc)) return false;
+            count = Kp;
+        }
     }
 
     // ---- outputs
@@ -912,34 +1247,72 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
     return true;
 }
 
-// Rows are dealt to the thread groups round robin (group b * kGroups + g of
-// the grid takes rows b * kGroups + g + k * groups).  Each group takes its
-// rows on the one-pass path; a row it cannot finish waits for the end of the
-// round, when the whole CTA takes the deferred rows on the exact path.
+// Without a workspace, rows are dealt to the thread groups round robin
+// (group b * kGroups + g of the grid takes rows b * kGroups + g + k * groups).
+// With one, each group takes its first row that way and every later row from
+// a counter in the workspace, one row per take with the next take always in
+// flight (its latency hides behind the row), so that the groups that drew
+// costly rows (a nucleus far below the candidates) take fewer rows.  Each
+// group takes its rows on the one-pass path; a row it cannot finish waits for
+// the end of the round, when the whole CTA takes the deferred rows on the
+// exact path.
 __global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_constant__ TopkArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     KernelShared& ks = *reinterpret_cast<KernelShared*>(smem_raw);
     const Group G{static_cast<int>(threadIdx.x) / kGT, static_cast<int>(threadIdx.x) % kGT,
                   static_cast<int>(threadIdx.x) & 31, (static_cast<int>(threadIdx.x) % kGT) >> 5};
     const long long ngroups = static_cast<long long>(gridDim.x) * kGroups;
-    const long long first = static_cast<long long>(blockIdx.x) * kGroups;  // this CTA's first group
-    // rounds: as many as the CTA's first group has rows (the others have at most as many)
-    const long long rows0 = first < a.T ? (a.T - first + ngroups - 1) / ngroups : 0;
+    const long long me = static_cast<long long>(blockIdx.x) * kGroups + G.id;  // this group's index
     if (threadIdx.x == 0) ks.ndefer = 0;
+    if (G.tid == 0) ks.gdone[G.id] = 0;
     __syncthreads();
-    for (long long k0 = 0; k0 < rows0; k0 += kRound) {
-        const long long k1 = min(rows0, k0 + kRound);
-        for (long long k = k0; k < k1; ++k) {
-            const long long t = first + G.id + k * ngroups;
-            if (t >= a.T) break;
+    long long k = 0;                  // rows this group has dealt itself
+    unsigned long long pend = 0ull;   // group thread 0: the value of the take in flight
+    if (a.ws && G.tid == 0 && me < a.T_static) pend = atomicAdd(a.ws + 2, 1ull);
+    bool done = false;                // this group has no rows left
+    for (;;) {
+        for (int r = 0; r < kRound && !done; ++r) {
+            long long t = me + k * ngroups;
+            if (t < a.T_static) {
+                ++k;
+            } else if (a.ws && me < a.T_static) {
+                // the take issued one row ago; issue the next
+                if (G.tid == 0) {
+                    ks.take[G.id] = static_cast<long long>(a.T_static + pend);
+                    if (a.T_static + pend < static_cast<unsigned long long>(a.T)) pend = atomicAdd(a.ws + 2, 1ull);
+                }
+                G.sync();
+                t = ks.take[G.id];
+                G.sync();
+            } else {
+                t = a.T;  // (no more rows: dealt out, or this group started past them)
+            }
+            if (t >= a.T) {
+                done = true;
+                break;
+            }
             if (!fast_row(ks.u.grp[G.id], G, a, t) && G.tid == 0) ks.defer[atomicAdd(&ks.ndefer, 1)] = t;
         }
+        if (G.tid == 0) ks.gdone[G.id] = done ? 1 : 0;
         __syncthreads();
         const int nd = ks.ndefer;
+        bool all_done = true;
+        for (int g = 0; g < kGroups; ++g) all_done = all_done && ks.gdone[g];
         for (int q = 0; q < nd; ++q) exact_row(ks.u.exact, a, ks.defer[q]);
         __syncthreads();
         if (threadIdx.x == 0) ks.ndefer = 0;
         __syncthreads();
+        if (all_done) break;
+    }
+    // The last CTA to finish leaves the workspace's words zero for the next
+    // launch (every CTA is past its last take by now).
+    if (a.ws && threadIdx.x == 0) {
+        __threadfence();
+        const unsigned long long fin = atomicAdd(a.ws + 3, 1ull);
+        if (fin == static_cast<unsigned long long>(gridDim.x) - 1ull) {
+            atomicExch(a.ws + 2, 0ull);
+            atomicExch(a.ws + 3, 0ull);
+        }
     }
 }
 
@@ -948,7 +1321,7 @@ __global__ void __launch_bounds__(kNT, 2) topk_capture_kernel(const __grid_const
 
 extern "C" int sc_topk_capture(const float* logits, long long T, int V, long long logits_stride, float inv_temperature,
                                int K, float top_p, int32_t* ids_out, float* logprobs_out, int32_t* count_out,
-                               sc_stream_t stream) {
+                               void* workspace, sc_stream_t stream) {
     using namespace sc;
     if (T < 0) return fail(SC_ERR_SHAPE, "T = %lld < 0", T);
     if (V < 1 || V > (1 << 24)) return fail(SC_ERR_SHAPE, "V = %d outside 1..2^24", V);
@@ -963,6 +1336,7 @@ extern "C" int sc_topk_capture(const float* logits, long long T, int V, long lon
         return fail(SC_ERR_ALIGN, "logits must be 16-byte aligned with a stride that is a multiple of 4");
     if (!aligned(ids_out, 4) || !aligned(logprobs_out, 4) || !aligned(count_out, 4))
         return fail(SC_ERR_ALIGN, "outputs must be 4-byte aligned");
+    if (!aligned(workspace, 16)) return fail(SC_ERR_ALIGN, "workspace must be 16-byte aligned");
     int dev = 0;
     int st = check_device(&dev);
     if (st != SC_OK) return st;
@@ -1000,6 +1374,11 @@ extern "C" int sc_topk_capture(const float* logits, long long T, int V, long lon
     ka.lps = logprobs_out;
     ka.counts = count_out;
     const long long g = T < grid ? T : grid;
+    // with a workspace, each thread group's first row is dealt at launch and
+    // the rest handed out at run time
+    ka.ws = static_cast<unsigned long long*>(workspace);
+    const long long ng = g * kGroups;
+    ka.T_static = workspace ? (T < ng ? T : ng) : T;
     topk_capture_kernel<<<static_cast<unsigned>(g), kNT, sizeof(KernelShared), reinterpret_cast<cudaStream_t>(stream)>>>(ka);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "topk_capture_kernel launch");

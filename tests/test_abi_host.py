@@ -50,7 +50,7 @@ def test_struct_layouts_match_header(L):
     assert (p.clip_low, p.clip_high, p.flag_layout) == (pytest.approx(0.2), pytest.approx(0.3), 0)
     assert (p.wait_limit_us, p.test_stall) == (0, 0)
     assert L.sc_params_default(None) == sc.SC_ERR_NULL
-    assert L.sc_abi_version() == 104
+    assert L.sc_abi_version() == 105
     assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
 
 
@@ -239,16 +239,18 @@ def test_rollout_mean_no_responses_is_a_no_op(L):
     (dict(logits=FAKE + 4), sc.SC_ERR_ALIGN),
     (dict(stride=66), sc.SC_ERR_ALIGN),
     (dict(cnt=FAKE * 4 + 2), sc.SC_ERR_ALIGN),
+    (dict(ws=FAKE * 5 + 8), sc.SC_ERR_ALIGN),
 ])
 def test_topk_capture_rejects_bad_arguments_on_the_host(L, kw, status):
-    a = dict(logits=FAKE, T=3, V=64, stride=64, inv_t=1.0, K=8, top_p=1.0, ids=FAKE * 2, lps=FAKE * 3, cnt=None)
+    a = dict(logits=FAKE, T=3, V=64, stride=64, inv_t=1.0, K=8, top_p=1.0, ids=FAKE * 2, lps=FAKE * 3, cnt=None,
+             ws=None)
     a.update(kw)
     assert L.sc_topk_capture(a["logits"], a["T"], a["V"], a["stride"], a["inv_t"], a["K"], a["top_p"], a["ids"],
-                             a["lps"], a["cnt"], None) == status, err(L)
+                             a["lps"], a["cnt"], a["ws"], None) == status, err(L)
 
 
 def test_topk_capture_empty_batch_is_a_no_op(L):
-    assert L.sc_topk_capture(None, 0, 64, 64, 1.0, 8, 1.0, None, None, None, None) == sc.SC_OK
+    assert L.sc_topk_capture(None, 0, 64, 64, 1.0, 8, 1.0, None, None, None, None, None) == sc.SC_OK
 
 
 def call_lmhead(L, T=4, d=64, V=100, hidden=FAKE, w=FAKE * 2, ids=FAKE * 3, lps=FAKE * 4, samp=FAKE * 5,

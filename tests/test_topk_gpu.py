@@ -48,25 +48,46 @@ def run(z, K, inv_t, top_p, stride=None):
     return ids.cpu().numpy(), lp.cpu().numpy(), cnt.cpu().numpy()
 
 
-def boundary_is_clear(z_row, inv_t, top_p, rel=1e-6):
-    """False when the nucleus boundary sits within rounding of top_p."""
+def boundary_is_clear(z_row, inv_t, top_p, K, rel=1e-6):
+    """(clear, extra) for one row's nucleus boundary, from FP64.
+
+    An entry whose preceding mass lies within `rel` of top_p may fall on
+    either side of the boundary under rounding.  When such an entry could
+    change the count (its position is within the first K), the row is not
+    clear.  Otherwise the ids and the count are fixed, and only the nucleus
+    mass, and with it every recorded log-probability, can move by the mass of
+    one such entry: `extra` is the largest of those masses over the nucleus
+    mass (0 when no entry is that close)."""
     if top_p >= 1.0:
-        return True
+        return True, 0.0
     x = z_row.astype(np.float64) * inv_t
     order = np.lexsort((np.arange(x.size), -x))
     p = np.exp(x[order] - x.max())
     p /= p.sum()
     before = np.concatenate([[0.0], np.cumsum(p)[:-1]])
-    return bool(np.all(np.abs(before - top_p) > rel))
+    near = np.nonzero(np.abs(before - top_p) <= rel)[0]
+    if near.size == 0:
+        return True, 0.0
+    if near.min() <= K:
+        return False, 0.0
+    nucleus = p[before < top_p].sum()
+    return True, float(p[np.clip(np.concatenate([near - 1, near]), 0, p.size - 1)].max() / nucleus)
 
 
-def check(z, K, inv_t, top_p, what, stride=None, lp_tol=2e-6):
+def check(z, K, inv_t, top_p, what, stride=None, lp_tol=2e-6, rows=None):
+    """GPU capture of every row of z, compared with the oracle on `rows` (all by default)."""
     ids, lp, cnt = run(z, K, inv_t, top_p, stride)
+    if rows is not None:
+        sel = torch.as_tensor(np.asarray(rows), device=z.device)
+        z = z.index_select(0, sel)
+        ids, lp, cnt = ids[rows], lp[rows], cnt[rows]
     zc = z.cpu().numpy()
     oids, olp, ocnt = oracle.topk_capture(zc, K, inv_t, top_p)
-    clear = np.array([boundary_is_clear(zc[t], inv_t, top_p) for t in range(zc.shape[0])])
+    verdicts = [boundary_is_clear(zc[t], inv_t, top_p, K) for t in range(zc.shape[0])]
+    clear = np.array([v[0] for v in verdicts])
     assert clear.sum() >= max(1, zc.shape[0] // 2), f"{what}: too few unambiguous rows"
     for t in np.nonzero(clear)[0]:
+        row_tol = lp_tol + verdicts[t][1]
         assert cnt[t] == ocnt[t], f"{what} row {t}: count {cnt[t]} vs {ocnt[t]}"
         np.testing.assert_array_equal(ids[t], oids[t], err_msg=f"{what} row {t}: ids")
         c = ocnt[t]
@@ -74,7 +95,7 @@ def check(z, K, inv_t, top_p, what, stride=None, lp_tol=2e-6):
         assert np.array_equal(lp[t, :c][~fin], olp[t, :c][~fin]), f"{what} row {t}: infinite logprobs"
         a, o = lp[t, :c][fin].astype(np.float64), olp[t, :c][fin].astype(np.float64)
         err = np.abs(a - o) / (1 + np.abs(o))
-        assert np.all(err <= lp_tol), f"{what} row {t}: logprob error {err.max():.3g} at {int(err.argmax())}"
+        assert np.all(err <= row_tol), f"{what} row {t}: logprob error {err.max():.3g} at {int(err.argmax())}"
         assert np.all(lp[t, c:] == 0)
     return ids, lp, cnt
 
@@ -121,3 +142,40 @@ def test_deterministic_across_calls():
     b = run(z, 128, 1 / 0.7, 0.95)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("inv_t,top_p", [(1.0, 0.95), (1.0, 0.99), (1 / 0.7, 0.99)])
+def test_nucleus_far_below_the_candidates(inv_t, top_p):
+    # flat rows: nuclei of thousands of entries, beyond the one-pass
+    # candidates, so their mass comes from the histogram and crossing-bin passes
+    z = sampler_logits("C2", 48)
+    _, _, cnt = check(z, 128, inv_t, top_p, f"wide nucleus inv_t={inv_t} top_p={top_p}")
+    assert np.mean(cnt == 128) > 0.5
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("inv_t,top_p", [(1 / 0.7, 0.95), (1.0, 0.95)])
+def test_full_batch_sampled_rows(inv_t, top_p):
+    # all 4096 rows of the quick-check batch's sampler logits through the
+    # persistent grid (rounds of rows per thread group, rows left to the exact
+    # path between rounds); 192 sampled rows and the first and last compared
+    z = sampler_logits("C2", 4096, seed=7)
+    rng = np.random.default_rng(4096)
+    rows = np.unique(np.concatenate([[0, 4095], rng.choice(4096, 192, replace=False)]))
+    check(z, 128, inv_t, top_p, f"4096 rows inv_t={inv_t} top_p={top_p}", rows=rows)
+
+
+@pytest.mark.slow
+def test_run_time_hand_out_matches_the_launch_deal_and_leaves_the_workspace_zero():
+    # the same rows with the last eighth handed out at run time and with every
+    # row dealt at launch: the same bits (every sum has a fixed order)
+    z = sampler_logits("C2", 2048, seed=9)
+    outs = []
+    for dynamic in (True, False, True):
+        ids, lp, cnt = sc.sc_topk_capture(z, 128, 1 / 0.7, 0.95, dynamic=dynamic)
+        torch.cuda.synchronize()
+        outs.append((ids.cpu(), lp.cpu(), cnt.cpu()))
+    for o in outs[1:]:
+        for x, y in zip(outs[0], o):
+            assert torch.equal(x, y)
+    assert int(sc.workspace(torch.device("cuda")).abs().sum().item()) == 0
