@@ -372,11 +372,15 @@ int sc_center_forward_backward_noalloc(const uint16_t* logits, long long T, int 
  * dw          : FP32 [V, d], written (not accumulated across calls):
  *               dW = g^T H.
  * logp_out, diag_out, status_dev : as sc_center_forward_backward.
- * workspace   : sc_lmhead_workspace_bytes(block_rows, V) bytes of device
+ * workspace   : sc_lmhead_workspace_bytes(block_rows, V, d) bytes of device
  *               memory, 256-byte aligned; its first SC_WORKSPACE_BYTES must
  *               be zero before the first call (they are left zero, as for
  *               sc_center_forward_backward).  It holds the block of logits
- *               (bf16 [block_rows, V rounded up to 8]).  Calls that may run
+ *               (bf16 [block_rows, V rounded up to 8]) and, when dH's
+ *               output tiles are too few for the SMs (block_rows / 128 x
+ *               d / 256 tiles), FP32 slices of dH's partial products over
+ *               parts of the vocabulary, summed in a fixed order.  Its size
+ *               depends on the current device's SM count.  Calls that may run
  *               at the same time need workspaces of their own.
  * Per block: z_b = H_b W^T (sc_gemm_bf16: FP32 accumulation, bf16 logits),
  * the fused score-centering kernel in place, dH_b = g_b W and dW (+)= g_b^T
@@ -412,7 +416,7 @@ int sc_gemm_bf16(const uint16_t* A, long long lda, int a_layout, const uint16_t*
                  void* C, long long ldc, int c_mode, long long M, long long N, long long K, uint32_t* status_dev,
                  sc_stream_t stream);
 
-size_t sc_lmhead_workspace_bytes(long long block_rows, int V);
+size_t sc_lmhead_workspace_bytes(long long block_rows, int V, int d);
 int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t* w, long long T, int d, int V,
                                const int32_t* rec_ids, const float* rec_logprobs, const int32_t* rec_count,
                                const int32_t* sampled_id, const float* rollout_logprob,

@@ -128,7 +128,7 @@ def lib():
             L.sc_center_forward_backward_noalloc.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp, vp, vp, vp, i32,
                                                              ctypes.POINTER(Params), vp, i64, vp, vp, vp, vp]
             L.sc_center_forward_backward_noalloc.restype = i32
-            L.sc_lmhead_workspace_bytes.argtypes = [i64, i32]
+            L.sc_lmhead_workspace_bytes.argtypes = [i64, i32, i32]
             L.sc_lmhead_workspace_bytes.restype = ctypes.c_size_t
             L.sc_lmhead_forward_backward.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, vp, i32,
                                                      ctypes.POINTER(Params), i64, vp, vp, vp, vp, vp, vp,
@@ -546,7 +546,7 @@ def sc_lmhead_forward_backward(hidden: torch.Tensor, w: torch.Tensor, rec_ids, r
     hidden bf16 [T, d], w bf16 [V, d] (contiguous, d % 8 == 0); the other
     inputs as :func:`sc_center_forward_backward`.  Returns (dhidden bf16
     [T, d], dw float32 [V, d], logp_out, diag_out).  workspace_buf: a uint8
-    tensor of sc_lmhead_workspace_bytes(block_rows, V) zero-initialised
+    tensor of sc_lmhead_workspace_bytes(block_rows, V, d) zero-initialised
     bytes; by default the binding's own for this device, stream and size.
     """
     dev = hidden.device
@@ -581,7 +581,7 @@ def sc_lmhead_forward_backward(hidden: torch.Tensor, w: torch.Tensor, rec_ids, r
     if T == 0:
         return dhidden, dw, logp_out, diag_out
     L = lib()
-    need = int(L.sc_lmhead_workspace_bytes(min(int(block_rows), T), V))
+    need = int(L.sc_lmhead_workspace_bytes(min(int(block_rows), T), V, d))
     if workspace_buf is None:
         s_obj = torch.cuda.current_stream(dev) if stream is None else stream
         key = (dev.index, int(s_obj.cuda_stream), need)

@@ -103,6 +103,6 @@ const char* sc_status_string(int status) {
 
 const char* sc_last_error(void) { return sc::last_error_text(); }
 
-int sc_abi_version(void) { return 105; }
+int sc_abi_version(void) { return 106; }
 
 }  // extern "C"

@@ -64,7 +64,9 @@ struct GemmArgs {
     void* C;           // C itself, for the columns past N_full (plain stores)
     long long ldc;
     int num_m, num_n, k_steps;
-    long long tiles;
+    int k_splits, kps;  // split-K: the K steps of a tile in k_splits ranges of kps
+    long long c_split_rows;  // split s stores its rows at C row s * c_split_rows + m
+    long long tiles;    // output tiles times k_splits
     int a_mn, b_mn;   // operand majorness: 0 K-major, 1 M- / N-major
     int c_mode;       // 0 bf16 store, 1 FP32 store, 2 FP32 reduce-add
     int m_fastest;    // tile order: consecutive tiles share their B tile (1) or their A tile (0)
@@ -209,14 +211,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g.status) atomicOr(g.status, kStatusTimeout);
         *abort_flag = 1;
     };
-    auto tile_coords = [&](long long t, int& mt, int& nt) {
+    // tile t: split t / (num_m num_n) (the slowest index, so that consecutive
+    // tiles share operand tiles as within one split), then m and n in the
+    // chosen order; its K steps [ks0, ks1)
+    auto tile_coords = [&](long long t, int& mt, int& nt, int& ks0, int& ks1) {
+        const long long t2 = static_cast<long long>(g.num_m) * g.num_n;
+        const int split = static_cast<int>(t / t2);
+        const long long r = t - split * t2;
         if (g.m_fastest) {
-            mt = static_cast<int>(t % g.num_m);
-            nt = static_cast<int>(t / g.num_m);
+            mt = static_cast<int>(r % g.num_m);
+            nt = static_cast<int>(r / g.num_m);
         } else {
-            nt = static_cast<int>(t % g.num_n);
-            mt = static_cast<int>(t / g.num_n);
+            nt = static_cast<int>(r % g.num_n);
+            mt = static_cast<int>(r / g.num_n);
         }
+        ks0 = split * g.kps;
+        ks1 = min(g.k_steps, ks0 + g.kps);
     };
 
     if (warp == 0) {
@@ -224,10 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;  // stages issued
             for (long long t = blockIdx.x; t < g.tiles && !*abort_flag; t += gridDim.x) {
-                int mt, nt;
-                tile_coords(t, mt, nt);
+                int mt, nt, ks0, ks1;
+                tile_coords(t, mt, nt, ks0, ks1);
                 const int m0 = mt * BM, n0 = nt * BN;
-                for (int ks = 0; ks < g.k_steps; ++ks, ++it) {
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     if (it >= static_cast<uint32_t>(kStages) &&
                         !mbar_wait_bounded(empty(s), ((it / kStages) - 1u) & 1u, kWaitNs)) {
@@ -269,7 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(acc * BN);
-                for (int ks = 0; ks < g.k_steps; ++ks, ++it) {
+                int mt, nt, ks0, ks1;
+                tile_coords(t, mt, nt, ks0, ks1);
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = static_cast<int>(it % kStages);
                     if (!mbar_wait_bounded(full(s), (it / kStages) & 1u, kWaitNs)) {
                         give_up();
@@ -281,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc_mma(d, operand_desc(sa, g.a_mn, kk), operand_desc(sb, g.b_mn, kk), g.idesc,
-                               (ks | kk) != 0 ? 1u : 0u);
+                               (ks != ks0 || kk != 0) ? 1u : 0u);
                     tc_commit(empty(s));  // the stage is free once these MMAs have read it
                 }
                 if (ok) tc_commit(acc_full(acc));
@@ -306,9 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            int mt, nt;
-            tile_coords(t, mt, nt);
+            int mt, nt, ks0, ks1;
+            tile_coords(t, mt, nt, ks0, ks1);
             const long long r0 = static_cast<long long>(mt) * BM + 32 * q;
+            const long long roff = g.kps > 0 ? static_cast<long long>(ks0 / g.kps) * g.c_split_rows : 0;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(acc * BN);
             for (int c = 0; c < nchunks; ++c) {
                 const long long c0 = static_cast<long long>(nt) * BN + c * cols;
@@ -326,17 +339,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // columns [max(c0, N_full), N) of this thread's row, one by one
                     const long long row = r0 + lane;
                     if (row < g.M) {
+                        const long long crow = roff + row;
 #pragma unroll
                         for (int j = 0; j < 64; ++j) {
                             const long long col = c0 + j;
                             if (j < cols && col >= g.N_full && col < g.N) {
                                 if (g.c_mode == 0) {
-                                    uint16_t* cp = static_cast<uint16_t*>(g.C) + row * g.ldc + col;
+                                    uint16_t* cp = static_cast<uint16_t*>(g.C) + crow * g.ldc + col;
                                     *cp = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(v[j]), 0.0f) & 0xFFFFu);
                                 } else if (g.c_mode == 1) {
-                                    static_cast<float*>(g.C)[row * g.ldc + col] = __uint_as_float(v[j]);
+                                    static_cast<float*>(g.C)[crow * g.ldc + col] = __uint_as_float(v[j]);
                                 } else {
-                                    atomicAdd(static_cast<float*>(g.C) + row * g.ldc + col, __uint_as_float(v[j]));
+                                    atomicAdd(static_cast<float*>(g.C) + crow * g.ldc + col, __uint_as_float(v[j]));
                                 }
                             }
                         }
@@ -367,9 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) {
                     if (g.c_mode == 2)
-                        tma_reduce_add_2d(&tmC, static_cast<int>(c0), static_cast<int>(r0), buf);
+                        tma_reduce_add_2d(&tmC, static_cast<int>(c0), static_cast<int>(roff + r0), buf);
                     else
-                        tma_store_2d(&tmC, static_cast<int>(c0), static_cast<int>(r0), buf);
+                        tma_store_2d(&tmC, static_cast<int>(c0), static_cast<int>(roff + r0), buf);
                     bulk_commit_group();
                 }
                 ++nst;
@@ -445,11 +459,12 @@ uint32_t instr_desc(int a_mn, int b_mn) {
 
 int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, long long ldb, int b_mn, void* C,
               long long ldc, int c_mode, long long M, long long N, long long K, int m_fastest, uint32_t* status,
-              cudaStream_t stream) {
+              cudaStream_t stream, int k_splits) {
     if (M < 1 || N < 1 || K < 1) return fail(SC_ERR_SHAPE, "GEMM sizes M=%lld N=%lld K=%lld must be >= 1", M, N, K);
     if (M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31))
         return fail(SC_ERR_SHAPE, "GEMM sizes must be below 2^31");
     if (c_mode < 0 || c_mode > 2) return fail(SC_ERR_ARG, "c_mode = %d", c_mode);
+    if (k_splits < 1 || (k_splits > 1 && c_mode != 1)) return fail(SC_ERR_ARG, "split K stores FP32 slices");
     if (!A || !B || !C) return fail(SC_ERR_NULL, "A, B and C are required");
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(status, 4))
         return fail(SC_ERR_ALIGN, "A, B and C must be 16-byte aligned");
@@ -471,8 +486,14 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     const long long per16 = 16 / cesize;              // elements in a 16-byte unit
     const long long n_full = N / per16 * per16;        // columns the tensor stores cover
     const long long n_map = n_full > 0 ? n_full : per16;  // (a map needs a nonzero extent; unused then)
-    st = c_mode == 0 ? make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, n_map, ldc, 64, 32)
-                     : make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, n_map, ldc, 32, 32);
+    // with split K, C holds one slice of round_up(M, BM) rows per split
+    const long long ksteps = (K + BK - 1) / BK;
+    const long long kps = (ksteps + k_splits - 1) / k_splits;
+    const long long splits = (ksteps + kps - 1) / kps;  // (no empty ranges)
+    const long long m_pad = (M + BM - 1) / BM * BM;
+    const long long c_rows = splits > 1 ? splits * m_pad : M;
+    st = c_mode == 0 ? make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c_rows, n_map, ldc, 64, 32)
+                     : make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c_rows, n_map, ldc, 32, 32);
     if (st != SC_OK) return st;
     int dev = 0;
     st = check_device(&dev);
@@ -502,8 +523,11 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     ga.ldc = ldc;
     ga.num_m = static_cast<int>((M + BM - 1) / BM);
     ga.num_n = static_cast<int>((N + BN - 1) / BN);
-    ga.k_steps = static_cast<int>((K + BK - 1) / BK);
-    ga.tiles = static_cast<long long>(ga.num_m) * ga.num_n;
+    ga.k_steps = static_cast<int>(ksteps);
+    ga.kps = static_cast<int>(kps);
+    ga.k_splits = static_cast<int>(splits);
+    ga.c_split_rows = splits > 1 ? m_pad : 0;
+    ga.tiles = static_cast<long long>(ga.num_m) * ga.num_n * ga.k_splits;
     ga.a_mn = a_mn ? 1 : 0;
     ga.b_mn = b_mn ? 1 : 0;
     ga.c_mode = c_mode;
@@ -517,6 +541,103 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     return SC_OK;
 }
 
+namespace {
+
+// The sum of `splits` FP32 slices [rows][cols] (row stride lds, slice s
+// starting s * slice rows further) -> bf16 (row stride ldd), round to nearest
+// even; the slices added in slice order.  Eight columns per thread.
+__global__ void sum_slices_to_bf16_kernel(const float* src, long long lds, long long slice, int splits, uint16_t* dst,
+                                          long long ldd, long long rows, long long cols) {
+    const long long c8 = (cols + 7) / 8;
+    const long long n = rows * c8;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / c8, c = (i - r * c8) * 8;
+        uint16_t* dp = dst + r * ldd + c;
+        if (c + 8 <= cols) {
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+            for (int sp = 0; sp < splits; ++sp) {
+                const float* p = src + (sp * slice + r) * lds + c;
+                const float4 x = *reinterpret_cast<const float4*>(p);
+                const float4 y = *reinterpret_cast<const float4*>(p + 4);
+                a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+                b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+            }
+            uint4 o;
+            o.x = pack_bf16x2(a.x, a.y);
+            o.y = pack_bf16x2(a.z, a.w);
+            o.z = pack_bf16x2(b.x, b.y);
+            o.w = pack_bf16x2(b.z, b.w);
+            *reinterpret_cast<uint4*>(dp) = o;
+        } else {
+            for (long long j = 0; c + j < cols; ++j) {
+                float v = 0.0f;
+                for (int sp = 0; sp < splits; ++sp) v += src[(sp * slice + r) * lds + c + j];
+                dp[j] = static_cast<uint16_t>(pack_bf16x2(v, 0.0f) & 0xFFFFu);
+            }
+        }
+    }
+}
+
+}  // namespace
+
+// Splits of K that fill the SMs best for an M x N output: the count in 1..8
+// whose tiles come closest to whole waves (the smallest on a tie).
+int best_k_splits(long long M, long long N, long long K, int sms) {
+    const long long tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const long long ksteps = (K + BK - 1) / BK;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= 8 && s <= ksteps / 8 + 1; ++s) {
+        const double waves = static_cast<double>(tiles * s) / sms;
+        const double eff = waves / static_cast<double>((tiles * s + sms - 1) / sms);
+        if (eff > best_eff + 1e-3) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+int sm_count(int* out) {
+    int dev = 0;
+    int st = check_device(&dev);
+    if (st != SC_OK) return st;
+    std::lock_guard<std::mutex> lock(g_gemm_mutex);
+    if (!g_sm_count.count(dev)) {
+        int n = 0;
+        const cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SMs)");
+        g_sm_count[dev] = n;
+    }
+    *out = g_sm_count[dev];
+    return SC_OK;
+}
+
+// Rows of the FP32 slices gemm_bf16_split needs for an M-row product.
+long long split_slice_rows(long long M) { return (M + BM - 1) / BM * BM; }
+
+// C (bf16) = A . B with K split `k_splits` ways: split s stores its FP32
+// partial product in slice s of acc (split_slice_rows(M) rows each, row
+// stride ldacc, a multiple of 4), and one kernel adds the slices in slice order
+// and rounds the sum to C -- the same bits whatever order the tiles ran in.
+int gemm_bf16_split(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, long long ldb, int b_mn,
+                    uint16_t* C, long long ldc, float* acc, long long ldacc, long long M, long long N, long long K,
+                    int m_fastest, int k_splits, uint32_t* status, cudaStream_t stream) {
+    if (k_splits <= 1)
+        return gemm_bf16(A, lda, a_mn, B, ldb, b_mn, C, ldc, 0, M, N, K, m_fastest, status, stream, 1);
+    int st = gemm_bf16(A, lda, a_mn, B, ldb, b_mn, acc, ldacc, 1, M, N, K, m_fastest, status, stream, k_splits);
+    if (st != SC_OK) return st;
+    const long long ksteps = (K + BK - 1) / BK, kps = (ksteps + k_splits - 1) / k_splits;
+    const int splits = static_cast<int>((ksteps + kps - 1) / kps);
+    const long long work = M * ((N + 7) / 8);
+    const int blocks = static_cast<int>(work / 256 + 1 < 4096 ? work / 256 + 1 : 4096);
+    sum_slices_to_bf16_kernel<<<blocks, 256, 0, stream>>>(acc, ldacc, split_slice_rows(M), splits, C, ldc, M, N);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "sum_slices_to_bf16_kernel launch");
+    return SC_OK;
+}
+
 }  // namespace sc
 
 extern "C" int sc_gemm_bf16(const uint16_t* A, long long lda, int a_layout, const uint16_t* B, long long ldb,
@@ -525,8 +646,11 @@ extern "C" int sc_gemm_bf16(const uint16_t* A, long long lda, int a_layout, cons
     using namespace sc;
     if (a_layout != 0 && a_layout != 1) return fail(SC_ERR_ARG, "a_layout = %d", a_layout);
     if (b_layout != 0 && b_layout != 1) return fail(SC_ERR_ARG, "b_layout = %d", b_layout);
-    const int st = gemm_bf16(A, lda, a_layout, B, ldb, b_layout, C, ldc, c_mode, M, N, K, 1, status_dev,
-                             reinterpret_cast<cudaStream_t>(stream));
+    // consecutive output tiles share the larger operand's tile, so that it
+    // streams from HBM once while the smaller one is re-read from L2
+    const int m_fastest = M <= N ? 1 : 0;
+    const int st = gemm_bf16(A, lda, a_layout, B, ldb, b_layout, C, ldc, c_mode, M, N, K, m_fastest, status_dev,
+                             reinterpret_cast<cudaStream_t>(stream), 1);
     if (st != SC_OK) return st;
     return ok();
 }

@@ -10,7 +10,9 @@
 // block_rows, each block
 //   1. z_b = H_b W^T          tensor-core GEMM (sc_gemm.cu), FP32 accumulate -> bf16
 //   2. g_b from z_b           the fused score-centering kernel, in place
-//   3. dH_b = g_b W           tensor-core GEMM, W read N-major, -> bf16
+//   3. dH_b = g_b W           tensor-core GEMM, W read N-major, -> bf16 (K = V
+//                             split into FP32 slices summed in a fixed order
+//                             when the output tiles are too few for the SMs)
 //   4. dW  (+)= g_b^T H_b     tensor-core GEMM, g read M-major, FP32 (stored by
 //                             block 0, added by the tensor-store engine after)
 // all on the caller's stream, so only one [block_rows, V] buffer is needed.
@@ -31,10 +33,36 @@ inline long long row_stride_for(int V) { return (static_cast<long long>(V) + 7) 
 }  // namespace
 }  // namespace sc
 
-extern "C" size_t sc_lmhead_workspace_bytes(long long block_rows, int V) {
+namespace sc {
+namespace {
+
+// K splits of the dH = g W product for blocks of n rows (its n/128 x d/256
+// output tiles are few next to the SMs): the count that fills whole waves
+// best on the current device (148 SMs assumed without one).
+int dh_splits(long long n, int d, int V) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+        (void)cudaGetLastError();  // (no device here: a size query only)
+        sms = 148;
+    }
+    return best_k_splits(n, d, V, sms);
+}
+
+// FP32 rows the workspace holds for the split dH of blocks of Tb rows.
+long long dh_acc_rows(long long Tb, int d, int V) {
+    const int s = dh_splits(Tb, d, V);
+    return s > 1 ? s * split_slice_rows(Tb) : 0;
+}
+
+}  // namespace
+}  // namespace sc
+
+extern "C" size_t sc_lmhead_workspace_bytes(long long block_rows, int V, int d) {
     using namespace sc;
-    if (block_rows < 1 || V < 1) return 0;
-    return kScHeader + round_up(static_cast<size_t>(block_rows) * row_stride_for(V) * 2, 256);
+    if (block_rows < 1 || V < 1 || d < 1) return 0;
+    const size_t acc = static_cast<size_t>(dh_acc_rows(block_rows, d, V)) * static_cast<size_t>(d) * 4;
+    return kScHeader + round_up(static_cast<size_t>(block_rows) * row_stride_for(V) * 2, 256) + round_up(acc, 256);
 }
 
 extern "C" int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t* w, long long T, int d, int V,
@@ -66,9 +94,9 @@ extern "C" int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t
         !aligned(workspace, 256))
         return fail(SC_ERR_ALIGN, "hidden, w, dhidden and dw must be 16-byte aligned, workspace 256-byte aligned");
     const long long Tb = block_rows < T ? block_rows : T;
-    if (workspace_bytes < sc_lmhead_workspace_bytes(Tb, V))
+    if (workspace_bytes < sc_lmhead_workspace_bytes(Tb, V, d))
         return fail(SC_ERR_SHAPE, "workspace holds %zu bytes, %zu needed", workspace_bytes,
-                    sc_lmhead_workspace_bytes(Tb, V));
+                    sc_lmhead_workspace_bytes(Tb, V, d));
     int dev = 0;
     int st = check_device(&dev);
     if (st != SC_OK) return st;
@@ -76,6 +104,8 @@ extern "C" int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t
     void* sc_ws = ws;
     uint16_t* zbuf = reinterpret_cast<uint16_t*>(ws + kScHeader);
     const long long Vs = row_stride_for(V);
+    float* acc = reinterpret_cast<float*>(ws + kScHeader + round_up(static_cast<size_t>(Tb) * Vs * 2, 256));
+    const long long acc_rows = dh_acc_rows(Tb, d, V);
     const int K = p->K_max;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (long long t0 = 0; t0 < T; t0 += Tb) {
@@ -83,7 +113,7 @@ extern "C" int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t
         const uint16_t* Hb = hidden + t0 * d;
         // 1. z_b [n x V] = H_b [n x d] . W^T: both operands K-major; consecutive
         //    tiles share W's tile (read once from HBM per block)
-        st = gemm_bf16(Hb, d, 0, w, d, 0, zbuf, Vs, 0, n, V, d, 1, status_dev, s);
+        st = gemm_bf16(Hb, d, 0, w, d, 0, zbuf, Vs, 0, n, V, d, 1, status_dev, s, 1);
         if (st != SC_OK) return st;
         // 2. the score-centered gradient of the block, in place
         st = sc_center_forward_backward(zbuf, n, V, Vs, K ? rec_ids + t0 * K : nullptr,
@@ -92,12 +122,17 @@ extern "C" int sc_lmhead_forward_backward(const uint16_t* hidden, const uint16_t
                                         row_response + t0, adv, n_resp, p, zbuf, Vs, logp_out + t0,
                                         diag_out ? diag_out + t0 : nullptr, status_dev, sc_ws, stream);
         if (st != SC_OK) return st;
-        // 3. dH_b [n x d] = g_b [n x V] . W [V x d]: W read N-major
-        st = gemm_bf16(zbuf, Vs, 0, w, d, 1, dhidden + t0 * d, d, 0, n, d, V, 1, status_dev, s);
+        // 3. dH_b [n x d] = g_b [n x V] . W [V x d]: W read N-major; K = V split
+        //    when the n/128 x d/256 output tiles would leave SMs idle
+        int splits = dh_splits(n, d, V);  // (a shorter last block: as many as its slices fit)
+        if (splits > 1 && splits * split_slice_rows(n) > acc_rows)
+            splits = static_cast<int>(acc_rows / split_slice_rows(n));
+        st = gemm_bf16_split(zbuf, Vs, 0, w, d, 1, dhidden + t0 * d, d, acc, d, n, d, V, 1, splits > 1 ? splits : 1,
+                             status_dev, s);
         if (st != SC_OK) return st;
         // 4. dW [V x d] (+)= g_b^T [V x n] . H_b [n x d]: g read M-major, H_b N-major;
         //    consecutive tiles share g's tile
-        st = gemm_bf16(zbuf, Vs, 1, Hb, d, 1, dw, d, t0 == 0 ? 1 : 2, V, d, n, 0, status_dev, s);
+        st = gemm_bf16(zbuf, Vs, 1, Hb, d, 1, dw, d, t0 == 0 ? 1 : 2, V, d, n, 0, status_dev, s, 1);
         if (st != SC_OK) return st;
     }
     return ok();

@@ -50,7 +50,7 @@ def test_struct_layouts_match_header(L):
     assert (p.clip_low, p.clip_high, p.flag_layout) == (pytest.approx(0.2), pytest.approx(0.3), 0)
     assert (p.wait_limit_us, p.test_stall) == (0, 0)
     assert L.sc_params_default(None) == sc.SC_ERR_NULL
-    assert L.sc_abi_version() == 105
+    assert L.sc_abi_version() == 106
     assert L.sc_status_string(sc.SC_ERR_ALIGN) == b"misaligned pointer or stride"
 
 
@@ -258,7 +258,7 @@ def call_lmhead(L, T=4, d=64, V=100, hidden=FAKE, w=FAKE * 2, ids=FAKE * 3, lps=
                 ws_bytes=None, block_rows=2, **pk):
     p = sc.params(**{"K_max": 8, **pk})
     if ws_bytes is None:
-        ws_bytes = L.sc_lmhead_workspace_bytes(min(block_rows, T) if block_rows > 0 else 1, V)
+        ws_bytes = L.sc_lmhead_workspace_bytes(min(block_rows, T) if block_rows > 0 else 1, V, d if d > 0 else 8)
     return L.sc_lmhead_forward_backward(hidden, w, T, d, V, ids, lps, None, samp, None, resp, adv, 2,
                                         ctypes.byref(p), block_rows, dh, dw, logp, None, None, ws, ws_bytes, None)
 
@@ -285,11 +285,13 @@ def test_lmhead_rejects_bad_arguments_on_the_host(L, kw, status):
 
 
 def test_lmhead_workspace_size(L):
-    assert L.sc_lmhead_workspace_bytes(0, 100) == 0
-    small = L.sc_lmhead_workspace_bytes(1, 100)
-    big = L.sc_lmhead_workspace_bytes(1024, 151936)
-    # the block of logits (rows padded to a multiple of 8 entries) on top of a fixed part
-    assert big - small == 1024 * 151936 * 2 - 256 and big % 256 == 0
+    assert L.sc_lmhead_workspace_bytes(0, 100, 64) == 0
+    small = L.sc_lmhead_workspace_bytes(1, 100, 64)
+    assert small == 256 + 256  # the fixed part and one row of logits, padded
+    # 4096 rows, d = 4096, V = 151936 (148 SMs without a GPU): the block of
+    # logits and two FP32 slices of dH (32 x 16 output tiles split in two)
+    big = L.sc_lmhead_workspace_bytes(4096, 151936, 4096)
+    assert big == 256 + 4096 * 151936 * 2 + 2 * 4096 * 4096 * 4 and big % 256 == 0
 
 
 @pytest.mark.parametrize("args,status", [
