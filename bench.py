@@ -498,6 +498,41 @@ def make_host_rows(cfg, n):
     return synth.make_batch(sub, device="cpu")
 
 
+def profile_run(args):
+    """Small launches for a profiler (no timing, no JSON line):
+    `topk`: three launches of the top-K capture on the quick-check batch's
+    sampler logits at --top-p / --inv-t; `gemm`: the logits product at 1024
+    rows (H [1024, 4096] W^T, V = 151936, bf16 out) and the head-gradient
+    product on a quarter vocabulary (g^T [37984, 1024] H [1024, 4096], FP32
+    out), one launch each."""
+    import precision_off_policy_gb300 as sc
+
+    sc.build()
+    dev = torch.device("cuda", 0)
+    if args.profile == "topk":
+        cfg = synth.config(WORKLOAD)
+        b = synth.make_batch(cfg, device=dev)
+        g = torch.Generator(device=dev).manual_seed(cfg["seed"] + 77)
+        z = b["logits"].float()
+        z.add_(torch.randn(z.shape, generator=g, device=dev), alpha=cfg["sigma_s"])
+        del b
+        for _ in range(3):
+            sc.sc_topk_capture(z, cfg["K"], args.inv_t, args.top_p)
+    else:
+        g = torch.Generator(device=dev).manual_seed(1)
+        T, d = 1024, 4096
+        H = torch.randn((T, d), generator=g, device=dev).to(torch.bfloat16)
+        W = (torch.randn((151936, d), generator=g, device=dev) * 0.05).to(torch.bfloat16)
+        z = torch.empty((T, 151936), dtype=torch.bfloat16, device=dev)
+        G = (torch.randn((T, 37984), generator=g, device=dev) * 0.01).to(torch.bfloat16)
+        dw = torch.empty((37984, d), dtype=torch.float32, device=dev)
+        sc.sc_gemm_bf16(H, W, z, True, True, sc.GEMM_BF16)
+        sc.sc_gemm_bf16(G, H, dw, False, False, sc.GEMM_FP32)
+    torch.cuda.synchronize()
+    print("profile run done")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,7 +542,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration lines")
+    ap.add_argument("--profile", choices=["topk", "gemm"], default=None,
+                    help="only run a few launches of one kernel for a profiler")
+    ap.add_argument("--top-p", type=float, default=1.0)
+    ap.add_argument("--inv-t", type=float, default=1.0)
     args = ap.parse_args()
+    if args.profile:
+        return profile_run(args)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
