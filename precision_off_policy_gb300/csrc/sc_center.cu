@@ -27,20 +27,23 @@
 //   shared memory.  Phase A: with one exponent offset (the largest logit of the
 //   slice's first vectors), sum 2^y and its entropy term over the unrecorded
 //   entries (recorded ids are skipped through the flags, so the unrecorded
-//   mass accumulates directly, with no 1 - P_H cancellation).  Then, once the
-//   cluster has the row scalars, the write pass: g_v = beta p_v with 16-byte
-//   stores and no special cases, handing every chunk back to the producer as
-//   soon as it is written, so the next row streams into the stage while this
-//   one is written.
+//   mass accumulates directly, with no 1 - P_H cancellation); each warp sends
+//   its 16-byte partial to every CTA of the cluster the moment it is done
+//   (st.async stores that complete as transaction bytes on the receiver's
+//   mbarrier).  Then, once the cluster has the row scalars, the write pass:
+//   g_v = beta p_v with 16-byte stores and no special cases, handing every
+//   chunk back to the producer as soon as it is written, so the next row
+//   streams into the stage while this one is written.
 // * The scalar warp does the per-row serial work off the streaming path.
-//   While phase A runs it picks up the recorded ids' logits from the slice and
-//   sums them relative to the pass's offset; when phase A ends it merges the
-//   streaming warps' partials into this CTA's 64-byte record and sends it to
-//   every CTA of the cluster with st.async stores that complete as transaction
-//   bytes on the receiver's mbarrier, patches the previous row's special
-//   entries (recorded ids and the sampled token) with their own gradients,
-//   and merges the C records into the row scalars (LSE, P_H, Q_H, rho, s,
-//   loss, k3, importance weight) the same way in every CTA.
+//   While phase A runs it picks up the recorded ids' logits from the slice,
+//   sums them relative to their own offset and sends this CTA's 64-byte record
+//   (those sums, the recorded probabilities, the sampled token's logit, the
+//   previous row's gradient sum) to every CTA of the cluster.  When the last
+//   partial of the row has landed it merges all C x (warps) partials and the C
+//   records lane-parallel (a butterfly: the same bits in every CTA) into the
+//   row scalars (LSE, P_H, Q_H, rho, s, loss, k3, importance weight), and then
+//   patches the previous row's special entries (recorded ids and the sampled
+//   token) with their own gradients.
 // * The zero warp writes the queued zero rows (padding and error rows) and
 //   their log p_a and diagnostics, so the producer never waits on them.
 // Every logit is read from HBM once and every gradient written once.  The
@@ -62,7 +65,11 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxChunks = 16;
 constexpr int kMaxStages = 4;  // data stages
 constexpr int kMetaSlots = 4;  // metadata ring: rows in the write pass, in phase A, and two prefetched
-constexpr int kXBufs = 4;      // exchange buffers (peers may run ahead by a row)
+// Exchange buffers.  Two suffice: a CTA sends its partials of row j + 2 only
+// after it has merged row j + 1, which took every peer's partials of row
+// j + 1, and a peer sends those only after its write pass of row j, which
+// follows its own merge (its reads) of row j.
+constexpr int kXBufs = 2;
 constexpr int kMaxK = 1024;
 constexpr int kMaxV = 1 << 20;
 constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per CTA
@@ -95,32 +102,44 @@ struct RowMeta {
 };
 static_assert(sizeof(RowMeta) == 64, "RowMeta layout");
 
-// One CTA's contribution to a row, exchanged across the cluster (64 bytes).
-// y' values are relative to this CTA's own slice maximum m (y' = (z - m) kscale).
-struct Partial {
-    float m;            // slice maximum of z (-inf for an empty slice)
-    float S1, S2;       // unrecorded entries: sum 2^y', sum 2^y' y'
-    float rs;           // FP32 gradient sum of this slice for the row two rows back
+// What a row's exchange carries to every CTA of the cluster.  Each streaming
+// warp sends its phase-A sums over its share of the unrecorded entries as soon
+// as it has them (16 bytes); y' values are relative to the warp's offset m
+// (y' = (z - m) kscale).
+struct WarpPart {
+    float m;       // the warp's exponent offset in z (-inf: nothing summed)
+    float S1, S2;  // sum 2^y', sum 2^y' y'
+    float pad;
+};
+static_assert(sizeof(WarpPart) == 16, "warp partial is 16 bytes");
+// The scalar warp sends the rest of the CTA's contribution (64 bytes), which
+// needs only the slice: the recorded ids owned here relative to their own
+// offset, their probabilities, the logit of the sampled token, and the
+// finished gradient sum of the previous row.
+struct CtaRec {
+    float m;            // offset of the recorded ids' sums in z (-inf: none)
     float lH, EH;       // recorded ids owned here: sum 2^y', sum 2^y' y'
-    float QY;           // sum q_k y'_k over the owned recorded ids
+    float QY;           // sum q_k y'_k over them
+    float rs;           // FP32 gradient sum of this slice for the previous row
     float qo_hi, qo_lo; // sum of q_k over them except the largest one (double-float)
     float qbest;        // the largest q_k owned here (0 if none)
     int kbest;          // its position k (INT_MAX if none)
     int nval;           // owned recorded ids used
     uint32_t flags;     // row flags found by this CTA's producer
-    float ya;           // y' of the sampled token, if this CTA owns it
+    float za;           // logit of the sampled token, if this CTA owns it
     int has_a;
     float omq;          // 1 - qbest, from its log-probability (-expm1)
+    int pad[2];
 };
-static_assert(sizeof(Partial) == 64, "partial record is 64 bytes");
+static_assert(sizeof(CtaRec) == 64, "CTA record is 64 bytes");
 
 struct Layout {
     int stage_bytes;  // bytes of one data stage (128-aligned)
     int list_cap;     // entries of one owned list (K_max)
     int nwords;       // flag words of one slice (a bit per entry, or per 8-entry vector)
     int mwords;       // mask words of one slot (per-vector flags: four 8-bit masks a word)
-    int off_meta, off_list_li, off_list_q, off_bitmap, off_vpre, off_vmask, off_bars, off_part, off_frs,
-        off_fixz, off_fixv, off_zav, off_red, off_rsw, off_scal, off_flag, off_grab, off_zq, off_zqf, total;
+    int off_meta, off_list_li, off_list_q, off_bitmap, off_vpre, off_vmask, off_bars, off_wpart, off_rec, off_frs,
+        off_fixz, off_fixv, off_zav, off_rsw, off_scal, off_flag, off_grab, off_zq, off_zqf, total;
 };
 
 struct KArgs {
@@ -232,27 +251,29 @@ __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
     return o;
 }
 
-// Barriers.  Data stage d: kChunkFull + i (copy of chunk i landed, tx bytes),
-// kChunkFree + i (every streaming warp is done with chunk i).  Meta slot s:
-// kMetaFull (producer wrote it), kMetaFree (its row is written).  Exchange
-// buffer x: a row's records (own expect_tx arrive + peers' bytes).  kADone[p]:
-// every streaming warp finished phase A of a row of parity p (and so the write
-// pass of the row before it).  kSReady[p]: the row scalars of a row of parity p
-// are published.  Grab ring slot g: kGrabFull (the row index from CTA 0 landed,
-// tx bytes), kGrabFree (in CTA 0: every CTA of the cluster has read it).  Zero
-// queue slot z: kZqFull (producer wrote it), kZqFree (the zero warp took it).
-constexpr int kChunkFull = 0;
-constexpr int kChunkFree = kMaxChunks;
-constexpr int kBarsPerStage = 2 * kMaxChunks;
-constexpr int kMetaBase = kMaxStages * kBarsPerStage;
+// Barriers.  Meta slot s: kMetaFull (producer wrote it), kMetaFree (its row
+// is written).  Exchange buffer x: a row's partials and records (own
+// expect_tx arrive + every CTA's bytes).  kWDone[p]: every streaming warp
+// finished the write pass of a row of parity p.  kSReady[p]: the row scalars of
+// a row of parity p are published.  Grab ring slot g: kGrabFull (the row index
+// from CTA 0 landed, tx bytes), kGrabFree (in CTA 0: every CTA of the cluster
+// has read it).  Zero queue slot z: kZqFull (producer wrote it), kZqFree (the
+// zero warp took it).  Then, per data stage d: kChunkFull + i (copy of chunk i
+// landed, tx bytes), kChunkFree + i (every streaming warp is done with chunk i);
+// only the plan's stages take space.
+constexpr int kMetaBase = 0;
 constexpr int kMetaFull = 0;
 constexpr int kMetaFree = 1;
 constexpr int kXBase = kMetaBase + 2 * kMetaSlots;
-constexpr int kADone = kXBase + kXBufs;
-constexpr int kSReady = kADone + 2;
+constexpr int kWDone = kXBase + kXBufs;
+constexpr int kSReady = kWDone + 2;
 constexpr int kGrabBase = kSReady + 2;
 constexpr int kZqBase = kGrabBase + 2 * kGrab;
-constexpr int kNumBars = kZqBase + 2 * kZq;
+constexpr int kDataBase = kZqBase + 2 * kZq;
+constexpr int kChunkFull = 0;
+constexpr int kChunkFree = kMaxChunks;
+constexpr int kBarsPerStage = 2 * kMaxChunks;
+constexpr int num_bars(int NB) { return kDataBase + NB * kBarsPerStage; }
 
 // Resident CTAs per SM the register allocation must allow.
 constexpr int min_blocks(int NC) { return NC <= 128 ? 4 : 2; }
@@ -277,22 +298,22 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + L.off_bitmap);   // [kMetaSlots][nwords] flags
     uint16_t* vpre = reinterpret_cast<uint16_t*>(smem + L.off_vpre);        // VF: [kMetaSlots][nwords]
     uint32_t* vmask = reinterpret_cast<uint32_t*>(smem + L.off_vmask);      // VF: [kMetaSlots][mwords]
-    Partial* part = reinterpret_cast<Partial*>(smem + L.off_part);         // [kXBufs][C]
+    WarpPart* wpart = reinterpret_cast<WarpPart*>(smem + L.off_wpart);    // [kXBufs][C][NCW]
+    CtaRec* crec = reinterpret_cast<CtaRec*>(smem + L.off_rec);            // [kXBufs][C]
     float2* frs = reinterpret_cast<float2*>(smem + L.off_frs);             // [kMaxCluster]
     float* fix_z = reinterpret_cast<float*>(smem + L.off_fixz);            // [2][cap] recorded logits
     float* fix_v = reinterpret_cast<float*>(smem + L.off_fixv);            // [2][cap] their gradients
     float* zav = reinterpret_cast<float*>(smem + L.off_zav);               // [2] logit of a
-    float* red = reinterpret_cast<float*>(smem + L.off_red);               // [2][3][NCW] warp partials
     float* rsw = reinterpret_cast<float*>(smem + L.off_rsw);               // [2][NCW] warp row sums
     float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [2][4] row scalars
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_flag);
     long long* grab_ring = reinterpret_cast<long long*>(smem + L.off_grab);  // [kGrab] row indices from CTA 0
     long long* zq_t = reinterpret_cast<long long*>(smem + L.off_zq);        // [kZq] zero rows
     uint32_t* zq_f = reinterpret_cast<uint32_t*>(smem + L.off_zqf);         // [kZq] their flags
-    auto data_bar = [&](int d, int i) { return smem_addr(&bars[d * kBarsPerStage + i]); };
+    auto data_bar = [&](int d, int i) { return smem_addr(&bars[kDataBase + d * kBarsPerStage + i]); };
     auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
     auto xbar = [&](int x) { return smem_addr(&bars[kXBase + x]); };
-    auto adone = [&](int p) { return smem_addr(&bars[kADone + p]); };
+    auto wdone = [&](int p) { return smem_addr(&bars[kWDone + p]); };
     auto sready = [&](int p) { return smem_addr(&bars[kSReady + p]); };
     auto grab_full = [&](int g) { return smem_addr(&bars[kGrabBase + 2 * g]); };
     auto grab_free = [&](int g) { return smem_addr(&bars[kGrabBase + 2 * g + 1]); };
@@ -323,7 +344,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         }
         for (int x = 0; x < kXBufs; ++x) mbar_init(xbar(x), 1u);
         for (int p = 0; p < 2; ++p) {
-            mbar_init(adone(p), static_cast<uint32_t>(NCW));
+            mbar_init(wdone(p), static_cast<uint32_t>(NCW));
             mbar_init(sready(p), 1u);
         }
         for (int g = 0; g < kGrab; ++g) {
@@ -698,6 +719,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             if (flag_up()) break;
             const int p = static_cast<int>(j & 1u);
             const int ms = static_cast<int>(j % kMetaSlots);
+            const int xi = static_cast<int>(j % kXBufs);
             // ---- while the streaming warps run phase A of row j: everything that
             // needs only the slice -- the streaming offset (the same largest logit of
             // the first vectors), the recorded ids' and a's logits, and the recorded
@@ -711,7 +733,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             const float* q_s = list_q + ms * cap;
             const float* fz = fix_z + p * cap;
             const int nown = m.nown, a_li = m.a_li;
-            float zmax = -INFINITY, Mo = -INFINITY, lH = 0.0f, EH = 0.0f, QY = 0.0f;
+            float Mo = -INFINITY, lH = 0.0f, EH = 0.0f, QY = 0.0f;
             auto head_sums = [&](float o_c) {  // owned recorded ids relative to o_c
                 lH = 0.0f;
                 EH = 0.0f;
@@ -753,6 +775,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 const uint16_t* sb16 = reinterpret_cast<const uint16_t*>(sb);
                 const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
                 float* fzw = fix_z + p * cap;
+                float zmax = -INFINITY;
                 for (int e = lane; e < nown; e += 32) {
                     const int li = li_s[e];
                     const float z = bf_to_f(li < n8 ? sb16[li] : lrow[li]);
@@ -763,20 +786,26 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (lane == 0 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? sb16[a_li] : lrow[a_li]);
                 __syncwarp();
                 Mo = fmaxf(mz, zmax);
-                if (Mo > -INFINITY) head_sums(Mo * kscale);
+                if (Mo > -INFINITY) {
+                    head_sums(Mo * kscale);
+                } else if (nown > 0) {
+                    // every recorded logit here is -inf: their sums carry the
+                    // infinities (relative to 0), not a row offset of -inf
+                    head_sums(0.0f);
+                }
             }
-            // ---- phase A of row j is done ----
-            const bool got = mbar_wait_bounded(adone(p), (j >> 1) & 1u, wait_ns);
-            if (!__all_sync(kFull, got)) {
-                give_up(SC_STATUS_TIMEOUT_LOAD);
-                break;
-            }
-            // The write pass of row j - 1 ended before phase A of row j in every
-            // streaming warp: its row sum is complete (it rides with this row's
-            // record), and its special entries can be patched once the record is
-            // on its way.
+            // ---- the write pass of row j - 1 is done in every streaming warp: its
+            // row sum is complete (it rides with this row's record), and its special
+            // entries can be patched once the scalars of row j are out ----
             float rs1 = 0.0f;
-            if (j >= 1) rs1 = warp_sum(lane < NCW ? rsw[((j - 1) & 1u) * NCW + lane] : 0.0f) + corr_m1;
+            if (j >= 1) {
+                const bool wd = mbar_wait_bounded(wdone(static_cast<int>((j - 1) & 1u)), ((j - 1) >> 1) & 1u, wait_ns);
+                if (!__all_sync(kFull, wd)) {
+                    give_up(SC_STATUS_TIMEOUT_LOAD);
+                    break;
+                }
+                rs1 = warp_sum(lane < NCW ? rsw[((j - 1) & 1u) * NCW + lane] : 0.0f) + corr_m1;
+            }
             auto finish_prev = [&]() {
                 if (j >= 1) {
                     patch_row(j - 1, t_m1);
@@ -791,91 +820,87 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 clean_end = true;
                 break;
             }
-            const int xi = static_cast<int>(j & 3u);
-            if (lane == 0) mbar_expect_tx(xbar(xi), static_cast<uint32_t>(sizeof(Partial)) * C);
-            // ---- this CTA's record of row j, sent from registers ----
-            {
-                const float* rp = red + p * 3 * NCW;
-                // one offset in every warp (the usual case): plain sums in warp
-                // order, read by every lane
-                bool same = true;
-                float q1 = 0.0f, q2 = 0.0f;
-                for (int w = 0; w < NCW; ++w) {
-                    same = same && rp[w] == rp[0];
-                    q1 += rp[NCW + w];
-                    q2 += rp[2 * NCW + w];
-                }
-                Mass cm = lane < NCW ? Mass{rp[lane], rp[NCW + lane], rp[2 * NCW + lane]}
-                                     : Mass{rp[0], 0.0f, 0.0f};
-                if (same) {
-                    cm = Mass{rp[0], q1, q2};
-                } else {
-                    if (lane >= NCW) cm.m = -INFINITY;
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) cm = mass_merge(cm, mass_shfl(cm, off), kscale);
-                }
-                // the owned recorded logits may lie above the streaming offset
-                cm = mass_merge(cm, Mass{zmax, 0.0f, 0.0f}, kscale);
-                if (cm.m != Mo) head_sums(cm.m * kscale);  // (an exact pass moved the offset)
-                const float o_c = cm.m * kscale;
-                if (lane < C) {  // lane r sends the record to CTA r
-                    const uint32_t dst = map_to_rank(smem_addr(part + xi * C + static_cast<int>(crank)), lane);
-                    const uint32_t rb = map_to_rank(xbar(xi), lane);
-                    const float ya = a_li >= 0 ? fmaf(zav[p], kscale, -o_c) : 0.0f;
-                    st_async_v4(dst, __float_as_uint(cm.m), __float_as_uint(cm.s1), __float_as_uint(cm.s2),
-                                __float_as_uint(rs1), rb);
-                    st_async_v4(dst + 16u, __float_as_uint(lH), __float_as_uint(EH), __float_as_uint(QY),
-                                __float_as_uint(m.oh), rb);
-                    st_async_v4(dst + 32u, __float_as_uint(m.ol), __float_as_uint(m.qbest),
-                                static_cast<uint32_t>(m.kbest), static_cast<uint32_t>(nown), rb);
-                    st_async_v4(dst + 48u, m.flags, __float_as_uint(ya), a_li >= 0 ? 1u : 0u,
-                                __float_as_uint(m.omq), rb);
-                }
+            // ---- this CTA's record of row j, to every CTA of the cluster (the
+            // streaming warps send their own partials as they finish phase A) ----
+            if (lane == 0)
+                mbar_expect_tx(xbar(xi), static_cast<uint32_t>(C * (NCW * static_cast<int>(sizeof(WarpPart)) +
+                                                                    static_cast<int>(sizeof(CtaRec)))));
+            if (lane < C) {  // lane r sends the record to CTA r
+                const uint32_t dst = map_to_rank(smem_addr(crec + xi * C + static_cast<int>(crank)), lane);
+                const uint32_t rb = map_to_rank(xbar(xi), lane);
+                const float za = a_li >= 0 ? zav[p] : 0.0f;
+                st_async_v4(dst, __float_as_uint(Mo), __float_as_uint(lH), __float_as_uint(EH), __float_as_uint(QY), rb);
+                st_async_v4(dst + 16u, __float_as_uint(rs1), __float_as_uint(m.oh), __float_as_uint(m.ol),
+                            __float_as_uint(m.qbest), rb);
+                st_async_v4(dst + 32u, static_cast<uint32_t>(m.kbest), static_cast<uint32_t>(nown), m.flags,
+                            __float_as_uint(za), rb);
+                st_async_v4(dst + 48u, a_li >= 0 ? 1u : 0u, __float_as_uint(m.omq), 0u, 0u, rb);
             }
-            // ---- all C records of row j: the row scalars ----
-            const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j >> 2) & 1u, wait_ns);
+            // ---- every partial and record of row j: the row scalars ----
+            const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j / kXBufs) & 1u, wait_ns);
             if (!__all_sync(kFull, ok)) {
                 give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                 break;
             }
             {
-                // Every lane reads the C records (broadcast loads) and merges them
-                // in CTA order: the same bits in every lane, no shuffles.  The
-                // previous row's sum is added in the same order as the
-                // end-of-stream flush adds the last row's, so a row's sum does not
-                // depend on which of the two paths finished it.
-                const Partial* pp = part + xi * C;
-                float mg = -INFINITY;
-                for (int r = 0; r < C; ++r) mg = fmaxf(mg, pp[r].m);
+                // Lane-parallel: each lane takes the warp partials lane, lane + 32, ...
+                // and (lane < C) the record of CTA lane, rescales them to the row
+                // offset and the lanes are summed by a butterfly.  Every step is
+                // commutative, so every lane of every CTA ends with the same bits.
+                const WarpPart* wp = wpart + xi * C * NCW;
+                const CtaRec* rp = crec + xi * C;
+                const int NP = C * NCW;
+                float mx = -INFINITY;
+                for (int q = lane; q < NP; q += 32) mx = fmaxf(mx, wp[q].m);
+                uint4 r0 = make_uint4(__float_as_uint(-INFINITY), 0u, 0u, 0u), r1 = make_uint4(0u, 0u, 0u, 0u),
+                      r2 = make_uint4(0x7FFFFFFFu, 0u, 0u, 0u), r3 = make_uint4(0u, __float_as_uint(1.0f), 0u, 0u);
+                if (lane < C) {
+                    const uint32_t pa = smem_addr(rp + lane);
+                    r0 = lds128(pa);
+                    r1 = lds128(pa + 16u);
+                    r2 = lds128(pa + 32u);
+                    r3 = lds128(pa + 48u);
+                }
+                const float Hm = __uint_as_float(r0.x);
+                mx = fmaxf(mx, Hm);
+                const float mg = warp_max(mx);
                 const float o = mg * kscale;
-                float lT = 0.0f, ET = 0.0f, lH = 0.0f, EH = 0.0f, QYg = 0.0f, ya = 0.0f, rsum = 0.0f;
-                int nval = 0;
-                uint32_t flags = 0u;
-                HeadMass hm{0.0f, 0x7FFFFFFF, 1.0f, 0.0f, 0.0f};
-                for (int r = 0; r < C; ++r) {
-                    const uint32_t pa = smem_addr(pp + r);
-                    const uint4 r0 = lds128(pa), r1 = lds128(pa + 16u), r2 = lds128(pa + 32u), r3 = lds128(pa + 48u);
-                    const float Pm = __uint_as_float(r0.x);
-                    const bool live = Pm > -INFINITY;
-                    const float d = live ? Pm * kscale - o : 0.0f;
-                    const float f = live ? ex2(d) : 0.0f;
-                    const float PS1 = __uint_as_float(r0.y), PS2 = __uint_as_float(r0.z);
-                    const float PlH = __uint_as_float(r1.x), PEH = __uint_as_float(r1.y);
-                    const int Pnval = static_cast<int>(r2.w);
-                    lT = fmaf(f, PS1, lT);
-                    ET = fmaf(f, fmaf(d, PS1, PS2), ET);
-                    lH = fmaf(f, PlH, lH);
-                    EH = fmaf(f, fmaf(d, PlH, PEH), EH);
-                    if (Pnval > 0) {
-                        const float Qc = (__uint_as_float(r2.y) + __uint_as_float(r1.w)) + __uint_as_float(r2.x);
-                        QYg += fmaf(d, Qc, __uint_as_float(r1.z));
+                float lT = 0.0f, ET = 0.0f, lHg = 0.0f, EHg = 0.0f, QYg = 0.0f, ya = 0.0f;
+                for (int q = lane; q < NP; q += 32) {
+                    const uint4 w = lds128(smem_addr(wp + q));
+                    const float Pm = __uint_as_float(w.x);
+                    if (Pm > -INFINITY) {
+                        const float d = Pm * kscale - o;
+                        const float f = ex2(d);
+                        const float S1 = __uint_as_float(w.y), S2 = __uint_as_float(w.z);
+                        lT = fmaf(f, S1, lT);
+                        ET = fmaf(f, fmaf(d, S1, S2), ET);
                     }
-                    if (r3.z) ya += __uint_as_float(r3.y) + d;
-                    rsum += __uint_as_float(r0.w);
-                    nval += Pnval;
-                    flags |= r3.x;
-                    hm = head_merge(hm, HeadMass{__uint_as_float(r2.y), static_cast<int>(r2.z), __uint_as_float(r3.w),
-                                                 __uint_as_float(r1.w), __uint_as_float(r2.x)});
+                }
+                const int Pnval = static_cast<int>(r2.y);
+                const float PlH = __uint_as_float(r0.y), PEH = __uint_as_float(r0.z), PQY = __uint_as_float(r0.w);
+                const float Pqb = __uint_as_float(r1.w), Poh = __uint_as_float(r1.y), Pol = __uint_as_float(r1.z);
+                if (Hm > -INFINITY) {
+                    const float d = Hm * kscale - o;
+                    const float f = ex2(d);
+                    lHg = f * PlH;
+                    EHg = f * fmaf(d, PlH, PEH);
+                    if (Pnval > 0) QYg = fmaf(d, (Pqb + Poh) + Pol, PQY);
+                } else if (Pnval > 0) {  // (recorded logits of -inf: their infinities)
+                    EHg = PEH;
+                    QYg = PQY;
+                }
+                if (r3.x) ya = fmaf(__uint_as_float(r2.w), kscale, -o);
+                int nval = Pnval;
+                HeadMass hm{Pqb, static_cast<int>(r2.x), __uint_as_float(r3.y), Poh, Pol};
+                // first what the write pass needs
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    lT += __shfl_xor_sync(kFull, lT, off);
+                    lHg += __shfl_xor_sync(kFull, lHg, off);
+                    ya += __shfl_xor_sync(kFull, ya, off);
+                    nval += __shfl_xor_sync(kFull, nval, off);
+                    hm = head_merge(hm, head_shfl(hm, off));
                 }
                 // 1 - Q_H without cancellation: (1 - q_max), taken from its
                 // log-probability, minus the others' mass
@@ -886,9 +911,9 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 }
                 // First what the write pass needs (bw, beta), published at once;
                 // the diagnostics and the recorded ids' own gradients after.
-                const float l = lT + lH;
+                const float l = lT + lHg;
                 const float log2l = log2f(l);
-                const float P_H = lH / l;
+                const float P_H = lHg / l;
                 const float tail_pi = lT / l;
                 const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
                 const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
@@ -899,15 +924,16 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 const float w = a.is_mode != SC_IS_NONE ? expf(dd) : 1.0f;
                 float wt = w;
                 float wc = w;  // clipped GRPO: the clipped ratio
+                uint32_t isf = 0u;
                 if (a.is_mode == SC_IS_TIS) {
                     if (w > a.tis_max) {
                         wt = a.tis_max;
-                        flags |= SC_FLAG_IS_TRUNC;
+                        isf = SC_FLAG_IS_TRUNC;
                     }
                 } else if (a.is_mode == SC_IS_MIS) {
                     if (!(w >= a.mis_min && w <= a.mis_max)) {
                         wt = 0.0f;
-                        flags |= SC_FLAG_IS_REJECT;
+                        isf = SC_FLAG_IS_REJECT;
                     }
                 } else if (a.is_mode == SC_IS_CLIP) {
                     // -min(w A, w_c A): the ratio's gradient where the unclipped
@@ -915,7 +941,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     wc = fminf(fmaxf(w, a.clip_lo), a.clip_hi);
                     if (!(wc == w || w * A < wc * A)) {
                         wt = 0.0f;
-                        flags |= SC_FLAG_CLIPPED;
+                        isf = SC_FLAG_CLIPPED;
                     }
                 }
                 const float Aw = A * wt;
@@ -930,6 +956,19 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (lane == 0) mbar_arrive(sready(p));
                 finish_prev();  // the previous row's special entries, off the critical path
 
+                // the rest of the sums, the flags, and the previous row's sum in CTA
+                // order (the order the end-of-stream flush adds the last row's in)
+                uint32_t flags = r2.z;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    ET += __shfl_xor_sync(kFull, ET, off);
+                    EHg += __shfl_xor_sync(kFull, EHg, off);
+                    QYg += __shfl_xor_sync(kFull, QYg, off);
+                    flags |= __shfl_xor_sync(kFull, flags, off);
+                }
+                flags |= isf;
+                float rsum = 0.0f;
+                for (int r = 0; r < C; ++r) rsum += rp[r].rs;
                 if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
                 if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
                 const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
@@ -939,11 +978,11 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 float csum = 0.0f;
                 if (a.centering && nval > 0) {
                     const float qlogp = kLn2 * fmaf(-log2l, Q_H, QYg);
-                    const float plogp = kLn2 * fmaf(-log2l, lH, EH) / l;
+                    const float plogp = kLn2 * fmaf(-log2l, lHg, EHg) / l;
                     csum = fmaf(-rho, plogp, qlogp);
                 }
                 const float loss = a.is_mode == SC_IS_CLIP ? -fminf(w * A, wc * A) : -Aw * (logp_a - csum);
-                const float entropy = kLn2 * (log2l - (ET + EH) / l);
+                const float entropy = kLn2 * (log2l - (ET + EHg) / l);
                 const float g_a_free = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
                 // gradient at the owned recorded ids, and how far it is from the
                 // beta p the write pass stores there (the row sum's correction)
@@ -994,11 +1033,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 break;
             }
             const RowMeta m = meta[ms];
-            if (m.t < 0) {  // end of the stream: every row of this warp is written
-                __syncwarp();
-                if (lane == 0) mbar_arrive(adone(static_cast<int>(i & 1u)));
-                break;
-            }
+            if (m.t < 0) break;  // end of the stream: every row of this warp is written
             const int p = static_cast<int>(i & 1u);
             const int ds = static_cast<int>(i % NB);  // the row's data stage
             const uint32_t buf_s = smem_addr(smem + ds * L.stage_bytes);
@@ -1165,14 +1200,14 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     for (int off = 16; off > 0; off >>= 1)
                         ms_acc = mass_merge(ms_acc, mass_shfl(ms_acc, off), kscale);
                 }
-                if (lane == 0) {
-                    float* rp = red + p * 3 * NCW;
-                    rp[warp] = ms_acc.m;
-                    rp[NCW + warp] = ms_acc.s1;
-                    rp[2 * NCW + warp] = ms_acc.s2;
+                // this warp's partial to every CTA of the cluster (lane r to CTA r)
+                if (lane < C) {
+                    const int xi = static_cast<int>(i % kXBufs);
+                    const uint32_t dst =
+                        map_to_rank(smem_addr(wpart + (xi * C + static_cast<int>(crank)) * NCW + warp), lane);
+                    st_async_v4(dst, __float_as_uint(ms_acc.m), __float_as_uint(ms_acc.s1), __float_as_uint(ms_acc.s2),
+                                0u, map_to_rank(xbar(xi), lane));
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(adone(p));
             }
             {
                 // ---- write pass of row i, once the cluster has its row scalars: g = beta p
@@ -1220,6 +1255,8 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 }
                 rs = warp_sum(rs + (f2_lo(RS) + f2_hi(RS)));
                 if (lane == 0) rsw[pp * NCW + warp] = rs;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(wdone(pp));
             }
         }
     }
@@ -1275,13 +1312,13 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C, bool vf) {
     L.off_bitmap = take(kMetaSlots * L.nwords * 4);
     L.off_vpre = take(vf ? kMetaSlots * L.nwords * 2 : 0);
     L.off_vmask = take(kMetaSlots * L.mwords * 4);
-    L.off_bars = take(kNumBars * 8);
-    L.off_part = take(kXBufs * C * static_cast<int>(sizeof(Partial)));
+    L.off_bars = take(num_bars(NB) * 8);
+    L.off_wpart = take(kXBufs * C * (NC / 32) * static_cast<int>(sizeof(WarpPart)));
+    L.off_rec = take(kXBufs * C * static_cast<int>(sizeof(CtaRec)));
     L.off_frs = take(kMaxCluster * 8);
     L.off_fixz = take(2 * L.list_cap * 4);
     L.off_fixv = take(2 * L.list_cap * 4);
     L.off_zav = take(2 * 4);
-    L.off_red = take(2 * 3 * (NC / 32) * 4);
     L.off_rsw = take(2 * (NC / 32) * 4);
     L.off_scal = take(2 * 4 * 4);
     L.off_flag = take(4);
