@@ -172,10 +172,10 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
 }
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-    return v;
+__device__ __forceinline__ float warp_max(float v) {  // exact: the same in every lane
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
 }
 __device__ __forceinline__ uint16_t f_to_bf_bits(float x) {
     return static_cast<uint16_t>(pack_bf16x2(x, 0.0f) & 0xFFFFu);
@@ -252,8 +252,8 @@ __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
 }
 
 // Barriers.  Meta slot s: kMetaFull (producer wrote it), kMetaFree (its row
-// is written).  Exchange buffer x: a row's partials and records (own
-// expect_tx arrive + every CTA's bytes).  kWDone[p]: every streaming warp
+// is written).  Exchange buffer x: kXRec (a row's C records) and kXPart (its
+// C x warps partials), each the own expect_tx arrive + every CTA's bytes.  kWDone[p]: every streaming warp
 // finished the write pass of a row of parity p.  kSReady[p]: the row scalars of
 // a row of parity p are published.  Grab ring slot g: kGrabFull (the row index
 // from CTA 0 landed, tx bytes), kGrabFree (in CTA 0: every CTA of the cluster
@@ -264,8 +264,9 @@ __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
 constexpr int kMetaBase = 0;
 constexpr int kMetaFull = 0;
 constexpr int kMetaFree = 1;
-constexpr int kXBase = kMetaBase + 2 * kMetaSlots;
-constexpr int kWDone = kXBase + kXBufs;
+constexpr int kXRec = kMetaBase + 2 * kMetaSlots;
+constexpr int kXPart = kXRec + kXBufs;
+constexpr int kWDone = kXPart + kXBufs;
 constexpr int kSReady = kWDone + 2;
 constexpr int kGrabBase = kSReady + 2;
 constexpr int kZqBase = kGrabBase + 2 * kGrab;
@@ -312,7 +313,8 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     uint32_t* zq_f = reinterpret_cast<uint32_t*>(smem + L.off_zqf);         // [kZq] their flags
     auto data_bar = [&](int d, int i) { return smem_addr(&bars[kDataBase + d * kBarsPerStage + i]); };
     auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
-    auto xbar = [&](int x) { return smem_addr(&bars[kXBase + x]); };
+    auto xrec = [&](int x) { return smem_addr(&bars[kXRec + x]); };
+    auto xpart = [&](int x) { return smem_addr(&bars[kXPart + x]); };
     auto wdone = [&](int p) { return smem_addr(&bars[kWDone + p]); };
     auto sready = [&](int p) { return smem_addr(&bars[kSReady + p]); };
     auto grab_full = [&](int g) { return smem_addr(&bars[kGrabBase + 2 * g]); };
@@ -342,7 +344,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             mbar_init(meta_bar(s, kMetaFree), 1u);
             meta[s].nown = 0;
         }
-        for (int x = 0; x < kXBufs; ++x) mbar_init(xbar(x), 1u);
+        for (int x = 0; x < kXBufs; ++x) {
+            mbar_init(xrec(x), 1u);
+            mbar_init(xpart(x), 1u);
+        }
         for (int p = 0; p < 2; ++p) {
             mbar_init(wdone(p), static_cast<uint32_t>(NCW));
             mbar_init(sready(p), 1u);
@@ -822,12 +827,13 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             }
             // ---- this CTA's record of row j, to every CTA of the cluster (the
             // streaming warps send their own partials as they finish phase A) ----
-            if (lane == 0)
-                mbar_expect_tx(xbar(xi), static_cast<uint32_t>(C * (NCW * static_cast<int>(sizeof(WarpPart)) +
-                                                                    static_cast<int>(sizeof(CtaRec)))));
+            if (lane == 0) {
+                mbar_expect_tx(xrec(xi), static_cast<uint32_t>(C * static_cast<int>(sizeof(CtaRec))));
+                mbar_expect_tx(xpart(xi), static_cast<uint32_t>(C * NCW * static_cast<int>(sizeof(WarpPart))));
+            }
             if (lane < C) {  // lane r sends the record to CTA r
                 const uint32_t dst = map_to_rank(smem_addr(crec + xi * C + static_cast<int>(crank)), lane);
-                const uint32_t rb = map_to_rank(xbar(xi), lane);
+                const uint32_t rb = map_to_rank(xrec(xi), lane);
                 const float za = a_li >= 0 ? zav[p] : 0.0f;
                 st_async_v4(dst, __float_as_uint(Mo), __float_as_uint(lH), __float_as_uint(EH), __float_as_uint(QY), rb);
                 st_async_v4(dst + 16u, __float_as_uint(rs1), __float_as_uint(m.oh), __float_as_uint(m.ol),
@@ -836,22 +842,17 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                             __float_as_uint(za), rb);
                 st_async_v4(dst + 48u, a_li >= 0 ? 1u : 0u, __float_as_uint(m.omq), 0u, 0u, rb);
             }
-            // ---- every partial and record of row j: the row scalars ----
-            const bool ok = mbar_wait_cluster_bounded(xbar(xi), (j / kXBufs) & 1u, wait_ns);
-            if (!__all_sync(kFull, ok)) {
+            // ---- the C records of row j, usually in before phase A ends: merged
+            // relative to their own largest offset Mh while the streaming partials
+            // are still on their way.  Lane r < C takes the record of CTA r and a
+            // butterfly of commutative steps sums the lanes, so every lane of every
+            // CTA ends with the same bits. ----
+            if (!__all_sync(kFull, mbar_wait_cluster_bounded(xrec(xi), (j / kXBufs) & 1u, wait_ns))) {
                 give_up(SC_STATUS_TIMEOUT_EXCHANGE);
                 break;
             }
             {
-                // Lane-parallel: each lane takes the warp partials lane, lane + 32, ...
-                // and (lane < C) the record of CTA lane, rescales them to the row
-                // offset and the lanes are summed by a butterfly.  Every step is
-                // commutative, so every lane of every CTA ends with the same bits.
-                const WarpPart* wp = wpart + xi * C * NCW;
                 const CtaRec* rp = crec + xi * C;
-                const int NP = C * NCW;
-                float mx = -INFINITY;
-                for (int q = lane; q < NP; q += 32) mx = fmaxf(mx, wp[q].m);
                 uint4 r0 = make_uint4(__float_as_uint(-INFINITY), 0u, 0u, 0u), r1 = make_uint4(0u, 0u, 0u, 0u),
                       r2 = make_uint4(0x7FFFFFFFu, 0u, 0u, 0u), r3 = make_uint4(0u, __float_as_uint(1.0f), 0u, 0u);
                 if (lane < C) {
@@ -862,10 +863,57 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     r3 = lds128(pa + 48u);
                 }
                 const float Hm = __uint_as_float(r0.x);
-                mx = fmaxf(mx, Hm);
-                const float mg = warp_max(mx);
-                const float o = mg * kscale;
-                float lT = 0.0f, ET = 0.0f, lHg = 0.0f, EHg = 0.0f, QYg = 0.0f, ya = 0.0f;
+                const float Mh = warp_max(Hm);
+                const int Pnval = static_cast<int>(r2.y);
+                const float PlH = __uint_as_float(r0.y), PEH = __uint_as_float(r0.z), PQY = __uint_as_float(r0.w);
+                const float Pqb = __uint_as_float(r1.w), Poh = __uint_as_float(r1.y), Pol = __uint_as_float(r1.z);
+                float lH1 = 0.0f, EH1 = 0.0f, QY1 = 0.0f;
+                if (Hm > -INFINITY) {
+                    const float d = (Hm - Mh) * kscale;
+                    const float f = ex2(d);
+                    lH1 = f * PlH;
+                    EH1 = f * fmaf(d, PlH, PEH);
+                    if (Pnval > 0) QY1 = fmaf(d, (Pqb + Poh) + Pol, PQY);
+                } else if (Pnval > 0) {  // (recorded logits of -inf: their infinities)
+                    EH1 = PEH;
+                    QY1 = PQY;
+                }
+                HeadMass hm{Pqb, static_cast<int>(r2.x), __uint_as_float(r3.y), Poh, Pol};
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    lH1 += __shfl_xor_sync(kFull, lH1, off);
+                    EH1 += __shfl_xor_sync(kFull, EH1, off);
+                    QY1 += __shfl_xor_sync(kFull, QY1, off);
+                    hm = head_merge(hm, head_shfl(hm, off));
+                }
+                const int nval = __reduce_add_sync(kFull, Pnval);
+                uint32_t flags = __reduce_or_sync(kFull, r2.z);
+                // the logit of a: only its owner's lane has nonzero bits
+                const bool has_a = __reduce_or_sync(kFull, r3.x) != 0u;
+                const float za = __uint_as_float(__reduce_or_sync(kFull, r3.x ? r2.w : 0u));
+                // 1 - Q_H without cancellation: (1 - q_max), taken from its
+                // log-probability, minus the others' mass
+                float tail_mu = 1.0f, Q_H = 0.0f;
+                if (nval > 0) {
+                    tail_mu = (hm.omq - hm.oh) - hm.ol;
+                    Q_H = (hm.q + hm.oh) + hm.ol;
+                }
+                // the previous row's sum, in CTA order (the order the end-of-stream
+                // flush adds the last row's in)
+                float rsum = 0.0f;
+                for (int r = 0; r < C; ++r) rsum += rp[r].rs;
+
+                // ---- the streaming partials of row j: the row scalars ----
+                if (!__all_sync(kFull, mbar_wait_cluster_bounded(xpart(xi), (j / kXBufs) & 1u, wait_ns))) {
+                    give_up(SC_STATUS_TIMEOUT_EXCHANGE);
+                    break;
+                }
+                const WarpPart* wp = wpart + xi * C * NCW;
+                const int NP = C * NCW;
+                float mx = Mh;
+                for (int q = lane; q < NP; q += 32) mx = fmaxf(mx, wp[q].m);
+                const float o = warp_max(mx) * kscale;
+                float lT = 0.0f, ET = 0.0f;
                 for (int q = lane; q < NP; q += 32) {
                     const uint4 w = lds128(smem_addr(wp + q));
                     const float Pm = __uint_as_float(w.x);
@@ -877,38 +925,13 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                         ET = fmaf(f, fmaf(d, S1, S2), ET);
                     }
                 }
-                const int Pnval = static_cast<int>(r2.y);
-                const float PlH = __uint_as_float(r0.y), PEH = __uint_as_float(r0.z), PQY = __uint_as_float(r0.w);
-                const float Pqb = __uint_as_float(r1.w), Poh = __uint_as_float(r1.y), Pol = __uint_as_float(r1.z);
-                if (Hm > -INFINITY) {
-                    const float d = Hm * kscale - o;
-                    const float f = ex2(d);
-                    lHg = f * PlH;
-                    EHg = f * fmaf(d, PlH, PEH);
-                    if (Pnval > 0) QYg = fmaf(d, (Pqb + Poh) + Pol, PQY);
-                } else if (Pnval > 0) {  // (recorded logits of -inf: their infinities)
-                    EHg = PEH;
-                    QYg = PQY;
-                }
-                if (r3.x) ya = fmaf(__uint_as_float(r2.w), kscale, -o);
-                int nval = Pnval;
-                HeadMass hm{Pqb, static_cast<int>(r2.x), __uint_as_float(r3.y), Poh, Pol};
-                // first what the write pass needs
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    lT += __shfl_xor_sync(kFull, lT, off);
-                    lHg += __shfl_xor_sync(kFull, lHg, off);
-                    ya += __shfl_xor_sync(kFull, ya, off);
-                    nval += __shfl_xor_sync(kFull, nval, off);
-                    hm = head_merge(hm, head_shfl(hm, off));
-                }
-                // 1 - Q_H without cancellation: (1 - q_max), taken from its
-                // log-probability, minus the others' mass
-                float tail_mu = 1.0f, Q_H = 0.0f;
-                if (nval > 0) {
-                    tail_mu = (hm.omq - hm.oh) - hm.ol;
-                    Q_H = (hm.q + hm.oh) + hm.ol;
-                }
+                for (int off = 16; off > 0; off >>= 1) lT += __shfl_xor_sync(kFull, lT, off);
+                // the recorded ids' sums moved from Mh to the row offset
+                const float dH = Mh > -INFINITY ? Mh * kscale - o : 0.0f;
+                const float fH = Mh > -INFINITY ? ex2(dH) : 0.0f;
+                const float lHg = fH * lH1;
+                const float ya = has_a ? fmaf(za, kscale, -o) : 0.0f;
                 // First what the write pass needs (bw, beta), published at once;
                 // the diagnostics and the recorded ids' own gradients after.
                 const float l = lT + lHg;
@@ -924,16 +947,15 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 const float w = a.is_mode != SC_IS_NONE ? expf(dd) : 1.0f;
                 float wt = w;
                 float wc = w;  // clipped GRPO: the clipped ratio
-                uint32_t isf = 0u;
                 if (a.is_mode == SC_IS_TIS) {
                     if (w > a.tis_max) {
                         wt = a.tis_max;
-                        isf = SC_FLAG_IS_TRUNC;
+                        flags |= SC_FLAG_IS_TRUNC;
                     }
                 } else if (a.is_mode == SC_IS_MIS) {
                     if (!(w >= a.mis_min && w <= a.mis_max)) {
                         wt = 0.0f;
-                        isf = SC_FLAG_IS_REJECT;
+                        flags |= SC_FLAG_IS_REJECT;
                     }
                 } else if (a.is_mode == SC_IS_CLIP) {
                     // -min(w A, w_c A): the ratio's gradient where the unclipped
@@ -941,7 +963,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     wc = fminf(fmaxf(w, a.clip_lo), a.clip_hi);
                     if (!(wc == w || w * A < wc * A)) {
                         wt = 0.0f;
-                        isf = SC_FLAG_CLIPPED;
+                        flags |= SC_FLAG_CLIPPED;
                     }
                 }
                 const float Aw = A * wt;
@@ -956,19 +978,14 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (lane == 0) mbar_arrive(sready(p));
                 finish_prev();  // the previous row's special entries, off the critical path
 
-                // the rest of the sums, the flags, and the previous row's sum in CTA
-                // order (the order the end-of-stream flush adds the last row's in)
-                uint32_t flags = r2.z;
+                // the rest of the sums
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    ET += __shfl_xor_sync(kFull, ET, off);
-                    EHg += __shfl_xor_sync(kFull, EHg, off);
-                    QYg += __shfl_xor_sync(kFull, QYg, off);
-                    flags |= __shfl_xor_sync(kFull, flags, off);
+                for (int off = 16; off > 0; off >>= 1) ET += __shfl_xor_sync(kFull, ET, off);
+                float EHg = EH1, QYg = QY1;
+                if (Mh > -INFINITY) {
+                    EHg = fH * fmaf(dH, lH1, EH1);
+                    if (nval > 0) QYg = fmaf(dH, Q_H, QY1);
                 }
-                flags |= isf;
-                float rsum = 0.0f;
-                for (int r = 0; r < C; ++r) rsum += rp[r].rs;
                 if (tail_pi < kTailFloor) flags |= SC_FLAG_CLAMP_PI;
                 if (tail_mu < kTailFloor) flags |= SC_FLAG_CLAMP_MU;
                 const float dsr = a.centering ? tail_mu - rho * tail_pi : 0.0f;  // s - rho
@@ -1206,7 +1223,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     const uint32_t dst =
                         map_to_rank(smem_addr(wpart + (xi * C + static_cast<int>(crank)) * NCW + warp), lane);
                     st_async_v4(dst, __float_as_uint(ms_acc.m), __float_as_uint(ms_acc.s1), __float_as_uint(ms_acc.s2),
-                                0u, map_to_rank(xbar(xi), lane));
+                                0u, map_to_rank(xpart(xi), lane));
                 }
             }
             {
