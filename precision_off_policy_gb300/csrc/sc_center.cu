@@ -12,17 +12,18 @@
 // GB300 design.  One row is shared by a cluster of C CTAs; CTA r owns the
 // vocabulary slice [r*S, min((r+1)*S, V)).  Each CTA is warp-specialised.
 //
-// * The producer warp walks the cluster's rows ahead of the others: the first
+// * The row warp walks the cluster's rows ahead of the others: the first
 //   seven eighths of the rows dealt round robin, the rest handed out at run
 //   time from a counter in the caller's workspace (CTA 0 takes each row and
 //   passes its index to its peers through their shared memory).  Padding and
 //   error rows go to the zero warp's queue.  For every valid row it fills a
-//   slot of a metadata ring -- the row's scalars and the compact
-//   list of recorded ids that fall in this CTA's slice (repeats dropped), with
-//   flags marking them (one bit per entry, or one bit per 8-entry vector with
-//   the flagged vectors' masks) -- and starts 1-D bulk copies (TMA
-//   engine) of the logit slice into shared memory, chunk by chunk, as soon as
-//   the streaming warps have released the buffer.
+//   slot of a metadata ring, up to three rows ahead -- the row's scalars and
+//   the compact list of recorded ids that fall in this CTA's slice (repeats
+//   dropped), with flags marking them (one bit per entry, or one bit per
+//   8-entry vector with the flagged vectors' masks).
+// * The copy warp takes the valid rows from that ring and starts 1-D bulk
+//   copies (TMA engine) of each logit slice into shared memory, chunk by
+//   chunk, each as soon as the streaming warps have released that chunk.
 // * The streaming warps take each row through two passes over the slice in
 //   shared memory.  Phase A: with one exponent offset (the largest logit of the
 //   slice's first vectors), sum 2^y and its entropy term over the unrecorded
@@ -32,7 +33,7 @@
 //   (st.async stores that complete as transaction bytes on the receiver's
 //   mbarrier).  Then, once the cluster has the row scalars, the write pass:
 //   g_v = beta p_v with 16-byte stores and no special cases, handing every
-//   chunk back to the producer as soon as it is written, so the next row
+//   chunk back to the copy warp as soon as it is written, so the next row
 //   streams into the stage while this one is written.
 // * The scalar warp does the per-row serial work off the streaming path.
 //   While phase A runs it picks up the recorded ids' logits from the slice,
@@ -45,7 +46,7 @@
 //   patches the previous row's special entries (recorded ids and the sampled
 //   token) with their own gradients.
 // * The zero warp writes the queued zero rows (padding and error rows) and
-//   their log p_a and diagnostics, so the producer never waits on them.
+//   their log p_a and diagnostics, so the row warp never waits on them.
 // Every logit is read from HBM once and every gradient written once.  The
 // grid is persistent (as many clusters as fit).  Every wait is bounded (about
 // 1 s) and reports through the status word.
@@ -76,7 +77,7 @@ constexpr int kMaxSmem = 232448;        // 227 KiB of dynamic shared memory per 
 constexpr int kTwoPerSmBytes = 114688;  // dynamic shared memory that still fits two CTAs on an SM
 constexpr int kChunkVecTarget = 2048;   // 16-byte vectors per bulk copy (32 KiB; measured best of 8-128 KiB)
 constexpr int kGrab = 8;                // grab ring: rows CTA 0 may hand out ahead of its peers
-constexpr int kZq = 16;                 // zero queue: zero rows the producer may queue ahead
+constexpr int kZq = 16;                 // zero queue: zero rows the row warp may queue ahead
 constexpr long long kDynamicShare = 8;  // 1 / (share of the rows handed out at run time; measured best of 3..20)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -85,13 +86,13 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // default limit of
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // bulk copies in flight before a CTA leaves
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
-// One valid row as the producer hands it to the consumers.
+// One valid row as the row warp hands it to the copy warp and the consumers.
 struct RowMeta {
     long long t;     // row index; -1 ends the consumers' loop
     int sa;          // sampled id
     int nown;        // recorded ids of this CTA's slice in the compact list
     int a_li;        // local index of a in this slice, -1 if another CTA owns it
-    uint32_t flags;  // row flags found by the producer (count, repeats, out of range)
+    uint32_t flags;  // row flags found by the row warp (count, repeats, out of range)
     float A, rl;     // advantage, rollout logprob
     // this slice's recorded ids, from their log-probabilities alone
     float qbest;     // the largest q (0 if none)
@@ -125,7 +126,7 @@ struct CtaRec {
     float qbest;        // the largest q_k owned here (0 if none)
     int kbest;          // its position k (INT_MAX if none)
     int nval;           // owned recorded ids used
-    uint32_t flags;     // row flags found by this CTA's producer
+    uint32_t flags;     // row flags found by this CTA's row warp
     float za;           // logit of the sampled token, if this CTA owns it
     int has_a;
     float omq;          // 1 - qbest, from its log-probability (-expm1)
@@ -139,7 +140,7 @@ struct Layout {
     int nwords;       // flag words of one slice (a bit per entry, or per 8-entry vector)
     int mwords;       // mask words of one slot (per-vector flags: four 8-bit masks a word)
     int off_meta, off_list_li, off_list_q, off_bitmap, off_vpre, off_vmask, off_bars, off_wpart, off_rec, off_frs,
-        off_fixz, off_fixv, off_zav, off_rsw, off_scal, off_flag, off_grab, off_zq, off_zqf, total;
+        off_fixz, off_fixv, off_zav, off_rsw, off_scal, off_flag, off_grab, off_zq, off_zqf, off_ticket, total;
 };
 
 struct KArgs {
@@ -251,14 +252,15 @@ __device__ __forceinline__ HeadMass head_shfl(const HeadMass& h, int off) {
     return o;
 }
 
-// Barriers.  Meta slot s: kMetaFull (producer wrote it), kMetaFree (its row
+// Barriers.  Meta slot s: kMetaFull (row warp wrote it), kMetaFree (its row
 // is written).  Exchange buffer x: kXRec (a row's C records) and kXPart (its
 // C x warps partials), each the own expect_tx arrive + every CTA's bytes.  kWDone[p]: every streaming warp
 // finished the write pass of a row of parity p.  kSReady[p]: the row scalars of
 // a row of parity p are published.  Grab ring slot g: kGrabFull (the row index
 // from CTA 0 landed, tx bytes), kGrabFree (in CTA 0: every CTA of the cluster
-// has read it).  Zero queue slot z: kZqFull (producer wrote it), kZqFree (the
-// zero warp took it).  Then, per data stage d: kChunkFull + i (copy of chunk i
+// has read it).  Zero queue slot z: kZqFull (row warp wrote it), kZqFree (the
+// zero warp took it).  Ticket s: the row index of a valid row is in ticket
+// slot s (row warp, before its metadata work).  Then, per data stage d: kChunkFull + i (copy of chunk i
 // landed, tx bytes), kChunkFree + i (every streaming warp is done with chunk i);
 // only the plan's stages take space.
 constexpr int kMetaBase = 0;
@@ -270,21 +272,25 @@ constexpr int kWDone = kXPart + kXBufs;
 constexpr int kSReady = kWDone + 2;
 constexpr int kGrabBase = kSReady + 2;
 constexpr int kZqBase = kGrabBase + 2 * kGrab;
-constexpr int kDataBase = kZqBase + 2 * kZq;
+constexpr int kTicketBase = kZqBase + 2 * kZq;
+constexpr int kDataBase = kTicketBase + kMetaSlots;
 constexpr int kChunkFull = 0;
 constexpr int kChunkFree = kMaxChunks;
 constexpr int kBarsPerStage = 2 * kMaxChunks;
 constexpr int num_bars(int NB) { return kDataBase + NB * kBarsPerStage; }
 
+// Threads of a CTA besides the NC streaming threads: the scalar, row, zero
+// and copy warps.
+constexpr int kAuxThreads = 128;
 // Resident CTAs per SM the register allocation must allow.
 constexpr int min_blocks(int NC) { return NC <= 128 ? 4 : 2; }
 
 // VF: recorded-id flags one bit per 8-entry vector (with the flagged vectors'
 // masks) instead of one bit per entry.
 template <int NC, bool VF>
-__global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
+__global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kernel(const __grid_constant__ KArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int NCW = NC / 32;  // streaming warps; warp NCW: row scalars; NCW + 1: producer; NCW + 2: zero rows
+    constexpr int NCW = NC / 32;  // streaming warps; warp NCW: row scalars; NCW + 1: rows; NCW + 2: zero rows; NCW + 3: copies
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t crank = cluster_ctarank();
     const uint32_t cid = cluster_id_x();
@@ -308,9 +314,11 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     float* rsw = reinterpret_cast<float*>(smem + L.off_rsw);               // [2][NCW] warp row sums
     float* scal = reinterpret_cast<float*>(smem + L.off_scal);             // [2][4] row scalars
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.off_flag);
+    volatile uint32_t* copied = reinterpret_cast<volatile uint32_t*>(smem + L.off_flag + 4);  // rows with all copies started
     long long* grab_ring = reinterpret_cast<long long*>(smem + L.off_grab);  // [kGrab] row indices from CTA 0
     long long* zq_t = reinterpret_cast<long long*>(smem + L.off_zq);        // [kZq] zero rows
     uint32_t* zq_f = reinterpret_cast<uint32_t*>(smem + L.off_zqf);         // [kZq] their flags
+    long long* ticket = reinterpret_cast<long long*>(smem + L.off_ticket);  // [kMetaSlots] valid rows' indices
     auto data_bar = [&](int d, int i) { return smem_addr(&bars[kDataBase + d * kBarsPerStage + i]); };
     auto meta_bar = [&](int s, int i) { return smem_addr(&bars[kMetaBase + 2 * s + i]); };
     auto xrec = [&](int x) { return smem_addr(&bars[kXRec + x]); };
@@ -321,6 +329,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     auto grab_free = [&](int g) { return smem_addr(&bars[kGrabBase + 2 * g + 1]); };
     auto zq_full = [&](int z) { return smem_addr(&bars[kZqBase + 2 * z]); };
     auto zq_free = [&](int z) { return smem_addr(&bars[kZqBase + 2 * z + 1]); };
+    auto ticket_bar = [&](int s) { return smem_addr(&bars[kTicketBase + s]); };
 
     const int lo = static_cast<int>(crank) * a.S;
     const int hi = min(lo + a.S, a.V);
@@ -342,6 +351,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         for (int s = 0; s < kMetaSlots; ++s) {
             mbar_init(meta_bar(s, kMetaFull), 1u);
             mbar_init(meta_bar(s, kMetaFree), 1u);
+            mbar_init(ticket_bar(s), 1u);
             meta[s].nown = 0;
         }
         for (int x = 0; x < kXBufs; ++x) {
@@ -362,9 +372,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         }
         for (int r = 0; r < kMaxCluster; ++r) frs[r] = make_float2(0.0f, 0.0f);
         *abort_flag = 0;
+        *copied = 0u;
         fence_mbar_init_cluster();
     }
-    for (int i = tid; i < kMetaSlots * nwords; i += NC + 96) bitmap[i] = 0u;
+    for (int i = tid; i < kMetaSlots * nwords; i += NC + kAuxThreads) bitmap[i] = 0u;
     // Launched with programmatic stream serialisation: everything above touches
     // only shared memory and may overlap the previous kernel in the stream; no
     // global input is read before that kernel has completed.
@@ -408,16 +419,16 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
     };
 
     if (warp == NCW + 1) {
-        // ================= producer warp =================
+        // ================= row warp: rows, zero queue, metadata =================
         // Rows [0, T_static) are dealt round robin (row cid + k * ncl).  The rest
         // are handed out at run time: CTA 0 of the cluster takes the next one
         // from the launch's counter (workspace; the following take is always in
         // flight) and sends it to every CTA of the cluster through a grab ring in
         // their shared memory, so the clusters that have run ahead take more of
-        // the last rows and all finish together.  Rows with a response get the
-        // full pass (metadata slot, slice copies); zero rows (padding, bad
+        // the last rows and all finish together.  Rows with a response get a
+        // metadata slot (the copy warp starts their slice copies); zero rows (padding, bad
         // response or sampled id) go to the zero warp's queue, so their stores
-        // never hold up the producer.
+        // never hold up the row warp.
         uint32_t nfill = 0, ng = 0, nz = 0;
         bool stop = false;
         long long t_static = cid;
@@ -440,6 +451,26 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                     if (ng >= static_cast<uint32_t>(kGrab))
                         ok = mbar_wait_cluster_bounded(grab_free(g), ((ng / kGrab) - 1u) & 1u, wait_ns);
                     if (!__all_sync(kFull, ok)) {
+                        give_up(SC_STATUS_TIMEOUT_LOAD);
+                        stop = true;
+                        break;
+                    }
+                    // A run-time row is taken only once every published row has had
+                    // its copies started: a row taken early is one that a cluster
+                    // further ahead could have finished first (measured: one row of
+                    // look-ahead lengthens the 4096-row batch's tail by ~1.5 us).
+                    bool paced = true;
+                    {
+                        const unsigned long long t0 = global_timer_ns();
+                        while (nfill > *copied) {
+                            if (global_timer_ns() - t0 > wait_ns) {
+                                paced = false;
+                                break;
+                            }
+                            __nanosleep(128);
+                        }
+                    }
+                    if (!__all_sync(kFull, paced)) {
                         give_up(SC_STATUS_TIMEOUT_LOAD);
                         stop = true;
                         break;
@@ -469,15 +500,14 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 t = static_cast<long long>(tu);
             }
             const int rj = __ldg(a.resp + t);
-            int sj = 0;
+            const int sj = __ldg(a.sampled + t);  // (both loads in flight together)
             uint32_t zf = 0;
             if (rj < 0) {
                 zf = SC_FLAG_MASKED;
             } else if (rj >= a.n_resp) {
                 zf = SC_FLAG_BAD_RESPONSE;
-            } else {
-                sj = __ldg(a.sampled + t);
-                if (sj < 0 || sj >= a.V) zf = SC_FLAG_BAD_SAMPLED;
+            } else if (sj < 0 || sj >= a.V) {
+                zf = SC_FLAG_BAD_SAMPLED;
             }
             if (zf) {  // zero row: to the zero warp's queue
                 const int z = static_cast<int>(nz % kZq);
@@ -501,6 +531,12 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (lane == 0) status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
                 stop = true;
                 break;
+            }
+            // the row's index to the copy warp, which can start the slice's copies
+            // while the metadata is built (the slot's previous row is written)
+            if (lane == 0) {
+                ticket[ms] = t;
+                mbar_arrive(ticket_bar(ms));  // release: the ticket
             }
             // ---- recorded ids of this slice: compact list, repeats dropped ----
             // (row scalars loaded first so their latency overlaps the list)
@@ -619,40 +655,10 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 mt->ol = hm.ol;
                 mt->kbest = hm.k;
             }
-            // The slot is published before the copies start: the consumers wait
-            // for each chunk on its own barrier, so they can start as soon as the
-            // first chunk lands.
+            // Published for the copy warp (which starts the slice's copies) and
+            // the consumers, usually rows before they need it.
             __syncwarp();
             if (lane == 0) mbar_arrive(meta_bar(ms, kMetaFull));  // release: slot contents
-            // ---- logit slice: chunk by chunk as the stage's slots free up ----
-            if (lane == 0) {
-                const int ds = static_cast<int>(nfill % NB);
-                const bool reuse = nfill >= static_cast<uint32_t>(NB);
-                const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
-                const uint16_t* lrow = a.logits + t * a.lstride + lo;
-                const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
-                for (int i = 0; i < nchunks; ++i) {
-                    if (reuse &&
-                        !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, wait_ns)) {
-                        status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
-                        for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
-                            (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
-                                                    kDrainLimitNs);
-                        stop = true;
-                        break;
-                    }
-                    // test hook: the first chunk of the first row is never copied,
-                    // so every wait for it runs out (the failure path, with no fault)
-                    if (a.stall && nfill == 0u && i == 0) continue;
-                    fence_proxy_async_smem();
-                    const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
-                    const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                    mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
-                    bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
-                }
-            }
-            stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
-            if (stop) break;
             ++nfill;
         }
         {  // end marker for the zero warp (it leaves on its own if the queue stalls)
@@ -674,10 +680,63 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
                 if (lane == 0) {
                     meta[ms].t = -1;
                     mbar_arrive(meta_bar(ms, kMetaFull));
+                    ticket[ms] = -1;
+                    mbar_arrive(ticket_bar(ms));
                 }
             } else if (lane == 0) {
                 status_or(a.status, SC_STATUS_TIMEOUT_LOAD);
             }
+        }
+    } else if (warp == NCW + 3) {
+        // ================= copy warp: each valid row's slice into the stage =================
+        // Takes the valid rows' indices in the row warp's order from the ticket
+        // ring (published before their metadata is built) and starts the
+        // slice's 1-D bulk copies chunk by chunk, each the moment the write pass
+        // of the row before hands that chunk back.  The row warp's metadata work
+        // (dependent global loads, padding rows in between) never sits between
+        // a freed chunk and its refill.
+        uint32_t nfill = 0;
+        bool stop = false;
+        for (;; ++nfill) {
+            if (flag_up()) break;
+            const int ms = static_cast<int>(nfill % kMetaSlots);
+            if (!__all_sync(kFull, mbar_wait_bounded(ticket_bar(ms), (nfill / kMetaSlots) & 1u, wait_ns))) {
+                give_up(SC_STATUS_TIMEOUT_LOAD);
+                break;
+            }
+            const long long t = ticket[ms];  // read before the slot can be refilled (its row is not written yet)
+            if (t < 0) break;                // end of the stream
+            if (lane == 0) {
+                const int ds = static_cast<int>(nfill % NB);
+                const bool reuse = nfill >= static_cast<uint32_t>(NB);
+                const uint32_t fpar = ((nfill / NB) - 1u) & 1u;
+                const uint16_t* lrow = a.logits + t * a.lstride + lo;
+                const uint32_t bs = smem_addr(smem + ds * L.stage_bytes);
+                for (int i = 0; i < nchunks; ++i) {
+                    if (reuse &&
+                        !mbar_wait_bounded(data_bar(ds, kChunkFree + i), fpar, wait_ns)) {
+                        for (int i2 = 0; i2 < i; ++i2)  // started copies land before the CTA leaves
+                            (void)mbar_wait_bounded(data_bar(ds, kChunkFull + i2), (nfill / NB) & 1u,
+                                                    kDrainLimitNs);
+                        stop = true;
+                        break;
+                    }
+                    // test hook: the first chunk of the first row is never copied,
+                    // so every wait for it runs out (the failure path, with no fault)
+                    if (a.stall && nfill == 0u && i == 0) continue;
+                    fence_proxy_async_smem();
+                    const int v0 = i * a.ncv, v1 = min(v0 + a.ncv, nvb);
+                    const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+                    mbar_expect_tx(data_bar(ds, kChunkFull + i), bytes);
+                    bulk_load(bs + 16u * v0, lrow + 8 * v0, bytes, data_bar(ds, kChunkFull + i), pol_keep);
+                }
+            }
+            stop = __shfl_sync(kFull, static_cast<int>(stop), 0) != 0;
+            if (stop) {
+                give_up(SC_STATUS_TIMEOUT_LOAD);
+                break;
+            }
+            if (lane == 0) *copied = nfill + 1u;
         }
         // copies still in flight land before the CTA can exit (bounded again)
         if (lane == 0) {
@@ -689,7 +748,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
         }
         __syncwarp();
     } else if (warp == NCW + 2) {
-        // ================= zero warp: zero rows from the producer's queue =================
+        // ================= zero warp: zero rows from the row warp's queue =================
         for (uint32_t iz = 0;; ++iz) {
             const int z = static_cast<int>(iz % kZq);
             if (!__all_sync(kFull, mbar_wait_bounded(zq_full(z), (iz / kZq) & 1u, wait_ns))) {
@@ -1229,7 +1288,7 @@ __global__ void __launch_bounds__(NC + 96, min_blocks(NC)) center_kernel(const _
             {
                 // ---- write pass of row i, once the cluster has its row scalars: g = beta p
                 // (the special entries are patched by the scalar warp afterwards), the
-                // slice read from its stage, every chunk handed back to the producer
+                // slice read from its stage, every chunk handed back to the copy warp
                 // as soon as this warp is done with it (the next row streams into it
                 // while this one is written) ----
                 const uint32_t ip = i;
@@ -1338,10 +1397,11 @@ Layout make_layout(int S, int K_max, int NC, int NB, int C, bool vf) {
     L.off_zav = take(2 * 4);
     L.off_rsw = take(2 * (NC / 32) * 4);
     L.off_scal = take(2 * 4 * 4);
-    L.off_flag = take(4);
+    L.off_flag = take(8);
     L.off_grab = take(kGrab * 8);
     L.off_zq = take(kZq * 8);
     L.off_zqf = take(kZq * 4);
+    L.off_ticket = take(kMetaSlots * 8);
     L.total = off;
     return L;
 }
@@ -1432,7 +1492,7 @@ int prepare_kernel(int dev, const Plan& P, int* max_clusters) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.C, 1, 1);
-    cfg.blockDim = dim3(P.NC + 96, 1, 1);
+    cfg.blockDim = dim3(P.NC + kAuxThreads, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1656,7 +1716,7 @@ int center_launch(CenterLaunch& cl, void* workspace, cudaStream_t stream) {
     cl.ka.ws = static_cast<unsigned long long*>(workspace);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(cl.G * P.C), 1, 1);
-    cfg.blockDim = dim3(P.NC + 96, 1, 1);
+    cfg.blockDim = dim3(P.NC + kAuxThreads, 1, 1);
     cfg.dynamicSmemBytes = P.L.total;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
