@@ -60,6 +60,20 @@ struct TopkArgs {
     long long T_static;      // rows dealt round robin to the thread groups (all of them without ws)
 };
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// read-only 16-byte global load with an L2 eviction hint
+__device__ __forceinline__ float4 ldg_f4_hint(const float4* ptr, uint64_t policy) {
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(ptr), "l"(policy));
+    return v;
+}
+
 // Order-preserving key: a larger float gives a larger key (-0 counts as +0).
 __device__ __forceinline__ uint32_t key_of(float z) {
     uint32_t b = __float_as_uint(z == 0.0f ? 0.0f : z);
@@ -1107,8 +1121,10 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
     if (V > kCap) {
         const int nruns = nv4 / kSampRun;
         float smax = -INFINITY;
+        // (kept in L2 until the pass below reads the same lines again)
+        const uint64_t keep = l2_policy_evict_last();
         for (int r = warp * kSampEvery; r < nruns; r += kGW * kSampEvery) {
-            const float4 v = __ldg(r4 + r * kSampRun + lane);
+            const float4 v = ldg_f4_hint(r4 + r * kSampRun + lane, keep);
             smax = fmaxf(smax, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
         }
         group_sort_keys_desc(gs, G, key_of(smax));
@@ -1168,15 +1184,16 @@ __device__ bool fast_row(GroupShared& gs, const Group& G, const TopkArgs& a, lon
         }
     };
     {
+        const uint64_t last = l2_policy_evict_first();  // the row's last read
         int i = tid;
         for (; i + (kUnroll - 1) * kGT < nv4; i += kUnroll * kGT) {
             float4 v[kUnroll];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) v[u] = __ldg(r4 + i + u * kGT);
+            for (int u = 0; u < kUnroll; ++u) v[u] = ldg_f4_hint(r4 + i + u * kGT, last);
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) take4(v[u], 4 * (i + u * kGT));
         }
-        for (; i < nv4; i += kGT) take4(__ldg(r4 + i), 4 * i);
+        for (; i < nv4; i += kGT) take4(ldg_f4_hint(r4 + i, last), 4 * i);
         for (int j = (nv4 << 2) + tid; j < V; j += kGT) {
             const float z = __ldg(row + j);
             if (z > m) raise(z);
