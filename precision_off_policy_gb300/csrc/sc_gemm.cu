@@ -7,7 +7,7 @@
 // A is stored either K-major ([M][K], K contiguous) or M-major ([K][M]); B
 // either K-major ([N][K]) or N-major ([K][N]).  C is row-major [M][N] and is
 // written as bf16 (round to nearest even), as FP32, or added in FP32 to what C
-// already holds (a reduce-add performed by the TMA engine in L2).
+// already holds (vector reductions performed in L2).
 //
 // Design (one CTA per SM, persistent over 128 x 256 output tiles):
 // * warp 0, one thread: the TMA producer.  For every K step of 64 it loads
@@ -20,11 +20,14 @@
 //   K = 16 per stage) and commits each stage back to the producer and each
 //   finished accumulator to the epilogue.
 // * warps 2-5: the epilogue.  Each warp owns 32 accumulator rows (the
-//   tensor-memory lanes its warp index selects); it reads 32 or 64 columns at
-//   a time with tcgen05.ld, converts them, writes them to a swizzled 4 KiB
-//   staging buffer and stores (or reduce-adds) them with a TMA tensor store,
-//   double-buffered, and hands the accumulator back as soon as it is read, so
-//   the next tile's MMAs overlap this tile's stores.
+//   tensor-memory lanes its warp index selects); it reads 32 or 64 columns at a time with tcgen05.ld, converts them, writes
+//   them to a swizzled 4 KiB staging buffer and stores them: bf16 with a TMA
+//   tensor store (double-buffered); FP32 read back transposed so that each
+//   store instruction writes four whole 128-byte row segments (plain 16-byte
+//   stores, or vector reductions for the reduce-add), which keeps the TMA unit
+//   free for the operand loads where the products with a short K would
+//   otherwise wait on it.  It hands the accumulator back as soon as it is read,
+//   so the next tile's MMAs overlap this tile's stores.
 // Every wait is bounded (about 1 s of %globaltimer); on expiry the kernel
 // sets a status bit, stops issuing work, lets the copies and MMAs it started
 // complete and frees its tensor memory before it returns.
@@ -47,7 +50,7 @@ constexpr int kABytes = BM * BK * 2;             // 16 KiB
 constexpr int kBBytes = BN * BK * 2;             // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KiB
 constexpr int kEpiBuf = 32 * 128;                // one warp's staging buffer: 32 rows x 128 B
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;  // one per tensor-memory lane quadrant (measured: eight were slower)
 constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer, MMA, four epilogue warps
 constexpr int kTmemCols = 512;                   // two accumulators of BN FP32 columns
 constexpr int kSmemData = kStages * kStageBytes + kEpiWarps * 2 * kEpiBuf;
@@ -60,7 +63,7 @@ static_assert(kSmemTotal <= 232448, "shared memory per CTA");
 
 struct GemmArgs {
     long long M, N, K;
-    long long N_full;  // columns written by tensor stores: N rounded down to whole 16-byte units
+    long long N_full;  // columns stored in whole 16-byte units: N rounded down to them
     void* C;           // C itself, for the columns past N_full (plain stores)
     long long ldc;
     int num_m, num_n, k_steps;
@@ -89,13 +92,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
                  "r"(x), "r"(y), "r"(src)
                  : "memory");
 }
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
-    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(x), "r"(y), "r"(src)
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// 16 bytes to global memory (16-byte aligned), and the FP32 vector reduction
+__device__ __forceinline__ void st_v4(void* p, const uint4& w) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
                  : "memory");
 }
-__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void red_add_v4f32(void* p, const uint4& w) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(w.x)),
+                 "f"(__uint_as_float(w.y)), "f"(__uint_as_float(w.z)), "f"(__uint_as_float(w.w))
+                 : "memory");
+}
 // At most one committed store group may still be reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -163,6 +170,9 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int mn_major, in
     return mn_major ? smem_desc(base + 2048u * kk, 8192u, 1024u) : smem_desc(base + 32u * kk, 16u, 1024u);
 }
 
+// CM: the output mode (0 bf16, 1 FP32, 2 FP32 reduce-add), one instance each,
+// so that each carries only its own epilogue.
+template <int CM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
@@ -306,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= epilogue: tensor memory -> global =================
         const int q = warp & 3;  // tensor-memory lanes 32q .. 32q + 31
         const uint32_t buf0 = epi0 + static_cast<uint32_t>((warp - 2) * 2 * kEpiBuf);
-        const int cols = g.c_mode == 0 ? 64 : 32;  // columns per 128-byte staging row
+        const int cols = CM == 0 ? 64 : 32;  // columns per 128-byte staging row
         const int nchunks = BN / cols;
         uint32_t lt = 0, nst = 0;
         for (long long t = blockIdx.x; t < g.tiles; t += gridDim.x, ++lt) {
@@ -326,9 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < nchunks; ++c) {
                 const long long c0 = static_cast<long long>(nt) * BN + c * cols;
                 if (r0 >= g.M || c0 >= g.N) break;  // (chunks are in column order)
-                // A tensor store writes whole 16-byte units of a row, so only the
-                // columns before N_full go through it; the few past it (N not a
-                // multiple of 16 bytes) are stored one by one below.
+                // The 16-byte units of a row before N_full are stored whole; the
+                // few columns past it (N not a multiple of 16 bytes) one by one below.
                 uint32_t v[64];
                 uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
                 uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
@@ -344,10 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 64; ++j) {
                             const long long col = c0 + j;
                             if (j < cols && col >= g.N_full && col < g.N) {
-                                if (g.c_mode == 0) {
+                                if (CM == 0) {
                                     uint16_t* cp = static_cast<uint16_t*>(g.C) + crow * g.ldc + col;
                                     *cp = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(v[j]), 0.0f) & 0xFFFFu);
-                                } else if (g.c_mode == 1) {
+                                } else if (CM == 1) {
                                     static_cast<float*>(g.C)[crow * g.ldc + col] = __uint_as_float(v[j]);
                                 } else {
                                     atomicAdd(static_cast<float*>(g.C) + crow * g.ldc + col, __uint_as_float(v[j]));
@@ -355,11 +364,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    if (c0 >= g.N_full) continue;  // nothing of this chunk for the tensor store
+                    if (c0 >= g.N_full) continue;  // nothing of this chunk in whole units
                 }
-                const uint32_t buf = buf0 + static_cast<uint32_t>((nst & 1u) * kEpiBuf);
-                if (lane == 0) bulk_wait_read_le1();  // the store that used this buffer has read it
-                __syncwarp();
+                if constexpr (CM == 0) {
+                    // bf16: a TMA tensor store per chunk, double-buffered (measured faster
+                    // than plain stores on the long-K products that write bf16)
+                    const uint32_t buf = buf0 + static_cast<uint32_t>((nst & 1u) * kEpiBuf);
+                    if (lane == 0) bulk_wait_read_le1();  // the store that used this buffer has read it
+                    __syncwarp();
+                    const uint32_t row = buf + 128u * lane;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t w0, w1, w2, w3;
+                        if (cols == 64) {  // eight bf16 per 16-byte chunk, round to nearest even
+                            w0 = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+                            w1 = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            w2 = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            w3 = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                        } else {
+                            w0 = v[4 * j + 0];
+                            w1 = v[4 * j + 1];
+                            w2 = v[4 * j + 2];
+                            w3 = v[4 * j + 3];
+                        }
+                        sts128(row + 16u * static_cast<uint32_t>(j ^ (lane & 7)), w0, w1, w2, w3);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, static_cast<int>(c0), static_cast<int>(roff + r0), buf);
+                        bulk_commit_group();
+                    }
+                    ++nst;
+                    continue;
+                }
+                // Staged through this warp's swizzled 4 KiB buffer and read back
+                // transposed, so that each store instruction writes four whole
+                // 128-byte row segments; plain stores (or vector reductions) keep
+                // the epilogue out of the TMA unit, which the operand loads need.
+                const uint32_t buf = buf0;
+                __syncwarp();  // every lane has read the previous chunk back
                 const uint32_t row = buf + 128u * lane;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -377,16 +421,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     sts128(row + 16u * static_cast<uint32_t>(j ^ (lane & 7)), w0, w1, w2, w3);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) {
-                    if (g.c_mode == 2)
-                        tma_reduce_add_2d(&tmC, static_cast<int>(c0), static_cast<int>(roff + r0), buf);
-                    else
-                        tma_store_2d(&tmC, static_cast<int>(c0), static_cast<int>(roff + r0), buf);
-                    bulk_commit_group();
+                {
+                    const int seg = lane & 7;  // 16-byte segment of a row
+                    const int esz = CM == 0 ? 2 : 4;
+                    const long long col = c0 + seg * (16 / esz);
+                    if (col < g.N_full) {  // (N_full counts whole 16-byte units)
+#pragma unroll
+                        for (int it = 0; it < 8; ++it) {
+                            const int rr = 4 * it + (lane >> 3);
+                            if (r0 + rr < g.M) {
+                                const uint4 w = lds128(buf + 128u * static_cast<uint32_t>(rr) +
+                                                       16u * static_cast<uint32_t>(seg ^ (rr & 7)));
+                                char* dst = static_cast<char*>(g.C) + ((roff + r0 + rr) * g.ldc + col) * esz;
+                                if (CM == 2)
+                                    red_add_v4f32(dst, w);
+                                else
+                                    st_v4(dst, w);
+                            }
+                        }
+                    }
                 }
-                ++nst;
             }
             // the accumulator is read: the MMAs of a later tile may use it
             tc_fence_before();
@@ -484,14 +539,16 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
               : make_map(enc, &tb, B, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, N, K, ldb, 64, BN);
     if (st != SC_OK) return st;
     const long long per16 = 16 / cesize;              // elements in a 16-byte unit
-    const long long n_full = N / per16 * per16;        // columns the tensor stores cover
-    const long long n_map = n_full > 0 ? n_full : per16;  // (a map needs a nonzero extent; unused then)
+    const long long n_full = N / per16 * per16;        // columns stored in whole 16-byte units
     // with split K, C holds one slice of round_up(M, BM) rows per split
     const long long ksteps = (K + BK - 1) / BK;
     const long long kps = (ksteps + k_splits - 1) / k_splits;
     const long long splits = (ksteps + kps - 1) / kps;  // (no empty ranges)
     const long long m_pad = (M + BM - 1) / BM * BM;
     const long long c_rows = splits > 1 ? splits * m_pad : M;
+    const long long n_map = n_full > 0 ? n_full : per16;  // (a map needs a nonzero extent)
+    // (the kernel's tensor stores use it for bf16 output; the FP32 modes store with
+    // plain 16-byte stores and vector reductions)
     st = c_mode == 0 ? make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c_rows, n_map, ldc, 64, 32)
                      : make_map(enc, &tc, C, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, c_rows, n_map, ldc, 32, 32);
     if (st != SC_OK) return st;
@@ -502,9 +559,12 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     {
         std::lock_guard<std::mutex> lock(g_gemm_mutex);
         if (!g_gemm_attr.count(dev)) {
-            const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(gemm_kernel),
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm smem)");
+            for (const void* fn : {reinterpret_cast<const void*>(gemm_kernel<0>),
+                                   reinterpret_cast<const void*>(gemm_kernel<1>),
+                                   reinterpret_cast<const void*>(gemm_kernel<2>)}) {
+                const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(gemm smem)");
+            }
             int n = 0;
             const cudaError_t e2 = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
             if (e2 != cudaSuccess) return cuda_fail(e2, "cudaDeviceGetAttribute(SMs)");
@@ -535,7 +595,13 @@ int gemm_bf16(const uint16_t* A, long long lda, int a_mn, const uint16_t* B, lon
     ga.idesc = instr_desc(ga.a_mn, ga.b_mn);
     ga.status = status;
     const long long grid = ga.tiles < sms ? ga.tiles : sms;
-    gemm_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemTotal, stream>>>(ga, ta, tb, tc);
+    const dim3 gdim(static_cast<unsigned>(grid));
+    if (c_mode == 0)
+        gemm_kernel<0><<<gdim, kThreads, kSmemTotal, stream>>>(ga, ta, tb, tc);
+    else if (c_mode == 1)
+        gemm_kernel<1><<<gdim, kThreads, kSmemTotal, stream>>>(ga, ta, tb, tc);
+    else
+        gemm_kernel<2><<<gdim, kThreads, kSmemTotal, stream>>>(ga, ta, tb, tc);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "gemm_kernel launch");
     return SC_OK;
