@@ -432,6 +432,31 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
         uint32_t nfill = 0, ng = 0, nz = 0;
         bool stop = false;
         long long t_static = cid;
+        // The cluster's first row is known at launch: all its inputs are loaded
+        // at once (the streaming warps wait on its metadata; later rows are built
+        // ahead of need).  If it is padding only these loads were spent.
+        const long long t_first = t_static < a.T_static ? t_static : -1;
+        int f_rj = -1, f_sj = 0, f_cnt = K_max, f_id[4];
+        float f_rl = 0.0f, f_lp[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            f_id[r] = -1;
+            f_lp[r] = 0.0f;
+        }
+        if (t_first >= 0) {
+            f_rj = __ldg(a.resp + t_first);
+            f_sj = __ldg(a.sampled + t_first);
+            if (a.cnt) f_cnt = __ldg(a.cnt + t_first);
+            if (a.rollout) f_rl = __ldg(a.rollout + t_first);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int k = 32 * r + lane;
+                if (k < K_max) {  // (in bounds whatever the row's count)
+                    f_id[r] = __ldg(a.ids + t_first * static_cast<long long>(K_max) + k);
+                    f_lp[r] = __ldg(a.lps + t_first * static_cast<long long>(K_max) + k);
+                }
+            }
+        }
         unsigned long long pend = 0;  // CTA 0, lane 0: the counter value of the take in flight
         bool pending = false;
         for (;;) {
@@ -499,8 +524,9 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                 if (tu >= static_cast<unsigned long long>(a.T)) break;  // no rows left
                 t = static_cast<long long>(tu);
             }
-            const int rj = __ldg(a.resp + t);
-            const int sj = __ldg(a.sampled + t);  // (both loads in flight together)
+            const bool first = t == t_first;
+            const int rj = first ? f_rj : __ldg(a.resp + t);
+            const int sj = first ? f_sj : __ldg(a.sampled + t);  // (both loads in flight together)
             uint32_t zf = 0;
             if (rj < 0) {
                 zf = SC_FLAG_MASKED;
@@ -541,8 +567,8 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
             // ---- recorded ids of this slice: compact list, repeats dropped ----
             // (row scalars loaded first so their latency overlaps the list)
             const float row_A = __ldg(a.adv + rj);
-            const float row_rl = a.rollout ? __ldg(a.rollout + t) : 0.0f;
-            int cnt = a.cnt ? __ldg(a.cnt + t) : K_max;
+            const float row_rl = first ? f_rl : (a.rollout ? __ldg(a.rollout + t) : 0.0f);
+            int cnt = first ? f_cnt : (a.cnt ? __ldg(a.cnt + t) : K_max);
             uint32_t flags = 0;
             if (cnt < 0 || cnt > K_max) {
                 flags |= SC_FLAG_BAD_COUNT;
@@ -570,8 +596,13 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {  // four rounds of loads in flight together
                     const int k = kb0 + 32 * r + lane;
-                    idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
-                    lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
+                    if (first && kb0 == 0) {
+                        idr[r] = f_id[r];
+                        lpr[r] = f_lp[r];
+                    } else {
+                        idr[r] = k < cnt ? __ldg(a.ids + kb + k) : -1;
+                        lpr[r] = k < cnt ? __ldg(a.lps + kb + k) : 0.0f;
+                    }
                 }
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -970,20 +1001,37 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                 const WarpPart* wp = wpart + xi * C * NCW;
                 const int NP = C * NCW;
                 float mx = Mh;
-                for (int q = lane; q < NP; q += 32) mx = fmaxf(mx, wp[q].m);
-                const float o = warp_max(mx) * kscale;
                 float lT = 0.0f, ET = 0.0f;
-                for (int q = lane; q < NP; q += 32) {
-                    const uint4 w = lds128(smem_addr(wp + q));
+                if (NP <= 32) {  // (the usual case) one partial a lane, loaded once
+                    const uint4 w = lane < NP ? lds128(smem_addr(wp + lane))
+                                              : make_uint4(__float_as_uint(-INFINITY), 0u, 0u, 0u);
                     const float Pm = __uint_as_float(w.x);
+                    const float o1 = warp_max(fmaxf(mx, Pm)) * kscale;
                     if (Pm > -INFINITY) {
-                        const float d = Pm * kscale - o;
+                        const float d = Pm * kscale - o1;
                         const float f = ex2(d);
                         const float S1 = __uint_as_float(w.y), S2 = __uint_as_float(w.z);
-                        lT = fmaf(f, S1, lT);
-                        ET = fmaf(f, fmaf(d, S1, S2), ET);
+                        lT = f * S1;
+                        ET = f * fmaf(d, S1, S2);
                     }
+                    mx = o1;
+                } else {
+                    for (int q = lane; q < NP; q += 32) mx = fmaxf(mx, wp[q].m);
+                    const float o1 = warp_max(mx) * kscale;
+                    for (int q = lane; q < NP; q += 32) {
+                        const uint4 w = lds128(smem_addr(wp + q));
+                        const float Pm = __uint_as_float(w.x);
+                        if (Pm > -INFINITY) {
+                            const float d = Pm * kscale - o1;
+                            const float f = ex2(d);
+                            const float S1 = __uint_as_float(w.y), S2 = __uint_as_float(w.z);
+                            lT = fmaf(f, S1, lT);
+                            ET = fmaf(f, fmaf(d, S1, S2), ET);
+                        }
+                    }
+                    mx = o1;
                 }
+                const float o = mx;  // the row's offset, scaled
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) lT += __shfl_xor_sync(kFull, lT, off);
                 // the recorded ids' sums moved from Mh to the row offset
@@ -1029,12 +1077,11 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                 const float alpha = -a.grad_scale * a.inv_t * Aw;
                 const float beta = -alpha * s;
                 const float bw = o + log2l;
-                if (lane == 0) {
+                if (lane == 0) {  // (the one writer arrives: its stores are released with it)
                     scal[4 * p + 0] = bw;
                     scal[4 * p + 1] = beta;
+                    mbar_arrive(sready(p));
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sready(p));
                 finish_prev();  // the previous row's special entries, off the critical path
 
                 // the rest of the sums
