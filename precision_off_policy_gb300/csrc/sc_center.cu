@@ -39,12 +39,14 @@
 //   While phase A runs it picks up the recorded ids' logits from the slice,
 //   sums them relative to their own offset and sends this CTA's 64-byte record
 //   (those sums, the recorded probabilities, the sampled token's logit, the
-//   previous row's gradient sum) to every CTA of the cluster.  When the last
-//   partial of the row has landed it merges all C x (warps) partials and the C
-//   records lane-parallel (a butterfly: the same bits in every CTA) into the
-//   row scalars (LSE, P_H, Q_H, rho, s, loss, k3, importance weight), and then
-//   patches the previous row's special entries (recorded ids and the sampled
-//   token) with their own gradients.
+//   previous row's gradient sum) to every CTA of the cluster.  The C records
+//   land on their own mbarrier and are merged lane-parallel (a butterfly: the
+//   same bits in every CTA) while the streaming partials are still on their
+//   way; once the last partial has landed, the short critical merge (the row
+//   maximum, one summed value) gives the row scalars the write pass needs (LSE,
+//   P_H, Q_H, rho, s, importance weight), published at once, then the loss, k3
+//   and entropy, and it patches the previous row's special entries (recorded
+//   ids and the sampled token) with their own gradients.
 // * The zero warp writes the queued zero rows (padding and error rows) and
 //   their log p_a and diagnostics, so the row warp never waits on them.
 // Every logit is read from HBM once and every gradient written once.  The
