@@ -817,10 +817,8 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
             const int p = static_cast<int>(j & 1u);
             const int ms = static_cast<int>(j % kMetaSlots);
             const int xi = static_cast<int>(j % kXBufs);
-            // ---- while the streaming warps run phase A of row j: everything that
-            // needs only the slice -- the streaming offset (the same largest logit of
-            // the first vectors), the recorded ids' and a's logits, and the recorded
-            // ids' sums relative to the larger of that offset and their own maximum ----
+            // ---- while the streaming warps run phase A of row j: the recorded ids'
+            // and a's logits and the recorded ids' sums relative to their maximum ----
             if (!__all_sync(kFull, mbar_wait_bounded(meta_bar(ms, kMetaFull), (j / kMetaSlots) & 1u, wait_ns))) {
                 give_up(SC_STATUS_TIMEOUT_LOAD);
                 break;
@@ -850,39 +848,22 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                 }
             };
             if (m.t >= 0) {
-                // The chunk waits also make the bulk copies' data visible to this warp.
-                const int ds = static_cast<int>(j % NB);
-                bool landed = true;
-                for (int c = 0; c < nchunks; ++c)
-                    landed = landed && mbar_wait_bounded(data_bar(ds, kChunkFull + c), (j / NB) & 1u, wait_ns);
-                if (!__all_sync(kFull, landed)) {
-                    give_up(SC_STATUS_TIMEOUT_LOAD);
-                    break;
-                }
-                const unsigned char* sb = smem + ds * L.stage_bytes;
-                float mz = -INFINITY;
-                if (nchunks > 0 && lane < nvb) {
-                    const uint4 w = lds128(smem_addr(sb) + 16u * lane);
-                    const uint32_t mx = bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w));
-                    mz = fmaxf(bf_lo(mx), bf_hi(mx));
-                }
-                mz = warp_max(mz);
-                // logits of the owned recorded ids and of a: from the stage, past the
-                // last whole vector from global memory
-                const uint16_t* sb16 = reinterpret_cast<const uint16_t*>(sb);
+                // The owned recorded ids' logits and a's, straight from global memory
+                // (coherent loads: the gradient may alias the logits, but this row is
+                // written only after its scalars): the record then waits for none of
+                // the slice's copies and its merge is done before phase A ends.
                 const uint16_t* lrow = a.logits + m.t * a.lstride + lo;
                 float* fzw = fix_z + p * cap;
                 float zmax = -INFINITY;
                 for (int e = lane; e < nown; e += 32) {
-                    const int li = li_s[e];
-                    const float z = bf_to_f(li < n8 ? sb16[li] : lrow[li]);
+                    const float z = bf_to_f(lrow[li_s[e]]);
                     fzw[e] = z;
                     zmax = fmaxf(zmax, z);
                 }
                 zmax = warp_max(zmax);
-                if (lane == 0 && a_li >= 0) zav[p] = bf_to_f(a_li < n8 ? sb16[a_li] : lrow[a_li]);
+                if (lane == 0 && a_li >= 0) zav[p] = bf_to_f(lrow[a_li]);
                 __syncwarp();
-                Mo = fmaxf(mz, zmax);
+                Mo = zmax;  // the recorded ids' sums are relative to their own maximum
                 if (Mo > -INFINITY) {
                     head_sums(Mo * kscale);
                 } else if (nown > 0) {
@@ -945,10 +926,15 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
             }
             {
                 const CtaRec* rp = crec + xi * C;
+                // Every group of RP lanes (the power of two >= C) holds the C records,
+                // lane r of a group record r, so log2(RP) butterfly steps leave the
+                // same sums in every lane.
+                const int RP = C <= 1 ? 1 : C <= 2 ? 2 : C <= 4 ? 4 : C <= 8 ? 8 : 16;
+                const int rl = lane & (RP - 1);
                 uint4 r0 = make_uint4(__float_as_uint(-INFINITY), 0u, 0u, 0u), r1 = make_uint4(0u, 0u, 0u, 0u),
                       r2 = make_uint4(0x7FFFFFFFu, 0u, 0u, 0u), r3 = make_uint4(0u, __float_as_uint(1.0f), 0u, 0u);
-                if (lane < C) {
-                    const uint32_t pa = smem_addr(rp + lane);
+                if (rl < C) {
+                    const uint32_t pa = smem_addr(rp + rl);
                     r0 = lds128(pa);
                     r1 = lds128(pa + 16u);
                     r2 = lds128(pa + 32u);
@@ -971,14 +957,13 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                     QY1 = PQY;
                 }
                 HeadMass hm{Pqb, static_cast<int>(r2.x), __uint_as_float(r3.y), Poh, Pol};
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
+                for (int off = 1; off < RP; off <<= 1) {
                     lH1 += __shfl_xor_sync(kFull, lH1, off);
                     EH1 += __shfl_xor_sync(kFull, EH1, off);
                     QY1 += __shfl_xor_sync(kFull, QY1, off);
                     hm = head_merge(hm, head_shfl(hm, off));
                 }
-                const int nval = __reduce_add_sync(kFull, Pnval);
+                const int nval = __reduce_add_sync(kFull, lane < RP ? Pnval : 0);  // one group's records
                 uint32_t flags = __reduce_or_sync(kFull, r2.z);
                 // the logit of a: only its owner's lane has nonzero bits
                 const bool has_a = __reduce_or_sync(kFull, r3.x) != 0u;
@@ -1015,6 +1000,27 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                         const float S1 = __uint_as_float(w.y), S2 = __uint_as_float(w.z);
                         lT = f * S1;
                         ET = f * fmaf(d, S1, S2);
+                    }
+                    mx = o1;
+                } else if (NP <= 64) {  // (clusters of 5 to 8) two partials a lane, both loaded at once
+                    const uint4 w0 = lds128(smem_addr(wp + lane));
+                    const uint4 w1 = lane + 32 < NP ? lds128(smem_addr(wp + lane + 32))
+                                                    : make_uint4(__float_as_uint(-INFINITY), 0u, 0u, 0u);
+                    const float P0 = __uint_as_float(w0.x), P1 = __uint_as_float(w1.x);
+                    const float o1 = warp_max(fmaxf(mx, fmaxf(P0, P1))) * kscale;
+                    if (P0 > -INFINITY) {
+                        const float d = P0 * kscale - o1;
+                        const float f = ex2(d);
+                        const float S1 = __uint_as_float(w0.y), S2 = __uint_as_float(w0.z);
+                        lT = f * S1;
+                        ET = f * fmaf(d, S1, S2);
+                    }
+                    if (P1 > -INFINITY) {
+                        const float d = P1 * kscale - o1;
+                        const float f = ex2(d);
+                        const float S1 = __uint_as_float(w1.y), S2 = __uint_as_float(w1.z);
+                        lT = fmaf(f, S1, lT);
+                        ET = fmaf(f, fmaf(d, S1, S2), ET);
                     }
                     mx = o1;
                 } else {
