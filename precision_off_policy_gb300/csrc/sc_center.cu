@@ -1049,11 +1049,14 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                 const float ya = has_a ? fmaf(za, kscale, -o) : 0.0f;
                 // First what the write pass needs (bw, beta), published at once;
                 // the diagnostics and the recorded ids' own gradients after.
+                // (the MUFU logarithm and one correctly rounded reciprocal: a few ulp
+                // on this path, which every later value of the row shares)
                 const float l = lT + lHg;
-                const float log2l = log2f(l);
-                const float P_H = lHg / l;
-                const float tail_pi = lT / l;
-                const float rho = fmaxf(tail_mu, kTailFloor) / fmaxf(tail_pi, kTailFloor);
+                const float log2l = __log2f(l);
+                const float inv_l = __frcp_rn(l);
+                const float P_H = lHg * inv_l;
+                const float tail_pi = lT * inv_l;
+                const float rho = fmaxf(tail_mu, kTailFloor) * __frcp_rn(fmaxf(tail_pi, kTailFloor));
                 const float s = a.centering ? tail_mu + rho * P_H : 1.0f;
                 const float logp_a = (ya - log2l) * kLn2;
                 const float dd = a.rollout ? logp_a - m.rl : 0.0f;
@@ -1109,11 +1112,11 @@ __global__ void __launch_bounds__(NC + kAuxThreads, min_blocks(NC)) center_kerne
                 float csum = 0.0f;
                 if (a.centering && nval > 0) {
                     const float qlogp = kLn2 * fmaf(-log2l, Q_H, QYg);
-                    const float plogp = kLn2 * fmaf(-log2l, lHg, EHg) / l;
+                    const float plogp = kLn2 * fmaf(-log2l, lHg, EHg) * inv_l;
                     csum = fmaf(-rho, plogp, qlogp);
                 }
                 const float loss = a.is_mode == SC_IS_CLIP ? -fminf(w * A, wc * A) : -Aw * (logp_a - csum);
-                const float entropy = kLn2 * (log2l - (ET + EHg) / l);
+                const float entropy = kLn2 * (log2l - (ET + EHg) * inv_l);
                 const float g_a_free = alpha * (1.0f - s * ex2(ya - log2l));  // g_a when a is unrecorded
                 // gradient at the owned recorded ids, and how far it is from the
                 // beta p the write pass stores there (the row sum's correction)
