@@ -1122,7 +1122,8 @@ __device__ void warp_walk(GroupShared& gs, int lane, int beg, int n, Pair base, 
 // stay in flight without holding registers, the loop unrolled over the ring so
 // that every slot offset is a constant (4096 x 151936 FP32 at top_p = 1: 0.479
 // ms with four 16-byte loads in flight per thread; 0.464 with the ring; 0.423
-// unrolled, with one compensated addition per round).  Returns
+// unrolled, with one compensated addition per round; 0.410 with the offset's
+// tests folded into the candidate test).  Returns
 // false -- outputs untouched, the same decision in every thread of the group
 // -- when the row needs the exact path: too few or too many candidates, a
 // nucleus that reaches below them, entries that are not finite, or K above
@@ -1205,14 +1206,18 @@ __device__ bool fast_row(GroupShared& gs, float4 (&ring)[kRing][kGT], const Grou
     // round's own sum, under 1e-6 of the row's normaliser (the per-vector
     // compensated form: 0.436 ms against 0.423 on 4096 x 151936 at top_p = 1).
     float bsum = 0.0f;  // this round's terms (relative to m)
+    // Whole rounds need kRing vectors per thread, so V > 4 (kRing - 1) kGT >=
+    // kCap there: the row had a sample, its offset o is finite, and so is m.
+    // And tau <= o <= m, so an entry above m is also a candidate.
+    static_assert(4 * (kRing - 1) * kGT >= kCap, "whole rounds only on sampled rows");
     auto take4b = [&](const float4& v, int id0) {
         const float m4 = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-        if (m4 > m) {
+        if (m4 >= tau && m4 > m) {
             add(bsum);
             bsum = 0.0f;
             raise(m4);
         }
-        if (m > -INFINITY) {
+        {
             const f2_t NM = f2_pack(-m, -m);
             const f2_t e01 = f2_ex2(f2_mul(f2_add(f2_pack(v.x, v.y), NM), KT2));
             const f2_t e23 = f2_ex2(f2_mul(f2_add(f2_pack(v.z, v.w), NM), KT2));
