@@ -1183,7 +1183,12 @@ __device__ bool fast_row(GroupShared& gs, float4 (&ring)[kRing][kGT], const Grou
         tau = float_of(gs.keys[rank - 1]);
         o = float_of(gs.keys[0]);
         G.sync();
-        if (!isfinite(o)) return false;
+        if (!isfinite(o)) {
+            // the ring's first copies land before its slots are written again
+            // (the next row's copies, or the exact path's shared memory)
+            cp_async_wait<0>();
+            return false;
+        }
     }
 
     // ---- one pass: the sums and the candidates
