@@ -132,6 +132,11 @@ def test_infinite_entries_short_rows_and_padded_strides():
         z = (rng.standard_normal((6, V)) * 2).astype(np.float32)
         z[0, ::3] = -np.inf
         z[1, 1:] = -np.inf  # a single finite entry
+        # a single finite entry outside the 1/16 threshold sample (at V = 4099 the
+        # sample reads entries 0-127 and 2048-2175): the one-pass path leaves at its
+        # sample, after its first copies have started, and the exact path takes the row
+        z[2, :] = -np.inf
+        z[2, 200 if V > 2048 else V // 2] = 1.5
         check(torch.from_numpy(z).cuda(), 8, 1.0, 1.0, f"V={V}", stride=stride)
         check(torch.from_numpy(z).cuda(), 8, 1.3, 0.8, f"V={V} top_p", stride=stride)
 
