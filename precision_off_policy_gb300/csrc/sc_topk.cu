@@ -668,7 +668,7 @@ struct KernelShared {
         OnePass one;                    // the one-pass path: per group its state and copy ring
     } u;
     int ndefer;
-    long long defer[kGroups * kRound];  // rows of this round left to the exact path
+    long long defer[kGroups * kRound];  // rows left to the exact path since it last ran
     long long take[kGroups];            // a group's row from the run-time hand-out
     int gdone[kGroups];                 // a group has no rows left
 };
@@ -1223,7 +1223,7 @@ __device__ bool fast_row(GroupShared& gs, float4 (&ring)[kRing][kGT], const Grou
     // each round's sum is Kahan-added once: at most a few FP32 roundings of a
     // round's own sum, under 1e-6 of the row's normaliser (the per-vector
     // compensated form: 0.436 ms against 0.423 on 4096 x 151936 at top_p = 1).
-    float bsum = 0.0f;  // this round's terms (relative to m)
+    float bsum = 0.0f;  // the current cycle's terms (relative to m)
     // Whole rounds need kRing vectors per thread, so V > 4 (kRing - 1) kGT >=
     // kCap there: the row had a sample, its offset o is finite, and so is m.
     // And tau <= o <= m, so an entry above m is also a candidate.
